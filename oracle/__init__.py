@@ -1,0 +1,290 @@
+"""CPU oracle for the decode step (TEST INFRASTRUCTURE).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package.  The product path never does: it shares no code
+with it.  The arithmetic lives in ``oracle.c`` (plain C, fp32 with fp64 norm and
+softmax accumulation); this file only compiles it and marshals arguments.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Dict, Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_HDR = os.path.join(_HERE, "oracle.h")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+_lock = threading.Lock()
+
+OK, EINVAL, ESTATE, EKVFULL, ENOMEM = 0, -1, -2, -3, -4
+LAYER_SLOTS = ("attn_norm", "wq", "wk", "wv", "q_norm", "k_norm", "wo", "mlp_norm", "wg", "wu", "wd")
+
+
+class OracleError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"oracle {what} failed with status {status}")
+        self.status = status
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc into ``liboracle.so`` (OpenMP, no FMA contraction).
+
+    ``ORACLE_LIB`` in the environment names a prebuilt library to load instead;
+    the mutation test uses it to run the pins against a deliberately broken copy."""
+    override = os.environ.get("ORACLE_LIB")
+    if override:
+        return override
+    newest = max(os.path.getmtime(_SRC), os.path.getmtime(_HDR))
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < newest:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fopenmp",
+                               "-ffp-contract=off", "-fno-fast-math", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+class Config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "hidden", "n_layers", "n_q_heads", "n_kv_heads", "head_dim", "ffn", "vocab", "embed_rows",
+        "w_bf16", "kv_bf16", "qk_norm", "n_heads_out", "eos_mask_id", "n_buckets")] + [
+        ("buckets", ctypes.c_int * 8), ("acc64", ctypes.c_int),
+        ("rms_eps", ctypes.c_double), ("rope_theta", ctypes.c_double), ("rep_penalty", ctypes.c_double)]
+
+
+def _lib_handle():
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = ctypes.CDLL(build())
+            vp, i32, dp = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
+            P = ctypes.POINTER
+            L.orc_create.argtypes = [P(Config), vp, P(i32)]
+            L.orc_create.restype = vp
+            L.orc_destroy.argtypes = [vp]
+            L.orc_destroy.restype = None
+            for f in (L.orc_reset, L.orc_pos, L.orc_smax):
+                f.argtypes = [vp]
+                f.restype = i32
+            L.orc_forward.argtypes = [vp, vp, i32, i32, i32, i32, P(i32), vp, vp, P(dp)]
+            L.orc_forward.restype = i32
+            L.orc_prefill.argtypes = [vp, vp, vp, i32, i32, P(i32), vp, P(dp)]
+            L.orc_prefill.restype = i32
+            L.orc_get_hidden.argtypes = [vp, vp]
+            L.orc_get_hidden.restype = i32
+            L.orc_get_kv.argtypes = [vp, i32, i32, vp]
+            L.orc_get_kv.restype = i32
+            L.orc_emitted_words.argtypes = [vp, vp]
+            L.orc_emitted_words.restype = i32
+            L.orc_recompute_logits.argtypes = [P(Config), vp, vp, vp, i32, i32, vp]
+            L.orc_recompute_logits.restype = i32
+            L.orc_rmsnorm.argtypes = [vp, vp, i32, dp, vp]
+            L.orc_rmsnorm.restype = None
+            L.orc_rope.argtypes = [vp, i32, i32, dp]
+            L.orc_rope.restype = None
+            L.orc_attend.argtypes = [vp, vp, vp, i32, i32, vp]
+            L.orc_attend.restype = None
+            L.orc_penalty_argmax.argtypes = [vp, i32, vp, ctypes.c_float, i32, P(dp)]
+            L.orc_penalty_argmax.restype = i32
+            L.orc_silu_mul.argtypes = [ctypes.c_float, ctypes.c_float]
+            L.orc_silu_mul.restype = ctypes.c_float
+            L.orc_round_bf16.argtypes = [ctypes.c_float]
+            L.orc_round_bf16.restype = ctypes.c_uint16
+            L.orc_num_threads.argtypes = []
+            L.orc_num_threads.restype = i32
+            L.orc_set_threads.argtypes = [i32]
+            L.orc_set_threads.restype = None
+            _lib = L
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data
+
+
+def make_config(shape, acc64: bool = False, buckets: Optional[Sequence[int]] = None) -> Config:
+    """Oracle config from a ``workloads.Shape``."""
+    c = Config()
+    c.hidden, c.n_layers = shape.hidden, shape.n_layers
+    c.n_q_heads, c.n_kv_heads, c.head_dim = shape.n_q_heads, shape.n_kv_heads, shape.head_dim
+    c.ffn, c.vocab, c.embed_rows = shape.ffn, shape.vocab, shape.embed_rows
+    c.w_bf16 = c.kv_bf16 = int(shape.bf16)
+    c.qk_norm, c.n_heads_out, c.eos_mask_id = int(shape.qk_norm), shape.n_heads_out, shape.eos_mask_id
+    b = list(shape.buckets if buckets is None else buckets)
+    c.n_buckets = len(b)
+    for i, v in enumerate(b):
+        c.buckets[i] = v
+    c.acc64 = int(acc64)
+    c.rms_eps, c.rope_theta, c.rep_penalty = shape.rms_eps, shape.rope_theta, shape.rep_penalty
+    return c
+
+
+def weight_table(shape, weights: Dict[str, np.ndarray]):
+    """Pointer table in the oracle's slot order; keeps the arrays alive."""
+    keep = []
+
+    def p(key):
+        a = weights.get(key)
+        if a is None:
+            return None
+        a = np.ascontiguousarray(a)
+        keep.append(a)
+        return a.ctypes.data
+
+    ptrs = [p("embed"), p("final_norm")] + [p(f"lm_head.{j}") for j in range(shape.n_heads_out)]
+    for l in range(shape.n_layers):
+        ptrs += [p(f"layers.{l}.{s}") for s in LAYER_SLOTS]
+    arr = (ctypes.c_void_p * len(ptrs))(*ptrs)
+    return arr, keep
+
+
+class Oracle:
+    """One decode stream on the CPU oracle."""
+
+    def __init__(self, shape, weights: Dict[str, np.ndarray], acc64: bool = False,
+                 buckets: Optional[Sequence[int]] = None):
+        self.L = _lib_handle()
+        self.shape = shape
+        self.cfg = make_config(shape, acc64, buckets)
+        self._table, self._keep = weight_table(shape, weights)
+        st = ctypes.c_int(0)
+        self.h = self.L.orc_create(ctypes.byref(self.cfg), ctypes.cast(self._table, ctypes.c_void_p), ctypes.byref(st))
+        if not self.h:
+            raise OracleError(st.value, "create")
+
+    def close(self):
+        if self.h:
+            self.L.orc_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _check(self, st, what):
+        if st != OK:
+            raise OracleError(st, what)
+
+    def reset(self):
+        self._check(self.L.orc_reset(self.h), "reset")
+
+    @property
+    def pos(self) -> int:
+        return self.L.orc_pos(self.h)
+
+    @property
+    def smax(self) -> int:
+        return self.L.orc_smax(self.h)
+
+    def prefill(self, embeds: Optional[np.ndarray] = None, tokens: Optional[np.ndarray] = None,
+                head_idx: int = 0, want_logits: bool = True):
+        n = len(embeds) if embeds is not None else len(tokens)
+        e = None if embeds is None else np.ascontiguousarray(embeds, dtype=np.float32)
+        t = None if tokens is None else np.ascontiguousarray(tokens, dtype=np.int32)
+        logits = np.empty(self.shape.vocab, np.float32) if want_logits else None
+        fid, margin = ctypes.c_int(-1), ctypes.c_double(0.0)
+        self._check(self.L.orc_prefill(self.h, _ptr(t), _ptr(e), n, head_idx, ctypes.byref(fid),
+                                       _ptr(logits), ctypes.byref(margin)), "prefill")
+        return fid.value, logits, margin.value
+
+    def step(self, token: int = -1, embed: Optional[np.ndarray] = None, head_idx: int = 0,
+             want_head: bool = True, want_logits: bool = True, taps: bool = False,
+             add_emitted: bool = True):
+        """One decode position.  Returns (id, raw logits, top-2 margin, hidden taps)."""
+        e = None if embed is None else np.ascontiguousarray(embed, dtype=np.float32)
+        logits = np.empty(self.shape.vocab, np.float32) if (want_head and want_logits) else None
+        tp = np.empty((self.shape.n_layers + 1, self.shape.hidden), np.float32) if taps else None
+        oid, margin = ctypes.c_int(-1), ctypes.c_double(0.0)
+        self._check(self.L.orc_forward(self.h, _ptr(e), int(token), int(add_emitted), int(want_head), head_idx,
+                                       ctypes.byref(oid), _ptr(logits), _ptr(tp), ctypes.byref(margin)), "forward")
+        return oid.value, logits, margin.value, tp
+
+    def hidden(self) -> np.ndarray:
+        out = np.empty(self.shape.hidden, np.float32)
+        self._check(self.L.orc_get_hidden(self.h, out.ctypes.data), "get_hidden")
+        return out
+
+    def kv(self, layer: int, which: int) -> np.ndarray:
+        s = self.shape
+        out = np.empty((s.n_kv_heads, self.pos, s.head_dim), np.float32)
+        self._check(self.L.orc_get_kv(self.h, layer, which, out.ctypes.data), "get_kv")
+        return out
+
+    def emitted(self) -> np.ndarray:
+        out = np.zeros((self.shape.vocab + 31) // 32, np.uint32)
+        self.L.orc_emitted_words(self.h, out.ctypes.data)
+        return out
+
+
+def recompute_logits(shape, weights, embeds=None, tokens=None, head_idx: int = 0, acc64: bool = False):
+    L = _lib_handle()
+    cfg = make_config(shape, acc64)
+    table, keep = weight_table(shape, weights)
+    n = len(embeds) if embeds is not None else len(tokens)
+    e = None if embeds is None else np.ascontiguousarray(embeds, dtype=np.float32)
+    t = None if tokens is None else np.ascontiguousarray(tokens, dtype=np.int32)
+    out = np.empty(shape.vocab, np.float32)
+    st = L.orc_recompute_logits(ctypes.byref(cfg), ctypes.cast(table, ctypes.c_void_p), _ptr(t), _ptr(e), n,
+                                head_idx, out.ctypes.data)
+    if st != OK:
+        raise OracleError(st, "recompute")
+    return out
+
+
+# ---- primitives (for the pins) ----
+
+def rmsnorm(x, gamma, eps):
+    x = np.ascontiguousarray(x, np.float32)
+    g = np.ascontiguousarray(gamma, np.float32)
+    out = np.empty_like(x)
+    _lib_handle().orc_rmsnorm(x.ctypes.data, g.ctypes.data, len(x), eps, out.ctypes.data)
+    return out
+
+
+def rope(v, pos, theta):
+    v = np.array(v, dtype=np.float32, copy=True)
+    _lib_handle().orc_rope(v.ctypes.data, len(v), int(pos), float(theta))
+    return v
+
+
+def attend(q, K, V):
+    q = np.ascontiguousarray(q, np.float32)
+    K = np.ascontiguousarray(K, np.float32)
+    V = np.ascontiguousarray(V, np.float32)
+    out = np.empty(len(q), np.float32)
+    _lib_handle().orc_attend(q.ctypes.data, K.ctypes.data, V.ctypes.data, K.shape[0], len(q), out.ctypes.data)
+    return out
+
+
+def penalty_argmax(logits, emitted_ids, penalty, eos_id=-1):
+    lg = np.array(logits, dtype=np.float32, copy=True)
+    mask = np.zeros((len(lg) + 31) // 32, np.uint32)
+    for i in emitted_ids:
+        mask[i >> 5] |= np.uint32(1 << (i & 31))
+    margin = ctypes.c_double(0.0)
+    idx = _lib_handle().orc_penalty_argmax(lg.ctypes.data, len(lg), mask.ctypes.data, float(penalty), int(eos_id),
+                                           ctypes.byref(margin))
+    return idx, lg, margin.value
+
+
+def silu_mul(g, u):
+    return _lib_handle().orc_silu_mul(float(g), float(u))
+
+
+def round_bf16(f):
+    return _lib_handle().orc_round_bf16(float(f))
+
+
+def num_threads() -> int:
+    return _lib_handle().orc_num_threads()
+
+
+def set_threads(n: int):
+    _lib_handle().orc_set_threads(int(n))

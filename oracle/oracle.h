@@ -1,0 +1,91 @@
+/*
+ * CPU oracle for the per-token autoregressive decode step of a Qwen3-style
+ * decoder over a static-shape, bucket-grown KV cache.
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the package's smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  It shares no code,
+ * header, table or constant with the GPU path; the two meet only in the seeded
+ * inputs drawn by the `workloads` module.
+ *
+ * Precision: fp32 storage and arithmetic; every RMSNorm mean-square and every
+ * softmax (max, exp-sum, weighted V sum) accumulates in fp64.  Dot products
+ * accumulate in fp32 in index order (or fp64 when `acc64` is set, a check on
+ * the oracle itself).  The KV cache stores entries in the path's KV type:
+ * bfloat16 (round-to-nearest-even) on the bf16 path, fp32 otherwise.
+ *
+ * Parity pins: see the tests; functions without a pin say so in oracle.c.
+ */
+#ifndef ORACLE_H
+#define ORACLE_H
+#include <stdint.h>
+
+#define ORC_OK 0
+#define ORC_EINVAL (-1)
+#define ORC_ESTATE (-2)
+#define ORC_EKVFULL (-3)
+#define ORC_ENOMEM (-4)
+
+#define ORC_MAX_BUCKETS 8
+#define ORC_MAX_HEADS 16
+
+typedef struct {
+    int hidden, n_layers, n_q_heads, n_kv_heads, head_dim, ffn, vocab, embed_rows;
+    int w_bf16;      /* weights are bfloat16 bit patterns (uint16), else float32 */
+    int kv_bf16;     /* KV cache entries are rounded to bfloat16 */
+    int qk_norm;     /* per-head RMSNorm of q and k over head_dim */
+    int n_heads_out; /* number of output heads (1, or 15 for the Code Predictor) */
+    int eos_mask_id; /* logit forced to -inf before the argmax; -1: none */
+    int n_buckets;
+    int buckets[ORC_MAX_BUCKETS]; /* ascending Smax ladder */
+    int acc64;       /* accumulate dot products in fp64 */
+    double rms_eps, rope_theta, rep_penalty;
+} orc_config;
+
+/* Weight pointer table, host memory, in this order:
+ *   [0] embed [embed_rows, hidden] (may be NULL when embed_rows == 0)
+ *   [1] final_norm [hidden]
+ *   [2 .. 2+n_heads_out) lm_head[j] [vocab, hidden]
+ *   then per layer l, 11 entries: attn_norm, wq, wk, wv, q_norm, k_norm, wo,
+ *   mlp_norm, wg, wu, wd (q_norm/k_norm may be NULL when qk_norm == 0).
+ * Matrices are row-major [out, in].  The oracle borrows them. */
+#define ORC_LAYER_SLOTS 11
+
+typedef struct orc_model orc_model;
+
+orc_model *orc_create(const orc_config *cfg, const void *const *weights, int *status);
+void orc_destroy(orc_model *m);
+int orc_reset(orc_model *m);
+int orc_pos(const orc_model *m);
+int orc_smax(const orc_model *m);
+
+/* One decoder position.  Input: embed (fp32 [hidden]) or, when embed is NULL,
+ * row `token` of the embedding table.  token >= 0 with add_emitted != 0 adds the
+ * id to the emitted set first.  want_head != 0 runs the final norm, head
+ * `head_idx`, the repetition penalty, the EOS mask and the argmax. */
+int orc_forward(orc_model *m, const float *embed, int token, int add_emitted, int want_head,
+                int head_idx, int *out_id, float *logits_raw, float *hidden_taps, double *margin);
+
+/* Prefill n positions from pos 0 (tokens or embeds [n, hidden]); head on the last. */
+int orc_prefill(orc_model *m, const int32_t *tokens, const float *embeds, int n, int head_idx,
+                int *first_id, float *logits_raw, double *margin);
+
+int orc_get_hidden(const orc_model *m, float *out);        /* final-norm output, last position */
+int orc_get_kv(const orc_model *m, int layer, int which, float *out); /* [kvh, pos, hd] */
+int orc_emitted_words(const orc_model *m, uint32_t *out);  /* bitmask copy */
+
+/* Logits at the last of n positions by full causal recompute (no cache). */
+int orc_recompute_logits(const orc_config *cfg, const void *const *weights, const int32_t *tokens,
+                         const float *embeds, int n, int head_idx, float *logits_raw);
+
+/* Primitives the model is built from, exposed for the pins. */
+void orc_rmsnorm(const float *x, const float *gamma, int n, double eps, float *out);
+void orc_rope(float *v, int head_dim, int pos, double theta);
+void orc_attend(const float *q, const float *K, const float *V, int L, int head_dim, float *out);
+int orc_penalty_argmax(float *logits, int n, const uint32_t *emitted, float penalty, int eos_id,
+                       double *margin);
+float orc_silu_mul(float g, float u);
+uint16_t orc_round_bf16(float f);
+int orc_num_threads(void);
+void orc_set_threads(int n);
+
+#endif

@@ -1,0 +1,54 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case copies the oracle's C source to a temporary directory, plants one
+mistake there (the committed oracle is never touched), compiles the copy and
+runs the pin suite against it through ``ORACLE_LIB``: at least one pin must fail.
+"""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "oracle.c")
+
+MUTANTS = {
+    "rope_rotation_sign": ("v[m + half] = b * cs + a * sn;", "v[m + half] = b * cs - a * sn;"),
+    "rope_frequency": ("pow(theta, -2.0 * (double)m / (double)head_dim)", "pow(theta, -1.0 * (double)m / (double)head_dim)"),
+    "attention_scale": ("(float)(1.0 / sqrt((double)head_dim))", "(float)(1.0 / (double)head_dim)"),
+    "rmsnorm_eps_outside_root": ("1.0 / sqrt(ss / (double)n + eps)", "1.0 / sqrt(ss / (double)n) + eps"),
+    "rmsnorm_sum_not_mean": ("1.0 / sqrt(ss / (double)n + eps)", "1.0 / sqrt(ss + eps)"),
+    "gqa_modulo_mapping": ("            int gi = i / grp;\n            orc_attend(q + i * hd, Kr",
+                           "            int gi = i % kvh;\n            orc_attend(q + i * hd, Kr"),
+    "cache_stores_q_for_k": ("kv_store(m, l, 0, i, p, k + i * hd);", "kv_store(m, l, 0, i, p, q + i * hd);"),
+    "cache_reads_one_short": ("kv_load_rows(m, l, 0, i, L, Kr", "kv_load_rows(m, l, 0, i, L - (L > 1), Kr"),
+    "penalty_sign_ignored": ("logits[i] = l > 0.0f ? l / penalty : l * penalty;", "logits[i] = l / penalty;"),
+    "argmax_last_tie": ("if (logits[i] > logits[best]) best = i;", "if (logits[i] >= logits[best]) best = i;"),
+    "migration_drops_last_row": ("for (int p = 0; p < m->pos; ++p)\n                    memcpy(nkv",
+                                 "for (int p = 0; p < m->pos - 1; ++p)\n                    memcpy(nkv"),
+    "dropped_attention_residual": ("matvec(c, W_(m, l, S_WO), h, qd, att, tmp);\n        for (int i = 0; i < h; ++i) x[i] = x[i] + tmp[i];",
+                                   "matvec(c, W_(m, l, S_WO), h, qd, att, tmp);\n        for (int i = 0; i < h; ++i) x[i] = tmp[i];"),
+    "silu_sign": ("gd / (1.0 + exp(-gd))", "gd / (1.0 + exp(gd))"),
+    "bf16_truncation": ("u += 0x7fffu + lsb;", "u += 0u * lsb;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    d = tmp_path / "orc"
+    d.mkdir()
+    shutil.copy(os.path.join(ROOT, "oracle", "oracle.h"), d / "oracle.h")
+    (d / "oracle.c").write_text(src.replace(old, new))
+    lib = d / "liboracle_mutant.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+                           "-o", str(lib), str(d / "oracle.c"), "-lm"])
+    env = dict(os.environ, ORACLE_LIB=str(lib), OMP_NUM_THREADS="2")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
