@@ -1,0 +1,315 @@
+#!/usr/bin/env python3
+"""Decode throughput of the GB300 decode path.
+
+Workload (default ``asr``): the ASR decoder (8 layers, hidden 512, 8 q / 8 kv heads,
+head_dim 64, FFN 2048, vocab 151936, bf16 weights, EOS masked off) on seeded
+synthetic weights.  One trajectory is: reset, prefill 110 N(0,1) embeddings, then
+290 greedy decode steps to KV length 400 with the bucket migrations 128 -> 256 ->
+512 on the way.  A benchmark "step" is one decode token; the timed region runs
+whole trajectories back to back (prefill included) until K tokens are produced.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle instead
+(on the host cores, a bounded sample of the same workload).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tokens/s at 1 GB300; per-step HBM GB/s as fraction of peak"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def _workload(name):
+    import workloads as W
+    s = W.CONFIGS[name]
+    desc = {
+        "asr": "ASR decoder: 8 layers, hidden 512, 8q/8kv heads x 64, FFN 2048, vocab 151936, EOS 151645 masked; "
+               "prefill 110, greedy to KV length 400, buckets 128->256->512, batch 1",
+        "talker": "Talker decoder: 28 layers, hidden 1024, 16q/8kv heads x 128, QK-norm, FFN 3072, vocab 3072, "
+                  "repetition penalty 1.05; prefill 64, 600 greedy steps, buckets 128->256->512->1024, batch 1",
+        "tiny": "tiny fp32 decoder: 1 layer, hidden 256, 4q/2kv x 64, FFN 768, vocab 1024; prefill 35, 8 steps",
+    }[name]
+    return s, desc
+
+
+class Clocks:
+    """nvidia-smi sampler running during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                       "-i", str(gpu_index), "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except Exception:
+            self.p.kill()
+        self.f.flush()
+        rows = []
+        with open(self.f.name) as fh:
+            for line in fh:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.f.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------------------------ oracle arm
+
+
+def run_oracle_sample(shape, max_tokens: int, budget_s: float = 20.0):
+    """Time the CPU oracle on a bounded sample of the workload: prefill (untimed),
+    then up to ``max_tokens`` greedy decode tokens or ``budget_s`` seconds."""
+    import oracle as O
+    import workloads as W
+    w = W.model_weights(shape)
+    e = W.prefill_embeds(shape)
+    o = O.Oracle(shape, w)
+    tok, _, _ = o.prefill(embeds=e, want_logits=False)
+    n = 0
+    t0 = time.perf_counter()
+    limit = min(max_tokens, shape.decode_steps)
+    while n < limit:
+        tok, _, _, _ = o.step(token=tok, want_logits=False)
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    o.close()
+    return n / dt, n, dt, O.num_threads()
+
+
+def reference_arm(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    shape, desc = _workload(args.workload)
+    _, _, _ = run_oracle_sample(shape, max(1, min(args.warmup, 3)), budget_s=5.0)  # warm-up (untimed)
+    tps, n, dt, cores = run_oracle_sample(shape, args.steps, budget_s=60.0)
+    sample = (f"prefill {shape.prefill} untimed, then {n} greedy decode tokens of the {args.workload} workload "
+              f"({dt:.1f} s)")
+    line = {"impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": ws,
+            "steps": n, "warmup": args.warmup, "ms_per_step": 1e3 * dt / max(n, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": desc},
+            "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------ GPU arm
+
+
+def gpu_arm(args):
+    import numpy as np
+    import torch
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+
+    import workloads as W
+    from transformer_autoregressive_decode_gb300.build import build
+    build()
+    import transformer_autoregressive_decode_gb300 as qd
+    from transformer_autoregressive_decode_gb300.torch_io import config_from_shape, upload
+
+    shape, desc = _workload(args.workload)
+    hbm_peak, _, peak_src = _peaks()
+    w_np = W.model_weights(shape)
+    e_np = W.prefill_embeds(shape)
+    dev_w = upload(w_np)
+    h = qd.qd_create(dev_w, config_from_shape(shape))
+    del dev_w
+    e_dev = torch.from_numpy(e_np).cuda()
+    traj = shape.decode_steps
+    ids = torch.empty(traj, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def tokens(n):
+        """Produce n decode tokens: whole trajectories (reset + prefill + greedy)."""
+        done = 0
+        pos_state = tokens.pos
+        while done < n:
+            if pos_state == 0 or pos_state >= traj:
+                qd.qd_reset(h)
+                first = qd.qd_prefill(h, embeds=e_dev)
+                qd.qd_decode_greedy(h, 1, first, ids)
+                pos_state = 1
+                done += 1
+                continue
+            k = min(n - done, traj - pos_state)
+            qd.qd_decode_greedy(h, k, -1, ids)
+            pos_state += k
+            done += k
+        tokens.pos = pos_state
+
+    tokens.pos = 0
+    W_ = max(3, args.warmup)
+    tokens(W_)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    k0, per_step = qd.qd_get_launch_count(h)
+    clocks = Clocks(dev if ws == 1 else local)
+    barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    tokens(args.steps)
+    ev1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    k1, _ = qd.qd_get_launch_count(h)
+    if ws > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = ws * args.steps / (ms / 1e3)
+
+    # whole-step HBM fraction over the timed trajectory mix (algorithmic bytes)
+    L_avg = shape.prefill + 0.5 * (traj + 1)
+    step_bytes = shape.step_bytes(int(round(L_avg)))
+    step_gbs = step_bytes / (ms / 1e3 / args.steps) / 1e9
+
+    # dominant kernel: the output head (norm + GEMV + penalty + argmax)
+    head_bytes = shape.vocab * shape.hidden * (2 if shape.bf16 else 4) + shape.hidden * 8 + shape.vocab // 8
+    gu_bytes = 2 * shape.ffn * shape.hidden * (2 if shape.bf16 else 4)
+    if shape.vocab * shape.hidden >= shape.n_layers * 2 * shape.ffn * shape.hidden:
+        which, kname, kbytes = qd.KERNEL_HEAD, "output head: RMSNorm + LM-head GEMV + penalty + EOS mask + argmax", head_bytes
+    else:
+        which, kname, kbytes = qd.KERNEL_GATE_UP, "RMSNorm + gate/up GEMV + SwiGLU", gu_bytes + shape.hidden * 8 + shape.ffn * 4
+    # the handle holds a prefilled state after the timed region
+    kms = qd.qd_time_kernel(h, which, 50)
+    achieved = kbytes / (kms / 1e3) / 1e9
+
+    # end to end through the public API with host buffers: the prompt embeddings
+    # come from pinned host memory each trajectory, the token goes in and the id
+    # comes out through host memory every step (synchronising call)
+    e_host = torch.from_numpy(e_np).pin_memory()
+    e_buf = torch.empty_like(e_dev)
+    n_e2e = min(args.steps, 4 * traj)
+    barrier()
+    t0 = time.perf_counter()
+    done = 0
+    h2d = d2h = 0
+    while done < n_e2e:
+        qd.qd_reset(h)
+        e_buf.copy_(e_host, non_blocking=True)
+        h2d += e_host.numel() * 4
+        tok = qd.qd_prefill(h, embeds=e_buf)
+        d2h += 12
+        for _ in range(min(traj, n_e2e - done)):
+            tok = qd.qd_decode_step(h, token=tok)
+            h2d += 16
+            d2h += 12
+            done += 1
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    e2e = {"value": ws * n_e2e / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d / n_e2e,
+           "d2h_bytes_per_step": d2h / n_e2e, "api": "qd_prefill + qd_decode_step (host token in, host id out)",
+           "steps": n_e2e}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        tps, n, dt, cores = run_oracle_sample(shape, shape.decode_steps, budget_s=20.0)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"prefill {shape.prefill} untimed, then {n} greedy decode tokens ({dt:.1f} s)"}
+
+    qd.qd_destroy(h)
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": W_, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic: seeded N(0,0.02) bf16 weights, 1+N(0,0.1) norm gammas, N(0,1) prompt embeddings",
+        "config": {"workload": desc, "storage": "bf16 weights and KV cache, fp32 activations and accumulation",
+                   "timed": f"{args.steps} decode tokens as whole trajectories (reset + prefill {shape.prefill} "
+                            f"+ greedy), prefill time included",
+                   "l2": f"inputs larger than L2: {shape.weight_bytes_per_step() / 1e6:.1f} MB of weights per step",
+                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": None, "kernel": kname,
+                     "bytes_per_launch": kbytes, "avg_launch_ms": kms, "peak_source": peak_src,
+                     "timing": "CUDA events on the library stream, 50 back-to-back launches with the step's arguments"},
+        "step_hbm": {"bytes_per_step": step_bytes, "achieved_gbs": step_gbs, "frac": step_gbs / hbm_peak,
+                     "note": f"weights + KV at mean L={L_avg:.0f}; prefill positions not counted as bytes"},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(k1 - k0), "kernels_per_decode_step": per_step,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=29000)
+    ap.add_argument("--warmup", type=int, default=870)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="asr", choices=["asr", "talker", "tiny"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,204 @@
+/*
+ * qd -- per-token autoregressive decode step of a Qwen3-style decoder over a
+ * static-shape, bucket-grown KV cache, on one GB300 (sm_103a).
+ *
+ * The operation (sources by page title and section):
+ *  - "Qwen3-TTS ncnn port: pure C++/ncnn end-to-end reproduction", section
+ *    "Talker: non-standard structure and two-level generation": a 28-layer
+ *    Qwen3-style stack with RMSNorm over head_dim on q and k after their
+ *    projections (QK-norm), 8 kv heads broadcast to 16 q heads (GQA), rotary
+ *    embedding that reduces to plain RoPE, a repetition penalty of 1.05 on ids
+ *    already emitted, greedy decoding; section "Integration and performance
+ *    optimisation": a KV cache computes only the new token's q/k/v and attends
+ *    over the cache.
+ *  - "Audio8-ASR: dynamic KV-cache buckets and multi-length end-to-end
+ *    acceptance", section "Implemented dynamic window mechanism": the cache is
+ *    a rank-3 [kv_heads, Smax, head_dim] buffer per layer written in place;
+ *    a sequence starts at the smallest usable Smax; when the write position
+ *    reaches Smax the valid K/V region of every layer is copied into a larger
+ *    buffer and decoding continues from the same token and RoPE position; the
+ *    host keeps the cache, the embedding lookup and the argmax.
+ *  - "qwen3-tts-hip OPTIMIZATION_LOG", decode-step profile entry: the step is
+ *    input_norm, qkv_gemm, qk_layout_cache, attention, output_gemm_residual,
+ *    post_norm, gate_up_gemm, swiglu, down_gemm_residual, then the logits and
+ *    the token.
+ *
+ * Per position p (0-based) and layer: x^ = RMSNorm(x); q,k,v = W x^; per-head
+ * RMSNorm of q and k (if qk_norm); RoPE at p; K/V row p appended to the cache;
+ * GQA attention of every q head over positions [0, p]; x += Wo o;
+ * x^ = RMSNorm(x); x += Wd (silu(Wg x^) * (Wu x^)).  After the last layer:
+ * y = RMSNorm(x); logits = Whead y; repetition penalty over the emitted ids;
+ * EOS mask; argmax (lowest index on ties).
+ *
+ * Conventions for every entry point:
+ *  - Every call validates its arguments before touching the device and returns
+ *    a qd_status.  On any error the handle's state is unchanged and it stays
+ *    usable; qd_last_error() gives the reason (with the CUDA runtime/driver
+ *    versions).  No call falls back to the CPU.
+ *  - "device" pointers are CUDA device memory of the handle's device; "host"
+ *    pointers are ordinary host memory.  Floating-point activations and
+ *    embeddings are fp32; weights are fp32 or bf16 as the config says.
+ *  - Work is ordered after prior work on the caller's stream (given at
+ *    qd_create) and later work on that stream is ordered after it.  Calls that
+ *    return a host value synchronise; *_async calls do not.
+ *  - A handle is used by one host thread at a time.
+ */
+#ifndef QD_H
+#define QD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct qd_model *qd_handle;
+
+typedef enum {
+    QD_OK = 0,
+    QD_EINVAL = -1,        /* bad argument or configuration */
+    QD_ESTATE = -2,        /* call not valid in the current state (e.g. decode before prefill) */
+    QD_EKVFULL = -3,       /* the position would exceed the last bucket of the ladder */
+    QD_ENOMEM = -4,        /* device allocation failed */
+    QD_ECUDA = -5,         /* a CUDA runtime call failed */
+    QD_EUNSUPPORTED = -6,  /* shape outside what the kernels implement */
+    QD_EDEVICE = -7        /* a kernel reported an error (bounded wait expired, bad index) */
+} qd_status;
+
+enum { QD_F32 = 0, QD_BF16 = 1 };
+#define QD_MAX_BUCKETS 8
+#define QD_MAX_HEADS 16
+
+/* Model configuration (plain data).  hidden, n_q_heads*head_dim and ffn must be
+ * multiples of 256 and at most 8192; head_dim is 64 or 128; n_q_heads is a
+ * multiple of n_kv_heads; bucket sizes ascend and are multiples of 32. */
+typedef struct {
+    int hidden, n_layers, n_q_heads, n_kv_heads, head_dim, ffn;
+    int vocab;       /* rows of every output head */
+    int embed_rows;  /* rows of the input embedding table (0: inputs are embeddings only) */
+    int dtype;       /* QD_F32 or QD_BF16: weights and KV cache entries */
+    int qk_norm;     /* 1: per-head RMSNorm of q and k over head_dim */
+    int n_heads_out; /* output heads (1, or 15 for a code predictor) */
+    int eos_mask_id; /* logit forced to -inf before the argmax; -1: none */
+    int n_buckets;
+    int buckets[QD_MAX_BUCKETS]; /* ascending Smax ladder, e.g. 128, 256, 512 */
+    double rms_eps;     /* e.g. 1e-6 */
+    double rope_theta;  /* e.g. 1e6 */
+    double rep_penalty; /* 1.0 = off */
+} qd_config;
+
+/* Per-layer weights: device pointers, row-major [out, in], in the config's
+ * dtype.  attn_norm/mlp_norm [hidden]; q_norm/k_norm [head_dim] (NULL when
+ * qk_norm == 0); wq [n_q_heads*head_dim, hidden]; wk, wv [n_kv_heads*head_dim,
+ * hidden]; wo [hidden, n_q_heads*head_dim]; wg, wu [ffn, hidden]; wd [hidden, ffn]. */
+typedef struct {
+    const void *attn_norm, *wq, *wk, *wv, *q_norm, *k_norm, *wo, *mlp_norm, *wg, *wu, *wd;
+} qd_layer_weights;
+
+typedef struct {
+    const void *embed;                  /* device [embed_rows, hidden] or NULL */
+    const void *final_norm;             /* device [hidden] */
+    const void *lm_head[QD_MAX_HEADS];  /* device [vocab, hidden], n_heads_out of them */
+    const qd_layer_weights *layers;     /* HOST array of n_layers entries */
+} qd_weights;
+
+/* qd_create -- validate cfg, copy the weights into a library-owned layout
+ * (fused [wq;wk;wv], row-interleaved [wg,wu], fp32 norm gammas), allocate the
+ * first KV bucket, the step scratch and the emitted-id bitmask, and build the
+ * RoPE table.  The caller's weight buffers are only read during this call and
+ * may be freed after it returns.  cuda_stream: the caller's cudaStream_t (may
+ * be the default stream).  Errors: QD_EINVAL (bad cfg or non-device pointer),
+ * QD_EUNSUPPORTED, QD_ENOMEM, QD_ECUDA; *out is NULL then. */
+qd_status qd_create(const qd_weights *weights, const qd_config *cfg, void *cuda_stream, qd_handle *out);
+
+/* qd_destroy -- synchronise, free every device resource. NULL is a no-op. */
+qd_status qd_destroy(qd_handle h);
+
+/* qd_reset -- position 0, emitted set cleared, back to the smallest bucket
+ * (the larger buckets' buffers are kept for reuse). Asynchronous. */
+qd_status qd_reset(qd_handle h);
+
+/* qd_prefill -- feed n prompt positions from position 0 and return the first
+ * generated id (head 0 for a single-head model, head `head_idx` otherwise).
+ * Exactly one of tokens (HOST int32 [n], ids < embed_rows) or embeds (DEVICE
+ * fp32 [n, hidden], row-major) is non-NULL.  Prompt ids do not join the emitted
+ * set.  The first bucket is the smallest Smax >= n.  Synchronises; first_id is
+ * a HOST pointer.  Errors: QD_EINVAL (n < 1, both/neither inputs, bad id),
+ * QD_ESTATE (position != 0: call qd_reset first), QD_EKVFULL (n > last bucket). */
+qd_status qd_prefill(qd_handle h, const int32_t *tokens, const void *embeds, int n, int head_idx,
+                     int32_t *first_id);
+
+/* qd_decode_step -- one position.  Input: embed (DEVICE fp32 [hidden]) if non-NULL,
+ * else row `token` of the embedding table.  token >= 0 marks the id that entered
+ * the sequence: it joins the emitted set (the repetition penalty's memory) in
+ * both cases.  Grows the cache to the next bucket first when the position has
+ * reached Smax.  Writes the argmax of head `head_idx` to *out_id (HOST) and
+ * synchronises.  Errors: QD_ESTATE (before prefill), QD_EKVFULL, QD_EINVAL. */
+qd_status qd_decode_step(qd_handle h, const void *embed, int32_t token, int head_idx, int32_t *out_id);
+
+/* qd_decode_step_async -- as qd_decode_step but token_dev (DEVICE int32, may be
+ * NULL for "no token") is read on the device and the id is written to out_id_dev
+ * (DEVICE int32, may be NULL); no host synchronisation.  Device-side errors are
+ * reported by the next synchronising call. */
+qd_status qd_decode_step_async(qd_handle h, const void *embed, const int32_t *token_dev, int head_idx,
+                               int32_t *out_id_dev);
+
+/* qd_decode_greedy -- n_steps positions of the greedy loop kept on the device:
+ * each step's input is the previous step's argmax (embedded and added to the
+ * emitted set), as in a decoder that feeds its own argmax back.  The first
+ * step's token is first_token if >= 0, else the last id produced.  Bucket
+ * growth happens between steps as needed.  ids_dev: DEVICE int32 [n_steps]
+ * receives the ids in order.  Asynchronous.  Errors: QD_ESTATE, QD_EKVFULL
+ * (pos + n_steps beyond the last bucket, checked before any work). */
+qd_status qd_decode_greedy(qd_handle h, int n_steps, int32_t first_token, int32_t *ids_dev);
+
+/* qd_grow_kv -- migrate now to bucket new_smax (a ladder entry larger than the
+ * current Smax): copy the valid [0, pos) region of every layer's K and V into
+ * that bucket's buffer.  Decoding also grows on its own when it needs to. */
+qd_status qd_grow_kv(qd_handle h, int new_smax);
+
+/* ---- inspection and test taps (not on the hot path) ---- */
+
+/* Final-norm output y [hidden] (fp32) of the last position that ran a head. */
+qd_status qd_get_hidden(qd_handle h, float *out_dev);
+
+/* When either pointer is non-NULL, following steps run without CUDA graphs and
+ * write x after the embedding and after every layer (fp32 [n_layers+1, hidden])
+ * and the raw logits before penalty/mask (fp32 [vocab]).  NULL, NULL restores
+ * the graph path.  Both are DEVICE pointers owned by the caller. */
+qd_status qd_set_debug_taps(qd_handle h, float *hidden_taps_dev, float *logits_dev);
+
+/* Turn CUDA-graph replay on (default) or off; results are identical. */
+qd_status qd_set_graphs(qd_handle h, int enable);
+
+/* Copy the current cache buffer, layout [n_layers][2 (K,V)][n_kv_heads][Smax][head_dim]
+ * in the KV dtype, into dst_dev (DEVICE, at least *bytes). Query the size by
+ * passing dst_dev = NULL. Synchronises. */
+qd_status qd_copy_kv(qd_handle h, void *dst_dev, size_t *bytes);
+
+/* Copy the emitted-id bitmask (uint32 [ceil(vocab/32)], bit i of word i/32) to dst_dev. */
+qd_status qd_get_emitted(qd_handle h, uint32_t *dst_dev);
+
+/* Host-side view of the position (positions held) and the current Smax. */
+qd_status qd_get_pos(qd_handle h, int *pos, int *smax);
+
+/* Number of this library's kernels launched so far by the handle (graph
+ * replays count each kernel node), and kernels per decode step. */
+qd_status qd_get_launch_count(qd_handle h, long long *kernels, int *kernels_per_step);
+
+/* Time `reps` back-to-back launches of one kernel of the decode step with the
+ * arguments the step uses, between CUDA events on the library's stream;
+ * which: 0 = output head (norm + GEMV + penalty + argmax), 1 = fused QKV GEMV
+ * of layer 0, 2 = gate/up GEMV of layer 0, 3 = down GEMV of layer 0,
+ * 4 = attention of layer 0, 5 = output projection of layer 0.  The state is
+ * restored afterwards.  Needs a prefilled handle. */
+qd_status qd_time_kernel(qd_handle h, int which, int reps, float *avg_ms);
+
+const char *qd_last_error(qd_handle h);
+const char *qd_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QD_H */

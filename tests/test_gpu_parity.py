@@ -1,0 +1,292 @@
+"""Parity of the CUDA decode path (through the C-ABI) with the CPU oracle.
+
+Shapes: the five decode workloads and reduced versions of them that the oracle
+finishes in seconds while still spanning several GEMV stages per CTA, several
+attention splits, ragged tails (KV lengths that are not multiples of the split
+size) and every bucket migration of the ladder.
+"""
+import numpy as np
+import pytest
+
+import workloads as W
+from _pair import MARGIN, REL_TOL, Pair, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda(cuda_ok):
+    import __graft_entry__
+    __graft_entry__.build()
+    yield
+
+
+def _tf(shape, n_steps, buckets=None, taps=True, graphs=True, prefill=None, seed=None):
+    w = W.model_weights(shape, seed=seed)
+    e = W.prefill_embeds(shape, prefill)
+    p = Pair(shape, w, buckets=buckets, taps=taps, graphs=graphs)
+    tr = p.run_teacher_forced(e, n_steps)
+    return p, tr
+
+
+# ------------------------------------------------------------------ workloads
+
+
+def test_tiny_fp32_full_workload():
+    s = W.TINY
+    p, tr = _tf(s, s.decode_steps)
+    tr.check()
+    assert max(tr.logits_rel) < 1e-4          # fp32 weights and cache: only summation order differs
+    assert tr.ids_gpu == tr.ids_ref           # every margin of this workload is above the bar
+    p.close()
+
+
+def test_asr_two_layers_crosses_both_migrations():
+    s = W.scaled(W.ASR, n_layers=2, name="asr2")
+    p, tr = _tf(s, 200)                        # prefill 110 -> KV length 311: 128 -> 256 -> 512
+    tr.check()
+    pos, smax = p.qd.qd_get_pos(p.h)
+    assert pos == 311 and smax == 512
+    assert all(i != s.eos_mask_id for i in tr.ids_gpu)
+    p.close()
+
+
+def test_talker_four_layers_gqa_qknorm_penalty():
+    s = W.scaled(W.TALKER, n_layers=4, name="talker4")
+    p, tr = _tf(s, 100)                        # 64 -> 165 positions: crosses 128
+    tr.check()
+    p.close()
+
+
+def test_asr_full_size_graph_path():
+    """The ASR workload at full size in the launch configuration the benchmark
+    times (CUDA graphs, no taps): prefill 110, greedy to KV length 400."""
+    s = W.ASR
+    p, tr = _tf(s, s.decode_steps, taps=False)
+    tr.check()
+    pos, smax = p.qd.qd_get_pos(p.h)
+    assert pos == 400 and smax == 512
+    p.close()
+
+
+def test_asr_full_size_logits_and_layers():
+    s = W.ASR
+    p, tr = _tf(s, 40, taps=True)
+    tr.check()
+    p.close()
+
+
+@pytest.mark.slow
+def test_talker_full_size_graph_path():
+    s = W.TALKER
+    p, tr = _tf(s, s.decode_steps, taps=False)
+    tr.check()
+    pos, smax = p.qd.qd_get_pos(p.h)
+    assert pos == 664 and smax == 1024
+    p.close()
+
+
+def test_code_predictor_heads_and_embedding_inputs():
+    s = W.CODE_PREDICTOR
+    w = W.model_weights(s)
+    p = Pair(s, w)
+    e = W.prefill_embeds(s, 2)
+    steps = W.normal("cp/step_embeds", (14, s.hidden), 0, 0.0, 1.0)
+    rid = p.prefill(embeds=e, head_idx=0)
+    for j in range(1, 15):
+        rid = p.step(token=rid, embed=steps[j - 1], head_idx=j)
+    p.trace.check()
+    pos, smax = p.qd.qd_get_pos(p.h)
+    assert pos == 16 and smax == 32
+    p.close()
+
+
+# ------------------------------------------------------------------ invariants on the GPU
+
+
+def _ids_logits(shape, w, e, n, buckets=None, graphs=True, grow_at=None):
+    import torch
+    import transformer_autoregressive_decode_gb300 as qd
+    from transformer_autoregressive_decode_gb300.torch_io import config_from_shape, upload
+    h = qd.qd_create(upload(w), config_from_shape(shape, buckets))
+    qd.qd_set_graphs(h, graphs)
+    y = torch.empty(shape.hidden, dtype=torch.float32, device="cuda")
+    ids = [qd.qd_prefill(h, embeds=torch.from_numpy(e).cuda())]
+    hid = []
+    for i in range(n):
+        if grow_at is not None and i == grow_at[0]:
+            qd.qd_grow_kv(h, grow_at[1])
+        ids.append(qd.qd_decode_step(h, token=ids[-1]))
+        qd.qd_get_hidden(h, y)
+        hid.append(y.cpu().numpy().copy())
+    n_bytes = qd.qd_copy_kv(h)
+    kv = torch.empty(n_bytes, dtype=torch.uint8, device="cuda")
+    qd.qd_copy_kv(h, kv)
+    pos, smax = qd.qd_get_pos(h)
+    qd.qd_destroy(h)
+    return ids, np.array(hid), kv.cpu().numpy(), pos, smax
+
+
+def _valid_kv(kv_bytes, shape, smax, pos):
+    es = 2 if shape.bf16 else 4
+    a = kv_bytes.reshape(shape.n_layers, 2, shape.n_kv_heads, smax, shape.head_dim * es)
+    return a[:, :, :, :pos, :]
+
+
+def test_bucket_migration_is_bit_identical_on_gpu():
+    s = W.scaled(W.ASR, n_layers=2, name="asr2")
+    w = W.model_weights(s)
+    e = W.prefill_embeds(s)
+    a = _ids_logits(s, w, e, 180)                       # 128 -> 256 -> 512
+    b = _ids_logits(s, w, e, 180, buckets=(512,))       # starts at 512
+    assert a[0] == b[0]
+    assert np.array_equal(a[1], b[1])
+    assert a[3] == b[3] == 290
+    assert np.array_equal(_valid_kv(a[2], s, a[4], a[3]), _valid_kv(b[2], s, b[4], b[3]))
+
+
+def test_explicit_grow_is_bit_identical():
+    s = W.scaled(W.TALKER, n_layers=2, name="talker2")
+    w = W.model_weights(s)
+    e = W.prefill_embeds(s)
+    a = _ids_logits(s, w, e, 30)
+    b = _ids_logits(s, w, e, 30, grow_at=(10, 1024))     # jump 128 -> 1024 mid-stream
+    assert a[0] == b[0] and np.array_equal(a[1], b[1])
+    assert b[4] == 1024
+    assert np.array_equal(_valid_kv(a[2], s, a[4], a[3]), _valid_kv(b[2], s, b[4], b[3]))
+
+
+def test_graph_replay_equals_eager_and_is_deterministic():
+    s = W.scaled(W.TALKER, n_layers=3, name="talker3")
+    w = W.model_weights(s)
+    e = W.prefill_embeds(s)
+    g1 = _ids_logits(s, w, e, 70)
+    g2 = _ids_logits(s, w, e, 70)
+    ea = _ids_logits(s, w, e, 70, graphs=False)
+    assert g1[0] == g2[0] == ea[0]
+    assert np.array_equal(g1[1], g2[1]) and np.array_equal(g1[1], ea[1])
+    assert np.array_equal(g1[2], g2[2])
+
+
+def test_kv_cache_and_emitted_set_match_oracle():
+    s = W.scaled(W.TALKER, n_layers=2, name="talker2")
+    w = W.model_weights(s)
+    e = W.prefill_embeds(s, 40)
+    p = Pair(s, w)
+    p.run_teacher_forced(e, 100)                        # crosses 128
+    kv, pos = p.kv()
+    assert pos == p.ref.pos == 141
+    for l in range(s.n_layers):
+        for which in (0, 1):
+            ref = p.ref.kv(l, which)                    # [kvh, pos, hd]
+            got = kv[l, which, :, :pos, :]
+            assert rel_l2(got, ref) <= REL_TOL
+    import torch
+    em = torch.empty((s.vocab + 31) // 32, dtype=torch.int32, device="cuda")
+    p.qd.qd_get_emitted(p.h, em)
+    assert np.array_equal(em.cpu().numpy().view(np.uint32), p.ref.emitted())   # integer work: bit-exact
+    p.close()
+
+
+def test_prefill_from_tokens():
+    s = W.scaled(W.ASR, n_layers=2, name="asr2")
+    w = W.model_weights(s)
+    toks = W.uniform_int("asr2/prompt", 77, 0, s.vocab - 1)
+    p = Pair(s, w)
+    rid = p.prefill(tokens=toks)
+    for _ in range(20):
+        rid = p.step(token=rid)
+    p.trace.check()
+    p.close()
+
+
+def test_device_greedy_loop_matches_stepwise():
+    import torch
+    import transformer_autoregressive_decode_gb300 as qd
+    from transformer_autoregressive_decode_gb300.torch_io import config_from_shape, upload
+    s = W.scaled(W.ASR, n_layers=2, name="asr2")
+    w = W.model_weights(s)
+    e = torch.from_numpy(W.prefill_embeds(s)).cuda()
+    h = qd.qd_create(upload(w), config_from_shape(s))
+    first = qd.qd_prefill(h, embeds=e)
+    ids = torch.empty(150, dtype=torch.int32, device="cuda")
+    qd.qd_decode_greedy(h, 150, first, ids)
+    torch.cuda.synchronize()
+    greedy = ids.cpu().tolist()
+    qd.qd_reset(h)
+    assert qd.qd_prefill(h, embeds=e) == first
+    step = []
+    tok = first
+    for _ in range(150):
+        tok = qd.qd_decode_step(h, token=tok)
+        step.append(tok)
+    assert greedy == step
+    # async variant with device-resident token / id
+    qd.qd_reset(h)
+    qd.qd_prefill(h, embeds=e)
+    t_dev = torch.tensor([first], dtype=torch.int32, device="cuda")
+    for i in range(10):
+        qd.qd_decode_step_async(h, None, t_dev, 0, t_dev)
+    torch.cuda.synchronize()
+    assert int(t_dev.item()) == step[9]
+    qd.qd_destroy(h)
+
+
+def test_errors_leave_the_handle_usable():
+    import torch
+    import transformer_autoregressive_decode_gb300 as qd
+    from transformer_autoregressive_decode_gb300.torch_io import config_from_shape, upload
+    s = W.scaled(W.TINY, buckets=(32, 64))
+    w = W.model_weights(W.TINY)
+    h = qd.qd_create(upload(w), config_from_shape(s))
+    with pytest.raises(qd.QDError) as ei:
+        qd.qd_decode_step(h, token=1)
+    assert ei.value.status == qd.QD_ESTATE
+    e = torch.from_numpy(W.prefill_embeds(W.TINY, 40)).cuda()
+    with pytest.raises(qd.QDError) as ei:
+        qd.qd_prefill(h, embeds=e[:0])
+    assert ei.value.status == qd.QD_EINVAL
+    with pytest.raises(qd.QDError) as ei:
+        qd.qd_prefill(h, embeds=torch.zeros((65, s.hidden), device="cuda"))
+    assert ei.value.status == qd.QD_EKVFULL
+    first = qd.qd_prefill(h, embeds=e)                  # 40 positions -> bucket 64
+    assert qd.qd_get_pos(h) == (40, 64)
+    with pytest.raises(qd.QDError) as ei:
+        qd.qd_prefill(h, embeds=e)
+    assert ei.value.status == qd.QD_ESTATE
+    with pytest.raises(qd.QDError) as ei:
+        qd.qd_decode_step(h, token=s.embed_rows)
+    assert ei.value.status == qd.QD_EINVAL
+    with pytest.raises(qd.QDError) as ei:
+        qd.qd_grow_kv(h, 48)
+    assert ei.value.status == qd.QD_EINVAL
+    tok = first
+    for _ in range(24):
+        tok = qd.qd_decode_step(h, token=tok)
+    assert qd.qd_get_pos(h) == (64, 64)
+    with pytest.raises(qd.QDError) as ei:
+        qd.qd_decode_step(h, token=tok)
+    assert ei.value.status == qd.QD_EKVFULL
+    assert qd.qd_get_pos(h) == (64, 64)
+    qd.qd_reset(h)
+    assert qd.qd_prefill(h, embeds=e) == first          # usable after every error
+    qd.qd_destroy(h)
+
+
+def test_time_kernel_leaves_state_unchanged():
+    import torch
+    import transformer_autoregressive_decode_gb300 as qd
+    s = W.scaled(W.TALKER, n_layers=2, name="talker2")
+    w = W.model_weights(s)
+    e = W.prefill_embeds(s)
+    ref = _ids_logits(s, w, e, 12)
+    from transformer_autoregressive_decode_gb300.torch_io import config_from_shape, upload
+    h = qd.qd_create(upload(w), config_from_shape(s))
+    ids = [qd.qd_prefill(h, embeds=torch.from_numpy(e).cuda())]
+    for i in range(12):
+        if i == 5:
+            for which in range(6):
+                assert qd.qd_time_kernel(h, which, 3) > 0
+        ids.append(qd.qd_decode_step(h, token=ids[-1]))
+    assert ids == ref[0]
+    qd.qd_destroy(h)

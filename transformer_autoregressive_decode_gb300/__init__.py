@@ -1,0 +1,246 @@
+"""Python binding of the qd C-ABI (``include/qd.h``): argument marshalling only.
+
+Every step of the decode path runs in the CUDA kernels of ``libqd.so``; this
+module converts Python/torch arguments into the C types the library takes.
+PyTorch serves only to hold device memory and to name the caller's stream.
+There is no fallback: importing fails loudly when ``libqd.so`` has not been
+built (``python -c "import __graft_entry__ as g; g.build()"``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional, Sequence
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libqd.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build the CUDA library first "
+                      "(transformer_autoregressive_decode_gb300.build.build())")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+QD_OK, QD_EINVAL, QD_ESTATE, QD_EKVFULL, QD_ENOMEM, QD_ECUDA, QD_EUNSUPPORTED, QD_EDEVICE = 0, -1, -2, -3, -4, -5, -6, -7
+QD_F32, QD_BF16 = 0, 1
+QD_MAX_BUCKETS = 8
+QD_MAX_HEADS = 16
+
+# Every symbol the header declares (tests check the library exports each one).
+EXPORTS = ("qd_create", "qd_destroy", "qd_reset", "qd_prefill", "qd_decode_step", "qd_decode_step_async",
+           "qd_decode_greedy", "qd_grow_kv", "qd_get_hidden", "qd_set_debug_taps", "qd_set_graphs", "qd_copy_kv",
+           "qd_get_emitted", "qd_get_pos", "qd_get_launch_count", "qd_time_kernel", "qd_last_error",
+           "qd_status_string")
+
+
+class qd_config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "hidden", "n_layers", "n_q_heads", "n_kv_heads", "head_dim", "ffn", "vocab", "embed_rows", "dtype",
+        "qk_norm", "n_heads_out", "eos_mask_id", "n_buckets")] + [
+        ("buckets", ctypes.c_int * QD_MAX_BUCKETS),
+        ("rms_eps", ctypes.c_double), ("rope_theta", ctypes.c_double), ("rep_penalty", ctypes.c_double)]
+
+
+class qd_layer_weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "attn_norm", "wq", "wk", "wv", "q_norm", "k_norm", "wo", "mlp_norm", "wg", "wu", "wd")]
+
+
+class qd_weights(ctypes.Structure):
+    _fields_ = [("embed", ctypes.c_void_p), ("final_norm", ctypes.c_void_p),
+                ("lm_head", ctypes.c_void_p * QD_MAX_HEADS), ("layers", ctypes.POINTER(qd_layer_weights))]
+
+
+_vp, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_size_t
+_P = ctypes.POINTER
+_SIGS = {
+    "qd_create": ([_P(qd_weights), _P(qd_config), _vp, _P(_vp)], _i32),
+    "qd_destroy": ([_vp], _i32),
+    "qd_reset": ([_vp], _i32),
+    "qd_prefill": ([_vp, _vp, _vp, _i32, _i32, _P(ctypes.c_int32)], _i32),
+    "qd_decode_step": ([_vp, _vp, ctypes.c_int32, _i32, _P(ctypes.c_int32)], _i32),
+    "qd_decode_step_async": ([_vp, _vp, _vp, _i32, _vp], _i32),
+    "qd_decode_greedy": ([_vp, _i32, ctypes.c_int32, _vp], _i32),
+    "qd_grow_kv": ([_vp, _i32], _i32),
+    "qd_get_hidden": ([_vp, _vp], _i32),
+    "qd_set_debug_taps": ([_vp, _vp, _vp], _i32),
+    "qd_set_graphs": ([_vp, _i32], _i32),
+    "qd_copy_kv": ([_vp, _vp, _P(_sz)], _i32),
+    "qd_get_emitted": ([_vp, _vp], _i32),
+    "qd_get_pos": ([_vp, _P(_i32), _P(_i32)], _i32),
+    "qd_get_launch_count": ([_vp, _P(_i64), _P(_i32)], _i32),
+    "qd_time_kernel": ([_vp, _i32, _i32, _P(ctypes.c_float)], _i32),
+    "qd_last_error": ([_vp], ctypes.c_char_p),
+    "qd_status_string": ([_i32], ctypes.c_char_p),
+}
+for _name, (_args, _res) in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = _args
+    _f.restype = _res
+
+
+class QDError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_lib.qd_status_string(status).decode()}: {message}")
+        self.status = status
+
+
+def _ptr(t) -> Optional[int]:
+    """Device address of a torch tensor (or None)."""
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+class Handle:
+    """Owns a ``qd_handle``; destroyed with the object or by ``qd_destroy``."""
+
+    def __init__(self, h: int, cfg: qd_config):
+        self.h = h
+        self.cfg = cfg
+
+    def __del__(self):
+        try:
+            qd_destroy(self)
+        except Exception:
+            pass
+
+
+def _check(h: Optional[Handle], st: int):
+    if st != QD_OK:
+        msg = _lib.qd_last_error(h.h if h is not None else None).decode(errors="replace") if h is not None else ""
+        raise QDError(st, msg)
+
+
+def make_config(hidden, n_layers, n_q_heads, n_kv_heads, head_dim, ffn, vocab, embed_rows, bf16, qk_norm,
+                n_heads_out=1, eos_mask_id=-1, buckets: Sequence[int] = (128,), rms_eps=1e-6, rope_theta=1e6,
+                rep_penalty=1.0) -> qd_config:
+    c = qd_config()
+    c.hidden, c.n_layers, c.n_q_heads, c.n_kv_heads = hidden, n_layers, n_q_heads, n_kv_heads
+    c.head_dim, c.ffn, c.vocab, c.embed_rows = head_dim, ffn, vocab, embed_rows
+    c.dtype = QD_BF16 if bf16 else QD_F32
+    c.qk_norm, c.n_heads_out, c.eos_mask_id = int(qk_norm), n_heads_out, eos_mask_id
+    c.n_buckets = len(buckets)
+    for i, b in enumerate(buckets):
+        c.buckets[i] = b
+    c.rms_eps, c.rope_theta, c.rep_penalty = rms_eps, rope_theta, rep_penalty
+    return c
+
+
+LAYER_KEYS = ("attn_norm", "wq", "wk", "wv", "q_norm", "k_norm", "wo", "mlp_norm", "wg", "wu", "wd")
+
+
+def qd_create(weights: Dict[str, "torch.Tensor"], cfg: qd_config, stream=None) -> Handle:
+    """weights: device tensors keyed ``embed``, ``final_norm``, ``lm_head.{j}``,
+    ``layers.{l}.{name}``.  ``stream``: a torch.cuda.Stream (default: current)."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    w = qd_weights()
+    w.embed = _ptr(weights.get("embed"))
+    w.final_norm = _ptr(weights["final_norm"])
+    for j in range(cfg.n_heads_out):
+        w.lm_head[j] = _ptr(weights[f"lm_head.{j}"])
+    layers = (qd_layer_weights * cfg.n_layers)()
+    for l in range(cfg.n_layers):
+        for k in LAYER_KEYS:
+            setattr(layers[l], k, _ptr(weights.get(f"layers.{l}.{k}")))
+    w.layers = layers
+    out = ctypes.c_void_p()
+    st = _lib.qd_create(ctypes.byref(w), ctypes.byref(cfg), ctypes.c_void_p(stream.cuda_stream), ctypes.byref(out))
+    if st != QD_OK:
+        raise QDError(st, "qd_create failed")
+    return Handle(out.value, cfg)
+
+
+def qd_destroy(h: Handle):
+    if h is not None and h.h:
+        _lib.qd_destroy(h.h)
+        h.h = None
+
+
+def qd_reset(h: Handle):
+    _check(h, _lib.qd_reset(h.h))
+
+
+def qd_prefill(h: Handle, tokens=None, embeds=None, head_idx: int = 0) -> int:
+    """tokens: host int sequence; embeds: device fp32 tensor [n, hidden]."""
+    fid = ctypes.c_int32(-1)
+    if tokens is not None:
+        arr = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        _check(h, _lib.qd_prefill(h.h, arr.ctypes.data, None, len(arr), head_idx, ctypes.byref(fid)))
+    else:
+        n = embeds.shape[0] if embeds is not None else 0
+        _check(h, _lib.qd_prefill(h.h, None, _ptr(embeds), n, head_idx, ctypes.byref(fid)))
+    return fid.value
+
+
+def qd_decode_step(h: Handle, embed=None, token: int = -1, head_idx: int = 0) -> int:
+    oid = ctypes.c_int32(-1)
+    _check(h, _lib.qd_decode_step(h.h, _ptr(embed), int(token), head_idx, ctypes.byref(oid)))
+    return oid.value
+
+
+def qd_decode_step_async(h: Handle, embed=None, token_dev=None, head_idx: int = 0, out_id_dev=None):
+    _check(h, _lib.qd_decode_step_async(h.h, _ptr(embed), _ptr(token_dev), head_idx, _ptr(out_id_dev)))
+
+
+def qd_decode_greedy(h: Handle, n_steps: int, first_token: int, ids_dev):
+    _check(h, _lib.qd_decode_greedy(h.h, int(n_steps), int(first_token), _ptr(ids_dev)))
+
+
+def qd_grow_kv(h: Handle, new_smax: int):
+    _check(h, _lib.qd_grow_kv(h.h, int(new_smax)))
+
+
+def qd_get_hidden(h: Handle, out_dev):
+    _check(h, _lib.qd_get_hidden(h.h, _ptr(out_dev)))
+
+
+def qd_set_debug_taps(h: Handle, hidden_dev=None, logits_dev=None):
+    _check(h, _lib.qd_set_debug_taps(h.h, _ptr(hidden_dev), _ptr(logits_dev)))
+
+
+def qd_set_graphs(h: Handle, enable: bool):
+    _check(h, _lib.qd_set_graphs(h.h, int(bool(enable))))
+
+
+def qd_copy_kv(h: Handle, dst_dev=None) -> int:
+    n = ctypes.c_size_t(0 if dst_dev is None else dst_dev.numel() * dst_dev.element_size())
+    _check(h, _lib.qd_copy_kv(h.h, _ptr(dst_dev), ctypes.byref(n)))
+    return n.value
+
+
+def qd_get_emitted(h: Handle, dst_dev):
+    _check(h, _lib.qd_get_emitted(h.h, _ptr(dst_dev)))
+
+
+def qd_get_pos(h: Handle):
+    p, s = ctypes.c_int(0), ctypes.c_int(0)
+    _check(h, _lib.qd_get_pos(h.h, ctypes.byref(p), ctypes.byref(s)))
+    return p.value, s.value
+
+
+def qd_get_launch_count(h: Handle):
+    k, per = ctypes.c_longlong(0), ctypes.c_int(0)
+    _check(h, _lib.qd_get_launch_count(h.h, ctypes.byref(k), ctypes.byref(per)))
+    return k.value, per.value
+
+
+def qd_time_kernel(h: Handle, which: int, reps: int) -> float:
+    ms = ctypes.c_float(0.0)
+    _check(h, _lib.qd_time_kernel(h.h, int(which), int(reps), ctypes.byref(ms)))
+    return ms.value
+
+
+def qd_last_error(h: Handle) -> str:
+    return _lib.qd_last_error(h.h).decode(errors="replace")
+
+
+def qd_status_string(status: int) -> str:
+    return _lib.qd_status_string(int(status)).decode()
+
+
+KERNEL_HEAD, KERNEL_QKV, KERNEL_GATE_UP, KERNEL_DOWN, KERNEL_ATTENTION, KERNEL_OPROJ = 0, 1, 2, 3, 4, 5
