@@ -158,8 +158,8 @@ def gpu_arm(args):
     dev = torch.cuda.current_device()
 
     import workloads as W
-    from transformer_autoregressive_decode_gb300.build import build
-    build()
+    import __graft_entry__
+    __graft_entry__.build_library()
     import transformer_autoregressive_decode_gb300 as qd
     from transformer_autoregressive_decode_gb300.torch_io import config_from_shape, upload
 
@@ -175,20 +175,32 @@ def gpu_arm(args):
     ids = torch.empty(traj, dtype=torch.int32, device="cuda")
     stream = torch.cuda.current_stream()
 
-    def tokens(n):
-        """Produce n decode tokens: whole trajectories (reset + prefill + greedy)."""
+    def tokens(n, events=None):
+        """Produce n decode tokens: whole trajectories (reset + prefill + greedy).
+        With ``events``, each greedy segment is bracketed by a pair of CUDA events
+        (used to time the decode steps without the prefill)."""
         done = 0
         pos_state = tokens.pos
         while done < n:
             if pos_state == 0 or pos_state >= traj:
                 qd.qd_reset(h)
                 first = qd.qd_prefill(h, embeds=e_dev)
+                if events is not None:
+                    events.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True), 1))
+                    events[-1][0].record(stream)
                 qd.qd_decode_greedy(h, 1, first, ids)
+                if events is not None:
+                    events[-1][1].record(stream)
                 pos_state = 1
                 done += 1
                 continue
             k = min(n - done, traj - pos_state)
+            if events is not None:
+                events.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True), k))
+                events[-1][0].record(stream)
             qd.qd_decode_greedy(h, k, -1, ids)
+            if events is not None:
+                events[-1][1].record(stream)
             pos_state += k
             done += k
         tokens.pos = pos_state
@@ -220,10 +232,21 @@ def gpu_arm(args):
         ms = float(t.item())
     value = ws * args.steps / (ms / 1e3)
 
-    # whole-step HBM fraction over the timed trajectory mix (algorithmic bytes)
+    # decode steps alone (prefill excluded): events around every greedy segment of
+    # one more pass over whole trajectories
+    tokens.pos = 0
+    evs = []
+    tokens(2 * traj, evs)
+    torch.cuda.synchronize()
+    dec_ms = sum(a.elapsed_time(b) for a, b, _ in evs)
+    dec_n = sum(k for _, _, k in evs)
+    dec_step_us = 1e3 * dec_ms / dec_n
+
+    # whole-step HBM fraction of the decode step (algorithmic bytes: weights + KV at
+    # the mean attended length of the trajectory)
     L_avg = shape.prefill + 0.5 * (traj + 1)
     step_bytes = shape.step_bytes(int(round(L_avg)))
-    step_gbs = step_bytes / (ms / 1e3 / args.steps) / 1e9
+    step_gbs = step_bytes / (dec_step_us / 1e6) / 1e9
 
     # dominant kernel: the output head (norm + GEMV + penalty + argmax)
     head_bytes = shape.vocab * shape.hidden * (2 if shape.bf16 else 4) + shape.hidden * 8 + shape.vocab // 8
@@ -286,8 +309,11 @@ def gpu_arm(args):
                      "frac": achieved / hbm_peak, "traffic": None, "kernel": kname,
                      "bytes_per_launch": kbytes, "avg_launch_ms": kms, "peak_source": peak_src,
                      "timing": "CUDA events on the library stream, 50 back-to-back launches with the step's arguments"},
-        "step_hbm": {"bytes_per_step": step_bytes, "achieved_gbs": step_gbs, "frac": step_gbs / hbm_peak,
-                     "note": f"weights + KV at mean L={L_avg:.0f}; prefill positions not counted as bytes"},
+        "step_hbm": {"bytes_per_step": step_bytes, "decode_step_us": dec_step_us,
+                     "decode_tokens_per_s": 1e6 / dec_step_us, "achieved_gbs": step_gbs,
+                     "frac": step_gbs / hbm_peak, "peak_source": peak_src,
+                     "note": f"decode steps only (prefill excluded), {dec_n} steps timed with CUDA events around "
+                             f"each device greedy segment; weights + KV at mean L={L_avg:.0f}"},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(k1 - k0), "kernels_per_decode_step": per_step,
         "clocks": clk,
     }

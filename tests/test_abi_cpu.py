@@ -14,8 +14,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def qd():
-    from transformer_autoregressive_decode_gb300.build import build
-    build()
+    import __graft_entry__
+    __graft_entry__.build_library()
     import transformer_autoregressive_decode_gb300 as m
     return m
 

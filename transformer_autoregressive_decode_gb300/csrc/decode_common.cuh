@@ -1,0 +1,401 @@
+// Device building blocks shared by the per-phase kernels (decode_kernels.cu) and
+// the persistent decode-step kernel (decode_persistent.cu).  Both paths call the
+// same functions with the same work partition, so they produce bitwise identical
+// results.
+//
+// Weight stream: a ring of `nst` shared-memory slots of kSlotBytes.  The producer
+// (one thread) issues cp.async.bulk copies of whole rows into the slots in a fixed
+// order; consumers walk the same order.  Slot i of stage index `sidx` is
+// sidx % nst and its phase parity is (sidx / nst) & 1; `full[i]` completes when the
+// bytes have landed, `empty[i]` when all kConsumerWarps consumer warps are done.
+#pragma once
+
+#include <float.h>
+#include <limits.h>
+
+#include "qd_device.cuh"
+#include "qd_internal.h"
+
+namespace qd {
+
+struct Ring {
+    uint8_t *base;
+    uint64_t *full;
+    uint64_t *empty;
+    int nst;
+};
+
+// Producer: stream `nrows` rows of `row_bytes` from `src` in stages of `rps` rows.
+// Returns false if a wait on a free slot expired.
+__device__ __forceinline__ bool produce_rows(const Ring &R, uint32_t &sidx, const uint8_t *src, int nrows,
+                                             uint32_t row_bytes, int rps, uint64_t pol) {
+    for (int r = 0; r < nrows; r += rps) {
+        const int slot = (int)(sidx % (uint32_t)R.nst);
+        const uint32_t use = sidx / (uint32_t)R.nst;
+        if (use > 0 && !mbar_wait_bounded(&R.empty[slot], (use - 1) & 1)) return false;
+        const int n = nrows - r < rps ? nrows - r : rps;
+        mbar_arrive_expect_tx(&R.full[slot], n * row_bytes);
+        bulk_copy_g2s(R.base + (size_t)slot * kSlotBytes, src + (size_t)r * row_bytes, n * row_bytes, &R.full[slot],
+                      pol);
+        ++sidx;
+    }
+    return true;
+}
+
+// Producer: one slot holding `bytes` (may be 0) from `src`.
+__device__ __forceinline__ bool produce_block(const Ring &R, uint32_t &sidx, const void *src, uint32_t bytes,
+                                              uint64_t pol) {
+    const int slot = (int)(sidx % (uint32_t)R.nst);
+    const uint32_t use = sidx / (uint32_t)R.nst;
+    if (use > 0 && !mbar_wait_bounded(&R.empty[slot], (use - 1) & 1)) return false;
+    mbar_arrive_expect_tx(&R.full[slot], bytes);
+    if (bytes) bulk_copy_g2s(R.base + (size_t)slot * kSlotBytes, src, bytes, &R.full[slot], pol);
+    ++sidx;
+    return true;
+}
+
+// Consumer side of one slot: wait until it is full; returns its address or null on timeout.
+__device__ __forceinline__ const uint8_t *slot_acquire(const Ring &R, uint32_t sidx) {
+    const int slot = (int)(sidx % (uint32_t)R.nst);
+    if (!mbar_wait_bounded(&R.full[slot], (sidx / (uint32_t)R.nst) & 1)) return nullptr;
+    return R.base + (size_t)slot * kSlotBytes;
+}
+// Each consumer warp releases the slot once (lane 0 after __syncwarp).
+__device__ __forceinline__ void slot_release(const Ring &R, uint32_t sidx, int lane) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&R.empty[sidx % (uint32_t)R.nst]);
+}
+
+// Consumers: reduce `nrows` rows (in stages of `rps`) against the register slice xr
+// of the input vector.  A row is split over `rs` warps (warp = rr * rs + sub); the
+// partial sum of each part goes to res[row * rs + sub].  R rows per warp at a time:
+// independent accumulators, then one butterfly that reduces all R rows together.
+template <typename WT, int NSEG>
+__device__ __forceinline__ bool gemv_consume(const Ring &R, uint32_t &sidx, int nrows, int rps, uint32_t row_bytes,
+                                             int rs, int colbase, const float *xr, float *res) {
+    constexpr int EPL = Elem<WT>::kPer16B;
+    constexpr int SEGW = 32 * EPL;
+    constexpr int RR = NSEG <= 2 ? 4 : 2;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = warp % rs, rr = warp / rs, rpp = kConsumerWarps / rs;
+    for (int rbase = 0; rbase < nrows; rbase += rps) {
+        const uint8_t *sbase = slot_acquire(R, sidx);
+        if (!sbase) return false;
+        const int n = nrows - rbase < rps ? nrows - rbase : rps;
+        for (int r = rr; r < n; r += RR * rpp) {
+            uint4 w[RR][NSEG];
+#pragma unroll
+            for (int q = 0; q < RR; ++q) {
+                const int rq = r + q * rpp;
+                const WT *wrow = reinterpret_cast<const WT *>(sbase + (size_t)(rq < n ? rq : r) * row_bytes) + colbase;
+#pragma unroll
+                for (int sg = 0; sg < NSEG; ++sg)
+                    w[q][sg] = rq < n ? *reinterpret_cast<const uint4 *>(wrow + sg * SEGW + lane * EPL)
+                                      : make_uint4(0u, 0u, 0u, 0u);
+            }
+            float acc[RR];
+#pragma unroll
+            for (int q = 0; q < RR; ++q) {
+                acc[q] = 0.f;
+#pragma unroll
+                for (int sg = 0; sg < NSEG; ++sg) {
+                    float f[EPL];
+                    Elem<WT>::unpack(w[q][sg], f);
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) acc[q] = fmaf(f[e], xr[sg * EPL + e], acc[q]);
+                }
+            }
+            const bool b4 = (lane & 16) != 0;
+            float v;
+            int q;
+            if (RR == 4) {
+                const bool b3 = (lane & 8) != 0;
+                float k0 = b4 ? acc[2 % RR] : acc[0], s0 = b4 ? acc[0] : acc[2 % RR];
+                float k1 = b4 ? acc[3 % RR] : acc[1], s1 = b4 ? acc[1] : acc[3 % RR];
+                k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+                k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+                v = b3 ? k1 : k0;
+                const float sx = b3 ? k0 : k1;
+                v += __shfl_xor_sync(0xffffffffu, sx, 8);
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                v += __shfl_xor_sync(0xffffffffu, v, 1);
+                q = (b4 ? 2 : 0) + (b3 ? 1 : 0);   // lanes 0, 8, 16, 24 hold rows 0..3
+            } else {
+                v = b4 ? acc[1] : acc[0];
+                const float sx = b4 ? acc[0] : acc[1];
+                v += __shfl_xor_sync(0xffffffffu, sx, 16);
+                v += __shfl_xor_sync(0xffffffffu, v, 8);
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                v += __shfl_xor_sync(0xffffffffu, v, 1);
+                q = b4 ? 1 : 0;                     // lanes 0, 16 hold rows 0, 1
+            }
+            const int rq = r + q * rpp;
+            if ((lane & (RR == 4 ? 7 : 15)) == 0 && rq < n) res[(rbase + rq) * rs + sub] = v;
+        }
+        slot_release(R, sidx, lane);
+        ++sidx;
+    }
+    return true;
+}
+
+// Register slice of a vector for the consumer thread: columns colbase + sg*SEGW + lane*EPL + e.
+template <typename WT, int NSEG>
+__device__ __forceinline__ void load_slice(const float *v, int colbase, float *xr) {
+    constexpr int EPL = Elem<WT>::kPer16B;
+    constexpr int SEGW = 32 * EPL;
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int sg = 0; sg < NSEG; ++sg)
+#pragma unroll
+        for (int e = 0; e < EPL; e += 4) {
+            const float4 v4 = __ldcg(reinterpret_cast<const float4 *>(v + colbase + sg * SEGW + lane * EPL + e));
+            xr[sg * EPL + e] = v4.x;
+            xr[sg * EPL + e + 1] = v4.y;
+            xr[sg * EPL + e + 2] = v4.z;
+            xr[sg * EPL + e + 3] = v4.w;
+        }
+}
+
+// Whole vector (n floats, n a multiple of 4) into shared memory, loaded once per CTA
+// by the consumer threads: every SM reads a freshly written activation vector right
+// after a dependency, so per-warp loads of the same lines would queue at the few L2
+// slices that hold them.  The caller synchronises the consumers before use.
+__device__ __forceinline__ void load_vec_smem(const float *src, int n, float *dst) {
+    for (int i = threadIdx.x * 4; i < n; i += kConsumerWarps * 32 * 4)
+        *reinterpret_cast<float4 *>(dst + i) = __ldcg(reinterpret_cast<const float4 *>(src + i));
+}
+
+// Register slice of a shared-memory vector for the consumer thread.
+template <typename WT, int NSEG>
+__device__ __forceinline__ void smem_slice(const float *v, int colbase, float *xr) {
+    constexpr int EPL = Elem<WT>::kPer16B;
+    constexpr int SEGW = 32 * EPL;
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int sg = 0; sg < NSEG; ++sg)
+#pragma unroll
+        for (int e = 0; e < EPL; e += 4) {
+            const float4 v4 = *reinterpret_cast<const float4 *>(v + colbase + sg * SEGW + lane * EPL + e);
+            xr[sg * EPL + e] = v4.x;
+            xr[sg * EPL + e + 1] = v4.y;
+            xr[sg * EPL + e + 2] = v4.z;
+            xr[sg * EPL + e + 3] = v4.w;
+        }
+}
+
+// RMSNorm of the register slices across the consumer warps (warps rr == 0 hold each
+// column once): xr <- xr * rsqrt(mean(x^2) + eps) * gamma.  `misc` holds >= 8 floats;
+// `gsm` is gamma staged in shared memory.  Named barrier 1 over the consumers.
+template <typename WT, int NSEG>
+__device__ __forceinline__ void rmsnorm_slice(float *xr, const float *gsm, int K, int rs, int colbase, float eps,
+                                              float *misc, float *y_out) {
+    constexpr int EPL = Elem<WT>::kPer16B;
+    constexpr int SEGW = 32 * EPL;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = warp % rs, rr = warp / rs;
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < NSEG * EPL; ++i) ss = fmaf(xr[i], xr[i], ss);
+    ss = warp_sum(ss);
+    if (lane == 0 && rr == 0) misc[sub] = ss;
+    named_sync(1, kConsumerWarps * 32);
+    float tot = 0.f;
+    for (int j = 0; j < rs; ++j) tot += misc[j];
+    const float inv = 1.0f / sqrtf(tot / (float)K + eps);
+    const bool wy = y_out != nullptr && rr == 0;
+#pragma unroll
+    for (int sg = 0; sg < NSEG; ++sg)
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+            const int i = sg * EPL + e;
+            const int col = colbase + sg * SEGW + lane * EPL + e;
+            xr[i] = xr[i] * inv * gsm[col];
+            if (wy) y_out[col] = xr[i];
+        }
+    named_sync(1, kConsumerWarps * 32);   // misc is reused by the caller
+}
+
+// The step's input vector (first phase of a step): the token row of the embedding
+// table, the caller's embedding, or the staged prompt input at position `pos`.
+// Thread 0 resolves the step description from the device state; CTA 0 records the
+// token in the emitted set.  Fills the register slice xr; warps rr == 0 of CTA
+// `writer_cta` also store the vector to x_out (and to tap when given).
+typedef StepInputArgs StepInput;
+
+template <typename WT, int NSEG>
+__device__ __forceinline__ void step_input_slice(const StepInput &in, DevState *st, int K, int rs, int colbase,
+                                                 float *xr, int *misc_i, float *x_out, float *tap) {
+    constexpr int EPL = Elem<WT>::kPer16B;
+    constexpr int SEGW = 32 * EPL;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        const int pos = st->pos;
+        const int mode = st->in_mode;
+        int tok = st->token_in;
+        if (mode == IN_FEEDBACK) tok = st->out_id;
+        else if (mode == IN_STAGED_TOKENS) tok = pos < in.S ? in.stage_tokens[pos] : -1;
+        else if (mode == IN_STAGED_EMBEDS) tok = -1;
+        int bad = 0;
+        if (pos >= in.S) {
+            bad = 1;
+            if (blockIdx.x == 0) atomicOr(&st->status, DEV_ERR_BAD_POS);
+        }
+        const bool needs_row = (mode == IN_TOKEN || mode == IN_FEEDBACK || mode == IN_STAGED_TOKENS);
+        if (!bad && needs_row && (tok < 0 || tok >= in.table_rows || in.table == nullptr)) {
+            bad = 1;
+            if (blockIdx.x == 0) atomicOr(&st->status, DEV_ERR_BAD_TOKEN);
+        }
+        if (blockIdx.x == 0 && st->add_emitted && tok >= 0 && tok < in.vocab)
+            in.emitted[tok >> 5] |= 1u << (tok & 31);
+        misc_i[0] = mode;
+        misc_i[1] = tok;
+        misc_i[2] = bad;
+        misc_i[3] = pos;
+    }
+    named_sync(1, kConsumerWarps * 32);
+    const int mode = misc_i[0], tok = misc_i[1], bad = misc_i[2], pos = misc_i[3];
+    const bool writer = blockIdx.x == 0 && (warp / rs) == 0;
+#pragma unroll
+    for (int sg = 0; sg < NSEG; ++sg) {
+        const int col = colbase + sg * SEGW + lane * EPL;
+        float v[EPL];
+        if (bad) {
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) v[e] = 0.f;
+        } else if (mode == IN_EMBED || mode == IN_STAGED_EMBEDS) {
+            const float *src = mode == IN_EMBED ? in.embed_in + col : in.stage_embeds + (size_t)pos * K + col;
+#pragma unroll
+            for (int e = 0; e < EPL; e += 4) {
+                const float4 f4 = __ldcg(reinterpret_cast<const float4 *>(src + e));
+                v[e] = f4.x; v[e + 1] = f4.y; v[e + 2] = f4.z; v[e + 3] = f4.w;
+            }
+        } else {
+            const uint4 u = *reinterpret_cast<const uint4 *>(reinterpret_cast<const WT *>(in.table) +
+                                                             (size_t)tok * K + col);
+            Elem<WT>::unpack(u, v);
+        }
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) xr[sg * EPL + e] = v[e];
+        if (writer) {
+#pragma unroll
+            for (int e = 0; e < EPL; e += 4) {
+                const float4 f4 = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+                *reinterpret_cast<float4 *>(x_out + col + e) = f4;
+                if (tap) *reinterpret_cast<float4 *>(tap + col + e) = f4;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ bool arg_better(float v, int i, float bv, int bi) {
+    return v > bv || (v == bv && i < bi);
+}
+
+// ---------------------------------------------------------------------------------
+// Attention of one (kv group, split) on shared-memory tiles.
+// Ks/Vs: n cached rows in the cache type (row n_old already holds position p when the
+// split owns it); qs: the G query heads (normalised, rotated), fp32; sc: [G][CM]
+// scratch.  Outputs the split's unnormalised output po[G][HD], max pm[G], sum pl[G].
+// Threads: kAttnWarps warps (the caller's first kAttnWarps * 32 threads).
+// ---------------------------------------------------------------------------------
+template <typename KT, int HD, int NW>
+__device__ __forceinline__ void attn_split(const KT *Ks, const KT *Vs, const float *qs, int G, int n, int CM,
+                                           float scale, float *sc, float *po, float *pm, float *pl, int bar_id) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr int NT = NW * 32;
+    // scores: a group of LPP lanes per position, 16 bytes of the key row per lane
+    constexpr int EPL = 16 / (int)sizeof(KT);     // key elements per lane
+    constexpr int LPP = HD / EPL;                 // lanes per position (8 or 16 for bf16)
+    constexpr int PPW = 32 / LPP;                 // positions per warp per pass
+    const int sub = lane / LPP, l8 = lane % LPP;
+    for (int j0 = warp * PPW; j0 < n; j0 += NW * PPW) {
+        const int j = j0 + sub;
+        const int jj = j < n ? j : n - 1;
+        float kf[EPL];
+        Elem<KT>::unpack(*reinterpret_cast<const uint4 *>(Ks + (size_t)jj * HD + l8 * EPL), kf);
+        for (int hh = 0; hh < G; ++hh) {
+            const float *q = qs + hh * HD + l8 * EPL;
+            float d = 0.f;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) d = fmaf(q[e], kf[e], d);
+#pragma unroll
+            for (int o = LPP / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+            if (l8 == 0 && j < n) sc[hh * CM + j] = d * scale;
+        }
+    }
+    named_sync(bar_id, NT);
+    for (int hh = warp; hh < G; hh += NW) {
+        float mx = -INFINITY;
+        for (int j = lane; j < n; j += 32) mx = fmaxf(mx, sc[hh * CM + j]);
+        mx = warp_max(mx);
+        float l = 0.f;
+        for (int j = lane; j < n; j += 32) {
+            const float e = expf(sc[hh * CM + j] - mx);
+            sc[hh * CM + j] = e;
+            l += e;
+        }
+        l = warp_sum(l);
+        if (lane == 0) {
+            pm[hh] = mx;
+            pl[hh] = l;
+        }
+    }
+    named_sync(bar_id, NT);
+    // P.V: thread per (head, pair of dims); positions in order, 4 independent partial sums
+    for (int idx = tid; idx < G * HD / 2; idx += NT) {
+        const int hh = idx / (HD / 2), d = (idx % (HD / 2)) * 2;
+        const float *p = sc + hh * CM;
+        float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f, c0 = 0.f, c1 = 0.f, e0 = 0.f, e1 = 0.f;
+        int j = 0;
+        for (; j + 4 <= n; j += 4) {
+            a0 = fmaf(p[j], Elem<KT>::load(Vs + (size_t)j * HD, d), a0);
+            a1 = fmaf(p[j], Elem<KT>::load(Vs + (size_t)j * HD, d + 1), a1);
+            b0 = fmaf(p[j + 1], Elem<KT>::load(Vs + (size_t)(j + 1) * HD, d), b0);
+            b1 = fmaf(p[j + 1], Elem<KT>::load(Vs + (size_t)(j + 1) * HD, d + 1), b1);
+            c0 = fmaf(p[j + 2], Elem<KT>::load(Vs + (size_t)(j + 2) * HD, d), c0);
+            c1 = fmaf(p[j + 2], Elem<KT>::load(Vs + (size_t)(j + 2) * HD, d + 1), c1);
+            e0 = fmaf(p[j + 3], Elem<KT>::load(Vs + (size_t)(j + 3) * HD, d), e0);
+            e1 = fmaf(p[j + 3], Elem<KT>::load(Vs + (size_t)(j + 3) * HD, d + 1), e1);
+        }
+        for (; j < n; ++j) {
+            a0 = fmaf(p[j], Elem<KT>::load(Vs + (size_t)j * HD, d), a0);
+            a1 = fmaf(p[j], Elem<KT>::load(Vs + (size_t)j * HD, d + 1), a1);
+        }
+        po[hh * HD + d] = (a0 + b0) + (c0 + e0);
+        po[hh * HD + d + 1] = (a1 + b1) + (c1 + e1);
+    }
+}
+
+// QK-RMSNorm (if gammas are given) and RoPE at position p of the G query heads in
+// qs and of the key in kn; cos/sin row in rc ([HD/2] cos then [HD/2] sin).
+template <int HD, int NW>
+__device__ __forceinline__ void qk_norm_rope(float *qs, float *kn, int G, const float *q_gamma, const float *k_gamma,
+                                             float eps, const float *rc, int bar_id) {
+    constexpr int HALF = HD / 2;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (q_gamma) {
+        for (int hh = warp; hh <= G; hh += NW) {
+            float *v = hh < G ? qs + hh * HD : kn;
+            const float *gam = hh < G ? q_gamma : k_gamma;
+            float ss = 0.f;
+            for (int i = lane; i < HD; i += 32) ss = fmaf(v[i], v[i], ss);
+            ss = warp_sum(ss);
+            const float inv = 1.0f / sqrtf(ss / (float)HD + eps);
+            for (int i = lane; i < HD; i += 32) v[i] = v[i] * inv * gam[i];
+        }
+        named_sync(bar_id, NW * 32);
+    }
+    for (int idx = tid; idx < (G + 1) * HALF; idx += NW * 32) {
+        const int hh = idx / HALF, m = idx % HALF;
+        float *v = hh < G ? qs + hh * HD : kn;
+        const float c = rc[m], si = rc[HALF + m];
+        const float x0 = v[m], x1 = v[m + HALF];
+        v[m] = x0 * c - x1 * si;
+        v[m + HALF] = x1 * c + x0 * si;
+    }
+    named_sync(bar_id, NW * 32);
+}
+
+}  // namespace qd

@@ -16,44 +16,42 @@
 //    repetition penalty on emitted ids, greedy argmax.
 //  - "Audio8-ASR: dynamic KV-cache buckets", section "Implemented dynamic
 //    window mechanism": [heads, Smax, head_dim] cache written in place; bucket
-//    migration copies the valid region of every layer's K and V.
-#include <float.h>
-#include <limits.h>
-
-#include "qd_device.cuh"
-#include "qd_internal.h"
+//    migration copies the valid region of every layer's K and V; the embedding
+//    lookup of the fed-back token is part of the step.
+#include "decode_common.cuh"
 
 namespace qd {
 
 // =====================================================================================
 // GEMV: out[r] = W[r, :] . v  with v = RMSNorm(in) (QKV, GU, HEAD) or v = in (RES).
 //
-// Each CTA owns a contiguous block of rows.  Thread 0 streams that block through a
-// ring of `nst` stages of kStageRows rows with cp.async.bulk; the copies for the
-// first stages are issued before griddepcontrol.wait, since weights never depend on
-// the previous kernel.  A row is reduced by `rs` warps; each lane keeps its slice of
-// v in registers (NSEG segments of 16 bytes of weights per lane).  Row sums are
-// combined in a fixed order, so results are bitwise reproducible.
+// Each CTA owns a contiguous block of rows.  A producer warp streams the block
+// through a ring of `nst` stages (kSlotBytes each) with cp.async.bulk, gated by
+// per-stage full/empty mbarriers; it never waits on the previous kernel, because
+// weights never depend on it, so under programmatic dependent launch the weight
+// stream starts while the previous kernel is still running.  Eight consumer warps
+// reduce the rows: a row is split over `rs` warps, each lane keeps its slice of v
+// in registers.  Partial sums go to shared memory and the epilogue runs once, over
+// all rows in parallel, after the stage loop.  All sums have a fixed order, so the
+// results are bitwise reproducible.
 // =====================================================================================
 
-__device__ __forceinline__ bool arg_better(float v, int i, float bv, int bi) {
-    return v > bv || (v == bv && i < bi);
-}
-
 template <typename WT, int NSEG, int MODE>
-__global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvArgs a) {
+__global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr int EPL = Elem<WT>::kPer16B;   // elements per lane per 16 bytes
     constexpr int SEGW = 32 * EPL;           // elements per warp segment
+    constexpr int NC = kConsumerWarps * 32;  // consumer threads
     const int K = a.K;
     const uint32_t row_bytes = (uint32_t)K * (uint32_t)sizeof(WT);
-    const uint32_t stage_bytes = kStageRows * row_bytes;
     uint8_t *ring = smem;
-    float *xs = reinterpret_cast<float *>(smem + (size_t)a.nst * stage_bytes);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(xs + K);
-    float *red = reinterpret_cast<float *>(bars + a.nst);   // [2][8 rows][8 parts]
-    float *misc = red + 128;                                 // [32]
-    int *misc_i = reinterpret_cast<int *>(misc + 16);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)a.nst * kSlotBytes);
+    uint64_t *empty = full + a.nst;
+    float *gsm = reinterpret_cast<float *>(empty + a.nst);   // [K] RMSNorm gamma (16-byte aligned)
+    float *misc = gsm + K;                                   // [64]
+    int *misc_i = reinterpret_cast<int *>(misc + 32);
+    float *xin = misc + 64;                                  // [K] input vector
+    float *res = xin + K;                                    // [rows_max][rs]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int units = a.rows / a.unit;
@@ -61,177 +59,161 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvArgs a) {
     const int u1 = (int)((long long)units * (blockIdx.x + 1) / gridDim.x);
     const int row0 = u0 * a.unit;
     const int nrows = (u1 - u0) * a.unit;
-    const int nstages = (nrows + kStageRows - 1) / kStageRows;
-    const WT *W = MODE == GEMV_HEAD ? reinterpret_cast<const WT *>(a.W_table[a.st->head_idx])
-                                    : reinterpret_cast<const WT *>(a.W);
-    const uint8_t *Wb = reinterpret_cast<const uint8_t *>(W) + (size_t)row0 * row_bytes;
+    const int rps = a.rps;
+    const int nstages = (nrows + rps - 1) / rps;
 
     if (tid == 0) {
-        for (int i = 0; i < a.nst; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < a.nst; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kConsumerWarps);
+        }
+        misc_i[4] = 0;   // failure flag
         fence_barrier_init();
-        const uint64_t pol = a.evict_last ? policy_evict_last() : policy_evict_first();
-        const int pre = nstages < a.nst ? nstages : a.nst;
-        for (int s = 0; s < pre; ++s) {
-            const int r = s * kStageRows;
-            const int n = nrows - r < kStageRows ? nrows - r : kStageRows;
-            mbar_arrive_expect_tx(&bars[s], n * row_bytes);
-            bulk_copy_g2s(ring + (size_t)s * stage_bytes, Wb + (size_t)r * row_bytes, n * row_bytes, &bars[s], pol);
-        }
-    }
-
-    // ---- activations: wait for the producer kernel
-    pdl_wait();
-    if (MODE == GEMV_RES) {
-        for (int i = tid; i < K; i += kGemvThreads) xs[i] = a.in[i];
-    } else {
-        float ss = 0.f;
-        for (int i = tid; i < K; i += kGemvThreads) {
-            const float v = a.in[i];
-            xs[i] = v;
-            ss = fmaf(v, v, ss);
-        }
-        ss = warp_sum(ss);
-        if (lane == 0) misc[warp] = ss;
-        __syncthreads();
-        float tot = 0.f;
-#pragma unroll
-        for (int w = 0; w < kGemvThreads / 32; ++w) tot += misc[w];
-        const float inv = 1.0f / sqrtf(tot / (float)K + a.eps);
-        const bool wy = (MODE == GEMV_HEAD) && blockIdx.x == 0 && a.y_out != nullptr;
-        for (int i = tid; i < K; i += kGemvThreads) {
-            const float v = xs[i] * inv * a.gamma[i];
-            xs[i] = v;
-            if (wy) a.y_out[i] = v;
-        }
     }
     __syncthreads();
-    pdl_launch_dependents();
 
+    const Ring R{ring, full, empty, a.nst};
+    if (warp == kConsumerWarps) {
+        // ---------------- producer: stream this CTA's rows through the ring
+        if (lane == 0 && nstages > 0) {
+            const WT *W = MODE == GEMV_HEAD ? reinterpret_cast<const WT *>(a.W_table[a.st->head_idx])
+                                            : reinterpret_cast<const WT *>(a.W);
+            const uint8_t *Wb = reinterpret_cast<const uint8_t *>(W) + (size_t)row0 * row_bytes;
+            uint32_t sidx = 0;
+            if (!produce_rows(R, sidx, Wb, nrows, row_bytes, rps,
+                              a.evict_last ? policy_evict_last() : policy_evict_first()))
+                atomicOr(&a.st->status, DEV_ERR_WAIT_TIMEOUT);
+        }
+        return;
+    }
+
+    // ---------------- consumers
     const int rs = a.rs;
     const int sub = warp % rs;
     const int rr = warp / rs;
-    const int rows_per_pass = (kGemvThreads / 32) / rs;
+    const int rpp = kConsumerWarps / rs;
     const int colbase = sub * (K / rs);
     float xr[NSEG * EPL];
-#pragma unroll
-    for (int sg = 0; sg < NSEG; ++sg) {
-#pragma unroll
-        for (int e = 0; e < EPL; e += 4) {
-            const float4 v4 = *reinterpret_cast<const float4 *>(xs + colbase + sg * SEGW + lane * EPL + e);
-            xr[sg * EPL + e + 0] = v4.x;
-            xr[sg * EPL + e + 1] = v4.y;
-            xr[sg * EPL + e + 2] = v4.z;
-            xr[sg * EPL + e + 3] = v4.w;
-        }
+    if (MODE != GEMV_RES) {
+        // gamma is a weight: stage it in shared memory before waiting on the previous kernel
+        for (int i = tid * 4; i < K; i += NC * 4)
+            *reinterpret_cast<float4 *>(gsm + i) = *reinterpret_cast<const float4 *>(a.gamma + i);
+    }
+    uint32_t *emw = reinterpret_cast<uint32_t *>(res + a.rows_max * a.rs);   // HEAD: emitted words of the rows
+    const int w0 = row0 >> 5;
+    const int nw = nrows > 0 ? ((row0 + nrows - 1) >> 5) - w0 + 1 : 0;
+    if (MODE == GEMV_HEAD && a.penalty != 1.0f) {
+        // the emitted set was last written by the first kernel of this step, at least
+        // two launches back, so it is complete before griddepcontrol.wait
+        for (int i = tid; i < nw; i += NC) emw[i] = __ldcg(a.emitted + w0 + i);
+    }
+    pdl_wait();
+    // RES: the residual rows this CTA updates, fetched now rather than in the epilogue
+    float xold = 0.f;
+    if (MODE == GEMV_RES && tid < nrows) xold = __ldcg(a.out + row0 + tid);
+
+    if (a.input_mode) {
+        // first kernel of the step: resolve the step's input vector
+        const StepInput in{a.table, a.table_rows, a.vocab, a.S, a.embed_in, a.stage_tokens, a.stage_embeds,
+                           a.emitted_w};
+        step_input_slice<WT, NSEG>(in, a.st, K, rs, colbase, xr, misc_i, a.x_out, nullptr);
+    } else {
+        load_vec_smem(a.in, K, xin);
+        named_sync(1, NC);
+        smem_slice<WT, NSEG>(xin, colbase, xr);
     }
 
-    float best_v = -INFINITY;
-    int best_i = INT_MAX;
-    bool failed = false;
-    int s = 0;
-    for (; s < nstages; ++s) {
-        const int slot = s % a.nst;
-        const bool ok = mbar_wait_bounded(&bars[slot], (uint32_t)((s / a.nst) & 1));
-        if (__syncthreads_or(!ok)) {
-            failed = true;
-            break;
-        }
-        const uint8_t *sbase = ring + (size_t)slot * stage_bytes;
-        const int rbase = s * kStageRows;
-        const int nr = nrows - rbase < kStageRows ? nrows - rbase : kStageRows;
-        float *redb = red + (s & 1) * 64;
-        for (int ps = 0; ps < rs; ++ps) {
-            const int r = ps * rows_per_pass + rr;
-            if (r < nr) {
-                const WT *wrow = reinterpret_cast<const WT *>(sbase + (size_t)r * row_bytes) + colbase;
-                float acc = 0.f;
-#pragma unroll
-                for (int sg = 0; sg < NSEG; ++sg) {
-                    const uint4 u = *reinterpret_cast<const uint4 *>(wrow + sg * SEGW + lane * EPL);
-                    float f[EPL];
-                    Elem<WT>::unpack(u, f);
-#pragma unroll
-                    for (int e = 0; e < EPL; ++e) acc = fmaf(f[e], xr[sg * EPL + e], acc);
-                }
-                acc = warp_sum(acc);
-                if (lane == 0) redb[r * 8 + sub] = acc;
-            }
-        }
-        __syncthreads();  // slot consumed, partial sums complete
-        if (tid == 0 && s + a.nst < nstages) {
-            const int s2 = s + a.nst;
-            const int r = s2 * kStageRows;
-            const int n = nrows - r < kStageRows ? nrows - r : kStageRows;
-            const uint64_t pol = a.evict_last ? policy_evict_last() : policy_evict_first();
-            mbar_arrive_expect_tx(&bars[slot], n * row_bytes);
-            bulk_copy_g2s(ring + (size_t)slot * stage_bytes, Wb + (size_t)r * row_bytes, n * row_bytes, &bars[slot],
-                          pol);
-        }
-        if (MODE == GEMV_GU) {
-            if (tid < nr / 2) {
-                float g = 0.f, u = 0.f;
-                for (int j = 0; j < rs; ++j) {
-                    g += redb[(2 * tid) * 8 + j];
-                    u += redb[(2 * tid + 1) * 8 + j];
-                }
-                const float sg = g / (1.0f + expf(-g));
-                a.out[(row0 + rbase) / 2 + tid] = sg * u;
-            }
-        } else if (tid < nr) {
-            float v = 0.f;
-            for (int j = 0; j < rs; ++j) v += redb[tid * 8 + j];
-            const int row = row0 + rbase + tid;
-            if (MODE == GEMV_QKV) {
-                a.out[row] = v;
-            } else if (MODE == GEMV_RES) {
-                a.out[row] += v;
-            } else {  // GEMV_HEAD
-                if (a.out) a.out[row] = v;
-                if (a.penalty != 1.0f && ((a.emitted[row >> 5] >> (row & 31)) & 1u))
-                    v = v > 0.f ? v / a.penalty : v * a.penalty;
-                if (row == a.eos) v = -INFINITY;
-                if (arg_better(v, row, best_v, best_i)) {
-                    best_v = v;
-                    best_i = row;
-                }
-            }
-        }
-    }
+    if (MODE != GEMV_RES)
+        rmsnorm_slice<WT, NSEG>(xr, gsm, K, rs, colbase, a.eps, misc,
+                                (MODE == GEMV_HEAD && blockIdx.x == 0) ? a.y_out : nullptr);
+    pdl_launch_dependents();
 
-    if (failed) {
+    // ---------------- stage loop
+    uint32_t sidx = 0;
+    const bool ok = gemv_consume<WT, NSEG>(R, sidx, nrows, rps, row_bytes, rs, colbase, xr, res);
+    if (!ok && lane == 0) {
+        atomicOr(&a.st->status, DEV_ERR_WAIT_TIMEOUT);
+        misc_i[4] = 1;
+    }
+    named_sync(1, NC);
+    if (misc_i[4]) {
         if (tid == 0) {
-            atomicOr(&a.st->status, DEV_ERR_WAIT_TIMEOUT);
             // let copies still in flight land before the CTA's shared memory is released
-            for (int s2 = s; s2 < nstages && s2 < s + a.nst; ++s2)
-                (void)mbar_wait_bounded(&bars[s2 % a.nst], (uint32_t)((s2 / a.nst) & 1));
+            for (uint32_t s2 = sidx; s2 < (uint32_t)nstages && s2 < sidx + (uint32_t)a.nst; ++s2)
+                (void)mbar_wait_bounded(&full[s2 % a.nst], (s2 / a.nst) & 1, 10000000ull);
         }
-        __syncthreads();
         if (MODE != GEMV_HEAD) return;
     }
 
-    if (MODE == GEMV_HEAD) {
-        // CTA argmax over its rows (threads 0..7 hold the candidates)
-        if (warp == 0) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, best_v, o);
-                const int oi = __shfl_xor_sync(0xffffffffu, best_i, o);
-                if (arg_better(ov, oi, best_v, best_i)) {
-                    best_v = ov;
-                    best_i = oi;
-                }
+    // ---------------- epilogue over all rows of the CTA
+    if (MODE == GEMV_GU) {
+        for (int i = tid; i < nrows / 2; i += NC) {
+            float g = 0.f, u = 0.f;
+            for (int j = 0; j < rs; ++j) {
+                g += res[(2 * i) * rs + j];
+                u += res[(2 * i + 1) * rs + j];
             }
-            if (lane == 0) {
-                a.part_v[blockIdx.x] = best_v;
-                a.part_i[blockIdx.x] = best_i;
-                __threadfence();
-                const int prev = atomicAdd(a.counter, 1);
-                misc_i[0] = (prev == (int)gridDim.x - 1);
+            a.out[row0 / 2 + i] = g / (1.0f + expf(-g)) * u;
+        }
+    } else if (MODE == GEMV_QKV) {
+        for (int r = tid; r < nrows; r += NC) {
+            float v = 0.f;
+            for (int j = 0; j < rs; ++j) v += res[r * rs + j];
+            a.out[row0 + r] = v;
+        }
+    } else if (MODE == GEMV_RES) {
+        if (tid < nrows) {
+            float v = 0.f;
+            for (int j = 0; j < rs; ++j) v += res[tid * rs + j];
+            a.out[row0 + tid] = xold + v;
+        }
+    } else {  // GEMV_HEAD
+        float best_v = -INFINITY;
+        int best_i = INT_MAX;
+        for (int r = tid; r < nrows; r += NC) {
+            float v = 0.f;
+            for (int j = 0; j < rs; ++j) v += res[r * rs + j];
+            const int row = row0 + r;
+            if (a.out) a.out[row] = v;
+            if (a.penalty != 1.0f && ((emw[(row >> 5) - w0] >> (row & 31)) & 1u))
+                v = v > 0.f ? v / a.penalty : v * a.penalty;
+            if (row == a.eos) v = -INFINITY;
+            if (arg_better(v, row, best_v, best_i)) {
+                best_v = v;
+                best_i = row;
             }
         }
-        __syncthreads();
-        if (misc_i[0] && warp == 0) {
-            // last CTA: reduce the per-CTA candidates
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, best_v, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, best_i, o);
+            if (arg_better(ov, oi, best_v, best_i)) {
+                best_v = ov;
+                best_i = oi;
+            }
+        }
+        if (lane == 0) {
+            misc[8 + warp] = best_v;
+            misc_i[8 + warp] = best_i;
+        }
+        named_sync(1, NC);
+        if (tid == 0) {
+            float bv = misc[8];
+            int bi = misc_i[8];
+            for (int w = 1; w < kConsumerWarps; ++w)
+                if (arg_better(misc[8 + w], misc_i[8 + w], bv, bi)) {
+                    bv = misc[8 + w];
+                    bi = misc_i[8 + w];
+                }
+            a.part_v[blockIdx.x] = bv;
+            a.part_i[blockIdx.x] = bi;
+            __threadfence();
+            const int prev = atomicAdd(a.counter, 1);
+            misc_i[5] = (prev == (int)gridDim.x - 1);
+        }
+        named_sync(1, NC);
+        if (misc_i[5] && warp == 0) {
+            // last CTA: reduce the per-CTA candidates, publish the id, advance the position
             __threadfence();
             float bv = -INFINITY;
             int bi = INT_MAX;
@@ -261,234 +243,151 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(const GemvArgs a) {
                     if (n < a.ids_cap) a.ids[n] = bi;
                     else atomicOr(&st->status, DEV_ERR_IDS_FULL);
                     st->n_gen = n + 1;
+                    st->pos = st->pos + 1;
                 }
             }
         }
     }
+    if (a.advance_pos && blockIdx.x == 0 && tid == 0) a.st->pos = a.st->pos + 1;
 }
 
 // =====================================================================================
-// Attention over the cache, one CTA per (kv group g, split s of kAttnChunk positions).
+// Attention over the cache.  Grid (kv group g, split s); the kAttnMaxSplits CTAs of a
+// group form one thread-block cluster.  The split size is attn_chunk(L), a function
+// of the attended length L only, so a bucket migration cannot change the partition.
 // Prologue: QK-RMSNorm and RoPE of the group's q heads and of k, rounding of k and v
 // to the cache type and, in the CTA whose split holds position p, the KV append.
 // Body: scores, softmax and P.V of the split for every q head of the group (GQA: the
-// group's K/V rows are read once for all of its q heads).  The last CTA of a group to
-// finish merges the splits in split order (flash-decoding combine), so the result
-// does not depend on which CTA finishes last, nor on Smax.
+// group's K/V rows are read once for all of its q heads).  The splits are then merged
+// through distributed shared memory (flash-decoding combine, splits in index order):
+// CTA rank r of the cluster produces slice r of the group's outputs.
 // =====================================================================================
 
 template <typename KT, int HD>
 __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
-    constexpr int C = kAttnChunk;
     constexpr int HALF = HD / 2;
     const int G = a.qh / a.kvh;
+    const int CM = a.chunk_max;
     KT *Ks = reinterpret_cast<KT *>(smem);
-    KT *Vs = Ks + C * HD;
-    float *qs = reinterpret_cast<float *>(Vs + C * HD);  // [G][HD]
-    float *kn = qs + G * HD;                             // [HD]
-    float *vn = kn + HD;                                 // [HD]
-    float *sc = vn + HD;                                 // [G][C]
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sc + G * C);
-    int *flag = reinterpret_cast<int *>(bar + 1);
+    KT *Vs = Ks + (size_t)CM * HD;
+    float *qs = reinterpret_cast<float *>(Vs + (size_t)CM * HD);  // [G][HD]
+    float *kn = qs + G * HD;                                       // [HD]
+    float *vn = kn + HD;                                           // [HD]
+    float *rc = vn + HD;                                           // [HALF] cos, [HALF] sin
+    float *sc = rc + HD;                                           // [G][CM]
+    float *po = sc + G * CM;                                       // [G][HD] split output (unnormalised)
+    float *pm = po + G * HD;                                       // [G] split max
+    float *pl = pm + G;                                            // [G] split exp-sum
+    // mbarrier: 8-byte aligned, after the G split sums
+    uint64_t *bar = reinterpret_cast<uint64_t *>((reinterpret_cast<uintptr_t>(pl + G) + 7) & ~uintptr_t(7));
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = blockIdx.x, s = blockIdx.y;
-    // The step's position was claimed by the first kernel of the step, at least two
+    // The position was advanced by the previous step's last kernel, at least two
     // launches back, so it is complete and visible before griddepcontrol.wait.
-    const int p = a.st->cur;
+    const int p = a.st->pos;
     const int L = p + 1;
-    const int nsplit = (L + C - 1) / C;
-    if (s >= nsplit) return;
-    if (p >= a.S) {
-        if (tid == 0 && s == 0 && g == 0) atomicOr(&a.st->status, DEV_ERR_BAD_POS);
-        return;
-    }
-    const int j0 = s * C;
-    const int n = L - j0 < C ? L - j0 : C;
-    const int n_old = (p - j0) < n ? (p - j0) : n;   // cached rows [j0, j0 + n_old)
-    const size_t grp_off = (size_t)g * a.S * HD;
-    const KT *kc = reinterpret_cast<const KT *>(a.kcache) + grp_off;
-    const KT *vc = reinterpret_cast<const KT *>(a.vcache) + grp_off;
+    const int C = attn_chunk(L);
+    const int nsplit = attn_splits(L);
+    const bool valid = p < a.S && C <= CM;
+    const bool active = valid && s < nsplit;
+    if (!valid && tid == 0 && s == 0 && g == 0) atomicOr(&a.st->status, DEV_ERR_BAD_POS);
 
-    if (tid == 0) {
-        mbar_init(bar, 1);
-        fence_barrier_init();
-        const uint32_t bytes = (uint32_t)(n_old * HD * sizeof(KT));
-        mbar_arrive_expect_tx(bar, 2 * bytes);
-        if (bytes) {
-            const uint64_t pol = policy_evict_first();
-            bulk_copy_g2s(Ks, kc + (size_t)j0 * HD, bytes, bar, pol);
-            bulk_copy_g2s(Vs, vc + (size_t)j0 * HD, bytes, bar, pol);
+    bool ok = true;
+    if (active) {
+        const int j0 = s * C;
+        const int n = L - j0 < C ? L - j0 : C;
+        const int n_old = (p - j0) < n ? (p - j0) : n;   // cached rows [j0, j0 + n_old)
+        const size_t grp_off = (size_t)g * a.S * HD;
+        const KT *kc = reinterpret_cast<const KT *>(a.kcache) + grp_off;
+        const KT *vc = reinterpret_cast<const KT *>(a.vcache) + grp_off;
+        if (tid == 0) {
+            mbar_init(bar, 1);
+            fence_barrier_init();
+            const uint32_t bytes = (uint32_t)(n_old * HD * sizeof(KT));
+            mbar_arrive_expect_tx(bar, 2 * bytes);
+            if (bytes) {
+                const uint64_t pol = policy_evict_first();
+                bulk_copy_g2s(Ks, kc + (size_t)j0 * HD, bytes, bar, pol);
+                bulk_copy_g2s(Vs, vc + (size_t)j0 * HD, bytes, bar, pol);
+            }
         }
-    }
-
-    pdl_wait();
-    const float *qsrc = a.qkv + (size_t)g * G * HD;
-    const float *ksrc = a.qkv + (size_t)a.qh * HD + (size_t)g * HD;
-    const float *vsrc = a.qkv + (size_t)(a.qh + a.kvh) * HD + (size_t)g * HD;
-    for (int i = tid; i < G * HD; i += kAttnThreads) qs[i] = qsrc[i];
-    for (int i = tid; i < HD; i += kAttnThreads) {
-        kn[i] = ksrc[i];
-        vn[i] = vsrc[i];
-    }
-    __syncthreads();
-    if (a.q_gamma) {
-        // QK-norm: RMSNorm over head_dim of each q head and of k (one warp per vector)
-        for (int hh = warp; hh <= G; hh += kAttnThreads / 32) {
-            float *v = hh < G ? qs + hh * HD : kn;
-            const float *gam = hh < G ? a.q_gamma : a.k_gamma;
-            float ss = 0.f;
-            for (int i = lane; i < HD; i += 32) ss = fmaf(v[i], v[i], ss);
-            ss = warp_sum(ss);
-            const float inv = 1.0f / sqrtf(ss / (float)HD + a.eps);
-            for (int i = lane; i < HD; i += 32) v[i] = v[i] * inv * gam[i];
+        // RoPE table row of position p: constant data
+        for (int m = tid; m < HALF; m += kAttnThreads) {
+            rc[m] = a.rope_cos[(size_t)p * HALF + m];
+            rc[HALF + m] = a.rope_sin[(size_t)p * HALF + m];
+        }
+        pdl_wait();
+        pdl_launch_dependents();
+        const float *qsrc = a.qkv + (size_t)g * G * HD;
+        const float *ksrc = a.qkv + (size_t)a.qh * HD + (size_t)g * HD;
+        const float *vsrc = a.qkv + (size_t)(a.qh + a.kvh) * HD + (size_t)g * HD;
+        for (int i = tid; i < G * HD; i += kAttnThreads) qs[i] = __ldcg(qsrc + i);
+        for (int i = tid; i < HD; i += kAttnThreads) {
+            kn[i] = __ldcg(ksrc + i);
+            vn[i] = __ldcg(vsrc + i);
         }
         __syncthreads();
-    }
-    // RoPE at position p: pairs (m, m + HD/2)
-    {
-        const float *cs = a.rope_cos + (size_t)p * HALF;
-        const float *sn = a.rope_sin + (size_t)p * HALF;
-        for (int idx = tid; idx < (G + 1) * HALF; idx += kAttnThreads) {
-            const int hh = idx / HALF, m = idx % HALF;
-            float *v = hh < G ? qs + hh * HD : kn;
-            const float c = cs[m], si = sn[m];
-            const float x0 = v[m], x1 = v[m + HALF];
-            v[m] = x0 * c - x1 * si;
-            v[m + HALF] = x1 * c + x0 * si;
+        qk_norm_rope<HD, kAttnThreads / 32>(qs, kn, G, a.q_gamma, a.k_gamma, a.eps, rc, 1);
+        if (n_old < n) {
+            // this split holds position p: append the new row (cache type) to the cache
+            KT *kw = reinterpret_cast<KT *>(a.kcache) + grp_off + (size_t)p * HD;
+            KT *vw = reinterpret_cast<KT *>(a.vcache) + grp_off + (size_t)p * HD;
+            for (int i = tid; i < HD; i += kAttnThreads) {
+                Elem<KT>::store(Ks + n_old * HD, i, kn[i]);
+                Elem<KT>::store(Vs + n_old * HD, i, vn[i]);
+                Elem<KT>::store(kw, i, kn[i]);
+                Elem<KT>::store(vw, i, vn[i]);
+            }
+            fence_proxy_async_global();
         }
-    }
-    __syncthreads();
-    if (n_old < n) {
-        // this split holds position p: append the new row (cache type) to the cache
-        KT *kw = reinterpret_cast<KT *>(a.kcache) + grp_off + (size_t)p * HD;
-        KT *vw = reinterpret_cast<KT *>(a.vcache) + grp_off + (size_t)p * HD;
-        for (int i = tid; i < HD; i += kAttnThreads) {
-            Elem<KT>::store(Ks + n_old * HD, i, kn[i]);
-            Elem<KT>::store(Vs + n_old * HD, i, vn[i]);
-            Elem<KT>::store(kw, i, kn[i]);
-            Elem<KT>::store(vw, i, vn[i]);
+        const bool got = mbar_wait_bounded(bar, 0);
+        if (__syncthreads_or(!got)) {
+            if (tid == 0) {
+                atomicOr(&a.st->status, DEV_ERR_WAIT_TIMEOUT);
+                (void)mbar_wait_bounded(bar, 0, 10000000ull);
+            }
+            ok = false;
         }
-        fence_proxy_async_global();
+        if (ok) attn_split<KT, HD, kAttnThreads / 32>(Ks, Vs, qs, G, n, CM, a.scale, sc, po, pm, pl, 1);
+    } else {
+        pdl_wait();
+        pdl_launch_dependents();
     }
-    pdl_launch_dependents();
-    const bool ok = mbar_wait_bounded(bar, 0);
-    if (__syncthreads_or(!ok)) {
-        if (tid == 0) {
-            atomicOr(&a.st->status, DEV_ERR_WAIT_TIMEOUT);
-            (void)mbar_wait_bounded(bar, 0);
+    if (!active || !ok) {
+        for (int hh = tid; hh < G; hh += kAttnThreads) {
+            pm[hh] = -INFINITY;
+            pl[hh] = 0.f;
         }
-        return;
     }
 
-    // scores: warp per position, lanes over head_dim
-    constexpr int DPL = HD / 32;
-    for (int j = warp; j < n; j += kAttnThreads / 32) {
-        float kr[DPL];
+    // ---- merge the splits of group g across the cluster
+    cluster_sync();
+    if (valid) {
+        const int per = G * HD / kAttnMaxSplits;
+        for (int i = tid; i < per; i += kAttnThreads) {
+            const int idx = s * per + i;
+            const int hh = idx / HD;
+            float m_t[kAttnMaxSplits], M = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) kr[e] = Elem<KT>::load(Ks + j * HD, lane * DPL + e);
-        for (int hh = 0; hh < G; ++hh) {
-            float d = 0.f;
+            for (int t = 0; t < kAttnMaxSplits; ++t) {
+                m_t[t] = t < nsplit ? ld_cluster_f32(cluster_map(pm + hh, t)) : -INFINITY;
+                M = fmaxf(M, m_t[t]);
+            }
+            float num = 0.f, den = 0.f;
 #pragma unroll
-            for (int e = 0; e < DPL; ++e) d = fmaf(qs[hh * HD + lane * DPL + e], kr[e], d);
-            d = warp_sum(d);
-            if (lane == 0) sc[hh * C + j] = d * a.scale;
+            for (int t = 0; t < kAttnMaxSplits; ++t) {
+                if (t < nsplit) {
+                    const float w = expf(m_t[t] - M);
+                    num = fmaf(ld_cluster_f32(cluster_map(po + idx, t)), w, num);
+                    den = fmaf(ld_cluster_f32(cluster_map(pl + hh, t)), w, den);
+                }
+            }
+            a.out[(size_t)g * G * HD + idx] = num / den;
         }
     }
-    __syncthreads();
-    float *part_base = a.part;
-    const int stride = HD + 2;
-    for (int hh = warp; hh < G; hh += kAttnThreads / 32) {
-        const float v = lane < n ? sc[hh * C + lane] : -INFINITY;
-        const float mx = warp_max(v);
-        const float e = lane < n ? expf(v - mx) : 0.f;
-        const float l = warp_sum(e);
-        if (lane < n) sc[hh * C + lane] = e;
-        if (lane == 0) {
-            float *pp = part_base + ((size_t)(g * G + hh) * a.max_splits + s) * stride;
-            pp[HD] = mx;
-            pp[HD + 1] = l;
-        }
-    }
-    __syncthreads();
-    for (int idx = tid; idx < G * HD; idx += kAttnThreads) {
-        const int hh = idx / HD, d = idx % HD;
-        float o = 0.f;
-        for (int j = 0; j < n; ++j) o = fmaf(sc[hh * C + j], Elem<KT>::load(Vs + j * HD, d), o);
-        part_base[((size_t)(g * G + hh) * a.max_splits + s) * stride + d] = o;
-    }
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        const int prev = atomicAdd(&a.counter[g], 1);
-        *flag = (prev == nsplit - 1);
-    }
-    __syncthreads();
-    if (!*flag) return;
-    __threadfence();
-    for (int idx = tid; idx < G * HD; idx += kAttnThreads) {
-        const int hh = idx / HD, d = idx % HD;
-        const float *base = part_base + (size_t)(g * G + hh) * a.max_splits * stride;
-        float M = -INFINITY;
-        for (int t = 0; t < nsplit; ++t) M = fmaxf(M, __ldcg(base + (size_t)t * stride + HD));
-        float num = 0.f, den = 0.f;
-        for (int t = 0; t < nsplit; ++t) {
-            const float w = expf(__ldcg(base + (size_t)t * stride + HD) - M);
-            num = fmaf(__ldcg(base + (size_t)t * stride + d), w, num);
-            den = fmaf(__ldcg(base + (size_t)t * stride + HD + 1), w, den);
-        }
-        a.out[(size_t)(g * G + hh) * HD + d] = num / den;
-    }
-    if (tid == 0) a.counter[g] = 0;
-}
-
-// =====================================================================================
-// Step input: claim the position, pick the token or embedding, record the emitted id.
-// =====================================================================================
-
-__global__ void __launch_bounds__(256) embed_kernel(const EmbedArgs a) {
-    __shared__ int s_tok, s_mode, s_cur, s_bad;
-    pdl_wait();
-    if (threadIdx.x == 0) {
-        DevState *st = a.st;
-        const int cur = st->pos;
-        st->cur = cur;
-        st->pos = cur + 1;
-        const int mode = st->in_mode;
-        int tok = st->token_in;
-        if (mode == IN_FEEDBACK) tok = st->out_id;
-        else if (mode == IN_STAGED_TOKENS) tok = cur < a.S ? a.stage_tokens[cur] : -1;
-        else if (mode == IN_STAGED_EMBEDS) tok = -1;
-        int bad = 0;
-        if (cur >= a.S) {
-            // never index the staged inputs outside the bucket
-            bad = 1;
-            atomicOr(&st->status, DEV_ERR_BAD_POS);
-        }
-        const bool needs_row = (mode == IN_TOKEN || mode == IN_FEEDBACK || mode == IN_STAGED_TOKENS);
-        if (!bad && needs_row && (tok < 0 || tok >= a.rows || a.table == nullptr)) {
-            bad = 1;
-            atomicOr(&st->status, DEV_ERR_BAD_TOKEN);
-        }
-        if (st->add_emitted && tok >= 0 && tok < a.vocab) a.emitted[tok >> 5] |= 1u << (tok & 31);
-        s_tok = tok;
-        s_mode = mode;
-        s_cur = cur;
-        s_bad = bad;
-    }
-    __syncthreads();
-    const int mode = s_mode, tok = s_tok;
-    for (int i = threadIdx.x; i < a.hidden; i += blockDim.x) {
-        float v;
-        if (s_bad) v = 0.f;
-        else if (mode == IN_EMBED) v = a.embed_in[i];
-        else if (mode == IN_STAGED_EMBEDS) v = a.stage_embeds[(size_t)s_cur * a.hidden + i];
-        else if (a.bf16) v = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(a.table)[(size_t)tok * a.hidden + i]);
-        else v = reinterpret_cast<const float *>(a.table)[(size_t)tok * a.hidden + i];
-        a.x[i] = v;
-    }
-    pdl_launch_dependents();
+    cluster_sync();   // no CTA leaves while another may still read its shared memory
 }
 
 // =====================================================================================
@@ -549,7 +448,7 @@ bool gemv_split(int K, bool bf16, int *nseg, int *rs) {
     const int segw = bf16 ? 256 : 128;
     if (K <= 0 || K % segw) return false;
     const int t = K / segw;
-    for (int r = 1; r <= 8; r *= 2) {
+    for (int r = 1; r <= kConsumerWarps; r *= 2) {
         if (t % r == 0 && t / r <= 4) {
             *nseg = t / r;
             *rs = r;
@@ -559,9 +458,9 @@ bool gemv_split(int K, bool bf16, int *nseg, int *rs) {
     return false;
 }
 
-size_t gemv_smem_bytes(int K, bool bf16, int nst) {
-    const size_t row = (size_t)K * (bf16 ? 2 : 4);
-    return (size_t)nst * kStageRows * row + (size_t)K * 4 + (size_t)nst * 8 + 128 * 4 + 32 * 4;
+size_t gemv_smem_bytes(int nst, int rows_max, int rs, int K) {
+    return (size_t)nst * kSlotBytes + (size_t)nst * 16 + (size_t)rows_max * rs * 4 + 64 * 4 + 2 * (size_t)K * 4 +
+           ((size_t)rows_max / 32 + 2) * 4;
 }
 
 typedef void (*GemvFn)(const GemvArgs);
@@ -599,7 +498,7 @@ static AttnFn attn_fn(bool bf16, int hd) {
 }
 
 cudaError_t kernels_init() {
-    const int max_smem = 200 * 1024;
+    const int max_smem = 220 * 1024;
     for (int bf = 0; bf < 2; ++bf)
         for (int mode = 0; mode < 4; ++mode)
             for (int ns = 1; ns <= 4; ++ns) {
@@ -610,7 +509,7 @@ cudaError_t kernels_init() {
     for (int bf = 0; bf < 2; ++bf)
         for (int hd = 64; hd <= 128; hd *= 2) {
             cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(attn_fn(bf, hd)),
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 64 * 1024);
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
             if (e != cudaSuccess) return e;
         }
     return cudaSuccess;
@@ -624,20 +523,31 @@ cudaError_t launch_gemv(int mode, bool bf16, const GemvArgs &a, int grid, size_t
     return launch_ex(f, dim3(grid), dim3(kGemvThreads), smem, s, pdl, &a);
 }
 
-size_t attention_smem_bytes(bool bf16, int hd, int group) {
+size_t attention_smem_bytes(bool bf16, int hd, int group, int chunk_max) {
     const size_t es = bf16 ? 2 : 4;
-    return 2 * (size_t)kAttnChunk * hd * es + (size_t)group * hd * 4 + 2 * (size_t)hd * 4 +
-           (size_t)group * kAttnChunk * 4 + 16 + 16;
+    return 2 * (size_t)chunk_max * hd * es + (size_t)group * hd * 4 + 3 * (size_t)hd * 4 +
+           (size_t)group * chunk_max * 4 + (size_t)group * hd * 4 + (2 * (size_t)group + 2) * 4 + 16;
 }
 
-cudaError_t launch_attention(bool bf16, int hd, const AttnArgs &a, int max_splits, cudaStream_t s, bool pdl) {
+cudaError_t launch_attention(bool bf16, int hd, const AttnArgs &a, cudaStream_t s, bool pdl) {
     AttnFn f = attn_fn(bf16, hd);
-    const size_t smem = attention_smem_bytes(bf16, hd, a.qh / a.kvh);
-    return launch_ex(f, dim3(a.kvh, max_splits), dim3(kAttnThreads), smem, s, pdl, &a);
-}
-
-cudaError_t launch_embed(const EmbedArgs &a, cudaStream_t s, bool pdl) {
-    return launch_ex(embed_kernel, dim3(1), dim3(256), 0, s, pdl, &a);
+    const size_t smem = attention_smem_bytes(bf16, hd, a.qh / a.kvh, a.chunk_max);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.kvh, kAttnMaxSplits);
+    cfg.blockDim = dim3(kAttnThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 1;
+    at[0].val.clusterDim.y = kAttnMaxSplits;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = pdl ? 2 : 1;
+    void *args[1] = {const_cast<AttnArgs *>(&a)};
+    return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(f), args);
 }
 
 cudaError_t launch_kv_migrate(const void *src, int S_old, void *dst, int S_new, int n_segments, size_t row_bytes,

@@ -16,12 +16,12 @@
 namespace qd {
 
 // ------------------------------------------------------------------ device state
-// Lives in device memory, one per handle.  The first kernel of a step reads the
-// input description, claims the position and advances `pos`; the head kernel
-// publishes the id.
+// Lives in device memory, one per handle.  Every kernel of a step works on
+// position `pos`; the last kernel of the step advances it.  The host writes the
+// input description (in_mode .. head_idx) before a step; the head kernel
+// publishes the id (out_id, n_gen) and any error bits (status).
 struct DevState {
-    int pos;          // positions committed to the cache
-    int cur;          // position written by the step in flight
+    int pos;          // positions held in the cache = position written by the step in flight
     int in_mode;      // IN_* below
     int token_in;     // token of the step (IN_TOKEN), -1: none
     int add_emitted;  // the step's token joins the emitted set
@@ -29,8 +29,7 @@ struct DevState {
     int out_id;       // id produced by the last step that ran a head
     int n_gen;        // ids produced since reset (index into the id history)
     int status;       // DEV_ERR_* bits, sticky until reset
-    int smax;         // Smax of the bucket the step runs in (checked by kernels)
-    int pad[6];
+    int pad[8];
 };
 
 enum : int {
@@ -87,12 +86,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for phase `parity` of the barrier to complete; false after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+// Wait for phase `parity` of the barrier to complete; false after `limit_ns`.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+        if (global_timer_ns() - t0 > limit_ns) return false;
     }
     return true;
 }
@@ -120,10 +120,63 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
         : "memory");
 }
 
+// Plain arrive (count 1) on a barrier.
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Barrier among the first `nthreads` threads of the CTA (named barrier `id`).
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---- thread-block clusters: distributed shared memory and the cluster barrier
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Address of `p` (a shared-memory variable of this CTA) in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+// Every thread of every CTA of the cluster arrives; shared-memory writes before it
+// are visible to the whole cluster after it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Named barrier `id` over `nthreads` threads that also ORs a predicate across them.
+__device__ __forceinline__ bool named_sync_or(int id, int nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+
 // Programmatic dependent launch.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Order this thread's generic-proxy shared-memory accesses before later async-proxy
+// (bulk copy) writes into the same shared memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // Order this thread's generic-proxy global writes before later async-proxy reads.

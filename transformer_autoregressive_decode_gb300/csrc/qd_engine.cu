@@ -17,6 +17,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -58,14 +59,14 @@ struct qd_model {
 
     // step scratch
     void *scratch = nullptr;
-    float *x = nullptr, *qkv = nullptr, *att = nullptr, *act = nullptr, *part = nullptr, *y = nullptr;
+    float *x = nullptr, *qkv = nullptr, *att = nullptr, *act = nullptr, *y = nullptr;
     float *embed_in = nullptr, *stage_embeds = nullptr, *head_pv = nullptr;
-    int *attn_cnt = nullptr, *head_cnt = nullptr, *head_pi = nullptr, *stage_tokens = nullptr;
+    int *head_cnt = nullptr, *head_pi = nullptr, *stage_tokens = nullptr;
     int32_t *ids = nullptr;
     uint32_t *emitted = nullptr;
     DevState *st = nullptr;
     int *pin = nullptr;  // pinned host words: out_id, n_gen, status
-    int max_splits = 0;
+    int chunk_max = 0;
 
     // buckets
     std::vector<void *> kv;                   // per bucket, allocated on first use
@@ -79,8 +80,18 @@ struct qd_model {
     int grid_qkv = 0, grid_o = 0, grid_gu = 0, grid_d = 0, grid_head = 0;
     int rs_h = 0, rs_q = 0, rs_f = 0;
     int nst_qkv = 0, nst_o = 0, nst_gu = 0, nst_d = 0, nst_head = 0;
+    int rps_h = 0, rps_q = 0, rps_f = 0;
+    int rmax_qkv = 0, rmax_o = 0, rmax_gu = 0, rmax_d = 0, rmax_head = 0;
     size_t smem_qkv = 0, smem_o = 0, smem_gu = 0, smem_d = 0, smem_head = 0;
     int evict_last_layers = 0;
+
+    // persistent decode step (one cooperative launch per step)
+    bool persistent = false;
+    LayerDev *d_layers = nullptr;
+    unsigned *barrier = nullptr;
+    float *part_o = nullptr, *part_ml = nullptr;
+    size_t smem_step = 0;
+    int nst_step = 0, off_full = 0, off_gsm = 0, off_misc = 0, off_res = 0, off_att = 0, off_emw = 0, off_xin = 0;
 
     bool use_graphs = true;
     bool use_pdl = true;
@@ -91,7 +102,9 @@ struct qd_model {
     int q_dim() const { return cfg.n_q_heads * cfg.head_dim; }
     int kv_dim() const { return cfg.n_kv_heads * cfg.head_dim; }
     int S() const { return cfg.buckets[cur_bucket]; }
-    int kernels_per_step(bool with_head) const { return 1 + 5 * cfg.n_layers + (with_head ? 1 : 0); }
+    int kernels_per_step(bool with_head) const {
+        return persistent ? 1 : 5 * cfg.n_layers + (with_head ? 1 : 0);
+    }
     size_t kv_bytes(int bucket) const {
         return (size_t)cfg.n_layers * 2 * kv_dim() * (size_t)cfg.buckets[bucket] * esize;
     }
@@ -151,13 +164,18 @@ static qd_status validate_config(qd_model *m, const qd_config *c) {
     if (c->eos_mask_id >= c->vocab) return fail(m, QD_EINVAL, "eos_mask_id >= vocab");
     if (c->n_buckets < 1 || c->n_buckets > QD_MAX_BUCKETS) return fail(m, QD_EINVAL, "n_buckets out of range");
     for (int i = 0; i < c->n_buckets; ++i) {
-        if (c->buckets[i] <= 0 || c->buckets[i] % kAttnChunk)
-            return fail(m, QD_EINVAL, "bucket %d (%d) must be a positive multiple of %d", i, c->buckets[i], kAttnChunk);
+        if (c->buckets[i] <= 0 || c->buckets[i] % 32)
+            return fail(m, QD_EINVAL, "bucket %d (%d) must be a positive multiple of 32", i, c->buckets[i]);
         if (i && c->buckets[i] <= c->buckets[i - 1]) return fail(m, QD_EINVAL, "buckets must ascend");
     }
     if (!(c->rms_eps >= 0.0) || !(c->rope_theta > 0.0) || !(c->rep_penalty > 0.0))
         return fail(m, QD_EINVAL, "rms_eps, rope_theta, rep_penalty out of range");
     const bool bf = c->dtype == QD_BF16;
+    const int max_pos = c->buckets[c->n_buckets - 1];
+    if (c->hidden > 16 * 1024)
+        return fail(m, QD_EUNSUPPORTED, "hidden %d too large", c->hidden);
+    if (attention_smem_bytes(bf, c->head_dim, c->n_q_heads / c->n_kv_heads, attn_chunk(max_pos)) > 160 * 1024)
+        return fail(m, QD_EUNSUPPORTED, "largest bucket %d too long for the attention tile", max_pos);
     int ns, rs;
     const int Ks[3] = {c->hidden, c->n_q_heads * c->head_dim, c->ffn};
     for (int K : Ks)
@@ -204,137 +222,233 @@ static qd_status migrate(qd_model *m, int to) {
     return QD_OK;
 }
 
+// Kernel arguments of the step's launches (shared by the step and by qd_time_kernel).
+static GemvArgs qkv_args(qd_model *m, int l, bool input) {
+    const qd_config &c = m->cfg;
+    GemvArgs g = {};
+    g.rows = m->q_dim() + 2 * m->kv_dim();
+    g.K = c.hidden;
+    g.rs = m->rs_h;
+    g.unit = 1;
+    g.nst = m->nst_qkv;
+    g.rps = m->rps_h;
+    g.rows_max = m->rmax_qkv;
+    g.evict_last = m->evict_last_layers;
+    g.W = m->layers[l].w_qkv;
+    g.in = m->x;
+    g.gamma = m->layers[l].attn_norm;
+    g.eps = (float)c.rms_eps;
+    g.out = m->qkv;
+    g.st = m->st;
+    if (input) {
+        g.input_mode = 1;
+        g.table = m->embed;
+        g.table_rows = c.embed_rows;
+        g.table_bf16 = m->bf16;
+        g.vocab = c.vocab;
+        g.S = m->S();
+        g.embed_in = m->embed_in;
+        g.stage_tokens = m->stage_tokens;
+        g.stage_embeds = m->stage_embeds;
+        g.emitted_w = m->emitted;
+        g.x_out = m->x;
+    }
+    return g;
+}
+
+static AttnArgs attn_args(qd_model *m, int l) {
+    const qd_config &c = m->cfg;
+    const int S = m->S();
+    const size_t layer_kv = (size_t)2 * m->kv_dim() * S * m->esize;
+    AttnArgs a = {};
+    a.qkv = m->qkv;
+    a.q_gamma = c.qk_norm ? m->layers[l].q_norm : nullptr;
+    a.k_gamma = c.qk_norm ? m->layers[l].k_norm : nullptr;
+    a.eps = (float)c.rms_eps;
+    a.scale = (float)(1.0 / std::sqrt((double)c.head_dim));
+    a.rope_cos = m->rope_cos;
+    a.rope_sin = m->rope_sin;
+    uint8_t *kvl = reinterpret_cast<uint8_t *>(m->kv[m->cur_bucket]) + (size_t)l * layer_kv;
+    a.kcache = kvl;
+    a.vcache = kvl + layer_kv / 2;
+    a.S = S;
+    a.qh = c.n_q_heads;
+    a.kvh = c.n_kv_heads;
+    a.chunk_max = m->chunk_max;
+    a.out = m->att;
+    a.st = m->st;
+    return a;
+}
+
+static GemvArgs o_args(qd_model *m, int l) {
+    const qd_config &c = m->cfg;
+    GemvArgs g = {};
+    g.rows = c.hidden;
+    g.K = m->q_dim();
+    g.rs = m->rs_q;
+    g.unit = 1;
+    g.nst = m->nst_o;
+    g.rps = m->rps_q;
+    g.rows_max = m->rmax_o;
+    g.evict_last = m->evict_last_layers;
+    g.W = m->layers[l].w_o;
+    g.in = m->att;
+    g.out = m->x;
+    g.st = m->st;
+    return g;
+}
+
+static GemvArgs gu_args(qd_model *m, int l) {
+    const qd_config &c = m->cfg;
+    GemvArgs g = {};
+    g.rows = 2 * c.ffn;
+    g.K = c.hidden;
+    g.rs = m->rs_h;
+    g.unit = 2;
+    g.nst = m->nst_gu;
+    g.rps = m->rps_h;
+    g.rows_max = m->rmax_gu;
+    g.evict_last = m->evict_last_layers;
+    g.W = m->layers[l].w_gu;
+    g.in = m->x;
+    g.gamma = m->layers[l].mlp_norm;
+    g.eps = (float)c.rms_eps;
+    g.out = m->act;
+    g.st = m->st;
+    return g;
+}
+
+static GemvArgs d_args(qd_model *m, int l) {
+    const qd_config &c = m->cfg;
+    GemvArgs g = {};
+    g.rows = c.hidden;
+    g.K = c.ffn;
+    g.rs = m->rs_f;
+    g.unit = 1;
+    g.nst = m->nst_d;
+    g.rps = m->rps_f;
+    g.rows_max = m->rmax_d;
+    g.evict_last = m->evict_last_layers;
+    g.W = m->layers[l].w_d;
+    g.in = m->act;
+    g.out = m->x;
+    g.st = m->st;
+    return g;
+}
+
+static GemvArgs head_args(qd_model *m, float *logits_tap, int commit) {
+    const qd_config &c = m->cfg;
+    GemvArgs g = {};
+    g.rows = c.vocab;
+    g.K = c.hidden;
+    g.rs = m->rs_h;
+    g.unit = 1;
+    g.nst = m->nst_head;
+    g.rps = m->rps_h;
+    g.rows_max = m->rmax_head;
+    g.evict_last = 0;
+    g.W_table = m->d_heads;
+    g.in = m->x;
+    g.gamma = m->final_norm;
+    g.eps = (float)c.rms_eps;
+    g.out = logits_tap;
+    g.emitted = m->emitted;
+    g.penalty = (float)c.rep_penalty;
+    g.eos = c.eos_mask_id;
+    g.y_out = commit ? m->y : nullptr;
+    g.part_v = m->head_pv;
+    g.part_i = m->head_pi;
+    g.counter = m->head_cnt;
+    g.ids = m->ids;
+    g.ids_cap = kIdsCap;
+    g.commit = commit;
+    g.st = m->st;
+    return g;
+}
+
+static StepArgs step_args(qd_model *m, bool with_head, bool taps) {
+    const qd_config &c = m->cfg;
+    StepArgs a = {};
+    a.layers = m->d_layers;
+    a.n_layers = c.n_layers;
+    a.hidden = c.hidden;
+    a.qh = c.n_q_heads;
+    a.kvh = c.n_kv_heads;
+    a.ffn = c.ffn;
+    a.vocab = c.vocab;
+    a.rs_h = m->rs_h;
+    a.rs_q = m->rs_q;
+    a.rs_f = m->rs_f;
+    a.rps_h = m->rps_h;
+    a.rps_q = m->rps_q;
+    a.rps_f = m->rps_f;
+    a.nst = m->nst_step;
+    a.evict_last = m->evict_last_layers;
+    a.eps = (float)c.rms_eps;
+    a.scale = (float)(1.0 / std::sqrt((double)c.head_dim));
+    a.off_full = m->off_full;
+    a.off_gsm = m->off_gsm;
+    a.off_misc = m->off_misc;
+    a.off_res = m->off_res;
+    a.off_att = m->off_att;
+    a.off_emw = m->off_emw;
+    a.off_xin = m->off_xin;
+    a.kv = m->kv[m->cur_bucket];
+    a.S = m->S();
+    a.chunk_max = m->chunk_max;
+    a.rope_cos = m->rope_cos;
+    a.rope_sin = m->rope_sin;
+    a.x = m->x;
+    a.qkv = m->qkv;
+    a.act = m->act;
+    a.part_o = m->part_o;
+    a.part_ml = m->part_ml;
+    a.in = StepInputArgs{m->embed, c.embed_rows, c.vocab, m->S(), m->embed_in, m->stage_tokens, m->stage_embeds,
+                         m->emitted};
+    a.with_head = with_head ? 1 : 0;
+    a.heads = m->d_heads;
+    a.final_norm = m->final_norm;
+    a.penalty = (float)c.rep_penalty;
+    a.eos = c.eos_mask_id;
+    a.y_out = m->y;
+    a.part_v = m->head_pv;
+    a.part_i = m->head_pi;
+    a.head_counter = m->head_cnt;
+    a.ids = m->ids;
+    a.ids_cap = kIdsCap;
+    a.tap_hidden = taps ? m->tap_hidden : nullptr;
+    a.tap_logits = taps ? m->tap_logits : nullptr;
+    a.barrier = m->barrier;
+    a.st = m->st;
+    return a;
+}
+
 // Enqueue one step's kernels on stream s.
 static qd_status enqueue_step(qd_model *m, cudaStream_t s, bool with_head, bool taps) {
     const qd_config &c = m->cfg;
     const bool bf = m->bf16, pdl = m->use_pdl;
-    const int S = m->S();
     const int h = c.hidden;
-
-    EmbedArgs e = {};
-    e.table = m->embed;
-    e.rows = c.embed_rows;
-    e.hidden = h;
-    e.bf16 = bf;
-    e.vocab = c.vocab;
-    e.S = S;
-    e.embed_in = m->embed_in;
-    e.stage_tokens = m->stage_tokens;
-    e.stage_embeds = m->stage_embeds;
-    e.emitted = m->emitted;
-    e.x = m->x;
-    e.st = m->st;
-    CU(launch_embed(e, s, pdl));
-    if (taps && m->tap_hidden) CU(cudaMemcpyAsync(m->tap_hidden, m->x, h * 4, cudaMemcpyDeviceToDevice, s));
-
-    const size_t layer_kv = (size_t)2 * m->kv_dim() * S * m->esize;
+    if (m->persistent) {
+        CU(launch_persistent(bf, c.head_dim, h, m->q_dim(), c.ffn, step_args(m, with_head, taps), m->num_sms,
+                             m->smem_step, s));
+        return QD_OK;
+    }
     for (int l = 0; l < c.n_layers; ++l) {
-        const Layer &L = m->layers[l];
-        GemvArgs g = {};
-        g.rows = m->q_dim() + 2 * m->kv_dim();
-        g.K = h;
-        g.rs = m->rs_h;
-        g.unit = 1;
-        g.nst = m->nst_qkv;
-        g.evict_last = m->evict_last_layers;
-        g.W = L.w_qkv;
-        g.in = m->x;
-        g.gamma = L.attn_norm;
-        g.eps = (float)c.rms_eps;
-        g.out = m->qkv;
-        g.st = m->st;
-        CU(launch_gemv(GEMV_QKV, bf, g, m->grid_qkv, m->smem_qkv, s, pdl));
-
-        AttnArgs a = {};
-        a.qkv = m->qkv;
-        a.q_gamma = c.qk_norm ? L.q_norm : nullptr;
-        a.k_gamma = c.qk_norm ? L.k_norm : nullptr;
-        a.eps = (float)c.rms_eps;
-        a.scale = (float)(1.0 / std::sqrt((double)c.head_dim));
-        a.rope_cos = m->rope_cos;
-        a.rope_sin = m->rope_sin;
-        uint8_t *kvl = reinterpret_cast<uint8_t *>(m->kv[m->cur_bucket]) + (size_t)l * layer_kv;
-        a.kcache = kvl;
-        a.vcache = kvl + layer_kv / 2;
-        a.S = S;
-        a.qh = c.n_q_heads;
-        a.kvh = c.n_kv_heads;
-        a.part = m->part;
-        a.max_splits = m->max_splits;
-        a.counter = m->attn_cnt;
-        a.out = m->att;
-        a.st = m->st;
-        CU(launch_attention(bf, c.head_dim, a, S / kAttnChunk, s, pdl));
-
-        g = GemvArgs{};
-        g.rows = h;
-        g.K = m->q_dim();
-        g.rs = m->rs_q;
-        g.unit = 1;
-        g.nst = m->nst_o;
-        g.evict_last = m->evict_last_layers;
-        g.W = L.w_o;
-        g.in = m->att;
-        g.out = m->x;
-        g.st = m->st;
-        CU(launch_gemv(GEMV_RES, bf, g, m->grid_o, m->smem_o, s, pdl));
-
-        g = GemvArgs{};
-        g.rows = 2 * c.ffn;
-        g.K = h;
-        g.rs = m->rs_h;
-        g.unit = 2;
-        g.nst = m->nst_gu;
-        g.evict_last = m->evict_last_layers;
-        g.W = L.w_gu;
-        g.in = m->x;
-        g.gamma = L.mlp_norm;
-        g.eps = (float)c.rms_eps;
-        g.out = m->act;
-        g.st = m->st;
-        CU(launch_gemv(GEMV_GU, bf, g, m->grid_gu, m->smem_gu, s, pdl));
-
-        g = GemvArgs{};
-        g.rows = h;
-        g.K = c.ffn;
-        g.rs = m->rs_f;
-        g.unit = 1;
-        g.nst = m->nst_d;
-        g.evict_last = m->evict_last_layers;
-        g.W = L.w_d;
-        g.in = m->act;
-        g.out = m->x;
-        g.st = m->st;
-        CU(launch_gemv(GEMV_RES, bf, g, m->grid_d, m->smem_d, s, pdl));
+        CU(launch_gemv(GEMV_QKV, bf, qkv_args(m, l, l == 0), m->grid_qkv, m->smem_qkv, s, pdl));
+        if (l == 0 && taps && m->tap_hidden)
+            CU(cudaMemcpyAsync(m->tap_hidden, m->x, h * 4, cudaMemcpyDeviceToDevice, s));
+        CU(launch_attention(bf, c.head_dim, attn_args(m, l), s, pdl));
+        CU(launch_gemv(GEMV_RES, bf, o_args(m, l), m->grid_o, m->smem_o, s, pdl));
+        CU(launch_gemv(GEMV_GU, bf, gu_args(m, l), m->grid_gu, m->smem_gu, s, pdl));
+        GemvArgs d = d_args(m, l);
+        d.advance_pos = (!with_head && l == c.n_layers - 1) ? 1 : 0;
+        CU(launch_gemv(GEMV_RES, bf, d, m->grid_d, m->smem_d, s, pdl));
         if (taps && m->tap_hidden)
             CU(cudaMemcpyAsync(m->tap_hidden + (size_t)(l + 1) * h, m->x, h * 4, cudaMemcpyDeviceToDevice, s));
     }
-    if (with_head) {
-        GemvArgs g = {};
-        g.rows = c.vocab;
-        g.K = h;
-        g.rs = m->rs_h;
-        g.unit = 1;
-        g.nst = m->nst_head;
-        g.evict_last = 0;
-        g.W_table = m->d_heads;
-        g.in = m->x;
-        g.gamma = m->final_norm;
-        g.eps = (float)c.rms_eps;
-        g.out = taps ? m->tap_logits : nullptr;
-        g.emitted = m->emitted;
-        g.penalty = (float)c.rep_penalty;
-        g.eos = c.eos_mask_id;
-        g.y_out = m->y;
-        g.part_v = m->head_pv;
-        g.part_i = m->head_pi;
-        g.counter = m->head_cnt;
-        g.ids = m->ids;
-        g.ids_cap = kIdsCap;
-        g.commit = 1;
-        g.st = m->st;
-        CU(launch_gemv(GEMV_HEAD, bf, g, m->grid_head, m->smem_head, s, pdl));
-    }
+    if (with_head)
+        CU(launch_gemv(GEMV_HEAD, bf, head_args(m, taps ? m->tap_logits : nullptr, 1), m->grid_head, m->smem_head, s,
+                       pdl));
     return QD_OK;
 }
 
@@ -482,7 +596,7 @@ static qd_status alloc_scratch(qd_model *m) {
     const qd_config &c = m->cfg;
     const int h = c.hidden;
     m->max_pos = c.buckets[c.n_buckets - 1];
-    m->max_splits = m->max_pos / kAttnChunk;
+    m->chunk_max = attn_chunk(m->max_pos);
     size_t off = 0;
     auto take = [&](size_t bytes) {
         size_t o = off;
@@ -490,10 +604,12 @@ static qd_status alloc_scratch(qd_model *m) {
         return o;
     };
     const size_t o_x = take(h * 4), o_qkv = take((size_t)(m->q_dim() + 2 * m->kv_dim()) * 4),
-                 o_att = take((size_t)m->q_dim() * 4), o_act = take((size_t)c.ffn * 4),
-                 o_part = take((size_t)c.n_q_heads * m->max_splits * (c.head_dim + 2) * 4), o_y = take(h * 4),
+                 o_act = take((size_t)c.ffn * 4),
+                 o_att = take((size_t)m->q_dim() * 4), o_y = take(h * 4),
+                 o_po = take((size_t)c.n_q_heads * kAttnMaxSplits * c.head_dim * 4),
+                 o_pml = take((size_t)c.n_q_heads * kAttnMaxSplits * 2 * 4), o_bar = take(128),
                  o_ein = take(h * 4), o_se = take((size_t)m->max_pos * h * 4), o_pv = take(4096 * 4),
-                 o_pi = take(4096 * 4), o_ac = take(64 * 4), o_hc = take(64 * 4), o_stok = take((size_t)m->max_pos * 4),
+                 o_pi = take(4096 * 4), o_hc = take(64 * 4), o_stok = take((size_t)m->max_pos * 4),
                  o_ids = take((size_t)kIdsCap * 4), o_em = take((size_t)((c.vocab + 31) / 32) * 4),
                  o_st = take(sizeof(DevState)), o_cos = take((size_t)m->max_pos * (c.head_dim / 2) * 4),
                  o_sin = take((size_t)m->max_pos * (c.head_dim / 2) * 4);
@@ -502,15 +618,16 @@ static qd_status alloc_scratch(qd_model *m) {
     uint8_t *B = reinterpret_cast<uint8_t *>(m->scratch);
     m->x = reinterpret_cast<float *>(B + o_x);
     m->qkv = reinterpret_cast<float *>(B + o_qkv);
-    m->att = reinterpret_cast<float *>(B + o_att);
     m->act = reinterpret_cast<float *>(B + o_act);
-    m->part = reinterpret_cast<float *>(B + o_part);
+    m->att = reinterpret_cast<float *>(B + o_att);
+    m->part_o = reinterpret_cast<float *>(B + o_po);
+    m->part_ml = reinterpret_cast<float *>(B + o_pml);
+    m->barrier = reinterpret_cast<unsigned *>(B + o_bar);
     m->y = reinterpret_cast<float *>(B + o_y);
     m->embed_in = reinterpret_cast<float *>(B + o_ein);
     m->stage_embeds = reinterpret_cast<float *>(B + o_se);
     m->head_pv = reinterpret_cast<float *>(B + o_pv);
     m->head_pi = reinterpret_cast<int *>(B + o_pi);
-    m->attn_cnt = reinterpret_cast<int *>(B + o_ac);
     m->head_cnt = reinterpret_cast<int *>(B + o_hc);
     m->stage_tokens = reinterpret_cast<int *>(B + o_stok);
     m->ids = reinterpret_cast<int32_t *>(B + o_ids);
@@ -523,30 +640,37 @@ static qd_status alloc_scratch(qd_model *m) {
     return QD_OK;
 }
 
-static void plan_launches(qd_model *m) {
+static bool plan_launches(qd_model *m) {
     const qd_config &c = m->cfg;
     const bool bf = m->bf16;
     int ns;
     gemv_split(c.hidden, bf, &ns, &m->rs_h);
     gemv_split(m->q_dim(), bf, &ns, &m->rs_q);
     gemv_split(c.ffn, bf, &ns, &m->rs_f);
+    m->rps_h = kSlotBytes / (int)(c.hidden * m->esize);
+    m->rps_q = kSlotBytes / (int)(m->q_dim() * m->esize);
+    m->rps_f = kSlotBytes / (int)(c.ffn * m->esize);
     const int sms = m->num_sms;
-    auto plan = [&](int rows, int unit, int K, int *grid, int *nst, size_t *smem) {
+    auto plan = [&](int rows, int unit, int K, int rps, int rs, int max_nst, int *grid, int *nst, int *rmax,
+                    size_t *smem) {
         const int units = rows / unit;
         *grid = std::min(sms, units);
-        const int rows_per_cta = (units + *grid - 1) / *grid * unit;
-        const int need = (rows_per_cta + kStageRows - 1) / kStageRows;
-        const size_t stage = (size_t)kStageRows * K * m->esize;
-        int cap = (int)(kRingBytes / stage);
-        cap = std::max(2, std::min(cap, 16));
-        *nst = std::max(1, std::min(need, cap));
-        *smem = gemv_smem_bytes(K, bf, *nst);
+        *rmax = (units + *grid - 1) / *grid * unit;
+        const int need = (*rmax + rps - 1) / rps;
+        *nst = std::max(1, std::min(need, max_nst));
+        *smem = gemv_smem_bytes(*nst, *rmax, rs, K);
     };
-    plan(m->q_dim() + 2 * m->kv_dim(), 1, c.hidden, &m->grid_qkv, &m->nst_qkv, &m->smem_qkv);
-    plan(c.hidden, 1, m->q_dim(), &m->grid_o, &m->nst_o, &m->smem_o);
-    plan(2 * c.ffn, 2, c.hidden, &m->grid_gu, &m->nst_gu, &m->smem_gu);
-    plan(c.hidden, 1, c.ffn, &m->grid_d, &m->nst_d, &m->smem_d);
-    plan(c.vocab, 1, c.hidden, &m->grid_head, &m->nst_head, &m->smem_head);
+    // Step kernels keep their ring at 4 stages (96 KB) so that the next kernel of the
+    // step fits beside them on the SM under programmatic dependent launch; the head is
+    // the last kernel of the step and takes a deeper ring.
+    const int ring = kRingBytes / kSlotBytes;
+    plan(m->q_dim() + 2 * m->kv_dim(), 1, c.hidden, m->rps_h, m->rs_h, ring, &m->grid_qkv, &m->nst_qkv,
+         &m->rmax_qkv, &m->smem_qkv);
+    plan(c.hidden, 1, m->q_dim(), m->rps_q, m->rs_q, ring, &m->grid_o, &m->nst_o, &m->rmax_o, &m->smem_o);
+    plan(2 * c.ffn, 2, c.hidden, m->rps_h, m->rs_h, ring, &m->grid_gu, &m->nst_gu, &m->rmax_gu, &m->smem_gu);
+    plan(c.hidden, 1, c.ffn, m->rps_f, m->rs_f, ring, &m->grid_d, &m->nst_d, &m->rmax_d, &m->smem_d);
+    plan(c.vocab, 1, c.hidden, m->rps_h, m->rs_h, 2 * ring, &m->grid_head, &m->nst_head, &m->rmax_head,
+         &m->smem_head);
     // Layer weights that fit in 60% of L2 stay resident across steps (evict_last);
     // the output head always streams (evict_first).
     size_t layer_bytes = 0;
@@ -556,6 +680,73 @@ static void plan_launches(qd_model *m) {
     int l2 = 0;
     cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, m->device);
     m->evict_last_layers = layer_bytes * 10 <= (size_t)l2 * 6 ? 1 : 0;
+    // residual kernels keep one row per consumer thread
+    return m->rmax_o <= kConsumerWarps * 32 && m->rmax_d <= kConsumerWarps * 32;
+}
+
+// Set up the persistent decode step when the shape has an instantiation: the device
+// layer table and the shared-memory layout (ring of up to 6 slots next to the
+// phase scratch), and check that one CTA fits on every SM.
+static qd_status setup_persistent(qd_model *m) {
+    const qd_config &c = m->cfg;
+    m->persistent = false;
+    if (std::getenv("QD_PER_PHASE")) return QD_OK;   // debug and profiling only
+    if (!persistent_supported(m->bf16, c.head_dim, c.hidden, m->q_dim(), c.ffn)) return QD_OK;
+    const int G = c.n_q_heads / c.n_kv_heads;
+    if (c.n_kv_heads * kAttnMaxSplits > m->num_sms) return QD_OK;
+    if (m->chunk_max * c.head_dim * (int)m->esize > kSlotBytes) return QD_OK;
+    // rows of any phase held by one CTA, times the warps per row
+    auto rmax = [&](int rows, int unit) { return (rows / unit + m->num_sms - 1) / m->num_sms * unit; };
+    const int res_words = std::max({rmax(m->q_dim() + 2 * m->kv_dim(), 1) * m->rs_h, rmax(c.hidden, 1) * m->rs_q,
+                                    rmax(2 * c.ffn, 2) * m->rs_h, rmax(c.hidden, 1) * m->rs_f,
+                                    rmax(c.vocab, 1) * m->rs_h});
+    const int head_rows = rmax(c.vocab, 1);
+    size_t off = 0;
+    auto take = [&](size_t bytes, size_t al) {
+        off = align_up(off, al);
+        const size_t o = off;
+        off += bytes;
+        return (int)o;
+    };
+    size_t tail = 0;
+    {
+        // everything but the ring
+        tail += 2 * 8 * 8 + 16;                                        // barriers (<= 8 slots)
+        tail += (size_t)c.hidden * 4 + 16;                             // gamma
+        tail += 64 * 4;                                                // misc
+        tail += (size_t)res_words * 4 + 16;                            // row partial sums
+        tail += persistent_att_bytes(G, c.head_dim, m->chunk_max) + 16;
+        tail += ((size_t)head_rows / 32 + 2) * 4 + 16;                 // emitted words of the head rows
+        tail += (size_t)std::max({m->q_dim(), c.hidden, c.ffn}) * 4 + 16;  // phase input vector
+    }
+    const size_t max_smem = 227 * 1024;
+    int nst = (int)((max_smem - tail) / kSlotBytes);
+    nst = std::min(nst, 6);
+    if (nst < 2) return QD_OK;
+    off = 0;
+    take((size_t)nst * kSlotBytes, 1024);
+    m->off_full = take((size_t)2 * nst * 8, 16);
+    m->off_gsm = take((size_t)c.hidden * 4, 16);
+    m->off_misc = take(64 * 4, 16);
+    m->off_res = take((size_t)res_words * 4, 16);
+    m->off_att = take(persistent_att_bytes(G, c.head_dim, m->chunk_max), 16);
+    m->off_emw = take(((size_t)head_rows / 32 + 2) * 4, 16);
+    m->off_xin = take((size_t)std::max({m->q_dim(), c.hidden, c.ffn}) * 4, 16);
+    m->smem_step = align_up(off, 16);
+    m->nst_step = nst;
+    if (m->smem_step > max_smem) return QD_OK;
+    CU(persistent_init(m->bf16, c.head_dim, c.hidden, m->q_dim(), c.ffn, m->smem_step));
+    // layer table
+    std::vector<LayerDev> host(c.n_layers);
+    for (int l = 0; l < c.n_layers; ++l) {
+        const Layer &L = m->layers[l];
+        host[l] = LayerDev{L.w_qkv, L.w_o, L.w_gu, L.w_d, L.attn_norm, L.mlp_norm, c.qk_norm ? L.q_norm : nullptr,
+                           c.qk_norm ? L.k_norm : nullptr};
+    }
+    CU(cudaMalloc(&m->d_layers, sizeof(LayerDev) * c.n_layers));
+    CU(cudaMemcpy(m->d_layers, host.data(), sizeof(LayerDev) * c.n_layers, cudaMemcpyHostToDevice));
+    m->persistent = true;
+    return QD_OK;
 }
 
 // ------------------------------------------------------------------ C-ABI
@@ -587,6 +778,7 @@ static void destroy_model(qd_model *m) {
     for (void *p : m->kv)
         if (p) cudaFree(p);
     if (m->arena) cudaFree(m->arena);
+    if (m->d_layers) cudaFree(m->d_layers);
     if (m->scratch) cudaFree(m->scratch);
     if (m->pin) cudaFreeHost(m->pin);
     if (m->ev_in) cudaEventDestroy(m->ev_in);
@@ -608,6 +800,9 @@ qd_status qd_create(const qd_weights *weights, const qd_config *cfg, void *cuda_
     m->bf16 = cfg->dtype == QD_BF16;
     m->esize = m->bf16 ? 2 : 4;
     m->user = reinterpret_cast<cudaStream_t>(cuda_stream);
+    // debug and profiling only: launch every kernel without programmatic dependent
+    // launch (results are identical; only the overlap between kernels changes)
+    m->use_pdl = std::getenv("QD_NO_PDL") == nullptr;
     auto bail = [&](qd_status st) {
         destroy_model(m);
         return st;
@@ -629,7 +824,12 @@ qd_status qd_create(const qd_weights *weights, const qd_config *cfg, void *cuda_
     if (st) return bail(st);
     st = alloc_scratch(m);
     if (st) return bail(st);
-    plan_launches(m);
+    if (!plan_launches(m)) {
+        destroy_model(m);
+        return QD_EUNSUPPORTED;
+    }
+    st = setup_persistent(m);
+    if (st) return bail(st);
     m->kv.assign(cfg->n_buckets, nullptr);
     m->graphs[0].assign(cfg->n_buckets, nullptr);
     m->graphs[1].assign(cfg->n_buckets, nullptr);
@@ -889,70 +1089,28 @@ qd_status qd_time_kernel(qd_handle h, int which, int reps, float *avg_ms) {
     if (m->h_pos == 0) return fail(m, QD_ESTATE, "time_kernel needs a prefilled handle");
     enter(m);
     CU(cudaStreamSynchronize(m->ls));
-    // save what the timed kernel overwrites: x, the device state and, for attention,
-    // the cache rows of the last position of layer 0
+    // Save what the timed kernel overwrites (x, the device state and, for attention,
+    // the cache rows of the last position of layer 0), then point the state at the
+    // last position so that the kernels see the arguments of the step that wrote it.
     std::vector<uint8_t> save_x(c.hidden * 4), save_st(sizeof(DevState));
     CU(cudaMemcpy(save_x.data(), m->x, save_x.size(), cudaMemcpyDeviceToHost));
     CU(cudaMemcpy(save_st.data(), m->st, save_st.size(), cudaMemcpyDeviceToHost));
     const int S = m->S();
-    const size_t layer_kv = (size_t)2 * m->kv_dim() * S * m->esize;
     const size_t rowb = (size_t)c.head_dim * m->esize;
     std::vector<uint8_t> save_kv(2 * (size_t)c.n_kv_heads * rowb);
     uint8_t *kv0 = reinterpret_cast<uint8_t *>(m->kv[m->cur_bucket]);
     const int last = m->h_pos - 1;
     CU(cudaMemcpy2D(save_kv.data(), rowb, kv0 + (size_t)last * rowb, (size_t)S * rowb, rowb, 2 * c.n_kv_heads,
                     cudaMemcpyDeviceToHost));
+    CU(cudaMemcpy(&m->st->pos, &last, sizeof(int), cudaMemcpyHostToDevice));
     auto one = [&]() -> qd_status {
-        const Layer &L = m->layers[0];
-        GemvArgs g = {};
-        g.st = m->st;
-        g.eps = (float)c.rms_eps;
-        g.unit = 1;
         switch (which) {
-            case 0:
-                g.rows = c.vocab; g.K = c.hidden; g.rs = m->rs_h; g.nst = m->nst_head; g.W_table = m->d_heads;
-                g.in = m->x; g.gamma = m->final_norm; g.emitted = m->emitted; g.penalty = (float)c.rep_penalty;
-                g.eos = c.eos_mask_id; g.part_v = m->head_pv; g.part_i = m->head_pi; g.counter = m->head_cnt;
-                g.ids = m->ids; g.ids_cap = kIdsCap; g.commit = 0;
-                CU(launch_gemv(GEMV_HEAD, m->bf16, g, m->grid_head, m->smem_head, m->ls, false));
-                break;
-            case 1:
-                g.rows = m->q_dim() + 2 * m->kv_dim(); g.K = c.hidden; g.rs = m->rs_h; g.nst = m->nst_qkv;
-                g.W = L.w_qkv; g.in = m->x; g.gamma = L.attn_norm; g.out = m->qkv;
-                g.evict_last = m->evict_last_layers;
-                CU(launch_gemv(GEMV_QKV, m->bf16, g, m->grid_qkv, m->smem_qkv, m->ls, false));
-                break;
-            case 2:
-                g.rows = 2 * c.ffn; g.K = c.hidden; g.rs = m->rs_h; g.unit = 2; g.nst = m->nst_gu; g.W = L.w_gu;
-                g.in = m->x; g.gamma = L.mlp_norm; g.out = m->act; g.evict_last = m->evict_last_layers;
-                CU(launch_gemv(GEMV_GU, m->bf16, g, m->grid_gu, m->smem_gu, m->ls, false));
-                break;
-            case 3:
-                g.rows = c.hidden; g.K = c.ffn; g.rs = m->rs_f; g.nst = m->nst_d; g.W = L.w_d; g.in = m->act;
-                g.out = m->x; g.evict_last = m->evict_last_layers;
-                CU(launch_gemv(GEMV_RES, m->bf16, g, m->grid_d, m->smem_d, m->ls, false));
-                break;
-            case 5:
-                g.rows = c.hidden; g.K = m->q_dim(); g.rs = m->rs_q; g.nst = m->nst_o; g.W = L.w_o; g.in = m->att;
-                g.out = m->x; g.evict_last = m->evict_last_layers;
-                CU(launch_gemv(GEMV_RES, m->bf16, g, m->grid_o, m->smem_o, m->ls, false));
-                break;
-            case 4: {
-                AttnArgs a = {};
-                a.qkv = m->qkv;
-                a.q_gamma = c.qk_norm ? L.q_norm : nullptr;
-                a.k_gamma = c.qk_norm ? L.k_norm : nullptr;
-                a.eps = (float)c.rms_eps;
-                a.scale = (float)(1.0 / std::sqrt((double)c.head_dim));
-                a.rope_cos = m->rope_cos;
-                a.rope_sin = m->rope_sin;
-                a.kcache = kv0;
-                a.vcache = kv0 + layer_kv / 2;
-                a.S = S; a.qh = c.n_q_heads; a.kvh = c.n_kv_heads; a.part = m->part; a.max_splits = m->max_splits;
-                a.counter = m->attn_cnt; a.out = m->att; a.st = m->st;
-                CU(launch_attention(m->bf16, c.head_dim, a, S / kAttnChunk, m->ls, false));
-                break;
-            }
+            case 0: CU(launch_gemv(GEMV_HEAD, m->bf16, head_args(m, nullptr, 0), m->grid_head, m->smem_head, m->ls, false)); break;
+            case 1: CU(launch_gemv(GEMV_QKV, m->bf16, qkv_args(m, 0, false), m->grid_qkv, m->smem_qkv, m->ls, false)); break;
+            case 2: CU(launch_gemv(GEMV_GU, m->bf16, gu_args(m, 0), m->grid_gu, m->smem_gu, m->ls, false)); break;
+            case 3: CU(launch_gemv(GEMV_RES, m->bf16, d_args(m, 0), m->grid_d, m->smem_d, m->ls, false)); break;
+            case 4: CU(launch_attention(m->bf16, c.head_dim, attn_args(m, 0), m->ls, false)); break;
+            case 5: CU(launch_gemv(GEMV_RES, m->bf16, o_args(m, 0), m->grid_o, m->smem_o, m->ls, false)); break;
         }
         return QD_OK;
     };
