@@ -248,16 +248,19 @@ def gpu_arm(args):
     step_bytes = shape.step_bytes(int(round(L_avg)))
     step_gbs = step_bytes / (dec_step_us / 1e6) / 1e9
 
-    # dominant kernel: the output head (norm + GEMV + penalty + argmax)
-    head_bytes = shape.vocab * shape.hidden * (2 if shape.bf16 else 4) + shape.hidden * 8 + shape.vocab // 8
-    gu_bytes = 2 * shape.ffn * shape.hidden * (2 if shape.bf16 else 4)
-    if shape.vocab * shape.hidden >= shape.n_layers * 2 * shape.ffn * shape.hidden:
-        which, kname, kbytes = qd.KERNEL_HEAD, "output head: RMSNorm + LM-head GEMV + penalty + EOS mask + argmax", head_bytes
-    else:
-        which, kname, kbytes = qd.KERNEL_GATE_UP, "RMSNorm + gate/up GEMV + SwiGLU", gu_bytes + shape.hidden * 8 + shape.ffn * 4
-    # the handle holds a prefilled state after the timed region
-    kms = qd.qd_time_kernel(h, which, 50)
+    # dominant kernel: the persistent decode-step kernel (every phase of the step in one
+    # launch); its algorithmic bytes per launch are the step's weights plus the KV rows
+    # it reads, at the position the handle holds after the timed region.
+    pos_now, smax_now = qd.qd_get_pos(h)
+    reps = max(1, min(64, smax_now - pos_now - 4))
+    kms = qd.qd_time_kernel(h, qd.KERNEL_STEP, reps)
+    kbytes = shape.step_bytes(pos_now + (reps + 1) // 2 + 3)
     achieved = kbytes / (kms / 1e3) / 1e9
+    kname = ("decode_step_kernel: RMSNorm+QKV, attention, O-proj, RMSNorm+gate/up+SwiGLU, down for every layer, "
+             "then RMSNorm+LM head+penalty+EOS mask+argmax, one cooperative launch")
+    # the output-head GEMV alone (per-phase kernel) as a pure streaming reference
+    head_bytes = shape.vocab * shape.hidden * (2 if shape.bf16 else 4)
+    head_ms = qd.qd_time_kernel(h, qd.KERNEL_HEAD, 20)
 
     # end to end through the public API with host buffers: the prompt embeddings
     # come from pinned host memory each trajectory, the token goes in and the id
@@ -308,7 +311,10 @@ def gpu_arm(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": None, "kernel": kname,
                      "bytes_per_launch": kbytes, "avg_launch_ms": kms, "peak_source": peak_src,
-                     "timing": "CUDA events on the library stream, 50 back-to-back launches with the step's arguments"},
+                     "timing": f"CUDA events on the library stream around {reps} decode steps (graph replays) at "
+                               f"positions {pos_now}..{pos_now + reps + 2}",
+                     "head_gemv_alone": {"bytes": head_bytes, "avg_launch_ms": head_ms,
+                                         "achieved_gbs": head_bytes / (head_ms / 1e3) / 1e9}},
         "step_hbm": {"bytes_per_step": step_bytes, "decode_step_us": dec_step_us,
                      "decode_tokens_per_s": 1e6 / dec_step_us, "achieved_gbs": step_gbs,
                      "frac": step_gbs / hbm_peak, "peak_source": peak_src,

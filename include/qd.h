@@ -191,8 +191,11 @@ qd_status qd_get_launch_count(qd_handle h, long long *kernels, int *kernels_per_
  * arguments the step uses, between CUDA events on the library's stream;
  * which: 0 = output head (norm + GEMV + penalty + argmax), 1 = fused QKV GEMV
  * of layer 0, 2 = gate/up GEMV of layer 0, 3 = down GEMV of layer 0,
- * 4 = attention of layer 0, 5 = output projection of layer 0.  The state is
- * restored afterwards.  Needs a prefilled handle. */
+ * 4 = attention of layer 0, 5 = output projection of layer 0, 6 = one whole decode
+ * step as the decode loop issues it (the persistent step kernel where the shape has
+ * one), repeated `reps` times at the following positions (they must fit in the
+ * current bucket).  The position, state, residual and emitted set are restored
+ * afterwards.  Needs a prefilled handle. */
 qd_status qd_time_kernel(qd_handle h, int which, int reps, float *avg_ms);
 
 const char *qd_last_error(qd_handle h);

@@ -243,4 +243,4 @@ def qd_status_string(status: int) -> str:
     return _lib.qd_status_string(int(status)).decode()
 
 
-KERNEL_HEAD, KERNEL_QKV, KERNEL_GATE_UP, KERNEL_DOWN, KERNEL_ATTENTION, KERNEL_OPROJ = 0, 1, 2, 3, 4, 5
+KERNEL_HEAD, KERNEL_QKV, KERNEL_GATE_UP, KERNEL_DOWN, KERNEL_ATTENTION, KERNEL_OPROJ, KERNEL_STEP = 0, 1, 2, 3, 4, 5, 6

@@ -1081,12 +1081,52 @@ qd_status qd_get_launch_count(qd_handle h, long long *kernels, int *kernels_per_
     return QD_OK;
 }
 
+// Time `reps` whole decode steps (the persistent step kernel, or the per-phase kernel
+// sequence) as issued by the decode loop, between CUDA events on the library
+// stream; then put back the position, the device state, the residual and the
+// emitted set.  Rows written past the restored position are never read before
+// being rewritten.
+static qd_status time_step(qd_model *m, int reps, float *avg_ms) {
+    const qd_config &c = m->cfg;
+    if (m->h_pos + reps + 3 > m->S())
+        return fail(m, QD_EINVAL, "%d timed steps do not fit in the current bucket from position %d", reps, m->h_pos);
+    enter(m);
+    CU(cudaStreamSynchronize(m->ls));
+    const size_t emw = (size_t)((c.vocab + 31) / 32) * 4;
+    std::vector<uint8_t> save_x(c.hidden * 4), save_st(sizeof(DevState)), save_em(emw);
+    CU(cudaMemcpy(save_x.data(), m->x, save_x.size(), cudaMemcpyDeviceToHost));
+    CU(cudaMemcpy(save_st.data(), m->st, save_st.size(), cudaMemcpyDeviceToHost));
+    CU(cudaMemcpy(save_em.data(), m->emitted, emw, cudaMemcpyDeviceToHost));
+    const int pos0 = m->h_pos;
+    const long long launches0 = m->launches;
+    qd_status st = QD_OK;
+    for (int i = 0; i < 3 && !st; ++i, ++m->h_pos) st = run_step(m, true);
+    if (!st) {
+        CU(cudaEventRecord(m->ev_t0, m->ls));
+        for (int i = 0; i < reps && !st; ++i, ++m->h_pos) st = run_step(m, true);
+        CU(cudaEventRecord(m->ev_t1, m->ls));
+        CU(cudaEventSynchronize(m->ev_t1));
+    }
+    m->h_pos = pos0;
+    m->launches = launches0;
+    if (st) return st;
+    float ms = 0.f;
+    CU(cudaEventElapsedTime(&ms, m->ev_t0, m->ev_t1));
+    *avg_ms = ms / reps;
+    CU(cudaMemcpy(m->x, save_x.data(), save_x.size(), cudaMemcpyHostToDevice));
+    CU(cudaMemcpy(m->st, save_st.data(), save_st.size(), cudaMemcpyHostToDevice));
+    CU(cudaMemcpy(m->emitted, save_em.data(), emw, cudaMemcpyHostToDevice));
+    leave(m);
+    return QD_OK;
+}
+
 qd_status qd_time_kernel(qd_handle h, int which, int reps, float *avg_ms) {
     if (!h || !avg_ms) return QD_EINVAL;
     qd_model *m = h;
     const qd_config &c = m->cfg;
-    if (reps < 1 || which < 0 || which > 5) return fail(m, QD_EINVAL, "bad which/reps");
+    if (reps < 1 || which < 0 || which > 6) return fail(m, QD_EINVAL, "bad which/reps");
     if (m->h_pos == 0) return fail(m, QD_ESTATE, "time_kernel needs a prefilled handle");
+    if (which == 6) return time_step(m, reps, avg_ms);
     enter(m);
     CU(cudaStreamSynchronize(m->ls));
     // Save what the timed kernel overwrites (x, the device state and, for attention,
