@@ -28,6 +28,22 @@ sys.path.insert(0, ROOT)
 METRIC = "decode tokens/s at 1 GB300; per-step HBM GB/s as fraction of peak"
 
 
+# DRAM bytes (read + write) of one decode_step_kernel launch from one ncu capture
+# (profiles/decode_step_kernel_asr.md), at attended length L, for the kernel sources
+# with this digest; null in the JSON line once the sources differ.
+_STEP_TRAFFIC = {"asr": {"digest": "d1e709b050fdc2f8", "bytes": 224744704 + 3667712, "L": 116}}
+_STEP_SOURCES = ("decode_persistent.cu", "decode_common.cuh", "qd_device.cuh", "qd_internal.h")
+
+
+def _step_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in _STEP_SOURCES:
+        with open(os.path.join(ROOT, "transformer_autoregressive_decode_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -254,8 +270,16 @@ def gpu_arm(args):
     pos_now, smax_now = qd.qd_get_pos(h)
     reps = max(1, min(64, smax_now - pos_now - 4))
     kms = qd.qd_time_kernel(h, qd.KERNEL_STEP, reps)
-    kbytes = shape.step_bytes(pos_now + (reps + 1) // 2 + 3)
+    L_timed = pos_now + (reps + 1) // 2 + 3
+    kbytes = shape.step_bytes(L_timed)
     achieved = kbytes / (kms / 1e3) / 1e9
+    traffic, traffic_note = None, "no ncu capture for this workload and kernel build"
+    tr = _STEP_TRAFFIC.get(args.workload)
+    if tr and tr["digest"] == _step_digest():
+        # scaled from the captured length to the timed one by the K/V rows read
+        traffic = tr["bytes"] + (L_timed - tr["L"]) * shape.kv_bytes_per_position()
+        traffic_note = (f"ncu dram__bytes_read+write of one launch at L={tr['L']} "
+                        f"({tr['bytes']} B), plus {shape.kv_bytes_per_position()} B of K/V per position to L={L_timed}")
     kname = ("decode_step_kernel: RMSNorm+QKV, attention, O-proj, RMSNorm+gate/up+SwiGLU, down for every layer, "
              "then RMSNorm+LM head+penalty+EOS mask+argmax, one cooperative launch")
     # the output-head GEMV alone (per-phase kernel) as a pure streaming reference
@@ -309,7 +333,7 @@ def gpu_arm(args):
                    "l2": f"inputs larger than L2: {shape.weight_bytes_per_step() / 1e6:.1f} MB of weights per step",
                    "parallelism": "replicas" if ws > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": None, "kernel": kname,
+                     "frac": achieved / hbm_peak, "traffic": traffic, "traffic_note": traffic_note, "kernel": kname,
                      "bytes_per_launch": kbytes, "avg_launch_ms": kms, "peak_source": peak_src,
                      "timing": f"CUDA events on the library stream around {reps} decode steps (graph replays) at "
                                f"positions {pos_now}..{pos_now + reps + 2}",
