@@ -201,6 +201,37 @@ qd_status qd_time_kernel(qd_handle h, int which, int reps, float *avg_ms);
 const char *qd_last_error(qd_handle h);
 const char *qd_status_string(int status);
 
+/* ---- output head without allocation ----
+ *
+ * The pages have no counterpart to this call; it exists for callers that cannot
+ * allocate device memory: a host application that owns all device memory through
+ * its own pool and forbids other allocators (an audio engine or plugin host, for
+ * example), or code on a real-time thread where an allocation's locking and implicit
+ * synchronisation are not allowed.  Such a caller passes its own buffers for every
+ * input and output, and the call allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine.
+ *
+ * qd_head_argmax_noalloc -- logits = W y (W [vocab, hidden] row-major in `dtype`,
+ * y fp32 [hidden] already RMS-normalised), then the repetition penalty over the ids
+ * set in emitted_dev (uint32 bitmask, may be NULL), the EOS mask (eos_mask_id, -1:
+ * none) and the argmax (lowest index on ties), written to *out_id_dev (DEVICE
+ * int32).  logits_dev (DEVICE fp32 [vocab], may be NULL) receives the raw logits.
+ * All pointers are DEVICE pointers; work is queued on cuda_stream and the call
+ * returns without synchronising.  It gives the same logits and id as the output
+ * head of qd_decode_step for the same y.
+ *
+ * Its scratch (one argmax candidate per CTA and a completion counter, about 8 KB)
+ * is a fixed array in the library's device memory, held by every device that loads
+ * the library until the process exits.  Limits: hidden a multiple of 256 and at most
+ * 8192, at most 1024 CTAs (one per SM is used); larger requests return
+ * QD_EUNSUPPORTED.  The first call on a device looks up that array's device
+ * address and configures the kernels; make that first call before any stream
+ * capture.  Every call shares the array: calls whose work overlaps on the GPU (on
+ * different streams, or from different host threads) race and must not be issued. */
+qd_status qd_head_argmax_noalloc(const float *y_dev, const void *w_dev, int vocab, int hidden, int dtype,
+                                 const uint32_t *emitted_dev, double rep_penalty, int eos_mask_id,
+                                 int32_t *out_id_dev, float *logits_dev, void *cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -32,7 +32,7 @@ QD_MAX_HEADS = 16
 EXPORTS = ("qd_create", "qd_destroy", "qd_reset", "qd_prefill", "qd_decode_step", "qd_decode_step_async",
            "qd_decode_greedy", "qd_grow_kv", "qd_get_hidden", "qd_set_debug_taps", "qd_set_graphs", "qd_copy_kv",
            "qd_get_emitted", "qd_get_pos", "qd_get_launch_count", "qd_time_kernel", "qd_last_error",
-           "qd_status_string")
+           "qd_status_string", "qd_head_argmax_noalloc")
 
 
 class qd_config(ctypes.Structure):
@@ -74,6 +74,7 @@ _SIGS = {
     "qd_time_kernel": ([_vp, _i32, _i32, _P(ctypes.c_float)], _i32),
     "qd_last_error": ([_vp], ctypes.c_char_p),
     "qd_status_string": ([_i32], ctypes.c_char_p),
+    "qd_head_argmax_noalloc": ([_vp, _vp, _i32, _i32, _i32, _vp, ctypes.c_double, _i32, _vp, _vp, _vp], _i32),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -244,3 +245,16 @@ def qd_status_string(status: int) -> str:
 
 
 KERNEL_HEAD, KERNEL_QKV, KERNEL_GATE_UP, KERNEL_DOWN, KERNEL_ATTENTION, KERNEL_OPROJ, KERNEL_STEP = 0, 1, 2, 3, 4, 5, 6
+
+
+def qd_head_argmax_noalloc(y_dev, w_dev, vocab: int, hidden: int, bf16: bool, emitted_dev, rep_penalty: float,
+                           eos_mask_id: int, out_id_dev, logits_dev=None, stream=None):
+    """Output head over device buffers the caller owns; allocates nothing."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    st = _lib.qd_head_argmax_noalloc(_ptr(y_dev), _ptr(w_dev), int(vocab), int(hidden), QD_BF16 if bf16 else QD_F32,
+                                     _ptr(emitted_dev), float(rep_penalty), int(eos_mask_id), _ptr(out_id_dev),
+                                     _ptr(logits_dev), ctypes.c_void_p(stream.cuda_stream))
+    if st != QD_OK:
+        raise QDError(st, "qd_head_argmax_noalloc failed")
