@@ -95,6 +95,8 @@ def _lib_handle():
             L.orc_silu_mul.restype = ctypes.c_float
             L.orc_round_bf16.argtypes = [ctypes.c_float]
             L.orc_round_bf16.restype = ctypes.c_uint16
+            L.orc_frame_sum.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
+            L.orc_frame_sum.restype = i32
             L.orc_num_threads.argtypes = []
             L.orc_num_threads.restype = i32
             L.orc_set_threads.argtypes = [i32]
@@ -236,6 +238,90 @@ def recompute_logits(shape, weights, embeds=None, tokens=None, head_idx: int = 0
     if st != OK:
         raise OracleError(st, "recompute")
     return out
+
+
+# ---- two-level frame generation ----
+
+FRAME_CODES = 16
+
+
+def table_row(table: np.ndarray, i: int) -> np.ndarray:
+    """Row i of an embedding table as float32 (bfloat16 bit patterns are widened)."""
+    r = np.asarray(table[int(i)])
+    if r.dtype == np.uint16:
+        return (r.astype(np.uint32) << 16).view(np.float32)
+    return r.astype(np.float32)
+
+
+def frame_sum(tables: Sequence[np.ndarray], ids: Sequence[int], text: np.ndarray) -> np.ndarray:
+    """((E_0[ids_0] + E_1[ids_1]) + ... ) + text in fp32, tables bf16 bits or float32."""
+    bf16 = tables[0].dtype == np.uint16
+    keep = [np.ascontiguousarray(t) for t in tables]
+    if any((t.dtype == np.uint16) != bf16 for t in keep):
+        raise ValueError("tables must share one dtype")
+    hidden = keep[0].shape[1]
+    ptrs = (ctypes.c_void_p * len(keep))(*[t.ctypes.data for t in keep])
+    rows = np.array([t.shape[0] for t in keep], np.int32)
+    idv = np.ascontiguousarray(ids, np.int32)
+    tx = np.ascontiguousarray(text, np.float32)
+    out = np.empty(hidden, np.float32)
+    st = _lib_handle().orc_frame_sum(ctypes.cast(ptrs, ctypes.c_void_p), rows.ctypes.data, idv.ctypes.data,
+                                     len(keep), hidden, int(bf16), tx.ctypes.data, out.ctypes.data)
+    if st != OK:
+        raise OracleError(st, "frame_sum")
+    return out
+
+
+class FrameLoop:
+    """Two-level frame generation over two oracle streams.
+
+    Per frame ("Qwen3-TTS ncnn port", section "Talker: non-standard structure and
+    two-level generation"; "qwen3-tts-hip OPTIMIZATION_LOG", Code Predictor
+    sub-stages), with p the Talker's last id and h_T its final-norm output:
+      1. reset the predictor, prefill it with [h_T, E_0[p]], head 0 -> code_1;
+      2. for j = 1..14: a step with input E_j[code_j] (code_j joins the predictor's
+         emitted set), head j -> code_{j+1};
+      3. next_in = E_0[p] + E_1[code_1] + ... + E_15[code_15] + text;
+      4. unless it is the last frame: a Talker step with input next_in and token p.
+    ``force`` [n, 16] replaces the fed-back ids (teacher forcing); the argmaxes are
+    still reported."""
+
+    def __init__(self, talker: Oracle, predictor: Oracle, e0: np.ndarray, code_tables: Sequence[np.ndarray]):
+        if len(code_tables) != FRAME_CODES - 1:
+            raise ValueError("need 15 code tables")
+        self.talker, self.predictor = talker, predictor
+        self.tables = [e0] + list(code_tables)
+
+    def generate(self, n_frames: int, text: np.ndarray, primary: int, primary_margin: float = float("inf"),
+                 force: Optional[np.ndarray] = None):
+        """Returns (codes [n, 16] argmaxes, margins [n, 16], next_in [n, hidden],
+        talker_hidden [n, hidden] = h_T of every frame)."""
+        hidden = self.tables[0].shape[1]
+        codes = np.zeros((n_frames, FRAME_CODES), np.int32)
+        margins = np.zeros((n_frames, FRAME_CODES), np.float64)
+        next_in = np.zeros((n_frames, hidden), np.float32)
+        h_t = np.zeros((n_frames, hidden), np.float32)
+        for f in range(n_frames):
+            codes[f, 0], margins[f, 0] = primary, primary_margin
+            p = int(force[f, 0]) if force is not None else primary
+            h_t[f] = self.talker.hidden()
+            self.predictor.reset()
+            cid, _, cm = self.predictor.prefill(embeds=np.stack([h_t[f], table_row(self.tables[0], p)]),
+                                                head_idx=0, want_logits=False)
+            codes[f, 1], margins[f, 1] = cid, cm
+            fed = [p]
+            for j in range(1, FRAME_CODES - 1):
+                c = int(force[f, j]) if force is not None else int(codes[f, j])
+                fed.append(c)
+                cid, _, cm, _ = self.predictor.step(token=c, embed=table_row(self.tables[j], c), head_idx=j,
+                                                    want_logits=False)
+                codes[f, j + 1], margins[f, j + 1] = cid, cm
+            fed.append(int(force[f, FRAME_CODES - 1]) if force is not None else int(codes[f, FRAME_CODES - 1]))
+            next_in[f] = frame_sum(self.tables, fed, text[f])
+            if f < n_frames - 1:
+                primary, _, primary_margin, _ = self.talker.step(token=p, embed=next_in[f], head_idx=0,
+                                                                 want_logits=False)
+        return codes, margins, next_in, h_t
 
 
 # ---- primitives (for the pins) ----

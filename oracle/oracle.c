@@ -609,3 +609,24 @@ int orc_recompute_logits(const orc_config *c, const void *const *w, const int32_
     free(att); free(tmp); free(g); free(u);
     return ORC_OK;
 }
+
+/* ---------------------------------------------------------------- frame input */
+
+/* Next Talker input of a frame, "Qwen3-TTS ncnn port", section "Talker:
+ * non-standard structure and two-level generation": the embeddings of the frame's
+ * 16 codes (primary code in the Talker's table, residual code j in table j) plus
+ * the text/pad embedding, added in fp32 from table 0 to table n-1, text last.
+ * Pinned by the tests against an fp64 sum (closed form) and exact small-integer
+ * tables. */
+int orc_frame_sum(const void *const *tables, const int *rows, const int32_t *ids, int n_tables, int hidden,
+                  int bf16, const float *text, float *out) {
+    if (n_tables < 1 || hidden < 1) return ORC_EINVAL;
+    for (int j = 0; j < n_tables; ++j)
+        if (!tables[j] || ids[j] < 0 || ids[j] >= rows[j]) return ORC_EINVAL;
+    for (int i = 0; i < hidden; ++i) {
+        float v = wat(bf16, tables[0], (size_t)ids[0] * hidden + i);
+        for (int j = 1; j < n_tables; ++j) v += wat(bf16, tables[j], (size_t)ids[j] * hidden + i);
+        out[i] = v + text[i];
+    }
+    return ORC_OK;
+}

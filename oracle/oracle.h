@@ -77,6 +77,12 @@ int orc_emitted_words(const orc_model *m, uint32_t *out);  /* bitmask copy */
 int orc_recompute_logits(const orc_config *cfg, const void *const *weights, const int32_t *tokens,
                          const float *embeds, int n, int head_idx, float *logits_raw);
 
+/* Two-level frame generation: the next Talker input of a frame,
+ * out = ((E_0[ids_0] + E_1[ids_1]) + ... + E_{n-1}[ids_{n-1}]) + text in fp32.
+ * tables[j] [rows[j], hidden] (bfloat16 bits when bf16, else float32). */
+int orc_frame_sum(const void *const *tables, const int *rows, const int32_t *ids, int n_tables, int hidden,
+                  int bf16, const float *text, float *out);
+
 /* Primitives the model is built from, exposed for the pins. */
 void orc_rmsnorm(const float *x, const float *gamma, int n, double eps, float *out);
 void orc_rope(float *v, int head_dim, int pos, double theta);

@@ -255,16 +255,27 @@ def prefill_embeds(s: Shape, n: Optional[int] = None, seed: Optional[int] = None
     return normal(f"{s.name}/{stream}", (n, s.hidden), seed, 0.0, 1.0)
 
 
-def frame_tables(seed: int = 0) -> Dict[str, np.ndarray]:
-    """Code-embedding tables of the frame workload: E1..E15 [2048, 1024] ~ N(0, 0.02)
-    (bf16 bits).  E0 is the talker's own embedding table."""
-    return {f"code_embed.{j}": normal(f"frame/code_embed.{j}", (FRAME_CODE_VOCAB, TALKER.hidden), seed,
-                                      0.0, 0.02, bf16=True) for j in range(1, 16)}
+def frame_tables(seed: int = 0, rows: int = FRAME_CODE_VOCAB, hidden: int = 1024,
+                 bf16: bool = True) -> Dict[str, np.ndarray]:
+    """Code-embedding tables of the frame workload: E1..E15 [rows, hidden] ~ N(0, 0.02)
+    (bf16 bits by default).  E0 is the talker's own embedding table."""
+    return {f"code_embed.{j}": normal(f"frame/code_embed.{j}", (rows, hidden), seed, 0.0, 0.02, bf16=bf16)
+            for j in range(1, 16)}
 
 
-def frame_text_embeds(n_frames: int = FRAME_COUNT, seed: int = 0) -> np.ndarray:
-    """Per-frame text/pad embedding ~ N(0, 1), float32 [n_frames, 1024]."""
-    return normal("frame/text_pad", (n_frames, TALKER.hidden), seed, 0.0, 1.0)
+def frame_text_embeds(n_frames: int = FRAME_COUNT, seed: int = 0, hidden: int = 1024) -> np.ndarray:
+    """Per-frame text/pad embedding ~ N(0, 1), float32 [n_frames, hidden]."""
+    return normal("frame/text_pad", (n_frames, hidden), seed, 0.0, 1.0)
+
+
+def frame_bytes(talker_L: int, talker_step: bool = True) -> int:
+    """Algorithmic bytes of one frame: the Talker step attending over talker_L
+    positions (when the frame has one) and the Code Predictor's 15 weight passes
+    (the two-position prefill needs its weights once; each pass reads one head and
+    the K/V of the positions it attends, 2..16), plus the K/V row of position 0."""
+    cp = CODE_PREDICTOR
+    b = sum(cp.step_bytes(L) for L in range(2, 17)) + cp.kv_bytes_per_position()
+    return b + (TALKER.step_bytes(talker_L) if talker_step else 0)
 
 
 def batch_initial_lengths(seed: int = 0) -> np.ndarray:
