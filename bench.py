@@ -31,7 +31,7 @@ METRIC = "decode tokens/s at 1 GB300; per-step HBM GB/s as fraction of peak"
 # DRAM bytes (read + write) of one decode_step_kernel launch from one ncu capture
 # (profiles/decode_step_kernel_asr.md), at attended length L, for the kernel sources
 # with this digest; null in the JSON line once the sources differ.
-_STEP_TRAFFIC = {"asr": {"digest": "d1e709b050fdc2f8", "bytes": 224744704 + 3667712, "L": 116}}
+_STEP_TRAFFIC = {"asr": {"digest": "6f2083bca17fa563", "bytes": 224744704 + 3667712, "L": 116}}
 _STEP_SOURCES = ("decode_persistent.cu", "decode_common.cuh", "qd_device.cuh", "qd_internal.h")
 
 
@@ -352,19 +352,242 @@ def gpu_arm(args):
         torch.distributed.destroy_process_group()
 
 
+# ------------------------------------------------------------------------------ frame workload
+
+FRAME_TRAJ = 150
+FRAMES_DESC = ("two-level frame generation: 28-layer Talker (hidden 1024, 16q/8kv heads x 128, QK-norm, FFN 3072, "
+               "vocab 3072, repetition penalty 1.05) emits the primary code, a 5-layer Code Predictor (same dims, 15 "
+               "heads of vocab 2048) the 15 residual codes; 16 code embeddings + N(0,1) text embedding feed the "
+               "Talker; prefill 64, 150 frames per trajectory, Talker buckets 128->256, batch 1")
+
+
+def run_oracle_frames(max_frames: int, budget_s: float = 20.0):
+    """Time the oracle's frame loop on a bounded sample: Talker prefill (untimed),
+    then up to ``max_frames`` frames or ``budget_s`` seconds."""
+    import oracle as O
+    import workloads as W
+    ts, cs = W.TALKER, W.CODE_PREDICTOR
+    tw = W.model_weights(ts)
+    tabs = W.frame_tables()
+    talker, cp = O.Oracle(ts, tw), O.Oracle(cs, W.model_weights(cs))
+    loop = O.FrameLoop(talker, cp, tw["embed"], [tabs[f"code_embed.{j}"] for j in range(1, 16)])
+    text = W.frame_text_embeds(FRAME_TRAJ)
+    p, _, m = talker.prefill(embeds=W.prefill_embeds(ts), want_logits=False)
+    n = 0
+    t0 = time.perf_counter()
+    while n < min(max_frames, FRAME_TRAJ - 1):
+        # one frame: the predictor loop and the sum, then the Talker step
+        _, _, nxt, _ = loop.generate(1, text[n:n + 1], p, m)
+        p, _, m, _ = talker.step(token=p, embed=nxt[0], want_logits=False)
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    talker.close()
+    cp.close()
+    return n / dt, n, dt, O.num_threads()
+
+
+def frames_reference_arm(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    run_oracle_frames(1, budget_s=5.0)                       # warm-up (untimed)
+    fps, n, dt, cores = run_oracle_frames(args.steps, budget_s=60.0)
+    sample = f"Talker prefill 64 untimed, then {n} frames ({dt:.1f} s)"
+    line = {"impl": "reference", "metric": METRIC, "value": fps, "unit": "frames/s", "n_gpus": ws,
+            "steps": n, "warmup": args.warmup, "ms_per_step": 1e3 * dt / max(n, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": FRAMES_DESC},
+            "cpu_baseline": {"value": fps, "unit": "frames/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": fps, "unit": "frames/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def frames_arm(args):
+    import numpy as np
+    import torch
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+
+    import workloads as W
+    import __graft_entry__
+    __graft_entry__.build_library()
+    import transformer_autoregressive_decode_gb300 as qd
+    from transformer_autoregressive_decode_gb300.torch_io import config_from_shape, to_device, upload
+
+    ts, cs = W.TALKER, W.CODE_PREDICTOR
+    hbm_peak, _, peak_src = _peaks()
+    T = qd.qd_create(upload(W.model_weights(ts)), config_from_shape(ts))
+    C = qd.qd_create(upload(W.model_weights(cs)), config_from_shape(cs))
+    tabs = W.frame_tables()
+    F = qd.qd_frame_create(T, C, [to_device(tabs[f"code_embed.{j}"]) for j in range(1, 16)], True)
+    prompt_np = W.prefill_embeds(ts)
+    text_np = W.frame_text_embeds(FRAME_TRAJ)
+    prompt = torch.from_numpy(prompt_np).cuda()
+    text = torch.from_numpy(text_np).cuda()
+    codes = torch.empty((FRAME_TRAJ, 16), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def frames(n, events=None):
+        """n frames as trajectories of up to 150 (reset + Talker prefill + frames)."""
+        done = 0
+        while done < n:
+            k = min(FRAME_TRAJ, n - done)
+            qd.qd_reset(T)
+            qd.qd_prefill(T, embeds=prompt)
+            if events is not None:
+                events.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True), k))
+                events[-1][0].record(stream)
+            qd.qd_frame_generate(F, k, text, codes)
+            if events is not None:
+                events[-1][1].record(stream)
+            done += k
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    W_ = max(3, args.warmup)
+    frames(W_)
+    barrier()
+    kt0, _ = qd.qd_get_launch_count(T)
+    kc0, _ = qd.qd_get_launch_count(C)
+    clocks = Clocks(dev if ws == 1 else local)
+    barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    frames(args.steps)
+    ev1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    kt1, _ = qd.qd_get_launch_count(T)
+    kc1, _ = qd.qd_get_launch_count(C)
+    if ws > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = ws * args.steps / (ms / 1e3)
+
+    # frame loop alone (Talker prefill excluded), two trajectories
+    evs = []
+    frames(2 * FRAME_TRAJ, evs)
+    torch.cuda.synchronize()
+    loop_ms = sum(a.elapsed_time(b) for a, b, _ in evs)
+    loop_n = sum(k for _, _, k in evs)
+    frame_us = 1e3 * loop_ms / loop_n
+    traj_bytes = sum(W.frame_bytes(ts.prefill + f + 1, talker_step=f < FRAME_TRAJ - 1) for f in range(FRAME_TRAJ))
+    frame_bytes = traj_bytes / FRAME_TRAJ
+    frame_gbs = frame_bytes / (frame_us / 1e6) / 1e9
+
+    # the step kernel on each model: predictor steps (positions 16..) and Talker steps
+    # at the positions the handles hold after a trajectory
+    pc, sc = qd.qd_get_pos(C)
+    reps_c = max(1, min(12, sc - pc - 4))
+    c_ms = qd.qd_time_kernel(C, qd.KERNEL_STEP, reps_c)
+    c_bytes = cs.step_bytes(pc + (reps_c + 1) // 2 + 3)
+    pt, st_ = qd.qd_get_pos(T)
+    reps_t = max(1, min(32, st_ - pt - 4))
+    t_ms = qd.qd_time_kernel(T, qd.KERNEL_STEP, reps_t)
+    t_bytes = ts.step_bytes(pt + (reps_t + 1) // 2 + 3)
+    c_gbs = c_bytes / (c_ms / 1e3) / 1e9
+
+    # end to end through the public API: prompt and text embeddings from pinned host
+    # memory every trajectory, the codes back to host memory
+    prompt_h = torch.from_numpy(prompt_np).pin_memory()
+    text_h = torch.from_numpy(text_np).pin_memory()
+    codes_h = torch.empty((FRAME_TRAJ, 16), dtype=torch.int32).pin_memory()
+    n_e2e = min(args.steps, 2 * FRAME_TRAJ)
+    barrier()
+    t0 = time.perf_counter()
+    done = h2d = d2h = 0
+    while done < n_e2e:
+        k = min(FRAME_TRAJ, n_e2e - done)
+        qd.qd_reset(T)
+        prompt.copy_(prompt_h, non_blocking=True)
+        text[:k].copy_(text_h[:k], non_blocking=True)
+        h2d += prompt_h.numel() * 4 + k * ts.hidden * 4
+        qd.qd_prefill(T, embeds=prompt)
+        d2h += 12
+        qd.qd_frame_generate(F, k, text, codes)
+        codes_h[:k].copy_(codes[:k], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        d2h += k * 16 * 4
+        done += k
+    e2e_s = time.perf_counter() - t0
+    e2e = {"value": ws * n_e2e / e2e_s, "unit": "frames/s", "h2d_bytes_per_step": h2d / n_e2e,
+           "d2h_bytes_per_step": d2h / n_e2e, "steps": n_e2e,
+           "api": "qd_prefill + qd_frame_generate (host embeddings in, host codes out per trajectory)"}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        fps, n, dt, cores = run_oracle_frames(FRAME_TRAJ, budget_s=20.0)
+        cpu = {"value": fps, "unit": "frames/s", "cores": cores, "kind": "oracle",
+               "sample": f"Talker prefill 64 untimed, then {n} frames ({dt:.1f} s)"}
+
+    qd.qd_frame_destroy(F)
+    qd.qd_destroy(C)
+    qd.qd_destroy(T)
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "frames/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": W_, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic: seeded N(0,0.02) bf16 weights and code tables, 1+N(0,0.1) norm gammas, N(0,1) prompt "
+                "and text embeddings",
+        "config": {"workload": FRAMES_DESC, "storage": "bf16 weights, tables and KV cache, fp32 activations",
+                   "timed": f"{args.steps} frames as whole trajectories (reset + Talker prefill 64 + frames), "
+                            "prefill time included; a step is one frame (16 codes)",
+                   "l2": f"inputs larger than L2: {frame_bytes / 1e9:.2f} GB of weights per frame",
+                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "codes_per_s": 16 * value,
+        "roofline": {"bound": "hbm", "achieved": c_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": c_gbs / hbm_peak,
+                     "traffic": None, "traffic_note": "no ncu capture for this workload and kernel build",
+                     "kernel": "decode_step_kernel on the Code Predictor (5 layers + one of 15 heads per launch)",
+                     "bytes_per_launch": c_bytes, "avg_launch_ms": c_ms, "peak_source": peak_src,
+                     "timing": f"CUDA events around {reps_c} predictor steps at positions {pc}..{pc + reps_c + 2}",
+                     "talker_step": {"bytes": t_bytes, "avg_launch_ms": t_ms,
+                                     "achieved_gbs": t_bytes / (t_ms / 1e3) / 1e9}},
+        "frame_hbm": {"bytes_per_frame": frame_bytes, "frame_us": frame_us, "frames_per_s": 1e6 / frame_us,
+                      "achieved_gbs": frame_gbs, "frac": frame_gbs / hbm_peak, "peak_source": peak_src,
+                      "note": f"frame loop only (Talker prefill excluded), {loop_n} frames timed with CUDA events "
+                              "around each qd_frame_generate call; algorithmic bytes per frame averaged over a "
+                              "trajectory (149 Talker steps, 150 x 15 predictor weight passes)"},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(kt1 - kt0 + kc1 - kc0), "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=29000)
     ap.add_argument("--warmup", type=int, default=870)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="asr", choices=["asr", "talker", "tiny"])
+    ap.add_argument("--workload", default="asr", choices=["asr", "talker", "tiny", "frames"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    if args.workload == "frames":
+        if args.steps == ap.get_default("steps"):
+            args.steps = 4 * FRAME_TRAJ
+        if args.warmup == ap.get_default("warmup"):
+            args.warmup = FRAME_TRAJ
     if args.impl == "reference":
-        reference_arm(args)
+        (frames_reference_arm if args.workload == "frames" else reference_arm)(args)
     else:
-        gpu_arm(args)
+        (frames_arm if args.workload == "frames" else gpu_arm)(args)
 
 
 if __name__ == "__main__":

@@ -201,6 +201,72 @@ qd_status qd_time_kernel(qd_handle h, int which, int reps, float *avg_ms);
 const char *qd_last_error(qd_handle h);
 const char *qd_status_string(int status);
 
+/* ---- two-level frame generation ----
+ *
+ * Sources: "Qwen3-TTS ncnn port", section "Talker: non-standard structure and
+ * two-level generation" (per frame the Talker emits one primary code, a Code
+ * Predictor emits 15 residual codes autoregressively from 15 output heads, and the
+ * 16 code embeddings plus the text/pad embedding form the Talker's next input; the
+ * predictor starts afresh every frame); "qwen3-tts-hip OPTIMIZATION_LOG", Code
+ * Predictor sub-stages (a two-position predictor prefill, then one decode step per
+ * further code).
+ *
+ * One frame, given the Talker's last id `p` and final-norm output h_T:
+ *   1. reset the predictor; prefill it with [h_T, E_0[p]] and decode code_1 with
+ *      head 0 (E_0 is the Talker's own embedding table);
+ *   2. for j = 1..14: decode step with input E_j[code_j] and head j -> code_{j+1}
+ *      (code_j joins the predictor's emitted set);
+ *   3. next_in = E_0[p] + E_1[code_1] + ... + E_15[code_15] + text[f], in fp32 in
+ *      that order;
+ *   4. unless this is the call's last frame: a Talker decode step with input next_in
+ *      and token p (p joins the Talker's emitted set) -> the next frame's primary.
+ * Everything stays on the device; one CUDA graph per frame and Talker bucket. */
+#define QD_FRAME_CODES 16
+
+typedef struct qd_frame *qd_frame_handle;
+
+/* qd_frame_create -- bind a Talker handle and a Code Predictor handle.  Talker: a
+ * single-head model with an embedding table (E_0).  Predictor: same hidden size and
+ * dtype, n_heads_out = 15, vocab <= code_rows, first bucket >= 16 positions.
+ * code_tables: HOST array of 15 DEVICE pointers E_1..E_15, each [code_rows, hidden]
+ * in `dtype` (which must be the models' dtype); they are copied into library-owned
+ * memory, so the caller may free them after the call.  Both handles stay owned by
+ * the caller; while the frame handle exists, use the three on one host thread.
+ * Destroying either model first detaches the frame handle (it waits for the frame
+ * work in flight); a detached frame handle accepts only qd_frame_destroy, and
+ * qd_frame_generate returns QD_ESTATE.  Errors (described by qd_last_error of the
+ * Talker): QD_EINVAL, QD_ENOMEM, QD_ECUDA. */
+qd_status qd_frame_create(qd_handle talker, qd_handle predictor, const void *const *code_tables, int code_rows,
+                          int dtype, qd_frame_handle *out);
+
+/* qd_frame_destroy -- synchronise and free the frame handle (not the models). */
+qd_status qd_frame_destroy(qd_frame_handle f);
+
+/* qd_frame_generate -- run n_frames frames.  The first frame starts from the
+ * Talker as it stands (after qd_prefill or any decode step that ran its head);
+ * each later frame starts with the Talker step of the previous one, so the call
+ * runs n_frames - 1 Talker steps and n_frames predictor loops (16 predictor
+ * positions each).
+ *   text_dev    DEVICE fp32 [n_frames, hidden]: text/pad embedding of each frame.
+ *   force_dev   DEVICE int32 [n_frames, 16] or NULL: when given, these ids are fed
+ *               back (embedded, summed, added to the emitted sets) instead of the
+ *               argmaxes, which are still reported; for teacher-forced comparison.
+ *   codes_dev   DEVICE int32 [n_frames, 16]: per frame the primary argmax, then the
+ *               15 residual argmaxes.
+ *   next_in_dev DEVICE fp32 [hidden] or NULL: the last frame's summed embedding
+ *               (the input of the Talker step that would start the next frame).
+ * Queued on the Talker's stream (ordered after both handles' prior work) without a
+ * host synchronisation; device-side errors (an id outside its table) are reported
+ * by the next synchronising call of either handle.  The Talker's cache grows along
+ * its ladder between frames.  Errors: QD_EINVAL, QD_ESTATE (the Talker has produced
+ * no id yet), QD_EKVFULL (the Talker steps would pass its last bucket; checked
+ * before any work). */
+qd_status qd_frame_generate(qd_frame_handle f, int n_frames, const float *text_dev, const int32_t *force_dev,
+                            int32_t *codes_dev, float *next_in_dev);
+
+/* Turn the per-frame CUDA graphs on (default) or off; results are identical. */
+qd_status qd_frame_set_graphs(qd_frame_handle f, int enable);
+
 /* ---- output head without allocation ----
  *
  * The pages have no counterpart to this call; it exists for callers that cannot

@@ -27,12 +27,14 @@ QD_OK, QD_EINVAL, QD_ESTATE, QD_EKVFULL, QD_ENOMEM, QD_ECUDA, QD_EUNSUPPORTED, Q
 QD_F32, QD_BF16 = 0, 1
 QD_MAX_BUCKETS = 8
 QD_MAX_HEADS = 16
+QD_FRAME_CODES = 16
 
 # Every symbol the header declares (tests check the library exports each one).
 EXPORTS = ("qd_create", "qd_destroy", "qd_reset", "qd_prefill", "qd_decode_step", "qd_decode_step_async",
            "qd_decode_greedy", "qd_grow_kv", "qd_get_hidden", "qd_set_debug_taps", "qd_set_graphs", "qd_copy_kv",
            "qd_get_emitted", "qd_get_pos", "qd_get_launch_count", "qd_time_kernel", "qd_last_error",
-           "qd_status_string", "qd_head_argmax_noalloc")
+           "qd_status_string", "qd_head_argmax_noalloc", "qd_frame_create", "qd_frame_destroy",
+           "qd_frame_generate", "qd_frame_set_graphs")
 
 
 class qd_config(ctypes.Structure):
@@ -75,6 +77,10 @@ _SIGS = {
     "qd_last_error": ([_vp], ctypes.c_char_p),
     "qd_status_string": ([_i32], ctypes.c_char_p),
     "qd_head_argmax_noalloc": ([_vp, _vp, _i32, _i32, _i32, _vp, ctypes.c_double, _i32, _vp, _vp, _vp], _i32),
+    "qd_frame_create": ([_vp, _vp, _P(_vp), _i32, _i32, _P(_vp)], _i32),
+    "qd_frame_destroy": ([_vp], _i32),
+    "qd_frame_generate": ([_vp, _i32, _vp, _vp, _vp, _vp], _i32),
+    "qd_frame_set_graphs": ([_vp, _i32], _i32),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -258,3 +264,48 @@ def qd_head_argmax_noalloc(y_dev, w_dev, vocab: int, hidden: int, bf16: bool, em
                                      _ptr(logits_dev), ctypes.c_void_p(stream.cuda_stream))
     if st != QD_OK:
         raise QDError(st, "qd_head_argmax_noalloc failed")
+
+
+class FrameHandle:
+    """Owns a ``qd_frame_handle``; keeps the two model handles alive while it exists.
+    Errors of its calls are described by ``qd_last_error(talker)``."""
+
+    def __init__(self, f: int, talker: Handle, predictor: Handle):
+        self.f = f
+        self.talker = talker
+        self.predictor = predictor
+
+    def __del__(self):
+        try:
+            qd_frame_destroy(self)
+        except Exception:
+            pass
+
+
+def qd_frame_create(talker: Handle, predictor: Handle, code_tables: Sequence["torch.Tensor"], bf16: bool) -> FrameHandle:
+    """code_tables: the 15 device tables E_1..E_15, each [code_rows, hidden]."""
+    if len(code_tables) != QD_FRAME_CODES - 1:
+        raise ValueError(f"need {QD_FRAME_CODES - 1} code tables")
+    rows = int(code_tables[0].shape[0])
+    arr = (ctypes.c_void_p * len(code_tables))(*[_ptr(t) for t in code_tables])
+    out = ctypes.c_void_p()
+    _check(talker, _lib.qd_frame_create(talker.h, predictor.h, arr, rows, QD_BF16 if bf16 else QD_F32,
+                                        ctypes.byref(out)))
+    return FrameHandle(out.value, talker, predictor)
+
+
+def qd_frame_destroy(f: FrameHandle):
+    if f is not None and f.f:
+        _lib.qd_frame_destroy(f.f)
+        f.f = None
+
+
+def qd_frame_set_graphs(f: FrameHandle, enable: bool):
+    _check(f.talker, _lib.qd_frame_set_graphs(f.f, int(bool(enable))))
+
+
+def qd_frame_generate(f: FrameHandle, n_frames: int, text_dev, codes_dev, force_dev=None, next_in_dev=None):
+    """text_dev fp32 [n_frames, hidden]; codes_dev int32 [n_frames, 16] (written);
+    force_dev int32 [n_frames, 16] or None; next_in_dev fp32 [hidden] or None."""
+    _check(f.talker, _lib.qd_frame_generate(f.f, int(n_frames), _ptr(text_dev), _ptr(force_dev), _ptr(codes_dev),
+                                            _ptr(next_in_dev)))

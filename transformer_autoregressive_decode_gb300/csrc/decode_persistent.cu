@@ -545,11 +545,11 @@ size_t persistent_att_bytes(int group, int hd, int chunk_max) {
            4;
 }
 
-cudaError_t persistent_init(bool bf16, int hd, int hidden, int q_dim, int ffn, size_t smem) {
+cudaError_t persistent_init(bool bf16, int hd, int hidden, int q_dim, int ffn) {
     StepFn f = step_fn(bf16, hd, hidden, q_dim, ffn);
     if (!f) return cudaErrorInvalidValue;
     return cudaFuncSetAttribute(reinterpret_cast<const void *>(f), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)smem);
+                                kStepMaxSmem);
 }
 
 cudaError_t launch_persistent(bool bf16, int hd, int hidden, int q_dim, int ffn, const StepArgs &a, int grid,

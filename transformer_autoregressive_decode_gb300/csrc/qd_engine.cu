@@ -22,97 +22,13 @@
 #include <string>
 #include <vector>
 
-#include "../../include/qd.h"
-#include "qd_device.cuh"
-#include "qd_internal.h"
+#include "qd_model.h"
 
 using namespace qd;
 
-namespace {
-
-struct Layer {
-    void *w_qkv, *w_o, *w_gu, *w_d;
-    float *attn_norm, *mlp_norm, *q_norm, *k_norm;
-};
-
-constexpr int kIdsCap = 1 << 20;
-
-}  // namespace
-
-struct qd_model {
-    qd_config cfg{};
-    bool bf16 = false;
-    size_t esize = 4;
-    int device = 0, num_sms = 0;
-    cudaStream_t user = nullptr, ls = nullptr;
-    cudaEvent_t ev_in = nullptr, ev_out = nullptr, ev_t0 = nullptr, ev_t1 = nullptr;
-
-    // library-owned weights
-    void *arena = nullptr;
-    std::vector<Layer> layers;
-    void *embed = nullptr;
-    void *heads[QD_MAX_HEADS] = {};
-    const void **d_heads = nullptr;
-    float *final_norm = nullptr;
-    float *rope_cos = nullptr, *rope_sin = nullptr;
-    int max_pos = 0;
-
-    // step scratch
-    void *scratch = nullptr;
-    float *x = nullptr, *qkv = nullptr, *att = nullptr, *act = nullptr, *y = nullptr;
-    float *embed_in = nullptr, *stage_embeds = nullptr, *head_pv = nullptr;
-    int *head_cnt = nullptr, *head_pi = nullptr, *stage_tokens = nullptr;
-    int32_t *ids = nullptr;
-    uint32_t *emitted = nullptr;
-    DevState *st = nullptr;
-    int *pin = nullptr;  // pinned host words: out_id, n_gen, status
-    int chunk_max = 0;
-
-    // buckets
-    std::vector<void *> kv;                   // per bucket, allocated on first use
-    std::vector<cudaGraphExec_t> graphs[2];   // [with_head][bucket]
-    int cur_bucket = 0;
-    int h_pos = 0;
-    int h_ngen = 0;
-    bool have_hidden = false;
-
-    // launch geometry
-    int grid_qkv = 0, grid_o = 0, grid_gu = 0, grid_d = 0, grid_head = 0;
-    int rs_h = 0, rs_q = 0, rs_f = 0;
-    int nst_qkv = 0, nst_o = 0, nst_gu = 0, nst_d = 0, nst_head = 0;
-    int rps_h = 0, rps_q = 0, rps_f = 0;
-    int rmax_qkv = 0, rmax_o = 0, rmax_gu = 0, rmax_d = 0, rmax_head = 0;
-    size_t smem_qkv = 0, smem_o = 0, smem_gu = 0, smem_d = 0, smem_head = 0;
-    int evict_last_layers = 0;
-
-    // persistent decode step (one cooperative launch per step)
-    bool persistent = false;
-    LayerDev *d_layers = nullptr;
-    unsigned *barrier = nullptr;
-    float *part_o = nullptr, *part_ml = nullptr;
-    size_t smem_step = 0;
-    int nst_step = 0, off_full = 0, off_gsm = 0, off_misc = 0, off_res = 0, off_att = 0, off_emw = 0, off_xin = 0;
-
-    bool use_graphs = true;
-    bool use_pdl = true;
-    float *tap_hidden = nullptr, *tap_logits = nullptr;
-    long long launches = 0;
-    std::string err;
-
-    int q_dim() const { return cfg.n_q_heads * cfg.head_dim; }
-    int kv_dim() const { return cfg.n_kv_heads * cfg.head_dim; }
-    int S() const { return cfg.buckets[cur_bucket]; }
-    int kernels_per_step(bool with_head) const {
-        return persistent ? 1 : 5 * cfg.n_layers + (with_head ? 1 : 0);
-    }
-    size_t kv_bytes(int bucket) const {
-        return (size_t)cfg.n_layers * 2 * kv_dim() * (size_t)cfg.buckets[bucket] * esize;
-    }
-};
-
 // ------------------------------------------------------------------ errors
 
-static qd_status fail(qd_model *m, qd_status st, const char *fmt, ...) {
+qd_status fail(qd_model *m, qd_status st, const char *fmt, ...) {
     if (m) {
         char buf[512];
         va_list ap;
@@ -129,17 +45,9 @@ static qd_status fail(qd_model *m, qd_status st, const char *fmt, ...) {
     return st;
 }
 
-#define CU(call)                                                                                   \
-    do {                                                                                           \
-        cudaError_t e_ = (call);                                                                   \
-        if (e_ != cudaSuccess)                                                                     \
-            return fail(m, e_ == cudaErrorMemoryAllocation ? QD_ENOMEM : QD_ECUDA, "%s: %s (%s:%d)", #call, \
-                        cudaGetErrorString(e_), __FILE__, __LINE__);                               \
-    } while (0)
-
 // ------------------------------------------------------------------ helpers
 
-static bool is_device_ptr(const void *p) {
+bool is_device_ptr(const void *p) {
     if (!p) return false;
     cudaPointerAttributes at;
     if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
@@ -184,11 +92,11 @@ static qd_status validate_config(qd_model *m, const qd_config *c) {
     return QD_OK;
 }
 
-static void enter(qd_model *m) {
+void enter(qd_model *m) {
     cudaEventRecord(m->ev_in, m->user);
     cudaStreamWaitEvent(m->ls, m->ev_in, 0);
 }
-static void leave(qd_model *m) {
+void leave(qd_model *m) {
     cudaEventRecord(m->ev_out, m->ls);
     cudaStreamWaitEvent(m->user, m->ev_out, 0);
 }
@@ -424,7 +332,7 @@ static StepArgs step_args(qd_model *m, bool with_head, bool taps) {
 }
 
 // Enqueue one step's kernels on stream s.
-static qd_status enqueue_step(qd_model *m, cudaStream_t s, bool with_head, bool taps) {
+qd_status enqueue_step(qd_model *m, cudaStream_t s, bool with_head, bool taps) {
     const qd_config &c = m->cfg;
     const bool bf = m->bf16, pdl = m->use_pdl;
     const int h = c.hidden;
@@ -481,14 +389,14 @@ static qd_status run_step(qd_model *m, bool with_head) {
 }
 
 // Grow along the ladder when the next write position has reached Smax.
-static qd_status grow_if_needed(qd_model *m) {
+qd_status grow_if_needed(qd_model *m) {
     if (m->h_pos < m->S()) return QD_OK;
     if (m->cur_bucket + 1 >= m->cfg.n_buckets)
         return fail(m, QD_EKVFULL, "position %d reaches the last bucket (%d)", m->h_pos, m->S());
     return migrate(m, m->cur_bucket + 1);
 }
 
-static qd_status sync_and_check(qd_model *m, int *out_id) {
+qd_status sync_and_check(qd_model *m, int *out_id) {
     CU(cudaMemcpyAsync(m->pin, &m->st->out_id, 3 * sizeof(int), cudaMemcpyDeviceToHost, m->ls));
     CU(cudaStreamSynchronize(m->ls));
     if (m->pin[2]) return fail(m, QD_EDEVICE, "device error bits 0x%x", m->pin[2]);
@@ -719,7 +627,7 @@ static qd_status setup_persistent(qd_model *m) {
         tail += ((size_t)head_rows / 32 + 2) * 4 + 16;                 // emitted words of the head rows
         tail += (size_t)std::max({m->q_dim(), c.hidden, c.ffn}) * 4 + 16;  // phase input vector
     }
-    const size_t max_smem = 227 * 1024;
+    const size_t max_smem = kStepMaxSmem;
     int nst = (int)((max_smem - tail) / kSlotBytes);
     nst = std::min(nst, 6);
     if (nst < 2) return QD_OK;
@@ -735,7 +643,7 @@ static qd_status setup_persistent(qd_model *m) {
     m->smem_step = align_up(off, 16);
     m->nst_step = nst;
     if (m->smem_step > max_smem) return QD_OK;
-    CU(persistent_init(m->bf16, c.head_dim, c.hidden, m->q_dim(), c.ffn, m->smem_step));
+    CU(persistent_init(m->bf16, c.head_dim, c.hidden, m->q_dim(), c.ffn));
     // layer table
     std::vector<LayerDev> host(c.n_layers);
     for (int l = 0; l < c.n_layers; ++l) {
@@ -771,6 +679,7 @@ const char *qd_last_error(qd_handle h) { return h ? h->err.c_str() : "null handl
 
 static void destroy_model(qd_model *m) {
     if (!m) return;
+    while (!m->frames.empty()) frame_detach(m->frames.back());
     if (m->ls) cudaStreamSynchronize(m->ls);
     for (int v = 0; v < 2; ++v)
         for (auto &g : m->graphs[v])

@@ -129,10 +129,15 @@ struct StepArgs {
     DevState *st;
 };
 
+// Dynamic shared memory ceiling of the persistent step kernel.  The kernel's
+// max-dynamic-smem attribute is set to this once for every instantiation, so
+// handles of the same shape with different layouts can coexist.
+constexpr int kStepMaxSmem = 227 * 1024;
+
 // Persistent kernel for (dtype, head_dim, hidden, q_dim, ffn): false if there is no
 // instantiation for the shape (the per-phase kernels are used then).
 bool persistent_supported(bool bf16, int hd, int hidden, int q_dim, int ffn);
-cudaError_t persistent_init(bool bf16, int hd, int hidden, int q_dim, int ffn, size_t smem);
+cudaError_t persistent_init(bool bf16, int hd, int hidden, int q_dim, int ffn);
 cudaError_t launch_persistent(bool bf16, int hd, int hidden, int q_dim, int ffn, const StepArgs &a, int grid,
                               size_t smem, cudaStream_t s);
 size_t persistent_att_bytes(int group, int hd, int chunk_max);
@@ -151,5 +156,39 @@ cudaError_t launch_kv_migrate(const void *src, int S_old, void *dst, int S_new, 
                               int n_pos, cudaStream_t s);
 cudaError_t launch_rope_table(float *cos_t, float *sin_t, int n_pos, int head_dim, double theta, cudaStream_t s);
 cudaError_t launch_to_f32(const void *src, bool bf16, float *dst, int n, cudaStream_t s);
+
+// ---------------------------------------------------------------------------------
+// Two-level frame loop: kernels that build the Code Predictor's and the Talker's
+// inputs from device-resident ids.
+// ---------------------------------------------------------------------------------
+constexpr int kFrameCodes = 16;    // primary code + 15 residual codes per frame
+
+struct FrameCtl {                  // device; written by the host once per call
+    int f;                         // frame index within the call, advanced by the sum kernel
+    int n_frames;
+    const float *text;             // [n_frames][hidden] text/pad embedding of each frame
+    const int32_t *force;          // [n_frames][16] ids fed back instead of the argmax, or null
+    int32_t *codes;                // [n_frames][16] argmax ids: primary, then the 15 residual codes
+    float *next_in;                // [hidden] the last frame's summed embedding, or null
+};
+
+struct FrameArgs {                 // fixed for a frame generator (graphs capture it)
+    const void *table[kFrameCodes];// [0] the Talker's embedding table, [1..15] code tables
+    int rows0, rows;               // rows of table 0 and of tables 1..15
+    int bf16, hidden;
+    FrameCtl *ctl;
+    DevState *t_st;                // Talker
+    const float *t_y;              // Talker final-norm output of its last position
+    float *t_embed_in;
+    DevState *c_st;                // Code Predictor
+    const int32_t *c_ids;          // its id history (codes of the frame in flight)
+    float *c_embed_in, *c_stage;
+    uint32_t *c_emitted;
+    int c_emitted_words;
+};
+
+cudaError_t launch_frame_cp_prefill(const FrameArgs &a, cudaStream_t s);
+cudaError_t launch_frame_cp_input(const FrameArgs &a, int j, cudaStream_t s);
+cudaError_t launch_frame_sum(const FrameArgs &a, cudaStream_t s);
 
 }  // namespace qd
