@@ -97,6 +97,10 @@ def _lib_handle():
             L.orc_round_bf16.restype = ctypes.c_uint16
             L.orc_frame_sum.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
             L.orc_frame_sum.restype = i32
+            L.orc_set_kv.argtypes = [vp, vp, i32]
+            L.orc_set_kv.restype = i32
+            L.orc_linear.argtypes = [vp, i32, i32, i32, vp, i32, vp]
+            L.orc_linear.restype = i32
             L.orc_num_threads.argtypes = []
             L.orc_num_threads.restype = i32
             L.orc_set_threads.argtypes = [i32]
@@ -207,6 +211,12 @@ class Oracle:
         self._check(self.L.orc_forward(self.h, _ptr(e), int(token), int(add_emitted), int(want_head), head_idx,
                                        ctypes.byref(oid), _ptr(logits), _ptr(tp), ctypes.byref(margin)), "forward")
         return oid.value, logits, margin.value, tp
+
+    def set_kv(self, kv: np.ndarray, length: int):
+        """Start from a cache [n_layers, 2, n_kv_heads, length, head_dim] in the cache
+        type (bf16 bits as uint16 on the bf16 path, else float32)."""
+        k = np.ascontiguousarray(kv)
+        self._check(self.L.orc_set_kv(self.h, k.ctypes.data if length else None, int(length)), "set_kv")
 
     def hidden(self) -> np.ndarray:
         out = np.empty(self.shape.hidden, np.float32)
@@ -322,6 +332,20 @@ class FrameLoop:
                 primary, _, primary_margin, _ = self.talker.step(token=p, embed=next_in[f], head_idx=0,
                                                                  want_logits=False)
         return codes, margins, next_in, h_t
+
+
+def linear(W: np.ndarray, x: np.ndarray) -> np.ndarray:
+    """out[t] = W x[t] for every row of x (W float32 or bfloat16 bits [R, K])."""
+    Wc = np.ascontiguousarray(W)
+    xc = np.ascontiguousarray(x, np.float32)
+    R, K = Wc.shape
+    T = xc.shape[0]
+    out = np.empty((T, R), np.float32)
+    st = _lib_handle().orc_linear(Wc.ctypes.data, int(Wc.dtype == np.uint16), R, K, xc.ctypes.data, T,
+                                  out.ctypes.data)
+    if st != OK:
+        raise OracleError(st, "linear")
+    return out
 
 
 # ---- primitives (for the pins) ----

@@ -630,3 +630,51 @@ int orc_frame_sum(const void *const *tables, const int *rows, const int32_t *ids
     }
     return ORC_OK;
 }
+
+/* ---------------------------------------------------------------- batched linear */
+
+/* out[t][r] = sum_k W[r][k] x[t][k] for T input rows: the projection of every
+ * token of a batch is the same matrix-vector product as one decode step's, row by
+ * row in index order ([hip] "qkv_gemm" / "gate_up_gemm" stages; a batch of tokens
+ * changes only how many vectors meet the same weights).  Pinned by the tests against
+ * an fp64 product within the fp32 summation bound. */
+int orc_linear(const void *W, int w_bf16, int R, int K, const float *x, int T, float *out) {
+    if (!W || !x || !out || R < 1 || K < 1 || T < 0) return ORC_EINVAL;
+    orc_config c;
+    memset(&c, 0, sizeof(c));
+    c.w_bf16 = w_bf16;
+    for (int t = 0; t < T; ++t) matvec(&c, W, R, K, x + (size_t)t * K, out + (size_t)t * R);
+    return ORC_OK;
+}
+
+/* Start a stream from a given cache (the multi-stream workload begins each stream
+ * with a cache of its own length instead of a prefill): positions [0, L) of every
+ * layer's K and V from `kv` ([n_layers][2][n_kv_heads][L][head_dim] in the cache
+ * type: bfloat16 bits when kv_bf16, else float32), position L, empty emitted set, in
+ * the smallest bucket that holds L positions.  The stored entries are taken as they
+ * are (they are already values of the cache type). */
+int orc_set_kv(orc_model *m, const void *kv, int L) {
+    const orc_config *c = &m->c;
+    if (L < 0 || (L > 0 && !kv)) return ORC_EINVAL;
+    int b = 0;
+    while (b < c->n_buckets && c->buckets[b] < L) ++b;
+    if (b == c->n_buckets) return ORC_EKVFULL;
+    int st = orc_reset(m);
+    if (st) return st;
+    if (b != 0) {
+        free(m->kv);
+        m->bucket = b;
+        m->S = c->buckets[b];
+        m->kv = calloc(kv_elems(c, m->S), kv_esize(c));
+        if (!m->kv) return ORC_ENOMEM;
+    }
+    const size_t es = kv_esize(c), row = (size_t)c->head_dim * es;
+    for (int l = 0; l < c->n_layers; ++l)
+        for (int w = 0; w < 2; ++w)
+            for (int g = 0; g < c->n_kv_heads; ++g) {
+                const char *src = (const char *)kv + (((size_t)l * 2 + w) * c->n_kv_heads + g) * (size_t)L * row;
+                memcpy((char *)m->kv + kv_index(c, m->S, l, w, g, 0) * es, src, (size_t)L * row);
+            }
+    m->pos = L;
+    return ORC_OK;
+}

@@ -83,6 +83,13 @@ int orc_recompute_logits(const orc_config *cfg, const void *const *weights, cons
 int orc_frame_sum(const void *const *tables, const int *rows, const int32_t *ids, int n_tables, int hidden,
                   int bf16, const float *text, float *out);
 
+/* Start from a given cache: kv [n_layers][2][n_kv_heads][L][head_dim] in the cache
+ * type (bf16 bits when kv_bf16), position L, empty emitted set. */
+int orc_set_kv(orc_model *m, const void *kv, int L);
+
+/* Batched linear: out[t][r] = sum_k W[r][k] x[t][k], x [T, K], out [T, R]. */
+int orc_linear(const void *W, int w_bf16, int R, int K, const float *x, int T, float *out);
+
 /* Primitives the model is built from, exposed for the pins. */
 void orc_rmsnorm(const float *x, const float *gamma, int n, double eps, float *out);
 void orc_rope(float *v, int head_dim, int pos, double theta);

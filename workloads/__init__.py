@@ -278,5 +278,19 @@ def frame_bytes(talker_L: int, talker_step: bool = True) -> int:
     return b + (TALKER.step_bytes(talker_L) if talker_step else 0)
 
 
-def batch_initial_lengths(seed: int = 0) -> np.ndarray:
-    return uniform_int("batched/L0", BATCH_STREAMS, BATCH_L0[0], BATCH_L0[1], seed)
+def batch_initial_lengths(seed: int = 0, n: int = BATCH_STREAMS, lo: int = BATCH_L0[0],
+                          hi: int = BATCH_L0[1]) -> np.ndarray:
+    """Cached length of each stream at the start of the batched workload, ~ U{lo..hi}."""
+    return uniform_int("batched/L0", n, lo, hi, seed)
+
+
+def batch_stream_kv(shape: "Shape", stream: int, length: int, seed: int = 0) -> np.ndarray:
+    """Initial cache of one stream, [n_layers, 2, n_kv_heads, length, head_dim] ~ N(0, 1)
+    as bf16 bits (the batched workload starts from filled caches, not from a prefill)."""
+    return normal(f"batched/kv/{stream}", (shape.n_layers, 2, shape.n_kv_heads, length, shape.head_dim), seed,
+                  0.0, 1.0, bf16=True)
+
+
+def batch_first_tokens(n: int, vocab: int, seed: int = 0) -> np.ndarray:
+    """Input token of each stream's first step, ~ U{0..vocab-1}."""
+    return uniform_int("batched/first_token", n, 0, vocab - 1, seed)
