@@ -172,6 +172,21 @@ qd_status qd_set_debug_taps(qd_handle h, float *hidden_taps_dev, float *logits_d
 /* Turn CUDA-graph replay on (default) or off; results are identical. */
 qd_status qd_set_graphs(qd_handle h, int enable);
 
+/* qd_gemm_bf16 -- the batched paths' tensor-core contraction on its own (a check
+ * and measurement tap): out[t][r] = sum_k W[r][k] * x[t][k] for W (DEVICE bf16
+ * [R, K] row-major, 16-byte aligned) and x (DEVICE fp32 [T, K] row-major), with x
+ * split into bf16 hi + lo parts (x_lo = bf16(x - bf16(x))) so the products carry
+ * ~16 bits of x; fp32 accumulation.  mode 0: out = the product (fp32 [T, R]);
+ * 1: out += the product; 2: rows (2i, 2i+1) are (gate_i, up_i) and out (fp32
+ * [T, R/2]) = silu(gate) * up.  R a multiple of 128, K of 64.  Allocates its
+ * scratch, runs on cuda_stream and synchronises it.  When avg_ms (HOST) is non-NULL
+ * the contraction kernel is then launched `reps` more times between CUDA events and
+ * its mean duration is written there (mode 1 accumulates into out each time).
+ * Errors: QD_EINVAL, QD_EUNSUPPORTED (shape), QD_ENOMEM, QD_ECUDA, QD_EDEVICE (a
+ * bounded wait expired). */
+qd_status qd_gemm_bf16(const void *w_dev, const float *x_dev, float *out_dev, int R, int K, int T, int mode,
+                       void *cuda_stream, int reps, float *avg_ms);
+
 /* Copy the current cache buffer, layout [n_layers][2 (K,V)][n_kv_heads][Smax][head_dim]
  * in the KV dtype, into dst_dev (DEVICE, at least *bytes). Query the size by
  * passing dst_dev = NULL. Synchronises. */
@@ -297,6 +312,55 @@ qd_status qd_frame_set_graphs(qd_frame_handle f, int enable);
 qd_status qd_head_argmax_noalloc(const float *y_dev, const void *w_dev, int vocab, int hidden, int dtype,
                                  const uint32_t *emitted_dev, double rep_penalty, int eos_mask_id,
                                  int32_t *out_id_dev, float *logits_dev, void *cuda_stream);
+
+/* ---- batched multi-stream decode ----
+ *
+ * B independent streams decoded together over one model's weights, one token per
+ * stream per step, so the projections and the MLP become dense contractions with the
+ * streams as one dimension; they run on the tensor cores (bf16 weights, activations
+ * as bf16 hi + lo parts, fp32 accumulation).  Each stream has its own cache
+ * [n_layers][K, V][n_kv_heads][smax][head_dim] (bf16), position, input token and
+ * emitted set; the step does for every stream what qd_decode_step does for one
+ * (embedding row of the input token, which joins the stream's emitted set; every
+ * layer; final norm, head, repetition penalty, EOS mask, argmax) and feeds each
+ * stream's argmax back as its next input token.  Sources: "Qwen3-TTS ncnn port",
+ * section "Talker: non-standard structure and two-level generation" (the per-stream
+ * step); "qwen3-tts-hip OPTIMIZATION_LOG", decode-step profile (its stages). */
+typedef struct qd_batch *qd_batch_handle;
+
+/* qd_batch_create -- n_streams streams of at most smax positions (a multiple of 32)
+ * over `model`'s weights (bf16, one output head, an embedding table; the model must
+ * outlive the batch).  Allocates n_streams caches.  Errors: QD_EINVAL,
+ * QD_EUNSUPPORTED (shape), QD_ENOMEM, QD_ECUDA; described by qd_last_error(model). */
+qd_status qd_batch_create(qd_handle model, int n_streams, int smax, qd_batch_handle *out);
+qd_status qd_batch_destroy(qd_batch_handle b);
+
+/* qd_batch_set_stream -- (re)start stream `stream` with `length` cached positions
+ * copied from kv_dev (DEVICE bf16 [n_layers][2][n_kv_heads][length][head_dim], may be
+ * NULL when length is 0) and input token `token` (< embed_rows) for its next step; its
+ * emitted set is cleared.  Synchronises. */
+qd_status qd_batch_set_stream(qd_batch_handle b, int stream, const void *kv_dev, int length, int32_t token);
+
+/* qd_batch_decode -- n_steps greedy steps of every stream.  ids_dev: DEVICE int32
+ * [n_steps][B] receives each stream's argmax per step.  force_dev: DEVICE int32
+ * [n_steps][B] or NULL: when given, these ids are fed back as the next input tokens
+ * instead of the argmaxes (teacher forcing).  Asynchronous; device-side errors are
+ * reported by qd_batch_sync.  Errors: QD_EINVAL, QD_ESTATE (a stream never set),
+ * QD_EKVFULL (a stream would pass smax; checked before any work). */
+qd_status qd_batch_decode(qd_batch_handle b, int n_steps, const int32_t *force_dev, int32_t *ids_dev);
+
+/* Synchronise; QD_EDEVICE if a kernel reported an error (bounded wait, bad id). */
+qd_status qd_batch_sync(qd_batch_handle b);
+
+/* Taps: raw logits of the last step (DEVICE fp32 [B][vocab]); one stream's cache
+ * (query the size with dst_dev = NULL); host view of a stream's position; launches. */
+qd_status qd_batch_get_logits(qd_batch_handle b, float *dst_dev);
+qd_status qd_batch_copy_kv(qd_batch_handle b, int stream, void *dst_dev, size_t *bytes);
+qd_status qd_batch_get_pos(qd_batch_handle b, int stream, int *pos);
+qd_status qd_batch_get_launch_count(qd_batch_handle b, long long *kernels, int *kernels_per_step);
+
+/* Turn the per-step CUDA graph on (default) or off; results are identical. */
+qd_status qd_batch_set_graphs(qd_batch_handle b, int enable);
 
 #ifdef __cplusplus
 }

@@ -23,7 +23,7 @@ def qd():
 def _declared():
     src = open(os.path.join(ROOT, "include", "qd.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(qd_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(qd_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_header_declares_the_boundary():

@@ -34,7 +34,9 @@ EXPORTS = ("qd_create", "qd_destroy", "qd_reset", "qd_prefill", "qd_decode_step"
            "qd_decode_greedy", "qd_grow_kv", "qd_get_hidden", "qd_set_debug_taps", "qd_set_graphs", "qd_copy_kv",
            "qd_get_emitted", "qd_get_pos", "qd_get_launch_count", "qd_time_kernel", "qd_last_error",
            "qd_status_string", "qd_head_argmax_noalloc", "qd_frame_create", "qd_frame_destroy",
-           "qd_frame_generate", "qd_frame_set_graphs")
+           "qd_frame_generate", "qd_frame_set_graphs", "qd_gemm_bf16", "qd_batch_create", "qd_batch_destroy",
+           "qd_batch_set_stream", "qd_batch_decode", "qd_batch_sync", "qd_batch_get_logits", "qd_batch_copy_kv",
+           "qd_batch_get_pos", "qd_batch_get_launch_count", "qd_batch_set_graphs")
 
 
 class qd_config(ctypes.Structure):
@@ -81,6 +83,17 @@ _SIGS = {
     "qd_frame_destroy": ([_vp], _i32),
     "qd_frame_generate": ([_vp, _i32, _vp, _vp, _vp, _vp], _i32),
     "qd_frame_set_graphs": ([_vp, _i32], _i32),
+    "qd_gemm_bf16": ([_vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32, _P(ctypes.c_float)], _i32),
+    "qd_batch_create": ([_vp, _i32, _i32, _P(_vp)], _i32),
+    "qd_batch_destroy": ([_vp], _i32),
+    "qd_batch_set_stream": ([_vp, _i32, _vp, _i32, ctypes.c_int32], _i32),
+    "qd_batch_decode": ([_vp, _i32, _vp, _vp], _i32),
+    "qd_batch_sync": ([_vp], _i32),
+    "qd_batch_get_logits": ([_vp, _vp], _i32),
+    "qd_batch_copy_kv": ([_vp, _i32, _vp, _P(_sz)], _i32),
+    "qd_batch_get_pos": ([_vp, _i32, _P(_i32)], _i32),
+    "qd_batch_get_launch_count": ([_vp, _P(_i64), _P(_i32)], _i32),
+    "qd_batch_set_graphs": ([_vp, _i32], _i32),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -309,3 +322,91 @@ def qd_frame_generate(f: FrameHandle, n_frames: int, text_dev, codes_dev, force_
     force_dev int32 [n_frames, 16] or None; next_in_dev fp32 [hidden] or None."""
     _check(f.talker, _lib.qd_frame_generate(f.f, int(n_frames), _ptr(text_dev), _ptr(force_dev), _ptr(codes_dev),
                                             _ptr(next_in_dev)))
+
+
+GEMM_STORE, GEMM_RESIDUAL, GEMM_SWIGLU = 0, 1, 2
+
+
+def qd_gemm_bf16(w_dev, x_dev, out_dev, mode: int = GEMM_STORE, stream=None, time_reps: int = 0):
+    """out = x @ W^T on the tensor cores (W bf16 [R, K], x fp32 [T, K]); see qd.h.
+    With time_reps > 0, returns the kernel's mean duration in ms over that many launches."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    R, K = int(w_dev.shape[0]), int(w_dev.shape[1])
+    T = int(x_dev.shape[0])
+    ms = ctypes.c_float(0.0)
+    st = _lib.qd_gemm_bf16(_ptr(w_dev), _ptr(x_dev), _ptr(out_dev), R, K, T, int(mode),
+                           ctypes.c_void_p(stream.cuda_stream), int(time_reps),
+                           ctypes.byref(ms) if time_reps > 0 else None)
+    if st != QD_OK:
+        raise QDError(st, "qd_gemm_bf16 failed")
+    return ms.value if time_reps > 0 else None
+
+
+class BatchHandle:
+    """Owns a ``qd_batch_handle``; keeps its model handle alive.  Errors are described
+    by ``qd_last_error(model)``."""
+
+    def __init__(self, b: int, model: Handle, n_streams: int, smax: int):
+        self.b = b
+        self.model = model
+        self.n_streams = n_streams
+        self.smax = smax
+
+    def __del__(self):
+        try:
+            qd_batch_destroy(self)
+        except Exception:
+            pass
+
+
+def qd_batch_create(model: Handle, n_streams: int, smax: int) -> BatchHandle:
+    out = ctypes.c_void_p()
+    _check(model, _lib.qd_batch_create(model.h, int(n_streams), int(smax), ctypes.byref(out)))
+    return BatchHandle(out.value, model, n_streams, smax)
+
+
+def qd_batch_destroy(b: BatchHandle):
+    if b is not None and b.b:
+        _lib.qd_batch_destroy(b.b)
+        b.b = None
+
+
+def qd_batch_set_stream(b: BatchHandle, stream: int, kv_dev, length: int, token: int):
+    """kv_dev: device bf16 tensor [n_layers, 2, n_kv_heads, length, head_dim] (or None when length is 0)."""
+    _check(b.model, _lib.qd_batch_set_stream(b.b, int(stream), _ptr(kv_dev), int(length), int(token)))
+
+
+def qd_batch_decode(b: BatchHandle, n_steps: int, ids_dev, force_dev=None):
+    _check(b.model, _lib.qd_batch_decode(b.b, int(n_steps), _ptr(force_dev), _ptr(ids_dev)))
+
+
+def qd_batch_sync(b: BatchHandle):
+    _check(b.model, _lib.qd_batch_sync(b.b))
+
+
+def qd_batch_get_logits(b: BatchHandle, dst_dev):
+    _check(b.model, _lib.qd_batch_get_logits(b.b, _ptr(dst_dev)))
+
+
+def qd_batch_copy_kv(b: BatchHandle, stream: int, dst_dev=None) -> int:
+    n = ctypes.c_size_t(0 if dst_dev is None else dst_dev.numel() * dst_dev.element_size())
+    _check(b.model, _lib.qd_batch_copy_kv(b.b, int(stream), _ptr(dst_dev), ctypes.byref(n)))
+    return n.value
+
+
+def qd_batch_get_pos(b: BatchHandle, stream: int) -> int:
+    p = ctypes.c_int(0)
+    _check(b.model, _lib.qd_batch_get_pos(b.b, int(stream), ctypes.byref(p)))
+    return p.value
+
+
+def qd_batch_get_launch_count(b: BatchHandle):
+    k, per = ctypes.c_longlong(0), ctypes.c_int(0)
+    _check(b.model, _lib.qd_batch_get_launch_count(b.b, ctypes.byref(k), ctypes.byref(per)))
+    return k.value, per.value
+
+
+def qd_batch_set_graphs(b: BatchHandle, enable: bool):
+    _check(b.model, _lib.qd_batch_set_graphs(b.b, int(bool(enable))))

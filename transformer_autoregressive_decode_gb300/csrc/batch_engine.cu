@@ -1,0 +1,488 @@
+// C-ABI entry points of the batched paths: the tensor-core contraction tap and the
+// multi-stream decode.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <vector>
+
+#include "qd_model.h"
+
+using namespace qd;
+
+namespace {
+
+struct DevBuf {
+    void *p = nullptr;
+    ~DevBuf() {
+        if (p) cudaFree(p);
+    }
+    cudaError_t alloc(size_t bytes) { return cudaMalloc(&p, std::max<size_t>(bytes, 16)); }
+};
+
+}  // namespace
+
+extern "C" {
+
+qd_status qd_gemm_bf16(const void *w_dev, const float *x_dev, float *out_dev, int R, int K, int T, int mode,
+                       void *cuda_stream, int reps, float *avg_ms) {
+    if (!is_device_ptr(w_dev) || !is_device_ptr(x_dev) || !is_device_ptr(out_dev)) return QD_EINVAL;
+    if (mode < TC_STORE || mode > TC_SWIGLU) return QD_EINVAL;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess)
+        return QD_ECUDA;
+    TcGemmPlan plan;
+    if (!tc_gemm_plan(R, K, T, sms, &plan)) return QD_EUNSUPPORTED;
+    if (tc_gemm_init() != cudaSuccess) return QD_ECUDA;
+    if (reinterpret_cast<uintptr_t>(w_dev) & 15) return QD_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    const size_t nx = (size_t)T * K;
+    DevBuf xh, xl, part, cnt, st, ah, al;
+    if (xh.alloc(nx * 2) || xl.alloc(nx * 2) || part.alloc(plan.partial_floats * 4) ||
+        cnt.alloc((size_t)plan.row_tiles * plan.tok_tiles * 4) || st.alloc(4) ||
+        ah.alloc((size_t)T * (R / 2) * 2) || al.alloc((size_t)T * (R / 2) * 2))
+        return QD_ENOMEM;
+    if (cudaMemsetAsync(cnt.p, 0, (size_t)plan.row_tiles * plan.tok_tiles * 4, s) ||
+        cudaMemsetAsync(st.p, 0, 4, s))
+        return QD_ECUDA;
+    if (launch_split_bf16(x_dev, static_cast<__nv_bfloat16 *>(xh.p), static_cast<__nv_bfloat16 *>(xl.p), nx, s))
+        return QD_ECUDA;
+    TcGemmArgs a = {};
+    a.R = R;
+    a.K = K;
+    a.T = T;
+    a.mode = mode;
+    a.out = out_dev;
+    a.ldo = mode == TC_SWIGLU ? R / 2 : R;
+    a.act_hi = static_cast<__nv_bfloat16 *>(ah.p);
+    a.act_lo = static_cast<__nv_bfloat16 *>(al.p);
+    a.partial = plan.splits > 1 ? static_cast<float *>(part.p) : nullptr;
+    a.tile_counter = static_cast<int *>(cnt.p);
+    a.status = static_cast<int *>(st.p);
+    if (launch_tc_gemm(plan, w_dev, xh.p, xl.p, a, s)) return QD_ECUDA;
+    if (avg_ms) {
+        if (reps < 1) return QD_EINVAL;
+        cudaEvent_t e0, e1;
+        if (cudaEventCreate(&e0) || cudaEventCreate(&e1)) return QD_ECUDA;
+        cudaEventRecord(e0, s);
+        for (int i = 0; i < reps; ++i)
+            if (launch_tc_gemm(plan, w_dev, xh.p, xl.p, a, s)) return QD_ECUDA;
+        cudaEventRecord(e1, s);
+        cudaEventSynchronize(e1);
+        float ms = 0.f;
+        cudaEventElapsedTime(&ms, e0, e1);
+        *avg_ms = ms / reps;
+        cudaEventDestroy(e0);
+        cudaEventDestroy(e1);
+    }
+    int status = 0;
+    if (cudaMemcpyAsync(&status, st.p, 4, cudaMemcpyDeviceToHost, s) || cudaStreamSynchronize(s)) return QD_ECUDA;
+    return status ? QD_EDEVICE : QD_OK;
+}
+
+}  // extern "C"
+
+// ====================================================================================
+// Batched multi-stream decode: B independent streams over one model's weights.
+//
+// Per step, for every stream at once: embedding gather of each stream's input token
+// (it joins that stream's emitted set) fused with the first RMSNorm; per layer the
+// fused QKV projection as a tensor-core GEMM (M = 128 weight rows, N = the streams),
+// attention of every stream over its own cache and length (QK-norm, RoPE and the KV
+// append in its prologue), the output projection GEMM with the residual add, RMSNorm,
+// the gate/up GEMM with SwiGLU in its epilogue, the down GEMM with the residual add;
+// then the final RMSNorm, the head GEMM and the per-stream penalty + argmax, which
+// feeds each stream's id (or the caller's forced id) back as its next input.  One
+// CUDA graph holds a whole step; the step index and the output pointers live in a
+// device control block.
+// ====================================================================================
+
+struct qd_batch {
+    qd_model *m = nullptr;
+    int B = 0, S = 0, chunk_max = 0;
+    cudaStream_t ls = nullptr;
+    void *arena = nullptr;
+    void *kv = nullptr;
+    size_t stream_elems = 0;
+    float *x = nullptr, *qkv = nullptr, *logits = nullptr, *rope_cos = nullptr, *rope_sin = nullptr;
+    __nv_bfloat16 *xh = nullptr, *xl = nullptr, *ah = nullptr, *al = nullptr;
+    float *partial = nullptr;
+    int *counters = nullptr, *pos = nullptr, *status = nullptr;
+    int32_t *tokens = nullptr;
+    uint32_t *emitted = nullptr;
+    int words = 0;
+    BatchCtl *ctl = nullptr;
+    TcGemmPlan p_qkv{}, p_o{}, p_gu{}, p_d{}, p_head{};
+    std::vector<int> h_pos;     // host view of each stream's position
+    std::vector<char> h_ready;  // stream has a cache and an input token
+    cudaGraphExec_t graph = nullptr;
+    bool use_graphs = true;
+    long long launches = 0;
+    int kernels_per_step = 0;
+};
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+qd_status batch_fail(qd_batch *b, qd_status st, const char *what) { return fail(b->m, st, "%s", what); }
+
+// Every launch of one step, on stream s.
+qd_status enqueue_batch_step(qd_batch *b, cudaStream_t s) {
+    qd_model *m = b->m;
+    const qd_config &c = m->cfg;
+    const int B = b->B, h = c.hidden, qd_ = m->q_dim(), rows_qkv = qd_ + 2 * m->kv_dim();
+    int n = 0;
+    auto gemm = [&](const TcGemmPlan &p, const void *w, const __nv_bfloat16 *xh, const __nv_bfloat16 *xl, int R,
+                    int K, int mode, float *out, int ldo) -> cudaError_t {
+        TcGemmArgs a = {};
+        a.R = R;
+        a.K = K;
+        a.T = B;
+        a.mode = mode;
+        a.out = out;
+        a.ldo = ldo;
+        a.act_hi = b->ah;
+        a.act_lo = b->al;
+        a.partial = p.splits > 1 ? b->partial : nullptr;
+        a.tile_counter = b->counters;
+        a.status = b->status;
+        ++n;
+        return launch_tc_gemm(p, w, xh, xl, a, s);
+    };
+    auto norm = [&](const float *gamma, bool gather) -> cudaError_t {
+        NormSplitArgs a = {};
+        a.x = b->x;
+        a.K = h;
+        a.gamma = gamma;
+        a.eps = (float)c.rms_eps;
+        a.hi = b->xh;
+        a.lo = b->xl;
+        if (gather) {
+            a.table = m->embed;
+            a.table_rows = c.embed_rows;
+            a.tokens = b->tokens;
+            a.emitted = b->emitted;
+            a.emitted_words = b->words;
+            a.vocab = c.vocab;
+        }
+        a.status = b->status;
+        ++n;
+        return launch_norm_split(a, B, s);
+    };
+    if (norm(m->layers[0].attn_norm, true)) return batch_fail(b, QD_ECUDA, "norm/embedding launch failed");
+    for (int l = 0; l < c.n_layers; ++l) {
+        const Layer &L = m->layers[l];
+        if (gemm(b->p_qkv, L.w_qkv, b->xh, b->xl, rows_qkv, h, TC_STORE, b->qkv, rows_qkv))
+            return batch_fail(b, QD_ECUDA, "QKV GEMM launch failed");
+        BatchAttnArgs at = {};
+        at.qkv = b->qkv;
+        at.qkv_ld = rows_qkv;
+        at.q_gamma = c.qk_norm ? L.q_norm : nullptr;
+        at.k_gamma = c.qk_norm ? L.k_norm : nullptr;
+        at.eps = (float)c.rms_eps;
+        at.scale = (float)(1.0 / std::sqrt((double)c.head_dim));
+        at.rope_cos = b->rope_cos;
+        at.rope_sin = b->rope_sin;
+        at.kv = b->kv;
+        at.stream_elems = b->stream_elems;
+        at.layer_elems = (size_t)l * 2 * c.n_kv_heads * b->S * c.head_dim;
+        at.S = b->S;
+        at.qh = c.n_q_heads;
+        at.kvh = c.n_kv_heads;
+        at.chunk_max = b->chunk_max;
+        at.pos = b->pos;
+        at.out_hi = b->xh;
+        at.out_lo = b->xl;
+        at.status = b->status;
+        ++n;
+        if (launch_batch_attention(c.head_dim, B, at, s)) return batch_fail(b, QD_ECUDA, "attention launch failed");
+        if (gemm(b->p_o, L.w_o, b->xh, b->xl, h, qd_, TC_RESIDUAL, b->x, h))
+            return batch_fail(b, QD_ECUDA, "O GEMM launch failed");
+        if (norm(L.mlp_norm, false)) return batch_fail(b, QD_ECUDA, "norm launch failed");
+        if (gemm(b->p_gu, L.w_gu, b->xh, b->xl, 2 * c.ffn, h, TC_SWIGLU, nullptr, c.ffn))
+            return batch_fail(b, QD_ECUDA, "gate/up GEMM launch failed");
+        if (gemm(b->p_d, L.w_d, b->ah, b->al, h, c.ffn, TC_RESIDUAL, b->x, h))
+            return batch_fail(b, QD_ECUDA, "down GEMM launch failed");
+        const float *next = l + 1 < c.n_layers ? m->layers[l + 1].attn_norm : m->final_norm;
+        if (norm(next, false)) return batch_fail(b, QD_ECUDA, "norm launch failed");
+    }
+    if (gemm(b->p_head, m->heads[0], b->xh, b->xl, c.vocab, h, TC_STORE, b->logits, c.vocab))
+        return batch_fail(b, QD_ECUDA, "head GEMM launch failed");
+    BatchArgmaxArgs am = {};
+    am.logits = b->logits;
+    am.V = c.vocab;
+    am.emitted = b->emitted;
+    am.words = b->words;
+    am.penalty = (float)c.rep_penalty;
+    am.eos = c.eos_mask_id;
+    am.ctl = b->ctl;
+    am.tokens = b->tokens;
+    am.pos = b->pos;
+    am.status = b->status;
+    ++n;
+    if (launch_batch_argmax(am, B, s)) return batch_fail(b, QD_ECUDA, "argmax launch failed");
+    b->kernels_per_step = n;
+    return QD_OK;
+}
+
+qd_status run_batch_step(qd_batch *b) {
+    qd_model *m = b->m;
+    if (!b->use_graphs) return enqueue_batch_step(b, b->ls);
+    if (!b->graph) {
+        cudaGraph_t g = nullptr;
+        CU(cudaStreamBeginCapture(b->ls, cudaStreamCaptureModeThreadLocal));
+        qd_status st = enqueue_batch_step(b, b->ls);
+        cudaError_t ce = cudaStreamEndCapture(b->ls, &g);
+        if (st) {
+            if (g) cudaGraphDestroy(g);
+            return st;
+        }
+        CU(ce);
+        cudaError_t ie = cudaGraphInstantiate(&b->graph, g, 0);
+        cudaGraphDestroy(g);
+        CU(ie);
+    }
+    CU(cudaGraphLaunch(b->graph, b->ls));
+    return QD_OK;
+}
+
+void destroy_batch(qd_batch *b) {
+    if (!b) return;
+    if (b->ls) cudaStreamSynchronize(b->ls);
+    if (b->graph) cudaGraphExecDestroy(b->graph);
+    if (b->arena) cudaFree(b->arena);
+    if (b->kv) cudaFree(b->kv);
+    if (b->ls) cudaStreamDestroy(b->ls);
+    delete b;
+}
+
+// Order the batch's stream after the model's caller stream and back.
+void batch_enter(qd_batch *b) {
+    cudaEventRecord(b->m->ev_in, b->m->user);
+    cudaStreamWaitEvent(b->ls, b->m->ev_in, 0);
+}
+void batch_leave(qd_batch *b) {
+    cudaEventRecord(b->m->ev_out, b->ls);
+    cudaStreamWaitEvent(b->m->user, b->m->ev_out, 0);
+}
+
+}  // namespace
+
+extern "C" {
+
+qd_status qd_batch_create(qd_handle model, int n_streams, int smax, qd_batch_handle *out) {
+    if (!out) return QD_EINVAL;
+    *out = nullptr;
+    if (!model) return QD_EINVAL;
+    qd_model *m = model;
+    const qd_config &c = m->cfg;
+    if (n_streams < 1 || n_streams > 1024) return fail(m, QD_EINVAL, "n_streams %d out of range", n_streams);
+    if (smax < 32 || smax % 32) return fail(m, QD_EINVAL, "smax must be a positive multiple of 32");
+    if (!m->bf16) return fail(m, QD_EUNSUPPORTED, "the batched path needs bf16 weights");
+    if (c.n_heads_out != 1 || !m->embed) return fail(m, QD_EUNSUPPORTED, "the batched path needs one head and an embedding table");
+    const int rows_qkv = m->q_dim() + 2 * m->kv_dim();
+    int sms = m->num_sms;
+    qd_batch *b = new qd_batch();
+    b->m = m;
+    b->B = n_streams;
+    b->S = smax;
+    b->chunk_max = attn_chunk(smax);
+    if (!tc_gemm_plan(rows_qkv, c.hidden, n_streams, sms, &b->p_qkv) ||
+        !tc_gemm_plan(c.hidden, m->q_dim(), n_streams, sms, &b->p_o) ||
+        !tc_gemm_plan(2 * c.ffn, c.hidden, n_streams, sms, &b->p_gu) ||
+        !tc_gemm_plan(c.hidden, c.ffn, n_streams, sms, &b->p_d) ||
+        !tc_gemm_plan(c.vocab, c.hidden, n_streams, sms, &b->p_head)) {
+        delete b;
+        return fail(m, QD_EUNSUPPORTED, "GEMM shapes: rows must be multiples of 128, K of 64");
+    }
+    if (batch_attention_smem_bytes(c.head_dim, c.n_q_heads / c.n_kv_heads, b->chunk_max) > 160 * 1024) {
+        delete b;
+        return fail(m, QD_EUNSUPPORTED, "smax %d too long for the attention tile", smax);
+    }
+    if (tc_gemm_init() != cudaSuccess || batch_kernels_init() != cudaSuccess) {
+        delete b;
+        return fail(m, QD_ECUDA, "tensor-core GEMM or attention kernel setup failed");
+    }
+    const int B = n_streams, h = c.hidden;
+    const int kmax = std::max({h, m->q_dim(), c.ffn});
+    b->words = (c.vocab + 31) / 32;
+    size_t part = 0;
+    int tiles = 0;
+    for (const TcGemmPlan *p : {&b->p_qkv, &b->p_o, &b->p_gu, &b->p_d, &b->p_head}) {
+        part = std::max(part, p->partial_floats);
+        tiles = std::max(tiles, p->row_tiles * p->tok_tiles);
+    }
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = (off + bytes + kAlign - 1) / kAlign * kAlign;
+        return o;
+    };
+    const size_t o_x = take((size_t)B * h * 4), o_qkv = take((size_t)B * rows_qkv * 4),
+                 o_lg = take((size_t)B * c.vocab * 4), o_xh = take((size_t)B * kmax * 2),
+                 o_xl = take((size_t)B * kmax * 2), o_ah = take((size_t)B * c.ffn * 2),
+                 o_al = take((size_t)B * c.ffn * 2), o_part = take(std::max<size_t>(part, 1) * 4),
+                 o_cnt = take((size_t)tiles * 4), o_pos = take((size_t)B * 4), o_st = take(16),
+                 o_tok = take((size_t)B * 4), o_em = take((size_t)B * b->words * 4), o_ctl = take(sizeof(BatchCtl)),
+                 o_cos = take((size_t)smax * (c.head_dim / 2) * 4), o_sin = take((size_t)smax * (c.head_dim / 2) * 4);
+    b->stream_elems = (size_t)c.n_layers * 2 * c.n_kv_heads * smax * c.head_dim;
+    qd_status st = QD_OK;
+    auto check = [&](cudaError_t e, const char *what) {
+        if (e != cudaSuccess && !st)
+            st = fail(m, e == cudaErrorMemoryAllocation ? QD_ENOMEM : QD_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+    };
+    check(cudaStreamCreateWithFlags(&b->ls, cudaStreamNonBlocking), "cudaStreamCreate");
+    check(cudaMalloc(&b->arena, off), "cudaMalloc(batch scratch)");
+    check(cudaMalloc(&b->kv, b->stream_elems * 2 * B), "cudaMalloc(batch KV caches)");
+    if (!st) {
+        uint8_t *A = static_cast<uint8_t *>(b->arena);
+        b->x = reinterpret_cast<float *>(A + o_x);
+        b->qkv = reinterpret_cast<float *>(A + o_qkv);
+        b->logits = reinterpret_cast<float *>(A + o_lg);
+        b->xh = reinterpret_cast<__nv_bfloat16 *>(A + o_xh);
+        b->xl = reinterpret_cast<__nv_bfloat16 *>(A + o_xl);
+        b->ah = reinterpret_cast<__nv_bfloat16 *>(A + o_ah);
+        b->al = reinterpret_cast<__nv_bfloat16 *>(A + o_al);
+        b->partial = reinterpret_cast<float *>(A + o_part);
+        b->counters = reinterpret_cast<int *>(A + o_cnt);
+        b->pos = reinterpret_cast<int *>(A + o_pos);
+        b->status = reinterpret_cast<int *>(A + o_st);
+        b->tokens = reinterpret_cast<int32_t *>(A + o_tok);
+        b->emitted = reinterpret_cast<uint32_t *>(A + o_em);
+        b->ctl = reinterpret_cast<BatchCtl *>(A + o_ctl);
+        b->rope_cos = reinterpret_cast<float *>(A + o_cos);
+        b->rope_sin = reinterpret_cast<float *>(A + o_sin);
+        check(cudaMemsetAsync(b->arena, 0, off, b->ls), "cudaMemsetAsync");
+        check(launch_rope_table(b->rope_cos, b->rope_sin, smax, c.head_dim, c.rope_theta, b->ls), "RoPE table");
+        check(cudaStreamSynchronize(b->ls), "cudaStreamSynchronize");
+    }
+    if (st) {
+        destroy_batch(b);
+        return st;
+    }
+    b->h_pos.assign(B, 0);
+    b->h_ready.assign(B, 0);
+    *out = b;
+    return QD_OK;
+}
+
+qd_status qd_batch_destroy(qd_batch_handle b) {
+    destroy_batch(b);
+    return QD_OK;
+}
+
+qd_status qd_batch_set_graphs(qd_batch_handle b, int enable) {
+    if (!b) return QD_EINVAL;
+    b->use_graphs = enable != 0;
+    return QD_OK;
+}
+
+qd_status qd_batch_set_stream(qd_batch_handle b, int stream, const void *kv_dev, int length, int32_t token) {
+    if (!b) return QD_EINVAL;
+    qd_model *m = b->m;
+    const qd_config &c = m->cfg;
+    if (stream < 0 || stream >= b->B) return fail(m, QD_EINVAL, "stream %d out of range", stream);
+    if (length < 0 || length >= b->S) return fail(m, QD_EINVAL, "length %d must be in [0, smax)", length);
+    if (length > 0 && !is_device_ptr(kv_dev)) return fail(m, QD_EINVAL, "kv_dev is not a device pointer");
+    if (token < 0 || token >= c.embed_rows) return fail(m, QD_EINVAL, "token %d outside the embedding table", token);
+    batch_enter(b);
+    const size_t row = (size_t)c.head_dim * 2;   // bytes of one position of one kv head
+    const int segs = c.n_layers * 2 * c.n_kv_heads;
+    uint8_t *dst = static_cast<uint8_t *>(b->kv) + (size_t)stream * b->stream_elems * 2;
+    if (length > 0)
+        CU(cudaMemcpy2DAsync(dst, (size_t)b->S * row, kv_dev, (size_t)length * row, (size_t)length * row, segs,
+                             cudaMemcpyDeviceToDevice, b->ls));
+    CU(cudaMemcpyAsync(b->pos + stream, &length, 4, cudaMemcpyHostToDevice, b->ls));
+    CU(cudaMemcpyAsync(b->tokens + stream, &token, 4, cudaMemcpyHostToDevice, b->ls));
+    CU(cudaMemsetAsync(b->emitted + (size_t)stream * b->words, 0, (size_t)b->words * 4, b->ls));
+    CU(cudaStreamSynchronize(b->ls));
+    batch_leave(b);
+    b->h_pos[stream] = length;
+    b->h_ready[stream] = 1;
+    return QD_OK;
+}
+
+qd_status qd_batch_decode(qd_batch_handle b, int n_steps, const int32_t *force_dev, int32_t *ids_dev) {
+    if (!b) return QD_EINVAL;
+    qd_model *m = b->m;
+    if (n_steps < 0) return fail(m, QD_EINVAL, "n_steps < 0");
+    if (n_steps == 0) return QD_OK;
+    if (!is_device_ptr(ids_dev)) return fail(m, QD_EINVAL, "ids_dev is not a device pointer");
+    if (force_dev && !is_device_ptr(force_dev)) return fail(m, QD_EINVAL, "force_dev is not a device pointer");
+    for (int i = 0; i < b->B; ++i) {
+        if (!b->h_ready[i]) return fail(m, QD_ESTATE, "stream %d has no cache and input token", i);
+        if (b->h_pos[i] + n_steps > b->S)
+            return fail(m, QD_EKVFULL, "stream %d: position %d + %d steps exceeds smax %d", i, b->h_pos[i], n_steps,
+                        b->S);
+    }
+    batch_enter(b);
+    BatchCtl h = {};
+    h.step = 0;
+    h.n_steps = n_steps;
+    h.force = force_dev;
+    h.ids = ids_dev;
+    h.done = 0;
+    CU(cudaMemcpyAsync(b->ctl, &h, sizeof(h), cudaMemcpyHostToDevice, b->ls));
+    for (int i = 0; i < n_steps; ++i) {
+        qd_status st = run_batch_step(b);
+        if (st) return st;
+        b->launches += b->kernels_per_step;
+    }
+    for (int i = 0; i < b->B; ++i) b->h_pos[i] += n_steps;
+    batch_leave(b);
+    return QD_OK;
+}
+
+// Synchronise and report device-side errors of the batch.
+qd_status qd_batch_sync(qd_batch_handle b) {
+    if (!b) return QD_EINVAL;
+    qd_model *m = b->m;
+    int status = 0;
+    CU(cudaMemcpyAsync(&status, b->status, 4, cudaMemcpyDeviceToHost, b->ls));
+    CU(cudaStreamSynchronize(b->ls));
+    if (status) return fail(m, QD_EDEVICE, "device error bits 0x%x", status);
+    return QD_OK;
+}
+
+qd_status qd_batch_get_logits(qd_batch_handle b, float *dst_dev) {
+    if (!b) return QD_EINVAL;
+    qd_model *m = b->m;
+    if (!is_device_ptr(dst_dev)) return fail(m, QD_EINVAL, "dst_dev is not a device pointer");
+    CU(cudaMemcpyAsync(dst_dev, b->logits, (size_t)b->B * m->cfg.vocab * 4, cudaMemcpyDeviceToDevice, b->ls));
+    CU(cudaStreamSynchronize(b->ls));
+    return QD_OK;
+}
+
+qd_status qd_batch_copy_kv(qd_batch_handle b, int stream, void *dst_dev, size_t *bytes) {
+    if (!b || !bytes) return QD_EINVAL;
+    qd_model *m = b->m;
+    if (stream < 0 || stream >= b->B) return fail(m, QD_EINVAL, "stream %d out of range", stream);
+    const size_t n = b->stream_elems * 2;
+    if (!dst_dev) {
+        *bytes = n;
+        return QD_OK;
+    }
+    if (*bytes < n || !is_device_ptr(dst_dev)) return fail(m, QD_EINVAL, "destination too small or not on the device");
+    CU(cudaMemcpyAsync(dst_dev, static_cast<uint8_t *>(b->kv) + (size_t)stream * n, n, cudaMemcpyDeviceToDevice,
+                       b->ls));
+    CU(cudaStreamSynchronize(b->ls));
+    *bytes = n;
+    return QD_OK;
+}
+
+qd_status qd_batch_get_pos(qd_batch_handle b, int stream, int *pos) {
+    if (!b || !pos || stream < 0 || stream >= b->B) return QD_EINVAL;
+    *pos = b->h_pos[stream];
+    return QD_OK;
+}
+
+qd_status qd_batch_get_launch_count(qd_batch_handle b, long long *kernels, int *kernels_per_step) {
+    if (!b) return QD_EINVAL;
+    if (kernels) *kernels = b->launches;
+    if (kernels_per_step) *kernels_per_step = b->kernels_per_step;
+    return QD_OK;
+}
+
+}  // extern "C"

@@ -1,6 +1,7 @@
 // Internal interface between the decode-step kernels and the engine (host C++).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -190,5 +191,112 @@ struct FrameArgs {                 // fixed for a frame generator (graphs captur
 cudaError_t launch_frame_cp_prefill(const FrameArgs &a, cudaStream_t s);
 cudaError_t launch_frame_cp_input(const FrameArgs &a, int j, cudaStream_t s);
 cudaError_t launch_frame_sum(const FrameArgs &a, cudaStream_t s);
+
+// ---------------------------------------------------------------------------------
+// Tensor-core GEMM (tcgen05 + TMA): out[t][r] = sum_k W[r][k] * x[t][k] for the
+// batched paths (prefill, multi-stream decode).  W [R, K] bf16 row-major; x is given
+// as two bf16 parts x = x_hi + x_lo ([T, K] row-major each), so the products carry
+// ~16 bits of the fp32 activation; accumulation is fp32 in tensor memory.
+// ---------------------------------------------------------------------------------
+enum TcEpilogue : int {
+    TC_STORE = 0,      // out[t][r] = acc
+    TC_RESIDUAL = 1,   // out[t][r] += acc
+    TC_SWIGLU = 2,     // rows (2i, 2i+1) = (gate_i, up_i): act[t][i] = silu(gate) * up,
+                       // written as bf16 hi/lo parts (and fp32 when out != null)
+};
+
+struct TcGemmArgs {
+    int R, K, T;                   // weight rows (multiple of 128), reduction (multiple of 64), tokens
+    int mode;                      // TcEpilogue
+    float *out;                    // [T][ldo] fp32 (TC_SWIGLU: optional fp32 act)
+    int ldo;
+    __nv_bfloat16 *act_hi, *act_lo;// TC_SWIGLU: [T][R/2]
+    float *partial;                // split-K partial sums [units][BN][128], or null when splits == 1
+    int *tile_counter;             // [row tiles x token tiles], zero at rest
+    int *status;                   // DEV_ERR_* bits
+};
+
+struct TcGemmPlan {
+    int bn;                        // token tile: 64 or 128
+    int row_tiles, tok_tiles, splits, units, grid;
+    size_t smem;
+    size_t partial_floats;         // scratch needed for split-K partials (floats)
+};
+
+// Resolve the tensor-map encoder and configure the kernels; call before any capture.
+cudaError_t tc_gemm_init();
+// Plan a GEMM of R x K over T tokens on `num_sms` SMs (split-K when the tiles alone
+// cannot fill the GPU).  False if the shape is not supported.
+bool tc_gemm_plan(int R, int K, int T, int num_sms, TcGemmPlan *p);
+// Launch; w, x_hi, x_lo are device pointers (16-byte aligned, row strides K*2 bytes).
+cudaError_t launch_tc_gemm(const TcGemmPlan &p, const void *w, const void *x_hi, const void *x_lo,
+                           const TcGemmArgs &a, cudaStream_t s);
+// x fp32 [n] -> hi = bf16(x), lo = bf16(x - hi)
+cudaError_t launch_split_bf16(const float *x, __nv_bfloat16 *hi, __nv_bfloat16 *lo, size_t n, cudaStream_t s);
+
+// ---------------------------------------------------------------------------------
+// Batched decode: B independent streams, one token each per step.
+// ---------------------------------------------------------------------------------
+struct BatchCtl {                  // device; written by the host once per call
+    int step;                      // step index within the call, advanced by the argmax kernel
+    int n_steps;
+    const int32_t *force;          // [n_steps][B] ids fed back instead of the argmax, or null
+    int32_t *ids;                  // [n_steps][B] argmax ids
+    int done;                      // CTAs of the argmax kernel finished in this step
+};
+
+struct BatchAttnArgs {
+    const float *qkv;              // [B][qkv_ld]: q heads, then k, then v of each stream
+    int qkv_ld;
+    const float *q_gamma, *k_gamma;// [hd] or null
+    float eps, scale;
+    const float *rope_cos, *rope_sin;
+    void *kv;                      // [B][n_layers][2][kvh][S][hd] bf16
+    size_t stream_elems;           // elements of one stream's cache
+    size_t layer_elems;            // offset of this layer within a stream (elements)
+    int S, qh, kvh, chunk_max;
+    const int *pos;                // [B] position written by this step (attended length pos + 1)
+    __nv_bfloat16 *out_hi, *out_lo;// [B][qh * hd] attention output as bf16 parts
+    int *status;
+};
+
+size_t batch_attention_smem_bytes(int hd, int group, int chunk_max);
+cudaError_t batch_kernels_init();   // call before any capture
+cudaError_t launch_batch_attention(int hd, int B, const BatchAttnArgs &a, cudaStream_t s);
+
+// Per row b < rows: optionally x[b] = E[tokens[b]] (the token joins stream b's emitted
+// set), then hi/lo bf16 parts of gamma * x[b] / sqrt(mean(x[b]^2) + eps).
+struct NormSplitArgs {
+    float *x;                      // [rows][K]
+    int K;
+    const float *gamma;
+    float eps;
+    __nv_bfloat16 *hi, *lo;        // [rows][K]
+    const void *table;             // embedding table (bf16) or null: no gather
+    int table_rows;
+    const int32_t *tokens;         // [rows]
+    uint32_t *emitted;             // [rows][emitted_words]
+    int emitted_words, vocab;
+    float *y;                      // optional fp32 copy of the normalised rows
+    int *status;
+};
+cudaError_t launch_norm_split(const NormSplitArgs &a, int rows, cudaStream_t s);
+
+// Per stream b: penalty over its emitted set, EOS mask, argmax (lowest index on ties)
+// of logits[b]; ids and the next input token go through the control block; the
+// stream's position advances.
+struct BatchArgmaxArgs {
+    const float *logits;           // [B][V]
+    int V;
+    const uint32_t *emitted;       // [B][words]
+    int words;
+    float penalty;
+    int eos;
+    BatchCtl *ctl;
+    int32_t *tokens;               // [B] next input tokens
+    int *pos;                      // [B]
+    int *status;
+};
+cudaError_t launch_batch_argmax(const BatchArgmaxArgs &a, int B, cudaStream_t s);
 
 }  // namespace qd

@@ -1,0 +1,463 @@
+// Tensor-core GEMM for the batched paths: prefill (thousands of tokens) and the
+// multi-stream decode (one token per stream), where the projections and the MLP are
+// real dense contractions.
+//
+//   out[t][r] = sum_k W[r][k] * x[t][k],   W [R, K] bf16,   x = x_hi + x_lo (bf16 parts)
+//
+// Blackwell path (sm_103a): TMA tiled loads with the 128-byte swizzle into a ring of
+// shared-memory stages, tcgen05.mma (kind::f16, bf16 inputs, fp32 accumulation) issued
+// by one thread with the accumulator in tensor memory, tcgen05.ld for the epilogue.
+// The weight tile is the MMA's A operand (M = 128 weight rows), the token tile the B
+// operand (N = 64 or 128 tokens); both are K-major, as the row-major matrices are.
+// Every k-step issues two MMAs on the same weight tile, one per activation part, so the
+// products keep ~16 bits of the fp32 activation (x_lo holds the rounding residue of
+// x_hi) while the weights stay bf16.
+//
+// Roles (192 threads): warp 0 lane 0 issues the TMA loads, warp 1 owns the tensor
+// memory and lane 0 issues the MMAs, warps 2-5 read the accumulator (each warp may
+// only touch its quarter of the 128 lanes: warp w reads lanes 32*(w%4)..+31) and run
+// the epilogue.  Two accumulators alternate so a tile's epilogue overlaps the next
+// tile's MMAs.  When the tiles alone cannot fill the GPU (decode: 64 tokens) the K
+// range is split over several CTAs; each writes its partial tile to scratch and the
+// last CTA of a tile (completion counter) sums the partials in split order and runs
+// the epilogue, so the result does not depend on timing.
+//
+// Every wait is bounded (1 s on %globaltimer); on expiry the kernel records
+// DEV_ERR_WAIT_TIMEOUT, every role stops, copies and MMAs in flight are drained, the
+// tensor memory is freed and the kernel returns.
+#include <cuda.h>
+
+#include <mutex>
+
+#include "qd_device.cuh"
+#include "qd_internal.h"
+
+namespace qd {
+
+namespace {
+
+constexpr int kTcThreads = 192;
+constexpr int kBM = 128;                       // weight rows per tile (MMA M)
+constexpr int kBK = 64;                        // K per stage: one 128-byte swizzle row of bf16
+constexpr uint32_t kTileA = kBM * kBK * 2;     // 16 KB
+constexpr unsigned long long kDrainNs = 20000000ull;   // 20 ms for clean-up waits
+
+template <int BN> struct TcCfg {
+    static constexpr uint32_t kTileB = BN * kBK * 2;
+    static constexpr uint32_t kStage = kTileA + 2 * kTileB;
+    static constexpr int kStages = BN == 64 ? 6 : 4;
+    static constexpr uint32_t kTmemCols = 2 * BN;   // two accumulators of BN fp32 columns
+    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + 256;
+};
+
+// ---- PTX wrappers (tensor memory, MMA, TMA)
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(slot)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D (tensor memory) (+)= A * B^T, A/B described by shared-memory descriptors.
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+        : "memory");
+}
+// Arrive on `bar` once every MMA issued so far by this thread has completed.
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+// 16 consecutive fp32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float *v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+// 2-D tiled TMA load of box (c0 = k element offset, c1 = row) into shared memory.
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile written by TMA with the 128-byte
+// swizzle: rows of 128 bytes, 8-row swizzle atoms of 1024 bytes (stride byte offset),
+// leading byte offset unused for this layout, descriptor version 1, layout 2 = 128B.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major,
+// N >> 3 at bit 17, M >> 4 at bit 24.
+template <int BN> __device__ __forceinline__ constexpr uint32_t tc_idesc() {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+}
+
+// Bounded wait that also gives up when another role has aborted.
+__device__ __forceinline__ bool role_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicOr(status, DEV_ERR_WAIT_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+struct Unit {
+    int tile, rt, nt, k0, k1;
+};
+__device__ __forceinline__ Unit unit_of(int u, int splits, int tok_tiles, int KC) {
+    Unit x;
+    x.tile = u / splits;
+    const int s = u - x.tile * splits;
+    x.rt = x.tile / tok_tiles;
+    x.nt = x.tile - x.rt * tok_tiles;
+    x.k0 = (int)((long long)s * KC / splits);
+    x.k1 = (int)((long long)(s + 1) * KC / splits);
+    return x;
+}
+
+// Epilogue of one output element: token t, weight row r (rows of a warp are
+// consecutive lanes; the SwiGLU pairing uses the neighbouring lane, so every lane of
+// the warp must call this together).
+__device__ __forceinline__ void epi_apply(const TcGemmArgs &a, int t, int r, float v, int lane) {
+    if (a.mode == TC_STORE) {
+        a.out[(size_t)t * a.ldo + r] = v;
+    } else if (a.mode == TC_RESIDUAL) {
+        float *p = a.out + (size_t)t * a.ldo + r;
+        *p = *p + v;
+    } else {
+        const float u = __shfl_down_sync(0xffffffffu, v, 1);
+        if ((lane & 1) == 0) {
+            const float act = v / (1.0f + expf(-v)) * u;
+            const __nv_bfloat16 hi = __float2bfloat16_rn(act);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(act - __bfloat162float(hi));
+            const size_t o = (size_t)t * (a.R / 2) + (r >> 1);
+            a.act_hi[o] = hi;
+            a.act_lo[o] = lo;
+            if (a.out) a.out[(size_t)t * a.ldo + (r >> 1)] = act;
+        }
+    }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_xh,
+                   const __grid_constant__ CUtensorMap tm_xl, const TcGemmArgs a, const int tok_tiles,
+                   const int splits, const int units) {
+    using C = TcCfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm + (size_t)C::kStages * C::kStage);
+    uint64_t *empty = full + C::kStages;
+    uint64_t *acc_full = empty + C::kStages;   // [2]
+    uint64_t *acc_empty = acc_full + 2;        // [2]
+    uint64_t *drain = acc_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *is_last = reinterpret_cast<int *>(tmem_slot + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int KC = a.K / kBK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 4);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---- TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t armed = 0, armed_parity = 0;   // per-stage bits: armed at least once / parity of last arming
+            for (int u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
+                const Unit x = unit_of(u, splits, tok_tiles, KC);
+                bool ok = true;
+                for (int kc = x.k0; kc < x.k1; ++kc) {
+                    if (!role_wait(&empty[stage], phase ^ 1, abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], C::kStage);
+                    uint8_t *st = sm + (size_t)stage * C::kStage;
+                    tma_load_2d(st, &tm_w, kc * kBK, x.rt * kBM, &full[stage]);
+                    tma_load_2d(st + kTileA, &tm_xh, kc * kBK, x.nt * BN, &full[stage]);
+                    tma_load_2d(st + kTileA + C::kTileB, &tm_xl, kc * kBK, x.nt * BN, &full[stage]);
+                    armed |= 1u << stage;
+                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == C::kStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+            }
+            if (*abort_flag) {
+                // let every copy this thread issued land before the CTA exits
+                for (int s = 0; s < C::kStages; ++s)
+                    if (armed >> s & 1) mbar_wait_bounded(&full[s], armed_parity >> s & 1, kDrainNs);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---- MMA issuer
+            constexpr uint32_t idesc = tc_idesc<BN>();
+            int stage = 0;
+            uint32_t phase = 0;
+            int local = 0;
+            for (int u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x, ++local) {
+                const Unit x = unit_of(u, splits, tok_tiles, KC);
+                const int acc = local & 1;
+                const uint32_t use = (uint32_t)(local >> 1);
+                if (!role_wait(&acc_empty[acc], (use & 1) ^ 1, abort_flag, a.status)) break;
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(acc * BN);
+                bool ok = true;
+                for (int kc = x.k0; kc < x.k1; ++kc) {
+                    if (!role_wait(&full[stage], phase, abort_flag, a.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_addr(sm + (size_t)stage * C::kStage);
+                    const uint32_t sh = sa + kTileA, sl = sh + C::kTileB;
+#pragma unroll
+                    for (int k = 0; k < kBK / 16; ++k) {
+                        const uint64_t ad = sw128_desc(sa + 32u * k);
+                        tc_mma(d, ad, sw128_desc(sh + 32u * k), idesc, (kc > x.k0 || k > 0) ? 1u : 0u);
+                        tc_mma(d, ad, sw128_desc(sl + 32u * k), idesc, 1u);
+                    }
+                    tc_commit(&empty[stage]);   // the stage is free once these MMAs have read it
+                    if (++stage == C::kStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(&acc_full[acc]);
+            }
+            // every MMA issued has completed before the tensor memory is released
+            tc_commit(drain);
+            mbar_wait_bounded(drain, 0, kDrainNs);
+        }
+    } else {
+        // ---- epilogue warps 2..5
+        const int q = warp & 3;                 // tensor-memory lane quarter of this warp
+        const int row_in_tile = q * 32 + lane;
+        int local = 0;
+        for (int u = blockIdx.x; u < units; u += gridDim.x, ++local) {
+            const Unit x = unit_of(u, splits, tok_tiles, KC);
+            const int acc = local & 1;
+            const uint32_t use = (uint32_t)(local >> 1);
+            bool ok = true;
+            if (lane == 0) ok = role_wait(&acc_full[acc], use & 1, abort_flag, a.status);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            // all four epilogue warps agree before any of them goes on
+            if (named_sync_or(1, 128, !ok)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+            const int r = x.rt * kBM + row_in_tile;
+            if (splits == 1) {
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN; c0 += 16) {
+                    float v[16];
+                    tc_ld16(tbase + (uint32_t)c0, v);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int t = x.nt * BN + c0 + j;
+                        if (t < a.T) epi_apply(a, t, r, v[j], lane);
+                    }
+                }
+            } else {
+                float *part = a.partial + (size_t)u * BN * kBM;
+#pragma unroll 1
+                for (int c0 = 0; c0 < BN; c0 += 16) {
+                    float v[16];
+                    tc_ld16(tbase + (uint32_t)c0, v);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) __stcg(part + (size_t)(c0 + j) * kBM + row_in_tile, v[j]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[acc]);
+            if (splits > 1) {
+                __threadfence();
+                named_sync(1, 128);
+                if (warp == 2 && lane == 0) {
+                    const int old = atomicAdd(&a.tile_counter[x.tile], 1);
+                    const int last = old == splits - 1;
+                    if (last) a.tile_counter[x.tile] = 0;   // at rest for the next launch
+                    *is_last = last;
+                }
+                named_sync(1, 128);
+                if (*is_last) {
+                    __threadfence();
+                    const float *p0 = a.partial + (size_t)x.tile * splits * BN * kBM;
+#pragma unroll 1
+                    for (int c = 0; c < BN; ++c) {
+                        const int t = x.nt * BN + c;
+                        if (t >= a.T) break;
+                        float v = 0.f;
+                        for (int s = 0; s < splits; ++s) v += __ldcg(p0 + ((size_t)s * BN + c) * kBM + row_in_tile);
+                        epi_apply(a, t, r, v, lane);
+                    }
+                }
+                named_sync(1, 128);   // is_last is reused by the next unit
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+__global__ void split_bf16_kernel(const float *x, __nv_bfloat16 *hi, __nv_bfloat16 *lo, size_t n) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const float v = x[i];
+        const __nv_bfloat16 h = __float2bfloat16_rn(v);
+        hi[i] = h;
+        lo[i] = __float2bfloat16_rn(v - __bfloat162float(h));
+    }
+}
+
+// ---- host side: tensor maps through the driver entry point (no libcuda link)
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// bf16 [rows, K] row-major, box of 64 elements (128 bytes, the swizzle span) x box_rows.
+bool make_map(CUtensorMap *m, const void *ptr, int rows, int K, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || (reinterpret_cast<uintptr_t>(ptr) & 15)) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN> cudaError_t set_attr() {
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(reinterpret_cast<const void *>(tc_gemm_kernel<BN>),
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TcCfg<BN>::kSmem);
+    });
+    return attr;
+}
+
+template <int BN> cudaError_t launch_bn(const TcGemmPlan &p, const void *w, const void *xh, const void *xl,
+                                        const TcGemmArgs &a, cudaStream_t s) {
+    cudaError_t attr = set_attr<BN>();
+    if (attr != cudaSuccess) return attr;
+    CUtensorMap mw, mh, ml;
+    if (!make_map(&mw, w, a.R, a.K, kBM) || !make_map(&mh, xh, a.T, a.K, BN) || !make_map(&ml, xl, a.T, a.K, BN))
+        return cudaErrorInvalidValue;
+    tc_gemm_kernel<BN><<<p.grid, kTcThreads, TcCfg<BN>::kSmem, s>>>(mw, mh, ml, a, p.tok_tiles, p.splits, p.units);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t tc_gemm_init() {
+    if (!encode_fn()) return cudaErrorNotSupported;
+    cudaError_t e = set_attr<64>();
+    return e != cudaSuccess ? e : set_attr<128>();
+}
+
+bool tc_gemm_plan(int R, int K, int T, int num_sms, TcGemmPlan *p) {
+    if (R <= 0 || K <= 0 || T <= 0 || R % kBM || K % kBK || num_sms <= 0) return false;
+    TcGemmPlan q = {};
+    q.bn = T <= 64 ? 64 : 128;
+    q.row_tiles = R / kBM;
+    q.tok_tiles = (T + q.bn - 1) / q.bn;
+    const int tiles = q.row_tiles * q.tok_tiles;
+    const int KC = K / kBK;
+    q.splits = 1;
+    if (tiles < num_sms) q.splits = std::max(1, std::min(KC, num_sms / tiles));
+    q.units = tiles * q.splits;
+    q.grid = std::min(q.units, num_sms);
+    q.smem = q.bn == 64 ? TcCfg<64>::kSmem : TcCfg<128>::kSmem;
+    q.partial_floats = q.splits > 1 ? (size_t)q.units * q.bn * kBM : 0;
+    *p = q;
+    return true;
+}
+
+cudaError_t launch_tc_gemm(const TcGemmPlan &p, const void *w, const void *x_hi, const void *x_lo,
+                           const TcGemmArgs &a, cudaStream_t s) {
+    if (p.splits > 1 && (!a.partial || !a.tile_counter)) return cudaErrorInvalidValue;
+    if (a.mode == TC_SWIGLU && (!a.act_hi || !a.act_lo)) return cudaErrorInvalidValue;
+    return p.bn == 64 ? launch_bn<64>(p, w, x_hi, x_lo, a, s) : launch_bn<128>(p, w, x_hi, x_lo, a, s);
+}
+
+cudaError_t launch_split_bf16(const float *x, __nv_bfloat16 *hi, __nv_bfloat16 *lo, size_t n, cudaStream_t s) {
+    const int grid = (int)std::min<size_t>((n + 255) / 256, 4096);
+    split_bf16_kernel<<<grid, 256, 0, s>>>(x, hi, lo, n);
+    return cudaGetLastError();
+}
+
+}  // namespace qd
