@@ -570,24 +570,248 @@ def frames_arm(args):
         torch.distributed.destroy_process_group()
 
 
+# ------------------------------------------------------------------------------ batched workload
+
+BATCH_DESC = ("batched multi-stream decode: 64 independent streams of the 28-layer Talker (hidden 1024, 16q/8kv "
+              "heads x 128, QK-norm, FFN 3072, vocab 3072, repetition penalty 1.05), each with its own bf16 cache "
+              "(smax 2048) filled with N(0,1) K/V to a seeded length U{256..1792} and a seeded first token; 256 "
+              "greedy steps per stream; projections, MLP and head as tcgen05 GEMMs over the 64 streams")
+
+
+def run_oracle_batch_stream(max_steps: int, budget_s: float = 20.0):
+    """The oracle decoding one stream of the batched workload (stream 0: its cache and
+    first token), up to max_steps or budget_s seconds; stream-tokens/s."""
+    import oracle as O
+    import workloads as W
+    s = W.TALKER
+    L0 = int(W.batch_initial_lengths()[0])
+    o = O.Oracle(s, W.model_weights(s), buckets=(W.BATCH_SMAX,))
+    o.set_kv(W.batch_stream_kv(s, 0, L0), L0)
+    tok = int(W.batch_first_tokens(W.BATCH_STREAMS, s.vocab)[0])
+    n = 0
+    t0 = time.perf_counter()
+    while n < max_steps:
+        tok, _, _, _ = o.step(token=tok, want_logits=False)
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    o.close()
+    return n / dt, n, dt, O.num_threads(), L0
+
+
+def batch_reference_arm(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    run_oracle_batch_stream(1, budget_s=5.0)
+    tps, n, dt, cores, L0 = run_oracle_batch_stream(args.steps, budget_s=60.0)
+    sample = f"stream 0 of the batched workload (cache length {L0}), {n} greedy steps ({dt:.1f} s)"
+    line = {"impl": "reference", "metric": METRIC, "value": tps, "unit": "stream-tokens/s", "n_gpus": ws,
+            "steps": n, "warmup": args.warmup, "ms_per_step": 1e3 * dt / max(n, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": BATCH_DESC},
+            "cpu_baseline": {"value": tps, "unit": "stream-tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": tps, "unit": "stream-tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def batch_arm(args):
+    import numpy as np
+    import torch
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.cuda.current_device()
+
+    import workloads as W
+    import __graft_entry__
+    __graft_entry__.build_library()
+    import transformer_autoregressive_decode_gb300 as qd
+    from transformer_autoregressive_decode_gb300.torch_io import config_from_shape, to_device, upload
+
+    s = W.TALKER
+    if args.layers:
+        # profiling case only: the same streams, lengths and per-layer kernels, fewer layers
+        s = W.scaled(W.TALKER, n_layers=args.layers, name=f"talker{args.layers}")
+    B, smax, traj = W.BATCH_STREAMS, W.BATCH_SMAX, W.BATCH_STEPS
+    hbm_peak, bf16_peak, peak_src = _peaks()
+    h = qd.qd_create(upload(W.model_weights(s)), config_from_shape(s))
+    bh = qd.qd_batch_create(h, B, smax)
+    lens = [int(v) for v in W.batch_initial_lengths()]
+    toks = [int(v) for v in W.batch_first_tokens(B, s.vocab)]
+    kv_dev = [to_device(W.batch_stream_kv(s, b, lens[b])) for b in range(B)]   # kept for restarts
+    ids = torch.empty((traj, B), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def restart():
+        for b in range(B):
+            qd.qd_batch_set_stream(bh, b, kv_dev[b], lens[b], toks[b])
+        steps.pos = 0
+
+    def steps(n):
+        """n batched steps; a trajectory is 256 steps from the initial caches."""
+        done = 0
+        while done < n:
+            if steps.pos >= traj:
+                restart()
+            k = min(n - done, traj - steps.pos)
+            qd.qd_batch_decode(bh, k, ids[steps.pos:steps.pos + k])
+            steps.pos += k
+            done += k
+
+    restart()
+    W_ = max(3, args.warmup)
+    steps(W_)
+    qd.qd_batch_sync(bh)
+
+    # per-kernel times at the start of a trajectory (positions = the initial lengths)
+    restart()
+    kms = {name: qd.qd_batch_time_kernel(bh, which, 10) for name, which in (
+        ("attention", qd.BATCH_ATTENTION), ("qkv", qd.BATCH_QKV), ("oproj", qd.BATCH_OPROJ),
+        ("gate_up", qd.BATCH_GATE_UP), ("down", qd.BATCH_DOWN), ("head", qd.BATCH_HEAD))}
+    restart()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    k0, per_step = qd.qd_batch_get_launch_count(bh)
+    clocks = Clocks(dev if ws == 1 else local)
+    barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    steps(args.steps)
+    ev1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    qd.qd_batch_sync(bh)
+    ms = ev0.elapsed_time(ev1)
+    k1, _ = qd.qd_batch_get_launch_count(bh)
+    if ws > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = ws * B * args.steps / (ms / 1e3)
+    step_ms = ms / args.steps
+
+    # algorithmic bytes: weights once per step + every stream's K/V over its attended
+    # length (mean over a trajectory)
+    kv_pos = s.kv_bytes_per_position()
+    mean_L = sum(L + (traj + 1) / 2 for L in lens) / B
+    step_bytes = s.weight_bytes_per_step() + B * mean_L * kv_pos
+    step_gbs = step_bytes / (step_ms / 1e3) / 1e9
+    # dominant kernel: attention of one layer, at the initial lengths (L = L0 + 1)
+    att_bytes = sum(L + 1 for L in lens) * kv_pos / s.n_layers
+    att_gbs = att_bytes / (kms["attention"] / 1e3) / 1e9
+    # the GEMMs: useful flops per step and their summed kernel time
+    layer_params = s.layer_matrix_params()
+    gemm_ms = s.n_layers * (kms["qkv"] + kms["oproj"] + kms["gate_up"] + kms["down"]) + kms["head"]
+    gemm_flops = 2.0 * B * (s.n_layers * layer_params + s.vocab * s.hidden)
+    gemm_tflops = gemm_flops / (gemm_ms / 1e3) / 1e12
+    gemm_bytes = s.weight_bytes_per_step()
+
+    # end to end: every step the 64 input tokens come from pinned host memory and the
+    # 64 ids go back to it (the ids of a step are the next step's tokens)
+    restart()
+    n_e2e = min(args.steps, 64)
+    tok_h = torch.tensor(toks, dtype=torch.int32).pin_memory()
+    ids_h = torch.empty(B, dtype=torch.int32).pin_memory()
+    force = torch.empty((1, B), dtype=torch.int32, device="cuda")
+    one = torch.empty((1, B), dtype=torch.int32, device="cuda")
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        force[0].copy_(tok_h, non_blocking=True)
+        qd.qd_batch_decode(bh, 1, one, force)
+        ids_h.copy_(one[0], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        tok_h.copy_(ids_h)
+    e2e_s = time.perf_counter() - t0
+    e2e = {"value": ws * B * n_e2e / e2e_s, "unit": "stream-tokens/s", "h2d_bytes_per_step": 4 * B,
+           "d2h_bytes_per_step": 4 * B, "steps": n_e2e,
+           "api": "qd_batch_decode one step per call, tokens in from and ids out to pinned host memory"}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        tps, n, dt, cores, L0 = run_oracle_batch_stream(traj, budget_s=20.0)
+        cpu = {"value": tps, "unit": "stream-tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"stream 0 (cache length {L0}), {n} greedy steps ({dt:.1f} s)"}
+
+    qd.qd_batch_destroy(bh)
+    qd.qd_destroy(h)
+    del kv_dev
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "stream-tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": W_, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic: seeded N(0,0.02) bf16 weights, 1+N(0,0.1) gammas, N(0,1) bf16 initial caches",
+        "config": {"workload": BATCH_DESC if not args.layers else
+                   f"PROFILING CASE, not the workload: {args.layers}-layer variant of: " + BATCH_DESC,
+                   "storage": "bf16 weights and caches; activations fp32, entering the "
+                                                      "GEMMs as bf16 hi + lo parts; fp32 accumulation",
+                   "timed": f"{args.steps} batched steps (each 64 stream-tokens) from the initial caches",
+                   "l2": f"inputs larger than L2: {step_bytes / 1e9:.2f} GB per step",
+                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": att_gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": att_gbs / hbm_peak, "traffic": None,
+                     "traffic_note": "no ncu capture for this workload and kernel build",
+                     "kernel": "batch_attn_kernel: one layer's attention of all 64 streams over their caches "
+                               "(QK-norm, RoPE, KV append, 8-way split, cluster merge)",
+                     "bytes_per_launch": att_bytes, "avg_launch_ms": kms["attention"], "peak_source": peak_src,
+                     "timing": "CUDA events around 10 graph-captured launches at the initial lengths"},
+        "step_hbm": {"bytes_per_step": step_bytes, "step_ms": step_ms, "achieved_gbs": step_gbs,
+                     "frac": step_gbs / hbm_peak, "peak_source": peak_src,
+                     "note": f"weights {s.weight_bytes_per_step() / 1e9:.3f} GB + K/V of every stream at the "
+                             f"trajectory's mean attended length {mean_L:.0f}"},
+        "gemm": {"kernel_ms": {k: v for k, v in kms.items() if k != "attention"},
+                 "per_step_ms": gemm_ms, "useful_tflops": gemm_tflops,
+                 "tensor_frac_useful": gemm_tflops / bf16_peak, "bf16_peak_tflops": bf16_peak,
+                 "weight_gbs": gemm_bytes / (gemm_ms / 1e3) / 1e9,
+                 "note": "useful flops 2 x 64 x weights per step; the hi/lo activation split issues two MMAs per "
+                         "useful one; at 64 streams the GEMMs stream their weights (HBM-bound)"},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(k1 - k0), "kernels_per_step": per_step,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=29000)
     ap.add_argument("--warmup", type=int, default=870)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="asr", choices=["asr", "talker", "tiny", "frames"])
+    ap.add_argument("--workload", default="asr", choices=["asr", "talker", "tiny", "frames", "batch"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="batch workload only: run a variant with this many layers (a profiling case)")
     args = ap.parse_args()
     if args.workload == "frames":
         if args.steps == ap.get_default("steps"):
             args.steps = 4 * FRAME_TRAJ
         if args.warmup == ap.get_default("warmup"):
             args.warmup = FRAME_TRAJ
-    if args.impl == "reference":
-        (frames_reference_arm if args.workload == "frames" else reference_arm)(args)
-    else:
-        (frames_arm if args.workload == "frames" else gpu_arm)(args)
+    if args.workload == "batch":
+        if args.steps == ap.get_default("steps"):
+            args.steps = 256
+        if args.warmup == ap.get_default("warmup"):
+            args.warmup = 8
+    ref = {"frames": frames_reference_arm, "batch": batch_reference_arm}.get(args.workload, reference_arm)
+    ours = {"frames": frames_arm, "batch": batch_arm}.get(args.workload, gpu_arm)
+    (ref if args.impl == "reference" else ours)(args)
 
 
 if __name__ == "__main__":

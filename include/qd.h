@@ -362,6 +362,14 @@ qd_status qd_batch_get_launch_count(qd_batch_handle b, long long *kernels, int *
 /* Turn the per-step CUDA graph on (default) or off; results are identical. */
 qd_status qd_batch_set_graphs(qd_batch_handle b, int enable);
 
+/* Time `reps` back-to-back launches of one kernel of the step with the step's
+ * arguments (captured in a graph; CUDA events on the batch's stream): 1 = attention
+ * of the last layer at the streams' current positions (it rewrites the rows the next
+ * step writes again), 2 = QKV GEMM, 3 = output-projection GEMM, 4 = gate/up GEMM,
+ * 5 = down GEMM of layer 0, 6 = head GEMM.  Between steps only; they change only
+ * step scratch.  Synchronises. */
+qd_status qd_batch_time_kernel(qd_batch_handle b, int which, int reps, float *avg_ms);
+
 #ifdef __cplusplus
 }
 #endif

@@ -40,10 +40,10 @@ qd_status qd_gemm_bf16(const void *w_dev, const float *x_dev, float *out_dev, in
     const size_t nx = (size_t)T * K;
     DevBuf xh, xl, part, cnt, st, ah, al;
     if (xh.alloc(nx * 2) || xl.alloc(nx * 2) || part.alloc(plan.partial_floats * 4) ||
-        cnt.alloc((size_t)plan.row_tiles * plan.tok_tiles * 4) || st.alloc(4) ||
+        cnt.alloc((size_t)plan.row_tiles * plan.tok_tiles * 8) || st.alloc(4) ||
         ah.alloc((size_t)T * (R / 2) * 2) || al.alloc((size_t)T * (R / 2) * 2))
         return QD_ENOMEM;
-    if (cudaMemsetAsync(cnt.p, 0, (size_t)plan.row_tiles * plan.tok_tiles * 4, s) ||
+    if (cudaMemsetAsync(cnt.p, 0, (size_t)plan.row_tiles * plan.tok_tiles * 8, s) ||
         cudaMemsetAsync(st.p, 0, 4, s))
         return QD_ECUDA;
     if (launch_split_bf16(x_dev, static_cast<__nv_bfloat16 *>(xh.p), static_cast<__nv_bfloat16 *>(xl.p), nx, s))
@@ -128,29 +128,58 @@ constexpr size_t kAlign = 256;
 
 qd_status batch_fail(qd_batch *b, qd_status st, const char *what) { return fail(b->m, st, "%s", what); }
 
+// One tensor-core GEMM of the step over the B streams.
+cudaError_t batch_gemm(qd_batch *b, const TcGemmPlan &p, const void *w, const __nv_bfloat16 *xh,
+                       const __nv_bfloat16 *xl, int R, int K, int mode, float *out, int ldo, cudaStream_t s) {
+    TcGemmArgs a = {};
+    a.R = R;
+    a.K = K;
+    a.T = b->B;
+    a.mode = mode;
+    a.out = out;
+    a.ldo = ldo;
+    a.act_hi = b->ah;
+    a.act_lo = b->al;
+    a.partial = p.splits > 1 ? b->partial : nullptr;
+    a.tile_counter = b->counters;
+    a.status = b->status;
+    return launch_tc_gemm(p, w, xh, xl, a, s);
+}
+
+// Attention arguments of layer l (output: the bf16 parts feeding the O GEMM).
+BatchAttnArgs batch_attn_args(qd_batch *b, int l) {
+    const qd_model *m = b->m;
+    const qd_config &c = m->cfg;
+    const Layer &L = m->layers[l];
+    BatchAttnArgs at = {};
+    at.qkv = b->qkv;
+    at.qkv_ld = m->q_dim() + 2 * m->kv_dim();
+    at.q_gamma = c.qk_norm ? L.q_norm : nullptr;
+    at.k_gamma = c.qk_norm ? L.k_norm : nullptr;
+    at.eps = (float)c.rms_eps;
+    at.scale = (float)(1.0 / std::sqrt((double)c.head_dim));
+    at.rope_cos = b->rope_cos;
+    at.rope_sin = b->rope_sin;
+    at.kv = b->kv;
+    at.stream_elems = b->stream_elems;
+    at.layer_elems = (size_t)l * 2 * c.n_kv_heads * b->S * c.head_dim;
+    at.S = b->S;
+    at.qh = c.n_q_heads;
+    at.kvh = c.n_kv_heads;
+    at.chunk_max = b->chunk_max;
+    at.pos = b->pos;
+    at.out_hi = b->xh;
+    at.out_lo = b->xl;
+    at.status = b->status;
+    return at;
+}
+
 // Every launch of one step, on stream s.
 qd_status enqueue_batch_step(qd_batch *b, cudaStream_t s) {
     qd_model *m = b->m;
     const qd_config &c = m->cfg;
     const int B = b->B, h = c.hidden, qd_ = m->q_dim(), rows_qkv = qd_ + 2 * m->kv_dim();
     int n = 0;
-    auto gemm = [&](const TcGemmPlan &p, const void *w, const __nv_bfloat16 *xh, const __nv_bfloat16 *xl, int R,
-                    int K, int mode, float *out, int ldo) -> cudaError_t {
-        TcGemmArgs a = {};
-        a.R = R;
-        a.K = K;
-        a.T = B;
-        a.mode = mode;
-        a.out = out;
-        a.ldo = ldo;
-        a.act_hi = b->ah;
-        a.act_lo = b->al;
-        a.partial = p.splits > 1 ? b->partial : nullptr;
-        a.tile_counter = b->counters;
-        a.status = b->status;
-        ++n;
-        return launch_tc_gemm(p, w, xh, xl, a, s);
-    };
     auto norm = [&](const float *gamma, bool gather) -> cudaError_t {
         NormSplitArgs a = {};
         a.x = b->x;
@@ -171,33 +200,19 @@ qd_status enqueue_batch_step(qd_batch *b, cudaStream_t s) {
         ++n;
         return launch_norm_split(a, B, s);
     };
+    auto gemm = [&](const TcGemmPlan &p, const void *w, const __nv_bfloat16 *xh, const __nv_bfloat16 *xl, int R,
+                    int K, int mode, float *out, int ldo) -> cudaError_t {
+        ++n;
+        return batch_gemm(b, p, w, xh, xl, R, K, mode, out, ldo, s);
+    };
     if (norm(m->layers[0].attn_norm, true)) return batch_fail(b, QD_ECUDA, "norm/embedding launch failed");
     for (int l = 0; l < c.n_layers; ++l) {
         const Layer &L = m->layers[l];
         if (gemm(b->p_qkv, L.w_qkv, b->xh, b->xl, rows_qkv, h, TC_STORE, b->qkv, rows_qkv))
             return batch_fail(b, QD_ECUDA, "QKV GEMM launch failed");
-        BatchAttnArgs at = {};
-        at.qkv = b->qkv;
-        at.qkv_ld = rows_qkv;
-        at.q_gamma = c.qk_norm ? L.q_norm : nullptr;
-        at.k_gamma = c.qk_norm ? L.k_norm : nullptr;
-        at.eps = (float)c.rms_eps;
-        at.scale = (float)(1.0 / std::sqrt((double)c.head_dim));
-        at.rope_cos = b->rope_cos;
-        at.rope_sin = b->rope_sin;
-        at.kv = b->kv;
-        at.stream_elems = b->stream_elems;
-        at.layer_elems = (size_t)l * 2 * c.n_kv_heads * b->S * c.head_dim;
-        at.S = b->S;
-        at.qh = c.n_q_heads;
-        at.kvh = c.n_kv_heads;
-        at.chunk_max = b->chunk_max;
-        at.pos = b->pos;
-        at.out_hi = b->xh;
-        at.out_lo = b->xl;
-        at.status = b->status;
         ++n;
-        if (launch_batch_attention(c.head_dim, B, at, s)) return batch_fail(b, QD_ECUDA, "attention launch failed");
+        if (launch_batch_attention(c.head_dim, B, batch_attn_args(b, l), s))
+            return batch_fail(b, QD_ECUDA, "attention launch failed");
         if (gemm(b->p_o, L.w_o, b->xh, b->xl, h, qd_, TC_RESIDUAL, b->x, h))
             return batch_fail(b, QD_ECUDA, "O GEMM launch failed");
         if (norm(L.mlp_norm, false)) return batch_fail(b, QD_ECUDA, "norm launch failed");
@@ -224,6 +239,29 @@ qd_status enqueue_batch_step(qd_batch *b, cudaStream_t s) {
     ++n;
     if (launch_batch_argmax(am, B, s)) return batch_fail(b, QD_ECUDA, "argmax launch failed");
     b->kernels_per_step = n;
+    return QD_OK;
+}
+
+// One kernel of the step with the step's arguments, for timing: 1 = attention of the
+// last layer at the current positions (it rewrites the row each stream would write
+// next, which the next step overwrites), 2..6 = the QKV, O, gate/up, down GEMMs of layer
+// 0 and the head GEMM (they overwrite step scratch only).
+qd_status enqueue_batch_kernel(qd_batch *b, int which, cudaStream_t s) {
+    qd_model *m = b->m;
+    const qd_config &c = m->cfg;
+    const int h = c.hidden, qd_ = m->q_dim(), rows_qkv = qd_ + 2 * m->kv_dim();
+    const Layer &L0 = m->layers[0];
+    cudaError_t e = cudaSuccess;
+    switch (which) {
+        case 1: e = launch_batch_attention(c.head_dim, b->B, batch_attn_args(b, c.n_layers - 1), s); break;
+        case 2: e = batch_gemm(b, b->p_qkv, L0.w_qkv, b->xh, b->xl, rows_qkv, h, TC_STORE, b->qkv, rows_qkv, s); break;
+        case 3: e = batch_gemm(b, b->p_o, L0.w_o, b->xh, b->xl, h, qd_, TC_RESIDUAL, b->x, h, s); break;
+        case 4: e = batch_gemm(b, b->p_gu, L0.w_gu, b->xh, b->xl, 2 * c.ffn, h, TC_SWIGLU, nullptr, c.ffn, s); break;
+        case 5: e = batch_gemm(b, b->p_d, L0.w_d, b->ah, b->al, h, c.ffn, TC_RESIDUAL, b->x, h, s); break;
+        case 6: e = batch_gemm(b, b->p_head, m->heads[0], b->xh, b->xl, c.vocab, h, TC_STORE, b->logits, c.vocab, s); break;
+        default: return fail(m, QD_EINVAL, "kernel %d: use 1..6", which);
+    }
+    CU(e);
     return QD_OK;
 }
 
@@ -288,7 +326,7 @@ qd_status qd_batch_create(qd_handle model, int n_streams, int smax, qd_batch_han
     b->m = m;
     b->B = n_streams;
     b->S = smax;
-    b->chunk_max = attn_chunk(smax);
+    b->chunk_max = batch_attn_chunk(smax);
     if (!tc_gemm_plan(rows_qkv, c.hidden, n_streams, sms, &b->p_qkv) ||
         !tc_gemm_plan(c.hidden, m->q_dim(), n_streams, sms, &b->p_o) ||
         !tc_gemm_plan(2 * c.ffn, c.hidden, n_streams, sms, &b->p_gu) ||
@@ -296,6 +334,10 @@ qd_status qd_batch_create(qd_handle model, int n_streams, int smax, qd_batch_han
         !tc_gemm_plan(c.vocab, c.hidden, n_streams, sms, &b->p_head)) {
         delete b;
         return fail(m, QD_EUNSUPPORTED, "GEMM shapes: rows must be multiples of 128, K of 64");
+    }
+    if (!batch_attention_supported(c.head_dim, c.n_q_heads / c.n_kv_heads)) {
+        delete b;
+        return fail(m, QD_EUNSUPPORTED, "the batched attention takes 1, 2, 4 or 8 q heads per kv head");
     }
     if (batch_attention_smem_bytes(c.head_dim, c.n_q_heads / c.n_kv_heads, b->chunk_max) > 160 * 1024) {
         delete b;
@@ -324,7 +366,7 @@ qd_status qd_batch_create(qd_handle model, int n_streams, int smax, qd_batch_han
                  o_lg = take((size_t)B * c.vocab * 4), o_xh = take((size_t)B * kmax * 2),
                  o_xl = take((size_t)B * kmax * 2), o_ah = take((size_t)B * c.ffn * 2),
                  o_al = take((size_t)B * c.ffn * 2), o_part = take(std::max<size_t>(part, 1) * 4),
-                 o_cnt = take((size_t)tiles * 4), o_pos = take((size_t)B * 4), o_st = take(16),
+                 o_cnt = take((size_t)tiles * 8), o_pos = take((size_t)B * 4), o_st = take(16),
                  o_tok = take((size_t)B * 4), o_em = take((size_t)B * b->words * 4), o_ctl = take(sizeof(BatchCtl)),
                  o_cos = take((size_t)smax * (c.head_dim / 2) * 4), o_sin = take((size_t)smax * (c.head_dim / 2) * 4);
     b->stream_elems = (size_t)c.n_layers * 2 * c.n_kv_heads * smax * c.head_dim;
@@ -469,6 +511,46 @@ qd_status qd_batch_copy_kv(qd_batch_handle b, int stream, void *dst_dev, size_t 
                        b->ls));
     CU(cudaStreamSynchronize(b->ls));
     *bytes = n;
+    return QD_OK;
+}
+
+qd_status qd_batch_time_kernel(qd_batch_handle b, int which, int reps, float *avg_ms) {
+    if (!b || !avg_ms || reps < 1) return QD_EINVAL;
+    qd_model *m = b->m;
+    for (int i = 0; i < b->B; ++i) {
+        if (!b->h_ready[i]) return fail(m, QD_ESTATE, "stream %d has no cache and input token", i);
+        if (b->h_pos[i] >= b->S) return fail(m, QD_EKVFULL, "stream %d is full", i);
+    }
+    // the launches are captured into a graph so that host work does not pace them
+    cudaGraph_t g = nullptr;
+    cudaGraphExec_t ex = nullptr;
+    CU(cudaStreamBeginCapture(b->ls, cudaStreamCaptureModeThreadLocal));
+    qd_status st = QD_OK;
+    for (int i = 0; i < reps && !st; ++i) st = enqueue_batch_kernel(b, which, b->ls);
+    cudaError_t ce = cudaStreamEndCapture(b->ls, &g);
+    if (st) {
+        if (g) cudaGraphDestroy(g);
+        return st;
+    }
+    CU(ce);
+    cudaError_t ie = cudaGraphInstantiate(&ex, g, 0);
+    cudaGraphDestroy(g);
+    CU(ie);
+    cudaEvent_t e0, e1;
+    CU(cudaEventCreate(&e0));
+    CU(cudaEventCreate(&e1));
+    CU(cudaGraphLaunch(ex, b->ls));   // warm-up
+    CU(cudaEventRecord(e0, b->ls));
+    CU(cudaGraphLaunch(ex, b->ls));
+    CU(cudaEventRecord(e1, b->ls));
+    CU(cudaEventSynchronize(e1));
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, e0, e1);
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    cudaGraphExecDestroy(ex);
+    *avg_ms = ms / reps;
+    b->launches += 2LL * reps;
     return QD_OK;
 }
 

@@ -212,7 +212,7 @@ struct TcGemmArgs {
     int ldo;
     __nv_bfloat16 *act_hi, *act_lo;// TC_SWIGLU: [T][R/2]
     float *partial;                // split-K partial sums [units][BN][128], or null when splits == 1
-    int *tile_counter;             // [row tiles x token tiles], zero at rest
+    int *tile_counter;             // [row tiles x token tiles][2] (arrive, depart), zero at rest
     int *status;                   // DEV_ERR_* bits
 };
 
@@ -260,7 +260,17 @@ struct BatchAttnArgs {
     int *status;
 };
 
+// Positions per attention split of the batched path: the attended length L divided
+// evenly over kAttnMaxSplits splits (a function of L only), so every split of a
+// cluster has work once L >= 57.
+__host__ __device__ inline int batch_attn_chunk(int L) { return (L + kAttnMaxSplits - 1) / kAttnMaxSplits; }
+__host__ __device__ inline int batch_attn_splits(int L) {
+    const int c = batch_attn_chunk(L);
+    return (L + c - 1) / c;
+}
+
 size_t batch_attention_smem_bytes(int hd, int group, int chunk_max);
+bool batch_attention_supported(int hd, int group);   // head_dim 64/128, 1, 2, 4 or 8 q heads per kv head
 cudaError_t batch_kernels_init();   // call before any capture
 cudaError_t launch_batch_attention(int hd, int B, const BatchAttnArgs &a, cudaStream_t s);
 

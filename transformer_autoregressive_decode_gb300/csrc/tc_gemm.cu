@@ -18,9 +18,10 @@
 // only touch its quarter of the 128 lanes: warp w reads lanes 32*(w%4)..+31) and run
 // the epilogue.  Two accumulators alternate so a tile's epilogue overlaps the next
 // tile's MMAs.  When the tiles alone cannot fill the GPU (decode: 64 tokens) the K
-// range is split over several CTAs; each writes its partial tile to scratch and the
-// last CTA of a tile (completion counter) sums the partials in split order and runs
-// the epilogue, so the result does not depend on timing.
+// range is split over several CTAs (launched cooperatively, one unit each, so all are
+// resident); each writes its partial tile to scratch, the split CTAs of a tile meet on
+// a counter, and each then sums its share of the tile's columns over all splits in
+// split order and runs the epilogue on it, so the result does not depend on timing.
 //
 // Every wait is bounded (1 s on %globaltimer); on expiry the kernel records
 // DEV_ERR_WAIT_TIMEOUT, every role stops, copies and MMAs in flight are drained, the
@@ -128,6 +129,12 @@ __device__ __forceinline__ bool role_wait(uint64_t *bar, uint32_t parity, volati
         }
     }
     return true;
+}
+
+__device__ __forceinline__ int ld_acquire_s32(const int *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
 struct Unit {
@@ -327,28 +334,60 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[acc]);
             if (splits > 1) {
+                // The split CTAs of a tile meet (the launch is cooperative, so all of them
+                // are resident), then each sums its share of the tile's columns over every
+                // split, in split order, and runs the epilogue on it.
                 __threadfence();
                 named_sync(1, 128);
+                int *arrive = a.tile_counter + 2 * x.tile;
+                int *depart = arrive + 1;
                 if (warp == 2 && lane == 0) {
-                    const int old = atomicAdd(&a.tile_counter[x.tile], 1);
-                    const int last = old == splits - 1;
-                    if (last) a.tile_counter[x.tile] = 0;   // at rest for the next launch
-                    *is_last = last;
+                    atomicAdd(arrive, 1);
+                    int met = 1;
+                    const unsigned long long t0 = global_timer_ns();
+                    while (ld_acquire_s32(arrive) < splits) {
+                        if (*abort_flag || global_timer_ns() - t0 > kWaitLimitNs) {
+                            if (!*abort_flag) atomicOr(a.status, DEV_ERR_WAIT_TIMEOUT);
+                            *abort_flag = 1;
+                            met = 0;
+                            break;
+                        }
+                    }
+                    *is_last = met;
                 }
                 named_sync(1, 128);
-                if (*is_last) {
+                const bool met = *is_last != 0;
+                if (met) {
                     __threadfence();
-                    const float *p0 = a.partial + (size_t)x.tile * splits * BN * kBM;
+                    const int s_idx = u - x.tile * splits;
+                    const int c_lo = s_idx * BN / splits, c_hi = (s_idx + 1) * BN / splits;
+                    const float *p0 = a.partial + (size_t)x.tile * splits * BN * kBM + row_in_tile;
 #pragma unroll 1
-                    for (int c = 0; c < BN; ++c) {
-                        const int t = x.nt * BN + c;
-                        if (t >= a.T) break;
-                        float v = 0.f;
-                        for (int s = 0; s < splits; ++s) v += __ldcg(p0 + ((size_t)s * BN + c) * kBM + row_in_tile);
-                        epi_apply(a, t, r, v, lane);
+                    for (int c = c_lo; c < c_hi; c += 4) {
+                        float v[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+                        for (int s2 = 0; s2 < splits; ++s2) {
+                            const float *ps = p0 + (size_t)s2 * BN * kBM;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                if (c + j < c_hi) v[j] += __ldcg(ps + (size_t)(c + j) * kBM);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int t = x.nt * BN + c + j;
+                            if (c + j < c_hi && t < a.T) epi_apply(a, t, r, v[j], lane);
+                        }
                     }
                 }
-                named_sync(1, 128);   // is_last is reused by the next unit
+                named_sync(1, 128);
+                if (warp == 2 && lane == 0 && met) {
+                    // the last CTA to leave puts the tile's counters back at rest
+                    if (atomicAdd(depart, 1) == splits - 1) {
+                        *arrive = 0;
+                        *depart = 0;
+                        __threadfence();
+                    }
+                }
             }
         }
     }
@@ -417,8 +456,26 @@ template <int BN> cudaError_t launch_bn(const TcGemmPlan &p, const void *w, cons
     CUtensorMap mw, mh, ml;
     if (!make_map(&mw, w, a.R, a.K, kBM) || !make_map(&mh, xh, a.T, a.K, BN) || !make_map(&ml, xl, a.T, a.K, BN))
         return cudaErrorInvalidValue;
-    tc_gemm_kernel<BN><<<p.grid, kTcThreads, TcCfg<BN>::kSmem, s>>>(mw, mh, ml, a, p.tok_tiles, p.splits, p.units);
-    return cudaGetLastError();
+    if (p.splits == 1) {
+        tc_gemm_kernel<BN><<<p.grid, kTcThreads, TcCfg<BN>::kSmem, s>>>(mw, mh, ml, a, p.tok_tiles, p.splits,
+                                                                          p.units);
+        return cudaGetLastError();
+    }
+    // split-K: the split CTAs of a tile wait for one another, so they must all be
+    // resident; a cooperative launch guarantees it (one unit per CTA, grid <= SMs)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.grid);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = TcCfg<BN>::kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeCooperative;
+    at[0].val.cooperative = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    int tok_tiles = p.tok_tiles, splits = p.splits, units = p.units;
+    void *args[7] = {&mw, &mh, &ml, const_cast<TcGemmArgs *>(&a), &tok_tiles, &splits, &units};
+    return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(tc_gemm_kernel<BN>), args);
 }
 
 }  // namespace
@@ -449,7 +506,7 @@ bool tc_gemm_plan(int R, int K, int T, int num_sms, TcGemmPlan *p) {
 
 cudaError_t launch_tc_gemm(const TcGemmPlan &p, const void *w, const void *x_hi, const void *x_lo,
                            const TcGemmArgs &a, cudaStream_t s) {
-    if (p.splits > 1 && (!a.partial || !a.tile_counter)) return cudaErrorInvalidValue;
+    if (p.splits > 1 && (!a.partial || !a.tile_counter || p.units > p.grid)) return cudaErrorInvalidValue;
     if (a.mode == TC_SWIGLU && (!a.act_hi || !a.act_lo)) return cudaErrorInvalidValue;
     return p.bn == 64 ? launch_bn<64>(p, w, x_hi, x_lo, a, s) : launch_bn<128>(p, w, x_hi, x_lo, a, s);
 }
