@@ -31,14 +31,18 @@ METRIC = "decode tokens/s at 1 GB300; per-step HBM GB/s as fraction of peak"
 # DRAM bytes (read + write) of one decode_step_kernel launch from one ncu capture
 # (profiles/decode_step_kernel_asr.md), at attended length L, for the kernel sources
 # with this digest; null in the JSON line once the sources differ.
-_STEP_TRAFFIC = {"asr": {"digest": "6f2083bca17fa563", "bytes": 224744704 + 3667712, "L": 116}}
+_STEP_TRAFFIC = {"asr": {"digest": "5c88e4b440df103b", "bytes": 224744704 + 3667712, "L": 116}}
 _STEP_SOURCES = ("decode_persistent.cu", "decode_common.cuh", "qd_device.cuh", "qd_internal.h")
+# DRAM bytes of one batch_attn_kernel launch (profiles/batch_attn_kernel_batch64.md) at
+# the initial lengths + 3, for the kernel sources with this digest.
+_BATT_TRAFFIC = {"digest": "c0279d7af4690efa", "bytes": 256616704 + 3798016, "rows": 62239 + 3 * 64}
+_BATT_SOURCES = ("batch_kernels.cu", "decode_common.cuh", "qd_device.cuh", "qd_internal.h")
 
 
-def _step_digest() -> str:
+def _step_digest(sources=_STEP_SOURCES) -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in _STEP_SOURCES:
+    for f in sources:
         with open(os.path.join(ROOT, "transformer_autoregressive_decode_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -712,6 +716,12 @@ def batch_arm(args):
     # dominant kernel: attention of one layer, at the initial lengths (L = L0 + 1)
     att_bytes = sum(L + 1 for L in lens) * kv_pos / s.n_layers
     att_gbs = att_bytes / (kms["attention"] / 1e3) / 1e9
+    att_traffic, att_note = None, "no ncu capture for this kernel build"
+    if not args.layers and _BATT_TRAFFIC["digest"] == _step_digest(_BATT_SOURCES):
+        rows = sum(L + 1 for L in lens)
+        att_traffic = _BATT_TRAFFIC["bytes"] * rows / _BATT_TRAFFIC["rows"]
+        att_note = (f"ncu dram__bytes_read+write of one launch with {_BATT_TRAFFIC['rows']} cached rows per group "
+                    f"({_BATT_TRAFFIC['bytes']} B), scaled to {rows} rows")
     # the GEMMs: useful flops per step and their summed kernel time
     layer_params = s.layer_matrix_params()
     gemm_ms = s.n_layers * (kms["qkv"] + kms["oproj"] + kms["gate_up"] + kms["down"]) + kms["head"]
@@ -764,8 +774,7 @@ def batch_arm(args):
                    "l2": f"inputs larger than L2: {step_bytes / 1e9:.2f} GB per step",
                    "parallelism": "replicas" if ws > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": att_gbs, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": att_gbs / hbm_peak, "traffic": None,
-                     "traffic_note": "no ncu capture for this workload and kernel build",
+                     "frac": att_gbs / hbm_peak, "traffic": att_traffic, "traffic_note": att_note,
                      "kernel": "batch_attn_kernel: one layer's attention of all 64 streams over their caches "
                                "(QK-norm, RoPE, KV append, 8-way split, cluster merge)",
                      "bytes_per_launch": att_bytes, "avg_launch_ms": kms["attention"], "peak_source": peak_src,

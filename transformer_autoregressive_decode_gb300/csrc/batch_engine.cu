@@ -100,7 +100,7 @@ qd_status qd_gemm_bf16(const void *w_dev, const float *x_dev, float *out_dev, in
 
 struct qd_batch {
     qd_model *m = nullptr;
-    int B = 0, S = 0, chunk_max = 0;
+    int B = 0, S = 0;
     cudaStream_t ls = nullptr;
     void *arena = nullptr;
     void *kv = nullptr;
@@ -108,6 +108,8 @@ struct qd_batch {
     float *x = nullptr, *qkv = nullptr, *logits = nullptr, *rope_cos = nullptr, *rope_sin = nullptr;
     __nv_bfloat16 *xh = nullptr, *xl = nullptr, *ah = nullptr, *al = nullptr;
     float *partial = nullptr;
+    float *att_part = nullptr;   // attention chunk records [B * kvh][chunks][G][hd + 2]
+    int *att_count = nullptr;    // [B * kvh]
     int *counters = nullptr, *pos = nullptr, *status = nullptr;
     int32_t *tokens = nullptr;
     uint32_t *emitted = nullptr;
@@ -166,7 +168,8 @@ BatchAttnArgs batch_attn_args(qd_batch *b, int l) {
     at.S = b->S;
     at.qh = c.n_q_heads;
     at.kvh = c.n_kv_heads;
-    at.chunk_max = b->chunk_max;
+    at.partial = b->att_part;
+    at.counter = b->att_count;
     at.pos = b->pos;
     at.out_hi = b->xh;
     at.out_lo = b->xl;
@@ -326,7 +329,6 @@ qd_status qd_batch_create(qd_handle model, int n_streams, int smax, qd_batch_han
     b->m = m;
     b->B = n_streams;
     b->S = smax;
-    b->chunk_max = batch_attn_chunk(smax);
     if (!tc_gemm_plan(rows_qkv, c.hidden, n_streams, sms, &b->p_qkv) ||
         !tc_gemm_plan(c.hidden, m->q_dim(), n_streams, sms, &b->p_o) ||
         !tc_gemm_plan(2 * c.ffn, c.hidden, n_streams, sms, &b->p_gu) ||
@@ -339,7 +341,7 @@ qd_status qd_batch_create(qd_handle model, int n_streams, int smax, qd_batch_han
         delete b;
         return fail(m, QD_EUNSUPPORTED, "the batched attention takes 1, 2, 4 or 8 q heads per kv head");
     }
-    if (batch_attention_smem_bytes(c.head_dim, c.n_q_heads / c.n_kv_heads, b->chunk_max) > 160 * 1024) {
+    if (batch_attention_smem_bytes(c.head_dim, c.n_q_heads / c.n_kv_heads) > 160 * 1024) {
         delete b;
         return fail(m, QD_EUNSUPPORTED, "smax %d too long for the attention tile", smax);
     }
@@ -368,7 +370,10 @@ qd_status qd_batch_create(qd_handle model, int n_streams, int smax, qd_batch_han
                  o_al = take((size_t)B * c.ffn * 2), o_part = take(std::max<size_t>(part, 1) * 4),
                  o_cnt = take((size_t)tiles * 8), o_pos = take((size_t)B * 4), o_st = take(16),
                  o_tok = take((size_t)B * 4), o_em = take((size_t)B * b->words * 4), o_ctl = take(sizeof(BatchCtl)),
-                 o_cos = take((size_t)smax * (c.head_dim / 2) * 4), o_sin = take((size_t)smax * (c.head_dim / 2) * 4);
+                 o_cos = take((size_t)smax * (c.head_dim / 2) * 4), o_sin = take((size_t)smax * (c.head_dim / 2) * 4),
+                 o_ap = take((size_t)B * c.n_kv_heads * batch_attn_max_chunks(smax) *
+                             (c.n_q_heads / c.n_kv_heads) * (c.head_dim + 2) * 4),
+                 o_ac = take((size_t)B * c.n_kv_heads * 4);
     b->stream_elems = (size_t)c.n_layers * 2 * c.n_kv_heads * smax * c.head_dim;
     qd_status st = QD_OK;
     auto check = [&](cudaError_t e, const char *what) {
@@ -396,6 +401,8 @@ qd_status qd_batch_create(qd_handle model, int n_streams, int smax, qd_batch_han
         b->ctl = reinterpret_cast<BatchCtl *>(A + o_ctl);
         b->rope_cos = reinterpret_cast<float *>(A + o_cos);
         b->rope_sin = reinterpret_cast<float *>(A + o_sin);
+        b->att_part = reinterpret_cast<float *>(A + o_ap);
+        b->att_count = reinterpret_cast<int *>(A + o_ac);
         check(cudaMemsetAsync(b->arena, 0, off, b->ls), "cudaMemsetAsync");
         check(launch_rope_table(b->rope_cos, b->rope_sin, smax, c.head_dim, c.rope_theta, b->ls), "RoPE table");
         check(cudaStreamSynchronize(b->ls), "cudaStreamSynchronize");

@@ -15,23 +15,25 @@ namespace qd {
 
 namespace {
 
-// ---- attention: grid (kv group, split, stream); the splits of one (stream, group)
-// form an 8-CTA cluster and merge through distributed shared memory (flash-decoding
-// combine, splits in index order); a split holds batch_attn_chunk(L) = ceil(L / 8)
-// positions, so all 8 CTAs of a cluster have work.  Each CTA streams its split's cached K rows, then its V rows,
-// in 32-position tiles through a 4-slot shared-memory ring (1-D bulk copies, one
-// mbarrier per slot), so several CTAs share an SM and one CTA's copies overlap the
-// others' arithmetic.  The new position's k and v (QK-norm and RoPE applied, rounded
-// to the cache type) are appended to the cache and enter the sums from shared memory.
-// Scores: warp w takes rows w, w+8, ... of a tile, each lane 4 (or 2) dimensions of
-// the row; P.V the same rows, each lane accumulating its dimensions, then the warps'
-// partial outputs are summed.
-constexpr int kBattThreads = 256;
-constexpr int kBattWarps = kBattThreads / 32;
+// ---- attention: one CTA per (stream, kv group, chunk of 256 cached positions), 8
+// consumer warps and a producer warp.  The producer streams the chunk's K rows, then
+// its V rows, in 32-position tiles through a 6-slot shared-memory ring (1-D bulk
+// copies; full/empty mbarriers per slot).  Consumer warp w owns rows 4w..4w+3 of every
+// tile, so 32 rows of the chunk, one per lane: pass 1 computes their scores (4 rows x
+// G heads reduced with one butterfly, then each score moved to its row's lane), a
+// softmax over the warp's rows runs lane-parallel, pass 2 accumulates P.V.  The
+// warps' partials (and, in the chunk that holds it, the new position, whose k and v
+// are QK-normed, rotated, rounded to the cache type and appended) are combined into
+// the chunk's (max, sum, output); the last chunk CTA of a (stream, group) to finish
+// merges the chunks in order (flash-decoding merge) and writes the output.  Equal
+// chunks keep the work balanced whatever the lengths; no CTA waits for another.
+constexpr int kBattConsumers = 8;
+constexpr int kBattThreads = (kBattConsumers + 1) * 32;
 constexpr int kBattTile = 32;        // positions per ring slot
-constexpr int kBattSlots = 4;
+constexpr int kBattSlots = 6;
 constexpr int kBattMaxGroup = 8;     // q heads per kv head
-constexpr int kBattRowsPerWarp = kBattTile / kBattWarps;   // 4
+constexpr int kBattRowsPerWarp = kBattTile / kBattConsumers;   // 4
+static_assert(kBattChunk / kBattTile * kBattRowsPerWarp == 32, "one chunk row per lane of each warp");
 
 // Sums N per-lane values over the lanes of a warp with one butterfly: each halving
 // step trades half of the values with the partner lane, so N values cost about N
@@ -79,283 +81,310 @@ __device__ __forceinline__ void tile_row(const __nv_bfloat16 *tile, int jj, int 
     }
 }
 
+// Owner lane of value i after ReduceScatter<N, 16>: the lane bits set by the halving
+// steps that kept the upper half.
+template <int N> __device__ __forceinline__ int scatter_owner(int i) {
+    int lane = 0, mask = 16;
+#pragma unroll
+    for (int half = N / 2; half >= 1; half >>= 1, mask >>= 1)
+        if (i & half) lane |= mask;
+    return lane;
+}
+
 template <int HD, int G>
-__global__ void __launch_bounds__(kBattThreads, 4) batch_attn_kernel(const BatchAttnArgs a) {
+__global__ void __launch_bounds__(kBattThreads, G <= 2 ? 4 : 2) batch_attn_kernel(const BatchAttnArgs a) {
     using KT = __nv_bfloat16;
     constexpr int HALF = HD / 2;
     constexpr int DPL = HD / 32;                       // dimensions per lane
     constexpr uint32_t kTileBytes = kBattTile * HD * 2;
-    static_assert(G >= 1 && G <= kBattMaxGroup, "group size");
+    constexpr int NV = kBattRowsPerWarp * G;           // scores of one warp per tile
+    constexpr int RS = HD + 2;                         // partial record: output, max, sum
+    static_assert(G >= 1 && G <= kBattMaxGroup && NV <= 32, "group size");
     extern __shared__ __align__(1024) uint8_t smem[];
-    const int CM = a.chunk_max;
     uint8_t *ring = smem;                                                    // [slots][tile]
-    float *red = reinterpret_cast<float *>(ring);                            // [warps][G][HD], after the ring
+    float *red = reinterpret_cast<float *>(ring);                            // [warps + 1][G][RS], after the ring
     float *qs = reinterpret_cast<float *>(ring + kBattSlots * kTileBytes);  // [G][HD]
     float *kn = qs + G * HD;                                                 // [HD]
     float *vn = kn + HD;                                                     // [HD]
     float *rc = vn + HD;                                                     // [HALF] cos, [HALF] sin
-    float *sc = rc + HD;                                                     // [G][CM]
-    float *po = sc + G * CM;                                                 // [G][HD]
-    float *pm = po + G * HD;                                                 // [G]
-    float *pl = pm + G;                                                      // [G]
-    uint64_t *full = reinterpret_cast<uint64_t *>((reinterpret_cast<uintptr_t>(pl + G) + 7) & ~uintptr_t(7));
+    uint64_t *full = reinterpret_cast<uint64_t *>(rc + HD);                  // [slots]
+    uint64_t *empty = full + kBattSlots;                                     // [slots]
+    int *flag = reinterpret_cast<int *>(empty + kBattSlots);                 // [0] abort, [1] last chunk
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = blockIdx.x, s = blockIdx.y, b = blockIdx.z;
+    const int pairs = gridDim.x / batch_attn_max_chunks(a.S);
+    const int c = blockIdx.x / pairs;                  // chunk
+    const int pair = blockIdx.x - c * pairs;           // (stream, kv group)
+    const int b = pair / a.kvh, g = pair - b * a.kvh;
     const int p = a.pos[b];
-    const int L = p + 1;
-    const int C = batch_attn_chunk(L);
-    const int nsplit = batch_attn_splits(L);
-    const bool valid = p >= 0 && p < a.S && C <= CM && a.qh == G * a.kvh;
-    const bool active = valid && s < nsplit;
-    if (!valid && tid == 0 && s == 0 && g == 0) atomicOr(a.status, DEV_ERR_BAD_POS);
-
-    KT *kbase = reinterpret_cast<KT *>(a.kv) + (size_t)b * a.stream_elems + a.layer_elems;
+    const bool valid = p >= 0 && p < a.S && a.qh == G * a.kvh;
+    if (!valid) {
+        if (tid == 0 && g == 0 && c == 0) atomicOr(a.status, DEV_ERR_BAD_POS);
+        return;
+    }
+    const int nC = p / kBattChunk + 1;                 // chunks of [0, p], the last holds p
+    if (c >= nC) return;
+    const bool holds_new = c == nC - 1;
+    const int j0 = c * kBattChunk;
+    const int rows_c = (holds_new ? p : j0 + kBattChunk) - j0;   // cached rows of the chunk
+    const int nT = (rows_c + kBattTile - 1) / kBattTile;
+    const int total = 2 * nT;                          // K tiles, then V tiles
+    const size_t grp_off = (size_t)g * a.S * HD;
+    KT *kbase = reinterpret_cast<KT *>(a.kv) + (size_t)b * a.stream_elems + a.layer_elems + grp_off;
     KT *vbase = kbase + (size_t)a.kvh * a.S * HD;
+
+    if (tid == 0) {
+        for (int i = 0; i < kBattSlots; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kBattConsumers);
+        }
+        flag[0] = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kBattConsumers) {
+        // ---- producer
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            int issued = 0;
+            for (; issued < total; ++issued) {
+                const int slot = issued % kBattSlots;
+                if (issued >= kBattSlots &&
+                    !mbar_wait_bounded(&empty[slot], (uint32_t)(issued / kBattSlots - 1) & 1u)) {
+                    atomicOr(a.status, DEV_ERR_WAIT_TIMEOUT);
+                    *reinterpret_cast<volatile int *>(flag) = 1;
+                    break;
+                }
+                const int i = issued < nT ? issued : issued - nT;
+                const int rows = rows_c - i * kBattTile < kBattTile ? rows_c - i * kBattTile : kBattTile;
+                const uint32_t bytes = (uint32_t)rows * HD * 2;
+                mbar_arrive_expect_tx(&full[slot], bytes);
+                bulk_copy_g2s(ring + (size_t)slot * kTileBytes,
+                              (issued < nT ? kbase : vbase) + (size_t)(j0 + i * kBattTile) * HD, bytes, &full[slot],
+                              pol);
+            }
+            // copies in flight land before the CTA can leave
+            for (int k = 0; k < kBattSlots; ++k) {
+                int last = -1;
+                for (int t = k; t < issued; t += kBattSlots) last = t;
+                if (last >= 0) (void)mbar_wait_bounded(&full[k], (uint32_t)(last / kBattSlots) & 1u, 10000000ull);
+            }
+        }
+        return;
+    }
+
+    // ---- consumers: q (and k, v) of the new position, QK-norm and RoPE
+    constexpr int NC = kBattConsumers * 32;
     const float *row = a.qkv + (size_t)b * a.qkv_ld;
+    for (int m = tid; m < HALF; m += NC) {
+        rc[m] = a.rope_cos[(size_t)p * HALF + m];
+        rc[HALF + m] = a.rope_sin[(size_t)p * HALF + m];
+    }
+    for (int i = tid; i < G * HD; i += NC) qs[i] = __ldcg(row + (size_t)g * G * HD + i);
+    for (int i = tid; i < HD; i += NC) {
+        kn[i] = __ldcg(row + (size_t)a.qh * HD + (size_t)g * HD + i);
+        vn[i] = __ldcg(row + (size_t)(a.qh + a.kvh) * HD + (size_t)g * HD + i);
+    }
+    named_sync(1, NC);
+    qk_norm_rope<HD, kBattConsumers>(qs, kn, G, a.q_gamma, a.k_gamma, a.eps, rc, 1);
+    if (holds_new) {
+        for (int i = tid; i < HD; i += NC) {
+            const KT kb = __float2bfloat16_rn(kn[i]), vb = __float2bfloat16_rn(vn[i]);
+            kbase[(size_t)p * HD + i] = kb;
+            vbase[(size_t)p * HD + i] = vb;
+            kn[i] = __bfloat162float(kb);
+            vn[i] = __bfloat162float(vb);
+        }
+        named_sync(1, NC);
+    }
+    float qr[G][DPL];
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) qr[hh][e] = qs[hh * HD + lane * DPL + e];
 
+    // pass 1: scores; lane l ends with the score of this warp's row l (tile l / 4,
+    // row 4 * warp + l % 4 of that tile), -inf past the chunk's rows
     bool ok = true;
-    if (active) {
-        const int j0 = s * C;
-        const int n = L - j0 < C ? L - j0 : C;
-        const int n_old = (p - j0) < n ? (p - j0) : n;   // cached rows [j0, j0 + n_old)
-        const int nT = (n_old + kBattTile - 1) / kBattTile;
-        const int total = 2 * nT;                         // K tiles, then V tiles
-        const size_t grp_off = (size_t)g * a.S * HD;
-        const KT *kc = kbase + grp_off;
-        const KT *vc = vbase + grp_off;
-        int issued = 0;                                   // thread 0: tiles issued so far
-        uint64_t pol = 0;
-        auto issue = [&](int t) {
-            const int slot = t % kBattSlots;
-            const int i = t < nT ? t : t - nT;
-            const int rows = n_old - i * kBattTile < kBattTile ? n_old - i * kBattTile : kBattTile;
-            const KT *src = (t < nT ? kc : vc) + (size_t)(j0 + i * kBattTile) * HD;
-            const uint32_t bytes = (uint32_t)rows * HD * 2;
-            mbar_arrive_expect_tx(&full[slot], bytes);
-            bulk_copy_g2s(ring + (size_t)slot * kTileBytes, src, bytes, &full[slot], pol);
-        };
-        if (tid == 0) {
-            for (int i = 0; i < kBattSlots; ++i) mbar_init(&full[i], 1);
-            fence_barrier_init();
-            pol = policy_evict_first();
-            for (; issued < total && issued < kBattSlots; ++issued) issue(issued);
-        }
-        for (int m = tid; m < HALF; m += kBattThreads) {
-            rc[m] = a.rope_cos[(size_t)p * HALF + m];
-            rc[HALF + m] = a.rope_sin[(size_t)p * HALF + m];
-        }
-        const float *qsrc = row + (size_t)g * G * HD;
-        const float *ksrc = row + (size_t)a.qh * HD + (size_t)g * HD;
-        const float *vsrc = row + (size_t)(a.qh + a.kvh) * HD + (size_t)g * HD;
-        for (int i = tid; i < G * HD; i += kBattThreads) qs[i] = __ldcg(qsrc + i);
-        for (int i = tid; i < HD; i += kBattThreads) {
-            kn[i] = __ldcg(ksrc + i);
-            vn[i] = __ldcg(vsrc + i);
-        }
-        __syncthreads();
-        qk_norm_rope<HD, kBattWarps>(qs, kn, G, a.q_gamma, a.k_gamma, a.eps, rc, 1);
-        if (n_old < n) {
-            // this split holds position p: append the new row and use its cache value
-            KT *kw = kbase + grp_off + (size_t)p * HD;
-            KT *vw = vbase + grp_off + (size_t)p * HD;
-            for (int i = tid; i < HD; i += kBattThreads) {
-                const KT kb = __float2bfloat16_rn(kn[i]), vb = __float2bfloat16_rn(vn[i]);
-                kw[i] = kb;
-                vw[i] = vb;
-                kn[i] = __bfloat162float(kb);
-                vn[i] = __bfloat162float(vb);
-            }
-            fence_proxy_async_global();
-        }
-        __syncthreads();
-        float qr[G][DPL];
+    float smine[G];
 #pragma unroll
-        for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-            for (int e = 0; e < DPL; ++e) qr[hh][e] = qs[hh * HD + lane * DPL + e];
-
-        // pass 1: scores of the cached rows
-        for (int t = 0; t < nT; ++t) {
-            const int slot = t % kBattSlots;
-            const bool got = mbar_wait_bounded(&full[slot], (uint32_t)(t / kBattSlots) & 1u);
-            if (got) {
-                const KT *tile = reinterpret_cast<const KT *>(ring + (size_t)slot * kTileBytes);
-                const int rows = n_old - t * kBattTile < kBattTile ? n_old - t * kBattTile : kBattTile;
-                // this warp's 4 rows x G heads, reduced together
-                constexpr int NV = kBattRowsPerWarp * G;
-                float v[NV];
-#pragma unroll
-                for (int r = 0; r < kBattRowsPerWarp; ++r) {
-                    const int jj = warp * kBattRowsPerWarp + r;
-                    float kf[DPL];
-                    tile_row<DPL, HD>(tile, jj, lane, jj < rows, kf);
-#pragma unroll
-                    for (int hh = 0; hh < G; ++hh) {
-                        float d = 0.f;
-#pragma unroll
-                        for (int e = 0; e < DPL; ++e) d = fmaf(qr[hh][e], kf[e], d);
-                        v[r * G + hh] = d;
-                    }
-                }
-                int idx = 0;
-                ReduceScatter<NV, 16>::run(v, lane, idx);
-                if ((lane & (32 / NV - 1)) == 0) {
-                    const int r = idx / G, hh = idx - r * G;
-                    const int jj = warp * kBattRowsPerWarp + r;
-                    if (jj < rows) sc[hh * CM + t * kBattTile + jj] = v[0] * a.scale;
-                }
-            }
-            if (__syncthreads_or(!got)) {
-                ok = false;
-                break;
-            }
-            if (tid == 0 && issued < total) {
-                fence_proxy_async_smem();
-                issue(issued++);
-            }
+    for (int hh = 0; hh < G; ++hh) smine[hh] = -INFINITY;
+    for (int t = 0; t < nT; ++t) {
+        const int slot = t % kBattSlots;
+        if (!mbar_wait_bounded(&full[slot], (uint32_t)(t / kBattSlots) & 1u)) {
+            ok = false;
+            break;
         }
-        if (ok && n_old < n && warp == 0) {
+        const KT *tile = reinterpret_cast<const KT *>(ring + (size_t)slot * kTileBytes);
+        const int rows = rows_c - t * kBattTile < kBattTile ? rows_c - t * kBattTile : kBattTile;
+        float v[NV];
+#pragma unroll
+        for (int r = 0; r < kBattRowsPerWarp; ++r) {
+            const int jj = warp * kBattRowsPerWarp + r;
+            float kf[DPL];
+            tile_row<DPL, HD>(tile, jj, lane, jj < rows, kf);
 #pragma unroll
             for (int hh = 0; hh < G; ++hh) {
                 float d = 0.f;
 #pragma unroll
-                for (int e = 0; e < DPL; ++e) d = fmaf(qr[hh][e], kn[lane * DPL + e], d);
-                d = warp_sum(d);
-                if (lane == 0) sc[hh * CM + n_old] = d * a.scale;
+                for (int e = 0; e < DPL; ++e) d = fmaf(qr[hh][e], kf[e], d);
+                v[r * G + hh] = d;
             }
         }
-        __syncthreads();
-        if (ok) {
-            for (int hh = warp; hh < G; hh += kBattWarps) {
-                float mx = -INFINITY;
-                for (int j = lane; j < n; j += 32) mx = fmaxf(mx, sc[hh * CM + j]);
-                mx = warp_max(mx);
-                float l = 0.f;
-                for (int j = lane; j < n; j += 32) {
-                    const float e = expf(sc[hh * CM + j] - mx);
-                    sc[hh * CM + j] = e;
-                    l += e;
-                }
-                l = warp_sum(l);
-                if (lane == 0) {
-                    pm[hh] = mx;
-                    pl[hh] = l;
-                }
-            }
-        }
-        __syncthreads();
-
-        // pass 2: P.V over the cached rows, then the new row
-        float acc[G][DPL];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        int idx = 0;
+        ReduceScatter<NV, 16>::run(v, lane, idx);
 #pragma unroll
-        for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-            for (int e = 0; e < DPL; ++e) acc[hh][e] = 0.f;
-        for (int t = nT; t < total && ok; ++t) {
-            const int slot = t % kBattSlots;
-            const bool got = mbar_wait_bounded(&full[slot], (uint32_t)(t / kBattSlots) & 1u);
-            if (got) {
-                const KT *tile = reinterpret_cast<const KT *>(ring + (size_t)slot * kTileBytes);
-                const int i = t - nT;
-                const int rows = n_old - i * kBattTile < kBattTile ? n_old - i * kBattTile : kBattTile;
-#pragma unroll
-                for (int r = 0; r < kBattRowsPerWarp; ++r) {
-                    const int jj = warp * kBattRowsPerWarp + r;
-                    if (jj < rows) {
-                        float vf[DPL];
-                        tile_row<DPL, HD>(tile, jj, lane, true, vf);
-                        const int j = i * kBattTile + jj;
-#pragma unroll
-                        for (int hh = 0; hh < G; ++hh) {
-                            const float pj = sc[hh * CM + j];
-#pragma unroll
-                            for (int e = 0; e < DPL; ++e) acc[hh][e] = fmaf(pj, vf[e], acc[hh][e]);
-                        }
-                    }
-                }
-            }
-            if (__syncthreads_or(!got)) {
-                ok = false;
-                break;
-            }
-            if (tid == 0 && issued < total) {
-                fence_proxy_async_smem();
-                issue(issued++);
-            }
-        }
-        if (ok && n_old < n && warp == 0) {
+        for (int r = 0; r < kBattRowsPerWarp; ++r)
 #pragma unroll
             for (int hh = 0; hh < G; ++hh) {
-                const float pj = sc[hh * CM + n_old];
-#pragma unroll
-                for (int e = 0; e < DPL; ++e) acc[hh][e] = fmaf(pj, vn[lane * DPL + e], acc[hh][e]);
+                const float x = __shfl_sync(0xffffffffu, v[0], scatter_owner<NV>(r * G + hh));
+                if (lane == t * kBattRowsPerWarp + r && warp * kBattRowsPerWarp + r < rows) smine[hh] = x * a.scale;
             }
+    }
+    // softmax over this warp's rows, one per lane
+    float pm_[G], pl_[G], pr[G];
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+        const float mx = warp_max(smine[hh]);
+        pr[hh] = mx == -INFINITY ? 0.f : expf(smine[hh] - mx);
+        pm_[hh] = mx;
+        pl_[hh] = warp_sum(pr[hh]);
+    }
+    // pass 2: P.V
+    float acc[G][DPL];
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) acc[hh][e] = 0.f;
+    for (int t = nT; t < total && ok; ++t) {
+        const int slot = t % kBattSlots;
+        if (!mbar_wait_bounded(&full[slot], (uint32_t)(t / kBattSlots) & 1u)) {
+            ok = false;
+            break;
         }
-        if (!ok) {
-            // let every copy issued land before the ring is reused or the CTA leaves
-            if (tid == 0) {
-                atomicOr(a.status, DEV_ERR_WAIT_TIMEOUT);
-                for (int k = 0; k < kBattSlots; ++k) {
-                    int last = -1;
-                    for (int t = 0; t < issued; ++t)
-                        if (t % kBattSlots == k) last = t;
-                    if (last >= 0) (void)mbar_wait_bounded(&full[k], (uint32_t)(last / kBattSlots) & 1u, 10000000ull);
+        const KT *tile = reinterpret_cast<const KT *>(ring + (size_t)slot * kTileBytes);
+        const int i = t - nT;
+        const int rows = rows_c - i * kBattTile < kBattTile ? rows_c - i * kBattTile : kBattTile;
+#pragma unroll
+        for (int r = 0; r < kBattRowsPerWarp; ++r) {
+            const int jj = warp * kBattRowsPerWarp + r;
+            if (jj < rows) {
+                float vf[DPL];
+                tile_row<DPL, HD>(tile, jj, lane, true, vf);
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) {
+                    const float pj = __shfl_sync(0xffffffffu, pr[hh], i * kBattRowsPerWarp + r);
+#pragma unroll
+                    for (int e = 0; e < DPL; ++e) acc[hh][e] = fmaf(pj, vf[e], acc[hh][e]);
                 }
             }
-            __syncthreads();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+    if (!ok) {
+        if (lane == 0) atomicOr(a.status, DEV_ERR_WAIT_TIMEOUT);
+        *reinterpret_cast<volatile int *>(flag) = 1;
+    }
+    // combine the warps and the new position into the chunk's record (the ring is
+    // idle once every tile was consumed)
+    named_sync(1, NC);
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+        float *rw = red + ((size_t)warp * G + hh) * RS;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) rw[lane * DPL + e] = acc[hh][e];
+        if (lane == 0) {
+            rw[HD] = pm_[hh];
+            rw[HD + 1] = pl_[hh];
+        }
+    }
+    const int nrec = holds_new ? kBattConsumers + 1 : kBattConsumers;
+    if (holds_new && warp == 0) {
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+            float d = 0.f;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) d = fmaf(qr[hh][e], kn[lane * DPL + e], d);
+            d = warp_sum(d) * a.scale;
+            float *rw = red + ((size_t)kBattConsumers * G + hh) * RS;
+            for (int i = lane; i < HD; i += 32) rw[i] = vn[i];
+            if (lane == 0) {
+                rw[HD] = d;
+                rw[HD + 1] = 1.f;
+            }
+        }
+    }
+    named_sync(1, NC);
+    const int nchunks_max = batch_attn_max_chunks(a.S);
+    float *prec = a.partial + ((size_t)pair * nchunks_max + c) * G * RS;   // this chunk's record
+    const size_t obase = (size_t)b * a.qh * HD + (size_t)g * G * HD;
+    for (int idx = tid; idx < G * RS; idx += NC) {
+        const int hh = idx / RS, d = idx - hh * RS;
+        float M = -INFINITY;
+        for (int w = 0; w < nrec; ++w) M = fmaxf(M, red[((size_t)w * G + hh) * RS + HD]);
+        float val;
+        if (d == HD) {
+            val = M;
         } else {
-            // the warps' partial outputs, summed through the (now idle) ring
-#pragma unroll
-            for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-                for (int e = 0; e < DPL; ++e) red[((size_t)warp * G + hh) * HD + lane * DPL + e] = acc[hh][e];
-            __syncthreads();
-            for (int idx = tid; idx < G * HD; idx += kBattThreads) {
-                float v = 0.f;
-#pragma unroll
-                for (int w = 0; w < kBattWarps; ++w) v += red[(size_t)w * G * HD + idx];
-                po[idx] = v;
+            float acc2 = 0.f;
+            for (int w = 0; w < nrec; ++w) {
+                const float *rw = red + ((size_t)w * G + hh) * RS;
+                const float wt = rw[HD] == -INFINITY ? 0.f : expf(rw[HD] - M);
+                acc2 = fmaf(rw[d], wt, acc2);   // d == HD + 1: the sums
             }
+            val = acc2;
+        }
+        if (nC == 1) {
+            red[(size_t)(kBattConsumers + 1) * G * RS + idx] = val;   // single chunk: finish below
+        } else {
+            __stcg(prec + idx, val);
         }
     }
-    if (!active || !ok) {
-        for (int i = tid; i < G * HD; i += kBattThreads) po[i] = 0.f;
-        for (int hh = tid; hh < G; hh += kBattThreads) {
-            pm[hh] = -INFINITY;
-            pl[hh] = 0.f;
-        }
-    }
-
-    cluster_sync();
-    if (valid) {
-        const int per = G * HD / kAttnMaxSplits;
-        const size_t obase = (size_t)b * a.qh * HD + (size_t)g * G * HD;
-        for (int i = tid; i < per; i += kBattThreads) {
-            const int idx = s * per + i;
-            const int hh = idx / HD;
-            float m_t[kAttnMaxSplits], M = -INFINITY;
-#pragma unroll
-            for (int t = 0; t < kAttnMaxSplits; ++t) {
-                m_t[t] = t < nsplit ? ld_cluster_f32(cluster_map(pm + hh, t)) : -INFINITY;
-                M = fmaxf(M, m_t[t]);
-            }
-            float num = 0.f, den = 0.f;
-#pragma unroll
-            for (int t = 0; t < kAttnMaxSplits; ++t) {
-                if (t < nsplit) {
-                    const float w = expf(m_t[t] - M);
-                    num = fmaf(ld_cluster_f32(cluster_map(po + idx, t)), w, num);
-                    den = fmaf(ld_cluster_f32(cluster_map(pl + hh, t)), w, den);
-                }
-            }
-            const float o = num / den;
+    if (nC == 1) {
+        named_sync(1, NC);
+        const float *fin = red + (size_t)(kBattConsumers + 1) * G * RS;
+        for (int idx = tid; idx < G * HD; idx += NC) {
+            const int hh = idx / HD, d = idx - hh * HD;
+            const float o = fin[hh * RS + d] / fin[hh * RS + HD + 1];
             const __nv_bfloat16 h = __float2bfloat16_rn(o);
             a.out_hi[obase + idx] = h;
             a.out_lo[obase + idx] = __float2bfloat16_rn(o - __bfloat162float(h));
         }
+        return;
     }
-    cluster_sync();
+    // the last chunk of the pair to finish merges every chunk's record, in order
+    __threadfence();
+    named_sync(1, NC);
+    if (tid == 0) {
+        const int done = atomicAdd(&a.counter[pair], 1);
+        flag[1] = done == nC - 1;
+        if (done == nC - 1) a.counter[pair] = 0;
+    }
+    named_sync(1, NC);
+    if (!flag[1]) return;
+    __threadfence();
+    const float *p0 = a.partial + (size_t)pair * nchunks_max * G * RS;
+    for (int idx = tid; idx < G * HD; idx += NC) {
+        const int hh = idx / HD, d = idx - hh * HD;
+        float M = -INFINITY;
+        for (int k = 0; k < nC; ++k) M = fmaxf(M, __ldcg(p0 + ((size_t)k * G + hh) * RS + HD));
+        float num = 0.f, den = 0.f;
+        for (int k = 0; k < nC; ++k) {
+            const float *rk = p0 + ((size_t)k * G + hh) * RS;
+            const float mk = __ldcg(rk + HD);
+            const float wt = mk == -INFINITY ? 0.f : expf(mk - M);
+            num = fmaf(__ldcg(rk + d), wt, num);
+            den = fmaf(__ldcg(rk + HD + 1), wt, den);
+        }
+        const float o = num / den;
+        const __nv_bfloat16 h = __float2bfloat16_rn(o);
+        a.out_hi[obase + idx] = h;
+        a.out_lo[obase + idx] = __float2bfloat16_rn(o - __bfloat162float(h));
+    }
 }
 
 // ---- RMSNorm + hi/lo split, one CTA per row (optional embedding gather first)
@@ -473,10 +502,12 @@ BattFn batt_fn(int hd, int group) {
 
 }  // namespace
 
-size_t batch_attention_smem_bytes(int hd, int group, int chunk_max) {
-    // ring, q heads, k, v, cos/sin, scores, split output, split max/sum, barriers
-    return (size_t)kBattSlots * kBattTile * hd * 2 + (size_t)group * hd * 4 + 3 * (size_t)hd * 4 +
-           (size_t)group * chunk_max * 4 + (size_t)group * hd * 4 + 2 * (size_t)group * 4 + 8 + kBattSlots * 8;
+size_t batch_attention_smem_bytes(int hd, int group) {
+    // ring (holds the records of the warps, the new position and the chunk at the
+    // end), q heads, k, v, cos/sin, barriers, flags
+    const size_t ring = (size_t)kBattSlots * kBattTile * hd * 2;
+    const size_t red = (size_t)(kBattConsumers + 2) * group * (hd + 2) * 4;
+    return (ring > red ? ring : red) + (size_t)group * hd * 4 + 3 * (size_t)hd * 4 + 2 * kBattSlots * 8 + 16;
 }
 
 bool batch_attention_supported(int hd, int group) { return batt_fn(hd, group) != nullptr; }
@@ -492,23 +523,12 @@ cudaError_t batch_kernels_init() {
 }
 
 cudaError_t launch_batch_attention(int hd, int B, const BatchAttnArgs &a, cudaStream_t s) {
-    const size_t smem = batch_attention_smem_bytes(hd, a.qh / a.kvh, a.chunk_max);
+    const size_t smem = batch_attention_smem_bytes(hd, a.qh / a.kvh);
     const BattFn fn = a.qh % a.kvh ? nullptr : batt_fn(hd, a.qh / a.kvh);
-    if (!fn || smem > 160 * 1024) return cudaErrorInvalidValue;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.kvh, kAttnMaxSplits, B);
-    cfg.blockDim = dim3(kBattThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = 1;
-    at[0].val.clusterDim.y = kAttnMaxSplits;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    void *args[1] = {const_cast<BatchAttnArgs *>(&a)};
-    return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(fn), args);
+    if (!fn || smem > 160 * 1024 || !a.partial || !a.counter) return cudaErrorInvalidValue;
+    // chunk-major order: every pair's first chunk, then every pair's second, ...
+    fn<<<batch_attn_max_chunks(a.S) * B * a.kvh, kBattThreads, smem, s>>>(a);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_norm_split(const NormSplitArgs &a, int rows, cudaStream_t s) {

@@ -254,22 +254,20 @@ struct BatchAttnArgs {
     void *kv;                      // [B][n_layers][2][kvh][S][hd] bf16
     size_t stream_elems;           // elements of one stream's cache
     size_t layer_elems;            // offset of this layer within a stream (elements)
-    int S, qh, kvh, chunk_max;
+    int S, qh, kvh;
     const int *pos;                // [B] position written by this step (attended length pos + 1)
     __nv_bfloat16 *out_hi, *out_lo;// [B][qh * hd] attention output as bf16 parts
+    float *partial;                // [B * kvh][S / kBattChunk][G][hd + 2] chunk results
+    int *counter;                  // [B * kvh] chunks done, zero at rest
     int *status;
 };
 
-// Positions per attention split of the batched path: the attended length L divided
-// evenly over kAttnMaxSplits splits (a function of L only), so every split of a
-// cluster has work once L >= 57.
-__host__ __device__ inline int batch_attn_chunk(int L) { return (L + kAttnMaxSplits - 1) / kAttnMaxSplits; }
-__host__ __device__ inline int batch_attn_splits(int L) {
-    const int c = batch_attn_chunk(L);
-    return (L + c - 1) / c;
-}
+// The batched attention works in chunks of kBattChunk cached positions: one CTA per
+// (stream, kv group, chunk); the chunks of a pair are merged by the last of them.
+constexpr int kBattChunk = 256;
+__host__ __device__ inline int batch_attn_max_chunks(int S) { return (S + kBattChunk - 1) / kBattChunk; }
 
-size_t batch_attention_smem_bytes(int hd, int group, int chunk_max);
+size_t batch_attention_smem_bytes(int hd, int group);
 bool batch_attention_supported(int hd, int group);   // head_dim 64/128, 1, 2, 4 or 8 q heads per kv head
 cudaError_t batch_kernels_init();   // call before any capture
 cudaError_t launch_batch_attention(int hd, int B, const BatchAttnArgs &a, cudaStream_t s);
