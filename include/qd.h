@@ -349,6 +349,19 @@ qd_status qd_batch_set_stream(qd_batch_handle b, int stream, const void *kv_dev,
  * QD_EKVFULL (a stream would pass smax; checked before any work). */
 qd_status qd_batch_decode(qd_batch_handle b, int n_steps, const int32_t *force_dev, int32_t *ids_dev);
 
+/* qd_batch_prefill -- (re)start ns streams (indices in HOST int[ns], distinct) from a
+ * prompt of n positions each: embeds_dev (DEVICE fp32 [ns][n][hidden]).  All ns x n
+ * positions go through each layer together: the projections and the MLP as tensor-core
+ * GEMMs over ns x n tokens, causal attention on the tensor cores; every position's K
+ * and V are written to its stream's cache.  The head runs on each stream's last
+ * position; its argmax (EOS mask, the emitted set is empty) goes to first_ids_dev
+ * (DEVICE int32 [ns]) and becomes the stream's next input token, at position n; its
+ * raw logits go to the stream's row of the qd_batch_get_logits tap.
+ * Queued on the batch's stream; returns after the launches are queued.  Errors:
+ * QD_EINVAL (streams, n not in [1, smax)), QD_ENOMEM, QD_ECUDA. */
+qd_status qd_batch_prefill(qd_batch_handle b, const int *streams, int ns, const float *embeds_dev, int n,
+                           int32_t *first_ids_dev);
+
 /* Synchronise; QD_EDEVICE if a kernel reported an error (bounded wait, bad id). */
 qd_status qd_batch_sync(qd_batch_handle b);
 

@@ -227,3 +227,98 @@ def test_batch_full_size_sampled_streams():
         assert lrel <= REL_TOL and (margin <= MARGIN or gid == rid), b
     _check_steps(bp, 8)
     bp.close()
+
+
+def _prefill_pair(shape, B, smax, streams, n, seed=0):
+    """GPU batch prefill of `streams` with n N(0,1) positions each, and the oracle's
+    prefill of the same prompts."""
+    import torch
+    import oracle as O
+    import transformer_autoregressive_decode_gb300 as qd
+    from transformer_autoregressive_decode_gb300.torch_io import config_from_shape, upload
+    w = W.model_weights(shape, seed=seed)
+    h = qd.qd_create(upload(w), config_from_shape(shape))
+    bh = qd.qd_batch_create(h, B, smax)
+    prompts = np.stack([W.normal(f"batched/prompt/{s}", (n, shape.hidden), seed) for s in streams])
+    first = torch.empty(len(streams), dtype=torch.int32, device="cuda")
+    qd.qd_batch_prefill(bh, streams, torch.from_numpy(prompts).cuda(), first)
+    qd.qd_batch_sync(bh)
+    logits = torch.empty((B, shape.vocab), dtype=torch.float32, device="cuda")
+    qd.qd_batch_get_logits(bh, logits)
+    refs = []
+    for k, s in enumerate(streams):
+        o = O.Oracle(shape, w, buckets=(smax,))
+        rid, rlog, margin = o.prefill(embeds=prompts[k])
+        refs.append((o, rid, rlog, margin))
+    return qd, h, bh, first.cpu().numpy(), logits.cpu().numpy(), refs
+
+
+def test_batch_prefill_matches_oracle_and_decodes_on():
+    import torch
+    B, smax, n = 4, 256, 100                      # 100 positions: ragged query and key tiles
+    streams = [3, 1]
+    qd, h, bh, first, logits, refs = _prefill_pair(TALKER2, B, smax, streams, n)
+    s = TALKER2
+    for k, st in enumerate(streams):
+        o, rid, rlog, margin = refs[k]
+        assert rel_l2(logits[st], rlog) <= REL_TOL
+        if margin > MARGIN:
+            assert first[k] == rid
+        assert qd.qd_batch_get_pos(bh, st) == n
+        # the cache the prefill wrote, every layer, K and V
+        nb = qd.qd_batch_copy_kv(bh, st)
+        buf = torch.empty(nb, dtype=torch.uint8, device="cuda")
+        qd.qd_batch_copy_kv(bh, st, buf)
+        g = buf.view(torch.int16).cpu().numpy().view(np.uint16).reshape(s.n_layers, 2, s.n_kv_heads, smax, s.head_dim)
+        for l in range(s.n_layers):
+            for w_ in range(2):
+                assert rel_l2(_bf16_to_f32(g[l, w_, :, :n]), o.kv(l, w_)) <= REL_TOL, (st, l, w_)
+    # decoding continues from the prefilled caches (the other streams start empty)
+    for b in range(B):
+        if b not in streams:
+            qd.qd_batch_set_stream(bh, b, None, 0, 7)
+    ids = torch.empty((3, B), dtype=torch.int32, device="cuda")
+    force = np.zeros((3, B), np.int32)
+    ref_steps = []
+    for k, st in enumerate(streams):
+        o, rid, _, _ = refs[k]
+        fed = rid
+        out = []
+        for i in range(3):
+            oid, olog, om, _ = o.step(token=fed)
+            out.append((oid, olog, om))
+            force[i, st] = oid
+            fed = oid
+        ref_steps.append(out)
+    # first step's input is the prefill's own argmax (equal to the oracle's when the margin allows)
+    qd.qd_batch_decode(bh, 3, ids, torch.from_numpy(force).cuda())
+    qd.qd_batch_sync(bh)
+    got = ids.cpu().numpy()
+    for k, st in enumerate(streams):
+        if refs[k][3] > MARGIN:                   # the fed first id agrees with the oracle's
+            for i in range(3):
+                oid, _, om = ref_steps[k][i]
+                if om > MARGIN:
+                    assert got[i, st] == oid, (st, i)
+    qd.qd_batch_destroy(bh)
+    qd.qd_destroy(h)
+    for o, *_ in refs:
+        o.close()
+
+
+@pytest.mark.slow
+def test_batch_prefill_full_size_two_streams():
+    """The 28-layer Talker prefilling 512 positions on two of the eight prompt streams
+    of the prefill workload (the oracle runs those two)."""
+    B, smax, n = W.BATCH_PREFILL[0], W.BATCH_SMAX, W.BATCH_PREFILL[1]
+    streams = [0, 5]
+    qd, h, bh, first, logits, refs = _prefill_pair(W.TALKER, B, smax, streams, n)
+    for k, st in enumerate(streams):
+        o, rid, rlog, margin = refs[k]
+        assert rel_l2(logits[st], rlog) <= REL_TOL
+        if margin > MARGIN:
+            assert first[k] == rid
+    qd.qd_batch_destroy(bh)
+    qd.qd_destroy(h)
+    for o, *_ in refs:
+        o.close()

@@ -36,7 +36,7 @@ EXPORTS = ("qd_create", "qd_destroy", "qd_reset", "qd_prefill", "qd_decode_step"
            "qd_status_string", "qd_head_argmax_noalloc", "qd_frame_create", "qd_frame_destroy",
            "qd_frame_generate", "qd_frame_set_graphs", "qd_gemm_bf16", "qd_batch_create", "qd_batch_destroy",
            "qd_batch_set_stream", "qd_batch_decode", "qd_batch_sync", "qd_batch_get_logits", "qd_batch_copy_kv",
-           "qd_batch_get_pos", "qd_batch_get_launch_count", "qd_batch_set_graphs", "qd_batch_time_kernel")
+           "qd_batch_get_pos", "qd_batch_get_launch_count", "qd_batch_set_graphs", "qd_batch_time_kernel", "qd_batch_prefill")
 
 
 class qd_config(ctypes.Structure):
@@ -95,6 +95,7 @@ _SIGS = {
     "qd_batch_get_launch_count": ([_vp, _P(_i64), _P(_i32)], _i32),
     "qd_batch_set_graphs": ([_vp, _i32], _i32),
     "qd_batch_time_kernel": ([_vp, _i32, _i32, _P(ctypes.c_float)], _i32),
+    "qd_batch_prefill": ([_vp, _vp, _i32, _vp, _i32, _vp], _i32),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -420,3 +421,12 @@ def qd_batch_time_kernel(b: BatchHandle, which: int, reps: int) -> float:
     ms = ctypes.c_float(0.0)
     _check(b.model, _lib.qd_batch_time_kernel(b.b, int(which), int(reps), ctypes.byref(ms)))
     return ms.value
+
+
+def qd_batch_prefill(b: BatchHandle, streams, embeds_dev, first_ids_dev):
+    """streams: host ints; embeds_dev: device fp32 [ns, n, hidden]; first_ids_dev: device int32 [ns]."""
+    arr = np.ascontiguousarray(np.asarray(streams, dtype=np.int32))
+    ns, n = int(embeds_dev.shape[0]), int(embeds_dev.shape[1])
+    if len(arr) != ns:
+        raise ValueError("one stream index per prompt")
+    _check(b.model, _lib.qd_batch_prefill(b.b, arr.ctypes.data, ns, _ptr(embeds_dev), n, _ptr(first_ids_dev)))

@@ -122,6 +122,15 @@ struct qd_batch {
     bool use_graphs = true;
     long long launches = 0;
     int kernels_per_step = 0;
+    // prefill scratch, sized for the largest prefill so far (tokens)
+    void *pf_arena = nullptr;
+    size_t pf_tokens = 0, pf_ns = 0, pf_part_cap = 0, pf_tiles_cap = 0;
+    float *pf_partial = nullptr;   // split-K partials of the prefill GEMMs
+    int *pf_counters = nullptr;    // their tile counters, zero at rest
+    float *pf_x = nullptr, *pf_qkv = nullptr, *pf_last = nullptr, *pf_logits = nullptr;
+    __nv_bfloat16 *pf_xh = nullptr, *pf_xl = nullptr, *pf_ah = nullptr, *pf_al = nullptr, *pf_qh = nullptr,
+                  *pf_ql = nullptr;
+    int *pf_streams = nullptr;
 };
 
 namespace {
@@ -268,6 +277,185 @@ qd_status enqueue_batch_kernel(qd_batch *b, int which, cudaStream_t s) {
     return QD_OK;
 }
 
+// The five contractions of a prefill of ns streams x n positions.
+bool prefill_plans(const qd_model *m, int ns, int n, TcGemmPlan *p) {
+    const qd_config &c = m->cfg;
+    const int h = c.hidden, T = ns * n;
+    return tc_gemm_plan(m->q_dim() + 2 * m->kv_dim(), h, T, m->num_sms, &p[0]) &&
+           tc_gemm_plan(h, m->q_dim(), T, m->num_sms, &p[1]) && tc_gemm_plan(2 * c.ffn, h, T, m->num_sms, &p[2]) &&
+           tc_gemm_plan(h, c.ffn, T, m->num_sms, &p[3]) && tc_gemm_plan(c.vocab, h, ns, m->num_sms, &p[4]);
+}
+
+// Prefill scratch for ns streams of n positions (grown, never shrunk).
+qd_status ensure_prefill_scratch(qd_batch *b, int ns, int n) {
+    qd_model *m = b->m;
+    const qd_config &c = m->cfg;
+    const size_t T = (size_t)ns * n;
+    TcGemmPlan plans[5];
+    if (!prefill_plans(m, ns, n, plans)) return fail(m, QD_EUNSUPPORTED, "prefill GEMM shapes");
+    size_t part = 1, tiles = 1;
+    for (const TcGemmPlan &p : plans) {
+        part = std::max(part, p.partial_floats);
+        tiles = std::max(tiles, (size_t)p.row_tiles * p.tok_tiles);
+    }
+    if (b->pf_arena && T <= b->pf_tokens && (size_t)ns <= b->pf_ns && part <= b->pf_part_cap &&
+        tiles <= b->pf_tiles_cap)
+        return QD_OK;
+    if (b->pf_arena) {
+        CU(cudaStreamSynchronize(b->ls));
+        cudaFree(b->pf_arena);
+        b->pf_arena = nullptr;
+    }
+    const int h = c.hidden, rows_qkv = m->q_dim() + 2 * m->kv_dim();
+    const size_t kmax = std::max({(size_t)h, (size_t)m->q_dim(), (size_t)c.ffn});
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off = (off + bytes + kAlign - 1) / kAlign * kAlign;
+        return o;
+    };
+    const size_t o_x = take(T * h * 4), o_qkv = take(T * rows_qkv * 4), o_xh = take(T * kmax * 2),
+                 o_xl = take(T * kmax * 2), o_ah = take(T * c.ffn * 2), o_al = take(T * c.ffn * 2),
+                 o_qh = take(T * m->q_dim() * 2), o_ql = take(T * m->q_dim() * 2), o_last = take((size_t)ns * h * 4),
+                 o_lg = take((size_t)ns * c.vocab * 4), o_st = take((size_t)ns * 4), o_part = take(part * 4),
+                 o_cnt = take(tiles * 8);
+    void *p = nullptr;
+    CU(cudaMalloc(&p, off));
+    uint8_t *A = static_cast<uint8_t *>(p);
+    b->pf_arena = p;
+    b->pf_tokens = T;
+    b->pf_ns = ns;
+    b->pf_part_cap = part;
+    b->pf_tiles_cap = tiles;
+    b->pf_partial = reinterpret_cast<float *>(A + o_part);
+    b->pf_counters = reinterpret_cast<int *>(A + o_cnt);
+    CU(cudaMemsetAsync(b->pf_counters, 0, tiles * 8, b->ls));
+    b->pf_x = reinterpret_cast<float *>(A + o_x);
+    b->pf_qkv = reinterpret_cast<float *>(A + o_qkv);
+    b->pf_xh = reinterpret_cast<__nv_bfloat16 *>(A + o_xh);
+    b->pf_xl = reinterpret_cast<__nv_bfloat16 *>(A + o_xl);
+    b->pf_ah = reinterpret_cast<__nv_bfloat16 *>(A + o_ah);
+    b->pf_al = reinterpret_cast<__nv_bfloat16 *>(A + o_al);
+    b->pf_qh = reinterpret_cast<__nv_bfloat16 *>(A + o_qh);
+    b->pf_ql = reinterpret_cast<__nv_bfloat16 *>(A + o_ql);
+    b->pf_last = reinterpret_cast<float *>(A + o_last);
+    b->pf_logits = reinterpret_cast<float *>(A + o_lg);
+    b->pf_streams = reinterpret_cast<int *>(A + o_st);
+    return QD_OK;
+}
+
+// Every launch of a prefill of ns streams x n positions, on the batch's stream.
+qd_status enqueue_prefill(qd_batch *b, int ns, int n, int32_t *first_ids) {
+    qd_model *m = b->m;
+    const qd_config &c = m->cfg;
+    const int h = c.hidden, qd_ = m->q_dim(), rows_qkv = qd_ + 2 * m->kv_dim();
+    const int T = ns * n;
+    cudaStream_t s = b->ls;
+    TcGemmPlan plans[5];
+    if (!prefill_plans(m, ns, n, plans)) return fail(m, QD_EUNSUPPORTED, "prefill GEMM shapes");
+    const TcGemmPlan &p_qkv = plans[0], &p_o = plans[1], &p_gu = plans[2], &p_d = plans[3], &p_head = plans[4];
+    auto gemm = [&](const TcGemmPlan &p, const void *w, const __nv_bfloat16 *xh, const __nv_bfloat16 *xl, int R,
+                    int K, int rows, int mode, float *out, int ldo) -> cudaError_t {
+        TcGemmArgs a = {};
+        a.R = R;
+        a.K = K;
+        a.T = rows;
+        a.mode = mode;
+        a.out = out;
+        a.ldo = ldo;
+        a.act_hi = b->pf_ah;
+        a.act_lo = b->pf_al;
+        a.partial = p.splits > 1 ? b->pf_partial : nullptr;
+        a.tile_counter = b->pf_counters;
+        a.status = b->status;
+        b->launches++;
+        return launch_tc_gemm(p, w, xh, xl, a, s);
+    };
+    auto norm = [&](float *x, int rows, const float *gamma) -> cudaError_t {
+        NormSplitArgs a = {};
+        a.x = x;
+        a.K = h;
+        a.gamma = gamma;
+        a.eps = (float)c.rms_eps;
+        a.hi = b->pf_xh;
+        a.lo = b->pf_xl;
+        a.status = b->status;
+        b->launches++;
+        return launch_norm_split(a, rows, s);
+    };
+    for (int l = 0; l < c.n_layers; ++l) {
+        const Layer &L = m->layers[l];
+        if (norm(b->pf_x, T, L.attn_norm)) return batch_fail(b, QD_ECUDA, "prefill norm launch failed");
+        if (gemm(p_qkv, L.w_qkv, b->pf_xh, b->pf_xl, rows_qkv, h, T, TC_STORE, b->pf_qkv, rows_qkv))
+            return batch_fail(b, QD_ECUDA, "prefill QKV GEMM launch failed");
+        PrefillQkArgs qa = {};
+        qa.qkv = b->pf_qkv;
+        qa.qkv_ld = rows_qkv;
+        qa.n = n;
+        qa.qh = c.n_q_heads;
+        qa.kvh = c.n_kv_heads;
+        qa.q_gamma = c.qk_norm ? L.q_norm : nullptr;
+        qa.k_gamma = c.qk_norm ? L.k_norm : nullptr;
+        qa.eps = (float)c.rms_eps;
+        qa.rope_cos = b->rope_cos;
+        qa.rope_sin = b->rope_sin;
+        qa.kv = b->kv;
+        qa.stream_elems = b->stream_elems;
+        qa.layer_elems = (size_t)l * 2 * c.n_kv_heads * b->S * c.head_dim;
+        qa.S = b->S;
+        qa.streams = b->pf_streams;
+        qa.q_hi = b->pf_qh;
+        qa.q_lo = b->pf_ql;
+        b->launches++;
+        if (launch_prefill_qk(c.head_dim, ns, qa, s)) return batch_fail(b, QD_ECUDA, "prefill q/k launch failed");
+        PrefillAttnArgs fa = {};
+        fa.q_hi = b->pf_qh;
+        fa.q_lo = b->pf_ql;
+        fa.kv = b->kv;
+        fa.stream_elems = b->stream_elems;
+        fa.layer_elems = qa.layer_elems;
+        fa.S = b->S;
+        fa.n = n;
+        fa.qh = c.n_q_heads;
+        fa.kvh = c.n_kv_heads;
+        fa.scale = (float)(1.0 / std::sqrt((double)c.head_dim));
+        fa.streams = b->pf_streams;
+        fa.out_hi = b->pf_xh;
+        fa.out_lo = b->pf_xl;
+        fa.status = b->status;
+        b->launches++;
+        if (launch_prefill_attention(c.head_dim, ns, fa, s))
+            return batch_fail(b, QD_ECUDA, "prefill attention launch failed");
+        if (gemm(p_o, L.w_o, b->pf_xh, b->pf_xl, h, qd_, T, TC_RESIDUAL, b->pf_x, h))
+            return batch_fail(b, QD_ECUDA, "prefill O GEMM launch failed");
+        if (norm(b->pf_x, T, L.mlp_norm)) return batch_fail(b, QD_ECUDA, "prefill norm launch failed");
+        if (gemm(p_gu, L.w_gu, b->pf_xh, b->pf_xl, 2 * c.ffn, h, T, TC_SWIGLU, nullptr, c.ffn))
+            return batch_fail(b, QD_ECUDA, "prefill gate/up GEMM launch failed");
+        if (gemm(p_d, L.w_d, b->pf_ah, b->pf_al, h, c.ffn, T, TC_RESIDUAL, b->pf_x, h))
+            return batch_fail(b, QD_ECUDA, "prefill down GEMM launch failed");
+    }
+    // the head on each stream's last position
+    b->launches++;
+    if (launch_gather_last(b->pf_x, n, h, ns, b->pf_last, s)) return batch_fail(b, QD_ECUDA, "gather launch failed");
+    if (norm(b->pf_last, ns, m->final_norm)) return batch_fail(b, QD_ECUDA, "prefill norm launch failed");
+    if (gemm(p_head, m->heads[0], b->pf_xh, b->pf_xl, c.vocab, h, ns, TC_STORE, b->pf_logits, c.vocab))
+        return batch_fail(b, QD_ECUDA, "prefill head GEMM launch failed");
+    PrefillFinishArgs fin = {};
+    fin.logits = b->pf_logits;
+    fin.V = c.vocab;
+    fin.eos = c.eos_mask_id;
+    fin.streams = b->pf_streams;
+    fin.n = n;
+    fin.first_ids = first_ids;
+    fin.logits_out = b->logits;
+    fin.tokens = b->tokens;
+    fin.pos = b->pos;
+    fin.status = b->status;
+    b->launches++;
+    if (launch_prefill_finish(fin, ns, s)) return batch_fail(b, QD_ECUDA, "prefill finish launch failed");
+    return QD_OK;
+}
+
 qd_status run_batch_step(qd_batch *b) {
     qd_model *m = b->m;
     if (!b->use_graphs) return enqueue_batch_step(b, b->ls);
@@ -293,6 +481,7 @@ void destroy_batch(qd_batch *b) {
     if (!b) return;
     if (b->ls) cudaStreamSynchronize(b->ls);
     if (b->graph) cudaGraphExecDestroy(b->graph);
+    if (b->pf_arena) cudaFree(b->pf_arena);
     if (b->arena) cudaFree(b->arena);
     if (b->kv) cudaFree(b->kv);
     if (b->ls) cudaStreamDestroy(b->ls);
@@ -345,7 +534,7 @@ qd_status qd_batch_create(qd_handle model, int n_streams, int smax, qd_batch_han
         delete b;
         return fail(m, QD_EUNSUPPORTED, "smax %d too long for the attention tile", smax);
     }
-    if (tc_gemm_init() != cudaSuccess || batch_kernels_init() != cudaSuccess) {
+    if (tc_gemm_init() != cudaSuccess || batch_kernels_init() != cudaSuccess || prefill_kernels_init() != cudaSuccess) {
         delete b;
         return fail(m, QD_ECUDA, "tensor-core GEMM or attention kernel setup failed");
     }
@@ -480,6 +669,41 @@ qd_status qd_batch_decode(qd_batch_handle b, int n_steps, const int32_t *force_d
         b->launches += b->kernels_per_step;
     }
     for (int i = 0; i < b->B; ++i) b->h_pos[i] += n_steps;
+    batch_leave(b);
+    return QD_OK;
+}
+
+qd_status qd_batch_prefill(qd_batch_handle b, const int *streams, int ns, const float *embeds_dev, int n,
+                           int32_t *first_ids_dev) {
+    if (!b) return QD_EINVAL;
+    qd_model *m = b->m;
+    const qd_config &c = m->cfg;
+    if (ns < 1 || ns > b->B || !streams) return fail(m, QD_EINVAL, "ns %d out of range", ns);
+    if (n < 1 || n >= b->S) return fail(m, QD_EINVAL, "n %d must be in [1, smax)", n);
+    std::vector<char> seen(b->B, 0);
+    for (int i = 0; i < ns; ++i) {
+        if (streams[i] < 0 || streams[i] >= b->B || seen[streams[i]])
+            return fail(m, QD_EINVAL, "stream list: index %d invalid or repeated", streams[i]);
+        seen[streams[i]] = 1;
+    }
+    if (!is_device_ptr(embeds_dev) || !is_device_ptr(first_ids_dev))
+        return fail(m, QD_EINVAL, "embeds_dev and first_ids_dev must be device pointers");
+    if ((size_t)ns * n * std::max(m->q_dim(), c.ffn) > ((size_t)1 << 31))
+        return fail(m, QD_EUNSUPPORTED, "prefill too large");
+    batch_enter(b);
+    qd_status st = ensure_prefill_scratch(b, ns, n);
+    if (st) return st;
+    CU(cudaMemcpyAsync(b->pf_streams, streams, (size_t)ns * 4, cudaMemcpyHostToDevice, b->ls));
+    CU(cudaMemcpyAsync(b->pf_x, embeds_dev, (size_t)ns * n * c.hidden * 4, cudaMemcpyDeviceToDevice, b->ls));
+    for (int i = 0; i < ns; ++i)
+        CU(cudaMemsetAsync(b->emitted + (size_t)streams[i] * b->words, 0, (size_t)b->words * 4, b->ls));
+    st = enqueue_prefill(b, ns, n, first_ids_dev);
+    if (st) return st;
+    CU(cudaStreamSynchronize(b->ls));   // the host copy of the stream list is staged
+    for (int i = 0; i < ns; ++i) {
+        b->h_pos[streams[i]] = n;
+        b->h_ready[streams[i]] = 1;
+    }
     batch_leave(b);
     return QD_OK;
 }

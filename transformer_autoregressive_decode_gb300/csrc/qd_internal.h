@@ -307,4 +307,51 @@ struct BatchArgmaxArgs {
 };
 cudaError_t launch_batch_argmax(const BatchArgmaxArgs &a, int B, cudaStream_t s);
 
+// ---------------------------------------------------------------------------------
+// Batched prefill: ns streams x n prompt positions, T = ns * n tokens per contraction.
+// ---------------------------------------------------------------------------------
+struct PrefillQkArgs {
+    const float *qkv;              // [T][qkv_ld] raw projections, token t = stream i * n + position j
+    int qkv_ld, n, qh, kvh;
+    const float *q_gamma, *k_gamma;// [hd] or null
+    float eps;
+    const float *rope_cos, *rope_sin;
+    void *kv;                      // batch caches [B][n_layers][2][kvh][S][hd] bf16
+    size_t stream_elems, layer_elems;
+    int S;
+    const int *streams;            // [ns] cache index of each prompt stream
+    __nv_bfloat16 *q_hi, *q_lo;    // [ns][qh][n][hd]: normalised, rotated q as bf16 parts
+};
+cudaError_t launch_prefill_qk(int hd, int ns, const PrefillQkArgs &a, cudaStream_t s);
+
+struct PrefillAttnArgs {
+    const __nv_bfloat16 *q_hi, *q_lo;  // [ns][qh][n][hd]
+    const void *kv;
+    size_t stream_elems, layer_elems;
+    int S, n, qh, kvh;
+    float scale;
+    const int *streams;
+    __nv_bfloat16 *out_hi, *out_lo;    // [ns * n][qh * hd]
+    int *status;
+};
+bool prefill_attention_supported(int hd, int group);
+cudaError_t prefill_kernels_init();
+cudaError_t launch_prefill_attention(int hd, int ns, const PrefillAttnArgs &a, cudaStream_t s);
+
+// ns rows of x [T][K] at rows (i * n + n - 1): the last position of each prompt stream.
+cudaError_t launch_gather_last(const float *x, int n, int K, int ns, float *out, cudaStream_t s);
+
+struct PrefillFinishArgs {
+    const float *logits;           // [ns][V]
+    int V, eos;
+    const int *streams;            // [ns]
+    int n;
+    int32_t *first_ids;            // [ns]
+    float *logits_out;             // [B][V]: each prompt stream's raw logits, in its row
+    int32_t *tokens;               // [B] next input token of each stream
+    int *pos;                      // [B]
+    int *status;
+};
+cudaError_t launch_prefill_finish(const PrefillFinishArgs &a, int ns, cudaStream_t s);
+
 }  // namespace qd
