@@ -31,12 +31,12 @@ METRIC = "decode tokens/s at 1 GB300; per-step HBM GB/s as fraction of peak"
 # DRAM bytes (read + write) of one decode_step_kernel launch from one ncu capture
 # (profiles/decode_step_kernel_asr.md), at attended length L, for the kernel sources
 # with this digest; null in the JSON line once the sources differ.
-_STEP_TRAFFIC = {"asr": {"digest": "5c88e4b440df103b", "bytes": 224744704 + 3667712, "L": 116}}
-_STEP_SOURCES = ("decode_persistent.cu", "decode_common.cuh", "qd_device.cuh", "qd_internal.h")
+_STEP_TRAFFIC = {"asr": {"digest": "bda1792e61c6e572", "bytes": 224744704 + 3667712, "L": 116}}
+_STEP_SOURCES = ("decode_persistent.cu", "decode_common.cuh", "qd_device.cuh")
 # DRAM bytes of one batch_attn_kernel launch (profiles/batch_attn_kernel_batch64.md) at
 # the initial lengths + 3, for the kernel sources with this digest.
-_BATT_TRAFFIC = {"digest": "c0279d7af4690efa", "bytes": 256616704 + 3798016, "rows": 62239 + 3 * 64}
-_BATT_SOURCES = ("batch_kernels.cu", "decode_common.cuh", "qd_device.cuh", "qd_internal.h")
+_BATT_TRAFFIC = {"digest": "b83df341d1ead2f2", "bytes": 256616704 + 3798016, "rows": 62239 + 3 * 64}
+_BATT_SOURCES = ("batch_kernels.cu", "decode_common.cuh", "qd_device.cuh")
 
 
 def _step_digest(sources=_STEP_SOURCES) -> str:
@@ -729,6 +729,36 @@ def batch_arm(args):
     gemm_tflops = gemm_flops / (gemm_ms / 1e3) / 1e12
     gemm_bytes = s.weight_bytes_per_step()
 
+    # prefill of the workload: 8 prompt streams x 512 N(0,1) positions, timed alone
+    ns_p, n_p = W.BATCH_PREFILL
+    prompts = torch.from_numpy(np.stack([W.normal(f"batched/prompt/{i}", (n_p, s.hidden), 0)
+                                         for i in range(ns_p)])).cuda()
+    first = torch.empty(ns_p, dtype=torch.int32, device="cuda")
+    pstreams = list(range(ns_p))
+    for _ in range(2):
+        qd.qd_batch_prefill(bh, pstreams, prompts, first)
+    qd.qd_batch_sync(bh)
+    pe0, pe1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 5
+    torch.cuda.nvtx.range_push("prefill")
+    pe0.record(stream)
+    for _ in range(reps):
+        qd.qd_batch_prefill(bh, pstreams, prompts, first)
+    pe1.record(stream)
+    torch.cuda.nvtx.range_pop()
+    qd.qd_batch_sync(bh)
+    prefill_ms = pe0.elapsed_time(pe1) / reps
+    T_p = ns_p * n_p
+    pf_gemm_flops = 2.0 * T_p * s.n_layers * layer_params + 2.0 * ns_p * s.vocab * s.hidden
+    pf_attn_flops = 4.0 * s.n_layers * ns_p * s.n_q_heads * s.head_dim * (n_p * (n_p + 1) / 2)
+    pf_tflops = (pf_gemm_flops + pf_attn_flops) / (prefill_ms / 1e3) / 1e12
+    prefill = {"streams": ns_p, "positions": n_p, "ms": prefill_ms, "tokens_per_s": T_p / (prefill_ms / 1e3),
+               "useful_tflop": (pf_gemm_flops + pf_attn_flops) / 1e12, "useful_tflops": pf_tflops,
+               "tensor_frac_useful": pf_tflops / bf16_peak, "bf16_peak_tflops": bf16_peak,
+               "note": "qd_batch_prefill between CUDA events, mean of 5 after 2 warm-up calls; useful flops = "
+                       "2 x tokens x weights (GEMMs) + causal attention; the hi/lo activation split issues two "
+                       "MMAs per useful one"}
+
     # end to end: every step the 64 input tokens come from pinned host memory and the
     # 64 ids go back to it (the ids of a step are the next step's tokens)
     restart()
@@ -789,6 +819,7 @@ def batch_arm(args):
                  "weight_gbs": gemm_bytes / (gemm_ms / 1e3) / 1e9,
                  "note": "useful flops 2 x 64 x weights per step; the hi/lo activation split issues two MMAs per "
                          "useful one; at 64 streams the GEMMs stream their weights (HBM-bound)"},
+        "prefill": prefill,
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(k1 - k0), "kernels_per_step": per_step,
         "clocks": clk,
     }

@@ -693,13 +693,13 @@ qd_status qd_batch_prefill(qd_batch_handle b, const int *streams, int ns, const 
     batch_enter(b);
     qd_status st = ensure_prefill_scratch(b, ns, n);
     if (st) return st;
+    // pageable source: staged by the runtime before the call returns
     CU(cudaMemcpyAsync(b->pf_streams, streams, (size_t)ns * 4, cudaMemcpyHostToDevice, b->ls));
     CU(cudaMemcpyAsync(b->pf_x, embeds_dev, (size_t)ns * n * c.hidden * 4, cudaMemcpyDeviceToDevice, b->ls));
     for (int i = 0; i < ns; ++i)
         CU(cudaMemsetAsync(b->emitted + (size_t)streams[i] * b->words, 0, (size_t)b->words * 4, b->ls));
     st = enqueue_prefill(b, ns, n, first_ids_dev);
     if (st) return st;
-    CU(cudaStreamSynchronize(b->ls));   // the host copy of the stream list is staged
     for (int i = 0; i < ns; ++i) {
         b->h_pos[streams[i]] = n;
         b->h_ready[streams[i]] = 1;
