@@ -330,7 +330,7 @@ typedef struct qd_batch *qd_batch_handle;
 
 /* qd_batch_create -- n_streams streams of at most smax positions (a multiple of 32)
  * over `model`'s weights (bf16, one output head, an embedding table; the model must
- * outlive the batch).  Allocates n_streams caches.  Errors: QD_EINVAL,
+ * outlive the batch).  Allocates n_streams caches, filled with zeros.  Errors: QD_EINVAL,
  * QD_EUNSUPPORTED (shape), QD_ENOMEM, QD_ECUDA; described by qd_last_error(model). */
 qd_status qd_batch_create(qd_handle model, int n_streams, int smax, qd_batch_handle *out);
 qd_status qd_batch_destroy(qd_batch_handle b);

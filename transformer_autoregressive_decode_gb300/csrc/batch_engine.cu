@@ -593,6 +593,8 @@ qd_status qd_batch_create(qd_handle model, int n_streams, int smax, qd_batch_han
         b->att_part = reinterpret_cast<float *>(A + o_ap);
         b->att_count = reinterpret_cast<int *>(A + o_ac);
         check(cudaMemsetAsync(b->arena, 0, off, b->ls), "cudaMemsetAsync");
+        // positions past a stream's length hold zeros or values this library wrote
+        check(cudaMemsetAsync(b->kv, 0, b->stream_elems * 2 * B, b->ls), "cudaMemsetAsync(batch KV caches)");
         check(launch_rope_table(b->rope_cos, b->rope_sin, smax, c.head_dim, c.rope_theta, b->ls), "RoPE table");
         check(cudaStreamSynchronize(b->ls), "cudaStreamSynchronize");
     }
