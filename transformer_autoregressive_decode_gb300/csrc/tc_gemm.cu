@@ -13,11 +13,13 @@
 // products keep ~16 bits of the fp32 activation (x_lo holds the rounding residue of
 // x_hi) while the weights stay bf16.
 //
-// Roles (192 threads): warp 0 lane 0 issues the TMA loads, warp 1 owns the tensor
-// memory and lane 0 issues the MMAs, warps 2-5 read the accumulator (each warp may
-// only touch its quarter of the 128 lanes: warp w reads lanes 32*(w%4)..+31) and run
-// the epilogue.  Two accumulators alternate so a tile's epilogue overlaps the next
-// tile's MMAs.  When the tiles alone cannot fill the GPU (decode: 64 tokens) the K
+// Roles (576 threads): warp 0 lane 0 issues the TMA loads, warp 1 owns the tensor
+// memory and lane 0 issues the MMAs, warps 2-17 read the accumulator and run the
+// epilogue: each warp may only touch its quarter of the 128 lanes (warp w reads lanes
+// 32*(w%4)..+31), so four warps share a quarter, each with a quarter of the columns.
+// The epilogue is a chain of dependent instructions per element (SwiGLU: exp, divide,
+// bf16 split); four warps per scheduler hide its latency.  Two accumulators alternate
+// so a tile's epilogue overlaps the next tile's MMAs.  When the tiles alone cannot fill the GPU (decode: 64 tokens) the K
 // range is split over several CTAs (launched cooperatively, one unit each, so all are
 // resident); each writes its partial tile to scratch, the split CTAs of a tile meet on
 // a counter, and each then sums its share of the tile's columns over all splits in
@@ -37,7 +39,9 @@ namespace qd {
 
 namespace {
 
-constexpr int kTcThreads = 192;
+constexpr int kEpiWarps = 16;                  // epilogue warps: 4 per tensor-memory lane quarter
+constexpr int kEpiGroups = kEpiWarps / 4;      // column groups of a quarter
+constexpr int kTcThreads = (2 + kEpiWarps) * 32;
 constexpr int kBM = 128;                       // weight rows per tile (MMA M)
 constexpr int kBK = 64;                        // K per stage: one 128-byte swizzle row of bf16
 constexpr uint32_t kTileA = kBM * kBK * 2;     // 16 KB
@@ -174,6 +178,25 @@ __device__ __forceinline__ void epi_apply(const TcGemmArgs &a, int t, int r, flo
     }
 }
 
+// Epilogue of tokens t0..t0+n-1 (n <= N) of weight row r.  The residual reads are all
+// issued before any write: a read after a write to the same array cannot be moved
+// ahead of it, so element-by-element read-add-write would queue N round trips.
+template <int N>
+__device__ __forceinline__ void epi_apply_n(const TcGemmArgs &a, int t0, int r, const float *v, int n, int lane) {
+    if (a.mode == TC_RESIDUAL) {
+        float old[N];
+#pragma unroll
+        for (int j = 0; j < N; ++j) old[j] = j < n ? a.out[(size_t)(t0 + j) * a.ldo + r] : 0.f;
+#pragma unroll
+        for (int j = 0; j < N; ++j)
+            if (j < n) a.out[(size_t)(t0 + j) * a.ldo + r] = old[j] + v[j];
+    } else {
+#pragma unroll
+        for (int j = 0; j < N; ++j)
+            if (j < n) epi_apply(a, t0 + j, r, v[j], lane);
+    }
+}
+
 template <int BN>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_xh,
@@ -201,7 +224,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&acc_full[i], 1);
-            mbar_init(&acc_empty[i], 4);
+            mbar_init(&acc_empty[i], kEpiWarps);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -293,9 +316,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_wait_bounded(drain, 0, kDrainNs);
         }
     } else {
-        // ---- epilogue warps 2..5
+        // ---- epilogue warps 2..17
         const int q = warp & 3;                 // tensor-memory lane quarter of this warp
+        const int cg = (warp - 2) >> 2;         // its column group within the quarter
         const int row_in_tile = q * 32 + lane;
+        constexpr int kEpiT = kEpiWarps * 32;
         int local = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++local) {
             const Unit x = unit_of(u, splits, tok_tiles, KC);
@@ -304,26 +329,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             bool ok = true;
             if (lane == 0) ok = role_wait(&acc_full[acc], use & 1, abort_flag, a.status);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-            // all four epilogue warps agree before any of them goes on
-            if (named_sync_or(1, 128, !ok)) break;
+            // all epilogue warps agree before any of them goes on
+            if (named_sync_or(1, kEpiT, !ok)) break;
             tc_fence_after();
             const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
             const int r = x.rt * kBM + row_in_tile;
             if (splits == 1) {
 #pragma unroll 1
-                for (int c0 = 0; c0 < BN; c0 += 16) {
+                for (int c0 = cg * 16; c0 < BN; c0 += 16 * kEpiGroups) {
                     float v[16];
                     tc_ld16(tbase + (uint32_t)c0, v);
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int t = x.nt * BN + c0 + j;
-                        if (t < a.T) epi_apply(a, t, r, v[j], lane);
-                    }
+                    const int t0 = x.nt * BN + c0;
+                    epi_apply_n<16>(a, t0, r, v, a.T - t0 < 16 ? a.T - t0 : 16, lane);
                 }
             } else {
                 float *part = a.partial + (size_t)u * BN * kBM;
 #pragma unroll 1
-                for (int c0 = 0; c0 < BN; c0 += 16) {
+                for (int c0 = cg * 16; c0 < BN; c0 += 16 * kEpiGroups) {
                     float v[16];
                     tc_ld16(tbase + (uint32_t)c0, v);
 #pragma unroll
@@ -338,7 +360,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // are resident), then each sums its share of the tile's columns over every
                 // split, in split order, and runs the epilogue on it.
                 __threadfence();
-                named_sync(1, 128);
+                named_sync(1, kEpiT);
                 int *arrive = a.tile_counter + 2 * x.tile;
                 int *depart = arrive + 1;
                 if (warp == 2 && lane == 0) {
@@ -355,7 +377,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     *is_last = met;
                 }
-                named_sync(1, 128);
+                named_sync(1, kEpiT);
                 const bool met = *is_last != 0;
                 if (met) {
                     __threadfence();
@@ -363,7 +385,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const int c_lo = s_idx * BN / splits, c_hi = (s_idx + 1) * BN / splits;
                     const float *p0 = a.partial + (size_t)x.tile * splits * BN * kBM + row_in_tile;
 #pragma unroll 1
-                    for (int c = c_lo; c < c_hi; c += 4) {
+                    for (int c = c_lo + 4 * cg; c < c_hi; c += 4 * kEpiGroups) {
                         float v[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
                         for (int s2 = 0; s2 < splits; ++s2) {
@@ -372,14 +394,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             for (int j = 0; j < 4; ++j)
                                 if (c + j < c_hi) v[j] += __ldcg(ps + (size_t)(c + j) * kBM);
                         }
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int t = x.nt * BN + c + j;
-                            if (c + j < c_hi && t < a.T) epi_apply(a, t, r, v[j], lane);
-                        }
+                        const int t0 = x.nt * BN + c;
+                        int n = c_hi - c < 4 ? c_hi - c : 4;
+                        if (a.T - t0 < n) n = a.T - t0;
+                        epi_apply_n<4>(a, t0, r, v, n, lane);
                     }
                 }
-                named_sync(1, 128);
+                named_sync(1, kEpiT);
                 if (warp == 2 && lane == 0 && met) {
                     // the last CTA to leave puts the tile's counters back at rest
                     if (atomicAdd(depart, 1) == splits - 1) {
