@@ -141,7 +141,8 @@ qd_status batch_fail(qd_batch *b, qd_status st, const char *what) { return fail(
 
 // One tensor-core GEMM of the step over the B streams.
 cudaError_t batch_gemm(qd_batch *b, const TcGemmPlan &p, const void *w, const __nv_bfloat16 *xh,
-                       const __nv_bfloat16 *xl, int R, int K, int mode, float *out, int ldo, cudaStream_t s) {
+                       const __nv_bfloat16 *xl, int R, int K, int mode, float *out, int ldo, cudaStream_t s,
+                       bool pdl = false) {
     TcGemmArgs a = {};
     a.R = R;
     a.K = K;
@@ -154,7 +155,7 @@ cudaError_t batch_gemm(qd_batch *b, const TcGemmPlan &p, const void *w, const __
     a.partial = p.splits > 1 ? b->partial : nullptr;
     a.tile_counter = b->counters;
     a.status = b->status;
-    return launch_tc_gemm(p, w, xh, xl, a, s);
+    return launch_tc_gemm(p, w, xh, xl, a, s, pdl);
 }
 
 // Attention arguments of layer l (output: the bf16 parts feeding the O GEMM).
@@ -210,12 +211,12 @@ qd_status enqueue_batch_step(qd_batch *b, cudaStream_t s) {
         }
         a.status = b->status;
         ++n;
-        return launch_norm_split(a, B, s);
+        return launch_norm_split(a, B, s, true);
     };
     auto gemm = [&](const TcGemmPlan &p, const void *w, const __nv_bfloat16 *xh, const __nv_bfloat16 *xl, int R,
                     int K, int mode, float *out, int ldo) -> cudaError_t {
         ++n;
-        return batch_gemm(b, p, w, xh, xl, R, K, mode, out, ldo, s);
+        return batch_gemm(b, p, w, xh, xl, R, K, mode, out, ldo, s, true);
     };
     if (norm(m->layers[0].attn_norm, true)) return batch_fail(b, QD_ECUDA, "norm/embedding launch failed");
     for (int l = 0; l < c.n_layers; ++l) {
@@ -223,7 +224,7 @@ qd_status enqueue_batch_step(qd_batch *b, cudaStream_t s) {
         if (gemm(b->p_qkv, L.w_qkv, b->xh, b->xl, rows_qkv, h, TC_STORE, b->qkv, rows_qkv))
             return batch_fail(b, QD_ECUDA, "QKV GEMM launch failed");
         ++n;
-        if (launch_batch_attention(c.head_dim, B, batch_attn_args(b, l), s))
+        if (launch_batch_attention(c.head_dim, B, batch_attn_args(b, l), s, true))
             return batch_fail(b, QD_ECUDA, "attention launch failed");
         if (gemm(b->p_o, L.w_o, b->xh, b->xl, h, qd_, TC_RESIDUAL, b->x, h))
             return batch_fail(b, QD_ECUDA, "O GEMM launch failed");
@@ -249,7 +250,7 @@ qd_status enqueue_batch_step(qd_batch *b, cudaStream_t s) {
     am.pos = b->pos;
     am.status = b->status;
     ++n;
-    if (launch_batch_argmax(am, B, s)) return batch_fail(b, QD_ECUDA, "argmax launch failed");
+    if (launch_batch_argmax(am, B, s, true)) return batch_fail(b, QD_ECUDA, "argmax launch failed");
     b->kernels_per_step = n;
     return QD_OK;
 }

@@ -26,7 +26,9 @@ namespace {
 // are QK-normed, rotated, rounded to the cache type and appended) are combined into
 // the chunk's (max, sum, output); the last chunk CTA of a (stream, group) to finish
 // merges the chunks in order (flash-decoding merge) and writes the output.  Equal
-// chunks keep the work balanced whatever the lengths; no CTA waits for another.
+// chunks keep the work balanced whatever the lengths; no CTA waits for another.  As a
+// programmatic dependent of the QKV GEMM, the producer starts on the cached rows
+// (written by earlier steps) before the consumers wait for the GEMM's q, k and v.
 constexpr int kBattConsumers = 8;
 constexpr int kBattThreads = (kBattConsumers + 1) * 32;
 constexpr int kBattTile = 32;        // positions per ring slot
@@ -176,6 +178,8 @@ __global__ void __launch_bounds__(kBattThreads, G <= 2 ? 4 : 2) batch_attn_kerne
 
     // ---- consumers: q (and k, v) of the new position, QK-norm and RoPE
     constexpr int NC = kBattConsumers * 32;
+    pdl_wait();
+    pdl_launch_dependents();
     const float *row = a.qkv + (size_t)b * a.qkv_ld;
     for (int m = tid; m < HALF; m += NC) {
         rc[m] = a.rope_cos[(size_t)p * HALF + m];
@@ -393,6 +397,8 @@ constexpr int kRowThreads = 256;
 __global__ void __launch_bounds__(kRowThreads) norm_split_kernel(const NormSplitArgs a) {
     __shared__ float red[kRowThreads / 32];
     __shared__ int sh_tok;
+    pdl_wait();
+    pdl_launch_dependents();
     const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     float *x = a.x + (size_t)b * a.K;
     if (a.table) {
@@ -435,6 +441,8 @@ __global__ void __launch_bounds__(kRowThreads) norm_split_kernel(const NormSplit
 __global__ void __launch_bounds__(kRowThreads) batch_argmax_kernel(const BatchArgmaxArgs a) {
     __shared__ float bv_s[kRowThreads / 32];
     __shared__ int bi_s[kRowThreads / 32];
+    pdl_wait();
+    pdl_launch_dependents();
     const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const float *lg = a.logits + (size_t)b * a.V;
     const uint32_t *em = a.emitted + (size_t)b * a.words;
@@ -522,23 +530,42 @@ cudaError_t batch_kernels_init() {
     return cudaSuccess;
 }
 
-cudaError_t launch_batch_attention(int hd, int B, const BatchAttnArgs &a, cudaStream_t s) {
+// Launch `fn` with `args` on `s`, as a programmatic dependent of the previous kernel
+// in the stream when `pdl` is set.
+cudaError_t launch_ex(const void *fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl, void **args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+cudaError_t launch_batch_attention(int hd, int B, const BatchAttnArgs &a, cudaStream_t s, bool pdl) {
     const size_t smem = batch_attention_smem_bytes(hd, a.qh / a.kvh);
     const BattFn fn = a.qh % a.kvh ? nullptr : batt_fn(hd, a.qh / a.kvh);
     if (!fn || smem > 160 * 1024 || !a.partial || !a.counter) return cudaErrorInvalidValue;
     // chunk-major order: every pair's first chunk, then every pair's second, ...
-    fn<<<batch_attn_max_chunks(a.S) * B * a.kvh, kBattThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    void *args[1] = {const_cast<BatchAttnArgs *>(&a)};
+    return launch_ex(reinterpret_cast<const void *>(fn), dim3(batch_attn_max_chunks(a.S) * B * a.kvh),
+                     dim3(kBattThreads), smem, s, pdl, args);
 }
 
-cudaError_t launch_norm_split(const NormSplitArgs &a, int rows, cudaStream_t s) {
-    norm_split_kernel<<<rows, kRowThreads, 0, s>>>(a);
-    return cudaGetLastError();
+cudaError_t launch_norm_split(const NormSplitArgs &a, int rows, cudaStream_t s, bool pdl) {
+    void *args[1] = {const_cast<NormSplitArgs *>(&a)};
+    return launch_ex(reinterpret_cast<const void *>(norm_split_kernel), dim3(rows), dim3(kRowThreads), 0, s, pdl,
+                     args);
 }
 
-cudaError_t launch_batch_argmax(const BatchArgmaxArgs &a, int B, cudaStream_t s) {
-    batch_argmax_kernel<<<B, kRowThreads, 0, s>>>(a);
-    return cudaGetLastError();
+cudaError_t launch_batch_argmax(const BatchArgmaxArgs &a, int B, cudaStream_t s, bool pdl) {
+    void *args[1] = {const_cast<BatchArgmaxArgs *>(&a)};
+    return launch_ex(reinterpret_cast<const void *>(batch_argmax_kernel), dim3(B), dim3(kRowThreads), 0, s, pdl,
+                     args);
 }
 
 }  // namespace qd

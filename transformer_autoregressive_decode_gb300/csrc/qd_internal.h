@@ -229,8 +229,11 @@ cudaError_t tc_gemm_init();
 // cannot fill the GPU).  False if the shape is not supported.
 bool tc_gemm_plan(int R, int K, int T, int num_sms, TcGemmPlan *p);
 // Launch; w, x_hi, x_lo are device pointers (16-byte aligned, row strides K*2 bytes).
+// pdl: launch as a programmatic dependent of the previous kernel in the stream (the
+// chains of the batched decode step; every kernel of such a chain waits before it
+// reads what its predecessor writes).
 cudaError_t launch_tc_gemm(const TcGemmPlan &p, const void *w, const void *x_hi, const void *x_lo,
-                           const TcGemmArgs &a, cudaStream_t s);
+                           const TcGemmArgs &a, cudaStream_t s, bool pdl = false);
 // x fp32 [n] -> hi = bf16(x), lo = bf16(x - hi)
 cudaError_t launch_split_bf16(const float *x, __nv_bfloat16 *hi, __nv_bfloat16 *lo, size_t n, cudaStream_t s);
 
@@ -270,7 +273,7 @@ __host__ __device__ inline int batch_attn_max_chunks(int S) { return (S + kBattC
 size_t batch_attention_smem_bytes(int hd, int group);
 bool batch_attention_supported(int hd, int group);   // head_dim 64/128, 1, 2, 4 or 8 q heads per kv head
 cudaError_t batch_kernels_init();   // call before any capture
-cudaError_t launch_batch_attention(int hd, int B, const BatchAttnArgs &a, cudaStream_t s);
+cudaError_t launch_batch_attention(int hd, int B, const BatchAttnArgs &a, cudaStream_t s, bool pdl = false);
 
 // Per row b < rows: optionally x[b] = E[tokens[b]] (the token joins stream b's emitted
 // set), then hi/lo bf16 parts of gamma * x[b] / sqrt(mean(x[b]^2) + eps).
@@ -288,7 +291,7 @@ struct NormSplitArgs {
     float *y;                      // optional fp32 copy of the normalised rows
     int *status;
 };
-cudaError_t launch_norm_split(const NormSplitArgs &a, int rows, cudaStream_t s);
+cudaError_t launch_norm_split(const NormSplitArgs &a, int rows, cudaStream_t s, bool pdl = false);
 
 // Per stream b: penalty over its emitted set, EOS mask, argmax (lowest index on ties)
 // of logits[b]; ids and the next input token go through the control block; the
@@ -305,7 +308,7 @@ struct BatchArgmaxArgs {
     int *pos;                      // [B]
     int *status;
 };
-cudaError_t launch_batch_argmax(const BatchArgmaxArgs &a, int B, cudaStream_t s);
+cudaError_t launch_batch_argmax(const BatchArgmaxArgs &a, int B, cudaStream_t s, bool pdl = false);
 
 // ---------------------------------------------------------------------------------
 // Batched prefill: ns streams x n prompt positions, T = ns * n tokens per contraction.

@@ -25,6 +25,10 @@
 // a counter, and each then sums its share of the tile's columns over all splits in
 // split order and runs the epilogue on it, so the result does not depend on timing.
 //
+// Launched as a programmatic dependent of the kernel before it, the producer loads the
+// weight tiles of its first stages (weights are never written) before waiting for that
+// kernel, then the activation tiles; the epilogue waits before it reads or writes.
+//
 // Every wait is bounded (1 s on %globaltimer); on expiry the kernel records
 // DEV_ERR_WAIT_TIMEOUT, every role stops, copies and MMAs in flight are drained, the
 // tensor memory is freed and the kernel returns.
@@ -245,10 +249,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             uint32_t armed = 0, armed_parity = 0;   // per-stage bits: armed at least once / parity of last arming
+            // the weight tiles of the first unit's first stages go out before the wait for
+            // the previous kernel, its activation tiles after it
+            int pre = 0;
+            if ((int)blockIdx.x < units) {
+                const Unit x0 = unit_of(blockIdx.x, splits, tok_tiles, KC);
+                pre = x0.k1 - x0.k0 < C::kStages ? x0.k1 - x0.k0 : C::kStages;
+                for (int i = 0; i < pre; ++i) {
+                    mbar_arrive_expect_tx(&full[i], C::kStage);
+                    tma_load_2d(sm + (size_t)i * C::kStage, &tm_w, (x0.k0 + i) * kBK, x0.rt * kBM, &full[i]);
+                }
+                pdl_wait();
+                pdl_launch_dependents();
+                for (int i = 0; i < pre; ++i) {
+                    uint8_t *st = sm + (size_t)i * C::kStage;
+                    tma_load_2d(st + kTileA, &tm_xh, (x0.k0 + i) * kBK, x0.nt * BN, &full[i]);
+                    tma_load_2d(st + kTileA + C::kTileB, &tm_xl, (x0.k0 + i) * kBK, x0.nt * BN, &full[i]);
+                }
+                armed = (1u << pre) - 1u;
+                stage = pre % C::kStages;
+                phase = pre == C::kStages ? 1u : 0u;
+            } else {
+                pdl_wait();
+                pdl_launch_dependents();
+            }
             for (int u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
                 const Unit x = unit_of(u, splits, tok_tiles, KC);
                 bool ok = true;
-                for (int kc = x.k0; kc < x.k1; ++kc) {
+                for (int kc = x.k0 + (u == (int)blockIdx.x ? pre : 0); kc < x.k1; ++kc) {
                     if (!role_wait(&empty[stage], phase ^ 1, abort_flag, a.status)) {
                         ok = false;
                         break;
@@ -321,6 +349,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int cg = (warp - 2) >> 2;         // its column group within the quarter
         const int row_in_tile = q * 32 + lane;
         constexpr int kEpiT = kEpiWarps * 32;
+        pdl_wait();   // outputs, residuals, scratch and counters may belong to the previous kernel
         int local = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++local) {
             const Unit x = unit_of(u, splits, tok_tiles, KC);
@@ -471,27 +500,35 @@ template <int BN> cudaError_t set_attr() {
 }
 
 template <int BN> cudaError_t launch_bn(const TcGemmPlan &p, const void *w, const void *xh, const void *xl,
-                                        const TcGemmArgs &a, cudaStream_t s) {
+                                        const TcGemmArgs &a, cudaStream_t s, bool pdl) {
     cudaError_t attr = set_attr<BN>();
     if (attr != cudaSuccess) return attr;
     CUtensorMap mw, mh, ml;
     if (!make_map(&mw, w, a.R, a.K, kBM) || !make_map(&mh, xh, a.T, a.K, BN) || !make_map(&ml, xl, a.T, a.K, BN))
         return cudaErrorInvalidValue;
-    if (p.splits == 1) {
+    if (p.splits == 1 && !pdl) {
         tc_gemm_kernel<BN><<<p.grid, kTcThreads, TcCfg<BN>::kSmem, s>>>(mw, mh, ml, a, p.tok_tiles, p.splits,
                                                                           p.units);
         return cudaGetLastError();
     }
     // split-K: the split CTAs of a tile wait for one another, so they must all be
-    // resident; a cooperative launch guarantees it (one unit per CTA, grid <= SMs)
+    // resident.  A cooperative launch guarantees it; as a programmatic dependent (one
+    // unit per CTA, grid <= SMs, one CTA per SM) every CTA has started before any
+    // kernel after it may (each signals only once running), and the kernel before it
+    // only ends, so all of them become resident.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.grid);
     cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = TcCfg<BN>::kSmem;
     cfg.stream = s;
     cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeCooperative;
-    at[0].val.cooperative = 1;
+    if (pdl) {
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
+    } else {
+        at[0].id = cudaLaunchAttributeCooperative;
+        at[0].val.cooperative = 1;
+    }
     cfg.attrs = at;
     cfg.numAttrs = 1;
     int tok_tiles = p.tok_tiles, splits = p.splits, units = p.units;
@@ -526,10 +563,10 @@ bool tc_gemm_plan(int R, int K, int T, int num_sms, TcGemmPlan *p) {
 }
 
 cudaError_t launch_tc_gemm(const TcGemmPlan &p, const void *w, const void *x_hi, const void *x_lo,
-                           const TcGemmArgs &a, cudaStream_t s) {
+                           const TcGemmArgs &a, cudaStream_t s, bool pdl) {
     if (p.splits > 1 && (!a.partial || !a.tile_counter || p.units > p.grid)) return cudaErrorInvalidValue;
     if (a.mode == TC_SWIGLU && (!a.act_hi || !a.act_lo)) return cudaErrorInvalidValue;
-    return p.bn == 64 ? launch_bn<64>(p, w, x_hi, x_lo, a, s) : launch_bn<128>(p, w, x_hi, x_lo, a, s);
+    return p.bn == 64 ? launch_bn<64>(p, w, x_hi, x_lo, a, s, pdl) : launch_bn<128>(p, w, x_hi, x_lo, a, s, pdl);
 }
 
 cudaError_t launch_split_bf16(const float *x, __nv_bfloat16 *hi, __nv_bfloat16 *lo, size_t n, cudaStream_t s) {
