@@ -35,7 +35,7 @@ _STEP_TRAFFIC = {"asr": {"digest": "bda1792e61c6e572", "bytes": 224744704 + 3667
 _STEP_SOURCES = ("decode_persistent.cu", "decode_common.cuh", "qd_device.cuh")
 # DRAM bytes of one batch_attn_kernel launch (profiles/batch_attn_kernel_batch64.md) at
 # the initial lengths + 3, for the kernel sources with this digest.
-_BATT_TRAFFIC = {"digest": "b83df341d1ead2f2", "bytes": 256616704 + 3798016, "rows": 62239 + 3 * 64}
+_BATT_TRAFFIC = {"digest": "cb3ff54f9f27eb8e", "bytes": 256617216 + 4111104, "rows": 62239 + 3 * 64}
 _BATT_SOURCES = ("batch_kernels.cu", "decode_common.cuh", "qd_device.cuh")
 
 
