@@ -307,3 +307,49 @@ def test_persistent_step_equals_per_phase_kernels(shape_name, monkeypatch):
     assert a[0] == b[0]
     assert np.array_equal(a[1], b[1])
     assert np.array_equal(_valid_kv(a[2], s, a[4], a[3]), _valid_kv(b[2], s, b[4], b[3]))
+
+
+@pytest.mark.parametrize("shape_name", ["asr2", "talker2"])
+def test_prompt_prefill_through_batched_kernels_matches_oracle(shape_name):
+    """qd_prefill from embeddings on a bf16 model runs every prompt position at once
+    (tensor-core GEMMs, causal flash attention, then the cache rows are copied into the
+    bucket): its cache, final-norm hidden state and first id against the oracle's
+    position-by-position prefill, and the state it leaves (position, first id) for the
+    decode steps after it; decoding on from it then tracks the oracle."""
+    import torch
+    import oracle as O
+    import transformer_autoregressive_decode_gb300 as qd
+    from transformer_autoregressive_decode_gb300.torch_io import config_from_shape, upload
+    s = {"asr2": W.scaled(W.ASR, n_layers=2, name="asr2"),
+         "talker2": W.scaled(W.TALKER, n_layers=2, name="talker2")}[shape_name]
+    w = W.model_weights(s)
+    e = W.prefill_embeds(s)
+    n = len(e)
+    h = qd.qd_create(upload(w), config_from_shape(s))
+    first = qd.qd_prefill(h, embeds=torch.from_numpy(e).cuda())
+    y = torch.empty(s.hidden, dtype=torch.float32, device="cuda")
+    qd.qd_get_hidden(h, y)
+    pos, smax = qd.qd_get_pos(h)
+    assert pos == n
+    nb = qd.qd_copy_kv(h)
+    kv = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    qd.qd_copy_kv(h, kv)
+    g = kv.cpu().numpy().view(np.uint16).reshape(s.n_layers, 2, s.n_kv_heads, smax, s.head_dim)
+    o = O.Oracle(s, w)
+    rid, rlog, margin = o.prefill(embeds=e)
+    assert margin <= MARGIN or first == rid, (first, rid, margin)
+    assert rel_l2(y.cpu().numpy(), o.hidden()) <= REL_TOL
+    for l in range(s.n_layers):
+        for which in range(2):
+            got = (g[l, which, :, :n].astype(np.uint32) << 16).view(np.float32)
+            assert rel_l2(got, o.kv(l, which)) <= REL_TOL, (l, which)
+    # decode on, teacher-forced with the oracle's ids
+    fed = rid
+    for i in range(6):
+        gid = qd.qd_decode_step(h, token=fed)
+        oid, _, om, _ = o.step(token=fed)
+        assert om <= MARGIN or gid == oid, (i, gid, oid, om)
+        fed = oid
+    assert qd.qd_get_pos(h)[0] == n + 6
+    o.close()
+    qd.qd_destroy(h)

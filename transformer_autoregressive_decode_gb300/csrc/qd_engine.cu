@@ -681,6 +681,9 @@ static void destroy_model(qd_model *m) {
     if (!m) return;
     while (!m->frames.empty()) frame_detach(m->frames.back());
     if (m->ls) cudaStreamSynchronize(m->ls);
+    if (m->pf_batch) qd_batch_destroy(m->pf_batch);
+    for (cudaEvent_t e : m->pf_ev)
+        if (e) cudaEventDestroy(e);
     for (int v = 0; v < 2; ++v)
         for (auto &g : m->graphs[v])
             if (g) cudaGraphExecDestroy(g);
@@ -793,6 +796,19 @@ qd_status qd_prefill(qd_handle h, const int32_t *tokens, const void *embeds, int
     qd_status st = ensure_bucket(m, b);
     if (st) return st;
     m->cur_bucket = b;
+    if (embeds && !m->tap_hidden && !m->tap_logits) {
+        // all positions at once through the batched prefill kernels, where they apply
+        st = model_prefill_batched(m, static_cast<const float *>(embeds), n, head_idx, b);
+        if (st == QD_OK) {
+            m->h_pos = n;
+            m->h_ngen++;
+            m->have_hidden = true;
+            st = sync_and_check(m, first_id);
+            leave(m);
+            return st;
+        }
+        if (st != QD_EUNSUPPORTED) return st;
+    }
     if (tokens) CU(cudaMemcpyAsync(m->stage_tokens, tokens, (size_t)n * 4, cudaMemcpyHostToDevice, m->ls));
     else CU(cudaMemcpyAsync(m->stage_embeds, embeds, (size_t)n * c.hidden * 4, cudaMemcpyDeviceToDevice, m->ls));
     st = set_params(m, tokens ? IN_STAGED_TOKENS : IN_STAGED_EMBEDS, -1, 0, head_idx);

@@ -356,5 +356,10 @@ struct PrefillFinishArgs {
     int *status;
 };
 cudaError_t launch_prefill_finish(const PrefillFinishArgs &a, int ns, cudaStream_t s);
+// After a single-stream prefill run through the batched kernels: the first id becomes
+// the model's last output and joins its id history, the position becomes n, and the
+// batch's error bits join the model's.
+cudaError_t launch_prefill_commit(DevState *st, int32_t *ids, int ids_cap, const int32_t *first, int n,
+                                  const int *batch_status, cudaStream_t s);
 
 }  // namespace qd

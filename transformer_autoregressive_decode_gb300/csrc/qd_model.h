@@ -72,6 +72,9 @@ struct qd_model {
 
     // persistent decode step (one cooperative launch per step)
     bool persistent = false;
+    // prompt prefill through the batched kernels: an internal one-stream batch
+    qd_batch *pf_batch = nullptr;
+    cudaEvent_t pf_ev[2] = {nullptr, nullptr};
     qd::LayerDev *d_layers = nullptr;
     unsigned *barrier = nullptr;
     float *part_o = nullptr, *part_ml = nullptr;
@@ -107,6 +110,10 @@ qd_status sync_and_check(qd_model *m, int *out_id);
 // Unbind a frame generator from both of its models (frame_engine.cu); called when
 // either model is destroyed first.
 void frame_detach(qd_frame *fr);
+// Prefill of n positions from device embeddings through the batched prefill kernels
+// into KV bucket `bucket` (batch_engine.cu); QD_EUNSUPPORTED, with nothing enqueued,
+// where the model or the shapes do not allow it.
+qd_status model_prefill_batched(qd_model *m, const float *embeds_dev, int n, int head_idx, int bucket);
 
 #define CU(call)                                                                                   \
     do {                                                                                           \
