@@ -123,12 +123,11 @@ qd_status qd_reset(qd_handle h);
  * generated id (head 0 for a single-head model, head `head_idx` otherwise).
  * Exactly one of tokens (HOST int32 [n], ids < embed_rows) or embeds (DEVICE
  * fp32 [n, hidden], row-major) is non-NULL.  Prompt ids do not join the emitted
- * set.  The first bucket is the smallest Smax >= n.  Embedding prompts of a bf16
- * model with one head and an embedding table run all positions at once through the
- * batched prefill kernels (tensor-core GEMMs, causal flash attention; an internal
- * one-stream qd_batch holds the scratch and is freed with the model), unless debug
- * taps are set; token prompts and the other models run position by position through
- * the decode step.  Synchronises; first_id is a HOST pointer.  Errors: QD_EINVAL
+ * set.  The first bucket is the smallest Smax >= n.  On a bf16 model with one head
+ * and an embedding table the prompt runs all positions at once through the batched
+ * prefill kernels (tensor-core GEMMs, causal flash attention; an internal one-stream
+ * qd_batch holds the scratch and is freed with the model), unless debug taps are set;
+ * the other models run it position by position through the decode step.  Synchronises; first_id is a HOST pointer.  Errors: QD_EINVAL
  * (n < 1, both/neither inputs, bad id), QD_ESTATE (position != 0: call qd_reset
  * first), QD_EKVFULL (n > last bucket), QD_ECUDA, QD_EDEVICE. */
 qd_status qd_prefill(qd_handle h, const int32_t *tokens, const void *embeds, int n, int head_idx,

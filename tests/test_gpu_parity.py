@@ -309,8 +309,8 @@ def test_persistent_step_equals_per_phase_kernels(shape_name, monkeypatch):
     assert np.array_equal(_valid_kv(a[2], s, a[4], a[3]), _valid_kv(b[2], s, b[4], b[3]))
 
 
-@pytest.mark.parametrize("shape_name", ["asr2", "talker2"])
-def test_prompt_prefill_through_batched_kernels_matches_oracle(shape_name):
+@pytest.mark.parametrize("shape_name,prompt", [("asr2", "embeds"), ("talker2", "embeds"), ("asr2", "tokens")])
+def test_prompt_prefill_through_batched_kernels_matches_oracle(shape_name, prompt):
     """qd_prefill from embeddings on a bf16 model runs every prompt position at once
     (tensor-core GEMMs, causal flash attention, then the cache rows are copied into the
     bucket): its cache, final-norm hidden state and first id against the oracle's
@@ -325,8 +325,12 @@ def test_prompt_prefill_through_batched_kernels_matches_oracle(shape_name):
     w = W.model_weights(s)
     e = W.prefill_embeds(s)
     n = len(e)
+    toks = W.uniform_int(f"{shape_name}/prompt_tokens", n, 0, s.embed_rows - 1).astype(np.int32)
     h = qd.qd_create(upload(w), config_from_shape(s))
-    first = qd.qd_prefill(h, embeds=torch.from_numpy(e).cuda())
+    if prompt == "embeds":
+        first = qd.qd_prefill(h, embeds=torch.from_numpy(e).cuda())
+    else:
+        first = qd.qd_prefill(h, tokens=toks)
     y = torch.empty(s.hidden, dtype=torch.float32, device="cuda")
     qd.qd_get_hidden(h, y)
     pos, smax = qd.qd_get_pos(h)
@@ -336,7 +340,7 @@ def test_prompt_prefill_through_batched_kernels_matches_oracle(shape_name):
     qd.qd_copy_kv(h, kv)
     g = kv.cpu().numpy().view(np.uint16).reshape(s.n_layers, 2, s.n_kv_heads, smax, s.head_dim)
     o = O.Oracle(s, w)
-    rid, rlog, margin = o.prefill(embeds=e)
+    rid, rlog, margin = o.prefill(embeds=e) if prompt == "embeds" else o.prefill(tokens=toks)
     assert margin <= MARGIN or first == rid, (first, rid, margin)
     assert rel_l2(y.cpu().numpy(), o.hidden()) <= REL_TOL
     for l in range(s.n_layers):

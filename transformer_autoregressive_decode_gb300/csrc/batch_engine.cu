@@ -505,12 +505,14 @@ void batch_leave(qd_batch *b) {
 }  // namespace
 
 // qd_prefill through the batched prefill kernels: an internal one-stream batch over the
-// model's weights runs the prompt (tensor-core GEMMs over all positions, causal flash
+// model's weights runs the prompt (device embeddings, or device token ids whose
+// embedding rows are gathered first) (tensor-core GEMMs over all positions, causal flash
 // attention), its K/V rows [0, n) are copied into the model's bucket buffer, and the
 // first id, the position and the id history are committed to the model's state.  The
 // model's stream waits for it.  QD_EUNSUPPORTED, with nothing enqueued, when the model
 // or the shapes do not allow it.
-qd_status model_prefill_batched(qd_model *m, const float *embeds_dev, int n, int head_idx, int bucket) {
+qd_status model_prefill_batched(qd_model *m, const float *embeds_dev, const int32_t *tokens_dev, int n, int head_idx,
+                                int bucket) {
     const qd_config &c = m->cfg;
     TcGemmPlan plans[5];
     if (!m->bf16 || c.n_heads_out != 1 || !m->embed || !prefill_plans(m, 1, n, plans)) return QD_EUNSUPPORTED;
@@ -533,7 +535,12 @@ qd_status model_prefill_batched(qd_model *m, const float *embeds_dev, int n, int
     const long long l0 = b->launches;
     CU(cudaMemsetAsync(b->pf_streams, 0, sizeof(int), b->ls));   // stream 0
     CU(cudaMemsetAsync(b->status, 0, sizeof(int), b->ls));
-    CU(cudaMemcpyAsync(b->pf_x, embeds_dev, (size_t)n * c.hidden * 4, cudaMemcpyDeviceToDevice, b->ls));
+    if (tokens_dev) {
+        CU(launch_embed_rows(m->embed, tokens_dev, n, c.hidden, b->pf_x, b->ls));
+        ++m->launches;
+    } else {
+        CU(cudaMemcpyAsync(b->pf_x, embeds_dev, (size_t)n * c.hidden * 4, cudaMemcpyDeviceToDevice, b->ls));
+    }
     st = enqueue_prefill(b, 1, n, b->tokens, head_idx, m->y);
     if (st) return st;
     // K/V rows [0, n) of every (layer, K/V, kv head) segment into the model's bucket

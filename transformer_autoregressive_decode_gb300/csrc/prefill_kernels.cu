@@ -164,6 +164,17 @@ cudaError_t launch_prefill_commit(DevState *st, int32_t *ids, int ids_cap, const
     return cudaGetLastError();
 }
 
+__global__ void embed_rows_kernel(const __nv_bfloat16 *table, const int32_t *tokens, int hidden, float *x) {
+    const __nv_bfloat16 *row = table + (size_t)tokens[blockIdx.x] * hidden;
+    float *o = x + (size_t)blockIdx.x * hidden;
+    for (int j = threadIdx.x; j < hidden; j += blockDim.x) o[j] = __bfloat162float(row[j]);
+}
+
+cudaError_t launch_embed_rows(const void *table, const int32_t *tokens, int n, int hidden, float *x, cudaStream_t s) {
+    embed_rows_kernel<<<n, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(table), tokens, hidden, x);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_prefill_finish(const PrefillFinishArgs &a, int ns, cudaStream_t s) {
     prefill_finish_kernel<<<ns, 256, 0, s>>>(a);
     return cudaGetLastError();

@@ -796,9 +796,11 @@ qd_status qd_prefill(qd_handle h, const int32_t *tokens, const void *embeds, int
     qd_status st = ensure_bucket(m, b);
     if (st) return st;
     m->cur_bucket = b;
-    if (embeds && !m->tap_hidden && !m->tap_logits) {
+    if (!m->tap_hidden && !m->tap_logits) {
         // all positions at once through the batched prefill kernels, where they apply
-        st = model_prefill_batched(m, static_cast<const float *>(embeds), n, head_idx, b);
+        if (tokens) CU(cudaMemcpyAsync(m->stage_tokens, tokens, (size_t)n * 4, cudaMemcpyHostToDevice, m->ls));
+        st = model_prefill_batched(m, static_cast<const float *>(embeds), tokens ? m->stage_tokens : nullptr, n,
+                                   head_idx, b);
         if (st == QD_OK) {
             m->h_pos = n;
             m->h_ngen++;

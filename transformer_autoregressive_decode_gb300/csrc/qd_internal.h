@@ -361,5 +361,8 @@ cudaError_t launch_prefill_finish(const PrefillFinishArgs &a, int ns, cudaStream
 // batch's error bits join the model's.
 cudaError_t launch_prefill_commit(DevState *st, int32_t *ids, int ids_cap, const int32_t *first, int n,
                                   const int *batch_status, cudaStream_t s);
+// x[i] = E[tokens[i]] (bf16 table [rows, hidden] -> fp32 [n, hidden]); ids were checked
+// against the table on the host.
+cudaError_t launch_embed_rows(const void *table, const int32_t *tokens, int n, int hidden, float *x, cudaStream_t s);
 
 }  // namespace qd
