@@ -91,6 +91,14 @@ def _lib_handle():
             L.orc_attend.restype = None
             L.orc_penalty_argmax.argtypes = [vp, i32, vp, ctypes.c_float, i32, P(dp)]
             L.orc_penalty_argmax.restype = i32
+            L.orc_set_sampling.argtypes = [vp, i32, ctypes.c_double, ctypes.c_double, ctypes.c_uint64]
+            L.orc_set_sampling.restype = i32
+            L.orc_splitmix64.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
+            L.orc_splitmix64.restype = ctypes.c_uint64
+            L.orc_uniform.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
+            L.orc_uniform.restype = ctypes.c_double
+            L.orc_sample.argtypes = [vp, i32, i32, ctypes.c_double, ctypes.c_double, ctypes.c_double, P(dp)]
+            L.orc_sample.restype = i32
             L.orc_silu_mul.argtypes = [ctypes.c_float, ctypes.c_float]
             L.orc_silu_mul.restype = ctypes.c_float
             L.orc_round_bf16.argtypes = [ctypes.c_float]
@@ -111,6 +119,23 @@ def _lib_handle():
 
 def _ptr(a: Optional[np.ndarray]):
     return None if a is None else a.ctypes.data
+
+
+def splitmix64(seed: int, counter: int) -> int:
+    return int(_lib_handle().orc_splitmix64(seed, counter))
+
+
+def uniform(seed: int, counter: int) -> float:
+    return float(_lib_handle().orc_uniform(seed, counter))
+
+
+def sample(logits: np.ndarray, top_k: int, temperature: float, top_p: float, u: float):
+    """The oracle's sampler on final logits: (index, decision margin)."""
+    lg = np.ascontiguousarray(logits, dtype=np.float32)
+    mg = ctypes.c_double(0.0)
+    i = _lib_handle().orc_sample(lg.ctypes.data, len(lg), int(top_k), float(temperature), float(top_p), float(u),
+                           ctypes.byref(mg))
+    return int(i), mg.value
 
 
 def make_config(shape, acc64: bool = False, buckets: Optional[Sequence[int]] = None) -> Config:
@@ -211,6 +236,12 @@ class Oracle:
         self._check(self.L.orc_forward(self.h, _ptr(e), int(token), int(add_emitted), int(want_head), head_idx,
                                        ctypes.byref(oid), _ptr(logits), _ptr(tp), ctypes.byref(margin)), "forward")
         return oid.value, logits, margin.value, tp
+
+    def set_sampling(self, top_k: int, temperature: float = 1.0, top_p: float = 1.0, seed: int = 0):
+        """Sample the heads' ids (top_k 0: greedy argmax); the draw counter is the
+        number of ids produced since reset."""
+        self._check(self.L.orc_set_sampling(self.h, int(top_k), float(temperature), float(top_p), int(seed)),
+                    "set_sampling")
 
     def set_kv(self, kv: np.ndarray, length: int):
         """Start from a cache [n_layers, 2, n_kv_heads, length, head_dim] in the cache

@@ -51,6 +51,10 @@ struct orc_model {
     int emitted_words;
     int have_hidden;
     float *y;       /* final-norm output of the last position with a head */
+    int n_gen;      /* ids produced by heads since reset: the sampler's counter */
+    int top_k;      /* sampling: 0 = greedy */
+    double temperature, top_p;
+    uint64_t seed;
 };
 
 /* ---------------------------------------------------------------- helpers */
@@ -232,7 +236,98 @@ int orc_penalty_argmax(float *logits, int n, const uint32_t *emitted, float pena
     return best;
 }
 
-/* ---------------------------------------------------------------- model */
+/* ---------------------------------------------------------------- sampling */
+
+/* SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom number
+ * generators", OOPSLA 2014): the state advances by the odd constant gamma and the
+ * output is the state passed through the mixing function of that paper (two
+ * xor-shift-multiply rounds and a final xor-shift).  Counter-based here: the state
+ * of draw `counter` is seed + (counter + 1) * gamma, so any draw is computed
+ * directly. */
+uint64_t orc_splitmix64(uint64_t seed, uint64_t counter) {
+    uint64_t z = seed + (counter + 1u) * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+double orc_uniform(uint64_t seed, uint64_t counter) {
+    return (double)(orc_splitmix64(seed, counter) >> 11) * (1.0 / 9007199254740992.0);   /* 2^-53 */
+}
+
+/* The sampling entry of the pages' generation settings ([hip] top_k 50, top_p 1.0,
+ * temperature 0.9, seeded): candidates by value then index, weights in fp64,
+ * top-p prefix, inverse-CDF draw. */
+int orc_sample(const float *logits, int n, int top_k, double temperature, double top_p, double u,
+               double *margin) {
+    int K = top_k < n ? top_k : n;
+    int idx[ORC_MAX_TOPK];
+    int taken = 0;
+    /* selection: K rounds of "largest not yet taken, lowest index on ties" */
+    for (int r = 0; r < K; ++r) {
+        int best = -1;
+        for (int i = 0; i < n; ++i) {
+            int used = 0;
+            for (int j = 0; j < taken; ++j) used |= idx[j] == i;
+            if (used) continue;
+            if (best < 0 || logits[i] > logits[best]) best = i;
+        }
+        idx[taken++] = best;
+    }
+    double w[ORC_MAX_TOPK], cum[ORC_MAX_TOPK];
+    const double top = (double)logits[idx[0]];
+    double total = 0.0;
+    for (int i = 0; i < K; ++i) {
+        w[i] = (double)logits[idx[i]] == -INFINITY ? 0.0 : exp(((double)logits[idx[i]] - top) / temperature);
+        total += w[i];
+        cum[i] = total;
+    }
+    int m = K;   /* smallest prefix reaching top_p of the total */
+    for (int i = 0; i < K; ++i)
+        if (cum[i] >= top_p * total) {
+            m = i + 1;
+            break;
+        }
+    const double z = cum[m - 1], t = u * z;
+    int pick = m - 1;
+    for (int i = 0; i < m; ++i)
+        if (cum[i] > t) {
+            pick = i;
+            break;
+        }
+    if (margin) {
+        double d = INFINITY;
+        for (int i = 0; i < m; ++i) {
+            const double e = fabs(cum[i] - t) / z;
+            if (e < d) d = e;
+        }
+        /* the candidate set: gap between the K-th and the best excluded logit */
+        if (K < n) {
+            double next = -INFINITY;
+            for (int i = 0; i < n; ++i) {
+                int used = 0;
+                for (int j = 0; j < K; ++j) used |= idx[j] == i;
+                if (!used && (double)logits[i] > next) next = (double)logits[i];
+            }
+            const double gap = (double)logits[idx[K - 1]] - next;
+            if (gap < d) d = gap;
+        }
+        *margin = d;
+    }
+    return idx[pick];
+}
+
+int orc_set_sampling(orc_model *m, int top_k, double temperature, double top_p, uint64_t seed) {
+    if (top_k < 0 || top_k > ORC_MAX_TOPK || !(temperature > 0.0) || !(top_p > 0.0) || top_p > 1.0)
+        return ORC_EINVAL;
+    m->top_k = top_k;
+    m->temperature = temperature;
+    m->top_p = top_p;
+    m->seed = seed;
+    return ORC_OK;
+}
+
+/* ---------------------------------------------------------------- model *//* ---------------------------------------------------------------- model */
 
 static const void *W_(const orc_model *m, int layer, int slot) {
     return m->w[2 + m->c.n_heads_out + layer * ORC_LAYER_SLOTS + slot];
@@ -305,6 +400,7 @@ int orc_reset(orc_model *m) {
     m->pos = 0;
     memset(m->emitted, 0, (size_t)m->emitted_words * 4);
     m->have_hidden = 0;
+    m->n_gen = 0;
     if (m->bucket != 0) {
         free(m->kv);
         m->bucket = 0;
@@ -474,7 +570,16 @@ int orc_forward(orc_model *m, const float *embed, int token, int add_emitted, in
         head_logits(c, (const void *const *)m->w, x, head_idx, m->y, logits);
         m->have_hidden = 1;
         if (logits_raw) memcpy(logits_raw, logits, sizeof(float) * (size_t)c->vocab);
-        int id = orc_penalty_argmax(logits, c->vocab, m->emitted, (float)c->rep_penalty, c->eos_mask_id, margin);
+        int id;
+        if (m->top_k > 0) {
+            /* penalty and mask as for the argmax, then the sampler */
+            (void)orc_penalty_argmax(logits, c->vocab, m->emitted, (float)c->rep_penalty, c->eos_mask_id, NULL);
+            id = orc_sample(logits, c->vocab, m->top_k, m->temperature, m->top_p,
+                            orc_uniform(m->seed, (uint64_t)m->n_gen), margin);
+        } else {
+            id = orc_penalty_argmax(logits, c->vocab, m->emitted, (float)c->rep_penalty, c->eos_mask_id, margin);
+        }
+        m->n_gen++;
         if (out_id) *out_id = id;
         free(logits);
     }

@@ -97,6 +97,26 @@ void orc_attend(const float *q, const float *K, const float *V, int L, int head_
 int orc_penalty_argmax(float *logits, int n, const uint32_t *emitted, float penalty, int eos_id,
                        double *margin);
 float orc_silu_mul(float g, float u);
+
+/* Sampling instead of the greedy argmax (after the penalty and the EOS mask):
+ * top_k candidates (largest logits, ties to the lower index; 1 = greedy), weights
+ * exp((l - l_max) / temperature), the smallest prefix of them whose sum reaches
+ * top_p of the total, and a draw u in [0, 1) of the counter-based generator
+ * orc_uniform(seed, counter) where counter = ids generated so far.  top_k 0 turns
+ * sampling off.  Errors: ORC_EINVAL (top_k > ORC_MAX_TOPK, temperature <= 0,
+ * top_p outside (0, 1]). */
+#define ORC_MAX_TOPK 64
+int orc_set_sampling(orc_model *m, int top_k, double temperature, double top_p, uint64_t seed);
+/* SplitMix64 output for state seed + (counter + 1) * 0x9E3779B97F4A7C15, and its top
+ * 53 bits as a double in [0, 1). */
+uint64_t orc_splitmix64(uint64_t seed, uint64_t counter);
+double orc_uniform(uint64_t seed, uint64_t counter);
+/* The sampler on final logits (penalty and mask applied): the chosen index and, in
+ * *margin, how far the decision is from changing: the smaller of the gap between
+ * the k-th and (k+1)-th logits and the distance of u * (kept sum) from the nearest
+ * cumulative-weight boundary, relative to the kept sum. */
+int orc_sample(const float *logits, int n, int top_k, double temperature, double top_p, double u,
+               double *margin);
 uint16_t orc_round_bf16(float f);
 int orc_num_threads(void);
 void orc_set_threads(int n);
