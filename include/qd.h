@@ -176,6 +176,21 @@ qd_status qd_set_debug_taps(qd_handle h, float *hidden_taps_dev, float *logits_d
 /* Turn CUDA-graph replay on (default) or off; results are identical. */
 qd_status qd_set_graphs(qd_handle h, int enable);
 
+/* qd_set_sampling -- draw the heads' ids instead of taking the greedy argmax, after the
+ * repetition penalty and the EOS mask (the pages' sampling settings: "qwen3-tts-hip
+ * OPTIMIZATION_LOG", sampling entries -- top_k 50, top_p 1.0, temperature 0.9,
+ * seeded): the top_k largest logits (ties to the lower id), weights
+ * exp((l - l_max) / temperature), the smallest prefix of them whose weight reaches
+ * top_p of their sum, then the first candidate whose running weight exceeds u times
+ * the kept weight, u in [0, 1) being draw n of the counter-based SplitMix64 sequence
+ * of `seed` (n = ids produced since the last reset).  top_k 0 restores the greedy
+ * argmax (top_k 1 gives the same ids).  The settings hold for every later step and
+ * survive qd_reset; the batched qd_batch_* path stays greedy.  Asynchronous, ordered
+ * with the model's steps; no graph is recaptured.  Errors: QD_EINVAL (top_k outside
+ * [0, 64], temperature not > 0, top_p outside (0, 1]), QD_EUNSUPPORTED (top_k too
+ * large for this model's head layout). */
+qd_status qd_set_sampling(qd_handle h, int top_k, float temperature, float top_p, uint64_t seed);
+
 /* qd_gemm_bf16 -- the batched paths' tensor-core contraction on its own (a check
  * and measurement tap): out[t][r] = sum_k W[r][k] * x[t][k] for W (DEVICE bf16
  * [R, K] row-major, 16-byte aligned) and x (DEVICE fp32 [T, K] row-major), with x

@@ -296,21 +296,33 @@ int orc_sample(const float *logits, int n, int top_k, double temperature, double
             break;
         }
     if (margin) {
+        /* how far the decision is from changing: the draw from the cumulative
+         * boundaries and the top-p cut from its prefix sums (fractions of the kept or
+         * the total weight); the picked logit from its neighbours in the order (logit
+         * units); when the pick is the last candidate, the k-th logit from the best
+         * excluded one */
         double d = INFINITY;
         for (int i = 0; i < m; ++i) {
             const double e = fabs(cum[i] - t) / z;
             if (e < d) d = e;
         }
-        /* the candidate set: gap between the K-th and the best excluded logit */
-        if (K < n) {
+        if (top_p < 1.0)
+            for (int i = m - 2; i < m; ++i)
+                if (i >= 0) {
+                    const double e = fabs(cum[i] - top_p * total) / total;
+                    if (e < d) d = e;
+                }
+        const double lp = (double)logits[idx[pick]];
+        if (pick > 0 && lp - (double)logits[idx[pick - 1]] > -d) d = (double)logits[idx[pick - 1]] - lp;
+        if (pick + 1 < K && lp - (double)logits[idx[pick + 1]] < d) d = lp - (double)logits[idx[pick + 1]];
+        if (pick == K - 1 && K < n) {
             double next = -INFINITY;
             for (int i = 0; i < n; ++i) {
                 int used = 0;
                 for (int j = 0; j < K; ++j) used |= idx[j] == i;
                 if (!used && (double)logits[i] > next) next = (double)logits[i];
             }
-            const double gap = (double)logits[idx[K - 1]] - next;
-            if (gap < d) d = gap;
+            if (lp - next < d) d = lp - next;
         }
         *margin = d;
     }

@@ -112,9 +112,11 @@ int orc_set_sampling(orc_model *m, int top_k, double temperature, double top_p, 
 uint64_t orc_splitmix64(uint64_t seed, uint64_t counter);
 double orc_uniform(uint64_t seed, uint64_t counter);
 /* The sampler on final logits (penalty and mask applied): the chosen index and, in
- * *margin, how far the decision is from changing: the smaller of the gap between
- * the k-th and (k+1)-th logits and the distance of u * (kept sum) from the nearest
- * cumulative-weight boundary, relative to the kept sum. */
+ * *margin, how far the decision is from changing: the smallest of the distance of
+ * u * (kept sum) from the cumulative-weight boundaries (relative to the kept sum), of
+ * the top-p cut from its neighbouring prefix sums (relative to the total, when top_p
+ * < 1), of the picked logit from its neighbours in the order, and, when the pick is
+ * the last of the top_k, of that logit from the best excluded one. */
 int orc_sample(const float *logits, int n, int top_k, double temperature, double top_p, double u,
                double *margin);
 uint16_t orc_round_bf16(float f);

@@ -116,3 +116,24 @@ def test_model_sampling_is_seeded_and_top1_is_greedy():
             o.set_sampling(65, 0.9, 1.0, 0)
         finally:
             o.close()
+
+
+def test_margin_bounds_the_decisions_sensitivity():
+    """Where the reported margin exceeds eps, moving every logit by less than eps / 10
+    (the logits' own scale ~1) leaves the drawn index unchanged; ties report 0."""
+    rng = np.random.default_rng(11)
+    eps = 1e-2
+    stable = 0
+    for trial in range(400):
+        lg = rng.normal(size=200).astype(np.float32)
+        u = O.uniform(3, trial)
+        k, t, p = int(rng.integers(1, 65)), float(rng.uniform(0.5, 1.5)), float(rng.choice([1.0, 0.9]))
+        i, m = O.sample(lg, k, t, p, u)
+        if m > eps:
+            stable += 1
+            for _ in range(3):
+                pert = (lg + rng.uniform(-eps / 10, eps / 10, size=lg.shape)).astype(np.float32)
+                assert O.sample(pert, k, t, p, u)[0] == i
+    assert stable > 100
+    lg = np.array([2.0, 1.0, 2.0], np.float32)
+    assert O.sample(lg, 3, 1.0, 1.0, 0.1)[1] == 0.0

@@ -31,7 +31,7 @@ QD_FRAME_CODES = 16
 
 # Every symbol the header declares (tests check the library exports each one).
 EXPORTS = ("qd_create", "qd_destroy", "qd_reset", "qd_prefill", "qd_decode_step", "qd_decode_step_async",
-           "qd_decode_greedy", "qd_grow_kv", "qd_get_hidden", "qd_set_debug_taps", "qd_set_graphs", "qd_copy_kv",
+           "qd_decode_greedy", "qd_grow_kv", "qd_get_hidden", "qd_set_debug_taps", "qd_set_graphs", "qd_set_sampling", "qd_copy_kv",
            "qd_get_emitted", "qd_get_pos", "qd_get_launch_count", "qd_time_kernel", "qd_last_error",
            "qd_status_string", "qd_head_argmax_noalloc", "qd_frame_create", "qd_frame_destroy",
            "qd_frame_generate", "qd_frame_set_graphs", "qd_gemm_bf16", "qd_batch_create", "qd_batch_destroy",
@@ -71,6 +71,7 @@ _SIGS = {
     "qd_get_hidden": ([_vp, _vp], _i32),
     "qd_set_debug_taps": ([_vp, _vp, _vp], _i32),
     "qd_set_graphs": ([_vp, _i32], _i32),
+    "qd_set_sampling": ([_vp, _i32, ctypes.c_float, ctypes.c_float, ctypes.c_uint64], _i32),
     "qd_copy_kv": ([_vp, _vp, _P(_sz)], _i32),
     "qd_get_emitted": ([_vp, _vp], _i32),
     "qd_get_pos": ([_vp, _P(_i32), _P(_i32)], _i32),
@@ -223,6 +224,11 @@ def qd_get_hidden(h: Handle, out_dev):
 
 def qd_set_debug_taps(h: Handle, hidden_dev=None, logits_dev=None):
     _check(h, _lib.qd_set_debug_taps(h.h, _ptr(hidden_dev), _ptr(logits_dev)))
+
+
+def qd_set_sampling(h: Handle, top_k: int, temperature: float = 1.0, top_p: float = 1.0, seed: int = 0):
+    """Sample the heads' ids (top_k 0: greedy argmax); see qd_set_sampling in qd.h."""
+    _check(h, _lib.qd_set_sampling(h.h, int(top_k), float(temperature), float(top_p), int(seed)))
 
 
 def qd_set_graphs(h: Handle, enable: bool):

@@ -345,10 +345,10 @@ qd_status ensure_prefill_scratch(qd_batch *b, int ns, int n) {
     return QD_OK;
 }
 
-// Every launch of a prefill of ns streams x n positions, on the batch's stream (output
-// head head_idx; y_last, if given, receives the normalised hidden state of each
-// stream's last position).
-qd_status enqueue_prefill(qd_batch *b, int ns, int n, int32_t *first_ids, int head_idx = 0, float *y_last = nullptr) {
+// Every launch of a prefill of ns streams x n positions, on the batch's stream.  With
+// with_head false it stops after gathering each stream's last hidden state into
+// pf_last (the caller runs a head on it).
+qd_status enqueue_prefill(qd_batch *b, int ns, int n, int32_t *first_ids, bool with_head = true) {
     qd_model *m = b->m;
     const qd_config &c = m->cfg;
     const int h = c.hidden, qd_ = m->q_dim(), rows_qkv = qd_ + 2 * m->kv_dim();
@@ -374,7 +374,7 @@ qd_status enqueue_prefill(qd_batch *b, int ns, int n, int32_t *first_ids, int he
         b->launches++;
         return launch_tc_gemm(p, w, xh, xl, a, s);
     };
-    auto norm = [&](float *x, int rows, const float *gamma, float *y = nullptr) -> cudaError_t {
+    auto norm = [&](float *x, int rows, const float *gamma) -> cudaError_t {
         NormSplitArgs a = {};
         a.x = x;
         a.K = h;
@@ -382,7 +382,6 @@ qd_status enqueue_prefill(qd_batch *b, int ns, int n, int32_t *first_ids, int he
         a.eps = (float)c.rms_eps;
         a.hi = b->pf_xh;
         a.lo = b->pf_xl;
-        a.y = y;
         a.status = b->status;
         b->launches++;
         return launch_norm_split(a, rows, s);
@@ -441,8 +440,9 @@ qd_status enqueue_prefill(qd_batch *b, int ns, int n, int32_t *first_ids, int he
     // the head on each stream's last position
     b->launches++;
     if (launch_gather_last(b->pf_x, n, h, ns, b->pf_last, s)) return batch_fail(b, QD_ECUDA, "gather launch failed");
-    if (norm(b->pf_last, ns, m->final_norm, y_last)) return batch_fail(b, QD_ECUDA, "prefill norm launch failed");
-    if (gemm(p_head, m->heads[head_idx], b->pf_xh, b->pf_xl, c.vocab, h, ns, TC_STORE, b->pf_logits, c.vocab))
+    if (!with_head) return QD_OK;
+    if (norm(b->pf_last, ns, m->final_norm)) return batch_fail(b, QD_ECUDA, "prefill norm launch failed");
+    if (gemm(p_head, m->heads[0], b->pf_xh, b->pf_xl, c.vocab, h, ns, TC_STORE, b->pf_logits, c.vocab))
         return batch_fail(b, QD_ECUDA, "prefill head GEMM launch failed");
     PrefillFinishArgs fin = {};
     fin.logits = b->pf_logits;
@@ -505,14 +505,14 @@ void batch_leave(qd_batch *b) {
 }  // namespace
 
 // qd_prefill through the batched prefill kernels: an internal one-stream batch over the
-// model's weights runs the prompt (device embeddings, or device token ids whose
-// embedding rows are gathered first) (tensor-core GEMMs over all positions, causal flash
-// attention), its K/V rows [0, n) are copied into the model's bucket buffer, and the
-// first id, the position and the id history are committed to the model's state.  The
-// model's stream waits for it.  QD_EUNSUPPORTED, with nothing enqueued, when the model
-// or the shapes do not allow it.
-qd_status model_prefill_batched(qd_model *m, const float *embeds_dev, const int32_t *tokens_dev, int n, int head_idx,
-                                int bucket) {
+// model's weights runs the prompt's layers (device embeddings, or device token ids
+// whose embedding rows are gathered first); its K/V rows [0, n) are copied into the
+// model's bucket buffer and the last position's hidden state into the model's x, and
+// the model's position becomes n - 1.  The model's stream waits for it; the caller then
+// runs the model's head step, which gives the first id (greedy or sampled, like every
+// later step) and advances the position to n.  QD_EUNSUPPORTED, with nothing enqueued,
+// when the model or the shapes do not allow it.
+qd_status model_prefill_batched(qd_model *m, const float *embeds_dev, const int32_t *tokens_dev, int n, int bucket) {
     const qd_config &c = m->cfg;
     TcGemmPlan plans[5];
     if (!m->bf16 || c.n_heads_out != 1 || !m->embed || !prefill_plans(m, 1, n, plans)) return QD_EUNSUPPORTED;
@@ -541,13 +541,14 @@ qd_status model_prefill_batched(qd_model *m, const float *embeds_dev, const int3
     } else {
         CU(cudaMemcpyAsync(b->pf_x, embeds_dev, (size_t)n * c.hidden * 4, cudaMemcpyDeviceToDevice, b->ls));
     }
-    st = enqueue_prefill(b, 1, n, b->tokens, head_idx, m->y);
+    st = enqueue_prefill(b, 1, n, nullptr, false);
     if (st) return st;
     // K/V rows [0, n) of every (layer, K/V, kv head) segment into the model's bucket
     const size_t row = (size_t)c.head_dim * m->esize;
     CU(cudaMemcpy2DAsync(m->kv[bucket], (size_t)c.buckets[bucket] * row, b->kv, (size_t)b->S * row, (size_t)n * row,
                          (size_t)c.n_layers * 2 * c.n_kv_heads, cudaMemcpyDeviceToDevice, b->ls));
-    CU(launch_prefill_commit(m->st, m->ids, kIdsCap, b->tokens, n, b->status, b->ls));
+    CU(cudaMemcpyAsync(m->x, b->pf_last, (size_t)c.hidden * 4, cudaMemcpyDeviceToDevice, b->ls));
+    CU(launch_prefill_commit(m->st, n - 1, b->status, b->ls));
     m->launches += b->launches - l0 + 1;
     CU(cudaEventRecord(m->pf_ev[1], b->ls));
     CU(cudaStreamWaitEvent(m->ls, m->pf_ev[1], 0));

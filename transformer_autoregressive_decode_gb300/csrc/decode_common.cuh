@@ -294,6 +294,162 @@ __device__ __forceinline__ bool arg_better(float v, int i, float bv, int bi) {
 }
 
 // ---------------------------------------------------------------------------------
+// Sampling: the top-k candidates of a set of logits, the counter-based draw, and the
+// pick (the same steps, in the same order, as the oracle's sampler).
+// ---------------------------------------------------------------------------------
+
+// Order-preserving unsigned key of a float: a larger float has a larger key; -0 counts
+// as +0 (they compare equal).
+__device__ __forceinline__ uint32_t order_key(float v) {
+    const uint32_t u = __float_as_uint(v == 0.f ? 0.f : v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Consumer threads (named barrier 1): the K (<= kMaxTopK) largest of n values -- value
+// i at vals[i * stride], its index idx[i] (or base + i when idx is null) -- with ties
+// to the lower index, into out_v / out_i[0..K) sorted by value descending, then index
+// ascending; entries past n are -inf / INT_MAX.  Among equal values the indices must
+// ascend with i.  Radix select of the K-th largest key (four 8-bit passes over shared
+// histograms), then every larger key and, in index order, as many equal keys as are
+// needed, then a rank sort.  out_* must not overlap the scratch.
+static __device__ __noinline__ void block_topk(const float *vals, int stride, const int *idx, int base, int n, int K,
+                                        float *out_v, int *out_i, int *scratch) {
+    constexpr int NC = kConsumerWarps * 32;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int *hist = scratch, *cnt = scratch + 256, *ctl = cnt + NC;
+    float *tv = reinterpret_cast<float *>(ctl + 8);
+    int *ti = reinterpret_cast<int *>(tv + kMaxTopK);
+    const int Ke = K < n ? K : n;
+    if (tid == 0) {
+        ctl[1] = Ke;
+        ctl[2] = 0;
+    }
+    if (Ke > 0) {
+        uint32_t prefix = 0, mask = 0;
+        for (int shift = 24; shift >= 0; shift -= 8) {
+            for (int b = tid; b < 256; b += NC) hist[b] = 0;
+            named_sync(1, NC);
+            for (int i = tid; i < n; i += NC) {
+                const uint32_t k = order_key(vals[(size_t)i * stride]);
+                if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
+            }
+            named_sync(1, NC);
+            if (tid == 0) {
+                int cum = 0;
+                const int need = ctl[1];
+                for (int b = 255; b >= 0; --b) {
+                    if (cum + hist[b] >= need) {
+                        ctl[0] = b;
+                        ctl[1] = need - cum;
+                        break;
+                    }
+                    cum += hist[b];
+                }
+            }
+            named_sync(1, NC);
+            prefix |= (uint32_t)ctl[0] << shift;
+            mask |= 255u << shift;
+        }
+        const uint32_t kth = prefix;
+        const int take_eq = ctl[1];
+        const int n_gt = Ke - take_eq;
+        // every key above the K-th (in any order)
+        for (int i = tid; i < n; i += NC) {
+            const float v = vals[(size_t)i * stride];
+            if (order_key(v) > kth) {
+                const int s = atomicAdd(&ctl[2], 1);
+                tv[s] = v;
+                ti[s] = idx ? idx[i] : base + i;
+            }
+        }
+        // keys equal to the K-th, lowest indices first: contiguous segments per thread
+        // and an exclusive prefix sum of their counts
+        const int seg = (n + NC - 1) / NC, lo = tid * seg, hi = lo + seg < n ? lo + seg : n;
+        int c = 0;
+        for (int i = lo; i < hi; ++i) c += order_key(vals[(size_t)i * stride]) == kth;
+        int x = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) cnt[warp] = x;
+        named_sync(1, NC);
+        int off = x - c;
+        for (int w = 0; w < warp; ++w) off += cnt[w];
+        for (int i = lo; i < hi && off < take_eq; ++i) {
+            const float v = vals[(size_t)i * stride];
+            if (order_key(v) == kth) {
+                tv[n_gt + off] = v;
+                ti[n_gt + off] = idx ? idx[i] : base + i;
+                ++off;
+            }
+        }
+        named_sync(1, NC);
+    }
+    // rank sort
+    if (tid < K) {
+        if (tid < Ke) {
+            const float v = tv[tid];
+            const int ix = ti[tid];
+            const uint32_t k = order_key(v);
+            int r = 0;
+            for (int j = 0; j < Ke; ++j) {
+                const uint32_t kj = order_key(tv[j]);
+                r += kj > k || (kj == k && ti[j] < ix);
+            }
+            out_v[r] = v;
+            out_i[r] = ix;
+        } else {
+            out_v[tid] = -INFINITY;
+            out_i[tid] = INT_MAX;
+        }
+    }
+    named_sync(1, NC);
+}
+
+// SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom number generators",
+// OOPSLA 2014) as a counter-based generator: draw `counter` of `seed` is the output for
+// state seed + (counter + 1) * gamma; its top 53 bits as a double in [0, 1).
+__device__ __forceinline__ uint64_t splitmix64(uint64_t seed, uint64_t counter) {
+    uint64_t z = seed + (counter + 1u) * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+__device__ __forceinline__ double uniform53(uint64_t seed, uint64_t counter) {
+    return (double)(splitmix64(seed, counter) >> 11) * (1.0 / 9007199254740992.0);
+}
+
+// One thread: the id drawn from K candidates sorted by value: weights
+// exp((v - v_max) / temperature), the smallest prefix reaching top_p of their sum,
+// the first whose running sum exceeds u times the kept sum.
+static __device__ __noinline__ int sample_candidates(const float *cv, const int *ci, int K, float temperature, float top_p,
+                                              double u) {
+    float cum[kMaxTopK];
+    float total = 0.f;
+    for (int i = 0; i < K; ++i) {
+        const float w = cv[i] == -INFINITY ? 0.f : expf((cv[i] - cv[0]) / temperature);
+        total += w;
+        cum[i] = total;
+    }
+    int m = K;
+    for (int i = 0; i < K; ++i)
+        if (cum[i] >= top_p * total) {
+            m = i + 1;
+            break;
+        }
+    const float t = (float)(u * (double)cum[m - 1]);
+    int pick = m - 1;
+    for (int i = 0; i < m; ++i)
+        if (cum[i] > t) {
+            pick = i;
+            break;
+        }
+    return ci[pick];
+}
+
+// ---------------------------------------------------------------------------------
 // Attention of one (kv group, split) on shared-memory tiles.
 // Ks/Vs: n cached rows in the cache type (row n_old already holds position p when the
 // split owns it); qs: the G query heads (normalised, rotated), fp32; sc: [G][CM]

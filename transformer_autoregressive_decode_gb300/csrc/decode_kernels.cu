@@ -168,6 +168,9 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a)
             a.out[row0 + tid] = xold + v;
         }
     } else {  // GEMV_HEAD
+        // greedy: per-thread, per-warp, per-CTA argmax.  Sampling (top-k > 0): the
+        // CTA's final logits stay in res and the CTA's top-k candidates go out.
+        const int sk = a.st->sample_k;
         float best_v = -INFINITY;
         int best_i = INT_MAX;
         for (int r = tid; r < nrows; r += NC) {
@@ -178,42 +181,91 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a)
             if (a.penalty != 1.0f && ((emw[(row >> 5) - w0] >> (row & 31)) & 1u))
                 v = v > 0.f ? v / a.penalty : v * a.penalty;
             if (row == a.eos) v = -INFINITY;
-            if (arg_better(v, row, best_v, best_i)) {
+            if (sk > 0) {
+                res[r * rs] = v;
+            } else if (arg_better(v, row, best_v, best_i)) {
                 best_v = v;
                 best_i = row;
             }
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, best_v, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, best_i, o);
-            if (arg_better(ov, oi, best_v, best_i)) {
-                best_v = ov;
-                best_i = oi;
+        // sampling scratch over the ring, idle now: the CTA's candidates, the selection
+        // scratch, then (last CTA) every CTA's candidates
+        float *cv = reinterpret_cast<float *>(ring);
+        int *ci = reinterpret_cast<int *>(cv + kMaxTopK);
+        int *scr = ci + kMaxTopK;
+        float *all_v = reinterpret_cast<float *>(scr + kTopkScratchWords);
+        int *all_i = reinterpret_cast<int *>(all_v + (size_t)gridDim.x * (sk > 0 ? sk : 1));
+        if (sk > 0) {
+            named_sync(1, NC);
+            block_topk(res, rs, nullptr, row0, nrows, sk, cv, ci, scr);
+            if (tid < sk) {
+                a.part_v[(size_t)blockIdx.x * sk + tid] = cv[tid];
+                a.part_i[(size_t)blockIdx.x * sk + tid] = ci[tid];
             }
-        }
-        if (lane == 0) {
-            misc[8 + warp] = best_v;
-            misc_i[8 + warp] = best_i;
+        } else {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, best_v, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, best_i, o);
+                if (arg_better(ov, oi, best_v, best_i)) {
+                    best_v = ov;
+                    best_i = oi;
+                }
+            }
+            if (lane == 0) {
+                misc[8 + warp] = best_v;
+                misc_i[8 + warp] = best_i;
+            }
         }
         named_sync(1, NC);
         if (tid == 0) {
-            float bv = misc[8];
-            int bi = misc_i[8];
-            for (int w = 1; w < kConsumerWarps; ++w)
-                if (arg_better(misc[8 + w], misc_i[8 + w], bv, bi)) {
-                    bv = misc[8 + w];
-                    bi = misc_i[8 + w];
-                }
-            a.part_v[blockIdx.x] = bv;
-            a.part_i[blockIdx.x] = bi;
+            if (sk == 0) {
+                float bv = misc[8];
+                int bi = misc_i[8];
+                for (int w = 1; w < kConsumerWarps; ++w)
+                    if (arg_better(misc[8 + w], misc_i[8 + w], bv, bi)) {
+                        bv = misc[8 + w];
+                        bi = misc_i[8 + w];
+                    }
+                a.part_v[blockIdx.x] = bv;
+                a.part_i[blockIdx.x] = bi;
+            }
             __threadfence();
             const int prev = atomicAdd(a.counter, 1);
             misc_i[5] = (prev == (int)gridDim.x - 1);
         }
         named_sync(1, NC);
-        if (misc_i[5] && warp == 0) {
-            // last CTA: reduce the per-CTA candidates, publish the id, advance the position
+        // last CTA: publish the id, advance the position
+        auto commit = [&](int id) {
+            *a.counter = 0;
+            if (a.commit) {
+                DevState *st = a.st;
+                st->out_id = id;
+                const int n = st->n_gen;
+                if (n < a.ids_cap) a.ids[n] = id;
+                else atomicOr(&st->status, DEV_ERR_IDS_FULL);
+                st->n_gen = n + 1;
+                st->pos = st->pos + 1;
+            }
+        };
+        if (misc_i[5] && sk > 0) {
+            // every CTA's candidates (in CTA order: ascending rows) -> the top-k -> the draw
+            __threadfence();
+            const int nc = (int)gridDim.x * sk;
+            for (int i = tid; i < nc; i += NC) {
+                all_v[i] = __ldcg(a.part_v + i);
+                all_i[i] = __ldcg(a.part_i + i);
+            }
+            named_sync(1, NC);
+            block_topk(all_v, 1, all_i, 0, nc, sk, cv, ci, scr);
+            if (tid == 0) {
+                const DevState *st = a.st;
+                const uint64_t seed = ((uint64_t)st->seed_hi << 32) | st->seed_lo;
+                commit(sample_candidates(cv, ci, sk, st->sample_temp, st->sample_top_p,
+                                         uniform53(seed, (uint64_t)st->n_gen)));
+            }
+        } else if (misc_i[5] && warp == 0) {
+            // reduce the per-CTA argmax candidates
             __threadfence();
             float bv = -INFINITY;
             int bi = INT_MAX;
@@ -234,18 +286,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a)
                     bi = oi;
                 }
             }
-            if (lane == 0) {
-                *a.counter = 0;
-                if (a.commit) {
-                    DevState *st = a.st;
-                    st->out_id = bi;
-                    const int n = st->n_gen;
-                    if (n < a.ids_cap) a.ids[n] = bi;
-                    else atomicOr(&st->status, DEV_ERR_IDS_FULL);
-                    st->n_gen = n + 1;
-                    st->pos = st->pos + 1;
-                }
-            }
+            if (lane == 0) commit(bi);
         }
     }
     if (a.advance_pos && blockIdx.x == 0 && tid == 0) a.st->pos = a.st->pos + 1;

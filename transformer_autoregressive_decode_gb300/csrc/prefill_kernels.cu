@@ -146,21 +146,13 @@ cudaError_t launch_gather_last(const float *x, int n, int K, int ns, float *out,
     return cudaGetLastError();
 }
 
-__global__ void prefill_commit_kernel(DevState *st, int32_t *ids, int ids_cap, const int32_t *first, int n,
-                                      const int *batch_status) {
-    const int id = *first;
-    st->out_id = id;
-    const int g = st->n_gen;
-    if (g < ids_cap) ids[g] = id;
-    else st->status |= DEV_ERR_IDS_FULL;
-    st->n_gen = g + 1;
-    st->pos = n;
+__global__ void prefill_commit_kernel(DevState *st, int pos, const int *batch_status) {
+    st->pos = pos;
     st->status |= *batch_status;
 }
 
-cudaError_t launch_prefill_commit(DevState *st, int32_t *ids, int ids_cap, const int32_t *first, int n,
-                                  const int *batch_status, cudaStream_t s) {
-    prefill_commit_kernel<<<1, 1, 0, s>>>(st, ids, ids_cap, first, n, batch_status);
+cudaError_t launch_prefill_commit(DevState *st, int pos, const int *batch_status, cudaStream_t s) {
+    prefill_commit_kernel<<<1, 1, 0, s>>>(st, pos, batch_status);
     return cudaGetLastError();
 }
 

@@ -29,8 +29,15 @@ struct DevState {
     int out_id;       // id produced by the last step that ran a head
     int n_gen;        // ids produced since reset (index into the id history)
     int status;       // DEV_ERR_* bits, sticky until reset
-    int pad[8];
+    // sampling (kept by a reset): sample_k 0 = greedy argmax, else top-k candidates,
+    // temperature, top-p, and the seed of the counter-based draws (draw n_gen)
+    int sample_k;
+    float sample_temp, sample_top_p;
+    uint32_t seed_lo, seed_hi;
+    int pad[3];
 };
+// bytes of DevState that a reset zeroes (the sampling settings follow them)
+#define QD_DEVSTATE_RESET_BYTES (8 * sizeof(int))
 
 enum : int {
     IN_TOKEN = 0,          // x = E[token_in]

@@ -516,8 +516,8 @@ static qd_status alloc_scratch(qd_model *m) {
                  o_att = take((size_t)m->q_dim() * 4), o_y = take(h * 4),
                  o_po = take((size_t)c.n_q_heads * kAttnMaxSplits * c.head_dim * 4),
                  o_pml = take((size_t)c.n_q_heads * kAttnMaxSplits * 2 * 4), o_bar = take(128),
-                 o_ein = take(h * 4), o_se = take((size_t)m->max_pos * h * 4), o_pv = take(4096 * 4),
-                 o_pi = take(4096 * 4), o_hc = take(64 * 4), o_stok = take((size_t)m->max_pos * 4),
+                 o_ein = take(h * 4), o_se = take((size_t)m->max_pos * h * 4), o_pv = take((size_t)kHeadCandidates * 4),
+                 o_pi = take((size_t)kHeadCandidates * 4), o_hc = take(64 * 4), o_stok = take((size_t)m->max_pos * 4),
                  o_ids = take((size_t)kIdsCap * 4), o_em = take((size_t)((c.vocab + 31) / 32) * 4),
                  o_st = take(sizeof(DevState)), o_cos = take((size_t)m->max_pos * (c.head_dim / 2) * 4),
                  o_sin = take((size_t)m->max_pos * (c.head_dim / 2) * 4);
@@ -560,12 +560,12 @@ static bool plan_launches(qd_model *m) {
     m->rps_f = kSlotBytes / (int)(c.ffn * m->esize);
     const int sms = m->num_sms;
     auto plan = [&](int rows, int unit, int K, int rps, int rs, int max_nst, int *grid, int *nst, int *rmax,
-                    size_t *smem) {
+                    size_t *smem, int min_nst = 1) {
         const int units = rows / unit;
         *grid = std::min(sms, units);
         *rmax = (units + *grid - 1) / *grid * unit;
         const int need = (*rmax + rps - 1) / rps;
-        *nst = std::max(1, std::min(need, max_nst));
+        *nst = std::max(min_nst, std::min(need, max_nst));
         *smem = gemv_smem_bytes(*nst, *rmax, rs, K);
     };
     // Step kernels keep their ring at 4 stages (96 KB) so that the next kernel of the
@@ -577,8 +577,10 @@ static bool plan_launches(qd_model *m) {
     plan(c.hidden, 1, m->q_dim(), m->rps_q, m->rs_q, ring, &m->grid_o, &m->nst_o, &m->rmax_o, &m->smem_o);
     plan(2 * c.ffn, 2, c.hidden, m->rps_h, m->rs_h, ring, &m->grid_gu, &m->nst_gu, &m->rmax_gu, &m->smem_gu);
     plan(c.hidden, 1, c.ffn, m->rps_f, m->rs_f, ring, &m->grid_d, &m->nst_d, &m->rmax_d, &m->smem_d);
+    // the head's ring also holds, once its rows are consumed, the sampling merge of
+    // every CTA's candidates (up to kMaxTopK each): at least three stages
     plan(c.vocab, 1, c.hidden, m->rps_h, m->rs_h, 2 * ring, &m->grid_head, &m->nst_head, &m->rmax_head,
-         &m->smem_head);
+         &m->smem_head, 3);
     // Layer weights that fit in 60% of L2 stay resident across steps (evict_last);
     // the output head always streams (evict_first).
     size_t layer_bytes = 0;
@@ -762,7 +764,7 @@ qd_status qd_reset(qd_handle h) {
     if (!h) return QD_EINVAL;
     qd_model *m = h;
     enter(m);
-    CU(cudaMemsetAsync(m->st, 0, sizeof(DevState), m->ls));
+    CU(cudaMemsetAsync(m->st, 0, QD_DEVSTATE_RESET_BYTES, m->ls));
     CU(cudaMemsetAsync(m->emitted, 0, (size_t)((m->cfg.vocab + 31) / 32) * 4, m->ls));
     m->h_pos = 0;
     m->h_ngen = 0;
@@ -799,9 +801,13 @@ qd_status qd_prefill(qd_handle h, const int32_t *tokens, const void *embeds, int
     if (!m->tap_hidden && !m->tap_logits) {
         // all positions at once through the batched prefill kernels, where they apply
         if (tokens) CU(cudaMemcpyAsync(m->stage_tokens, tokens, (size_t)n * 4, cudaMemcpyHostToDevice, m->ls));
-        st = model_prefill_batched(m, static_cast<const float *>(embeds), tokens ? m->stage_tokens : nullptr, n,
-                                   head_idx, b);
+        st = model_prefill_batched(m, static_cast<const float *>(embeds), tokens ? m->stage_tokens : nullptr, n, b);
         if (st == QD_OK) {
+            // the head on the last position: the model's own head kernel, as in every step
+            st = set_params(m, IN_EMBED, -1, 0, head_idx);
+            if (st) return st;
+            CU(launch_gemv(GEMV_HEAD, m->bf16, head_args(m, nullptr, 1), m->grid_head, m->smem_head, m->ls, false));
+            m->launches += 1;
             m->h_pos = n;
             m->h_ngen++;
             m->have_hidden = true;
@@ -946,6 +952,36 @@ qd_status qd_get_hidden(qd_handle h, float *out_dev) {
     if (!is_device_ptr(out_dev)) return fail(m, QD_EINVAL, "out_dev is not a device pointer");
     enter(m);
     CU(cudaMemcpyAsync(out_dev, m->y, (size_t)m->cfg.hidden * 4, cudaMemcpyDeviceToDevice, m->ls));
+    leave(m);
+    return QD_OK;
+}
+
+qd_status qd_set_sampling(qd_handle h, int top_k, float temperature, float top_p, uint64_t seed) {
+    if (!h) return QD_EINVAL;
+    qd_model *m = h;
+    if (top_k < 0 || top_k > kMaxTopK) return fail(m, QD_EINVAL, "top_k %d outside [0, %d]", top_k, kMaxTopK);
+    if (!(temperature > 0.f) || !std::isfinite(temperature))
+        return fail(m, QD_EINVAL, "temperature must be > 0 (got %g)", (double)temperature);
+    if (!(top_p > 0.f) || top_p > 1.f) return fail(m, QD_EINVAL, "top_p must be in (0, 1] (got %g)", (double)top_p);
+    if (top_k > 0) {
+        // every head CTA's candidates in the global scratch; the last CTA's selection
+        // scratch and all candidates in its idle ring
+        auto fits = [&](int grid, int nst) {
+            const size_t words = 2 * (size_t)kMaxTopK + kTopkScratchWords + 2 * (size_t)grid * top_k;
+            return (size_t)grid * top_k <= (size_t)kHeadCandidates && words * 4 <= (size_t)nst * kSlotBytes;
+        };
+        if (!fits(m->grid_head, m->nst_head) || (m->persistent && !fits(m->num_sms, m->nst_step)))
+            return fail(m, QD_EUNSUPPORTED, "top_k %d too large for this model's head layout", top_k);
+    }
+    struct {
+        int k;
+        float t, p;
+        uint32_t lo, hi;
+    } v = {top_k, temperature, top_p, (uint32_t)seed, (uint32_t)(seed >> 32)};
+    static_assert(sizeof(v) == 5 * 4, "sampling fields");
+    enter(m);
+    // pageable source: staged by the runtime before the call returns
+    CU(cudaMemcpyAsync(&m->st->sample_k, &v, sizeof(v), cudaMemcpyHostToDevice, m->ls));
     leave(m);
     return QD_OK;
 }

@@ -11,6 +11,10 @@ namespace qd {
 struct DevState;
 
 constexpr int kConsumerWarps = 8;
+constexpr int kMaxTopK = 64;             // most sampling candidates (qd_set_sampling)
+constexpr int kHeadCandidates = 16384;   // per-CTA head candidates in global scratch (CTAs x top-k)
+// Shared-memory scratch of the block top-k selection, in 32-bit words.
+constexpr int kTopkScratchWords = 256 + kConsumerWarps * 32 + 8 + 2 * kMaxTopK;
 constexpr int kGemvThreads = (kConsumerWarps + 1) * 32;   // 8 consumer warps + 1 producer warp
 constexpr int kAttnThreads = 128;
 constexpr int kAttnMaxSplits = 8;       // splits of a kv group = CTAs of one cluster
@@ -356,11 +360,9 @@ struct PrefillFinishArgs {
     int *status;
 };
 cudaError_t launch_prefill_finish(const PrefillFinishArgs &a, int ns, cudaStream_t s);
-// After a single-stream prefill run through the batched kernels: the first id becomes
-// the model's last output and joins its id history, the position becomes n, and the
-// batch's error bits join the model's.
-cudaError_t launch_prefill_commit(DevState *st, int32_t *ids, int ids_cap, const int32_t *first, int n,
-                                  const int *batch_status, cudaStream_t s);
+// After a single-stream prefill's layers ran through the batched kernels: the model's
+// position becomes `pos` and the batch's error bits join the model's.
+cudaError_t launch_prefill_commit(DevState *st, int pos, const int *batch_status, cudaStream_t s);
 // x[i] = E[tokens[i]] (bf16 table [rows, hidden] -> fp32 [n, hidden]); ids were checked
 // against the table on the host.
 cudaError_t launch_embed_rows(const void *table, const int32_t *tokens, int n, int hidden, float *x, cudaStream_t s);

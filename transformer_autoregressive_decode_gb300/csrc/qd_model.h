@@ -110,11 +110,12 @@ qd_status sync_and_check(qd_model *m, int *out_id);
 // Unbind a frame generator from both of its models (frame_engine.cu); called when
 // either model is destroyed first.
 void frame_detach(qd_frame *fr);
-// Prefill of n positions from device embeddings (or device token ids of the embedding
-// table) through the batched prefill kernels into KV bucket `bucket` (batch_engine.cu);
-// QD_EUNSUPPORTED, with nothing enqueued, where the model or the shapes do not allow it.
-qd_status model_prefill_batched(qd_model *m, const float *embeds_dev, const int32_t *tokens_dev, int n, int head_idx,
-                                int bucket);
+// The layers of a prefill of n positions from device embeddings (or device token ids of
+// the embedding table) through the batched prefill kernels into KV bucket `bucket`; the
+// last position's hidden state lands in x, the position at n - 1, for the head step
+// (batch_engine.cu).  QD_EUNSUPPORTED, with nothing enqueued, where the model or the
+// shapes do not allow it.
+qd_status model_prefill_batched(qd_model *m, const float *embeds_dev, const int32_t *tokens_dev, int n, int bucket);
 
 #define CU(call)                                                                                   \
     do {                                                                                           \
