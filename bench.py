@@ -262,6 +262,18 @@ def gpu_arm(args):
     dec_n = sum(k for _, _, k in evs)
     dec_step_us = 1e3 * dec_ms / dec_n
 
+    # the same decode steps with on-device sampling at the wrapper's default generation
+    # settings ("qwen3-tts-hip OPTIMIZATION_LOG", generation-defaults entry: top-k 50,
+    # temperature 0.9, top-p 1.0): the head's candidate selection and draw on top of
+    # the greedy step
+    qd.qd_set_sampling(h, 50, 0.9, 1.0, 1)
+    tokens.pos = 0
+    evs = []
+    tokens(traj, evs)
+    torch.cuda.synchronize()
+    samp_step_us = 1e3 * sum(a.elapsed_time(b) for a, b, _ in evs) / sum(k for _, _, k in evs)
+    qd.qd_set_sampling(h, 0, 1.0, 1.0, 0)
+
     # whole-step HBM fraction of the decode step (algorithmic bytes: weights + KV at
     # the mean attended length of the trajectory)
     L_avg = shape.prefill + 0.5 * (traj + 1)
@@ -348,6 +360,10 @@ def gpu_arm(args):
                      "frac": step_gbs / hbm_peak, "peak_source": peak_src,
                      "note": f"decode steps only (prefill excluded), {dec_n} steps timed with CUDA events around "
                              f"each device greedy segment; weights + KV at mean L={L_avg:.0f}"},
+        "sampling": {"top_k": 50, "temperature": 0.9, "top_p": 1.0, "decode_step_us": samp_step_us,
+                     "greedy_decode_step_us": dec_step_us,
+                     "note": "the same decode trajectories with qd_set_sampling on: per-CTA top-k selection in "
+                             "the head, last-CTA merge and counter-based draw"},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(k1 - k0), "kernels_per_decode_step": per_step,
         "clocks": clk,
     }

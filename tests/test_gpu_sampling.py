@@ -104,6 +104,35 @@ def test_sampling_persistent_step_equals_per_phase_kernels(shape_name, monkeypat
     assert a == b
 
 
+@pytest.mark.parametrize("shape_name", ["tiny", "asr2"])
+@pytest.mark.parametrize("per_phase", [False, True])
+@pytest.mark.parametrize("k,p", [(50, 1.0), (64, 0.93)])
+def test_all_equal_logits(shape_name, per_phase, k, p, monkeypatch):
+    """A zero LM head makes every logit exactly 0 on both sides (the EOS id -inf): the
+    candidates are the k lowest ids, every per-CTA selection runs into ties and the merge
+    keeps far more entries than it ranks directly.  With exact logits the draws agree
+    without a margin (the cumulative weights are small integers)."""
+    import torch
+    import oracle as O
+    s = SHAPES[shape_name]
+    w = W.model_weights(s)
+    for j in range(s.n_heads_out):
+        w[f"lm_head.{j}"] = np.zeros_like(w[f"lm_head.{j}"])
+    e = W.prefill_embeds(s, 20)
+    if per_phase:
+        monkeypatch.setenv("QD_PER_PHASE", "1")
+    t, seed, n = 0.9, 21, 10
+    got = _free_run(s, w, e, n, (k, t, p, seed))
+    o = O.Oracle(s, w)
+    o.set_sampling(k, t, p, seed)
+    ref = [o.prefill(embeds=e)[0]]
+    for _ in range(n):
+        ref.append(o.step(token=ref[-1])[0])
+    o.close()
+    assert got == ref
+    assert max(ref) < k + 1 and len(set(ref)) > 1
+
+
 def test_sampling_settings_seed_reset_and_errors():
     import torch
     s = SHAPES["asr2"]

@@ -305,107 +305,160 @@ __device__ __forceinline__ uint32_t order_key(float v) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// One 64-bit key per candidate (value, index >= 0): a larger key is the better
+// candidate (the larger value, then the lower index).  The value and the index come
+// back out of it (a -0 as +0).
+__device__ __forceinline__ uint64_t cand_key(float v, int i) {
+    return ((uint64_t)order_key(v) << 32) | (uint32_t)(0x7fffffff - i);
+}
+__device__ __forceinline__ float cand_value(uint64_t c) {
+    const uint32_t k = (uint32_t)(c >> 32);
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+__device__ __forceinline__ int cand_index(uint64_t c) { return 0x7fffffff - (int)(uint32_t)c; }
+
+// Consumer threads (named barrier 1; ck written and synchronised by the caller): the
+// m <= NC keys ck ranked by counting, for each, the keys above it (equal keys -- only
+// identical padding -- by position); the best Ke go to out_v / out_i[0..Ke) and slots
+// Ke..K get -inf / INT_MAX.
+static __device__ __noinline__ void rank_keys(const uint64_t *ck, int m, int Ke, int K, float *out_v, int *out_i) {
+    constexpr int NC = kConsumerWarps * 32;
+    const int tid = threadIdx.x;
+    if (tid < m) {
+        const uint64_t c = ck[tid];
+        int r = 0;
+#pragma unroll 8
+        for (int j = 0; j < m; ++j) {
+            const uint64_t cj = ck[j];
+            r += (int)(cj > c) | ((int)(cj == c) & (int)(j < tid));
+        }
+        if (r < Ke) {
+            out_v[r] = cand_value(c);
+            out_i[r] = cand_index(c);
+        }
+    }
+    if (tid >= Ke && tid < K) {
+        out_v[tid] = -INFINITY;
+        out_i[tid] = INT_MAX;
+    }
+    named_sync(1, NC);
+}
+
 // Consumer threads (named barrier 1): the K (<= kMaxTopK) largest of n values -- value
 // i at vals[i * stride], its index idx[i] (or base + i when idx is null) -- with ties
 // to the lower index, into out_v / out_i[0..K) sorted by value descending, then index
 // ascending; entries past n are -inf / INT_MAX.  Among equal values the indices must
-// ascend with i.  Radix select of the K-th largest key (four 8-bit passes over shared
-// histograms), then every larger key and, in index order, as many equal keys as are
-// needed, then a rank sort.  out_* must not overlap the scratch.
+// ascend with i.  Radix select of the K-th largest key (8-bit passes over shared
+// histograms): as soon as the keys in or above the K-th key's bin fit one per thread
+// they are gathered and ranked; otherwise, after four passes, every larger key and, in
+// index order, as many equal keys as are needed are ranked.  out_* must not overlap
+// the scratch (8-byte aligned, kTopkScratchWords words).
+static_assert(kConsumerWarps * 32 <= 256, "block_topk gathers at most one key per histogram bin");
 static __device__ __noinline__ void block_topk(const float *vals, int stride, const int *idx, int base, int n, int K,
-                                        float *out_v, int *out_i, int *scratch) {
+                                               float *out_v, int *out_i, int *scratch) {
     constexpr int NC = kConsumerWarps * 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // ctl[0]: the bin of the pass, ctl[2]: slot counter, ctl[4 + p]: keys still needed
+    // entering pass p (ctl[8]: equal keys to take after the last pass), ctl[9]: keys in
+    // or above the bin of the pass.  The gathered keys reuse hist and cnt.
     int *hist = scratch, *cnt = scratch + 256, *ctl = cnt + NC;
-    float *tv = reinterpret_cast<float *>(ctl + 8);
+    uint64_t *gk = reinterpret_cast<uint64_t *>(scratch);
+    float *tv = reinterpret_cast<float *>(ctl + 16);
     int *ti = reinterpret_cast<int *>(tv + kMaxTopK);
     const int Ke = K < n ? K : n;
     if (tid == 0) {
-        ctl[1] = Ke;
+        ctl[4] = Ke;
         ctl[2] = 0;
     }
-    if (Ke > 0) {
-        uint32_t prefix = 0, mask = 0;
-        for (int shift = 24; shift >= 0; shift -= 8) {
-            for (int b = tid; b < 256; b += NC) hist[b] = 0;
-            named_sync(1, NC);
-            for (int i = tid; i < n; i += NC) {
-                const uint32_t k = order_key(vals[(size_t)i * stride]);
-                if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
+    if (Ke == 0) {
+        named_sync(1, NC);
+        rank_keys(gk, 0, 0, K, out_v, out_i);
+        return;
+    }
+    uint32_t prefix = 0, mask = 0;
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        for (int b = tid; b < 256; b += NC) hist[b] = 0;
+        named_sync(1, NC);
+        for (int i = tid; i < n; i += NC) {
+            const uint32_t k = order_key(vals[(size_t)i * stride]);
+            if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1);
+        }
+        named_sync(1, NC);
+        if (warp == 0) {
+            // the bin holding the need-th largest key: lane l sums bins 255-8l .. 248-8l,
+            // a prefix sum from the top finds the lane, the lane finds the bin
+            const int need = ctl[4 + pass];
+            int hb[8], sum = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                hb[j] = hist[255 - 8 * lane - j];
+                sum += hb[j];
             }
-            named_sync(1, NC);
-            if (tid == 0) {
-                int cum = 0;
-                const int need = ctl[1];
-                for (int b = 255; b >= 0; --b) {
-                    if (cum + hist[b] >= need) {
-                        ctl[0] = b;
-                        ctl[1] = need - cum;
+            int x = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            const int before = x - sum;
+            if (before < need && need <= x) {
+                int cum = before;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (cum + hb[j] >= need) {
+                        ctl[0] = 255 - 8 * lane - j;
+                        ctl[5 + pass] = need - cum;
+                        ctl[9] = ctl[4] - need + cum + hb[j];
                         break;
                     }
-                    cum += hist[b];
+                    cum += hb[j];
                 }
             }
+        }
+        named_sync(1, NC);
+        prefix |= (uint32_t)ctl[0] << shift;
+        mask |= 255u << shift;
+        if (ctl[9] <= NC) {
+            // every key >= the bin's lower bound, one per thread
+            for (int i = tid; i < n; i += NC) {
+                const float v = vals[(size_t)i * stride];
+                if (order_key(v) >= prefix) gk[atomicAdd(&ctl[2], 1)] = cand_key(v, idx ? idx[i] : base + i);
+            }
             named_sync(1, NC);
-            prefix |= (uint32_t)ctl[0] << shift;
-            mask |= 255u << shift;
+            rank_keys(gk, ctl[2], Ke, K, out_v, out_i);
+            return;
         }
-        const uint32_t kth = prefix;
-        const int take_eq = ctl[1];
-        const int n_gt = Ke - take_eq;
-        // every key above the K-th (in any order)
-        for (int i = tid; i < n; i += NC) {
-            const float v = vals[(size_t)i * stride];
-            if (order_key(v) > kth) {
-                const int s = atomicAdd(&ctl[2], 1);
-                tv[s] = v;
-                ti[s] = idx ? idx[i] : base + i;
-            }
-        }
-        // keys equal to the K-th, lowest indices first: contiguous segments per thread
-        // and an exclusive prefix sum of their counts
-        const int seg = (n + NC - 1) / NC, lo = tid * seg, hi = lo + seg < n ? lo + seg : n;
-        int c = 0;
-        for (int i = lo; i < hi; ++i) c += order_key(vals[(size_t)i * stride]) == kth;
-        int x = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
-        }
-        if (lane == 31) cnt[warp] = x;
-        named_sync(1, NC);
-        int off = x - c;
-        for (int w = 0; w < warp; ++w) off += cnt[w];
-        for (int i = lo; i < hi && off < take_eq; ++i) {
-            const float v = vals[(size_t)i * stride];
-            if (order_key(v) == kth) {
-                tv[n_gt + off] = v;
-                ti[n_gt + off] = idx ? idx[i] : base + i;
-                ++off;
-            }
-        }
-        named_sync(1, NC);
     }
-    // rank sort
-    if (tid < K) {
-        if (tid < Ke) {
-            const float v = tv[tid];
-            const int ix = ti[tid];
-            const uint32_t k = order_key(v);
-            int r = 0;
-            for (int j = 0; j < Ke; ++j) {
-                const uint32_t kj = order_key(tv[j]);
-                r += kj > k || (kj == k && ti[j] < ix);
-            }
-            out_v[r] = v;
-            out_i[r] = ix;
-        } else {
-            out_v[tid] = -INFINITY;
-            out_i[tid] = INT_MAX;
-        }
+    // after four passes prefix is the K-th largest key: every larger key (in any order),
+    // then the equal keys with the lowest indices, from contiguous per-thread segments
+    // placed by an exclusive prefix sum of their counts
+    const uint32_t kth = prefix;
+    const int take_eq = ctl[8];
+    const int n_gt = Ke - take_eq;
+    for (int i = tid; i < n; i += NC) {
+        const float v = vals[(size_t)i * stride];
+        if (order_key(v) > kth) gk[atomicAdd(&ctl[2], 1)] = cand_key(v, idx ? idx[i] : base + i);
+    }
+    const int seg = (n + NC - 1) / NC, lo = tid * seg, hi = lo + seg < n ? lo + seg : n;
+    int c = 0;
+    for (int i = lo; i < hi; ++i) c += order_key(vals[(size_t)i * stride]) == kth;
+    int x = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) cnt[warp] = x;
+    named_sync(1, NC);
+    int off = x - c;
+    for (int w = 0; w < warp; ++w) off += cnt[w];
+    for (int i = lo; i < hi && off < take_eq; ++i) {
+        const float v = vals[(size_t)i * stride];
+        if (order_key(v) == kth) gk[n_gt + off++] = cand_key(v, idx ? idx[i] : base + i);
     }
     named_sync(1, NC);
+    rank_keys(gk, Ke, Ke, K, out_v, out_i);
 }
 
 // SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom number generators",
@@ -421,31 +474,126 @@ __device__ __forceinline__ double uniform53(uint64_t seed, uint64_t counter) {
     return (double)(splitmix64(seed, counter) >> 11) * (1.0 / 9007199254740992.0);
 }
 
-// One thread: the id drawn from K candidates sorted by value: weights
-// exp((v - v_max) / temperature), the smallest prefix reaching top_p of their sum,
-// the first whose running sum exceeds u times the kept sum.
-static __device__ __noinline__ int sample_candidates(const float *cv, const int *ci, int K, float temperature, float top_p,
-                                              double u) {
-    float cum[kMaxTopK];
-    float total = 0.f;
-    for (int i = 0; i < K; ++i) {
-        const float w = cv[i] == -INFINITY ? 0.f : expf((cv[i] - cv[0]) / temperature);
-        total += w;
-        cum[i] = total;
+// Consumer threads (named barrier 1): the K best entries, sorted, of L lists of K
+// entries each in global memory (list c at part_v / part_i [c * K ..]), every list
+// sorted by value descending then index ascending, the lists' index ranges disjoint.
+// No entry worse than the K-th best list head can be among the K best, so only each
+// list's prefix down to that head is kept and selected from (by rank counting when
+// the kept entries fit one per thread, else by block_topk).  sm: 2 * L * K words of
+// scratch (8-byte aligned); scratch: as for block_topk.
+static __device__ __noinline__ void merge_candidate_lists(const float *part_v, const int *part_i, int L, int K,
+                                                          uint64_t *sm, float *out_v, int *out_i, int *scratch) {
+    constexpr int NC = kConsumerWarps * 32;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // the K-th best list head (every list when there are fewer than K)
+    uint64_t tkey = 0;
+    if (L >= K && L <= NC) {
+        if (tid < L) sm[tid] = cand_key(__ldcg(part_v + (size_t)tid * K), __ldcg(part_i + (size_t)tid * K));
+        named_sync(1, NC);
+        rank_keys(sm, L, K, K, out_v, out_i);
+        tkey = cand_key(out_v[K - 1], out_i[K - 1]);
+    } else if (L > NC) {
+        float *hv = reinterpret_cast<float *>(sm);
+        int *hx = reinterpret_cast<int *>(hv + L);
+        for (int c = tid; c < L; c += NC) {
+            hv[c] = __ldcg(part_v + (size_t)c * K);
+            hx[c] = __ldcg(part_i + (size_t)c * K);
+        }
+        named_sync(1, NC);
+        block_topk(hv, 1, hx, 0, L, K, out_v, out_i, scratch);
+        tkey = cand_key(out_v[K - 1], out_i[K - 1]);
     }
-    int m = K;
-    for (int i = 0; i < K; ++i)
-        if (cum[i] >= top_p * total) {
-            m = i + 1;
-            break;
+    // the kept prefixes of this thread's contiguous lists (their first 8 entries loaded
+    // at once: the prefixes are short), then a block prefix sum of their lengths
+    const int seg = (L + NC - 1) / NC, lo = tid * seg, hi = lo + seg < L ? lo + seg : L;
+    int cnt = 0;
+    for (int c = lo; c < hi; ++c) {
+        int m = 0;
+        bool more = true;
+        while (more && m < K) {
+            uint64_t b[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                b[j] = m + j < K ? cand_key(__ldcg(part_v + (size_t)c * K + m + j), __ldcg(part_i + (size_t)c * K + m + j)) : 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                more = more && m < K && b[j] >= tkey;
+                m += more;
+            }
         }
-    const float t = (float)(u * (double)cum[m - 1]);
-    int pick = m - 1;
-    for (int i = 0; i < m; ++i)
-        if (cum[i] > t) {
-            pick = i;
-            break;
+        cnt += m;
+    }
+    int x = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    int *wsum = scratch + 256;   // free between the selections
+    named_sync(1, NC);
+    if (lane == 31) wsum[warp] = x;
+    named_sync(1, NC);
+    int off = x - cnt, total = 0;
+    for (int w = 0; w < kConsumerWarps; ++w) {
+        if (w < warp) off += wsum[w];
+        total += wsum[w];
+    }
+    // kept entries as keys to rank, or (more than one per thread) as values and indices
+    // in list order for the radix select
+    float *kv = reinterpret_cast<float *>(sm);
+    int *ki = reinterpret_cast<int *>(kv + total);
+    for (int c = lo; c < hi; ++c)
+        for (int m = 0; m < K; ++m) {
+            const float v = __ldcg(part_v + (size_t)c * K + m);
+            const int i = __ldcg(part_i + (size_t)c * K + m);
+            const uint64_t k = cand_key(v, i);
+            if (k < tkey) break;
+            if (total <= NC) {
+                sm[off] = k;
+            } else {
+                kv[off] = v;
+                ki[off] = i;
+            }
+            ++off;
         }
+    named_sync(1, NC);
+    if (total <= NC)
+        rank_keys(sm, total, total < K ? total : K, K, out_v, out_i);
+    else
+        block_topk(kv, 1, ki, 0, total, K, out_v, out_i, scratch);
+}
+
+// One warp: the id drawn from K (<= 64) candidates sorted by value: weights
+// exp((v - v_max) / temperature), the smallest prefix reaching top_p of their sum,
+// the first whose running sum exceeds u times the kept sum.  Lane l holds candidates
+// l and l + 32; the running sums are a warp prefix sum.
+static __device__ __noinline__ int warp_sample(const float *cv, const int *ci, int K, float temperature,
+                                               float top_p, double u) {
+    const int lane = threadIdx.x & 31;
+    const float v0 = cv[0];
+    auto weight = [&](int j) {
+        return (j < K && cv[j] != -INFINITY) ? expf((cv[j] - v0) / temperature) : 0.f;
+    };
+    float c0 = weight(lane), c1 = weight(lane + 32);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y0 = __shfl_up_sync(0xffffffffu, c0, o), y1 = __shfl_up_sync(0xffffffffu, c1, o);
+        if (lane >= o) {
+            c0 += y0;
+            c1 += y1;
+        }
+    }
+    c1 += __shfl_sync(0xffffffffu, c0, 31);
+    const float total = __shfl_sync(0xffffffffu, K > 32 ? c1 : c0, (K > 32 ? K - 33 : K - 1) & 31);
+    // the top-p prefix: the first running sum reaching top_p of the total
+    const unsigned r0 = __ballot_sync(0xffffffffu, lane < K && c0 >= top_p * total);
+    const unsigned r1 = __ballot_sync(0xffffffffu, lane + 32 < K && c1 >= top_p * total);
+    const int m = r0 ? __ffs(r0) : (r1 ? 32 + __ffs(r1) : K);
+    const float z = __shfl_sync(0xffffffffu, m > 32 ? c1 : c0, (m - 1) & 31);
+    const float t = (float)(u * (double)z);
+    const unsigned p0 = __ballot_sync(0xffffffffu, lane < m && c0 > t);
+    const unsigned p1 = __ballot_sync(0xffffffffu, lane + 32 < m && c1 > t);
+    const int pick = p0 ? __ffs(p0) - 1 : (p1 ? 32 + __ffs(p1) - 1 : m - 1);
     return ci[pick];
 }
 

@@ -193,8 +193,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a)
         float *cv = reinterpret_cast<float *>(ring);
         int *ci = reinterpret_cast<int *>(cv + kMaxTopK);
         int *scr = ci + kMaxTopK;
-        float *all_v = reinterpret_cast<float *>(scr + kTopkScratchWords);
-        int *all_i = reinterpret_cast<int *>(all_v + (size_t)gridDim.x * (sk > 0 ? sk : 1));
+        uint64_t *all_k = reinterpret_cast<uint64_t *>(scr + kTopkScratchWords);   // 8-byte aligned
         if (sk > 0) {
             named_sync(1, NC);
             block_topk(res, rs, nullptr, row0, nrows, sk, cv, ci, scr);
@@ -249,20 +248,15 @@ __global__ void __launch_bounds__(kGemvThreads, 2) gemv_kernel(const GemvArgs a)
             }
         };
         if (misc_i[5] && sk > 0) {
-            // every CTA's candidates (in CTA order: ascending rows) -> the top-k -> the draw
+            // every CTA's sorted candidates -> merged -> the draw
             __threadfence();
-            const int nc = (int)gridDim.x * sk;
-            for (int i = tid; i < nc; i += NC) {
-                all_v[i] = __ldcg(a.part_v + i);
-                all_i[i] = __ldcg(a.part_i + i);
-            }
-            named_sync(1, NC);
-            block_topk(all_v, 1, all_i, 0, nc, sk, cv, ci, scr);
-            if (tid == 0) {
+            merge_candidate_lists(a.part_v, a.part_i, (int)gridDim.x, sk, all_k, cv, ci, scr);
+            if (warp == 0) {
                 const DevState *st = a.st;
                 const uint64_t seed = ((uint64_t)st->seed_hi << 32) | st->seed_lo;
-                commit(sample_candidates(cv, ci, sk, st->sample_temp, st->sample_top_p,
-                                         uniform53(seed, (uint64_t)st->n_gen)));
+                const int id = warp_sample(cv, ci, sk, st->sample_temp, st->sample_top_p,
+                                           uniform53(seed, (uint64_t)st->n_gen));
+                if (lane == 0) commit(id);
             }
         } else if (misc_i[5] && warp == 0) {
             // reduce the per-CTA argmax candidates

@@ -14,7 +14,9 @@ constexpr int kConsumerWarps = 8;
 constexpr int kMaxTopK = 64;             // most sampling candidates (qd_set_sampling)
 constexpr int kHeadCandidates = 16384;   // per-CTA head candidates in global scratch (CTAs x top-k)
 // Shared-memory scratch of the block top-k selection, in 32-bit words.
-constexpr int kTopkScratchWords = 256 + kConsumerWarps * 32 + 8 + 2 * kMaxTopK;
+constexpr int kTopkScratchWords = 256 + kConsumerWarps * 32 + 16 + 2 * kMaxTopK;
+// the candidate keys after the per-CTA candidates and this scratch are 64-bit
+static_assert((2 * kMaxTopK + kTopkScratchWords) % 2 == 0, "sampling scratch alignment");
 constexpr int kGemvThreads = (kConsumerWarps + 1) * 32;   // 8 consumer warps + 1 producer warp
 constexpr int kAttnThreads = 128;
 constexpr int kAttnMaxSplits = 8;       // splits of a kv group = CTAs of one cluster
