@@ -31,11 +31,11 @@ METRIC = "decode tokens/s at 1 GB300; per-step HBM GB/s as fraction of peak"
 # DRAM bytes (read + write) of one decode_step_kernel launch from one ncu capture
 # (profiles/decode_step_kernel_asr.md), at attended length L, for the kernel sources
 # with this digest; null in the JSON line once the sources differ.
-_STEP_TRAFFIC = {"asr": {"digest": "bda1792e61c6e572", "bytes": 224744704 + 3667712, "L": 116}}
+_STEP_TRAFFIC = {"asr": {"digest": "e36b7235e79f2cac", "bytes": 224748288 + 3366400, "L": 116}}
 _STEP_SOURCES = ("decode_persistent.cu", "decode_common.cuh", "qd_device.cuh")
 # DRAM bytes of one batch_attn_kernel launch (profiles/batch_attn_kernel_batch64.md) at
 # the initial lengths + 3, for the kernel sources with this digest.
-_BATT_TRAFFIC = {"digest": "cb3ff54f9f27eb8e", "bytes": 256617216 + 4111104, "rows": 62239 + 3 * 64}
+_BATT_TRAFFIC = {"digest": "f6747ad5a33a24da", "bytes": 256617472 + 3596800, "rows": 62239 + 3 * 64}
 _BATT_SOURCES = ("batch_kernels.cu", "decode_common.cuh", "qd_device.cuh")
 
 
@@ -240,7 +240,9 @@ def gpu_arm(args):
     barrier()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
+    torch.cuda.nvtx.range_push("timed")
     tokens(args.steps)
+    torch.cuda.nvtx.range_pop()
     ev1.record(stream)
     barrier()
     clk = clocks.stop()
