@@ -53,7 +53,7 @@ class Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "hidden", "n_layers", "n_q_heads", "n_kv_heads", "head_dim", "ffn", "vocab", "embed_rows",
         "w_bf16", "kv_bf16", "qk_norm", "n_heads_out", "eos_mask_id", "n_buckets")] + [
-        ("buckets", ctypes.c_int * 8), ("acc64", ctypes.c_int),
+        ("buckets", ctypes.c_int * 8), ("acc64", ctypes.c_int), ("mrope_section", ctypes.c_int * 3),
         ("rms_eps", ctypes.c_double), ("rope_theta", ctypes.c_double), ("rep_penalty", ctypes.c_double)]
 
 
@@ -75,6 +75,8 @@ def _lib_handle():
             L.orc_forward.restype = i32
             L.orc_prefill.argtypes = [vp, vp, vp, i32, i32, P(i32), vp, P(dp)]
             L.orc_prefill.restype = i32
+            L.orc_prefill_positions.argtypes = [vp, vp, vp, i32, i32, vp, P(i32), vp, P(dp)]
+            L.orc_prefill_positions.restype = i32
             L.orc_get_hidden.argtypes = [vp, vp]
             L.orc_get_hidden.restype = i32
             L.orc_get_kv.argtypes = [vp, i32, i32, vp]
@@ -87,6 +89,10 @@ def _lib_handle():
             L.orc_rmsnorm.restype = None
             L.orc_rope.argtypes = [vp, i32, i32, dp]
             L.orc_rope.restype = None
+            L.orc_rope_mrope.argtypes = [vp, i32, P(i32), P(i32), dp]
+            L.orc_rope_mrope.restype = None
+            L.orc_mrope_stream.argtypes = [i32, P(i32)]
+            L.orc_mrope_stream.restype = i32
             L.orc_attend.argtypes = [vp, vp, vp, i32, i32, vp]
             L.orc_attend.restype = None
             L.orc_penalty_argmax.argtypes = [vp, i32, vp, ctypes.c_float, i32, P(dp)]
@@ -151,6 +157,8 @@ def make_config(shape, acc64: bool = False, buckets: Optional[Sequence[int]] = N
     for i, v in enumerate(b):
         c.buckets[i] = v
     c.acc64 = int(acc64)
+    for i, v in enumerate(getattr(shape, "mrope_section", (0, 0, 0))):
+        c.mrope_section[i] = int(v)
     c.rms_eps, c.rope_theta, c.rep_penalty = shape.rms_eps, shape.rope_theta, shape.rep_penalty
     return c
 
@@ -215,14 +223,24 @@ class Oracle:
         return self.L.orc_smax(self.h)
 
     def prefill(self, embeds: Optional[np.ndarray] = None, tokens: Optional[np.ndarray] = None,
-                head_idx: int = 0, want_logits: bool = True):
+                head_idx: int = 0, want_logits: bool = True, positions: Optional[np.ndarray] = None):
+        """Prefill from position 0; ``positions`` ([3, n] int32: the t, h, w rotary
+        positions of each prompt position) replaces the default (i, i, i)."""
         n = len(embeds) if embeds is not None else len(tokens)
         e = None if embeds is None else np.ascontiguousarray(embeds, dtype=np.float32)
         t = None if tokens is None else np.ascontiguousarray(tokens, dtype=np.int32)
         logits = np.empty(self.shape.vocab, np.float32) if want_logits else None
         fid, margin = ctypes.c_int(-1), ctypes.c_double(0.0)
-        self._check(self.L.orc_prefill(self.h, _ptr(t), _ptr(e), n, head_idx, ctypes.byref(fid),
-                                       _ptr(logits), ctypes.byref(margin)), "prefill")
+        if positions is None:
+            self._check(self.L.orc_prefill(self.h, _ptr(t), _ptr(e), n, head_idx, ctypes.byref(fid),
+                                           _ptr(logits), ctypes.byref(margin)), "prefill")
+        else:
+            pos = np.ascontiguousarray(positions, dtype=np.int32)
+            if pos.shape != (3, n):
+                raise ValueError(f"positions must be [3, {n}], got {pos.shape}")
+            self._check(self.L.orc_prefill_positions(self.h, _ptr(t), _ptr(e), n, head_idx, _ptr(pos),
+                                                     ctypes.byref(fid), _ptr(logits), ctypes.byref(margin)),
+                        "prefill_positions")
         return fid.value, logits, margin.value
 
     def step(self, token: int = -1, embed: Optional[np.ndarray] = None, head_idx: int = 0,
@@ -393,6 +411,22 @@ def rope(v, pos, theta):
     v = np.array(v, dtype=np.float32, copy=True)
     _lib_handle().orc_rope(v.ctypes.data, len(v), int(pos), float(theta))
     return v
+
+
+def rope_mrope(v, pos3, section, theta):
+    """Rotary embedding with one position per stream (t, h, w) and the interleaved
+    section sizes ``section``."""
+    v = np.array(v, dtype=np.float32, copy=True)
+    p = (ctypes.c_int * 3)(*[int(x) for x in pos3])
+    sec = (ctypes.c_int * 3)(*[int(x) for x in section])
+    _lib_handle().orc_rope_mrope(v.ctypes.data, len(v), p, sec, float(theta))
+    return v
+
+
+def mrope_stream(m, section):
+    """The position stream (0 t, 1 h, 2 w) frequency m takes."""
+    sec = (ctypes.c_int * 3)(*[int(x) for x in section])
+    return _lib_handle().orc_mrope_stream(int(m), sec)
 
 
 def attend(q, K, V):

@@ -55,6 +55,7 @@ struct orc_model {
     int top_k;      /* sampling: 0 = greedy */
     double temperature, top_p;
     uint64_t seed;
+    int rope_delta; /* rotary position of a decode step = cache position + rope_delta */
 };
 
 /* ---------------------------------------------------------------- helpers */
@@ -164,10 +165,43 @@ void orc_rmsnorm(const float *x, const float *gamma, int n, double eps, float *o
  * m + head_dim/2, angle pos * theta^(-2m/head_dim); cos/sin are evaluated in
  * fp64 and rounded to fp32, the rotation itself runs in fp32. */
 void orc_rope(float *v, int head_dim, int pos, double theta) {
+    const int pos3[3] = {pos, pos, pos}, plain[3] = {0, 0, 0};
+    orc_rope_mrope(v, head_dim, pos3, plain, theta);
+}
+
+/* Interleaved multimodal RoPE ([ncnn] Talker section: the position encoding comes
+ * in three sections, [24, 20, 20] for head_dim 128, interleaved over the channel
+ * dimension, one position stream each).  Frequency m takes its position from the
+ * stream the interleave deals it: the streams t, h, w in turn, each while it has
+ * frequencies left in its section (once the shorter sections run out, the rest go
+ * to t).  The two channels of a rotation pair (m, m + head_dim/2) share m.  With
+ * every section 0 all frequencies take stream t: plain RoPE. */
+int orc_mrope_stream(int m, const int section[3]) {
+    if (section[0] + section[1] + section[2] == 0) return 0;
+    int left[3] = {section[0], section[1], section[2]};
+    int s = 0;
+    for (int j = 0; j <= m; ++j) {
+        /* deal frequency j to the next stream in turn that still has room */
+        int tries = 0;
+        while (left[s] == 0 && tries < 3) {
+            s = (s + 1) % 3;
+            ++tries;
+        }
+        if (j == m) return s;
+        --left[s];
+        s = (s + 1) % 3;
+    }
+    return 0;
+}
+
+/* Rotary embedding with a position per stream: pair (m, m + head_dim/2) rotates by
+ * pos3[stream(m)] * theta^(-2m/head_dim); cos/sin are evaluated in fp64 and rounded
+ * to fp32, the rotation itself runs in fp32. */
+void orc_rope_mrope(float *v, int head_dim, const int pos3[3], const int section[3], double theta) {
     int half = head_dim / 2;
     for (int m = 0; m < half; ++m) {
         double inv_freq = pow(theta, -2.0 * (double)m / (double)head_dim);
-        double ang = (double)pos * inv_freq;
+        double ang = (double)pos3[orc_mrope_stream(m, section)] * inv_freq;
         float cs = (float)cos(ang), sn = (float)sin(ang);
         float a = v[m], b = v[m + half];
         v[m] = a * cs - b * sn;
@@ -364,6 +398,11 @@ static int validate(const orc_config *c) {
     if (c->head_dim % 2) return ORC_EINVAL;
     if (c->n_heads_out < 1 || c->n_heads_out > ORC_MAX_HEADS) return ORC_EINVAL;
     if (c->n_buckets < 1 || c->n_buckets > ORC_MAX_BUCKETS) return ORC_EINVAL;
+    {
+        const int *sec = c->mrope_section;
+        int sum = sec[0] + sec[1] + sec[2];
+        if (sec[0] < 0 || sec[1] < 0 || sec[2] < 0 || (sum != 0 && sum != c->head_dim / 2)) return ORC_EINVAL;
+    }
     for (int i = 0; i < c->n_buckets; ++i) {
         if (c->buckets[i] <= 0) return ORC_EINVAL;
         if (i && c->buckets[i] <= c->buckets[i - 1]) return ORC_EINVAL;
@@ -413,6 +452,7 @@ int orc_reset(orc_model *m) {
     memset(m->emitted, 0, (size_t)m->emitted_words * 4);
     m->have_hidden = 0;
     m->n_gen = 0;
+    m->rope_delta = 0;
     if (m->bucket != 0) {
         free(m->kv);
         m->bucket = 0;
@@ -489,8 +529,11 @@ static void head_logits(const orc_config *c, const void *const *w, const float *
 
 /* One position through the layer stack with the cache: q/k/v of the new token
  * only, attention over positions [0, pos] ([ncnn] integration section). */
-int orc_forward(orc_model *m, const float *embed, int token, int add_emitted, int want_head,
-                int head_idx, int *out_id, float *logits_raw, float *hidden_taps, double *margin) {
+/* One position; pos3: its rotary positions (t, h, w), or NULL for the decode
+ * rule: cache position + rope_delta in every stream. */
+static int forward_at(orc_model *m, const float *embed, int token, int add_emitted, int want_head,
+                      int head_idx, int *out_id, float *logits_raw, float *hidden_taps, double *margin,
+                      const int *pos3) {
     const orc_config *c = &m->c;
     if (!embed && (token < 0 || token >= c->embed_rows || !m->w[0])) return ORC_EINVAL;
     if (token >= c->vocab && add_emitted) return ORC_EINVAL;
@@ -504,6 +547,8 @@ int orc_forward(orc_model *m, const float *embed, int token, int add_emitted, in
     const int h = c->hidden, hd = c->head_dim, qh = c->n_q_heads, kvh = c->n_kv_heads;
     const int qd = qh * hd, kd = kvh * hd, F = c->ffn, grp = qh / kvh;
     const int L = p + 1;
+    int r3[3] = {p + m->rope_delta, p + m->rope_delta, p + m->rope_delta};
+    if (pos3) memcpy(r3, pos3, sizeof(r3));
     float *x = (float *)malloc(sizeof(float) * (size_t)h);
     float *xn = (float *)malloc(sizeof(float) * (size_t)h);
     float *gam = (float *)malloc(sizeof(float) * (size_t)(h > hd ? h : hd));
@@ -543,9 +588,9 @@ int orc_forward(orc_model *m, const float *embed, int token, int add_emitted, in
                 orc_rmsnorm(tmp, gam, hd, c->rms_eps, k + i * hd);
             }
         }
-        /* RoPE at the absolute position */
-        for (int i = 0; i < qh; ++i) orc_rope(q + i * hd, hd, p, c->rope_theta);
-        for (int i = 0; i < kvh; ++i) orc_rope(k + i * hd, hd, p, c->rope_theta);
+        /* RoPE at the rotary positions (the absolute position unless the prompt gave others) */
+        for (int i = 0; i < qh; ++i) orc_rope_mrope(q + i * hd, hd, r3, c->mrope_section, c->rope_theta);
+        for (int i = 0; i < kvh; ++i) orc_rope_mrope(k + i * hd, hd, r3, c->mrope_section, c->rope_theta);
         /* KV append in the cache's type, then attention reads the cache */
         for (int i = 0; i < kvh; ++i) {
             kv_store(m, l, 0, i, p, k + i * hd);
@@ -600,13 +645,22 @@ int orc_forward(orc_model *m, const float *embed, int token, int add_emitted, in
     return st;
 }
 
+int orc_forward(orc_model *m, const float *embed, int token, int add_emitted, int want_head,
+                int head_idx, int *out_id, float *logits_raw, float *hidden_taps, double *margin) {
+    return forward_at(m, embed, token, add_emitted, want_head, head_idx, out_id, logits_raw, hidden_taps,
+                      margin, NULL);
+}
+
 /* Prefill: positions 0..n-1 in order, head on the last one ([asr]: prefill of
  * the prompt produces the first token; the first bucket is the smallest Smax
  * that holds the prompt).  Prompt tokens do not join the emitted set. */
-int orc_prefill(orc_model *m, const int32_t *tokens, const float *embeds, int n, int head_idx,
-                int *first_id, float *logits_raw, double *margin) {
+static int prefill_impl(orc_model *m, const int32_t *tokens, const float *embeds, int n, int head_idx,
+                        const int32_t *positions, int *first_id, float *logits_raw, double *margin) {
     const orc_config *c = &m->c;
     if (n <= 0 || (!tokens && !embeds)) return ORC_EINVAL;
+    if (positions)
+        for (int i = 0; i < 3 * n; ++i)
+            if (positions[i] < 0) return ORC_EINVAL;
     if (m->pos != 0) return ORC_ESTATE;
     if (n > c->buckets[c->n_buckets - 1]) return ORC_EKVFULL;
     int b = 0;
@@ -618,14 +672,35 @@ int orc_prefill(orc_model *m, const int32_t *tokens, const float *embeds, int n,
         m->kv = calloc(kv_elems(c, m->S), kv_esize(c));
         if (!m->kv) return ORC_ENOMEM;
     }
+    int top = n - 1;
     for (int i = 0; i < n; ++i) {
         int last = (i == n - 1);
-        int st = orc_forward(m, embeds ? embeds + (size_t)i * c->hidden : NULL, tokens ? tokens[i] : -1, 0,
-                             last, head_idx, last ? first_id : NULL, last ? logits_raw : NULL, NULL,
-                             last ? margin : NULL);
+        int p3[3];
+        if (positions) {
+            for (int s = 0; s < 3; ++s) {
+                p3[s] = positions[(size_t)s * n + i];
+                if (p3[s] > top) top = p3[s];
+            }
+        }
+        int st = forward_at(m, embeds ? embeds + (size_t)i * c->hidden : NULL, tokens ? tokens[i] : -1, 0,
+                            last, head_idx, last ? first_id : NULL, last ? logits_raw : NULL, NULL,
+                            last ? margin : NULL, positions ? p3 : NULL);
         if (st) return st;
     }
+    /* decode steps continue after the largest rotary position of the prompt */
+    m->rope_delta = top + 1 - n;
     return ORC_OK;
+}
+
+int orc_prefill(orc_model *m, const int32_t *tokens, const float *embeds, int n, int head_idx,
+                int *first_id, float *logits_raw, double *margin) {
+    return prefill_impl(m, tokens, embeds, n, head_idx, NULL, first_id, logits_raw, margin);
+}
+
+int orc_prefill_positions(orc_model *m, const int32_t *tokens, const float *embeds, int n, int head_idx,
+                          const int32_t *positions, int *first_id, float *logits_raw, double *margin) {
+    if (!positions) return ORC_EINVAL;
+    return prefill_impl(m, tokens, embeds, n, head_idx, positions, first_id, logits_raw, margin);
 }
 
 int orc_get_hidden(const orc_model *m, float *out) {

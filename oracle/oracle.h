@@ -38,6 +38,8 @@ typedef struct {
     int n_buckets;
     int buckets[ORC_MAX_BUCKETS]; /* ascending Smax ladder */
     int acc64;       /* accumulate dot products in fp64 */
+    int mrope_section[3]; /* frequencies per position stream (t, h, w), interleaved;
+                             all 0: plain RoPE (one stream) */
     double rms_eps, rope_theta, rep_penalty;
 } orc_config;
 
@@ -69,6 +71,12 @@ int orc_forward(orc_model *m, const float *embed, int token, int add_emitted, in
 int orc_prefill(orc_model *m, const int32_t *tokens, const float *embeds, int n, int head_idx,
                 int *first_id, float *logits_raw, double *margin);
 
+/* The same prefill with explicit rotary positions: positions[s * n + i] is the
+ * position of prompt position i in stream s (t, h, w).  The decode steps after it
+ * continue at the largest of them + 1, equal in the three streams. */
+int orc_prefill_positions(orc_model *m, const int32_t *tokens, const float *embeds, int n, int head_idx,
+                          const int32_t *positions, int *first_id, float *logits_raw, double *margin);
+
 int orc_get_hidden(const orc_model *m, float *out);        /* final-norm output, last position */
 int orc_get_kv(const orc_model *m, int layer, int which, float *out); /* [kvh, pos, hd] */
 int orc_emitted_words(const orc_model *m, uint32_t *out);  /* bitmask copy */
@@ -93,6 +101,8 @@ int orc_linear(const void *W, int w_bf16, int R, int K, const float *x, int T, f
 /* Primitives the model is built from, exposed for the pins. */
 void orc_rmsnorm(const float *x, const float *gamma, int n, double eps, float *out);
 void orc_rope(float *v, int head_dim, int pos, double theta);
+void orc_rope_mrope(float *v, int head_dim, const int pos3[3], const int section[3], double theta);
+int orc_mrope_stream(int m, const int section[3]);
 void orc_attend(const float *q, const float *K, const float *V, int L, int head_dim, float *out);
 int orc_penalty_argmax(float *logits, int n, const uint32_t *emitted, float penalty, int eos_id,
                        double *margin);

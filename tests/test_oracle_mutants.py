@@ -32,7 +32,10 @@ MUTANTS = {
                                    "matvec(c, W_(m, l, S_WO), h, qd, att, tmp);\n        for (int i = 0; i < h; ++i) x[i] = tmp[i];"),
     "silu_sign": ("gd / (1.0 + exp(-gd))", "gd / (1.0 + exp(gd))"),
     "bf16_truncation": ("u += 0x7fffu + lsb;", "u += 0u * lsb;"),
+    "mrope_streams_h_w_swapped": ("--left[s];\n        s = (s + 1) % 3;", "--left[s];\n        s = (s + 2) % 3;"),
+    "mrope_decode_restarts_at_cache_position": ("m->rope_delta = top + 1 - n;", "m->rope_delta = 0;"),
 }
+PIN_FILES = ("test_oracle_pins.py", "test_oracle_mrope.py")
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
@@ -48,7 +51,7 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
                            "-o", str(lib), str(d / "oracle.c"), "-lm"])
     env = dict(os.environ, ORACLE_LIB=str(lib), OMP_NUM_THREADS="2")
-    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider"] +
+                       [os.path.join(ROOT, "tests", f) for f in PIN_FILES],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"

@@ -132,6 +132,7 @@ class Shape:
     rep_penalty: float = 1.0   # 1.0 = off
     eos_mask_id: int = -1      # id whose logit is forced to -inf (-1: none)
     buckets: tuple = (128,)
+    mrope_section: tuple = (0, 0, 0)   # frequencies per rotary stream (t, h, w); 0s: plain RoPE
     # workload
     prefill: int = 0
     decode_steps: int = 0
