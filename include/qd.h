@@ -86,6 +86,13 @@ typedef struct {
     double rms_eps;     /* e.g. 1e-6 */
     double rope_theta;  /* e.g. 1e6 */
     double rep_penalty; /* 1.0 = off */
+    /* Interleaved multimodal RoPE ("Qwen3-TTS ncnn port", Talker section): the
+     * head_dim/2 rotation frequencies are dealt to three position streams t, h, w
+     * in turn, each while its section has room, the rest to t ([24, 20, 20] for
+     * head_dim 128: frequency m < 60 takes stream m % 3, the last four take t).
+     * All 0: plain RoPE.  Otherwise t >= h == w > 0 and t + h + w == head_dim/2.
+     * The streams differ only for prompt positions given to qd_prefill_mrope. */
+    int mrope_section[3];
 } qd_config;
 
 /* Per-layer weights: device pointers, row-major [out, in], in the config's
@@ -132,6 +139,18 @@ qd_status qd_reset(qd_handle h);
  * first), QD_EKVFULL (n > last bucket), QD_ECUDA, QD_EDEVICE. */
 qd_status qd_prefill(qd_handle h, const int32_t *tokens, const void *embeds, int n, int head_idx,
                      int32_t *first_id);
+
+/* qd_prefill_mrope -- qd_prefill with explicit rotary positions: positions is a
+ * HOST int32 array [3][n], positions[s * n + i] the position of prompt position i
+ * in stream s (t, h, w; see qd_config.mrope_section -- a plain-RoPE model reads
+ * stream t only).  Every position lies in [0, last bucket).  The cache rows are
+ * still 0..n-1; the decode steps that follow rotate at the prompt's largest
+ * position + 1 (then + 2, ...) in all three streams, and qd_reset returns to the
+ * plain positions.  Errors: as qd_prefill, and QD_EINVAL for a NULL positions
+ * array or a position outside [0, last bucket); a decode step whose rotary
+ * position would reach the last bucket returns QD_EKVFULL. */
+qd_status qd_prefill_mrope(qd_handle h, const int32_t *tokens, const void *embeds, int n, int head_idx,
+                           const int32_t *positions, int32_t *first_id);
 
 /* qd_decode_step -- one position.  Input: embed (DEVICE fp32 [hidden]) if non-NULL,
  * else row `token` of the embedding table.  token >= 0 marks the id that entered

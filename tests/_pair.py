@@ -83,11 +83,14 @@ class Pair:
         else:
             t.low_margin.append(step)
 
-    def prefill(self, embeds=None, tokens=None, head_idx=0):
+    def prefill(self, embeds=None, tokens=None, head_idx=0, positions=None):
         torch = self.torch
         e_dev = None if embeds is None else torch.from_numpy(np.ascontiguousarray(embeds)).cuda()
-        got = self.qd.qd_prefill(self.h, tokens=tokens, embeds=e_dev, head_idx=head_idx)
-        rid, rlog, margin = self.ref.prefill(embeds=embeds, tokens=tokens, head_idx=head_idx)
+        if positions is None:
+            got = self.qd.qd_prefill(self.h, tokens=tokens, embeds=e_dev, head_idx=head_idx)
+        else:
+            got = self.qd.qd_prefill_mrope(self.h, positions, tokens=tokens, embeds=e_dev, head_idx=head_idx)
+        rid, rlog, margin = self.ref.prefill(embeds=embeds, tokens=tokens, head_idx=head_idx, positions=positions)
         self._record(got, rid, rlog, margin)
         return rid
 

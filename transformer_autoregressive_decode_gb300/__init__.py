@@ -30,7 +30,7 @@ QD_MAX_HEADS = 16
 QD_FRAME_CODES = 16
 
 # Every symbol the header declares (tests check the library exports each one).
-EXPORTS = ("qd_create", "qd_destroy", "qd_reset", "qd_prefill", "qd_decode_step", "qd_decode_step_async",
+EXPORTS = ("qd_create", "qd_destroy", "qd_reset", "qd_prefill", "qd_prefill_mrope", "qd_decode_step", "qd_decode_step_async",
            "qd_decode_greedy", "qd_grow_kv", "qd_get_hidden", "qd_set_debug_taps", "qd_set_graphs", "qd_set_sampling", "qd_copy_kv",
            "qd_get_emitted", "qd_get_pos", "qd_get_launch_count", "qd_time_kernel", "qd_last_error",
            "qd_status_string", "qd_head_argmax_noalloc", "qd_frame_create", "qd_frame_destroy",
@@ -44,7 +44,8 @@ class qd_config(ctypes.Structure):
         "hidden", "n_layers", "n_q_heads", "n_kv_heads", "head_dim", "ffn", "vocab", "embed_rows", "dtype",
         "qk_norm", "n_heads_out", "eos_mask_id", "n_buckets")] + [
         ("buckets", ctypes.c_int * QD_MAX_BUCKETS),
-        ("rms_eps", ctypes.c_double), ("rope_theta", ctypes.c_double), ("rep_penalty", ctypes.c_double)]
+        ("rms_eps", ctypes.c_double), ("rope_theta", ctypes.c_double), ("rep_penalty", ctypes.c_double),
+        ("mrope_section", ctypes.c_int * 3)]
 
 
 class qd_layer_weights(ctypes.Structure):
@@ -64,6 +65,7 @@ _SIGS = {
     "qd_destroy": ([_vp], _i32),
     "qd_reset": ([_vp], _i32),
     "qd_prefill": ([_vp, _vp, _vp, _i32, _i32, _P(ctypes.c_int32)], _i32),
+    "qd_prefill_mrope": ([_vp, _vp, _vp, _i32, _i32, _vp, _P(ctypes.c_int32)], _i32),
     "qd_decode_step": ([_vp, _vp, ctypes.c_int32, _i32, _P(ctypes.c_int32)], _i32),
     "qd_decode_step_async": ([_vp, _vp, _vp, _i32, _vp], _i32),
     "qd_decode_greedy": ([_vp, _i32, ctypes.c_int32, _vp], _i32),
@@ -139,7 +141,7 @@ def _check(h: Optional[Handle], st: int):
 
 def make_config(hidden, n_layers, n_q_heads, n_kv_heads, head_dim, ffn, vocab, embed_rows, bf16, qk_norm,
                 n_heads_out=1, eos_mask_id=-1, buckets: Sequence[int] = (128,), rms_eps=1e-6, rope_theta=1e6,
-                rep_penalty=1.0) -> qd_config:
+                rep_penalty=1.0, mrope_section: Sequence[int] = (0, 0, 0)) -> qd_config:
     c = qd_config()
     c.hidden, c.n_layers, c.n_q_heads, c.n_kv_heads = hidden, n_layers, n_q_heads, n_kv_heads
     c.head_dim, c.ffn, c.vocab, c.embed_rows = head_dim, ffn, vocab, embed_rows
@@ -149,6 +151,8 @@ def make_config(hidden, n_layers, n_q_heads, n_kv_heads, head_dim, ffn, vocab, e
     for i, b in enumerate(buckets):
         c.buckets[i] = b
     c.rms_eps, c.rope_theta, c.rep_penalty = rms_eps, rope_theta, rep_penalty
+    for i, v in enumerate(mrope_section):
+        c.mrope_section[i] = int(v)
     return c
 
 
@@ -197,6 +201,21 @@ def qd_prefill(h: Handle, tokens=None, embeds=None, head_idx: int = 0) -> int:
     else:
         n = embeds.shape[0] if embeds is not None else 0
         _check(h, _lib.qd_prefill(h.h, None, _ptr(embeds), n, head_idx, ctypes.byref(fid)))
+    return fid.value
+
+
+def qd_prefill_mrope(h: Handle, positions, tokens=None, embeds=None, head_idx: int = 0) -> int:
+    """qd_prefill with rotary positions: host int array [3, n] (t, h, w streams)."""
+    fid = ctypes.c_int32(-1)
+    n = len(tokens) if tokens is not None else (embeds.shape[0] if embeds is not None else 0)
+    pos = np.ascontiguousarray(np.asarray(positions, dtype=np.int32))
+    if pos.shape != (3, n):
+        raise ValueError(f"positions must be [3, {n}], got {pos.shape}")
+    if tokens is not None:
+        arr = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        _check(h, _lib.qd_prefill_mrope(h.h, arr.ctypes.data, None, n, head_idx, pos.ctypes.data, ctypes.byref(fid)))
+    else:
+        _check(h, _lib.qd_prefill_mrope(h.h, None, _ptr(embeds), n, head_idx, pos.ctypes.data, ctypes.byref(fid)))
     return fid.value
 
 

@@ -348,7 +348,8 @@ qd_status ensure_prefill_scratch(qd_batch *b, int ns, int n) {
 // Every launch of a prefill of ns streams x n positions, on the batch's stream.  With
 // with_head false it stops after gathering each stream's last hidden state into
 // pf_last (the caller runs a head on it).
-qd_status enqueue_prefill(qd_batch *b, int ns, int n, int32_t *first_ids, bool with_head = true) {
+qd_status enqueue_prefill(qd_batch *b, int ns, int n, int32_t *first_ids, bool with_head = true,
+                          const int *rope_pos = nullptr, int rope_stride = 0) {
     qd_model *m = b->m;
     const qd_config &c = m->cfg;
     const int h = c.hidden, qd_ = m->q_dim(), rows_qkv = qd_ + 2 * m->kv_dim();
@@ -402,6 +403,10 @@ qd_status enqueue_prefill(qd_batch *b, int ns, int n, int32_t *first_ids, bool w
         qa.eps = (float)c.rms_eps;
         qa.rope_cos = b->rope_cos;
         qa.rope_sin = b->rope_sin;
+        qa.rope_rows = b->S;
+        qa.mrope_h = c.mrope_section[1];
+        qa.rope_pos = rope_pos;
+        qa.rope_stride = rope_stride;
         qa.kv = b->kv;
         qa.stream_elems = b->stream_elems;
         qa.layer_elems = (size_t)l * 2 * c.n_kv_heads * b->S * c.head_dim;
@@ -512,7 +517,8 @@ void batch_leave(qd_batch *b) {
 // runs the model's head step, which gives the first id (greedy or sampled, like every
 // later step) and advances the position to n.  QD_EUNSUPPORTED, with nothing enqueued,
 // when the model or the shapes do not allow it.
-qd_status model_prefill_batched(qd_model *m, const float *embeds_dev, const int32_t *tokens_dev, int n, int bucket) {
+qd_status model_prefill_batched(qd_model *m, const float *embeds_dev, const int32_t *tokens_dev, int n, int bucket,
+                                const int *rope_pos, int rope_stride) {
     const qd_config &c = m->cfg;
     TcGemmPlan plans[5];
     if (!m->bf16 || c.n_heads_out != 1 || !m->embed || !prefill_plans(m, 1, n, plans)) return QD_EUNSUPPORTED;
@@ -541,7 +547,7 @@ qd_status model_prefill_batched(qd_model *m, const float *embeds_dev, const int3
     } else {
         CU(cudaMemcpyAsync(b->pf_x, embeds_dev, (size_t)n * c.hidden * 4, cudaMemcpyDeviceToDevice, b->ls));
     }
-    st = enqueue_prefill(b, 1, n, nullptr, false);
+    st = enqueue_prefill(b, 1, n, nullptr, false, rope_pos, rope_stride);
     if (st) return st;
     // K/V rows [0, n) of every (layer, K/V, kv head) segment into the model's bucket
     const size_t row = (size_t)c.head_dim * m->esize;

@@ -672,6 +672,16 @@ __device__ __forceinline__ void attn_split(const KT *Ks, const KT *Vs, const flo
     }
 }
 
+// Row of the RoPE tables for frequency m.  Interleaved multimodal RoPE deals the
+// frequencies to the position streams t, h, w in turn while the h and w sections (mh
+// frequencies each) have room, the rest to t: frequency m < 3 mh takes stream m % 3.
+// stage: [3][stride] per-stream positions of the staged prompt (position index p), or
+// null for the single position r.  Clamped into the table (the host validates).
+__device__ __forceinline__ int rope_row(int m, int mh, const int *stage, int stride, int p, int r, int rows) {
+    if (stage) r = stage[(m < 3 * mh ? m % 3 : 0) * stride + p];
+    return r < 0 ? 0 : (r >= rows ? rows - 1 : r);
+}
+
 // QK-RMSNorm (if gammas are given) and RoPE at position p of the G query heads in
 // qs and of the key in kn; cos/sin row in rc ([HD/2] cos then [HD/2] sin).
 template <int HD, int NW>

@@ -348,10 +348,14 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnArg
                 bulk_copy_g2s(Vs, vc + (size_t)j0 * HD, bytes, bar, pol);
             }
         }
-        // RoPE table row of position p: constant data
+        // RoPE table rows of the rotary position (the cache position + delta, or per
+        // stream from the staged prompt): constant data during the chain
+        const int *stage = a.st->rope_staged ? a.rope_stage : nullptr;
+        const int pr = p + a.st->rope_delta;
         for (int m = tid; m < HALF; m += kAttnThreads) {
-            rc[m] = a.rope_cos[(size_t)p * HALF + m];
-            rc[HALF + m] = a.rope_sin[(size_t)p * HALF + m];
+            const size_t r = (size_t)rope_row(m, a.mrope_h, stage, a.rope_stride, p, pr, a.rope_rows);
+            rc[m] = a.rope_cos[r * HALF + m];
+            rc[HALF + m] = a.rope_sin[r * HALF + m];
         }
         pdl_wait();
         pdl_launch_dependents();

@@ -222,11 +222,16 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
     float *qs = reinterpret_cast<float *>(smem + a.off_att);
     float *kn = qs + G * HD, *vn = kn + HD, *rc = vn + HD, *qg = rc + HD, *kg = qg + HD, *sc = kg + HD;
     float *po = sc + G * CM, *pm = po + G * HD, *pl = pm + G;
-    if (has_item)
+    if (has_item) {
+        // rotary position: the cache position + delta, or per stream from the staged prompt
+        const int *stage = a.st->rope_staged ? a.rope_stage : nullptr;
+        const int pr = p + a.st->rope_delta;
         for (int m = tid; m < HALF; m += NC) {
-            rc[m] = a.rope_cos[(size_t)p * HALF + m];
-            rc[HALF + m] = a.rope_sin[(size_t)p * HALF + m];
+            const size_t r = (size_t)rope_row(m, a.mrope_h, stage, a.rope_stride, p, pr, a.rope_rows);
+            rc[m] = a.rope_cos[r * HALF + m];
+            rc[HALF + m] = a.rope_sin[r * HALF + m];
         }
+    }
     const int rr_h = warp / a.rs_h, colb_h = (warp % a.rs_h) * (hidden / a.rs_h);
     const int colb_q = (warp % a.rs_q) * (q_dim / a.rs_q);
     const int colb_f = (warp % a.rs_f) * (a.ffn / a.rs_f);

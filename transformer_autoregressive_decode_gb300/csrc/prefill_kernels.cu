@@ -51,7 +51,8 @@ __global__ void __launch_bounds__(kPqThreads) prefill_qk_kernel(const PrefillQkA
 #pragma unroll
                 for (int e = 0; e < DPL; ++e) v[e] = v[e] * inv * gam[lane * DPL + e];
             }
-            // rotate-half RoPE at position j: dims d and d + HD/2 sit 16 lanes apart
+            // rotate-half RoPE at position j (or the prompt's rotary positions): dims d
+            // and d + HD/2 sit 16 lanes apart
             float w[DPL];
 #pragma unroll
             for (int e = 0; e < DPL; ++e) w[e] = __shfl_xor_sync(0xffffffffu, v[e], 16);
@@ -59,7 +60,8 @@ __global__ void __launch_bounds__(kPqThreads) prefill_qk_kernel(const PrefillQkA
 #pragma unroll
             for (int e = 0; e < DPL; ++e) {
                 const int m = (lane & 15) * DPL + e;
-                const float c = a.rope_cos[(size_t)j * HALF + m], sn = a.rope_sin[(size_t)j * HALF + m];
+                const size_t r = (size_t)rope_row(m, a.mrope_h, a.rope_pos, a.rope_stride, j, j, a.rope_rows);
+                const float c = a.rope_cos[r * HALF + m], sn = a.rope_sin[r * HALF + m];
                 v[e] = low ? v[e] * c - w[e] * sn : v[e] * c + w[e] * sn;
             }
         }

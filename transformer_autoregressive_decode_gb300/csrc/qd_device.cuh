@@ -29,15 +29,17 @@ struct DevState {
     int out_id;       // id produced by the last step that ran a head
     int n_gen;        // ids produced since reset (index into the id history)
     int status;       // DEV_ERR_* bits, sticky until reset
+    int rope_delta;   // rotary position of a step = its cache position + rope_delta
+    int rope_staged;  // 1: the rotary positions come per stream from the staged prompt positions
     // sampling (kept by a reset): sample_k 0 = greedy argmax, else top-k candidates,
     // temperature, top-p, and the seed of the counter-based draws (draw n_gen)
     int sample_k;
     float sample_temp, sample_top_p;
     uint32_t seed_lo, seed_hi;
-    int pad[3];
+    int pad[1];
 };
 // bytes of DevState that a reset zeroes (the sampling settings follow them)
-#define QD_DEVSTATE_RESET_BYTES (8 * sizeof(int))
+#define QD_DEVSTATE_RESET_BYTES (10 * sizeof(int))
 
 enum : int {
     IN_TOKEN = 0,          // x = E[token_in]

@@ -78,6 +78,13 @@ static qd_status validate_config(qd_model *m, const qd_config *c) {
     }
     if (!(c->rms_eps >= 0.0) || !(c->rope_theta > 0.0) || !(c->rep_penalty > 0.0))
         return fail(m, QD_EINVAL, "rms_eps, rope_theta, rep_penalty out of range");
+    {
+        const int *sec = c->mrope_section;
+        const bool plain = sec[0] == 0 && sec[1] == 0 && sec[2] == 0;
+        if (!plain && !(sec[1] > 0 && sec[1] == sec[2] && sec[0] >= sec[1] && sec[0] + sec[1] + sec[2] == c->head_dim / 2))
+            return fail(m, QD_EINVAL, "mrope_section (%d, %d, %d): need t >= h == w > 0 and t + h + w == head_dim/2",
+                        sec[0], sec[1], sec[2]);
+    }
     const bool bf = c->dtype == QD_BF16;
     const int max_pos = c->buckets[c->n_buckets - 1];
     if (c->hidden > 16 * 1024)
@@ -176,6 +183,10 @@ static AttnArgs attn_args(qd_model *m, int l) {
     a.scale = (float)(1.0 / std::sqrt((double)c.head_dim));
     a.rope_cos = m->rope_cos;
     a.rope_sin = m->rope_sin;
+    a.rope_rows = m->max_pos;
+    a.mrope_h = c.mrope_section[1];
+    a.rope_stage = m->stage_rpos;
+    a.rope_stride = m->max_pos;
     uint8_t *kvl = reinterpret_cast<uint8_t *>(m->kv[m->cur_bucket]) + (size_t)l * layer_kv;
     a.kcache = kvl;
     a.vcache = kvl + layer_kv / 2;
@@ -306,6 +317,10 @@ static StepArgs step_args(qd_model *m, bool with_head, bool taps) {
     a.chunk_max = m->chunk_max;
     a.rope_cos = m->rope_cos;
     a.rope_sin = m->rope_sin;
+    a.rope_rows = m->max_pos;
+    a.mrope_h = c.mrope_section[1];
+    a.rope_stage = m->stage_rpos;
+    a.rope_stride = m->max_pos;
     a.x = m->x;
     a.qkv = m->qkv;
     a.act = m->act;
@@ -520,7 +535,7 @@ static qd_status alloc_scratch(qd_model *m) {
                  o_pi = take((size_t)kHeadCandidates * 4), o_hc = take(64 * 4), o_stok = take((size_t)m->max_pos * 4),
                  o_ids = take((size_t)kIdsCap * 4), o_em = take((size_t)((c.vocab + 31) / 32) * 4),
                  o_st = take(sizeof(DevState)), o_cos = take((size_t)m->max_pos * (c.head_dim / 2) * 4),
-                 o_sin = take((size_t)m->max_pos * (c.head_dim / 2) * 4);
+                 o_sin = take((size_t)m->max_pos * (c.head_dim / 2) * 4), o_rpos = take((size_t)3 * m->max_pos * 4);
     CU(cudaMalloc(&m->scratch, off));
     CU(cudaMemsetAsync(m->scratch, 0, off, m->ls));
     uint8_t *B = reinterpret_cast<uint8_t *>(m->scratch);
@@ -543,6 +558,7 @@ static qd_status alloc_scratch(qd_model *m) {
     m->st = reinterpret_cast<DevState *>(B + o_st);
     m->rope_cos = reinterpret_cast<float *>(B + o_cos);
     m->rope_sin = reinterpret_cast<float *>(B + o_sin);
+    m->stage_rpos = reinterpret_cast<int *>(B + o_rpos);
     CU(launch_rope_table(m->rope_cos, m->rope_sin, m->max_pos, c.head_dim, c.rope_theta, m->ls));
     CU(cudaMallocHost(&m->pin, 16 * sizeof(int)));
     return QD_OK;
@@ -768,13 +784,26 @@ qd_status qd_reset(qd_handle h) {
     CU(cudaMemsetAsync(m->emitted, 0, (size_t)((m->cfg.vocab + 31) / 32) * 4, m->ls));
     m->h_pos = 0;
     m->h_ngen = 0;
+    m->h_rope_delta = 0;
     m->cur_bucket = 0;
     m->have_hidden = false;
     leave(m);
     return QD_OK;
 }
 
-qd_status qd_prefill(qd_handle h, const int32_t *tokens, const void *embeds, int n, int head_idx, int32_t *first_id) {
+}  // extern "C"
+
+// The rotary-position fields of the device state: the decode steps' delta and whether
+// the steps read the staged prompt positions.
+static qd_status set_rope(qd_model *m, int delta, int staged) {
+    const int v[2] = {delta, staged};
+    // pageable source: staged by the runtime before the call returns
+    CU(cudaMemcpyAsync(&m->st->rope_delta, v, sizeof(v), cudaMemcpyHostToDevice, m->ls));
+    return QD_OK;
+}
+
+static qd_status prefill_impl(qd_handle h, const int32_t *tokens, const void *embeds, int n, int head_idx,
+                              const int32_t *positions, int32_t *first_id) {
     if (!h) return QD_EINVAL;
     qd_model *m = h;
     const qd_config &c = m->cfg;
@@ -792,24 +821,42 @@ qd_status qd_prefill(qd_handle h, const int32_t *tokens, const void *embeds, int
     } else if (!is_device_ptr(embeds)) {
         return fail(m, QD_EINVAL, "embeds is not a device pointer");
     }
+    // the decode steps after the prompt rotate at its largest position + 1
+    int top = n - 1;
+    if (positions)
+        for (int i = 0; i < 3 * n; ++i) {
+            if (positions[i] < 0 || positions[i] >= m->max_pos)
+                return fail(m, QD_EINVAL, "rotary position %d (stream %d, prompt position %d) outside [0, %d)",
+                            positions[i], i / n, i % n, m->max_pos);
+            top = positions[i] > top ? positions[i] : top;
+        }
+    const int delta = top + 1 - n;
     int b = 0;
     while (c.buckets[b] < n) ++b;
     enter(m);
     qd_status st = ensure_bucket(m, b);
     if (st) return st;
     m->cur_bucket = b;
+    if (positions)
+        for (int s = 0; s < 3; ++s)
+            CU(cudaMemcpyAsync(m->stage_rpos + (size_t)s * m->max_pos, positions + (size_t)s * n, (size_t)n * 4,
+                               cudaMemcpyHostToDevice, m->ls));
     if (!m->tap_hidden && !m->tap_logits) {
         // all positions at once through the batched prefill kernels, where they apply
         if (tokens) CU(cudaMemcpyAsync(m->stage_tokens, tokens, (size_t)n * 4, cudaMemcpyHostToDevice, m->ls));
-        st = model_prefill_batched(m, static_cast<const float *>(embeds), tokens ? m->stage_tokens : nullptr, n, b);
+        st = model_prefill_batched(m, static_cast<const float *>(embeds), tokens ? m->stage_tokens : nullptr, n, b,
+                                   positions ? m->stage_rpos : nullptr, m->max_pos);
         if (st == QD_OK) {
             // the head on the last position: the model's own head kernel, as in every step
             st = set_params(m, IN_EMBED, -1, 0, head_idx);
             if (st) return st;
             CU(launch_gemv(GEMV_HEAD, m->bf16, head_args(m, nullptr, 1), m->grid_head, m->smem_head, m->ls, false));
             m->launches += 1;
+            st = set_rope(m, delta, 0);
+            if (st) return st;
             m->h_pos = n;
             m->h_ngen++;
+            m->h_rope_delta = delta;
             m->have_hidden = true;
             st = sync_and_check(m, first_id);
             leave(m);
@@ -821,16 +868,33 @@ qd_status qd_prefill(qd_handle h, const int32_t *tokens, const void *embeds, int
     else CU(cudaMemcpyAsync(m->stage_embeds, embeds, (size_t)n * c.hidden * 4, cudaMemcpyDeviceToDevice, m->ls));
     st = set_params(m, tokens ? IN_STAGED_TOKENS : IN_STAGED_EMBEDS, -1, 0, head_idx);
     if (st) return st;
+    st = set_rope(m, 0, positions ? 1 : 0);
+    if (st) return st;
     for (int i = 0; i < n; ++i) {
         st = run_step(m, i == n - 1);
         if (st) return st;
         m->h_pos++;
     }
+    st = set_rope(m, delta, 0);
+    if (st) return st;
     m->h_ngen++;
+    m->h_rope_delta = delta;
     m->have_hidden = true;
     st = sync_and_check(m, first_id);
     leave(m);
     return st;
+}
+
+extern "C" {
+
+qd_status qd_prefill(qd_handle h, const int32_t *tokens, const void *embeds, int n, int head_idx, int32_t *first_id) {
+    return prefill_impl(h, tokens, embeds, n, head_idx, nullptr, first_id);
+}
+
+qd_status qd_prefill_mrope(qd_handle h, const int32_t *tokens, const void *embeds, int n, int head_idx,
+                           const int32_t *positions, int32_t *first_id) {
+    if (h && !positions) return fail(h, QD_EINVAL, "positions is NULL");
+    return prefill_impl(h, tokens, embeds, n, head_idx, positions, first_id);
 }
 
 static qd_status check_decode(qd_model *m, int head_idx, int n_steps) {
@@ -838,6 +902,9 @@ static qd_status check_decode(qd_model *m, int head_idx, int n_steps) {
     if (head_idx < 0 || head_idx >= m->cfg.n_heads_out) return fail(m, QD_EINVAL, "head_idx %d out of range", head_idx);
     if (m->h_pos + n_steps > m->max_pos)
         return fail(m, QD_EKVFULL, "position %d + %d steps exceeds the last bucket (%d)", m->h_pos, n_steps, m->max_pos);
+    if (m->h_pos + m->h_rope_delta + n_steps > m->max_pos)
+        return fail(m, QD_EKVFULL, "rotary position %d + %d steps exceeds the RoPE table (%d rows)",
+                    m->h_pos + m->h_rope_delta, n_steps, m->max_pos);
     return QD_OK;
 }
 

@@ -81,6 +81,10 @@ struct AttnArgs {
     float eps;
     float scale;                   // 1/sqrt(hd), rounded to fp32 on the host
     const float *rope_cos, *rope_sin;  // [max_pos][hd/2]
+    int rope_rows;                 // rows of the tables
+    int mrope_h;                   // interleaved multimodal RoPE: the h (= w) section size, 0: plain
+    const int *rope_stage;         // [3][rope_stride] staged prompt positions (t, h, w)
+    int rope_stride;
     void *kcache, *vcache;         // this layer's [kvh][S][hd]
     int S;
     int qh, kvh;
@@ -118,6 +122,10 @@ struct StepArgs {
     void *kv;                      // bucket buffer [n_layers][2][kvh][S][hd]
     int S, chunk_max;
     const float *rope_cos, *rope_sin;
+    int rope_rows;                 // rows of the tables
+    int mrope_h;                   // interleaved multimodal RoPE: the h (= w) section size, 0: plain
+    const int *rope_stage;         // [3][rope_stride] staged prompt positions (t, h, w)
+    int rope_stride;
     float *x, *qkv, *act;
     float *part_o;                 // [qh][kAttnMaxSplits][hd]
     float *part_ml;                // [qh][kAttnMaxSplits][2]
@@ -325,6 +333,10 @@ struct PrefillQkArgs {
     const float *q_gamma, *k_gamma;// [hd] or null
     float eps;
     const float *rope_cos, *rope_sin;
+    int rope_rows;                 // rows of the tables
+    int mrope_h;                   // interleaved multimodal RoPE: the h (= w) section size, 0: plain
+    const int *rope_pos;           // [3][rope_stride] rotary positions of the prompt (t, h, w), null: position j
+    int rope_stride;
     void *kv;                      // batch caches [B][n_layers][2][kvh][S][hd] bf16
     size_t stream_elems, layer_elems;
     int S;

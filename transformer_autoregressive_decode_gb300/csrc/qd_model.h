@@ -59,6 +59,8 @@ struct qd_model {
     int cur_bucket = 0;
     int h_pos = 0;
     int h_ngen = 0;
+    int h_rope_delta = 0;          // rotary position of a decode step - its cache position
+    int *stage_rpos = nullptr;     // [3][max_pos] staged prompt rotary positions (t, h, w)
     bool have_hidden = false;
 
     // launch geometry
@@ -115,7 +117,8 @@ void frame_detach(qd_frame *fr);
 // last position's hidden state lands in x, the position at n - 1, for the head step
 // (batch_engine.cu).  QD_EUNSUPPORTED, with nothing enqueued, where the model or the
 // shapes do not allow it.
-qd_status model_prefill_batched(qd_model *m, const float *embeds_dev, const int32_t *tokens_dev, int n, int bucket);
+qd_status model_prefill_batched(qd_model *m, const float *embeds_dev, const int32_t *tokens_dev, int n, int bucket,
+                                const int *rope_pos = nullptr, int rope_stride = 0);
 
 #define CU(call)                                                                                   \
     do {                                                                                           \

@@ -29,4 +29,5 @@ def config_from_shape(s, buckets=None) -> qd_config:
                        head_dim=s.head_dim, ffn=s.ffn, vocab=s.vocab, embed_rows=s.embed_rows, bf16=s.bf16,
                        qk_norm=s.qk_norm, n_heads_out=s.n_heads_out, eos_mask_id=s.eos_mask_id,
                        buckets=tuple(s.buckets if buckets is None else buckets), rms_eps=s.rms_eps,
-                       rope_theta=s.rope_theta, rep_penalty=s.rep_penalty)
+                       rope_theta=s.rope_theta, rep_penalty=s.rep_penalty,
+                       mrope_section=tuple(getattr(s, "mrope_section", (0, 0, 0))))

@@ -256,6 +256,25 @@ def prefill_embeds(s: Shape, n: Optional[int] = None, seed: Optional[int] = None
     return normal(f"{s.name}/{stream}", (n, s.hidden), seed, 0.0, 1.0)
 
 
+def grid_prompt_positions(n: int, text_before: int, grid_h: int, grid_w: int) -> np.ndarray:
+    """Rotary positions [3, n] (t, h, w streams) of a prompt laid out as text, one
+    grid_h x grid_w image, text: the text positions are equal in the three streams
+    and count up; the image holds t at the next position while h and w run over its
+    rows and columns from there; the text after it resumes at the largest position
+    so far + 1.  (The shape of a multimodal prompt; no values of any dataset.)"""
+    assert text_before + grid_h * grid_w <= n
+    pos = np.empty((3, n), np.int32)
+    pos[:, :text_before] = np.arange(text_before)
+    k, b = text_before, text_before
+    for r in range(grid_h):
+        for c in range(grid_w):
+            pos[:, k] = (b, b + r, b + c)
+            k += 1
+    nxt = b + max(grid_h, grid_w)
+    pos[:, k:] = np.arange(nxt, nxt + n - k)
+    return pos
+
+
 def frame_tables(seed: int = 0, rows: int = FRAME_CODE_VOCAB, hidden: int = 1024,
                  bf16: bool = True) -> Dict[str, np.ndarray]:
     """Code-embedding tables of the frame workload: E1..E15 [rows, hidden] ~ N(0, 0.02)
