@@ -276,6 +276,7 @@ def gpu_arm(args):
     samp_step_us = 1e3 * sum(a.elapsed_time(b) for a, b, _ in evs) / sum(k for _, _, k in evs)
     qd.qd_set_sampling(h, 0, 1.0, 1.0, 0)
 
+
     # whole-step HBM fraction of the decode step (algorithmic bytes: weights + KV at
     # the mean attended length of the trajectory)
     L_avg = shape.prefill + 0.5 * (traj + 1)
@@ -337,6 +338,29 @@ def gpu_arm(args):
         cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"prefill {shape.prefill} untimed, then {n} greedy decode tokens ({dt:.1f} s)"}
 
+    # a prompt with distinct rotary streams (text, a 6 x 8 image grid, text) beside the
+    # plain prompt, on a model with interleaved multimodal RoPE sections
+    mrope = None
+    if any(shape.mrope_section):
+        def prefill_ms(positions, reps=10):
+            ts = []
+            for _ in range(reps):
+                qd.qd_reset(h)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                if positions is None:
+                    qd.qd_prefill(h, embeds=e_dev)
+                else:
+                    qd.qd_prefill_mrope(h, positions, embeds=e_dev)
+                b.record(stream)
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b))
+            return float(np.median(ts[2:]))
+        grid = W.grid_prompt_positions(shape.prefill, shape.prefill // 6, 6, 8)
+        mrope = {"section": list(shape.mrope_section), "prefill_ms_plain": prefill_ms(None),
+                 "prefill_ms_grid_positions": prefill_ms(grid),
+                 "note": f"qd_prefill vs qd_prefill_mrope of the {shape.prefill}-position prompt (median of 8 "
+                         "after 2), text + 6 x 8 image grid + text positions"}
     qd.qd_destroy(h)
     if rank != 0:
         return
@@ -366,6 +390,7 @@ def gpu_arm(args):
                      "greedy_decode_step_us": dec_step_us,
                      "note": "the same decode trajectories with qd_set_sampling on: per-CTA top-k selection in "
                              "the head, last-CTA merge and counter-based draw"},
+        **({"mrope": mrope} if mrope else {}),
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(k1 - k0), "kernels_per_decode_step": per_step,
         "clocks": clk,
     }
