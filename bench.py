@@ -338,30 +338,38 @@ def gpu_arm(args):
         cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"prefill {shape.prefill} untimed, then {n} greedy decode tokens ({dt:.1f} s)"}
 
+    qd.qd_destroy(h)
+    # the same Talker weights with the interleaved multimodal RoPE sections [24, 20, 20]:
     # a prompt with distinct rotary streams (text, a 6 x 8 image grid, text) beside the
-    # plain prompt, on a model with interleaved multimodal RoPE sections
+    # plain prompt
     mrope = None
-    if any(shape.mrope_section):
+    if args.workload == "talker":
+        ms_shape = W.scaled(shape, name="talker_mrope", mrope_section=(24, 20, 20))
+        dev_w = upload(w_np)
+        hm = qd.qd_create(dev_w, config_from_shape(ms_shape))
+        del dev_w
+
         def prefill_ms(positions, reps=10):
             ts = []
             for _ in range(reps):
-                qd.qd_reset(h)
+                qd.qd_reset(hm)
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
                 if positions is None:
-                    qd.qd_prefill(h, embeds=e_dev)
+                    qd.qd_prefill(hm, embeds=e_dev)
                 else:
-                    qd.qd_prefill_mrope(h, positions, embeds=e_dev)
+                    qd.qd_prefill_mrope(hm, positions, embeds=e_dev)
                 b.record(stream)
                 torch.cuda.synchronize()
                 ts.append(a.elapsed_time(b))
             return float(np.median(ts[2:]))
         grid = W.grid_prompt_positions(shape.prefill, shape.prefill // 6, 6, 8)
-        mrope = {"section": list(shape.mrope_section), "prefill_ms_plain": prefill_ms(None),
+        mrope = {"section": [24, 20, 20], "prefill_ms_plain_positions": prefill_ms(None),
                  "prefill_ms_grid_positions": prefill_ms(grid),
-                 "note": f"qd_prefill vs qd_prefill_mrope of the {shape.prefill}-position prompt (median of 8 "
-                         "after 2), text + 6 x 8 image grid + text positions"}
-    qd.qd_destroy(h)
+                 "note": f"a second handle on the same weights with mRoPE sections: qd_prefill vs "
+                         f"qd_prefill_mrope of the {shape.prefill}-position prompt (median of 8 after 2), "
+                         "text + 6 x 8 image grid + text positions"}
+        qd.qd_destroy(hm)
     if rank != 0:
         return
     line = {

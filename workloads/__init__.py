@@ -179,7 +179,7 @@ ASR = Shape("asr", hidden=512, n_layers=8, n_q_heads=8, n_kv_heads=8, head_dim=6
             eos_mask_id=151645, buckets=(128, 256, 512), prefill=110, decode_steps=290)
 TALKER = Shape("talker", hidden=1024, n_layers=28, n_q_heads=16, n_kv_heads=8, head_dim=128,
                ffn=3072, vocab=3072, embed_rows=3072, bf16=True, qk_norm=True, rep_penalty=1.05,
-               buckets=(128, 256, 512, 1024), mrope_section=(24, 20, 20), prefill=64, decode_steps=600)
+               buckets=(128, 256, 512, 1024), prefill=64, decode_steps=600)
 CODE_PREDICTOR = Shape("code_predictor", hidden=1024, n_layers=5, n_q_heads=16, n_kv_heads=8,
                        head_dim=128, ffn=3072, vocab=2048, embed_rows=0, bf16=True, qk_norm=True,
                        n_heads_out=15, rep_penalty=1.0, buckets=(32,), prefill=2, decode_steps=14)
