@@ -14,7 +14,7 @@
 //    dynamic window mechanism": the arithmetic of each phase (shared with the
 //    per-phase kernels through decode_common.cuh).
 //
-// Phases of layer l (each followed by a grid barrier):
+// Phases of layer l:
 //   A  x^ = RMSNorm(x), qkv = [Wq;Wk;Wv] x^   (layer 0 also resolves the step input)
 //   B  attention: CTA i < kv_heads * splits takes (group, split) i; QK-norm, RoPE, KV
 //      append, scores/softmax/P.V of the split -> partials
@@ -22,6 +22,16 @@
 //   D  x^ = RMSNorm(x), act = silu(Wg x^) * (Wu x^)
 //   E  x += Wd act
 // then the head: y = RMSNorm(x), logits, penalty, EOS mask, argmax (last CTA reduces).
+//
+// Between phases.  The vectors every CTA gathers (qkv after A, x after C and E, act
+// after D) are also written as 64-bit words {tag, value}, the tag naming the launch
+// (a sequence number advanced once per launch) and the phase; a reader polls the words
+// it needs until their tags match, so the data and its readiness travel in one access
+// and these four boundaries need no barrier round trip.  A buffer is only rewritten
+// after every CTA has read its previous contents: each rewrite depends, through the
+// chain of gathers, on every CTA having finished the phase that read them.  Only the
+// attention partials (B -> C) cross a grid barrier, which also orders the plain
+// writes of the step input and the emitted set.
 #include "decode_common.cuh"
 
 namespace qd {
@@ -51,6 +61,73 @@ __device__ __forceinline__ bool grid_sync(unsigned *counter, unsigned &epoch, in
     }
     named_sync(1, kConsumerWarps * 32);
     return *flag != 0;
+}
+
+// Tagged words: the value's bits low, the tag high, in one 64-bit access.
+__device__ __forceinline__ void st_tagged(uint64_t *p, float v, uint32_t tag) {
+    const uint64_t w = ((uint64_t)tag << 32) | __float_as_uint(v);
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_tagged(const uint64_t *p) {
+    uint64_t w;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+    return w;
+}
+// The tag of phase k of layer l in the launch with sequence number seq (1 + 5l + k < 256).
+__device__ __forceinline__ uint32_t phase_tag(uint32_t seq, int l, int k) { return (seq << 8) | (uint32_t)(1 + 5 * l + k); }
+
+struct TagSeg {                    // dst[i] = value of src[i], i < n
+    const uint64_t *src;
+    int n;
+    float *dst;
+};
+// Consumer threads: the values of up to three tagged segments once their tags equal
+// `tag`, into shared memory.  Each thread loads a batch of words at once and re-polls
+// every still-stale word of the batch together (one round trip per poll, not one per
+// word), for at most kWaitLimitNs.  False (uniform across the CTA) on timeout.  Ends
+// with a consumer barrier.
+__device__ __noinline__ bool gather_tagged(TagSeg s0, TagSeg s1, TagSeg s2, uint32_t tag) {
+    constexpr int NC = kConsumerWarps * 32, B = 8;
+    const int tid = threadIdx.x;
+    const int n01 = s0.n + s1.n, n = n01 + s2.n;
+    bool ok = true;
+    unsigned long long t0 = 0;
+    for (int base = tid; base < n; base += B * NC) {
+        const uint64_t *src[B];
+        uint64_t w[B];
+        unsigned pending = 0;
+#pragma unroll
+        for (int k = 0; k < B; ++k) {
+            const int i = base + k * NC;
+            src[k] = i < s0.n ? s0.src + i : (i < n01 ? s1.src + (i - s0.n) : s2.src + (i - n01));
+            w[k] = i < n ? ld_tagged(src[k]) : (uint64_t)tag << 32;
+        }
+#pragma unroll
+        for (int k = 0; k < B; ++k)
+            if ((uint32_t)(w[k] >> 32) != tag) pending |= 1u << k;
+        while (pending && ok) {
+            const unsigned long long t = global_timer_ns();
+            if (t0 == 0) t0 = t;
+            else if (t - t0 > kWaitLimitNs) ok = false;
+#pragma unroll
+            for (int k = 0; k < B; ++k)
+                if ((pending >> k) & 1u) w[k] = ld_tagged(src[k]);
+#pragma unroll
+            for (int k = 0; k < B; ++k)
+                if ((uint32_t)(w[k] >> 32) == tag) pending &= ~(1u << k);
+        }
+#pragma unroll
+        for (int k = 0; k < B; ++k) {
+            const int i = base + k * NC;
+            if (i >= n) continue;
+            float *dst = i < s0.n ? s0.dst + i : (i < n01 ? s1.dst + (i - s0.n) : s2.dst + (i - n01));
+            *dst = __uint_as_float((uint32_t)w[k]);
+        }
+    }
+    return !named_sync_or(1, NC, !ok);
+}
+__device__ __forceinline__ bool gather_tagged(const uint64_t *src, int n, float *dst, uint32_t tag) {
+    return gather_tagged(TagSeg{src, n, dst}, TagSeg{nullptr, 0, nullptr}, TagSeg{nullptr, 0, nullptr}, tag);
 }
 
 // Stage a vector of weights (gamma) into shared memory (consumer threads).
@@ -238,6 +315,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
     uint32_t sidx = 0;
     unsigned epoch = 0;
     bool ok = true;
+    // this launch's sequence number (advanced once every CTA has read it: at the commit)
+    const uint32_t seq = *reinterpret_cast<volatile const unsigned *>(a.seq);
 
     for (int l = 0; l < a.n_layers && ok; ++l) {
         const LayerDev &Ld = a.layers[l];
@@ -248,10 +327,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
             if (l == 0) {
                 step_input_slice<WT, NS_H>(a.in, a.st, hidden, a.rs_h, colb_h, xr, misc_i, a.x, a.tap_hidden);
             } else {
-                ok = grid_sync(a.barrier, epoch, flag);
+                ok = gather_tagged(a.x_t, hidden, xin, phase_tag(seq, l - 1, 4));
                 if (!ok) break;
-                load_vec_smem(a.x, hidden, xin);
-                named_sync(1, NC);
                 smem_slice<WT, NS_H>(xin, colb_h, xr);
                 if (a.tap_hidden && blockIdx.x == 0 && rr_h == 0) {
 #pragma unroll
@@ -270,26 +347,22 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
             float v = 0.f;
             for (int j = 0; j < a.rs_h; ++j) v += res[r * a.rs_h + j];
             a.qkv[r0_qkv + r] = v;
+            st_tagged(a.qkv_t + r0_qkv + r, v, phase_tag(seq, l, 0));
         }
         if (has_item && Ld.q_norm)
             for (int i = tid; i < HD; i += NC) {
                 qg[i] = Ld.q_norm[i];
                 kg[i] = Ld.k_norm[i];
             }
-        ok = grid_sync(a.barrier, epoch, flag);
-        if (!ok) break;
 
         // ---- B: attention of this CTA's (group, split)
         if (has_item) {
-            const float *qsrc = a.qkv + (size_t)ig * G * HD;
-            const float *ksrc = a.qkv + (size_t)q_dim + (size_t)ig * HD;
-            const float *vsrc = a.qkv + (size_t)(q_dim + kv_dim) + (size_t)ig * HD;
-            for (int i = tid; i < G * HD; i += NC) qs[i] = __ldcg(qsrc + i);
-            for (int i = tid; i < HD; i += NC) {
-                kn[i] = __ldcg(ksrc + i);
-                vn[i] = __ldcg(vsrc + i);
-            }
-            named_sync(1, NC);
+            // the group's q heads, k and v, as their writers tag them
+            ok = gather_tagged(TagSeg{a.qkv_t + (size_t)ig * G * HD, G * HD, qs},
+                               TagSeg{a.qkv_t + (size_t)q_dim + (size_t)ig * HD, HD, kn},
+                               TagSeg{a.qkv_t + (size_t)(q_dim + kv_dim) + (size_t)ig * HD, HD, vn},
+                               phase_tag(seq, l, 0));
+            if (!ok) break;
             qk_norm_rope<HD, kConsumerWarps>(qs, kn, G, Ld.q_norm ? qg : nullptr, kg, a.eps, rc, 1);
             const uint8_t *kslot = slot_acquire(R, sidx);
             const uint8_t *vslot = kslot ? slot_acquire(R, sidx + 1) : nullptr;
@@ -346,17 +419,16 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
                 float v = 0.f;
                 for (int j = 0; j < a.rs_q; ++j) v += res[tid * a.rs_q + j];
                 a.x[r0_o + tid] = xold + v;
+                st_tagged(a.x_t + r0_o + tid, xold + v, phase_tag(seq, l, 2));
             }
         }
         stage_vec(gsm, Ld.mlp_norm, hidden);
-        ok = grid_sync(a.barrier, epoch, flag);
-        if (!ok) break;
 
         // ---- D: act = silu(Wg x^) * (Wu x^), x^ = RMSNorm(x)
         {
             float xr[NS_H * EPL];
-            load_vec_smem(a.x, hidden, xin);
-            named_sync(1, NC);
+            ok = gather_tagged(a.x_t, hidden, xin, phase_tag(seq, l, 2));
+            if (!ok) break;
             smem_slice<WT, NS_H>(xin, colb_h, xr);
             rmsnorm_slice<WT, NS_H>(xr, gsm, hidden, a.rs_h, colb_h, a.eps, misc, nullptr);
             const bool got = gemv_consume<WT, NS_H>(R, sidx, n_gu, a.rps_h, rb_h, a.rs_h, colb_h, xr, res);
@@ -369,17 +441,17 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
                 g += res[(2 * i) * a.rs_h + j];
                 u += res[(2 * i + 1) * a.rs_h + j];
             }
-            a.act[r0_gu / 2 + i] = g / (1.0f + expf(-g)) * u;
+            const float act = g / (1.0f + expf(-g)) * u;
+            a.act[r0_gu / 2 + i] = act;
+            st_tagged(a.act_t + r0_gu / 2 + i, act, phase_tag(seq, l, 3));
         }
-        ok = grid_sync(a.barrier, epoch, flag);
-        if (!ok) break;
 
-        // ---- E: x += Wd act
+        // ---- E: x += Wd act (x rows: this thread's own, written in C)
         {
             const float xold = tid < n_d ? __ldcg(a.x + r0_d + tid) : 0.f;
             float xr[NS_F * EPL];
-            load_vec_smem(a.act, a.ffn, xin);
-            named_sync(1, NC);
+            ok = gather_tagged(a.act_t, a.ffn, xin, phase_tag(seq, l, 3));
+            if (!ok) break;
             smem_slice<WT, NS_F>(xin, colb_f, xr);
             const bool got = gemv_consume<WT, NS_F>(R, sidx, n_d, a.rps_f, rb_f, a.rs_f, colb_f, xr, res);
             ok = !named_sync_or(1, NC, !got);
@@ -388,6 +460,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
                 float v = 0.f;
                 for (int j = 0; j < a.rs_f; ++j) v += res[tid * a.rs_f + j];
                 a.x[r0_d + tid] = xold + v;
+                st_tagged(a.x_t + r0_d + tid, xold + v, phase_tag(seq, l, 4));
             }
         }
     }
@@ -399,11 +472,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
         const int nw = n_hd > 0 ? ((r0_hd + n_hd - 1) >> 5) - w0 + 1 : 0;
         if (a.penalty != 1.0f)
             for (int i = tid; i < nw; i += NC) emw[i] = __ldcg(a.in.emitted + w0 + i);
-        ok = grid_sync(a.barrier, epoch, flag);
+        ok = gather_tagged(a.x_t, hidden, xin, phase_tag(seq, a.n_layers - 1, 4));
         if (ok) {
             float xr[NS_H * EPL];
-            load_vec_smem(a.x, hidden, xin);
-            named_sync(1, NC);
             smem_slice<WT, NS_H>(xin, colb_h, xr);
             if (a.tap_hidden && blockIdx.x == 0 && rr_h == 0) {
 #pragma unroll
@@ -495,6 +566,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
                 else atomicOr(&st->status, DEV_ERR_IDS_FULL);
                 st->n_gen = n + 1;
                 st->pos = p + 1;
+                atomicMax(a.seq, seq + 1);
             };
             if (misc_i[5] && sk > 0) {
                 // every CTA's sorted candidates -> merged -> the draw
@@ -539,7 +611,10 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
             if (a.tap_hidden)
                 for (int i = tid; i < hidden; i += NC)
                     a.tap_hidden[(size_t)a.n_layers * hidden + i] = __ldcg(a.x + i);
-            if (tid == 0) a.st->pos = p + 1;
+            if (tid == 0) {
+                a.st->pos = p + 1;
+                atomicMax(a.seq, seq + 1);
+            }
         }
     }
 
@@ -548,6 +623,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
         named_sync(1, NC);
         if (tid == 0) {
             atomicOr(&a.st->status, DEV_ERR_WAIT_TIMEOUT);
+            atomicMax(a.seq, seq + 1);   // no tag of this launch is ever taken as fresh
             ctl[0] = 1;
             const unsigned long long t0 = global_timer_ns();
             while (!ctl[2] && global_timer_ns() - t0 < 2 * kWaitLimitNs + 100000000ull) {

@@ -343,6 +343,12 @@ static StepArgs step_args(qd_model *m, bool with_head, bool taps) {
     a.tap_logits = taps ? m->tap_logits : nullptr;
     a.barrier = m->barrier;
     a.st = m->st;
+    if (m->tag_buf) {
+        a.x_t = m->tag_buf;
+        a.act_t = a.x_t + c.hidden;
+        a.qkv_t = a.act_t + c.ffn;
+        a.seq = reinterpret_cast<unsigned *>(a.qkv_t + m->q_dim() + 2 * m->kv_dim());
+    }
     return a;
 }
 
@@ -620,6 +626,7 @@ static qd_status setup_persistent(qd_model *m) {
     if (!persistent_supported(m->bf16, c.head_dim, c.hidden, m->q_dim(), c.ffn)) return QD_OK;
     const int G = c.n_q_heads / c.n_kv_heads;
     if (c.n_kv_heads * kAttnMaxSplits > m->num_sms) return QD_OK;
+    if (c.n_layers > 50) return QD_OK;              // phase tags: 1 + 5 * layer + phase < 256
     if (m->chunk_max * c.head_dim * (int)m->esize > kSlotBytes) return QD_OK;
     // rows of any phase held by one CTA, times the warps per row
     auto rmax = [&](int rows, int unit) { return (rows / unit + m->num_sms - 1) / m->num_sms * unit; };
@@ -671,6 +678,12 @@ static qd_status setup_persistent(qd_model *m) {
     }
     CU(cudaMalloc(&m->d_layers, sizeof(LayerDev) * c.n_layers));
     CU(cudaMemcpy(m->d_layers, host.data(), sizeof(LayerDev) * c.n_layers, cudaMemcpyHostToDevice));
+    // tagged vectors (all tags 0: never a launch's) and the sequence number, from 1
+    const size_t words = (size_t)c.hidden + c.ffn + m->q_dim() + 2 * m->kv_dim() + 1;
+    CU(cudaMalloc(&m->tag_buf, words * 8));
+    CU(cudaMemset(m->tag_buf, 0, words * 8));
+    const unsigned one = 1;
+    CU(cudaMemcpy(m->tag_buf + words - 1, &one, sizeof(one), cudaMemcpyHostToDevice));
     m->persistent = true;
     return QD_OK;
 }
@@ -709,6 +722,7 @@ static void destroy_model(qd_model *m) {
         if (p) cudaFree(p);
     if (m->arena) cudaFree(m->arena);
     if (m->d_layers) cudaFree(m->d_layers);
+    if (m->tag_buf) cudaFree(m->tag_buf);
     if (m->scratch) cudaFree(m->scratch);
     if (m->pin) cudaFreeHost(m->pin);
     if (m->ev_in) cudaEventDestroy(m->ev_in);

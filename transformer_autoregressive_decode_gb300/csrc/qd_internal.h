@@ -141,6 +141,8 @@ struct StepArgs {
     int ids_cap;
     float *tap_hidden, *tap_logits;
     unsigned *barrier;             // zeroed before every launch
+    uint64_t *x_t, *act_t, *qkv_t; // tagged copies of the gathered vectors: [hidden], [ffn], [q + 2 kv]
+    unsigned *seq;                 // launch sequence number (starts at 1, never reset)
     DevState *st;
 };
 

@@ -78,6 +78,7 @@ struct qd_model {
     qd_batch *pf_batch = nullptr;
     cudaEvent_t pf_ev[2] = {nullptr, nullptr};
     qd::LayerDev *d_layers = nullptr;
+    uint64_t *tag_buf = nullptr;   // persistent step: tagged x, act, qkv, then the launch sequence number
     unsigned *barrier = nullptr;
     float *part_o = nullptr, *part_ml = nullptr;
     size_t smem_step = 0;
