@@ -89,6 +89,14 @@ def _lib_handle():
             L.orc_rmsnorm.restype = None
             L.orc_rope.argtypes = [vp, i32, i32, dp]
             L.orc_rope.restype = None
+            L.orc_f32_to_f16.argtypes = [ctypes.c_float]
+            L.orc_f32_to_f16.restype = ctypes.c_uint16
+            L.orc_f16_to_f32.argtypes = [ctypes.c_uint16]
+            L.orc_f16_to_f32.restype = ctypes.c_float
+            L.orc_quantize_q8.argtypes = [vp, i32, i32, vp, vp]
+            L.orc_quantize_q8.restype = i32
+            L.orc_gemv_q8.argtypes = [vp, vp, i32, i32, vp, vp]
+            L.orc_gemv_q8.restype = i32
             L.orc_rope_mrope.argtypes = [vp, i32, P(i32), P(i32), dp]
             L.orc_rope_mrope.restype = None
             L.orc_mrope_stream.argtypes = [i32, P(i32)]
@@ -463,3 +471,36 @@ def num_threads() -> int:
 
 def set_threads(n: int):
     _lib_handle().orc_set_threads(int(n))
+
+
+def f32_to_f16(f) -> int:
+    """IEEE half bits of a float (round to nearest even)."""
+    return int(_lib_handle().orc_f32_to_f16(float(np.float32(f))))
+
+
+def f16_to_f32(h) -> float:
+    return float(_lib_handle().orc_f16_to_f32(int(h)))
+
+
+def quantize_q8(w: np.ndarray):
+    """Codes int8 [rows, K] and half-bit scales uint16 [rows, K/32] of W [rows, K] (fp32)."""
+    w = np.ascontiguousarray(w, np.float32)
+    rows, K = w.shape
+    codes = np.empty((rows, K), np.int8)
+    scales = np.empty((rows, K // 32), np.uint16)
+    st = _lib_handle().orc_quantize_q8(w.ctypes.data, rows, K, codes.ctypes.data, scales.ctypes.data)
+    if st != OK:
+        raise OracleError(st, "quantize_q8")
+    return codes, scales
+
+
+def gemv_q8(codes: np.ndarray, scales: np.ndarray, x: np.ndarray) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, np.int8)
+    scales = np.ascontiguousarray(scales, np.uint16)
+    x = np.ascontiguousarray(x, np.float32)
+    rows, K = codes.shape
+    y = np.empty(rows, np.float32)
+    st = _lib_handle().orc_gemv_q8(codes.ctypes.data, scales.ctypes.data, rows, K, x.ctypes.data, y.ctypes.data)
+    if st != OK:
+        raise OracleError(st, "gemv_q8")
+    return y

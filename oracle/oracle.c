@@ -67,6 +67,85 @@ static inline float bf16_to_f32(uint16_t b) {
     return f;
 }
 
+/* IEEE half from float, round to nearest even (subnormals and overflow to infinity
+ * included): the storage of the 8-bit blocks' scales. */
+uint16_t orc_f32_to_f16(float f) {
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    const uint32_t sign = (u >> 16) & 0x8000u;
+    const uint32_t absu = u & 0x7fffffffu;
+    if (absu > 0x7f800000u) return (uint16_t)(sign | 0x7e00u);          /* NaN */
+    if (absu >= 0x477ff000u) return (uint16_t)(sign | 0x7c00u);         /* rounds past 65504 */
+    const int e = (int)(absu >> 23) - 127;
+    if (e >= -14) {                                                     /* normal half */
+        uint32_t mant = absu & 0x7fffffu;
+        uint32_t h = ((uint32_t)(e + 15) << 10) | (mant >> 13);
+        const uint32_t rest = mant & 0x1fffu;
+        if (rest > 0x1000u || (rest == 0x1000u && (h & 1u))) ++h;       /* carries into the exponent */
+        return (uint16_t)(sign | h);
+    }
+    if (e < -25) return (uint16_t)sign;                                 /* below half the least subnormal */
+    /* subnormal: the value in units of 2^-24, rounded to nearest even */
+    const uint32_t mant = (absu & 0x7fffffu) | 0x800000u;
+    const int shift = -e - 1;                                           /* 14 .. 24 */
+    uint32_t h = mant >> shift;
+    const uint32_t rest = mant & ((1u << shift) - 1u), half = 1u << (shift - 1);
+    if (rest > half || (rest == half && (h & 1u))) ++h;
+    return (uint16_t)(sign | h);
+}
+
+float orc_f16_to_f32(uint16_t h) {
+    const uint32_t sign = (uint32_t)(h & 0x8000u) << 16;
+    const int e = (h >> 10) & 0x1f;
+    const uint32_t m = h & 0x3ffu;
+    float f;
+    if (e == 0x1f) {
+        uint32_t u = sign | 0x7f800000u | (m << 13);
+        memcpy(&f, &u, 4);
+        return f;
+    }
+    if (e == 0) {
+        f = (float)m * 5.9604644775390625e-8f;                         /* m * 2^-24, exact */
+        return sign ? -f : f;
+    }
+    uint32_t u = sign | ((uint32_t)(e - 15 + 127) << 23) | (m << 13);
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+int orc_quantize_q8(const float *w, int rows, int K, int8_t *codes, uint16_t *scales) {
+    if (rows < 0 || K <= 0 || K % 32) return ORC_EINVAL;
+    for (int r = 0; r < rows; ++r)
+        for (int b = 0; b < K / 32; ++b) {
+            const float *blk = w + (size_t)r * K + (size_t)b * 32;
+            float amax = 0.0f;
+            for (int i = 0; i < 32; ++i) {
+                const float a = fabsf(blk[i]);
+                if (a > amax) amax = a;
+            }
+            const float d = amax / 127.0f;
+            for (int i = 0; i < 32; ++i) {
+                const float q = d > 0.0f ? roundf(blk[i] / d) : 0.0f;
+                codes[(size_t)r * K + (size_t)b * 32 + i] = (int8_t)q;
+            }
+            scales[(size_t)r * (K / 32) + b] = orc_f32_to_f16(d);
+        }
+    return ORC_OK;
+}
+
+int orc_gemv_q8(const int8_t *codes, const uint16_t *scales, int rows, int K, const float *x, float *y) {
+    if (rows < 0 || K <= 0 || K % 32) return ORC_EINVAL;
+    for (int r = 0; r < rows; ++r) {
+        double acc = 0.0;
+        for (int k = 0; k < K; ++k) {
+            const float wq = (float)codes[(size_t)r * K + k] * orc_f16_to_f32(scales[(size_t)r * (K / 32) + k / 32]);
+            acc += (double)(wq * x[k]);
+        }
+        y[r] = (float)acc;
+    }
+    return ORC_OK;
+}
+
 /* Round-to-nearest-even float -> bfloat16 (the KV-cache storage rounding). */
 uint16_t orc_round_bf16(float f) {
     uint32_t u;

@@ -130,6 +130,17 @@ double orc_uniform(uint64_t seed, uint64_t counter);
 int orc_sample(const float *logits, int n, int top_k, double temperature, double top_p, double u,
                double *margin);
 uint16_t orc_round_bf16(float f);
+
+/* Weight-only 8-bit block quantisation (the talker's Q8_0 weights, "audio.cpp Rockchip
+ * NPU build notes"): each row of W [rows, K] in blocks of 32 along K; per block the
+ * scale d = max|w| / 127 (fp32), the codes round(w / d) (half away from zero, fp32
+ * division; 0 for an all-zero block), d stored as IEEE half.  K % 32 == 0. */
+uint16_t orc_f32_to_f16(float f);   /* round to nearest even */
+float orc_f16_to_f32(uint16_t h);
+int orc_quantize_q8(const float *w, int rows, int K, int8_t *codes, uint16_t *scales);
+/* y[r] = sum_k (codes[r][k] * half(scales[r][k / 32])) * x[k], fp32 products summed in
+ * fp64 in index order, rounded to fp32. */
+int orc_gemv_q8(const int8_t *codes, const uint16_t *scales, int rows, int K, const float *x, float *y);
 int orc_num_threads(void);
 void orc_set_threads(int n);
 
