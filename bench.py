@@ -305,6 +305,40 @@ def gpu_arm(args):
     head_bytes = shape.vocab * shape.hidden * (2 if shape.bf16 else 4)
     head_ms = qd.qd_time_kernel(h, qd.KERNEL_HEAD, 20)
 
+    # the same head as weight-only 8-bit blocks (qd_quantize_q8 / qd_gemv_q8): 1 + 1/16
+    # bytes per weight; the GEMV alone, on the HBM roofline, beside the bf16 head GEMV
+    q8 = None
+    if shape.bf16 and shape.hidden in (512, 1024, 2048):
+        from transformer_autoregressive_decode_gb300.torch_io import to_device
+        w_head = to_device(w_np["lm_head.0"])
+        codes = torch.empty((shape.vocab, shape.hidden), dtype=torch.int8, device="cuda")
+        scales = torch.empty((shape.vocab, shape.hidden // 32), dtype=torch.int16, device="cuda")
+        qd.qd_quantize_q8(w_head, codes, scales)
+        del w_head
+        xq = torch.from_numpy(W.normal("bench/q8_x", (shape.hidden,), 0, 0.0, 1.0)).cuda()
+        yq = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
+        # L2 flushed (256 MB written) before every timed launch: the codes fit in L2
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        ts = []
+        for _ in range(12):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            qd.qd_gemv_q8(codes, scales, xq, yq)
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        del flush
+        q8_ms = float(np.median(ts[2:]))
+        q8_bytes = shape.vocab * shape.hidden * (1 + 2 / 32)
+        q8 = {"kernel": "gemv_q8_kernel (qd_gemv_q8)", "rows": shape.vocab, "K": shape.hidden,
+              "bytes": q8_bytes, "avg_launch_ms": q8_ms, "achieved_gbs": q8_bytes / (q8_ms / 1e3) / 1e9,
+              "frac": q8_bytes / (q8_ms / 1e3) / 1e9 / hbm_peak, "peak_source": peak_src,
+              "bf16_head_gemv_ms": head_ms,
+              "note": "the LM head quantised to 32-weight blocks with half scales; median of 10 launches "
+                      "(after 2), each between CUDA events after a 256 MB write that flushes L2"}
+        del codes, scales
+
     # end to end through the public API with host buffers: the prompt embeddings
     # come from pinned host memory each trajectory, the token goes in and the id
     # comes out through host memory every step (synchronising call)
@@ -399,6 +433,7 @@ def gpu_arm(args):
                      "note": "the same decode trajectories with qd_set_sampling on: per-CTA top-k selection in "
                              "the head, last-CTA merge and counter-based draw"},
         **({"mrope": mrope} if mrope else {}),
+        **({"q8_head_gemv": q8} if q8 else {}),
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(k1 - k0), "kernels_per_decode_step": per_step,
         "clocks": clk,
     }

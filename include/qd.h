@@ -210,6 +210,29 @@ qd_status qd_set_graphs(qd_handle h, int enable);
  * large for this model's head layout). */
 qd_status qd_set_sampling(qd_handle h, int top_k, float temperature, float top_p, uint64_t seed);
 
+/* qd_quantize_q8 -- weight-only 8-bit block quantisation of W (DEVICE [rows, K],
+ * row-major, fp32 or bf16 per dtype): per row, blocks of 32 weights along K, each with
+ * the scale d = max|w| / 127 (fp32 division) stored as an IEEE half in scales (DEVICE
+ * uint16 [rows, K/32]) and the codes round(w / d) (fp32 division, half away from
+ * zero; 0 for an all-zero block) in codes (DEVICE int8 [rows, K]) -- the talker's
+ * Q8_0 weights of "audio.cpp Rockchip NPU build notes" ("The talker is the only
+ * DRAM-bound candidate, and it is not at the ceiling").  K a multiple of 32.  Runs on
+ * cuda_stream and synchronises it.  Errors: QD_EINVAL (shape, dtype, a non-device
+ * pointer), QD_ECUDA. */
+qd_status qd_quantize_q8(const void *w_dev, int dtype, int rows, int K, int8_t *codes_dev, uint16_t *scales_dev,
+                         void *cuda_stream);
+
+/* qd_gemv_q8 -- y[r] = sum_k codes[r][k] * d[r][k/32] * x[k] for the layout of
+ * qd_quantize_q8 (codes DEVICE int8 [rows, K], 16-byte aligned; scales DEVICE half
+ * bits [rows, K/32]; x DEVICE fp32 [K], 16-byte aligned; y DEVICE fp32 [rows]): 1 +
+ * 1/16 bytes per weight streamed once.  K is 512, 1024 or 2048.  Asynchronous: the kernel
+ * is enqueued on cuda_stream; when avg_ms (HOST) is non-NULL it is then launched
+ * `reps` more times between CUDA events, synchronised, and the mean duration of those
+ * launches is written there.
+ * Errors: QD_EINVAL (arguments, alignment), QD_EUNSUPPORTED (K), QD_ECUDA. */
+qd_status qd_gemv_q8(const int8_t *codes_dev, const uint16_t *scales_dev, const float *x_dev, float *y_dev, int rows,
+                     int K, void *cuda_stream, int reps, float *avg_ms);
+
 /* qd_gemm_bf16 -- the batched paths' tensor-core contraction on its own (a check
  * and measurement tap): out[t][r] = sum_k W[r][k] * x[t][k] for W (DEVICE bf16
  * [R, K] row-major, 16-byte aligned) and x (DEVICE fp32 [T, K] row-major), with x

@@ -34,7 +34,7 @@ EXPORTS = ("qd_create", "qd_destroy", "qd_reset", "qd_prefill", "qd_prefill_mrop
            "qd_decode_greedy", "qd_grow_kv", "qd_get_hidden", "qd_set_debug_taps", "qd_set_graphs", "qd_set_sampling", "qd_copy_kv",
            "qd_get_emitted", "qd_get_pos", "qd_get_launch_count", "qd_time_kernel", "qd_last_error",
            "qd_status_string", "qd_head_argmax_noalloc", "qd_frame_create", "qd_frame_destroy",
-           "qd_frame_generate", "qd_frame_set_graphs", "qd_gemm_bf16", "qd_batch_create", "qd_batch_destroy",
+           "qd_frame_generate", "qd_frame_set_graphs", "qd_gemm_bf16", "qd_quantize_q8", "qd_gemv_q8", "qd_batch_create", "qd_batch_destroy",
            "qd_batch_set_stream", "qd_batch_decode", "qd_batch_sync", "qd_batch_get_logits", "qd_batch_copy_kv",
            "qd_batch_get_pos", "qd_batch_get_launch_count", "qd_batch_set_graphs", "qd_batch_time_kernel", "qd_batch_prefill")
 
@@ -87,6 +87,8 @@ _SIGS = {
     "qd_frame_generate": ([_vp, _i32, _vp, _vp, _vp, _vp], _i32),
     "qd_frame_set_graphs": ([_vp, _i32], _i32),
     "qd_gemm_bf16": ([_vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _i32, _P(ctypes.c_float)], _i32),
+    "qd_quantize_q8": ([_vp, _i32, _i32, _i32, _vp, _vp, _vp], _i32),
+    "qd_gemv_q8": ([_vp, _vp, _vp, _vp, _i32, _i32, _vp, _i32, _P(ctypes.c_float)], _i32),
     "qd_batch_create": ([_vp, _i32, _i32, _P(_vp)], _i32),
     "qd_batch_destroy": ([_vp], _i32),
     "qd_batch_set_stream": ([_vp, _i32, _vp, _i32, ctypes.c_int32], _i32),
@@ -455,3 +457,30 @@ def qd_batch_prefill(b: BatchHandle, streams, embeds_dev, first_ids_dev):
     if len(arr) != ns:
         raise ValueError("one stream index per prompt")
     _check(b.model, _lib.qd_batch_prefill(b.b, arr.ctypes.data, ns, _ptr(embeds_dev), n, _ptr(first_ids_dev)))
+
+
+def qd_quantize_q8(w_dev, codes_dev, scales_dev, stream=None):
+    """Weight-only 8-bit block quantisation of the device matrix w_dev [rows, K] (fp32 or
+    bf16) into codes_dev (int8 [rows, K]) and scales_dev (half bits, int16/uint16
+    [rows, K/32])."""
+    import torch
+    rows, K = w_dev.shape
+    s = (stream or torch.cuda.current_stream()).cuda_stream
+    st = _lib.qd_quantize_q8(_ptr(w_dev), QD_BF16 if w_dev.dtype == torch.bfloat16 else QD_F32, rows, K,
+                             _ptr(codes_dev), _ptr(scales_dev), s)
+    if st != QD_OK:
+        raise QDError(st, "qd_quantize_q8 failed")
+
+
+def qd_gemv_q8(codes_dev, scales_dev, x_dev, y_dev, stream=None, time_reps: int = 0):
+    """y = dequant(codes, scales) x on the device; returns the mean kernel time (ms) of
+    ``time_reps`` extra launches, or None."""
+    import torch
+    rows, K = codes_dev.shape
+    s = (stream or torch.cuda.current_stream()).cuda_stream
+    ms = ctypes.c_float(0.0)
+    st = _lib.qd_gemv_q8(_ptr(codes_dev), _ptr(scales_dev), _ptr(x_dev), _ptr(y_dev), rows, K, s, int(time_reps),
+                         ctypes.byref(ms) if time_reps else None)
+    if st != QD_OK:
+        raise QDError(st, "qd_gemv_q8 failed")
+    return ms.value if time_reps else None

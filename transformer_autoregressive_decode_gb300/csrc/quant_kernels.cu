@@ -1,0 +1,214 @@
+// Weight-only 8-bit block quantisation and its GEMV.
+//
+// Sources (page title, section):
+//  - "audio.cpp Rockchip NPU build notes", "The talker is the only DRAM-bound candidate,
+//    and it is not at the ceiling": the talker's matrices stream as Q8_0 weights every
+//    token, and the bytes of the weight stream are what a decode step pays for.  The
+//    layout read here: each row in blocks of 32 weights along K, one half-precision
+//    scale d = max|w| / 127 per block, codes round(w / d) (half away from zero; an
+//    all-zero block has d = 0 and codes 0).  The product y = W x then reads 1 + 1/16
+//    bytes per weight instead of 2 (bf16).
+//
+// qd_quantize_q8: one warp per block (lane = weight); the maximum by a warp reduction,
+// then the same fp32 division and rounding as the definition, so the codes are exact.
+// qd_gemv_q8: HBM-bound streaming.  A lane owns 16 consecutive codes of every row
+// (one 16-byte load per 512 columns; K = 512, 1024 or 2048), their x values sit in
+// registers, and a warp keeps 4 loads per lane in flight (4, 2 or 1 rows; two CTAs of
+// 16 warps per SM for K = 512: occupancy beat double-buffering the loads); int8 ->
+// fp32 goes through the exponent of 2^23 (exact for |code| <= 128) instead of a
+// conversion instruction; each 16-code chunk's partial sum is scaled by its block's
+// scale.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "qd.h"
+#include "qd_device.cuh"
+#include "qd_internal.h"
+#include "qd_model.h"
+
+namespace qd {
+namespace {
+
+constexpr int kQBlock = 32;
+constexpr int kGemvQWarps = 16;
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T v);
+template <>
+__device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T>
+__global__ void __launch_bounds__(256) quantize_q8_kernel(const T *w, long long n_blocks, int8_t *codes,
+                                                          uint16_t *scales) {
+    const int lane = threadIdx.x & 31;
+    const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+    for (long long b = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < n_blocks; b += warps) {
+        const float v = to_f32(w[b * kQBlock + lane]);
+        float amax = fabsf(v);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float d = __fdiv_rn(amax, 127.0f);
+        const float q = d > 0.0f ? roundf(__fdiv_rn(v, d)) : 0.0f;
+        codes[b * kQBlock + lane] = (int8_t)q;
+        if (lane == 0) scales[b] = __half_as_ushort(__float2half_rn(d));
+    }
+}
+
+__device__ __forceinline__ uint4 ld_stream16(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Dot product of the 16 codes of `u` with x[0..16): each code c becomes the float
+// 2^23 + (c + 128) through its biased byte, minus 2^23 + 128, exactly.
+__device__ __forceinline__ float dot16(const uint4 &u, const float *x) {
+    const uint32_t w[4] = {u.x ^ 0x80808080u, u.y ^ 0x80808080u, u.z ^ 0x80808080u, u.w ^ 0x80808080u};
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const float c = __uint_as_float(__byte_perm(w[j], 0x4B000000u, 0x7540u + b)) - 8388736.0f;
+            acc = fmaf(c, x[4 * j + b], acc);
+        }
+    }
+    return acc;
+}
+
+template <int NCH, int MINB>
+__global__ void __launch_bounds__(kGemvQWarps * 32, MINB)
+    gemv_q8_kernel(const int8_t *codes, const uint16_t *scales, const float *x, float *y, int rows) {
+    constexpr int K = NCH * 512;
+    constexpr int RU = 4 / NCH;   // rows per warp in flight
+    const int lane = threadIdx.x & 31;
+    float xr[NCH * 16];
+#pragma unroll
+    for (int c = 0; c < NCH; ++c)
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+            const float4 f = *reinterpret_cast<const float4 *>(x + c * 512 + lane * 16 + e);
+            xr[c * 16 + e] = f.x;
+            xr[c * 16 + e + 1] = f.y;
+            xr[c * 16 + e + 2] = f.z;
+            xr[c * 16 + e + 3] = f.w;
+        }
+    const int warps = gridDim.x * kGemvQWarps;
+    for (int r0 = (blockIdx.x * kGemvQWarps + (threadIdx.x >> 5)) * RU; r0 < rows; r0 += warps * RU) {
+        uint4 u[RU][NCH];
+        float s[RU][NCH];
+#pragma unroll
+        for (int q = 0; q < RU; ++q) {
+            const int r = r0 + q < rows ? r0 + q : rows - 1;
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) {
+                u[q][c] = ld_stream16(codes + (size_t)r * K + c * 512 + lane * 16);
+                s[q][c] = __half2float(__ushort_as_half(__ldg(scales + (size_t)r * (K / kQBlock) + c * 16 + lane / 2)));
+            }
+        }
+        float acc[RU];
+#pragma unroll
+        for (int q = 0; q < RU; ++q) {
+            acc[q] = 0.f;
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) acc[q] = fmaf(dot16(u[q][c], xr + c * 16), s[q][c], acc[q]);
+        }
+#pragma unroll
+        for (int q = 0; q < RU; ++q)
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
+        if (lane < RU && r0 + lane < rows) {
+            float v = acc[0];
+#pragma unroll
+            for (int q = 1; q < RU; ++q) v = lane == q ? acc[q] : v;
+            y[r0 + lane] = v;
+        }
+    }
+}
+
+typedef void (*GemvQFn)(const int8_t *, const uint16_t *, const float *, float *, int);
+
+GemvQFn gemv_q8_fn(int nch) {
+    switch (nch) {
+        case 1: return gemv_q8_kernel<1, 2>;
+        case 2: return gemv_q8_kernel<2, 1>;
+        case 4: return gemv_q8_kernel<4, 1>;
+        default: return nullptr;
+    }
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+}  // namespace qd
+
+using namespace qd;
+
+extern "C" {
+
+qd_status qd_quantize_q8(const void *w_dev, int dtype, int rows, int K, int8_t *codes_dev, uint16_t *scales_dev,
+                         void *cuda_stream) {
+    if (rows <= 0 || K <= 0 || K % kQBlock || (dtype != QD_F32 && dtype != QD_BF16)) return QD_EINVAL;
+    if (!is_device_ptr(w_dev) || !is_device_ptr(codes_dev) || !is_device_ptr(scales_dev)) return QD_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    const long long n_blocks = (long long)rows * (K / kQBlock);
+    const int grid = (int)std::min<long long>((n_blocks + 7) / 8, (long long)sm_count() * 16);
+    if (dtype == QD_BF16)
+        quantize_q8_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(w_dev), n_blocks,
+                                                               codes_dev, scales_dev);
+    else
+        quantize_q8_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float *>(w_dev), n_blocks, codes_dev,
+                                                       scales_dev);
+    if (cudaGetLastError() != cudaSuccess) return QD_ECUDA;
+    return cudaStreamSynchronize(s) == cudaSuccess ? QD_OK : QD_ECUDA;
+}
+
+qd_status qd_gemv_q8(const int8_t *codes_dev, const uint16_t *scales_dev, const float *x_dev, float *y_dev, int rows,
+                     int K, void *cuda_stream, int reps, float *avg_ms) {
+    if (rows <= 0 || K <= 0 || reps < 0) return QD_EINVAL;
+    if (!is_device_ptr(codes_dev) || !is_device_ptr(scales_dev) || !is_device_ptr(x_dev) || !is_device_ptr(y_dev))
+        return QD_EINVAL;
+    if (!aligned(codes_dev, 16) || !aligned(x_dev, 16) || !aligned(scales_dev, 2)) return QD_EINVAL;
+    const GemvQFn fn = K % 512 == 0 ? gemv_q8_fn(K / 512) : nullptr;
+    if (!fn) return QD_EUNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    const int nch = K / 512, per_cta = kGemvQWarps * (4 / nch);
+    const int grid = std::max(1, std::min((rows + per_cta - 1) / per_cta, (nch == 1 ? 2 : 1) * sm_count()));
+    fn<<<grid, kGemvQWarps * 32, 0, s>>>(codes_dev, scales_dev, x_dev, y_dev, rows);
+    if (cudaGetLastError() != cudaSuccess) return QD_ECUDA;
+    if (reps > 0 && avg_ms) {
+        cudaEvent_t e0, e1;
+        if (cudaEventCreate(&e0) != cudaSuccess) return QD_ECUDA;
+        if (cudaEventCreate(&e1) != cudaSuccess) {
+            cudaEventDestroy(e0);
+            return QD_ECUDA;
+        }
+        cudaEventRecord(e0, s);
+        for (int i = 0; i < reps; ++i) fn<<<grid, kGemvQWarps * 32, 0, s>>>(codes_dev, scales_dev, x_dev, y_dev, rows);
+        cudaEventRecord(e1, s);
+        const bool ok = cudaEventSynchronize(e1) == cudaSuccess && cudaGetLastError() == cudaSuccess;
+        float ms = 0.f;
+        cudaEventElapsedTime(&ms, e0, e1);
+        *avg_ms = ms / (float)reps;
+        cudaEventDestroy(e0);
+        cudaEventDestroy(e1);
+        if (!ok) return QD_ECUDA;
+    }
+    return QD_OK;
+}
+
+}  // extern "C"
