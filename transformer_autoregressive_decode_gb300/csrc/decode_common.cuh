@@ -205,14 +205,20 @@ __device__ __forceinline__ void rmsnorm_slice(float *xr, const float *gsm, int K
     for (int j = 0; j < rs; ++j) tot += misc[j];
     const float inv = 1.0f / sqrtf(tot / (float)K + eps);
     const bool wy = y_out != nullptr && rr == 0;
+    // the gammas (and y) four at a time: a lane's EPL columns are contiguous, so one
+    // scalar access per column would put every fourth (fp32: eighth) lane on one bank
 #pragma unroll
     for (int sg = 0; sg < NSEG; ++sg)
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) {
+        for (int e = 0; e < EPL; e += 4) {
             const int i = sg * EPL + e;
             const int col = colbase + sg * SEGW + lane * EPL + e;
-            xr[i] = xr[i] * inv * gsm[col];
-            if (wy) y_out[col] = xr[i];
+            const float4 g = *reinterpret_cast<const float4 *>(gsm + col);
+            xr[i] = xr[i] * inv * g.x;
+            xr[i + 1] = xr[i + 1] * inv * g.y;
+            xr[i + 2] = xr[i + 2] * inv * g.z;
+            xr[i + 3] = xr[i + 3] * inv * g.w;
+            if (wy) *reinterpret_cast<float4 *>(y_out + col) = make_float4(xr[i], xr[i + 1], xr[i + 2], xr[i + 3]);
         }
     named_sync(1, kConsumerWarps * 32);   // misc is reused by the caller
 }

@@ -181,8 +181,9 @@ __device__ __forceinline__ void combine_to_smem(const float *part_o, const float
                 den = fmaf(m_l[t].y, w, den);
             }
         }
-#pragma unroll
-        for (int e = 0; e < CPT; ++e) dst[c0 + e] = acc[e] / den;
+        // two 16-byte stores (one per column would put every fourth lane on one bank)
+        *reinterpret_cast<float4 *>(dst + c0) = make_float4(acc[0] / den, acc[1] / den, acc[2] / den, acc[3] / den);
+        *reinterpret_cast<float4 *>(dst + c0 + 4) = make_float4(acc[4] / den, acc[5] / den, acc[6] / den, acc[7] / den);
     }
 }
 
