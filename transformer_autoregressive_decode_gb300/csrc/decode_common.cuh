@@ -626,7 +626,16 @@ __device__ __forceinline__ void attn_split(const KT *Ks, const KT *Vs, const flo
         float kf[EPL];
         Elem<KT>::unpack(*reinterpret_cast<const uint4 *>(Ks + (size_t)jj * HD + l8 * EPL), kf);
         for (int hh = 0; hh < G; ++hh) {
-            const float *q = qs + hh * HD + l8 * EPL;
+            // this lane's EPL query values as float4 loads (scalar loads: 2-way bank conflicts)
+            float q[EPL];
+#pragma unroll
+            for (int e = 0; e < EPL; e += 4) {
+                const float4 q4 = *reinterpret_cast<const float4 *>(qs + hh * HD + l8 * EPL + e);
+                q[e] = q4.x;
+                q[e + 1] = q4.y;
+                q[e + 2] = q4.z;
+                q[e + 3] = q4.w;
+            }
             float d = 0.f;
 #pragma unroll
             for (int e = 0; e < EPL; ++e) d = fmaf(q[e], kf[e], d);
@@ -660,18 +669,23 @@ __device__ __forceinline__ void attn_split(const KT *Ks, const KT *Vs, const flo
         float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f, c0 = 0.f, c1 = 0.f, e0 = 0.f, e1 = 0.f;
         int j = 0;
         for (; j + 4 <= n; j += 4) {
-            a0 = fmaf(p[j], Elem<KT>::load(Vs + (size_t)j * HD, d), a0);
-            a1 = fmaf(p[j], Elem<KT>::load(Vs + (size_t)j * HD, d + 1), a1);
-            b0 = fmaf(p[j + 1], Elem<KT>::load(Vs + (size_t)(j + 1) * HD, d), b0);
-            b1 = fmaf(p[j + 1], Elem<KT>::load(Vs + (size_t)(j + 1) * HD, d + 1), b1);
-            c0 = fmaf(p[j + 2], Elem<KT>::load(Vs + (size_t)(j + 2) * HD, d), c0);
-            c1 = fmaf(p[j + 2], Elem<KT>::load(Vs + (size_t)(j + 2) * HD, d + 1), c1);
-            e0 = fmaf(p[j + 3], Elem<KT>::load(Vs + (size_t)(j + 3) * HD, d), e0);
-            e1 = fmaf(p[j + 3], Elem<KT>::load(Vs + (size_t)(j + 3) * HD, d + 1), e1);
+            const float2 v0 = Elem<KT>::load2(Vs + (size_t)j * HD, d);
+            const float2 v1 = Elem<KT>::load2(Vs + (size_t)(j + 1) * HD, d);
+            const float2 v2 = Elem<KT>::load2(Vs + (size_t)(j + 2) * HD, d);
+            const float2 v3 = Elem<KT>::load2(Vs + (size_t)(j + 3) * HD, d);
+            a0 = fmaf(p[j], v0.x, a0);
+            a1 = fmaf(p[j], v0.y, a1);
+            b0 = fmaf(p[j + 1], v1.x, b0);
+            b1 = fmaf(p[j + 1], v1.y, b1);
+            c0 = fmaf(p[j + 2], v2.x, c0);
+            c1 = fmaf(p[j + 2], v2.y, c1);
+            e0 = fmaf(p[j + 3], v3.x, e0);
+            e1 = fmaf(p[j + 3], v3.y, e1);
         }
         for (; j < n; ++j) {
-            a0 = fmaf(p[j], Elem<KT>::load(Vs + (size_t)j * HD, d), a0);
-            a1 = fmaf(p[j], Elem<KT>::load(Vs + (size_t)j * HD, d + 1), a1);
+            const float2 v0 = Elem<KT>::load2(Vs + (size_t)j * HD, d);
+            a0 = fmaf(p[j], v0.x, a0);
+            a1 = fmaf(p[j], v0.y, a1);
         }
         po[hh * HD + d] = (a0 + b0) + (c0 + e0);
         po[hh * HD + d + 1] = (a1 + b1) + (c1 + e1);

@@ -214,6 +214,8 @@ template <typename T> struct Elem;
 template <> struct Elem<float> {
     static constexpr int kPer16B = 4;
     __device__ static float load(const float *p, int i) { return p[i]; }
+    // elements i, i + 1 (i even) in one 8-byte access
+    __device__ static float2 load2(const float *p, int i) { return *reinterpret_cast<const float2 *>(p + i); }
     __device__ static void store(float *p, int i, float v) { p[i] = v; }
     // 16 bytes -> 4 floats
     __device__ static void unpack(const uint4 &u, float *f) {
@@ -224,6 +226,11 @@ template <> struct Elem<float> {
 template <> struct Elem<__nv_bfloat16> {
     static constexpr int kPer16B = 8;
     __device__ static float load(const __nv_bfloat16 *p, int i) { return __bfloat162float(p[i]); }
+    // elements i, i + 1 (i even) in one 4-byte access
+    __device__ static float2 load2(const __nv_bfloat16 *p, int i) {
+        const uint32_t u = *reinterpret_cast<const uint32_t *>(p + i);
+        return make_float2(bf16lo(u), bf16hi(u));
+    }
     __device__ static void store(__nv_bfloat16 *p, int i, float v) { p[i] = __float2bfloat16_rn(v); }
     __device__ static void unpack(const uint4 &u, float *f) {
         f[0] = bf16lo(u.x); f[1] = bf16hi(u.x); f[2] = bf16lo(u.y); f[3] = bf16hi(u.y);
