@@ -118,6 +118,24 @@ def _dist():
     return ws, rank, local
 
 
+def max_over_ranks(ms: float, ws: int) -> float:
+    """The slowest rank's time of the timed region: every rank takes part (a MAX
+    all-reduce on the process group's device; CPU tensors under gloo); one rank: ms."""
+    if ws <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, ws: int, ms: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest rank's time."""
+    return ws * units_per_rank / (ms / 1e3)
+
+
 # ------------------------------------------------------------------------------ oracle arm
 
 
@@ -148,7 +166,7 @@ def reference_arm(args):
     if rank != 0:
         return
     shape, desc = _workload(args.workload)
-    _, _, _ = run_oracle_sample(shape, max(1, min(args.warmup, 3)), budget_s=5.0)  # warm-up (untimed)
+    run_oracle_sample(shape, max(1, min(args.warmup, 3)), budget_s=5.0)  # warm-up (untimed)
     tps, n, dt, cores = run_oracle_sample(shape, args.steps, budget_s=60.0)
     sample = (f"prefill {shape.prefill} untimed, then {n} greedy decode tokens of the {args.workload} workload "
               f"({dt:.1f} s)")
@@ -248,11 +266,8 @@ def gpu_arm(args):
     clk = clocks.stop()
     ms = ev0.elapsed_time(ev1)
     k1, _ = qd.qd_get_launch_count(h)
-    if ws > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = ws * args.steps / (ms / 1e3)
+    ms = max_over_ranks(ms, ws)
+    value = whole_job_rate(args.steps, ws, ms)
 
     # decode steps alone (prefill excluded): events around every greedy segment of
     # one more pass over whole trajectories
@@ -562,11 +577,8 @@ def frames_arm(args):
     ms = ev0.elapsed_time(ev1)
     kt1, _ = qd.qd_get_launch_count(T)
     kc1, _ = qd.qd_get_launch_count(C)
-    if ws > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = ws * args.steps / (ms / 1e3)
+    ms = max_over_ranks(ms, ws)
+    value = whole_job_rate(args.steps, ws, ms)
 
     # frame loop alone (Talker prefill excluded), two trajectories
     evs = []
@@ -786,11 +798,8 @@ def batch_arm(args):
     qd.qd_batch_sync(bh)
     ms = ev0.elapsed_time(ev1)
     k1, _ = qd.qd_batch_get_launch_count(bh)
-    if ws > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = ws * B * args.steps / (ms / 1e3)
+    ms = max_over_ranks(ms, ws)
+    value = whole_job_rate(B * args.steps, ws, ms)
     step_ms = ms / args.steps
 
     # algorithmic bytes: weights once per step + every stream's K/V over its attended
