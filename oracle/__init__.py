@@ -89,6 +89,10 @@ def _lib_handle():
             L.orc_rmsnorm.restype = None
             L.orc_rope.argtypes = [vp, i32, i32, dp]
             L.orc_rope.restype = None
+            L.orc_conv1d_causal.argtypes = [vp, i32, i32, vp, vp, i32, i32, i32, vp]
+            L.orc_conv1d_causal.restype = i32
+            L.orc_conv_transpose1d_causal.argtypes = [vp, i32, i32, vp, vp, i32, i32, vp]
+            L.orc_conv_transpose1d_causal.restype = i32
             L.orc_f32_to_f16.argtypes = [ctypes.c_float]
             L.orc_f32_to_f16.restype = ctypes.c_uint16
             L.orc_f16_to_f32.argtypes = [ctypes.c_uint16]
@@ -503,4 +507,37 @@ def gemv_q8(codes: np.ndarray, scales: np.ndarray, x: np.ndarray) -> np.ndarray:
     st = _lib_handle().orc_gemv_q8(codes.ctypes.data, scales.ctypes.data, rows, K, x.ctypes.data, y.ctypes.data)
     if st != OK:
         raise OracleError(st, "gemv_q8")
+    return y
+
+
+def conv1d_causal(x: np.ndarray, W: np.ndarray, bias: Optional[np.ndarray] = None, dilation: int = 1) -> np.ndarray:
+    """x [Cin, T], W [Cout, Cin, K] -> y [Cout, T] (causal: zero history)."""
+    x = np.ascontiguousarray(x, np.float32)
+    W = np.ascontiguousarray(W, np.float32)
+    Cin, T = x.shape
+    Cout, _, K = W.shape
+    b = None if bias is None else np.ascontiguousarray(bias, np.float32)
+    y = np.empty((Cout, T), np.float32)
+    st = _lib_handle().orc_conv1d_causal(x.ctypes.data, Cin, T, W.ctypes.data, _ptr(b), Cout, K, int(dilation),
+                                         y.ctypes.data)
+    if st != OK:
+        raise OracleError(st, "conv1d_causal")
+    return y
+
+
+def conv_transpose1d_causal(x: np.ndarray, W: np.ndarray, bias: Optional[np.ndarray] = None,
+                            stride: int = 2) -> np.ndarray:
+    """x [Cin, T], W [Cin, Cout, 2*stride] -> y [Cout, T*stride]."""
+    x = np.ascontiguousarray(x, np.float32)
+    W = np.ascontiguousarray(W, np.float32)
+    Cin, T = x.shape
+    _, Cout, K = W.shape
+    if K != 2 * stride:
+        raise ValueError("kernel must be 2 * stride")
+    b = None if bias is None else np.ascontiguousarray(bias, np.float32)
+    y = np.empty((Cout, T * stride), np.float32)
+    st = _lib_handle().orc_conv_transpose1d_causal(x.ctypes.data, Cin, T, W.ctypes.data, _ptr(b), Cout,
+                                                   int(stride), y.ctypes.data)
+    if st != OK:
+        raise OracleError(st, "conv_transpose1d_causal")
     return y

@@ -146,6 +146,47 @@ int orc_gemv_q8(const int8_t *codes, const uint16_t *scales, int rows, int K, co
     return ORC_OK;
 }
 
+/* Causal dilated 1-D convolution, written out from its definition: each output is the
+ * bias plus the K taps of every input channel at t, t - d, ..., t - (K-1) d. */
+int orc_conv1d_causal(const float *x, int Cin, int T, const float *W, const float *bias, int Cout, int K, int dil,
+                      float *y) {
+    if (Cin <= 0 || T < 0 || Cout <= 0 || K <= 0 || dil <= 0) return ORC_EINVAL;
+    for (int o = 0; o < Cout; ++o)
+        for (int t = 0; t < T; ++t) {
+            double acc = bias ? (double)bias[o] : 0.0;
+            for (int i = 0; i < Cin; ++i)
+                for (int k = 0; k < K; ++k) {
+                    const int ts = t - (K - 1 - k) * dil;
+                    if (ts < 0) continue;
+                    acc += (double)(W[((size_t)o * Cin + i) * K + k] * x[(size_t)i * T + ts]);
+                }
+            y[(size_t)o * T + t] = (float)acc;
+        }
+    return ORC_OK;
+}
+
+/* Causal transposed 1-D convolution, kernel 2 * stride, as the scatter that defines it:
+ * input frame t adds W[i][o][k] x[i][t] to output t*stride + k; outputs at or past
+ * T*stride are dropped. */
+int orc_conv_transpose1d_causal(const float *x, int Cin, int T, const float *W, const float *bias, int Cout,
+                                int stride, float *y) {
+    if (Cin <= 0 || T < 0 || Cout <= 0 || stride <= 0) return ORC_EINVAL;
+    const int K = 2 * stride, n = T * stride;
+    double *acc = (double *)calloc((size_t)Cout * (n > 0 ? n : 1), sizeof(double));
+    if (!acc) return ORC_ENOMEM;
+    for (int i = 0; i < Cin; ++i)
+        for (int t = 0; t < T; ++t)
+            for (int o = 0; o < Cout; ++o)
+                for (int k = 0; k < K; ++k) {
+                    const int u = t * stride + k;
+                    if (u < n) acc[(size_t)o * n + u] += (double)(W[((size_t)i * Cout + o) * K + k] * x[(size_t)i * T + t]);
+                }
+    for (int o = 0; o < Cout; ++o)
+        for (int u = 0; u < n; ++u) y[(size_t)o * n + u] = (float)(acc[(size_t)o * n + u] + (bias ? (double)bias[o] : 0.0));
+    free(acc);
+    return ORC_OK;
+}
+
 /* Round-to-nearest-even float -> bfloat16 (the KV-cache storage rounding). */
 uint16_t orc_round_bf16(float f) {
     uint32_t u;

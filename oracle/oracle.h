@@ -141,6 +141,21 @@ int orc_quantize_q8(const float *w, int rows, int K, int8_t *codes, uint16_t *sc
 /* y[r] = sum_k (codes[r][k] * half(scales[r][k / 32])) * x[k], fp32 products summed in
  * fp64 in index order, rounded to fp32. */
 int orc_gemv_q8(const int8_t *codes, const uint16_t *scales, int rows, int K, const float *x, float *y);
+
+/* Codec decoder convolution stages ("qwen3-tts-hip OPTIMIZATION_LOG", codec-profile and
+ * transposed-convolution entries; the codec's SEANet upsampler in "Qwen3-TTS ncnn
+ * port").  Channel-major signals x [Cin][T], y [Cout][...]; fp32 products summed in
+ * fp64, rounded to fp32; bias may be NULL.
+ *
+ * Causal dilated convolution: y[o][t] = b[o] + sum_i sum_k W[o][i][k] x[i][t - (K-1-k) d],
+ * x = 0 before t = 0; W [Cout][Cin][K]; y [Cout][T]. */
+int orc_conv1d_causal(const float *x, int Cin, int T, const float *W, const float *bias, int Cout, int K, int dil,
+                      float *y);
+/* Causal transposed convolution with kernel 2 * stride: every input frame t spreads
+ * into outputs t*stride + k, k < 2*stride, through W [Cin][Cout][2*stride]; the first
+ * T*stride outputs are kept (y [Cout][T*stride]). */
+int orc_conv_transpose1d_causal(const float *x, int Cin, int T, const float *W, const float *bias, int Cout,
+                                int stride, float *y);
 int orc_num_threads(void);
 void orc_set_threads(int n);
 

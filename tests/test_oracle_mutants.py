@@ -34,8 +34,10 @@ MUTANTS = {
     "bf16_truncation": ("u += 0x7fffu + lsb;", "u += 0u * lsb;"),
     "mrope_streams_h_w_swapped": ("--left[s];\n        s = (s + 1) % 3;", "--left[s];\n        s = (s + 2) % 3;"),
     "mrope_decode_restarts_at_cache_position": ("m->rope_delta = top + 1 - n;", "m->rope_delta = 0;"),
+    "conv_taps_reversed": ("const int ts = t - (K - 1 - k) * dil;", "const int ts = t - k * dil;"),
+    "transconv_one_frame_late": ("const int u = t * stride + k;", "const int u = (t + 1) * stride + k;"),
 }
-PIN_FILES = ("test_oracle_pins.py", "test_oracle_mrope.py")
+PIN_FILES = ("test_oracle_pins.py", "test_oracle_mrope.py", "test_oracle_codec_conv.py")
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
