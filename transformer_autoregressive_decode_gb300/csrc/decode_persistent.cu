@@ -5,10 +5,11 @@
 //  - "qwen3-tts-hip OPTIMIZATION_LOG", decode-step profile and graph-replay entries:
 //    the step is a chain of small dependent operations per layer whose launch and
 //    synchronisation costs dominate at batch 1; replaying it as a graph helped only a
-//    little.  Here the chain lives inside one kernel: phases are separated by grid
-//    barriers, and each CTA's producer warp streams that CTA's slice of every phase's
-//    weights (and its attention K/V tile) through one shared-memory ring without
-//    waiting on the barriers, so HBM keeps streaming while the phases synchronise.
+//    little.  Here the chain lives inside one kernel: each phase waits for the data it
+//    gathers from the others (below), and each CTA's producer warp streams that CTA's
+//    slice of every phase's weights (and its attention K/V tile) through one
+//    shared-memory ring without waiting on them, so HBM keeps streaming while the
+//    phases synchronise.
 //  - "Qwen3-TTS ncnn port", section "Talker: non-standard structure and two-level
 //    generation", and "Audio8-ASR: dynamic KV-cache buckets", section "Implemented
 //    dynamic window mechanism": the arithmetic of each phase (shared with the
