@@ -233,6 +233,24 @@ qd_status qd_quantize_q8(const void *w_dev, int dtype, int rows, int K, int8_t *
 qd_status qd_gemv_q8(const int8_t *codes_dev, const uint16_t *scales_dev, const float *x_dev, float *y_dev, int rows,
                      int K, void *cuda_stream, int reps, float *avg_ms);
 
+/* qd_conv1d_causal -- the codec decoder's causal dilated convolution ("qwen3-tts-hip
+ * OPTIMIZATION_LOG", codec entries): y[o][t] = bias[o] + sum_i sum_k W[o][i][k] *
+ * x[i][t - (K-1-k) * dilation], zero history.  x DEVICE fp32 [Cin][T], W DEVICE fp32
+ * [Cout][Cin][K], bias DEVICE fp32 [Cout] or NULL, y DEVICE fp32 [Cout][T].  K <= 16,
+ * (K-1) * dilation <= 512.  Asynchronous on cuda_stream.  Errors: QD_EINVAL,
+ * QD_EUNSUPPORTED (history span), QD_ECUDA. */
+qd_status qd_conv1d_causal(const float *x_dev, int Cin, int T, const float *w_dev, const float *bias_dev, int Cout,
+                           int K, int dilation, float *y_dev, void *cuda_stream);
+
+/* qd_conv_transpose1d_causal -- the codec decoder's transposed convolution with kernel
+ * 2 * stride, in the page's per-phase form: y[o][t * stride + p] = bias[o] + sum_i
+ * W[i][o][p] x[i][t] + W[i][o][p + stride] x[i][t - 1] (x[-1] = 0), t < T, p < stride.
+ * x DEVICE fp32 [Cin][T], W DEVICE fp32 [Cin][Cout][2 * stride], bias DEVICE fp32 [Cout]
+ * or NULL, y DEVICE fp32 [Cout][T * stride].  stride <= 64.  Asynchronous on
+ * cuda_stream.  Errors: QD_EINVAL, QD_ECUDA. */
+qd_status qd_conv_transpose1d_causal(const float *x_dev, int Cin, int T, const float *w_dev, const float *bias_dev,
+                                     int Cout, int stride, float *y_dev, void *cuda_stream);
+
 /* qd_gemm_bf16 -- the batched paths' tensor-core contraction on its own (a check
  * and measurement tap): out[t][r] = sum_k W[r][k] * x[t][k] for W (DEVICE bf16
  * [R, K] row-major, 16-byte aligned) and x (DEVICE fp32 [T, K] row-major), with x
