@@ -355,6 +355,44 @@ def gpu_arm(args):
                       "(after 2), each between CUDA events after a 256 MB write that flushes L2"}
         del codes, scales
 
+    # the codec decoder's convolution stages (fp32, CUDA cores: "alu" bound against the
+    # fp32 FMA rate of 152 SMs x 128 lanes x 2 flops at the sampled SM clock), each launch
+    # after a 256 MB write that flushes L2
+    codec = None
+    if args.workload == "asr":
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+        def timed(fn, reps=6):
+            fn()
+            ts = []
+            for _ in range(reps):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b))
+            return float(np.median(ts[1:]))
+        cx = torch.from_numpy(W.normal("bench/codec_x", (512, 4096), 0, 0.0, 1.0)).cuda()
+        cw = torch.from_numpy(W.normal("bench/codec_w", (512, 512, 7), 0, 0.0, 0.02)).cuda()
+        tw = torch.from_numpy(W.normal("bench/codec_tw", (512, 256, 8), 0, 0.0, 0.02)).cuda()
+        tx = cx[:, :1024].contiguous()
+        conv_ms = timed(lambda: qd.qd_conv1d_causal(cx, cw, None, dilation=1))
+        tconv_ms = timed(lambda: qd.qd_conv_transpose1d_causal(tx, tw, None, stride=4))
+        sm_mhz = (clk or {}).get("sm_mhz") or 2070.0
+        alu_peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+        conv_tf = 2 * 512 * 512 * 7 * 4096 / (conv_ms / 1e3) / 1e12
+        tconv_tf = 2 * 512 * 256 * 2 * 1024 * 4 / (tconv_ms / 1e3) / 1e12
+        codec = {"conv1d_causal": {"shape": "512 -> 512 channels, K 7, 4096 frames", "ms": conv_ms,
+                                   "tflops": conv_tf, "frac": conv_tf / alu_peak},
+                 "conv_transpose1d_causal": {"shape": "512 -> 256 channels, stride 4, 1024 -> 4096 frames",
+                                             "ms": tconv_ms, "tflops": tconv_tf, "frac": tconv_tf / alu_peak},
+                 "bound": "alu", "peak_tflops": alu_peak,
+                 "note": "fp32 CUDA-core kernels (parity first); peak = 152 SMs x 128 fp32 lanes x 2 flops x SM "
+                         "clock; median of 5 after a warm launch, L2 flushed before each"}
+        del flush, cx, cw, tw, tx
+
     # end to end through the public API with host buffers: the prompt embeddings
     # come from pinned host memory each trajectory, the token goes in and the id
     # comes out through host memory every step (synchronising call)
@@ -450,6 +488,7 @@ def gpu_arm(args):
                              "the head, last-CTA merge and counter-based draw"},
         **({"mrope": mrope} if mrope else {}),
         **({"q8_head_gemv": q8} if q8 else {}),
+        **({"codec_conv": codec} if codec else {}),
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(k1 - k0), "kernels_per_decode_step": per_step,
         "clocks": clk,
     }
