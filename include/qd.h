@@ -243,8 +243,10 @@ qd_status qd_conv1d_causal(const float *x_dev, int Cin, int T, const float *w_de
                            int K, int dilation, float *y_dev, void *cuda_stream);
 
 /* qd_conv_transpose1d_causal -- the codec decoder's transposed convolution with kernel
- * 2 * stride, in the page's per-phase form: y[o][t * stride + p] = bias[o] + sum_i
- * W[i][o][p] x[i][t] + W[i][o][p + stride] x[i][t - 1] (x[-1] = 0), t < T, p < stride.
+ * length 2 * stride ("qwen3-tts-hip OPTIMIZATION_LOG", transposed-convolution
+ * entries), evaluated per output phase: sample t * stride + p (t < T, p < stride) of
+ * output channel o is bias[o] plus, over input channels i, tap p of W[i][o] times
+ * x[i][t] and tap p + stride of W[i][o] times x[i][t - 1] (x[i][-1] = 0).
  * x DEVICE fp32 [Cin][T], W DEVICE fp32 [Cin][Cout][2 * stride], bias DEVICE fp32 [Cout]
  * or NULL, y DEVICE fp32 [Cout][T * stride].  stride <= 64.  Asynchronous on
  * cuda_stream.  Errors: QD_EINVAL, QD_ECUDA. */
@@ -376,9 +378,13 @@ qd_status qd_frame_set_graphs(qd_frame_handle f, int enable);
  * set in emitted_dev (uint32 bitmask, may be NULL), the EOS mask (eos_mask_id, -1:
  * none) and the argmax (lowest index on ties), written to *out_id_dev (DEVICE
  * int32).  logits_dev (DEVICE fp32 [vocab], may be NULL) receives the raw logits.
- * All pointers are DEVICE pointers; work is queued on cuda_stream and the call
- * returns without synchronising.  It gives the same logits and id as the output
- * head of qd_decode_step for the same y.
+ * All pointers are DEVICE pointers (a host pointer returns QD_EINVAL before any
+ * work); work is queued on cuda_stream and the call returns without synchronising.
+ * It gives the same logits and id as the output head of qd_decode_step for the same
+ * y.  *out_id_dev == -1 after the work completes means the kernel gave up: a stage
+ * of the weight stream did not arrive within its one-second bound, and no id was
+ * produced.  Errors: QD_EINVAL (null or non-device pointer, vocab or hidden < 1,
+ * eos_mask_id outside [-1, vocab), rep_penalty <= 0, unknown dtype).
  *
  * Its scratch (one argmax candidate per CTA and a completion counter, about 8 KB)
  * is a fixed array in the library's device memory, held by every device that loads

@@ -25,7 +25,10 @@ def _check(y, ref, mag, terms):
 
 
 @pytest.mark.parametrize("Cin,Cout,K,d,T", [(3, 4, 3, 1, 20), (16, 40, 7, 3, 300), (9, 33, 3, 9, 129),
-                                           (256, 256, 7, 1, 1000), (1, 1, 1, 1, 5)])
+                                           (256, 256, 7, 1, 1000), (1, 1, 1, 1, 5),
+                                           # the largest staged layouts: 16 taps, and a
+                                           # history span of 510 and of exactly 512 frames
+                                           (12, 35, 16, 34, 700), (10, 33, 3, 256, 900)])
 def test_causal_conv_matches_oracle(Cin, Cout, K, d, T):
     import torch
     import oracle as O

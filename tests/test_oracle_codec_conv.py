@@ -1,13 +1,16 @@
 """Pins of the oracle's codec-decoder convolution stages.
 
-"qwen3-tts-hip OPTIMIZATION_LOG" profiles the codec decoder as causal dilated
-convolutions and transposed convolutions, and reformulates the transposed convolution
-by output phase: with kernel 2 * stride, output t * stride + p is
-x[t] @ W[p] + x[t - 1] @ W[p + stride] + bias.  The oracle computes both stages from
-their definitions (a tap sum and a scatter); the pins check them against other
-formulations: numpy's full convolution with the reversed dilated kernel, the page's
-per-phase GEMMs, torch's transposed convolution trimmed to the causal length, impulse
-responses, causality and linearity.
+"qwen3-tts-hip OPTIMIZATION_LOG" (decoder transposed-convolution entries) profiles the
+codec decoder as causal dilated convolutions and transposed convolutions, and rewrites
+the transposed convolution per output phase.  In this repository's notation, with
+kernel length 2 * stride and weights W[i][o][k], the output sample s = t * stride + p
+(0 <= p < stride) only receives two taps: k = p from input frame t and k = p + stride
+from frame t - 1, so y[o][s] = b[o] + sum_i (W[i][o][p] x[i][t] + W[i][o][p + stride]
+x[i][t - 1]), one matrix product per tap and phase.  The oracle computes both stages
+from their definitions (a tap sum and a scatter); the pins check them against other
+formulations: numpy's full convolution with the reversed dilated kernel, the two
+products per phase, torch's transposed convolution trimmed to the causal length,
+impulse responses, causality and linearity.
 """
 import numpy as np
 import pytest

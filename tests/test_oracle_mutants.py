@@ -36,19 +36,29 @@ MUTANTS = {
     "mrope_decode_restarts_at_cache_position": ("m->rope_delta = top + 1 - n;", "m->rope_delta = 0;"),
     "conv_taps_reversed": ("const int ts = t - (K - 1 - k) * dil;", "const int ts = t - k * dil;"),
     "transconv_one_frame_late": ("const int u = t * stride + k;", "const int u = (t + 1) * stride + k;"),
+    # the same swap of gate and up in the cached step and in the full recompute, so
+    # the two still agree with each other
+    "gate_up_swapped": [("matvec(c, W_(m, l, S_WG), F, h, xn, g);\n        matvec(c, W_(m, l, S_WU), F, h, xn, u);",
+                         "matvec(c, W_(m, l, S_WG), F, h, xn, u);\n        matvec(c, W_(m, l, S_WU), F, h, xn, g);"),
+                        ("matvec(c, lw[S_WG], F, h, xn, g);\n            matvec(c, lw[S_WU], F, h, xn, u);",
+                         "matvec(c, lw[S_WG], F, h, xn, u);\n            matvec(c, lw[S_WU], F, h, xn, g);")],
 }
 PIN_FILES = ("test_oracle_pins.py", "test_oracle_mrope.py", "test_oracle_codec_conv.py")
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
 def test_pins_catch_planted_mistake(name, tmp_path):
-    old, new = MUTANTS[name]
+    edits = MUTANTS[name]
+    if isinstance(edits, tuple):
+        edits = [edits]
     src = open(SRC).read()
-    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    for old, new in edits:
+        assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+        src = src.replace(old, new)
     d = tmp_path / "orc"
     d.mkdir()
     shutil.copy(os.path.join(ROOT, "oracle", "oracle.h"), d / "oracle.h")
-    (d / "oracle.c").write_text(src.replace(old, new))
+    (d / "oracle.c").write_text(src)
     lib = d / "liboracle_mutant.so"
     subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
                            "-o", str(lib), str(d / "oracle.c"), "-lm"])

@@ -326,6 +326,35 @@ def test_zero_query_attends_uniformly_over_the_prefix():
     assert np.allclose(kvv.transpose(1, 0, 2).reshape(6, -1), np.array(V), rtol=1e-5, atol=1e-6)
 
 
+def test_mlp_branch_is_down_of_silu_gate_times_up():
+    # wq = 0 makes the attention branch x + Wo . mean(v) (pinned above); the layer's
+    # output must then add Wd (silu(Wg x^) * (Wu x^)) with x^ = RMSNorm(x1; mlp gamma):
+    # the gate, not the up projection, goes through silu, and Wd multiplies the
+    # product.  Evaluated here in float64 from the definition.
+    s = W.scaled(W.TINY, qk_norm=False, name="tiny_noqk")
+    w = W.model_weights(s)
+    w["layers.0.wq"] = np.zeros_like(w["layers.0.wq"])
+    e = W.prefill_embeds(s, 6)
+    o = O.Oracle(s, w)
+    o.prefill(embeds=e[:5], want_logits=False)
+    _, _, _, taps = o.step(embed=e[5], taps=True)
+    f64 = lambda k: w[k].astype(np.float64)
+    V = [f64("layers.0.wv") @ O.rmsnorm(e[t], w["layers.0.attn_norm"], s.rms_eps).astype(np.float64)
+         for t in range(6)]
+    vbar = np.mean(V, axis=0)
+    hd, grp = s.head_dim, s.n_q_heads // s.n_kv_heads
+    att = np.concatenate([vbar[(i // grp) * hd:(i // grp + 1) * hd] for i in range(s.n_q_heads)])
+    x1 = e[5].astype(np.float64) + f64("layers.0.wo") @ att
+    xn = x1 / np.sqrt(np.mean(x1 * x1) + s.rms_eps) * f64("layers.0.mlp_norm")
+    g, u = f64("layers.0.wg") @ xn, f64("layers.0.wu") @ xn
+    ref = x1 + f64("layers.0.wd") @ (g / (1.0 + np.exp(-g)) * u)
+    assert np.allclose(taps[1], ref, rtol=1e-4, atol=1e-5)
+    # the branch is not negligible here: dropping it or swapping gate and up is visible
+    swapped = x1 + f64("layers.0.wd") @ (u / (1.0 + np.exp(-u)) * g)
+    assert not np.allclose(taps[1], swapped, rtol=1e-4, atol=1e-5)
+    assert not np.allclose(taps[1], x1, rtol=1e-4, atol=1e-5)
+
+
 def test_emitted_set_follows_fed_tokens_not_prompt():
     s = W.TINY
     w = W.model_weights(s)

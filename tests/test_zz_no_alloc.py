@@ -6,14 +6,16 @@ thread where an allocation's locking and synchronisation are not allowed): it ta
 only the caller's buffers and keeps its scratch in a fixed device array.  For the
 normalised hidden state of a decode step (qd_get_hidden) and the step's emitted set,
 it must produce the step's logits and id, on two calls in a row (the second call
-reuses the array the first one left behind).  Collected last so that a failure here
-comes after every other test has run.
+reuses the array the first one left behind), and the oracle's: W_head . y in the
+oracle's own matvec, then its penalty, EOS mask and argmax over the same emitted set
+(equal ids wherever the oracle's top-2 margin exceeds the acceptance margin).
+Collected last so that a failure here comes after every other test has run.
 """
 import numpy as np
 import pytest
 
 import workloads as W
-from _pair import REL_TOL, rel_l2
+from _pair import MARGIN, REL_TOL, rel_l2
 
 pytestmark = pytest.mark.gpu
 
@@ -22,6 +24,7 @@ pytestmark = pytest.mark.gpu
 def test_noalloc_head_matches_decode_step(shape_name, cuda_ok):
     import torch
     import __graft_entry__
+    import oracle as O
     __graft_entry__.build_library()
     import transformer_autoregressive_decode_gb300 as qd
     from transformer_autoregressive_decode_gb300.torch_io import config_from_shape, upload
@@ -46,5 +49,23 @@ def test_noalloc_head_matches_decode_step(shape_name, cuda_ok):
                                   s.eos_mask_id, out_id, logits)
         torch.cuda.synchronize()
         assert int(out_id.item()) == tok
-        assert rel_l2(logits.cpu().numpy(), logits_tap.cpu().numpy()) <= REL_TOL
+        got = logits.cpu().numpy()
+        assert rel_l2(got, logits_tap.cpu().numpy()) <= REL_TOL
+        # against the oracle, from the same normalised hidden state and emitted set
+        em = emitted.cpu().numpy().view(np.uint32)
+        ids_em = [i for i in range(s.vocab) if (em[i >> 5] >> (i & 31)) & 1]
+        ref = O.linear(w["lm_head.0"], y.cpu().numpy()[None])[0]
+        ref_id, _, margin = O.penalty_argmax(ref, ids_em, s.rep_penalty, s.eos_mask_id)
+        assert rel_l2(got, ref) <= REL_TOL
+        if margin > MARGIN:
+            assert int(out_id.item()) == ref_id
+    # host buffers are refused before any work
+    with pytest.raises(qd.QDError) as ei:
+        qd.qd_head_argmax_noalloc(y.cpu(), dev_w["lm_head.0"], s.vocab, s.hidden, s.bf16, emitted, s.rep_penalty,
+                                  s.eos_mask_id, out_id, logits)
+    assert ei.value.status == qd.QD_EINVAL
+    with pytest.raises(qd.QDError) as ei:
+        qd.qd_head_argmax_noalloc(y, dev_w["lm_head.0"], s.vocab, s.hidden, s.bf16, emitted, s.rep_penalty,
+                                  -2, out_id, logits)
+    assert ei.value.status == qd.QD_EINVAL
     qd.qd_destroy(h)

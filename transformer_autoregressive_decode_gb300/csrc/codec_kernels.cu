@@ -3,8 +3,9 @@
 // Sources (page title, section):
 //  - "qwen3-tts-hip OPTIMIZATION_LOG", codec-profile and transposed-convolution
 //    entries: the codec decoder's time goes to causal dilated convolutions and to
-//    transposed convolutions; with kernel 2 * stride the transposed convolution is, per
-//    output phase p, output[t * stride + p] = x[t] W[p] + x[t - 1] W[p + stride] + bias.
+//    transposed convolutions.  With kernel length 2 * stride, output sample
+//    s = t * stride + p (p < stride) of a transposed convolution takes tap p of input
+//    frame t and tap p + stride of frame t - 1, nothing else (the per-phase form).
 //  - "Qwen3-TTS ncnn port", pipeline overview: the codec's SEANet upsampler.
 //
 // qd_conv1d_causal: y[o][t] = b[o] + sum_i sum_k W[o][i][k] x[i][t - (K-1-k) d], zero

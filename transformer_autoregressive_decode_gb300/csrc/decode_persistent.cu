@@ -75,7 +75,14 @@ __device__ __forceinline__ uint64_t ld_tagged(const uint64_t *p) {
     return w;
 }
 // The tag of phase k of layer l in the launch with sequence number seq (1 + 5l + k < 256).
+// The tag keeps the low 24 bits of seq: consecutive launches always differ, and a word
+// could only pass as fresh if no launch had rewritten it for 2^24 launches.  The phase
+// field is never 0, so the zeroed words of a new handle never match.
 __device__ __forceinline__ uint32_t phase_tag(uint32_t seq, int l, int k) { return (seq << 8) | (uint32_t)(1 + 5 * l + k); }
+
+// Advance the launch sequence number from `seq` (the value this launch read) to seq + 1,
+// modulo 2^32, exactly once however many threads of the launch call it.
+__device__ __forceinline__ void advance_seq(unsigned *p, uint32_t seq) { (void)atomicCAS(p, seq, seq + 1u); }
 
 struct TagSeg {                    // dst[i] = value of src[i], i < n
     const uint64_t *src;
@@ -568,7 +575,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
                 else atomicOr(&st->status, DEV_ERR_IDS_FULL);
                 st->n_gen = n + 1;
                 st->pos = p + 1;
-                atomicMax(a.seq, seq + 1);
+                advance_seq(a.seq, seq);
             };
             if (misc_i[5] && sk > 0) {
                 // every CTA's sorted candidates -> merged -> the draw
@@ -615,7 +622,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
                     a.tap_hidden[(size_t)a.n_layers * hidden + i] = __ldcg(a.x + i);
             if (tid == 0) {
                 a.st->pos = p + 1;
-                atomicMax(a.seq, seq + 1);
+                advance_seq(a.seq, seq);
             }
         }
     }
@@ -625,7 +632,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
         named_sync(1, NC);
         if (tid == 0) {
             atomicOr(&a.st->status, DEV_ERR_WAIT_TIMEOUT);
-            atomicMax(a.seq, seq + 1);   // no tag of this launch is ever taken as fresh
+            advance_seq(a.seq, seq);   // no tag of this launch is ever taken as fresh
             ctl[0] = 1;
             const unsigned long long t0 = global_timer_ns();
             while (!ctl[2] && global_timer_ns() - t0 < 2 * kWaitLimitNs + 100000000ull) {

@@ -12,6 +12,7 @@
 
 #include "../../include/qd.h"
 #include "decode_common.cuh"
+#include "qd_model.h"
 
 namespace qd {
 
@@ -240,8 +241,12 @@ extern "C" qd_status qd_head_argmax_noalloc(const float *y_dev, const void *w_de
                                             const uint32_t *emitted_dev, double rep_penalty, int eos_mask_id,
                                             int32_t *out_id_dev, float *logits_dev, void *cuda_stream) {
     if (!y_dev || !w_dev || !out_id_dev) return QD_EINVAL;
+    // every buffer must be device memory: a host pointer is refused here rather than
+    // faulting inside the kernel (the pointer queries allocate nothing)
+    if (!is_device_ptr(y_dev) || !is_device_ptr(w_dev) || !is_device_ptr(out_id_dev)) return QD_EINVAL;
+    if ((emitted_dev && !is_device_ptr(emitted_dev)) || (logits_dev && !is_device_ptr(logits_dev))) return QD_EINVAL;
     if (dtype != QD_F32 && dtype != QD_BF16) return QD_EINVAL;
-    if (vocab < 1 || hidden < 1 || eos_mask_id >= vocab || !(rep_penalty > 0.0)) return QD_EINVAL;
+    if (vocab < 1 || hidden < 1 || eos_mask_id < -1 || eos_mask_id >= vocab || !(rep_penalty > 0.0)) return QD_EINVAL;
     const bool bf16 = dtype == QD_BF16;
     int nseg = 0, rs = 0;
     if (hidden > kNoAllocMaxHidden || hidden % 256 || !gemv_split(hidden, bf16, &nseg, &rs)) return QD_EUNSUPPORTED;
