@@ -127,6 +127,11 @@ def _ids_logits(shape, w, e, n, buckets=None, graphs=True, grow_at=None):
     return ids, np.array(hid), kv.cpu().numpy(), pos, smax
 
 
+def _bf16_to_f32(b):
+    u = np.ascontiguousarray(b).view(np.uint16).astype(np.uint32) << 16
+    return u.view(np.float32)
+
+
 def _valid_kv(kv_bytes, shape, smax, pos):
     es = 2 if shape.bf16 else 4
     a = kv_bytes.reshape(shape.n_layers, 2, shape.n_kv_heads, smax, shape.head_dim * es)
@@ -294,8 +299,11 @@ def test_time_kernel_leaves_state_unchanged():
 
 @pytest.mark.parametrize("shape_name", ["tiny", "asr2", "talker2"])
 def test_persistent_step_equals_per_phase_kernels(shape_name, monkeypatch):
-    """The persistent decode step and the per-phase kernels share every arithmetic
-    routine and reduction order, so their ids, hidden states and caches are identical."""
+    """The persistent decode step and the per-phase kernels compute the same step with
+    fp32 sums in different orders (the persistent step splits each GEMV's K over its
+    warps and applies the RMSNorm scale after the dot products): equal ids, hidden
+    states within fp32 summation noise, caches equal up to the odd last-bit bf16
+    rounding of those sums."""
     s = {"tiny": W.TINY, "asr2": W.scaled(W.ASR, n_layers=2, name="asr2"),
          "talker2": W.scaled(W.TALKER, n_layers=2, name="talker2")}[shape_name]
     w = W.model_weights(s)
@@ -305,8 +313,15 @@ def test_persistent_step_equals_per_phase_kernels(shape_name, monkeypatch):
     monkeypatch.setenv("QD_PER_PHASE", "1")
     b = _ids_logits(s, w, e, n)
     assert a[0] == b[0]
-    assert np.array_equal(a[1], b[1])
-    assert np.array_equal(_valid_kv(a[2], s, a[4], a[3]), _valid_kv(b[2], s, b[4], b[3]))
+    for ya, yb in zip(a[1], b[1]):
+        assert rel_l2(ya, yb) <= 1e-4
+    ka = _valid_kv(a[2], s, a[4], a[3])
+    kb = _valid_kv(b[2], s, b[4], b[3])
+    if s.bf16:
+        ka, kb = _bf16_to_f32(ka), _bf16_to_f32(kb)
+    else:
+        ka, kb = ka.view(np.float32), kb.view(np.float32)
+    assert rel_l2(ka, kb) <= 1e-3
 
 
 @pytest.mark.parametrize("shape_name,prompt", [("asr2", "embeds"), ("talker2", "embeds"), ("asr2", "tokens")])

@@ -5,68 +5,83 @@
 //  - "qwen3-tts-hip OPTIMIZATION_LOG", decode-step profile and graph-replay entries:
 //    the step is a chain of small dependent operations per layer whose launch and
 //    synchronisation costs dominate at batch 1; replaying it as a graph helped only a
-//    little.  Here the chain lives inside one kernel: each phase waits for the data it
-//    gathers from the others (below), and each CTA's producer warp streams that CTA's
-//    slice of every phase's weights (and its attention K/V tile) through one
-//    shared-memory ring without waiting on them, so HBM keeps streaming while the
-//    phases synchronise.
+//    little.  Here the chain lives inside one kernel: each phase waits only for the
+//    words it reads, and each CTA's producer warp streams that CTA's slice of every
+//    phase's weights (and its attention K/V tile) through one shared-memory ring
+//    without waiting on them, so HBM keeps streaming while the phases synchronise.
 //  - "Qwen3-TTS ncnn port", section "Talker: non-standard structure and two-level
 //    generation", and "Audio8-ASR: dynamic KV-cache buckets", section "Implemented
-//    dynamic window mechanism": the arithmetic of each phase (shared with the
-//    per-phase kernels through decode_common.cuh).
+//    dynamic window mechanism": the arithmetic of each phase.
 //
 // Phases of layer l:
-//   A  x^ = RMSNorm(x), qkv = [Wq;Wk;Wv] x^   (layer 0 also resolves the step input)
+//   A  qkv = [Wq;Wk;Wv] RMSNorm(x)   (layer 0 also resolves the step input)
 //   B  attention: CTA i < kv_heads * splits takes (group, split) i; QK-norm, RoPE, KV
-//      append, scores/softmax/P.V of the split -> partials
-//   C  output projection: merge the splits, x += Wo o
-//   D  x^ = RMSNorm(x), act = silu(Wg x^) * (Wu x^)
+//      append, scores/softmax/P.V of the split -> the split's partial; then the
+//      split CTAs of a group merge the partials, each a slice of the group's columns
+//   C  x += Wo o
+//   D  act = silu(Wg x^) * (Wu x^), x^ = RMSNorm(x)
 //   E  x += Wd act
 // then the head: y = RMSNorm(x), logits, penalty, EOS mask, argmax (last CTA reduces).
 //
-// Between phases.  The vectors every CTA gathers (qkv after A, x after C and E, act
-// after D) are also written as 64-bit words {tag, value}, the tag naming the launch
-// (a sequence number advanced once per launch) and the phase; a reader polls the words
-// it needs until their tags match, so the data and its readiness travel in one access
-// and these four boundaries need no barrier round trip.  A buffer is only rewritten
-// after every CTA has read its previous contents: each rewrite depends, through the
-// chain of gathers, on every CTA having finished the phase that read them.  Only the
-// attention partials (B -> C) cross a grid barrier, which also orders the plain
-// writes of the step input and the emitted set.
+// Between phases.  Every vector a phase hands to other CTAs (qkv, the attention
+// partials and merged output, x after C and after E, act) is written once per launch
+// into its own buffer of 64-bit words {launch sequence number, value}, one buffer per
+// layer and phase, with one relaxed 64-bit store per value.  A reader polls the words
+// it needs until their sequence number is the launch's: the data and its readiness
+// travel in one access, no barrier round trip is needed, and a word is never rewritten
+// within a launch.
+//
+// The GEMV phases split K over the consumer warps: warp w owns a contiguous chunk of
+// the input vector's columns and polls exactly those words, straight into registers,
+// so it can start on its rows as soon as its own chunk has arrived.  Each lane
+// multiplies its columns of every row of a ring stage; one transposing butterfly per
+// stage reduces the stage's rows across the lanes (lane i ends with row i's chunk
+// sum), and after the last stage one CTA barrier lets a thread per row add the warps'
+// chunk sums in warp order.  RMSNorm is a scalar per vector, so W (g * x * r) is
+// computed as r * W (g * x): the chunk sums of squares travel beside the row partials
+// and r is applied by the row's thread.
 #include "decode_common.cuh"
 
 namespace qd {
+
+constexpr int kNW = kConsumerWarps;          // consumer warps
+constexpr int kNC = kNW * 32;                // consumer threads
+constexpr int kGMax = kStepGroupMax;         // q heads per kv head handled by the step kernel
+
+__host__ __device__ constexpr int pow2_ceil(int v) { return v <= 1 ? 1 : 2 * pow2_ceil((v + 1) / 2); }
 
 // Grid barrier over all CTAs (consumer threads of every CTA arrive).  Thread 0
 // publishes the CTA's writes with a release reduction and polls with acquire loads,
 // for at most kWaitLimitNs.  Returns false on timeout (uniform across the CTA).
 __device__ __forceinline__ bool grid_sync(unsigned *counter, unsigned &epoch, int *flag) {
-    named_sync(1, kConsumerWarps * 32);
+    named_sync(1, kNC);
     ++epoch;
     if (threadIdx.x == 0) {
         const unsigned target = epoch * gridDim.x;
         __threadfence();
         asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(counter) : "memory");
-        const unsigned long long t0 = global_timer_ns();
+        const unsigned long long t0 = cycles_now();
         int ok = 1;
         while (true) {
             unsigned v;
             asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
             if (v >= target) break;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (cycles_now() - t0 > wait_cycles(kWaitLimitNs)) {
                 ok = 0;
                 break;
             }
         }
         *flag = ok;
     }
-    named_sync(1, kConsumerWarps * 32);
+    named_sync(1, kNC);
     return *flag != 0;
 }
 
-// Tagged words: the value's bits low, the tag high, in one 64-bit access.
-__device__ __forceinline__ void st_tagged(uint64_t *p, float v, uint32_t tag) {
-    const uint64_t w = ((uint64_t)tag << 32) | __float_as_uint(v);
+// ---------------------------------------------------------------- tagged words
+// {seq, value}: the value's bits low, the launch's sequence number high.  A new
+// handle's words are all zero and no launch has sequence number 0.
+__device__ __forceinline__ void st_tag(uint64_t *p, float v, uint32_t seq) {
+    const uint64_t w = ((uint64_t)seq << 32) | __float_as_uint(v);
     asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
 }
 __device__ __forceinline__ uint64_t ld_tagged(const uint64_t *p) {
@@ -74,125 +89,129 @@ __device__ __forceinline__ uint64_t ld_tagged(const uint64_t *p) {
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
     return w;
 }
-// The tag of phase k of layer l in the launch with sequence number seq (1 + 5l + k < 256).
-// The tag keeps the low 24 bits of seq: consecutive launches always differ, and a word
-// could only pass as fresh if no launch had rewritten it for 2^24 launches.  The phase
-// field is never 0, so the zeroed words of a new handle never match.
-__device__ __forceinline__ uint32_t phase_tag(uint32_t seq, int l, int k) { return (seq << 8) | (uint32_t)(1 + 5 * l + k); }
+__device__ __forceinline__ void ld_tagged2(const uint64_t *p, uint64_t &a, uint64_t &b) {
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
 
-// Advance the launch sequence number from `seq` (the value this launch read) to seq + 1,
-// modulo 2^32, exactly once however many threads of the launch call it.
-__device__ __forceinline__ void advance_seq(unsigned *p, uint32_t seq) { (void)atomicCAS(p, seq, seq + 1u); }
+// Advance the launch sequence number from `seq` (the value this launch read) to the
+// next non-zero value, exactly once however many threads of the launch call it.
+__device__ __forceinline__ void advance_seq(unsigned *p, uint32_t seq) {
+    (void)atomicCAS(p, seq, seq + 1u == 0u ? 1u : seq + 1u);
+}
+
+// One thread: the N consecutive words at p (16-byte aligned when N is even) once all
+// carry `seq`; every still-stale word is re-polled together (one round trip per poll),
+// for at most kWaitLimitNs.  False on timeout.
+template <int N>
+__device__ __forceinline__ bool poll_tagged(const uint64_t *p, uint32_t seq, float *v) {
+    uint64_t w[N];
+    if constexpr (N % 2 == 0) {
+#pragma unroll
+        for (int e = 0; e < N; e += 2) ld_tagged2(p + e, w[e], w[e + 1]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < N; ++e) w[e] = ld_tagged(p + e);
+    }
+    unsigned pending = 0;
+#pragma unroll
+    for (int e = 0; e < N; ++e)
+        if ((uint32_t)(w[e] >> 32) != seq) pending |= 1u << e;
+    unsigned long long t0 = 0;
+    while (pending) {
+        const unsigned long long t = cycles_now();
+        if (t0 == 0) t0 = t;
+        else if (t - t0 > wait_cycles(kWaitLimitNs)) return false;
+#pragma unroll
+        for (int e = 0; e < N; ++e)
+            if ((pending >> e) & 1u) w[e] = ld_tagged(p + e);
+#pragma unroll
+        for (int e = 0; e < N; ++e)
+            if ((uint32_t)(w[e] >> 32) == seq) pending &= ~(1u << e);
+    }
+#pragma unroll
+    for (int e = 0; e < N; ++e) v[e] = __uint_as_float((uint32_t)w[e]);
+    return true;
+}
+
+// One thread: n <= N scattered words, addr(i) the address of word i, all loaded at
+// once and every still-stale word re-polled together until each carries `seq`, for
+// at most kWaitLimitNs.  False on timeout.
+template <int N, typename Addr>
+__device__ __forceinline__ bool poll_batch(int n, uint32_t seq, Addr addr, float *v) {
+    static_assert(N <= 32, "pending mask");
+    uint64_t w[N];
+    uint32_t pending = 0;
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+        if (i < n) w[i] = ld_tagged(addr(i));
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+        if (i < n && (uint32_t)(w[i] >> 32) != seq) pending |= 1u << i;
+    unsigned long long t0 = 0;
+    while (pending) {
+        const unsigned long long t = cycles_now();
+        if (t0 == 0) t0 = t;
+        else if (t - t0 > wait_cycles(kWaitLimitNs)) return false;
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            if ((pending >> i) & 1u) w[i] = ld_tagged(addr(i));
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            if (((pending >> i) & 1u) && (uint32_t)(w[i] >> 32) == seq) pending &= ~(1u << i);
+    }
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+        if (i < n) v[i] = __uint_as_float((uint32_t)w[i]);
+    return true;
+}
 
 struct TagSeg {                    // dst[i] = value of src[i], i < n
     const uint64_t *src;
     int n;
     float *dst;
 };
-// Consumer threads: the values of up to three tagged segments once their tags equal
-// `tag`, into shared memory.  Each thread loads a batch of words at once and re-polls
-// every still-stale word of the batch together (one round trip per poll, not one per
-// word), for at most kWaitLimitNs.  False (uniform across the CTA) on timeout.  Ends
-// with a consumer barrier.
-__device__ __noinline__ bool gather_tagged(TagSeg s0, TagSeg s1, TagSeg s2, uint32_t tag) {
-    constexpr int NC = kConsumerWarps * 32, B = 8;
+// Consumer threads: the values of a tagged vector once its words carry `seq`, into
+// shared memory (each thread a batch of words in flight, stale words re-polled
+// together), for at most kWaitLimitNs.  False (uniform across the CTA) on timeout.
+// Ends with a consumer barrier.
+__device__ __noinline__ bool gather_tagged(const uint64_t *src, int n, float *dst, uint32_t seq) {
+    constexpr int B = 8;
     const int tid = threadIdx.x;
-    const int n01 = s0.n + s1.n, n = n01 + s2.n;
     bool ok = true;
     unsigned long long t0 = 0;
-    for (int base = tid; base < n; base += B * NC) {
-        const uint64_t *src[B];
+    for (int base = tid; base < n; base += B * kNC) {
         uint64_t w[B];
         unsigned pending = 0;
 #pragma unroll
         for (int k = 0; k < B; ++k) {
-            const int i = base + k * NC;
-            src[k] = i < s0.n ? s0.src + i : (i < n01 ? s1.src + (i - s0.n) : s2.src + (i - n01));
-            w[k] = i < n ? ld_tagged(src[k]) : (uint64_t)tag << 32;
+            const int i = base + k * kNC;
+            w[k] = i < n ? ld_tagged(src + i) : (uint64_t)seq << 32;
+            if ((uint32_t)(w[k] >> 32) != seq) pending |= 1u << k;
         }
-#pragma unroll
-        for (int k = 0; k < B; ++k)
-            if ((uint32_t)(w[k] >> 32) != tag) pending |= 1u << k;
         while (pending && ok) {
-            const unsigned long long t = global_timer_ns();
+            const unsigned long long t = cycles_now();
             if (t0 == 0) t0 = t;
-            else if (t - t0 > kWaitLimitNs) ok = false;
+            else if (t - t0 > wait_cycles(kWaitLimitNs)) ok = false;
 #pragma unroll
             for (int k = 0; k < B; ++k)
-                if ((pending >> k) & 1u) w[k] = ld_tagged(src[k]);
+                if ((pending >> k) & 1u) w[k] = ld_tagged(src + base + k * kNC);
 #pragma unroll
             for (int k = 0; k < B; ++k)
-                if ((uint32_t)(w[k] >> 32) == tag) pending &= ~(1u << k);
+                if ((uint32_t)(w[k] >> 32) == seq) pending &= ~(1u << k);
         }
 #pragma unroll
         for (int k = 0; k < B; ++k) {
-            const int i = base + k * NC;
-            if (i >= n) continue;
-            float *dst = i < s0.n ? s0.dst + i : (i < n01 ? s1.dst + (i - s0.n) : s2.dst + (i - n01));
-            *dst = __uint_as_float((uint32_t)w[k]);
+            const int i = base + k * kNC;
+            if (i < n) dst[i] = __uint_as_float((uint32_t)w[k]);
         }
     }
-    return !named_sync_or(1, NC, !ok);
-}
-__device__ __forceinline__ bool gather_tagged(const uint64_t *src, int n, float *dst, uint32_t tag) {
-    return gather_tagged(TagSeg{src, n, dst}, TagSeg{nullptr, 0, nullptr}, TagSeg{nullptr, 0, nullptr}, tag);
+    return !named_sync_or(1, kNC, !ok);
 }
 
 // Stage a vector of weights (gamma) into shared memory (consumer threads).
 __device__ __forceinline__ void stage_vec(float *dst, const float *src, int n) {
-    for (int i = threadIdx.x * 4; i < n; i += kConsumerWarps * 32 * 4)
+    for (int i = threadIdx.x * 4; i < n; i += kNC * 4)
         *reinterpret_cast<float4 *>(dst + i) = *reinterpret_cast<const float4 *>(src + i);
-}
-
-// Merge the attention splits into `dst` (shared memory, q_dim floats): thread t of
-// the consumers merges 8 consecutive columns (one head), with every load it needs in
-// flight at once (flash-decoding combine, splits in index order; the same operations
-// in the same order as the cluster merge of the per-phase attention kernel).
-template <int HD>
-__device__ __forceinline__ void combine_to_smem(const float *part_o, const float *part_ml, int ns, int q_dim,
-                                                float *dst) {
-    constexpr int CPT = 8;   // columns per thread
-    for (int c0 = threadIdx.x * CPT; c0 < q_dim; c0 += kConsumerWarps * 32 * CPT) {
-        const int h = c0 / HD, d0 = c0 % HD;
-        const float *ml = part_ml + (size_t)h * kAttnMaxSplits * 2;
-        const float *po = part_o + (size_t)h * kAttnMaxSplits * HD + d0;
-        float2 m_l[kAttnMaxSplits];
-        float4 oa[kAttnMaxSplits], ob[kAttnMaxSplits];
-#pragma unroll
-        for (int t = 0; t < kAttnMaxSplits; ++t) {
-            if (t < ns) {
-                m_l[t] = __ldcg(reinterpret_cast<const float2 *>(ml + 2 * t));
-                oa[t] = __ldcg(reinterpret_cast<const float4 *>(po + (size_t)t * HD));
-                ob[t] = __ldcg(reinterpret_cast<const float4 *>(po + (size_t)t * HD + 4));
-            } else {
-                m_l[t] = make_float2(-INFINITY, 0.f);
-                oa[t] = ob[t] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        }
-        float M = -INFINITY;
-#pragma unroll
-        for (int t = 0; t < kAttnMaxSplits; ++t) M = fmaxf(M, m_l[t].x);
-        float acc[CPT] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        float den = 0.f;
-#pragma unroll
-        for (int t = 0; t < kAttnMaxSplits; ++t) {
-            if (t < ns) {
-                const float w = expf(m_l[t].x - M);
-                acc[0] = fmaf(oa[t].x, w, acc[0]);
-                acc[1] = fmaf(oa[t].y, w, acc[1]);
-                acc[2] = fmaf(oa[t].z, w, acc[2]);
-                acc[3] = fmaf(oa[t].w, w, acc[3]);
-                acc[4] = fmaf(ob[t].x, w, acc[4]);
-                acc[5] = fmaf(ob[t].y, w, acc[5]);
-                acc[6] = fmaf(ob[t].z, w, acc[6]);
-                acc[7] = fmaf(ob[t].w, w, acc[7]);
-                den = fmaf(m_l[t].y, w, den);
-            }
-        }
-        // two 16-byte stores (one per column would put every fourth lane on one bank)
-        *reinterpret_cast<float4 *>(dst + c0) = make_float4(acc[0] / den, acc[1] / den, acc[2] / den, acc[3] / den);
-        *reinterpret_cast<float4 *>(dst + c0 + 4) = make_float4(acc[4] / den, acc[5] / den, acc[6] / den, acc[7] / den);
-    }
 }
 
 __device__ __forceinline__ void cta_rows(int rows, int unit, int &r0, int &nr) {
@@ -203,15 +222,368 @@ __device__ __forceinline__ void cta_rows(int rows, int unit, int &r0, int &nr) {
     nr = (u1 - u0) * unit;
 }
 
-template <typename WT, int HD, int NS_H, int NS_Q, int NS_F>
-__global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const StepArgs a) {
+// ---------------------------------------------------------------- K-chunk GEMV
+// E consecutive elements at p as floats, in 16-, 8- or 4-byte pieces (p aligned to
+// the piece).
+template <typename WT, int E>
+__device__ __forceinline__ void load_elems(const WT *p, float *f) {
+    constexpr int B = E * (int)sizeof(WT);
+    constexpr int PER4 = 4 / (int)sizeof(WT);
+    if constexpr (B % 16 == 0) {
+#pragma unroll
+        for (int i = 0; i < B / 16; ++i)
+            Elem<WT>::unpack(reinterpret_cast<const uint4 *>(p)[i], f + i * 4 * PER4);
+    } else if constexpr (B % 8 == 0) {
+#pragma unroll
+        for (int i = 0; i < B / 8; ++i) {
+            const uint2 u = reinterpret_cast<const uint2 *>(p)[i];
+            if constexpr (sizeof(WT) == 2) {
+                f[4 * i] = bf16lo(u.x); f[4 * i + 1] = bf16hi(u.x);
+                f[4 * i + 2] = bf16lo(u.y); f[4 * i + 3] = bf16hi(u.y);
+            } else {
+                f[2 * i] = __uint_as_float(u.x); f[2 * i + 1] = __uint_as_float(u.y);
+            }
+        }
+    } else if constexpr (B % 4 != 0) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) f[e] = Elem<WT>::load(p, e);
+    } else {
+#pragma unroll
+        for (int i = 0; i < B / 4; ++i) {
+            const uint32_t u = reinterpret_cast<const uint32_t *>(p)[i];
+            if constexpr (sizeof(WT) == 2) {
+                f[2 * i] = bf16lo(u); f[2 * i + 1] = bf16hi(u);
+            } else {
+                f[i] = __uint_as_float(u);
+            }
+        }
+    }
+}
+
+// Transposing butterfly over a warp: lane l holds RP values (RP a power of two <= 32);
+// afterwards lane l holds the sum over the 32 lanes of value l / (32 / RP).  Each
+// level keeps half of the values and receives the partner's other half.
+template <int RP, int O = 16>
+__device__ __forceinline__ float treduce(float *v, int lane) {
+    if constexpr (RP == 1) {
+        float s = v[0];
+#pragma unroll
+        for (int o = O; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        return s;
+    } else {
+        constexpr int H = RP / 2;
+        const bool up = (lane & O) != 0;
+#pragma unroll
+        for (int i = 0; i < H; ++i) {
+            const float send = up ? v[i] : v[i + H];
+            const float keep = up ? v[i + H] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+        }
+        return treduce<H, O / 2>(v, lane);
+    }
+}
+
+// Ring stages of the persistent step: a compile-time count, so a stage's slot and
+// phase parity are cheap to compute (the host checks that the layout has exactly it).
+constexpr int kStepStages = kStepRingStages;
+
+// Consumer side of stage sidx: a non-blocking test first (the weights are normally
+// there long before), then the bounded wait.  Null on timeout.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ const uint8_t *stage_get(const Ring &R, uint32_t sidx) {
+    const uint32_t slot = sidx % kStepStages, par = (sidx / kStepStages) & 1u;
+    if (!mbar_test_wait(&R.full[slot], par) && !mbar_wait_bounded(&R.full[slot], par)) return nullptr;
+    return R.base + (size_t)slot * kSlotBytes;
+}
+__device__ __forceinline__ void stage_put(const Ring &R, uint32_t sidx, int lane) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&R.empty[sidx % kStepStages]);
+}
+
+// Compile-time shape of a GEMV phase: the most rows a CTA holds (the step runs on at
+// least kMinSms SMs), and the rows of a ring stage (padded to a power of two) that can
+// be the CTA's.
+constexpr int kMinSms = kStepMinSms;
+__host__ __device__ constexpr int phase_rows_max(int rows, int unit) {
+    return ((rows / unit) + kMinSms - 1) / kMinSms * unit;
+}
+__host__ __device__ constexpr int min_c(int a, int b) { return a < b ? a : b; }
+__host__ __device__ constexpr int phase_rps(int rows, int unit, int K, int es) {
+    return min_c(pow2_ceil(kSlotBytes / (K * es)), pow2_ceil(phase_rows_max(rows, unit)));
+}
+
+// Consumer warp: the CTA's `nrows` rows of W, arriving in ring stages of `rps` rows,
+// against this warp's K-chunk (lane: E values xv of columns col0 ..).  Rows go in
+// groups of RG (a power of two <= 8): all loads of a group in flight at once, then one
+// transposing butterfly; part[r] (this warp's row of the partial-sum table) gets the
+// chunk's sum of row r.  The loops stay rolled: this code runs once per layer and
+// phase, and its size, not its trip count, is what the instruction cache sees.
+// False if a stage never arrived.
+template <typename WT, int E, int RG>
+__device__ __forceinline__ bool kc_consume(const Ring &R, uint32_t &sidx, int nrows, int rps, uint32_t row_bytes,
+                                           int col0, const float *xv, float *part) {
+    static_assert(RG >= 1 && RG <= 8, "row group");
+    const int lane = threadIdx.x & 31;
+    const int nst = (nrows + rps - 1) / rps;
+#pragma unroll 1
+    for (int st = 0; st < nst; ++st) {
+        const uint8_t *sb = stage_get(R, sidx + st);
+        if (!sb) return false;
+        const int n = min_c(rps, nrows - st * rps);
+#pragma unroll 1
+        for (int g0 = 0; g0 < n; g0 += RG) {
+            // every load unconditional (rows past n re-read row n - 1 and count zero)
+            float acc[RG];
+#pragma unroll
+            for (int r = 0; r < RG; ++r) {
+                const int row = g0 + r < n ? g0 + r : n - 1;
+                float f[E];
+                load_elems<WT, E>(reinterpret_cast<const WT *>(sb + (size_t)row * row_bytes) + col0, f);
+                float d = 0.f;
+#pragma unroll
+                for (int e = 0; e < E; ++e) d = fmaf(f[e], xv[e], d);
+                acc[r] = g0 + r < n ? d : 0.f;
+            }
+            const float v = treduce<RG>(acc, lane);
+            const int row = g0 + lane / (32 / RG);
+            if (lane % (32 / RG) == 0 && row < n) part[st * rps + row] = v;
+        }
+        stage_put(R, sidx + st, lane);
+    }
+    sidx += nst;
+    return true;
+}
+
+// Consumer warp: the CTA's `nrows` rows of W, arriving in ring stages of `rps` rows,
+// against this warp's K-chunk held as NC column chunks of 32 x EL: lane l holds
+// columns colw + c * 32 EL + l EL .. + EL of chunk c in x[c].  Rows go in groups of 8
+// (all loads of a group in flight at once), each group through one transposing
+// butterfly; part[r] (this warp's row of the partial-sum table) gets the chunk's sum
+// of row r.  The loops stay rolled: this code runs for every phase of every layer,
+// and what the instruction cache holds, not trip counts, sets its speed.  False if a
+// stage never arrived.
+template <typename WT, int EL, int NC, int NCMAX>
+__device__ __forceinline__ bool kc_gemv(const Ring &R, uint32_t &sidx, int nrows, int rps, uint32_t row_bytes,
+                                        int colw, const float (*x)[EL], float *part) {
+    const int lane = threadIdx.x & 31;
+    const int nst = (nrows + rps - 1) / rps;
+#pragma unroll 1
+    for (int st = 0; st < nst; ++st) {
+        const uint8_t *sb = stage_get(R, sidx + st);
+        if (!sb) return false;
+        const int n = min_c(rps, nrows - st * rps);
+#pragma unroll 1
+        for (int g0 = 0; g0 < n; g0 += 8) {
+            // every load unconditional (rows past n re-read row n - 1 and count zero)
+            float acc[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int row = g0 + r < n ? g0 + r : n - 1;
+                const WT *wr = reinterpret_cast<const WT *>(sb + (size_t)row * row_bytes) + colw + lane * EL;
+                float d = 0.f;
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                    float f[EL];
+                    load_elems<WT, EL>(wr + c * 32 * EL, f);
+#pragma unroll
+                    for (int e = 0; e < EL; ++e) d = fmaf(f[e], x[c][e], d);
+                }
+                acc[r] = g0 + r < n ? d : 0.f;
+            }
+            const float v = treduce<8>(acc, lane);
+            const int row = g0 + lane / 4;
+            if ((lane & 3) == 0 && row < n) part[st * rps + row] = v;
+        }
+        stage_put(R, sidx + st, lane);
+    }
+    sidx += nst;
+    return true;
+}
+
+// Sum over the consumer warps, in warp order, of entry i of a [kNW][ps] table.
+__device__ __forceinline__ float warp_parts(const float *tab, int ps, int i) {
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < kNW; ++w) v += tab[w * ps + i];
+    return v;
+}
+// RMSNorm scale from the warps' chunk sums of squares.
+__device__ __forceinline__ float rms_scale(const float *ss, int K, float eps) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < kNW; ++w) t += ss[w];
+    return 1.0f / sqrtf(t / (float)K + eps);
+}
+
+// This lane's E columns of the step's input vector (token row of the embedding
+// table, caller embedding, or staged prompt row), resolved from the description
+// that thread 0 staged in misc_i.
+template <typename WT, int E>
+__device__ __forceinline__ void input_cols(const StepInputArgs &in, int K, int mode, int tok, int pos, bool bad, int col,
+                                           float *v) {
+    if (bad) {
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[e] = 0.f;
+    } else if (mode == IN_EMBED || mode == IN_STAGED_EMBEDS) {
+        const float *src = mode == IN_EMBED ? in.embed_in + col : in.stage_embeds + (size_t)pos * K + col;
+#pragma unroll
+        for (int e = 0; e < E; ++e) v[e] = __ldcg(src + e);
+    } else {
+        load_elems<WT, E>(reinterpret_cast<const WT *>(in.table) + (size_t)tok * K + col, v);
+    }
+}
+
+// Rotate-half RoPE of one head held across a warp: lane l holds elements
+// [l E, l E + E); the partner element of the first half sits E * 16 further, in lane
+// l ^ 16.  cs / sn: this lane's frequencies ((l & 15) E + e).
+template <int E>
+__device__ __forceinline__ void rope_lane(float *v, const float *cs, const float *sn, int lane) {
+    const bool second = (lane & 16) != 0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        const float o = __shfl_xor_sync(0xffffffffu, v[e], 16);
+        v[e] = second ? v[e] * cs[e] + o * sn[e] : v[e] * cs[e] - o * sn[e];
+    }
+}
+
+// Per-head RMSNorm of one head held across a warp (E elements per lane).
+template <int E>
+__device__ __forceinline__ void head_norm(float *v, const float *gam, int hd, float eps) {
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) ss = fmaf(v[e], v[e], ss);
+    ss = warp_sum(ss);
+    const float inv = 1.0f / sqrtf(ss / (float)hd + eps);
+#pragma unroll
+    for (int e = 0; e < E; ++e) v[e] = v[e] * inv * gam[e];
+}
+
+template <typename T> __device__ __forceinline__ float round_to(float v);
+template <> __device__ __forceinline__ float round_to<float>(float v) { return v; }
+template <> __device__ __forceinline__ float round_to<__nv_bfloat16>(float v) {
+    return __bfloat162float(__float2bfloat16_rn(v));
+}
+
+// E values of one cache row in the cache type (one 16-, 8- or 4-byte store).
+template <typename KT, int E>
+__device__ __forceinline__ void store_row_elems(KT *dst, const float *v) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) Elem<KT>::store(dst, e, v[e]);
+}
+
+// Scores, softmax and P.V of one warp's positions [jw0, jw0 + nwp) of the split, for
+// the G query heads q (lane: E elements of each), in blocks of 8 positions with a
+// running max and sum (the blocks in order).  Row jp (the new position) comes from kr /
+// vr, the others from the shared-memory tiles.  Outputs the warp's unnormalised o, and
+// per head its max and sum of exponentials (-inf and 0 for a warp without positions).
+template <typename KT, int HD, int G>
+__device__ __forceinline__ void warp_attention(const KT *Ks, const KT *Vs, const float (*q)[HD / 32], int jw0, int nwp,
+                                               int jp, const float *kr, const float *vr, float scale,
+                                               float (*o)[HD / 32], float *mh, float *lh) {
+    constexpr int E = HD / 32;
+    constexpr int RA = 8, LPV = 32 / RA;   // positions per block, lanes holding each score
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        mh[h] = -INFINITY;
+        lh[h] = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[h][e] = 0.f;
+    }
+#pragma unroll 1
+    for (int b0 = 0; b0 < nwp; b0 += RA) {
+        const int nb = nwp - b0 < RA ? nwp - b0 : RA;
+        float pr[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            // unconditional loads of a clamped row, the new position's row from the
+            // register copy; dead positions count zero
+            float acc[RA];
+#pragma unroll
+            for (int jj = 0; jj < RA; ++jj) {
+                const int j = jw0 + b0 + (jj < nb ? jj : nb - 1);
+                float kf[E];
+                load_elems<KT, E>(Ks + (size_t)j * HD + lane * E, kf);
+                float d = 0.f;
+#pragma unroll
+                for (int e = 0; e < E; ++e) d = fmaf(q[h][e], j == jp ? kr[e] : kf[e], d);
+                acc[jj] = jj < nb ? d : 0.f;
+            }
+            float sc = treduce<RA>(acc, lane);
+            const bool live = lane / LPV < nb;
+            sc = live ? sc * scale : -INFINITY;
+            const float mn = fmaxf(mh[h], warp_max(sc));
+            const float corr = expf(mh[h] - mn);   // 0 for the first block
+            const float ex = live ? expf(sc - mn) : 0.f;
+            lh[h] = lh[h] * corr + warp_sum(lane % LPV == 0 ? ex : 0.f);
+#pragma unroll
+            for (int e = 0; e < E; ++e) o[h][e] *= corr;
+            mh[h] = mn;
+            pr[h] = ex;
+        }
+#pragma unroll
+        for (int jj = 0; jj < RA; ++jj) {
+            // dead positions carry weight 0 and re-read a live row
+            const int j = jw0 + b0 + (jj < nb ? jj : nb - 1);
+            float vf[E];
+            load_elems<KT, E>(Vs + (size_t)j * HD + lane * E, vf);
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float ph = __shfl_sync(0xffffffffu, pr[h], jj * LPV);
+#pragma unroll
+                for (int e = 0; e < E; ++e) o[h][e] = fmaf(ph, j == jp ? vr[e] : vf[e], o[h][e]);
+            }
+        }
+    }
+}
+
+// Threads: kNW consumer warps and one producer warpgroup, whose first lane issues the
+// weight stream.  Launched with 168 registers a thread (12 warps on one SM); the
+// producer warpgroup gives back all but 40 of its registers and the consumers take
+// them, 232 each: 128 x 40 + 256 x 232 = 384 x 168, the launch's whole register file.
+constexpr int kStepThreads = (kNW + 4) * 32;
+constexpr int kProducerRegs = 40, kConsumerRegs = 232;
+static_assert(4 * 32 * kProducerRegs + kNW * 32 * kConsumerRegs == kStepThreads * 168, "register split");
+
+template <typename WT, int HD, int KH, int KQ, int KF, int KVH>
+__global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const StepArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     typedef WT KT;
     constexpr int EPL = Elem<WT>::kPer16B;
     constexpr int SEGW = 32 * EPL;
-    constexpr int NC = kConsumerWarps * 32;
+    constexpr int NS_H = KH / SEGW;                       // the head's segments per warp
+    constexpr int ES = (int)sizeof(WT);
+    constexpr int EA = KH / kNC, EQ = KQ / kNC, EF = KF / kNC;   // columns per lane of each K-chunk
+    constexpr int KV = KVH * HD;                                  // k (and v) rows
+    constexpr int GQ = KQ / KV;                                   // q heads per kv head
+    // stage shapes of the GEMV phases (rows per stage padded, stages per butterfly)
+    // GEMV K-chunks: a warp holds K / 8 columns as chunks of 32 lanes x EL (EL from the
+    // hidden size); the phases need NC0 <= NC1 <= NC2 chunks (one GEMV body each)
+    constexpr int EL = KH / kNC;
+    constexpr int NCA = KH / (256 * EL), NCQ = KQ / (256 * EL), NCF = KF / (256 * EL);
+    constexpr int NC0 = NCA, NC1 = NCQ, NC2 = NCF, NCMAX = NCF;
+    static_assert(NCA == 1 && NCQ >= 1 && NCF >= NCQ && KQ == NCQ * 256 * EL && KF == NCF * 256 * EL, "chunks");
+    // row groups of the GEMV phases: 8, or fewer when a CTA holds fewer rows
+    constexpr int A_RG = min_c(8, phase_rps(KQ + 2 * KV, 1, KH, ES));
+    constexpr int C_RG = min_c(8, phase_rps(KH, 1, KQ, ES));
+    constexpr int D_RG = min_c(8, phase_rps(2 * KF, 2, KH, ES));
+    constexpr int E_RG = min_c(8, phase_rps(KH, 1, KF, ES));
+    constexpr int EH = HD / 32;
     constexpr int HALF = HD / 2;
-    constexpr size_t ES = sizeof(WT);
+    constexpr int PS = kStepRowsMax;
+    static_assert(KH % kNC == 0 && KQ % kNC == 0 && KF % kNC == 0, "K-chunks of whole lanes");
+    static_assert(GQ >= 1 && GQ <= kGMax && KQ == GQ * KV, "q heads per kv head");
+    static_assert(NS_H >= 1 && NS_H <= 4 && KH == NS_H * SEGW, "head segments");
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + a.off_full);
     uint64_t *empty = full + a.nst;
     float *gsm = reinterpret_cast<float *>(smem + a.off_gsm);
@@ -221,12 +593,15 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
     int *flag = misc_i + 20;
     float *res = reinterpret_cast<float *>(smem + a.off_res);
     uint32_t *emw = reinterpret_cast<uint32_t *>(smem + a.off_emw);
-    float *xin = reinterpret_cast<float *>(smem + a.off_xin);   // phase input vector
+    float *xin = reinterpret_cast<float *>(smem + a.off_xin);   // the head's gathered input
+    float *kc_part = reinterpret_cast<float *>(smem + a.off_kc);  // [2][kNW][PS] row partials
+    float *kc_ss = kc_part + 2 * kNW * PS;                          // [2][kNW] sums of squares
+    float *xres = reinterpret_cast<float *>(smem + a.off_xres);    // residual rows of this CTA
     const Ring R{smem, full, empty, a.nst};
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int G = a.qh / a.kvh;
-    const int hidden = a.hidden, q_dim = a.qh * HD, kv_dim = a.kvh * HD;
+    constexpr int G = GQ;
+    const int hidden = KH, q_dim = KQ, kv_dim = KV;
     const int CM = a.chunk_max;
 
     // The step's position: the previous launch has completed, so it is final.
@@ -234,19 +609,22 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
     const int L = p + 1;
     const int C = attn_chunk(L);
     const int nsplit = attn_splits(L);
-    const bool valid = p < a.S && C <= CM;
-    const bool has_item = valid && (int)blockIdx.x < a.kvh * nsplit;
+    if (!(p < a.S && C <= CM)) {
+        // outside the bucket: the host never launches this; report it and leave
+        if (blockIdx.x == 0 && tid == 0) atomicOr(&a.st->status, DEV_ERR_BAD_POS);
+        return;
+    }
+    const bool has_item = (int)blockIdx.x < a.kvh * nsplit;
     const int ig = has_item ? (int)blockIdx.x / nsplit : 0;
     const int is = has_item ? (int)blockIdx.x % nsplit : 0;
     const int j0 = is * C;
     const int n_att = has_item ? (L - j0 < C ? L - j0 : C) : 0;
     const int n_old = has_item ? ((p - j0) < n_att ? (p - j0) : n_att) : 0;
 
-    int r0_qkv, n_qkv, r0_o, n_o, r0_gu, n_gu, r0_d, n_d, r0_hd, n_hd;
+    int r0_qkv, n_qkv, r0_x, n_x, r0_gu, n_gu, r0_hd, n_hd;
     cta_rows(q_dim + 2 * kv_dim, 1, r0_qkv, n_qkv);
-    cta_rows(hidden, 1, r0_o, n_o);
+    cta_rows(hidden, 1, r0_x, n_x);                  // rows of Wo and Wd: the residual rows this CTA owns
     cta_rows(2 * a.ffn, 2, r0_gu, n_gu);
-    cta_rows(hidden, 1, r0_d, n_d);
     cta_rows(a.vocab, 1, r0_hd, n_hd);
     const uint32_t rb_h = (uint32_t)(hidden * ES), rb_q = (uint32_t)(q_dim * ES), rb_f = (uint32_t)(a.ffn * ES);
     const size_t layer_kv = (size_t)2 * kv_dim * a.S * ES;
@@ -254,19 +632,20 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
     if (tid == 0) {
         for (int i = 0; i < a.nst; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kConsumerWarps);
+            mbar_init(&empty[i], kNW);
         }
         ctl[0] = 0;
         ctl[1] = 0;
         ctl[2] = 0;
-        if (!valid && blockIdx.x == 0) atomicOr(&a.st->status, DEV_ERR_BAD_POS);
+        misc_i[6] = 0;   // the head's wait for the emitted-set flag timed out
         fence_barrier_init();
     }
     __syncthreads();
 
-    if (warp == kConsumerWarps) {
+    if (warp >= kNW) {
         // ---------------- producer: every phase's weights, in consumption order
-        if (lane == 0) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kProducerRegs) : "memory");
+        if (warp == kNW && lane == 0) {
             const uint64_t pw = a.evict_last ? policy_evict_last() : policy_evict_first();
             const uint64_t pf = policy_evict_first();
             uint32_t sidx = 0;
@@ -283,11 +662,11 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
                     ok = ok && produce_block(R, sidx, kb, bytes, pf);
                     ok = ok && produce_block(R, sidx, kb + layer_kv / 2, bytes, pf);
                 }
-                ok = ok && produce_rows(R, sidx, reinterpret_cast<const uint8_t *>(Ld.w_o) + (size_t)r0_o * rb_q, n_o,
+                ok = ok && produce_rows(R, sidx, reinterpret_cast<const uint8_t *>(Ld.w_o) + (size_t)r0_x * rb_q, n_x,
                                         rb_q, a.rps_q, pw);
                 ok = ok && produce_rows(R, sidx, reinterpret_cast<const uint8_t *>(Ld.w_gu) + (size_t)r0_gu * rb_h,
                                         n_gu, rb_h, a.rps_h, pw);
-                ok = ok && produce_rows(R, sidx, reinterpret_cast<const uint8_t *>(Ld.w_d) + (size_t)r0_d * rb_f, n_d,
+                ok = ok && produce_rows(R, sidx, reinterpret_cast<const uint8_t *>(Ld.w_d) + (size_t)r0_x * rb_f, n_x,
                                         rb_f, a.rps_f, pw);
             }
             if (ok && a.with_head && !ctl[0]) {
@@ -303,174 +682,350 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
     }
 
     // ---------------- consumers
-    // attention scratch: q heads, k, v, RoPE row of position p, QK-norm gammas, scores,
-    // split output; the RoPE row is constant for the launch
-    float *qs = reinterpret_cast<float *>(smem + a.off_att);
-    float *kn = qs + G * HD, *vn = kn + HD, *rc = vn + HD, *qg = rc + HD, *kg = qg + HD, *sc = kg + HD;
-    float *po = sc + G * CM, *pm = po + G * HD, *pl = pm + G;
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kConsumerRegs) : "memory");
+    float *wo = reinterpret_cast<float *>(smem + a.off_att);   // [kNW][G][HD] warp partials of the split
+    float *wml = wo + (size_t)kNW * G * HD;                    // [kNW][G][2]
+    float *rc = wml + (size_t)kNW * G * 2;                     // [HD]: cos then sin of each frequency
     if (has_item) {
-        // rotary position: the cache position + delta, or per stream from the staged prompt
+        // rotary cos / sin at the step's rotary position (per stream from the staged
+        // prompt positions for a multimodal prompt row); constant for the launch
         const int *stage = a.st->rope_staged ? a.rope_stage : nullptr;
         const int pr = p + a.st->rope_delta;
-        for (int m = tid; m < HALF; m += NC) {
+        for (int m = tid; m < HALF; m += kNC) {
             const size_t r = (size_t)rope_row(m, a.mrope_h, stage, a.rope_stride, p, pr, a.rope_rows);
             rc[m] = a.rope_cos[r * HALF + m];
             rc[HALF + m] = a.rope_sin[r * HALF + m];
         }
     }
     const int rr_h = warp / a.rs_h, colb_h = (warp % a.rs_h) * (hidden / a.rs_h);
-    const int colb_q = (warp % a.rs_q) * (q_dim / a.rs_q);
-    const int colb_f = (warp % a.rs_f) * (a.ffn / a.rs_f);
     uint32_t sidx = 0;
     unsigned epoch = 0;
     bool ok = true;
+    int buf = 0;   // partial-sum table of the phase (alternates: a phase's row threads read
+                   // one table while warps already on the next phase fill the other)
     // this launch's sequence number (advanced once every CTA has read it: at the commit)
     const uint32_t seq = *reinterpret_cast<volatile const unsigned *>(a.seq);
 
+    // the layer table in shared memory: each layer's gamma pointers are one
+    // shared-memory load away, not a global round trip
+    LayerDev *ldev = reinterpret_cast<LayerDev *>(smem + a.off_ldev);
+    for (int i = tid; i < a.n_layers * (int)(sizeof(LayerDev) / 8); i += kNC)
+        reinterpret_cast<uint64_t *>(ldev)[i] = reinterpret_cast<const uint64_t *>(a.layers)[i];
+    named_sync(1, kNC);
+
     for (int l = 0; l < a.n_layers && ok; ++l) {
-        const LayerDev &Ld = a.layers[l];
-        // ---- A: qkv = [Wq; Wk; Wv] RMSNorm(x)
-        stage_vec(gsm, Ld.attn_norm, hidden);
-        {
-            float xr[NS_H * EPL];
-            if (l == 0) {
-                step_input_slice<WT, NS_H>(a.in, a.st, hidden, a.rs_h, colb_h, xr, misc_i, a.x, a.tap_hidden);
+        const LayerDev &Ld = ldev[l];
+        uint64_t *T = a.tg + (size_t)l * a.tg_stride;
+        float gq[EH], gk[EH];
+        if (has_item && Ld.q_norm) {
+            load_elems<float, EH>(Ld.q_norm + lane * EH, gq);
+            load_elems<float, EH>(Ld.k_norm + lane * EH, gk);
+        }
+        // The four GEMV phases share one body (rolled, so its code is fetched once per
+        // layer): A qkv = [Wq; Wk; Wv] RMSNorm(x); then the attention; C x += Wo o;
+        // D act = silu(Wg x^) * (Wu x^), x^ = RMSNorm(x); E x += Wd act.
+#pragma unroll 1
+        for (int ph = 0; ph < 4 && ok; ++ph) {
+            if (ph == 1) {
+                // ---- B: attention of this CTA's (group, split), then its share of the merge
+                bool okb = true;
+                do {
+            // ---- B: attention of this CTA's (group, split), then its share of the merge
+            if (has_item) {
+                const int pw = (n_att + kNW - 1) / kNW;     // positions per warp
+                const int jw0 = warp * pw;
+                const int nwp = n_att - jw0 < pw ? (n_att - jw0 > 0 ? n_att - jw0 : 0) : pw;
+                const int jp = p - j0;                      // the new position within the split
+                const bool owner = n_old < n_att && jp >= jw0 && jp < jw0 + nwp;
+                // this lane's columns of the group's q heads, and (owner) of k and v, in one
+                // batch of polls
+                const uint64_t *qb = T + a.tg_qkv + (size_t)ig * G * HD + lane * EH;
+                const uint64_t *kb = T + a.tg_qkv + q_dim + (size_t)ig * HD + lane * EH;
+                const int nq = G * EH;
+                float wv[(kGMax + 2) * EH];
+                bool okw = poll_batch<(kGMax + 2) * EH>(nq + (owner ? 2 * EH : 0), seq,
+                                                        [&](int i) {
+                                                            return i < nq ? qb + (size_t)(i / EH) * HD + i % EH
+                                                                          : kb + (size_t)((i - nq) / EH) * kv_dim +
+                                                                                (i - nq) % EH;
+                                                        },
+                                                        wv);
+                okw = __all_sync(0xffffffffu, okw);
+                float q[kGMax][EH], kr[EH], vr[EH];
+    #pragma unroll
+                for (int h = 0; h < kGMax; ++h)
+    #pragma unroll
+                    for (int e = 0; e < EH; ++e) q[h][e] = wv[h * EH + e];
+    #pragma unroll
+                for (int e = 0; e < EH; ++e) {
+                    kr[e] = 0.f;
+                    vr[e] = 0.f;
+    #pragma unroll
+                    for (int h = 0; h <= kGMax; ++h)
+                        if (h == G) {
+                            kr[e] = wv[h * EH + e];
+                            vr[e] = wv[(h + 1) * EH + e];
+                        }
+                }
+                if (Ld.q_norm) {
+    #pragma unroll
+                    for (int h = 0; h < kGMax; ++h)
+                        if (h < G) head_norm<EH>(q[h], gq, HD, a.eps);
+                    if (owner) head_norm<EH>(kr, gk, HD, a.eps);
+                }
+                float rcs[EH], rsn[EH];
+    #pragma unroll
+                for (int e = 0; e < EH; ++e) {
+                    rcs[e] = rc[(lane & 15) * EH + e];
+                    rsn[e] = rc[HALF + (lane & 15) * EH + e];
+                }
+    #pragma unroll
+                for (int h = 0; h < kGMax; ++h)
+                    if (h < G) rope_lane<EH>(q[h], rcs, rsn, lane);
+                if (owner) {
+                    // append the new row to the cache (cache type), and use the rounded row
+                    rope_lane<EH>(kr, rcs, rsn, lane);
+    #pragma unroll
+                    for (int e = 0; e < EH; ++e) {
+                        kr[e] = round_to<KT>(kr[e]);
+                        vr[e] = round_to<KT>(vr[e]);
+                    }
+                    KT *kw = reinterpret_cast<KT *>(reinterpret_cast<uint8_t *>(a.kv) + (size_t)l * layer_kv) +
+                             ((size_t)ig * a.S + p) * HD + lane * EH;
+                    KT *vw = reinterpret_cast<KT *>(reinterpret_cast<uint8_t *>(a.kv) + (size_t)l * layer_kv +
+                                                    layer_kv / 2) +
+                             ((size_t)ig * a.S + p) * HD + lane * EH;
+                    store_row_elems<KT, EH>(kw, kr);
+                    store_row_elems<KT, EH>(vw, vr);
+                    fence_proxy_async_global();   // later bulk copies read the row
+                }
+                const uint8_t *kslot = okw ? stage_get(R, sidx) : nullptr;
+                const uint8_t *vslot = kslot ? stage_get(R, sidx + 1) : nullptr;
+                okw = __all_sync(0xffffffffu, vslot != nullptr);
+                float o[kGMax][EH], mh[kGMax], lh[kGMax];
+                if (okw) {
+                    const KT *Ks = reinterpret_cast<const KT *>(kslot);
+                    const KT *Vs = reinterpret_cast<const KT *>(vslot);
+                    warp_attention<KT, HD, G>(Ks, Vs, q, jw0, nwp, jp, kr, vr, a.scale, o, mh, lh);
+    #pragma unroll
+                    for (int h = 0; h < kGMax; ++h) {
+                        if (h >= G) continue;
+                        float *dst = wo + ((size_t)warp * G + h) * HD + lane * EH;
+    #pragma unroll
+                        for (int e = 0; e < EH; ++e) dst[e] = o[h][e];
+                        if (lane == 0) {
+                            wml[((size_t)warp * G + h) * 2] = mh[h];
+                            wml[((size_t)warp * G + h) * 2 + 1] = lh[h];
+                        }
+                    }
+                    stage_put(R, sidx, lane);
+                    stage_put(R, sidx + 1, lane);
+                }
+                sidx += 2;
+                ok = !named_sync_or(1, kNC, !okw);
+                if (!ok) { okb = false; break; }
+                // the split's partial, the warps merged in warp order: its normalised output
+                // o / l and, per head, its log-sum-exp m + log(l)
+                const int GD = G * HD;
+                uint64_t *Tpo = T + a.tg_po + ((size_t)ig * kAttnMaxSplits + is) * GD;
+                uint64_t *Tml = T + a.tg_ml + ((size_t)ig * kAttnMaxSplits + is) * G * 2;
+                for (int t = tid; t < GD; t += kNC) {
+                    const int h = t / HD, d = t % HD;
+                    float M = -INFINITY;
+    #pragma unroll
+                    for (int w = 0; w < kNW; ++w) M = fmaxf(M, wml[((size_t)w * G + h) * 2]);
+                    float den = 0.f, num = 0.f;
+    #pragma unroll
+                    for (int w = 0; w < kNW; ++w) {
+                        const float mw = wml[((size_t)w * G + h) * 2];
+                        if (mw != -INFINITY) {
+                            const float f = expf(mw - M);
+                            den = fmaf(f, wml[((size_t)w * G + h) * 2 + 1], den);
+                            num = fmaf(f, wo[((size_t)w * G + h) * HD + d], num);
+                        }
+                    }
+                    st_tag(Tpo + t, num / den, seq);
+                    if (d == 0) st_tag(Tml + 2 * h, M + logf(den), seq);
+                }
+                // this CTA's slice [d0, d1) of the group's merged output: every split's output
+                // weighted by exp(lse_s - max) over their sum.  A group of LP lanes (LP >=
+                // splits, a power of two) takes one column, lane s its split s; each thread
+                // takes two (column, split) pairs, polled in one batch, and the group reduces
+                // them with shuffles.
+                const int d0 = is * GD / nsplit, d1 = (is + 1) * GD / nsplit;
+                const int LP = nsplit <= 1 ? 1 : (nsplit <= 2 ? 2 : (nsplit <= 4 ? 4 : 8));
+                const uint64_t *Gpo = T + a.tg_po + (size_t)ig * kAttnMaxSplits * GD;
+                const uint64_t *Gml = T + a.tg_ml + (size_t)ig * kAttnMaxSplits * G * 2;
+                bool okm = true;
+                for (int c0 = 0; c0 < (d1 - d0) * LP; c0 += 2 * kNC) {
+                    // pairs c and c + kNC: the same split (LP divides kNC), so the second is
+                    // live only when the first is
+                    const int ca = c0 + tid, cb = ca + kNC;
+                    const int sp = ca % LP, cola = d0 + ca / LP, colb = d0 + cb / LP;
+                    const bool la = cola < d1 && sp < nsplit, lb = colb < d1 && sp < nsplit;
+                    float wv[4];
+                    const bool got = poll_batch<4>(la ? (lb ? 4 : 2) : 0, seq,
+                                                   [&](int i) {
+                                                       const int cl = i < 2 ? cola : colb;
+                                                       return (i & 1) ? Gpo + (size_t)sp * GD + cl
+                                                                      : Gml + ((size_t)sp * G + cl / HD) * 2;
+                                                   },
+                                                   wv);
+                    okm = okm && got;
+    #pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const bool lv = k == 0 ? la : lb;
+                        const float lse = lv ? wv[2 * k] : -INFINITY;
+                        const float ov = lv ? wv[2 * k + 1] : 0.f;
+                        float M = lse;
+                        for (int o = 1; o < LP; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+                        float f = lv ? expf(lse - M) : 0.f;
+                        float num = f * ov;
+                        for (int o = 1; o < LP; o <<= 1) {
+                            f += __shfl_xor_sync(0xffffffffu, f, o);
+                            num += __shfl_xor_sync(0xffffffffu, num, o);
+                        }
+                        if (lv && sp == 0) st_tag(T + a.tg_att + (size_t)ig * GD + (k == 0 ? cola : colb), num / f, seq);
+                    }
+                }
+                if (!okm) ok = false;
+            }
+
+                } while (false);
+                if (!okb) break;
+            }
+            // this phase: input words, RMSNorm gamma (A, D), K, rows of W
+            const uint64_t *src;
+            const float *gam;
+            int K, nrows, rps;
+            uint32_t rbytes;
+            if (ph == 0) {
+                src = l ? a.tg + (size_t)(l - 1) * a.tg_stride + a.tg_xe : nullptr;
+                gam = Ld.attn_norm; K = KH; nrows = n_qkv; rps = a.rps_h; rbytes = rb_h;
+            } else if (ph == 1) {
+                src = T + a.tg_att; gam = nullptr; K = KQ; nrows = n_x; rps = a.rps_q; rbytes = rb_q;
+            } else if (ph == 2) {
+                src = T + a.tg_xc; gam = Ld.mlp_norm; K = KH; nrows = n_gu; rps = a.rps_h; rbytes = rb_h;
             } else {
-                ok = gather_tagged(a.x_t, hidden, xin, phase_tag(seq, l - 1, 4));
-                if (!ok) break;
-                smem_slice<WT, NS_H>(xin, colb_h, xr);
-                if (a.tap_hidden && blockIdx.x == 0 && rr_h == 0) {
+                src = T + a.tg_act; gam = nullptr; K = KF; nrows = n_x; rps = a.rps_f; rbytes = rb_f;
+            }
+            const int nc = K / (256 * EL);          // column chunks of 32 x EL per warp
+            const int colw = warp * (K / kNW);       // this warp's first column
+            float x[NCMAX][EL], gv[NCMAX][EL];
 #pragma unroll
-                    for (int sg = 0; sg < NS_H; ++sg)
+            for (int cc = 0; cc < NCMAX; ++cc)
 #pragma unroll
-                        for (int e = 0; e < EPL; ++e)
-                            a.tap_hidden[(size_t)l * hidden + colb_h + sg * SEGW + lane * EPL + e] = xr[sg * EPL + e];
+                for (int e = 0; e < EL; ++e) {
+                    x[cc][e] = 0.f;
+                    gv[cc][e] = 1.f;
+                }
+            if (gam)
+#pragma unroll
+                for (int cc = 0; cc < NCMAX; ++cc)
+                    if (cc < nc) load_elems<float, EL>(gam + colw + cc * 32 * EL + lane * EL, gv[cc]);
+            bool okw = true;
+            if (src) {
+                // this lane's words of every chunk, in one batch of polls
+                float wv[NCMAX * EL];
+                okw = poll_batch<NCMAX * EL>(nc * EL, seq,
+                                             [&](int i) { return src + colw + (i / EL) * 32 * EL + lane * EL + i % EL; },
+                                             wv);
+#pragma unroll
+                for (int cc = 0; cc < NCMAX; ++cc)
+#pragma unroll
+                    for (int e = 0; e < EL; ++e) x[cc][e] = cc < nc ? wv[cc * EL + e] : 0.f;
+                if (ph == 0 && a.tap_hidden && blockIdx.x == 0)
+#pragma unroll
+                    for (int cc = 0; cc < NCMAX; ++cc)
+#pragma unroll
+                        for (int e = 0; e < EL; ++e)
+                            if (cc < nc) a.tap_hidden[(size_t)l * hidden + colw + cc * 32 * EL + lane * EL + e] = x[cc][e];
+            } else {
+                // the step input: thread 0 resolves the step description; CTA 0 records
+                // the token in the emitted set and publishes that with a release flag
+                if (tid == 0) {
+                    DevState *st = a.st;
+                    const int mode = st->in_mode;
+                    int tok = st->token_in;
+                    if (mode == IN_FEEDBACK) tok = st->out_id;
+                    else if (mode == IN_STAGED_TOKENS) tok = p < a.in.S ? a.in.stage_tokens[p] : -1;
+                    else if (mode == IN_STAGED_EMBEDS) tok = -1;
+                    const bool needs_row = (mode == IN_TOKEN || mode == IN_FEEDBACK || mode == IN_STAGED_TOKENS);
+                    int bad = 0;
+                    if (needs_row && (tok < 0 || tok >= a.in.table_rows || a.in.table == nullptr)) {
+                        bad = 1;
+                        if (blockIdx.x == 0) atomicOr(&st->status, DEV_ERR_BAD_TOKEN);
+                    }
+                    if (blockIdx.x == 0) {
+                        if (st->add_emitted && tok >= 0 && tok < a.in.vocab)
+                            a.in.emitted[tok >> 5] |= 1u << (tok & 31);
+                        asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a.emit_flag), "r"(seq) : "memory");
+                    }
+                    misc_i[0] = mode;
+                    misc_i[1] = tok;
+                    misc_i[2] = bad;
+                }
+                named_sync(1, kNC);
+                const int mode = misc_i[0], tok = misc_i[1];
+                const bool bad = misc_i[2] != 0;
+#pragma unroll
+                for (int cc = 0; cc < NCMAX; ++cc)
+                    if (cc < nc) {
+                        const int col = colw + cc * 32 * EL + lane * EL;
+                        input_cols<WT, EL>(a.in, hidden, mode, tok, p, bad, col, x[cc]);
+                        if (blockIdx.x == 0)
+#pragma unroll
+                            for (int e = 0; e < EL; ++e) {
+                                a.x[col + e] = x[cc][e];
+                                if (a.tap_hidden) a.tap_hidden[col + e] = x[cc][e];
+                            }
+                    }
+                if (tid < n_x) {
+                    float xo;
+                    input_cols<WT, 1>(a.in, hidden, mode, tok, p, bad, r0_x + tid, &xo);
+                    xres[tid] = xo;
                 }
             }
-            rmsnorm_slice<WT, NS_H>(xr, gsm, hidden, a.rs_h, colb_h, a.eps, misc, nullptr);
-            const bool got = gemv_consume<WT, NS_H>(R, sidx, n_qkv, a.rps_h, rb_h, a.rs_h, colb_h, xr, res);
-            ok = !named_sync_or(1, NC, !got);
-            if (!ok) break;
-        }
-        for (int r = tid; r < n_qkv; r += NC) {
-            float v = 0.f;
-            for (int j = 0; j < a.rs_h; ++j) v += res[r * a.rs_h + j];
-            a.qkv[r0_qkv + r] = v;
-            st_tagged(a.qkv_t + r0_qkv + r, v, phase_tag(seq, l, 0));
-        }
-        if (has_item && Ld.q_norm)
-            for (int i = tid; i < HD; i += NC) {
-                qg[i] = Ld.q_norm[i];
-                kg[i] = Ld.k_norm[i];
-            }
-
-        // ---- B: attention of this CTA's (group, split)
-        if (has_item) {
-            // the group's q heads, k and v, as their writers tag them
-            ok = gather_tagged(TagSeg{a.qkv_t + (size_t)ig * G * HD, G * HD, qs},
-                               TagSeg{a.qkv_t + (size_t)q_dim + (size_t)ig * HD, HD, kn},
-                               TagSeg{a.qkv_t + (size_t)(q_dim + kv_dim) + (size_t)ig * HD, HD, vn},
-                               phase_tag(seq, l, 0));
-            if (!ok) break;
-            qk_norm_rope<HD, kConsumerWarps>(qs, kn, G, Ld.q_norm ? qg : nullptr, kg, a.eps, rc, 1);
-            const uint8_t *kslot = slot_acquire(R, sidx);
-            const uint8_t *vslot = kslot ? slot_acquire(R, sidx + 1) : nullptr;
-            ok = !named_sync_or(1, NC, vslot == nullptr);
-            if (!ok) break;
-            KT *Ks = reinterpret_cast<KT *>(const_cast<uint8_t *>(kslot));
-            KT *Vs = reinterpret_cast<KT *>(const_cast<uint8_t *>(vslot));
-            if (n_old < n_att) {
-                // this split holds position p: append the new row (cache type)
-                KT *kw = reinterpret_cast<KT *>(reinterpret_cast<uint8_t *>(a.kv) + (size_t)l * layer_kv) +
-                         ((size_t)ig * a.S + p) * HD;
-                KT *vw = reinterpret_cast<KT *>(reinterpret_cast<uint8_t *>(a.kv) + (size_t)l * layer_kv +
-                                                layer_kv / 2) +
-                         ((size_t)ig * a.S + p) * HD;
-                for (int i = tid; i < HD; i += NC) {
-                    Elem<KT>::store(Ks + n_old * HD, i, kn[i]);
-                    Elem<KT>::store(Vs + n_old * HD, i, vn[i]);
-                    Elem<KT>::store(kw, i, kn[i]);
-                    Elem<KT>::store(vw, i, vn[i]);
+            okw = __all_sync(0xffffffffu, okw);
+            float ss = 0.f;
+#pragma unroll
+            for (int cc = 0; cc < NCMAX; ++cc)
+#pragma unroll
+                for (int e = 0; e < EL; ++e) {
+                    ss = fmaf(x[cc][e], x[cc][e], ss);
+                    x[cc][e] *= gv[cc][e];
                 }
-                fence_proxy_async_global();
+            float *part = kc_part + buf * kNW * PS;
+            if (okw) {
+                if (nc == NC0) okw = kc_gemv<WT, EL, NC0, NCMAX>(R, sidx, nrows, rps, rbytes, colw, x, part + warp * PS);
+                else if (nc == NC1) okw = kc_gemv<WT, EL, NC1, NCMAX>(R, sidx, nrows, rps, rbytes, colw, x, part + warp * PS);
+                else okw = kc_gemv<WT, EL, NC2, NCMAX>(R, sidx, nrows, rps, rbytes, colw, x, part + warp * PS);
             }
-            named_sync(1, NC);
-            attn_split<KT, HD, kConsumerWarps>(Ks, Vs, qs, G, n_att, CM, a.scale, sc, po, pm, pl, 1);
-            named_sync(1, NC);
-            for (int i = tid; i < G * HD; i += NC) {
-                const int hh = i / HD, d = i % HD;
-                a.part_o[((size_t)(ig * G + hh) * kAttnMaxSplits + is) * HD + d] = po[i];
+            if (gam) {
+                ss = warp_sum(ss);
+                if (lane == 0) kc_ss[buf * kNW + warp] = ss;
             }
-            for (int hh = tid; hh < G; hh += NC) {
-                float *ml = a.part_ml + ((size_t)(ig * G + hh) * kAttnMaxSplits + is) * 2;
-                ml[0] = pm[hh];
-                ml[1] = pl[hh];
-            }
-            fence_proxy_async_smem();   // generic writes into the slots precede their next bulk fill
-            slot_release(R, sidx, lane);
-            slot_release(R, sidx + 1, lane);
-            sidx += 2;
-        }
-        ok = grid_sync(a.barrier, epoch, flag);
-        if (!ok) break;
-
-        // ---- C: x += Wo (merged attention output)
-        {
-            const float xold = tid < n_o ? __ldcg(a.x + r0_o + tid) : 0.f;
-            float xr[NS_Q * EPL];
-            combine_to_smem<HD>(a.part_o, a.part_ml, valid ? nsplit : 0, q_dim, xin);
-            named_sync(1, NC);
-            smem_slice<WT, NS_Q>(xin, colb_q, xr);
-            const bool got = gemv_consume<WT, NS_Q>(R, sidx, n_o, a.rps_q, rb_q, a.rs_q, colb_q, xr, res);
-            ok = !named_sync_or(1, NC, !got);
+            ok = !named_sync_or(1, kNC, !okw);
             if (!ok) break;
-            if (tid < n_o) {
-                float v = 0.f;
-                for (int j = 0; j < a.rs_q; ++j) v += res[tid * a.rs_q + j];
-                a.x[r0_o + tid] = xold + v;
-                st_tagged(a.x_t + r0_o + tid, xold + v, phase_tag(seq, l, 2));
+            // the phase's rows: thread i sums row i over the warps, in warp order
+            if (ph == 0) {
+                if (tid < n_qkv)
+                    st_tag(T + a.tg_qkv + r0_qkv + tid,
+                           rms_scale(kc_ss + buf * kNW, hidden, a.eps) * warp_parts(part, PS, tid), seq);
+            } else if (ph == 2) {
+                if (tid < n_gu / 2) {
+                    const float r = rms_scale(kc_ss + buf * kNW, hidden, a.eps);
+                    const float gt = r * warp_parts(part, PS, 2 * tid);
+                    const float up = r * warp_parts(part, PS, 2 * tid + 1);
+                    st_tag(T + a.tg_act + r0_gu / 2 + tid, gt / (1.0f + expf(-gt)) * up, seq);
+                }
+            } else if (tid < n_x) {
+                const float xn = xres[tid] + warp_parts(part, PS, tid);
+                xres[tid] = xn;
+                a.x[r0_x + tid] = xn;
+                st_tag(T + (ph == 1 ? a.tg_xc : a.tg_xe) + r0_x + tid, xn, seq);
             }
-        }
-        stage_vec(gsm, Ld.mlp_norm, hidden);
-
-        // ---- D: act = silu(Wg x^) * (Wu x^), x^ = RMSNorm(x)
-        {
-            float xr[NS_H * EPL];
-            ok = gather_tagged(a.x_t, hidden, xin, phase_tag(seq, l, 2));
-            if (!ok) break;
-            smem_slice<WT, NS_H>(xin, colb_h, xr);
-            rmsnorm_slice<WT, NS_H>(xr, gsm, hidden, a.rs_h, colb_h, a.eps, misc, nullptr);
-            const bool got = gemv_consume<WT, NS_H>(R, sidx, n_gu, a.rps_h, rb_h, a.rs_h, colb_h, xr, res);
-            ok = !named_sync_or(1, NC, !got);
-            if (!ok) break;
-        }
-        for (int i = tid; i < n_gu / 2; i += NC) {
-            float g = 0.f, u = 0.f;
-            for (int j = 0; j < a.rs_h; ++j) {
-                g += res[(2 * i) * a.rs_h + j];
-                u += res[(2 * i + 1) * a.rs_h + j];
-            }
-            const float act = g / (1.0f + expf(-g)) * u;
-            a.act[r0_gu / 2 + i] = act;
-            st_tagged(a.act_t + r0_gu / 2 + i, act, phase_tag(seq, l, 3));
-        }
-
-        // ---- E: x += Wd act (x rows: this thread's own, written in C)
-        {
-            const float xold = tid < n_d ? __ldcg(a.x + r0_d + tid) : 0.f;
-            float xr[NS_F * EPL];
-            ok = gather_tagged(a.act_t, a.ffn, xin, phase_tag(seq, l, 3));
-            if (!ok) break;
-            smem_slice<WT, NS_F>(xin, colb_f, xr);
-            const bool got = gemv_consume<WT, NS_F>(R, sidx, n_d, a.rps_f, rb_f, a.rs_f, colb_f, xr, res);
-            ok = !named_sync_or(1, NC, !got);
-            if (!ok) break;
-            if (tid < n_d) {
-                float v = 0.f;
-                for (int j = 0; j < a.rs_f; ++j) v += res[tid * a.rs_f + j];
-                a.x[r0_d + tid] = xold + v;
-                st_tagged(a.x_t + r0_d + tid, xold + v, phase_tag(seq, l, 4));
-            }
+            buf ^= 1;
         }
     }
 
@@ -479,9 +1034,22 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
         stage_vec(gsm, a.final_norm, hidden);
         const int w0 = r0_hd >> 5;
         const int nw = n_hd > 0 ? ((r0_hd + n_hd - 1) >> 5) - w0 + 1 : 0;
-        if (a.penalty != 1.0f)
-            for (int i = tid; i < nw; i += NC) emw[i] = __ldcg(a.in.emitted + w0 + i);
-        ok = gather_tagged(a.x_t, hidden, xin, phase_tag(seq, a.n_layers - 1, 4));
+        if (tid == 0 && a.penalty != 1.0f) {
+            // the emitted set as CTA 0 left it at this step's start (its release flag)
+            const unsigned long long t0 = cycles_now();
+            while (true) {
+                unsigned v;
+                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a.emit_flag) : "memory");
+                if (v == seq) break;
+                if (cycles_now() - t0 > wait_cycles(kWaitLimitNs)) {
+                    misc_i[6] = 1;
+                    break;
+                }
+            }
+        }
+        ok = gather_tagged(a.tg + (size_t)(a.n_layers - 1) * a.tg_stride + a.tg_xe, hidden, xin, seq);
+        if (ok && a.penalty != 1.0f)
+            for (int i = tid; i < nw; i += kNC) emw[i] = __ldcg(a.in.emitted + w0 + i);
         if (ok) {
             float xr[NS_H * EPL];
             smem_slice<WT, NS_H>(xin, colb_h, xr);
@@ -496,7 +1064,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
             rmsnorm_slice<WT, NS_H>(xr, gsm, hidden, a.rs_h, colb_h, a.eps, misc,
                                     blockIdx.x == 0 ? a.y_out : nullptr);
             const bool got = gemv_consume<WT, NS_H>(R, sidx, n_hd, a.rps_h, rb_h, a.rs_h, colb_h, xr, res);
-            ok = !named_sync_or(1, NC, !got);
+            ok = !named_sync_or(1, kNC, !got || (tid == 0 && misc_i[6] != 0));
         }
         if (ok) {
             // greedy: per-thread, per-warp, per-CTA argmax.  Sampling (top-k > 0): the
@@ -504,7 +1072,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
             const int sk = a.st->sample_k;
             float best_v = -INFINITY;
             int best_i = INT_MAX;
-            for (int r = tid; r < n_hd; r += NC) {
+            for (int r = tid; r < n_hd; r += kNC) {
                 float v = 0.f;
                 for (int j = 0; j < a.rs_h; ++j) v += res[r * a.rs_h + j];
                 const int row = r0_hd + r;
@@ -526,7 +1094,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
             int *scr = ci + kMaxTopK;
             uint64_t *all_k = reinterpret_cast<uint64_t *>(scr + kTopkScratchWords);   // 8-byte aligned
             if (sk > 0) {
-                named_sync(1, NC);
+                named_sync(1, kNC);
                 block_topk(res, a.rs_h, nullptr, r0_hd, n_hd, sk, cv, ci, scr);
                 if (tid < sk) {
                     a.part_v[(size_t)blockIdx.x * sk + tid] = cv[tid];
@@ -547,7 +1115,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
                     misc_i[8 + warp] = best_i;
                 }
             }
-            named_sync(1, NC);
+            named_sync(1, kNC);
             if (tid == 0) {
                 if (sk == 0) {
                     float bv = misc[8];
@@ -564,7 +1132,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
                 const int prev = atomicAdd(a.head_counter, 1);
                 misc_i[5] = (prev == (int)gridDim.x - 1);
             }
-            named_sync(1, NC);
+            named_sync(1, kNC);
             // last CTA: the step's id, published; the position advanced
             auto commit = [&](int id) {
                 *a.head_counter = 0;
@@ -618,7 +1186,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
         ok = grid_sync(a.barrier, epoch, flag);
         if (ok && blockIdx.x == 0) {
             if (a.tap_hidden)
-                for (int i = tid; i < hidden; i += NC)
+                for (int i = tid; i < hidden; i += kNC)
                     a.tap_hidden[(size_t)a.n_layers * hidden + i] = __ldcg(a.x + i);
             if (tid == 0) {
                 a.st->pos = p + 1;
@@ -629,13 +1197,13 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
 
     if (!ok) {
         // timeout: stop the producer, let copies already issued land, leave
-        named_sync(1, NC);
+        named_sync(1, kNC);
         if (tid == 0) {
             atomicOr(&a.st->status, DEV_ERR_WAIT_TIMEOUT);
             advance_seq(a.seq, seq);   // no tag of this launch is ever taken as fresh
             ctl[0] = 1;
-            const unsigned long long t0 = global_timer_ns();
-            while (!ctl[2] && global_timer_ns() - t0 < 2 * kWaitLimitNs + 100000000ull) {
+            const unsigned long long t0 = cycles_now();
+            while (!ctl[2] && cycles_now() - t0 < wait_cycles(2 * kWaitLimitNs + 100000000ull)) {
             }
             const uint32_t issued = (uint32_t)ctl[1];
             for (uint32_t s2 = sidx; s2 < issued; ++s2)
@@ -651,41 +1219,42 @@ __global__ void __launch_bounds__(kGemvThreads, 1) decode_step_kernel(const Step
 typedef void (*StepFn)(const StepArgs);
 
 // Shapes with an instantiation: (dtype, head_dim, hidden, q_dim, ffn)
-static StepFn step_fn(bool bf16, int hd, int hidden, int q_dim, int ffn) {
-    if (!bf16 && hd == 64 && hidden == 256 && q_dim == 256 && ffn == 768)
-        return decode_step_kernel<float, 64, 2, 2, 3>;          // one-layer fp32 decoder
-    if (bf16 && hd == 64 && hidden == 512 && q_dim == 512 && ffn == 2048)
-        return decode_step_kernel<__nv_bfloat16, 64, 2, 2, 4>;  // ASR decoder
-    if (bf16 && hd == 128 && hidden == 1024 && q_dim == 2048 && ffn == 3072)
-        return decode_step_kernel<__nv_bfloat16, 128, 4, 4, 3>; // talker / code predictor
+static StepFn step_fn(bool bf16, int hd, int hidden, int q_dim, int ffn, int kvh) {
+    if (!bf16 && hd == 64 && hidden == 256 && q_dim == 256 && ffn == 768 && kvh == 2)
+        return decode_step_kernel<float, 64, 256, 256, 768, 2>;             // one-layer fp32 decoder
+    if (bf16 && hd == 64 && hidden == 512 && q_dim == 512 && ffn == 2048 && kvh == 8)
+        return decode_step_kernel<__nv_bfloat16, 64, 512, 512, 2048, 8>;    // ASR decoder
+    if (bf16 && hd == 128 && hidden == 1024 && q_dim == 2048 && ffn == 3072 && kvh == 8)
+        return decode_step_kernel<__nv_bfloat16, 128, 1024, 2048, 3072, 8>; // talker / code predictor
     return nullptr;
 }
 
-bool persistent_supported(bool bf16, int hd, int hidden, int q_dim, int ffn) {
-    return step_fn(bf16, hd, hidden, q_dim, ffn) != nullptr;
+bool persistent_supported(bool bf16, int hd, int hidden, int q_dim, int ffn, int kvh) {
+    return step_fn(bf16, hd, hidden, q_dim, ffn, kvh) != nullptr;
 }
 
 size_t persistent_att_bytes(int group, int hd, int chunk_max) {
-    return ((size_t)group * hd + 5 * (size_t)hd + (size_t)group * chunk_max + (size_t)group * hd + 2 * (size_t)group) *
-           4;
+    (void)chunk_max;
+    // warp partials of a split, their (max, sum), the RoPE row
+    return ((size_t)kNW * group * hd + (size_t)kNW * group * 2 + (size_t)hd) * 4;
 }
 
-cudaError_t persistent_init(bool bf16, int hd, int hidden, int q_dim, int ffn) {
-    StepFn f = step_fn(bf16, hd, hidden, q_dim, ffn);
+cudaError_t persistent_init(bool bf16, int hd, int hidden, int q_dim, int ffn, int kvh) {
+    StepFn f = step_fn(bf16, hd, hidden, q_dim, ffn, kvh);
     if (!f) return cudaErrorInvalidValue;
     return cudaFuncSetAttribute(reinterpret_cast<const void *>(f), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kStepMaxSmem);
 }
 
-cudaError_t launch_persistent(bool bf16, int hd, int hidden, int q_dim, int ffn, const StepArgs &a, int grid,
+cudaError_t launch_persistent(bool bf16, int hd, int hidden, int q_dim, int ffn, int kvh, const StepArgs &a, int grid,
                               size_t smem, cudaStream_t s) {
-    StepFn f = step_fn(bf16, hd, hidden, q_dim, ffn);
+    StepFn f = step_fn(bf16, hd, hidden, q_dim, ffn, kvh);
     if (!f) return cudaErrorInvalidValue;
     cudaError_t e = cudaMemsetAsync(a.barrier, 0, sizeof(unsigned), s);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kGemvThreads);
+    cfg.blockDim = dim3(kStepThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute at[1];

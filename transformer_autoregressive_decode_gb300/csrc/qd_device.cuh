@@ -95,13 +95,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Bounded spins count SM cycles (clock64: cheap to read, unlike the global timer,
+// whose reads in a spinning warp held back the other warps of its scheduler).  A
+// limit of n ns is taken as 4n cycles: at least n ns at any SM clock up to 4 GHz.
+__device__ __forceinline__ unsigned long long cycles_now() { return (unsigned long long)clock64(); }
+__host__ __device__ constexpr unsigned long long wait_cycles(unsigned long long ns) { return 4ull * ns; }
+
 // Wait for phase `parity` of the barrier to complete; false after `limit_ns`.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
                                                   unsigned long long limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_timer_ns();
+    const unsigned long long t0 = cycles_now();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > limit_ns) return false;
+        if (cycles_now() - t0 > wait_cycles(limit_ns)) return false;
     }
     return true;
 }

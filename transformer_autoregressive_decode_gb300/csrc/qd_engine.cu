@@ -322,10 +322,6 @@ static StepArgs step_args(qd_model *m, bool with_head, bool taps) {
     a.rope_stage = m->stage_rpos;
     a.rope_stride = m->max_pos;
     a.x = m->x;
-    a.qkv = m->qkv;
-    a.act = m->act;
-    a.part_o = m->part_o;
-    a.part_ml = m->part_ml;
     a.in = StepInputArgs{m->embed, c.embed_rows, c.vocab, m->S(), m->embed_in, m->stage_tokens, m->stage_embeds,
                          m->emitted};
     a.with_head = with_head ? 1 : 0;
@@ -344,11 +340,21 @@ static StepArgs step_args(qd_model *m, bool with_head, bool taps) {
     a.barrier = m->barrier;
     a.st = m->st;
     if (m->tag_buf) {
-        a.x_t = m->tag_buf;
-        a.act_t = a.x_t + c.hidden;
-        a.qkv_t = a.act_t + c.ffn;
-        a.seq = reinterpret_cast<unsigned *>(a.qkv_t + m->q_dim() + 2 * m->kv_dim());
+        a.tg = m->tag_buf;
+        a.tg_stride = m->tg_stride;
+        a.tg_qkv = m->tg_qkv;
+        a.tg_po = m->tg_po;
+        a.tg_ml = m->tg_ml;
+        a.tg_att = m->tg_att;
+        a.tg_xc = m->tg_xc;
+        a.tg_xe = m->tg_xe;
+        a.tg_act = m->tg_act;
+        a.seq = reinterpret_cast<unsigned *>(m->tag_buf + m->tg_words);
+        a.emit_flag = a.seq + 1;
     }
+    a.off_kc = m->off_kc;
+    a.off_xres = m->off_xres;
+    a.off_ldev = m->off_ldev;
     return a;
 }
 
@@ -358,7 +364,7 @@ qd_status enqueue_step(qd_model *m, cudaStream_t s, bool with_head, bool taps) {
     const bool bf = m->bf16, pdl = m->use_pdl;
     const int h = c.hidden;
     if (m->persistent) {
-        CU(launch_persistent(bf, c.head_dim, h, m->q_dim(), c.ffn, step_args(m, with_head, taps), m->num_sms,
+        CU(launch_persistent(bf, c.head_dim, h, m->q_dim(), c.ffn, c.n_kv_heads, step_args(m, with_head, taps), m->num_sms,
                              m->smem_step, s));
         return QD_OK;
     }
@@ -535,8 +541,7 @@ static qd_status alloc_scratch(qd_model *m) {
     const size_t o_x = take(h * 4), o_qkv = take((size_t)(m->q_dim() + 2 * m->kv_dim()) * 4),
                  o_act = take((size_t)c.ffn * 4),
                  o_att = take((size_t)m->q_dim() * 4), o_y = take(h * 4),
-                 o_po = take((size_t)c.n_q_heads * kAttnMaxSplits * c.head_dim * 4),
-                 o_pml = take((size_t)c.n_q_heads * kAttnMaxSplits * 2 * 4), o_bar = take(128),
+                 o_bar = take(128),
                  o_ein = take(h * 4), o_se = take((size_t)m->max_pos * h * 4), o_pv = take((size_t)kHeadCandidates * 4),
                  o_pi = take((size_t)kHeadCandidates * 4), o_hc = take(64 * 4), o_stok = take((size_t)m->max_pos * 4),
                  o_ids = take((size_t)kIdsCap * 4), o_em = take((size_t)((c.vocab + 31) / 32) * 4),
@@ -549,8 +554,6 @@ static qd_status alloc_scratch(qd_model *m) {
     m->qkv = reinterpret_cast<float *>(B + o_qkv);
     m->act = reinterpret_cast<float *>(B + o_act);
     m->att = reinterpret_cast<float *>(B + o_att);
-    m->part_o = reinterpret_cast<float *>(B + o_po);
-    m->part_ml = reinterpret_cast<float *>(B + o_pml);
     m->barrier = reinterpret_cast<unsigned *>(B + o_bar);
     m->y = reinterpret_cast<float *>(B + o_y);
     m->embed_in = reinterpret_cast<float *>(B + o_ein);
@@ -623,13 +626,21 @@ static qd_status setup_persistent(qd_model *m) {
     const qd_config &c = m->cfg;
     m->persistent = false;
     if (std::getenv("QD_PER_PHASE")) return QD_OK;   // debug and profiling only
-    if (!persistent_supported(m->bf16, c.head_dim, c.hidden, m->q_dim(), c.ffn)) return QD_OK;
+    if (!persistent_supported(m->bf16, c.head_dim, c.hidden, m->q_dim(), c.ffn, c.n_kv_heads)) return QD_OK;
+    if (m->num_sms < kStepMinSms) return QD_OK;
     const int G = c.n_q_heads / c.n_kv_heads;
     if (c.n_kv_heads * kAttnMaxSplits > m->num_sms) return QD_OK;
-    if (c.n_layers > 50) return QD_OK;              // phase tags: 1 + 5 * layer + phase < 256
+    if (G > kStepGroupMax) return QD_OK;
     if (m->chunk_max * c.head_dim * (int)m->esize > kSlotBytes) return QD_OK;
     // rows of any phase held by one CTA, times the warps per row
     auto rmax = [&](int rows, int unit) { return (rows / unit + m->num_sms - 1) / m->num_sms * unit; };
+    if (rmax(m->q_dim() + 2 * m->kv_dim(), 1) > kStepRowsMax || rmax(c.hidden, 1) > kStepRowsMax ||
+        rmax(2 * c.ffn, 2) > kStepRowsMax)
+        return QD_OK;
+    // a ring stage holds at most 32 rows of every phase (one transposing butterfly)
+    if (kSlotBytes / (c.hidden * (int)m->esize) > 32 || kSlotBytes / (m->q_dim() * (int)m->esize) > 32 ||
+        kSlotBytes / (c.ffn * (int)m->esize) > 32)
+        return QD_OK;
     const int res_words = std::max({rmax(m->q_dim() + 2 * m->kv_dim(), 1) * m->rs_h, rmax(c.hidden, 1) * m->rs_q,
                                     rmax(2 * c.ffn, 2) * m->rs_h, rmax(c.hidden, 1) * m->rs_f,
                                     rmax(c.vocab, 1) * m->rs_h});
@@ -650,12 +661,14 @@ static qd_status setup_persistent(qd_model *m) {
         tail += (size_t)res_words * 4 + 16;                            // row partial sums
         tail += persistent_att_bytes(G, c.head_dim, m->chunk_max) + 16;
         tail += ((size_t)head_rows / 32 + 2) * 4 + 16;                 // emitted words of the head rows
-        tail += (size_t)std::max({m->q_dim(), c.hidden, c.ffn}) * 4 + 16;  // phase input vector
+        tail += (size_t)c.hidden * 4 + 16;                             // the head's input vector
+        tail += ((size_t)2 * kConsumerWarps * kStepRowsMax + 2 * kConsumerWarps) * 4 + 16;   // row partials
+        tail += (size_t)kStepRowsMax * 4 + 16;                         // residual rows
+        tail += sizeof(LayerDev) * (size_t)c.n_layers + 16;            // layer table
     }
     const size_t max_smem = kStepMaxSmem;
-    int nst = (int)((max_smem - tail) / kSlotBytes);
-    nst = std::min(nst, 6);
-    if (nst < 2) return QD_OK;
+    const int nst = kStepRingStages;
+    if (tail + (size_t)nst * kSlotBytes > max_smem) return QD_OK;
     off = 0;
     take((size_t)nst * kSlotBytes, 1024);
     m->off_full = take((size_t)2 * nst * 8, 16);
@@ -664,11 +677,14 @@ static qd_status setup_persistent(qd_model *m) {
     m->off_res = take((size_t)res_words * 4, 16);
     m->off_att = take(persistent_att_bytes(G, c.head_dim, m->chunk_max), 16);
     m->off_emw = take(((size_t)head_rows / 32 + 2) * 4, 16);
-    m->off_xin = take((size_t)std::max({m->q_dim(), c.hidden, c.ffn}) * 4, 16);
+    m->off_xin = take((size_t)c.hidden * 4, 16);
+    m->off_kc = take(((size_t)2 * kConsumerWarps * kStepRowsMax + 2 * kConsumerWarps) * 4, 16);
+    m->off_xres = take((size_t)kStepRowsMax * 4, 16);
+    m->off_ldev = take(sizeof(LayerDev) * (size_t)c.n_layers, 16);
     m->smem_step = align_up(off, 16);
     m->nst_step = nst;
     if (m->smem_step > max_smem) return QD_OK;
-    CU(persistent_init(m->bf16, c.head_dim, c.hidden, m->q_dim(), c.ffn));
+    CU(persistent_init(m->bf16, c.head_dim, c.hidden, m->q_dim(), c.ffn, c.n_kv_heads));
     // layer table
     std::vector<LayerDev> host(c.n_layers);
     for (int l = 0; l < c.n_layers; ++l) {
@@ -678,12 +694,24 @@ static qd_status setup_persistent(qd_model *m) {
     }
     CU(cudaMalloc(&m->d_layers, sizeof(LayerDev) * c.n_layers));
     CU(cudaMemcpy(m->d_layers, host.data(), sizeof(LayerDev) * c.n_layers, cudaMemcpyHostToDevice));
-    // tagged vectors (all tags 0: never a launch's) and the sequence number, from 1
-    const size_t words = (size_t)c.hidden + c.ffn + m->q_dim() + 2 * m->kv_dim() + 1;
-    CU(cudaMalloc(&m->tag_buf, words * 8));
-    CU(cudaMemset(m->tag_buf, 0, words * 8));
+    // tagged words of every layer (all zero: no launch has sequence number 0), then the
+    // sequence number (from 1) and the emitted-set flag; pieces start on 256-byte lines
+    auto words32 = [](size_t n) { return (int)((n + 31) / 32 * 32); };
+    int o = 0;
+    m->tg_qkv = o; o += words32((size_t)m->q_dim() + 2 * m->kv_dim());
+    m->tg_po = o;  o += words32((size_t)c.n_kv_heads * kAttnMaxSplits * G * c.head_dim);
+    m->tg_ml = o;  o += words32((size_t)c.n_kv_heads * kAttnMaxSplits * G * 2);
+    m->tg_att = o; o += words32((size_t)m->q_dim());
+    m->tg_xc = o;  o += words32((size_t)c.hidden);
+    m->tg_xe = o;  o += words32((size_t)c.hidden);
+    m->tg_act = o; o += words32((size_t)c.ffn);
+    m->tg_stride = o;
+    m->tg_words = (size_t)o * c.n_layers;
+    const size_t bytes = (m->tg_words + 32) * 8;
+    CU(cudaMalloc(&m->tag_buf, bytes));
+    CU(cudaMemset(m->tag_buf, 0, bytes));
     const unsigned one = 1;
-    CU(cudaMemcpy(m->tag_buf + words - 1, &one, sizeof(one), cudaMemcpyHostToDevice));
+    CU(cudaMemcpy(m->tag_buf + m->tg_words, &one, sizeof(one), cudaMemcpyHostToDevice));
     m->persistent = true;
     return QD_OK;
 }

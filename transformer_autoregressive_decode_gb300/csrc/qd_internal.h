@@ -126,9 +126,7 @@ struct StepArgs {
     int mrope_h;                   // interleaved multimodal RoPE: the h (= w) section size, 0: plain
     const int *rope_stage;         // [3][rope_stride] staged prompt positions (t, h, w)
     int rope_stride;
-    float *x, *qkv, *act;
-    float *part_o;                 // [qh][kAttnMaxSplits][hd]
-    float *part_ml;                // [qh][kAttnMaxSplits][2]
+    float *x;                      // the residual stream (plain copy, written by its row owners)
     StepInputArgs in;
     int with_head;
     const void *const *heads;
@@ -141,10 +139,28 @@ struct StepArgs {
     int ids_cap;
     float *tap_hidden, *tap_logits;
     unsigned *barrier;             // zeroed before every launch
-    uint64_t *x_t, *act_t, *qkv_t; // tagged copies of the gathered vectors: [hidden], [ffn], [q + 2 kv]
-    unsigned *seq;                 // launch sequence number (starts at 1, never reset)
+    // Tagged words {launch sequence number, value}, one block of tg_stride words per
+    // layer; word offsets within a block: qkv [q + 2 kv], attention partials
+    // [kvh][kAttnMaxSplits][G * hd] and their (max, sum) [kvh][kAttnMaxSplits][G][2],
+    // merged attention output [q], x after the output projection [hidden], x after the
+    // down projection [hidden], act [ffn]
+    uint64_t *tg;
+    int tg_stride, tg_qkv, tg_po, tg_ml, tg_att, tg_xc, tg_xe, tg_act;
+    unsigned *seq;                 // launch sequence number (starts at 1, never 0)
+    unsigned *emit_flag;           // CTA 0 stores the launch's seq (release) once the step's
+                                   // token is in the emitted set
+    int off_kc, off_xres, off_ldev;// shared memory: row-partial tables, residual rows, layer table
     DevState *st;
 };
+
+// Rows of one GEMV phase a CTA of the persistent step may hold (its partial-sum
+// tables and residual rows are sized by it), the largest q-heads-per-kv-head ratio it
+// handles, its ring stages and the fewest SMs it runs on; other shapes and GPUs use
+// the per-phase kernels.
+constexpr int kStepRowsMax = 64;
+constexpr int kStepRingStages = 6;
+constexpr int kStepMinSms = 148;
+constexpr int kStepGroupMax = 2;
 
 // Dynamic shared memory ceiling of the persistent step kernel.  The kernel's
 // max-dynamic-smem attribute is set to this once for every instantiation, so
@@ -153,9 +169,9 @@ constexpr int kStepMaxSmem = 227 * 1024;
 
 // Persistent kernel for (dtype, head_dim, hidden, q_dim, ffn): false if there is no
 // instantiation for the shape (the per-phase kernels are used then).
-bool persistent_supported(bool bf16, int hd, int hidden, int q_dim, int ffn);
-cudaError_t persistent_init(bool bf16, int hd, int hidden, int q_dim, int ffn);
-cudaError_t launch_persistent(bool bf16, int hd, int hidden, int q_dim, int ffn, const StepArgs &a, int grid,
+bool persistent_supported(bool bf16, int hd, int hidden, int q_dim, int ffn, int kvh);
+cudaError_t persistent_init(bool bf16, int hd, int hidden, int q_dim, int ffn, int kvh);
+cudaError_t launch_persistent(bool bf16, int hd, int hidden, int q_dim, int ffn, int kvh, const StepArgs &a, int grid,
                               size_t smem, cudaStream_t s);
 size_t persistent_att_bytes(int group, int hd, int chunk_max);
 

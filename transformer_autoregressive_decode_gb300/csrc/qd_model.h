@@ -78,11 +78,15 @@ struct qd_model {
     qd_batch *pf_batch = nullptr;
     cudaEvent_t pf_ev[2] = {nullptr, nullptr};
     qd::LayerDev *d_layers = nullptr;
-    uint64_t *tag_buf = nullptr;   // persistent step: tagged x, act, qkv, then the launch sequence number
+    // persistent step: the tagged words of every layer, then the launch sequence number
+    // and the emitted-set flag
+    uint64_t *tag_buf = nullptr;
+    int tg_stride = 0, tg_qkv = 0, tg_po = 0, tg_ml = 0, tg_att = 0, tg_xc = 0, tg_xe = 0, tg_act = 0;
+    size_t tg_words = 0;
     unsigned *barrier = nullptr;
-    float *part_o = nullptr, *part_ml = nullptr;
     size_t smem_step = 0;
     int nst_step = 0, off_full = 0, off_gsm = 0, off_misc = 0, off_res = 0, off_att = 0, off_emw = 0, off_xin = 0;
+    int off_kc = 0, off_xres = 0, off_ldev = 0;
 
     std::vector<qd_frame *> frames;          // frame generators bound to this handle
     bool use_graphs = true;
