@@ -683,9 +683,9 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
 
     // ---------------- consumers
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kConsumerRegs) : "memory");
-    float *wo = reinterpret_cast<float *>(smem + a.off_att);   // [kNW][G][HD] warp partials of the split
-    float *wml = wo + (size_t)kNW * G * HD;                    // [kNW][G][2]
-    float *rc = wml + (size_t)kNW * G * 2;                     // [HD]: cos then sin of each frequency
+    float *wo = reinterpret_cast<float *>(smem + a.off_att);   // [kNW][HD] warp partials of the split
+    float *wml = wo + (size_t)kNW * HD;                        // [kNW][2]
+    float *rc = wml + (size_t)kNW * 2;                         // [HD]: cos then sin of each frequency
     if (has_item) {
         // rotary cos / sin at the step's rotary position (per stream from the staged
         // prompt positions for a multimodal prompt row); constant for the launch
@@ -730,93 +730,75 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
                 // ---- B: attention of this CTA's (group, split), then its share of the merge
                 bool okb = true;
                 do {
-            // ---- B: attention of this CTA's (group, split), then its share of the merge
+            // kNW / G warps per q head of the group, each over a slice of the split's
+            // positions; the warps of a head are merged, then the splits.
             if (has_item) {
-                const int pw = (n_att + kNW - 1) / kNW;     // positions per warp
-                const int jw0 = warp * pw;
+                constexpr int WPH = kNW / G;
+                const int hq = warp / WPH, ws = warp % WPH;
+                const int pw = (n_att + WPH - 1) / WPH;     // positions per warp
+                const int jw0 = ws * pw;
                 const int nwp = n_att - jw0 < pw ? (n_att - jw0 > 0 ? n_att - jw0 : 0) : pw;
                 const int jp = p - j0;                      // the new position within the split
                 const bool owner = n_old < n_att && jp >= jw0 && jp < jw0 + nwp;
-                // this lane's columns of the group's q heads, and (owner) of k and v, in one
-                // batch of polls
-                const uint64_t *qb = T + a.tg_qkv + (size_t)ig * G * HD + lane * EH;
+                // this lane's columns of q head hq, and (owner) of k and v, in one batch
+                const uint64_t *qb = T + a.tg_qkv + (size_t)(ig * G + hq) * HD + lane * EH;
                 const uint64_t *kb = T + a.tg_qkv + q_dim + (size_t)ig * HD + lane * EH;
-                const int nq = G * EH;
-                float wv[(kGMax + 2) * EH];
-                bool okw = poll_batch<(kGMax + 2) * EH>(nq + (owner ? 2 * EH : 0), seq,
-                                                        [&](int i) {
-                                                            return i < nq ? qb + (size_t)(i / EH) * HD + i % EH
-                                                                          : kb + (size_t)((i - nq) / EH) * kv_dim +
-                                                                                (i - nq) % EH;
-                                                        },
-                                                        wv);
+                float wv[3 * EH];
+                bool okw = poll_batch<3 * EH>(owner ? 3 * EH : EH, seq,
+                                              [&](int i) {
+                                                  return i < EH ? qb + i
+                                                                : kb + (size_t)((i - EH) / EH) * kv_dim + (i - EH) % EH;
+                                              },
+                                              wv);
                 okw = __all_sync(0xffffffffu, okw);
-                float q[kGMax][EH], kr[EH], vr[EH];
-    #pragma unroll
-                for (int h = 0; h < kGMax; ++h)
-    #pragma unroll
-                    for (int e = 0; e < EH; ++e) q[h][e] = wv[h * EH + e];
-    #pragma unroll
+                float q[1][EH], kr[EH], vr[EH];
+#pragma unroll
                 for (int e = 0; e < EH; ++e) {
-                    kr[e] = 0.f;
-                    vr[e] = 0.f;
-    #pragma unroll
-                    for (int h = 0; h <= kGMax; ++h)
-                        if (h == G) {
-                            kr[e] = wv[h * EH + e];
-                            vr[e] = wv[(h + 1) * EH + e];
-                        }
+                    q[0][e] = wv[e];
+                    kr[e] = wv[EH + e];
+                    vr[e] = wv[2 * EH + e];
                 }
                 if (Ld.q_norm) {
-    #pragma unroll
-                    for (int h = 0; h < kGMax; ++h)
-                        if (h < G) head_norm<EH>(q[h], gq, HD, a.eps);
+                    head_norm<EH>(q[0], gq, HD, a.eps);
                     if (owner) head_norm<EH>(kr, gk, HD, a.eps);
                 }
                 float rcs[EH], rsn[EH];
-    #pragma unroll
+#pragma unroll
                 for (int e = 0; e < EH; ++e) {
                     rcs[e] = rc[(lane & 15) * EH + e];
                     rsn[e] = rc[HALF + (lane & 15) * EH + e];
                 }
-    #pragma unroll
-                for (int h = 0; h < kGMax; ++h)
-                    if (h < G) rope_lane<EH>(q[h], rcs, rsn, lane);
+                rope_lane<EH>(q[0], rcs, rsn, lane);
                 if (owner) {
-                    // append the new row to the cache (cache type), and use the rounded row
+                    // the new row in the cache type; head 0's owner appends it to the cache
                     rope_lane<EH>(kr, rcs, rsn, lane);
-    #pragma unroll
+#pragma unroll
                     for (int e = 0; e < EH; ++e) {
                         kr[e] = round_to<KT>(kr[e]);
                         vr[e] = round_to<KT>(vr[e]);
                     }
-                    KT *kw = reinterpret_cast<KT *>(reinterpret_cast<uint8_t *>(a.kv) + (size_t)l * layer_kv) +
-                             ((size_t)ig * a.S + p) * HD + lane * EH;
-                    KT *vw = reinterpret_cast<KT *>(reinterpret_cast<uint8_t *>(a.kv) + (size_t)l * layer_kv +
-                                                    layer_kv / 2) +
-                             ((size_t)ig * a.S + p) * HD + lane * EH;
-                    store_row_elems<KT, EH>(kw, kr);
-                    store_row_elems<KT, EH>(vw, vr);
-                    fence_proxy_async_global();   // later bulk copies read the row
+                    if (hq == 0) {
+                        const size_t row = ((size_t)ig * a.S + p) * HD + lane * EH;
+                        KT *kw = reinterpret_cast<KT *>(reinterpret_cast<uint8_t *>(a.kv) + (size_t)l * layer_kv) + row;
+                        KT *vw = reinterpret_cast<KT *>(reinterpret_cast<uint8_t *>(a.kv) + (size_t)l * layer_kv +
+                                                        layer_kv / 2) + row;
+                        store_row_elems<KT, EH>(kw, kr);
+                        store_row_elems<KT, EH>(vw, vr);
+                    }
                 }
                 const uint8_t *kslot = okw ? stage_get(R, sidx) : nullptr;
                 const uint8_t *vslot = kslot ? stage_get(R, sidx + 1) : nullptr;
                 okw = __all_sync(0xffffffffu, vslot != nullptr);
-                float o[kGMax][EH], mh[kGMax], lh[kGMax];
                 if (okw) {
-                    const KT *Ks = reinterpret_cast<const KT *>(kslot);
-                    const KT *Vs = reinterpret_cast<const KT *>(vslot);
-                    warp_attention<KT, HD, G>(Ks, Vs, q, jw0, nwp, jp, kr, vr, a.scale, o, mh, lh);
-    #pragma unroll
-                    for (int h = 0; h < kGMax; ++h) {
-                        if (h >= G) continue;
-                        float *dst = wo + ((size_t)warp * G + h) * HD + lane * EH;
-    #pragma unroll
-                        for (int e = 0; e < EH; ++e) dst[e] = o[h][e];
-                        if (lane == 0) {
-                            wml[((size_t)warp * G + h) * 2] = mh[h];
-                            wml[((size_t)warp * G + h) * 2 + 1] = lh[h];
-                        }
+                    float o[1][EH], mh[1], lh[1];
+                    warp_attention<KT, HD, 1>(reinterpret_cast<const KT *>(kslot), reinterpret_cast<const KT *>(vslot), q,
+                                              jw0, nwp, jp, kr, vr, a.scale, o, mh, lh);
+                    float *dst = wo + (size_t)warp * HD + lane * EH;
+#pragma unroll
+                    for (int e = 0; e < EH; ++e) dst[e] = o[0][e];
+                    if (lane == 0) {
+                        wml[warp * 2] = mh[0];
+                        wml[warp * 2 + 1] = lh[0];
                     }
                     stage_put(R, sidx, lane);
                     stage_put(R, sidx + 1, lane);
@@ -824,24 +806,24 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
                 sidx += 2;
                 ok = !named_sync_or(1, kNC, !okw);
                 if (!ok) { okb = false; break; }
-                // the split's partial, the warps merged in warp order: its normalised output
-                // o / l and, per head, its log-sum-exp m + log(l)
+                // the split's partial, the warps of each head merged in order: its
+                // normalised output o / l and, per head, its log-sum-exp m + log(l)
                 const int GD = G * HD;
                 uint64_t *Tpo = T + a.tg_po + ((size_t)ig * kAttnMaxSplits + is) * GD;
                 uint64_t *Tml = T + a.tg_ml + ((size_t)ig * kAttnMaxSplits + is) * G * 2;
                 for (int t = tid; t < GD; t += kNC) {
                     const int h = t / HD, d = t % HD;
                     float M = -INFINITY;
-    #pragma unroll
-                    for (int w = 0; w < kNW; ++w) M = fmaxf(M, wml[((size_t)w * G + h) * 2]);
+#pragma unroll 1
+                    for (int w = h * WPH; w < (h + 1) * WPH; ++w) M = fmaxf(M, wml[w * 2]);
                     float den = 0.f, num = 0.f;
-    #pragma unroll
-                    for (int w = 0; w < kNW; ++w) {
-                        const float mw = wml[((size_t)w * G + h) * 2];
+#pragma unroll 1
+                    for (int w = h * WPH; w < (h + 1) * WPH; ++w) {
+                        const float mw = wml[w * 2];
                         if (mw != -INFINITY) {
                             const float f = expf(mw - M);
-                            den = fmaf(f, wml[((size_t)w * G + h) * 2 + 1], den);
-                            num = fmaf(f, wo[((size_t)w * G + h) * HD + d], num);
+                            den = fmaf(f, wml[w * 2 + 1], den);
+                            num = fmaf(f, wo[(size_t)w * HD + d], num);
                         }
                     }
                     st_tag(Tpo + t, num / den, seq);
@@ -1235,8 +1217,9 @@ bool persistent_supported(bool bf16, int hd, int hidden, int q_dim, int ffn, int
 
 size_t persistent_att_bytes(int group, int hd, int chunk_max) {
     (void)chunk_max;
+    (void)group;
     // warp partials of a split, their (max, sum), the RoPE row
-    return ((size_t)kNW * group * hd + (size_t)kNW * group * 2 + (size_t)hd) * 4;
+    return ((size_t)kNW * hd + (size_t)kNW * 2 + (size_t)hd) * 4;
 }
 
 cudaError_t persistent_init(bool bf16, int hd, int hidden, int q_dim, int ffn, int kvh) {
