@@ -1,15 +1,22 @@
 #!/usr/bin/env python3
 """Decode throughput of the GB300 decode path.
 
-Workload (default ``asr``): the ASR decoder (8 layers, hidden 512, 8 q / 8 kv heads,
-head_dim 64, FFN 2048, vocab 151936, bf16 weights, EOS masked off) on seeded
-synthetic weights.  One trajectory is: reset, prefill 110 N(0,1) embeddings, then
-290 greedy decode steps to KV length 400 with the bucket migrations 128 -> 256 ->
-512 on the way.  A benchmark "step" is one decode token; the timed region runs
-whole trajectories back to back (prefill included) until K tokens are produced.
+Default (``--workload all``): one JSON line whose headline is the Talker decoder
+(28 layers, hidden 1024, 16 q / 8 kv heads x 128, QK-norm, FFN 3072, vocab 3072,
+repetition penalty 1.05, bf16 weights and KV cache) on seeded synthetic weights.  A
+trajectory is reset, prefill 64 N(0,1) embeddings, then 600 greedy decode steps with
+the bucket migrations 128 -> 256 -> 512 -> 1024.  A benchmark "step" is one decode
+token; the timed region continues the trajectory in progress (graph replays of the
+step) and restarts a trajectory (reset + prefill, timed with the tokens) when one
+ends.  The same line carries, as keys ``asr``, ``frames`` and ``batch``, the ASR
+decoder (8 layers, hidden 512, vocab 151936, EOS masked), the two-level frame loop
+(Talker + 15-code predictor, 150 frames) and the batched 64-stream Talker decode, each
+with its own value, roofline, CPU baseline and end-to-end figure.  ``--workload``
+selects one of them alone.
 
-Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle instead
-(on the host cores, a bounded sample of the same workload).
+``--impl reference`` times the CPU oracle instead (on the host cores, a bounded
+sample of the headline's workload).  Under torchrun every rank runs the decoders as
+replicas; the batched decode partitions its 64 streams over the ranks.
 """
 from __future__ import annotations
 
@@ -119,6 +126,35 @@ def _dist():
     return ws, rank, local
 
 
+def _init_dist():
+    """One process per GPU: (world size, rank, local rank, device); NCCL process group
+    when launched by torchrun with more than one rank."""
+    import torch
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        if not dist.is_initialized():
+            dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return ws, rank, local, torch.cuda.current_device()
+
+
+def _close_dist(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+def stream_shard(n_streams: int, rank: int, ws: int):
+    """The streams [lo, hi) of the batched workload that rank `rank` of `ws` decodes:
+    contiguous, disjoint, covering all of them (streams are independent decoders, so
+    the ranks exchange nothing)."""
+    return n_streams * rank // ws, n_streams * (rank + 1) // ws
+
+
 def max_over_ranks(ms: float, ws: int) -> float:
     """The slowest rank's time of the timed region: every rank takes part (a MAX
     all-reduce on the process group's device; CPU tensors under gloo); one rank: ms."""
@@ -166,14 +202,15 @@ def reference_arm(args):
     ws, rank, _ = _dist()
     if rank != 0:
         return
-    shape, desc = _workload(args.workload)
+    wl = "talker" if args.workload == "all" else args.workload
+    shape, desc = _workload(wl)
     run_oracle_sample(shape, max(1, min(args.warmup, 3)), budget_s=5.0)  # warm-up (untimed)
     tps, n, dt, cores = run_oracle_sample(shape, args.steps, budget_s=60.0)
-    sample = (f"prefill {shape.prefill} untimed, then {n} greedy decode tokens of the {args.workload} workload "
+    sample = (f"prefill {shape.prefill} untimed, then {n} greedy decode tokens of the {wl} workload "
               f"({dt:.1f} s)")
     line = {"impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": ws,
             "steps": n, "warmup": args.warmup, "ms_per_step": 1e3 * dt / max(n, 1), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if shape.bf16 else "f32", "data": "synthetic",
             "config": {"workload": desc},
             "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -183,26 +220,20 @@ def reference_arm(args):
 # ------------------------------------------------------------------------------ GPU arm
 
 
-def gpu_arm(args):
+def gpu_line(args, workload, ctx):
+    """The decode workload `workload` (asr, talker, tiny) on this rank: its JSON line
+    (rank 0) or None."""
     import numpy as np
     import torch
 
-    ws, rank, local = _dist()
-    if ws > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    else:
-        torch.cuda.set_device(0)
-    dev = torch.cuda.current_device()
-
+    ws, rank, local, dev = ctx
     import workloads as W
     import __graft_entry__
     __graft_entry__.build_library()
     import transformer_autoregressive_decode_gb300 as qd
     from transformer_autoregressive_decode_gb300.torch_io import config_from_shape, upload
 
-    shape, desc = _workload(args.workload)
+    shape, desc = _workload(workload)
     hbm_peak, _, peak_src = _peaks()
     w_np = W.model_weights(shape)
     e_np = W.prefill_embeds(shape)
@@ -215,14 +246,16 @@ def gpu_arm(args):
     stream = torch.cuda.current_stream()
 
     def tokens(n, events=None):
-        """Produce n decode tokens: whole trajectories (reset + prefill + greedy).
-        With ``events``, each greedy segment is bracketed by a pair of CUDA events
-        (used to time the decode steps without the prefill)."""
+        """Produce n decode tokens, continuing the trajectory in progress: a trajectory
+        is reset + prefill + greedy decode to its end.  With ``events``, each greedy
+        segment is bracketed by a pair of CUDA events (used to time the decode steps
+        without the prefill)."""
         done = 0
         pos_state = tokens.pos
         while done < n:
             if pos_state == 0 or pos_state >= traj:
                 qd.qd_reset(h)
+                tokens.prefills += 1
                 first = qd.qd_prefill(h, embeds=e_dev)
                 if events is not None:
                     events.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True), 1))
@@ -245,6 +278,7 @@ def gpu_arm(args):
         tokens.pos = pos_state
 
     tokens.pos = 0
+    tokens.prefills = 0
     W_ = max(3, args.warmup)
     tokens(W_)
     torch.cuda.synchronize()
@@ -255,8 +289,11 @@ def gpu_arm(args):
         torch.cuda.synchronize()
 
     k0, per_step = qd.qd_get_launch_count(h)
+    # clocks sampled from the timed region through the long decode-only pass below
     clocks = Clocks(dev if ws == 1 else local)
     barrier()
+    pos0 = tokens.pos
+    pf0 = tokens.prefills
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     torch.cuda.nvtx.range_push("timed")
@@ -264,7 +301,7 @@ def gpu_arm(args):
     torch.cuda.nvtx.range_pop()
     ev1.record(stream)
     barrier()
-    clk = clocks.stop()
+    timed_prefills = tokens.prefills - pf0
     ms = ev0.elapsed_time(ev1)
     k1, _ = qd.qd_get_launch_count(h)
     ms = max_over_ranks(ms, ws)
@@ -279,6 +316,7 @@ def gpu_arm(args):
     dec_ms = sum(a.elapsed_time(b) for a, b, _ in evs)
     dec_n = sum(k for _, _, k in evs)
     dec_step_us = 1e3 * dec_ms / dec_n
+    clk = clocks.stop()
 
     # the same decode steps with on-device sampling at the wrapper's default generation
     # settings ("qwen3-tts-hip OPTIMIZATION_LOG", generation-defaults entry: top-k 50,
@@ -309,7 +347,7 @@ def gpu_arm(args):
     kbytes = shape.step_bytes(L_timed)
     achieved = kbytes / (kms / 1e3) / 1e9
     traffic, traffic_note = None, "no ncu capture for this workload and kernel build"
-    tr = _STEP_TRAFFIC.get(args.workload)
+    tr = _STEP_TRAFFIC.get(workload)
     if tr and tr["digest"] == _step_digest():
         # scaled from the captured length to the timed one by the K/V rows read
         traffic = tr["bytes"] + (L_timed - tr["L"]) * shape.kv_bytes_per_position()
@@ -359,7 +397,7 @@ def gpu_arm(args):
     # fp32 FMA rate of 152 SMs x 128 lanes x 2 flops at the sampled SM clock), each launch
     # after a 256 MB write that flushes L2
     codec = None
-    if args.workload == "asr":
+    if workload == "asr":
         flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
 
         def timed(fn, reps=6):
@@ -431,7 +469,7 @@ def gpu_arm(args):
     # a prompt with distinct rotary streams (text, a 6 x 8 image grid, text) beside the
     # plain prompt
     mrope = None
-    if args.workload == "talker":
+    if workload == "talker":
         ms_shape = W.scaled(shape, name="talker_mrope", mrope_section=(24, 20, 20))
         dev_w = upload(w_np)
         hm = qd.qd_create(dev_w, config_from_shape(ms_shape))
@@ -459,15 +497,23 @@ def gpu_arm(args):
                          "text + 6 x 8 image grid + text positions"}
         qd.qd_destroy(hm)
     if rank != 0:
-        return
+        return None
+    if timed_prefills:
+        timed = (f"{args.steps} decode tokens continuing the trajectory at position {pos0} of {traj} "
+                 f"(graph replays of the step); {timed_prefills} trajectory restart(s) inside, each a reset and "
+                 f"a {shape.prefill}-position prefill, timed with the tokens")
+    else:
+        timed = (f"{args.steps} decode tokens continuing the trajectory at position {pos0} of {traj} "
+                 f"(graph replays of the step; no prefill inside the timed region)")
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": W_, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic: seeded N(0,0.02) bf16 weights, 1+N(0,0.1) norm gammas, N(0,1) prompt embeddings",
-        "config": {"workload": desc, "storage": "bf16 weights and KV cache, fp32 activations and accumulation",
-                   "timed": f"{args.steps} decode tokens as whole trajectories (reset + prefill {shape.prefill} "
-                            f"+ greedy), prefill time included",
+        "vs_baseline": None, "dtype": "bf16" if shape.bf16 else "f32",
+        "data": "synthetic: seeded N(0,0.02) " + ("bf16" if shape.bf16 else "fp32") +
+                " weights, 1+N(0,0.1) norm gammas, N(0,1) prompt embeddings",
+        "config": {"workload": desc, "storage": ("bf16 weights and KV cache" if shape.bf16 else
+                                                 "fp32 weights and KV cache") + ", fp32 activations and accumulation",
+                   "timed": timed,
                    "l2": f"inputs larger than L2: {shape.weight_bytes_per_step() / 1e6:.1f} MB of weights per step",
                    "parallelism": "replicas" if ws > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
@@ -492,9 +538,15 @@ def gpu_arm(args):
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(k1 - k0), "kernels_per_decode_step": per_step,
         "clocks": clk,
     }
-    print(json.dumps(line), flush=True)
-    if ws > 1:
-        torch.distributed.destroy_process_group()
+    return line
+
+
+def gpu_arm(args):
+    ctx = _init_dist()
+    line = gpu_line(args, args.workload, ctx)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    _close_dist(ctx[0])
 
 
 # ------------------------------------------------------------------------------ frame workload
@@ -549,19 +601,12 @@ def frames_reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
-def frames_arm(args):
+def frames_line(args, ctx):
+    """The two-level frame workload on this rank: its JSON line (rank 0) or None."""
     import numpy as np
     import torch
 
-    ws, rank, local = _dist()
-    if ws > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    else:
-        torch.cuda.set_device(0)
-    dev = torch.cuda.current_device()
-
+    ws, rank, local, dev = ctx
     import workloads as W
     import __graft_entry__
     __graft_entry__.build_library()
@@ -680,11 +725,11 @@ def frames_arm(args):
     qd.qd_destroy(C)
     qd.qd_destroy(T)
     if rank != 0:
-        return
+        return None
     line = {
         "metric": METRIC, "value": value, "unit": "frames/s", "n_gpus": ws, "steps": args.steps,
         "warmup": W_, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32",
+        "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: seeded N(0,0.02) bf16 weights and code tables, 1+N(0,0.1) norm gammas, N(0,1) prompt "
                 "and text embeddings",
         "config": {"workload": FRAMES_DESC, "storage": "bf16 weights, tables and KV cache, fp32 activations",
@@ -707,9 +752,15 @@ def frames_arm(args):
                               "trajectory (149 Talker steps, 150 x 15 predictor weight passes)"},
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(kt1 - kt0 + kc1 - kc0), "clocks": clk,
     }
-    print(json.dumps(line), flush=True)
-    if ws > 1:
-        torch.distributed.destroy_process_group()
+    return line
+
+
+def frames_arm(args):
+    ctx = _init_dist()
+    line = frames_line(args, ctx)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    _close_dist(ctx[0])
 
 
 # ------------------------------------------------------------------------------ batched workload
@@ -759,19 +810,14 @@ def batch_reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
-def batch_arm(args):
+def batch_line(args, ctx):
+    """The batched workload on this rank: its JSON line (rank 0) or None.  With more
+    than one rank the 64 streams are partitioned: rank r decodes streams
+    stream_shard(64, r, N) over a full weight replica, with no exchange."""
     import numpy as np
     import torch
 
-    ws, rank, local = _dist()
-    if ws > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    else:
-        torch.cuda.set_device(0)
-    dev = torch.cuda.current_device()
-
+    ws, rank, local, dev = ctx
     import workloads as W
     import __graft_entry__
     __graft_entry__.build_library()
@@ -782,13 +828,15 @@ def batch_arm(args):
     if args.layers:
         # profiling case only: the same streams, lengths and per-layer kernels, fewer layers
         s = W.scaled(W.TALKER, n_layers=args.layers, name=f"talker{args.layers}")
-    B, smax, traj = W.BATCH_STREAMS, W.BATCH_SMAX, W.BATCH_STEPS
+    B_all, smax, traj = W.BATCH_STREAMS, W.BATCH_SMAX, W.BATCH_STEPS
+    lo, hi = stream_shard(B_all, rank, ws)       # this rank's streams (all of them on one GPU)
+    B = hi - lo
     hbm_peak, bf16_peak, peak_src = _peaks()
     h = qd.qd_create(upload(W.model_weights(s)), config_from_shape(s))
     bh = qd.qd_batch_create(h, B, smax)
-    lens = [int(v) for v in W.batch_initial_lengths()]
-    toks = [int(v) for v in W.batch_first_tokens(B, s.vocab)]
-    kv_dev = [to_device(W.batch_stream_kv(s, b, lens[b])) for b in range(B)]   # kept for restarts
+    lens = [int(v) for v in W.batch_initial_lengths()][lo:hi]
+    toks = [int(v) for v in W.batch_first_tokens(B_all, s.vocab)][lo:hi]
+    kv_dev = [to_device(W.batch_stream_kv(s, lo + b, lens[b])) for b in range(B)]   # kept for restarts
     ids = torch.empty((traj, B), dtype=torch.int32, device="cuda")
     stream = torch.cuda.current_stream()
 
@@ -839,7 +887,7 @@ def batch_arm(args):
     ms = ev0.elapsed_time(ev1)
     k1, _ = qd.qd_batch_get_launch_count(bh)
     ms = max_over_ranks(ms, ws)
-    value = whole_job_rate(B * args.steps, ws, ms)
+    value = B_all * args.steps / (ms / 1e3)      # every stream of the workload over the slowest rank
     step_ms = ms / args.steps
 
     # algorithmic bytes: weights once per step + every stream's K/V over its attended
@@ -866,6 +914,7 @@ def batch_arm(args):
 
     # prefill of the workload: 8 prompt streams x 512 N(0,1) positions, timed alone
     ns_p, n_p = W.BATCH_PREFILL
+    ns_p = min(ns_p, B)                         # this rank's share of the prompt streams fits its streams
     prompts = torch.from_numpy(np.stack([W.normal(f"batched/prompt/{i}", (n_p, s.hidden), 0)
                                          for i in range(ns_p)])).cuda()
     first = torch.empty(ns_p, dtype=torch.int32, device="cuda")
@@ -911,7 +960,7 @@ def batch_arm(args):
         torch.cuda.current_stream().synchronize()
         tok_h.copy_(ids_h)
     e2e_s = time.perf_counter() - t0
-    e2e = {"value": ws * B * n_e2e / e2e_s, "unit": "stream-tokens/s", "h2d_bytes_per_step": 4 * B,
+    e2e = {"value": B_all * n_e2e / e2e_s, "unit": "stream-tokens/s", "h2d_bytes_per_step": 4 * B,
            "d2h_bytes_per_step": 4 * B, "steps": n_e2e,
            "api": "qd_batch_decode one step per call, tokens in from and ids out to pinned host memory"}
 
@@ -925,11 +974,12 @@ def batch_arm(args):
     qd.qd_destroy(h)
     del kv_dev
     if rank != 0:
-        return
+        return None
     line = {
         "metric": METRIC, "value": value, "unit": "stream-tokens/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": W_, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32",
+        "warmup": W_, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "strong" if ws > 1 else "weak",
+        "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: seeded N(0,0.02) bf16 weights, 1+N(0,0.1) gammas, N(0,1) bf16 initial caches",
         "config": {"workload": BATCH_DESC if not args.layers else
                    f"PROFILING CASE, not the workload: {args.layers}-layer variant of: " + BATCH_DESC,
@@ -937,7 +987,9 @@ def batch_arm(args):
                                                       "GEMMs as bf16 hi + lo parts; fp32 accumulation",
                    "timed": f"{args.steps} batched steps (each 64 stream-tokens) from the initial caches",
                    "l2": f"inputs larger than L2: {step_bytes / 1e9:.2f} GB per step",
-                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+                   "parallelism": (f"streams partitioned: rank r of {ws} decodes streams "
+                                   f"[64 r / {ws}, 64 (r + 1) / {ws}) over a full weight replica, no exchange")
+                                  if ws > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": att_gbs, "peak": hbm_peak, "unit": "GB/s",
                      "frac": att_gbs / hbm_peak, "traffic": att_traffic, "traffic_note": att_note,
                      "kernel": "batch_attn_kernel: one layer's attention of all 64 streams over their caches "
@@ -958,18 +1010,52 @@ def batch_arm(args):
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(k1 - k0), "kernels_per_step": per_step,
         "clocks": clk,
     }
-    print(json.dumps(line), flush=True)
-    if ws > 1:
-        torch.distributed.destroy_process_group()
+    return line
+
+
+def batch_arm(args):
+    ctx = _init_dist()
+    line = batch_line(args, ctx)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    _close_dist(ctx[0])
+
+
+def all_arm(args):
+    """The default line: the Talker decode step (the DRAM-bound batch-1 decoder the metric
+    is about) as the headline, with the ASR decoder, the two-level frame loop and the
+    batched multi-stream decode as keys of the same line, each with its own value,
+    roofline, CPU baseline and end-to-end number.  The driver's --steps / --warmup apply
+    to the headline and the ASR decoder (decode tokens); the frame loop runs one
+    150-frame trajectory and the batched decode 64 steps of its 256."""
+    import copy
+    ctx = _init_dist()
+    line = gpu_line(args, "talker", ctx)
+    sub = {}
+    sub["asr"] = gpu_line(args, "asr", ctx)
+    fa = copy.copy(args)
+    fa.steps, fa.warmup = FRAME_TRAJ, 8
+    sub["frames"] = frames_line(fa, ctx)
+    ba = copy.copy(args)
+    ba.steps, ba.warmup, ba.layers = 64, 8, 0
+    sub["batch"] = batch_line(ba, ctx)
+    if line is not None:
+        for k, v in sub.items():
+            line[k] = v
+        line["config"]["also"] = ("keys asr, frames and batch: the ASR decoder, the two-level frame loop and the "
+                                  "batched 64-stream decode, each measured in this run with its own value, "
+                                  "roofline, cpu_baseline and e2e")
+        print(json.dumps(line), flush=True)
+    _close_dist(ctx[0])
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=29000)
-    ap.add_argument("--warmup", type=int, default=870)
+    ap.add_argument("--steps", type=int, default=600)
+    ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="asr", choices=["asr", "talker", "tiny", "frames", "batch"])
+    ap.add_argument("--workload", default="all", choices=["all", "asr", "talker", "tiny", "frames", "batch"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="batch workload only: run a variant with this many layers (a profiling case)")
@@ -985,7 +1071,7 @@ def main():
         if args.warmup == ap.get_default("warmup"):
             args.warmup = 8
     ref = {"frames": frames_reference_arm, "batch": batch_reference_arm}.get(args.workload, reference_arm)
-    ours = {"frames": frames_arm, "batch": batch_arm}.get(args.workload, gpu_arm)
+    ours = {"frames": frames_arm, "batch": batch_arm, "all": all_arm}.get(args.workload, gpu_arm)
     (ref if args.impl == "reference" else ours)(args)
 
 

@@ -4,6 +4,12 @@ Batch-1 decode runs as independent replicas, one per GPU, so ranks exchange only
 timing: the slowest rank's time (a MAX all-reduce) and the whole-job rate over all
 ranks' units.  Here two gloo ranks run that reduction, and the reference arm runs under
 torchrun with two processes: only rank 0 works and prints its single JSON line.
+
+The batched workload partitions its streams over the ranks (each stream is an
+independent decoder, "Qwen3-TTS ncnn port", section "Talker: non-standard structure and
+two-level generation"): two gloo ranks each decode their slice of a small batched
+workload with the oracle, and the slices put back together equal one rank decoding
+every stream.
 """
 import json
 import os
@@ -64,3 +70,74 @@ def test_reference_arm_under_torchrun_prints_one_line_from_rank_0():
     line = lines[0]
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
+
+
+def _small_batch():
+    import workloads as W
+    s = W.scaled(W.TALKER, name="talker_kv", hidden=128, n_layers=2, n_q_heads=4, n_kv_heads=2, head_dim=32,
+                 ffn=256, vocab=96, embed_rows=96, buckets=(32, 64), prefill=20)
+    n = 5                                                       # not a multiple of the ranks
+    lens = W.uniform_int("multirank/L0", n, 3, 40)
+    toks = W.batch_first_tokens(n, s.vocab)
+    return s, n, lens, toks
+
+
+def _decode_streams(streams, steps=6):
+    """The oracle's greedy ids of the given streams of the small batched workload."""
+    import oracle as O
+    import workloads as W
+    s, _, lens, toks = _small_batch()
+    w = W.model_weights(s)
+    out = {}
+    for b in streams:
+        o = O.Oracle(s, w)
+        o.set_kv(W.batch_stream_kv(s, b, int(lens[b])), int(lens[b]))
+        tok, ids = int(toks[b]), []
+        for _ in range(steps):
+            tok, _, _, _ = o.step(token=tok, want_logits=False)
+            ids.append(int(tok))
+        o.close()
+        out[b] = ids
+    return out
+
+
+def _shard_rank_main(rank, world, port, out_dir):
+    sys.path.insert(0, ROOT)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    os.environ["OMP_NUM_THREADS"] = "1"
+    import torch.distributed as dist
+    import bench
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    _, n, _, _ = _small_batch()
+    lo, hi = bench.stream_shard(n, rank, world)
+    mine = _decode_streams(range(lo, hi))
+    parts = [None] * world
+    dist.all_gather_object(parts, {"lo": lo, "hi": hi, "ids": mine})
+    if rank == 0:
+        with open(os.path.join(out_dir, "shards.json"), "w") as f:
+            json.dump(parts, f)
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_stream_shards_cover_every_stream_once():
+    sys.path.insert(0, ROOT)
+    import bench
+    for n in (1, 5, 64):
+        for ws in (1, 2, 3, 4, 8):
+            got = [bench.stream_shard(n, r, ws) for r in range(ws)]
+            assert got[0][0] == 0 and got[-1][1] == n
+            assert all(got[r][1] == got[r + 1][0] for r in range(ws - 1))
+            assert max(h - l for l, h in got) - min(h - l for l, h in got) <= 1
+
+
+def test_batched_streams_partitioned_over_two_gloo_ranks_equal_one_rank(tmp_path):
+    import torch.multiprocessing as mp
+    port = _free_port()
+    mp.start_processes(_shard_rank_main, args=(2, port, str(tmp_path)), nprocs=2, join=True, start_method="spawn")
+    parts = json.load(open(tmp_path / "shards.json"))
+    _, n, _, _ = _small_batch()
+    assert [p["lo"] for p in parts] == [0, parts[0]["hi"]] and parts[-1]["hi"] == n
+    joined = {int(k): v for p in parts for k, v in p["ids"].items()}
+    assert sorted(joined) == list(range(n))
+    assert joined == _decode_streams(range(n))
