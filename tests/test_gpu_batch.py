@@ -201,8 +201,8 @@ def test_batch_errors():
 @pytest.mark.slow
 def test_batch_full_size_sampled_streams():
     """The batched workload's shapes: 28-layer Talker, 64 streams, smax 2048, lengths
-    U{256..1792}.  The first step of all 64 streams, then 8 teacher-forced steps of
-    streams 0, 21, 42 and 63, against the oracle."""
+    U{256..1792}.  The first step of all 64 streams, then all of the workload's 256
+    teacher-forced steps of streams 0, 21, 42 and 63, against the oracle."""
     import oracle as O
     B, smax = W.BATCH_STREAMS, W.BATCH_SMAX
     lens = W.batch_initial_lengths()
@@ -225,7 +225,10 @@ def test_batch_full_size_sampled_streams():
         assert rel_l2(g_log[b], rlog) <= REL_TOL, b
     for b, (gid, rid, margin, lrel) in out.items():
         assert lrel <= REL_TOL and (margin <= MARGIN or gid == rid), b
-    _check_steps(bp, 8)
+    checked = _check_steps(bp, W.BATCH_STEPS - 1)
+    assert checked > 4 * (W.BATCH_STEPS - 1) // 2          # the comparison is not vacuous
+    for b in (0, 21, 42, 63):
+        assert bp.qd.qd_batch_get_pos(bp.bh, b) == bp.lens[b] + W.BATCH_STEPS
     bp.close()
 
 

@@ -247,3 +247,72 @@ def test_frames_full_size():
     fp, codes, margins = _teacher_forced(W.TALKER, W.CODE_PREDICTOR, n)
     assert fp.qd.qd_get_pos(fp.T) == (W.TALKER.prefill + n - 1, 256)
     fp.close()
+
+
+@pytest.mark.slow
+def test_frames_full_size_per_frame_logits():
+    """The full-size frame workload one frame per call, with debug taps on both models:
+    for every one of the 150 frames, the Code Predictor's last head (14) logits and
+    final-norm state, and the Talker step's logits and per-layer hidden states, against
+    the oracle's, within relative L2 2e-3; every code above the margin equal.  The
+    oracle's predictor starts each frame from the GPU Talker's final-norm state (the
+    predictor's first input), so its comparison measures the predictor alone; the
+    Talker chains run side by side, fed the same ids."""
+    import oracle as O
+    ts, cs = W.TALKER, W.CODE_PREDICTOR
+    n = W.FRAME_COUNT
+    fp = FramePair(ts, cs)
+    torch = fp.torch
+    qd = fp.qd
+    cw = W.model_weights(cs)
+    head14 = cw["lm_head.14"]
+    c_logits = torch.empty(cs.vocab, dtype=torch.float32, device="cuda")
+    c_hidden = torch.empty((cs.n_layers + 1, cs.hidden), dtype=torch.float32, device="cuda")
+    t_logits = torch.empty(ts.vocab, dtype=torch.float32, device="cuda")
+    t_hidden = torch.empty((ts.n_layers + 1, ts.hidden), dtype=torch.float32, device="cuda")
+    qd.qd_set_debug_taps(fp.C, c_hidden, c_logits)
+    qd.qd_set_debug_taps(fp.T, t_hidden, t_logits)
+    text = W.frame_text_embeds(n, hidden=ts.hidden)
+    g0, r0, m0 = fp.prefill()
+    if m0 > MARGIN:
+        assert g0 == r0
+    primary, pm = r0, m0
+    nxt = torch.empty(ts.hidden, dtype=torch.float32, device="cuda")
+    codes = torch.empty((1, 16), dtype=torch.int32, device="cuda")
+    worst = {"cp_logits": 0.0, "cp_y": 0.0, "talker_logits": 0.0, "talker_hidden": 0.0}
+    class _GpuTalkerState:
+        """The Talker as the predictor's frame start sees it: the GPU's final-norm state."""
+        def hidden(self):
+            return _final_y(qd, fp.T, ts)
+    loop = O.FrameLoop(_GpuTalkerState(), fp.oc, fp.loop.tables[0], fp.loop.tables[1:])
+    for f in range(n):
+        codes_r, margins_r, next_r, _ = loop.generate(1, text[f:f + 1], primary, pm)
+        force = codes_r.copy()
+        qd.qd_frame_generate(fp.F, 1, fp.dev(text[f:f + 1]), codes, fp.dev(force), nxt)
+        got = codes.cpu().numpy()
+        _assert_ids(got, codes_r, margins_r)
+        y_ref = fp.oc.hidden()
+        worst["cp_y"] = max(worst["cp_y"], rel_l2(_final_y(qd, fp.C, cs), y_ref))
+        worst["cp_logits"] = max(worst["cp_logits"],
+                                 rel_l2(c_logits.cpu().numpy(), O.linear(head14, y_ref[None])[0]))
+        assert rel_l2(nxt.cpu().numpy(), next_r[0]) <= REL_TOL, f
+        if f < n - 1:
+            p = int(force[0, 0])
+            pid = qd.qd_decode_step(fp.T, embed=nxt, token=p)
+            primary, rlog, pm, rtaps = fp.ot.step(token=p, embed=next_r[0], head_idx=0, taps=True)
+            if pm > MARGIN:
+                assert pid == primary, f
+            worst["talker_logits"] = max(worst["talker_logits"], rel_l2(t_logits.cpu().numpy(), rlog))
+            g = t_hidden.cpu().numpy()
+            worst["talker_hidden"] = max(worst["talker_hidden"],
+                                         max(rel_l2(g[l], rtaps[l]) for l in range(len(rtaps))))
+    assert max(worst.values()) <= REL_TOL, worst
+    assert qd.qd_get_pos(fp.T) == (ts.prefill + n - 1, 256)
+    fp.close()
+
+
+def _final_y(qd, h, shape):
+    import torch
+    y = torch.empty(shape.hidden, dtype=torch.float32, device="cuda")
+    qd.qd_get_hidden(h, y)
+    return y.cpu().numpy()

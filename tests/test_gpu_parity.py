@@ -77,6 +77,22 @@ def test_asr_full_size_logits_and_layers():
 
 
 @pytest.mark.slow
+def test_talker_full_size_every_layer_every_step():
+    """The full Talker workload (28 layers, prefill 64, 600 teacher-forced steps across
+    the buckets 128 -> 256 -> 512 -> 1024) with the debug taps on: every step's logits
+    and the hidden state after every layer against the oracle's, relative L2 <= 2e-3,
+    and every id above the margin equal."""
+    s = W.TALKER
+    p, tr = _tf(s, s.decode_steps, taps=True)
+    tr.check()
+    assert len(tr.logits_rel) == s.decode_steps + 1 and len(tr.hidden_rel) == s.decode_steps
+    assert len(tr.ids_ref) - len(tr.low_margin) > s.decode_steps // 2     # the id comparison is not vacuous
+    pos, smax = p.qd.qd_get_pos(p.h)
+    assert pos == 664 and smax == 1024
+    p.close()
+
+
+@pytest.mark.slow
 def test_talker_full_size_graph_path():
     s = W.TALKER
     p, tr = _tf(s, s.decode_steps, taps=False)

@@ -48,16 +48,19 @@ int kernels_per_frame_predictor(const qd_model *C) {
 qd_status enqueue_frame(qd_frame *fr, cudaStream_t s, bool talker_step) {
     qd_model *m = fr->T;
     qd_model *C = fr->C;
+    // debug taps (eager frames only: a frame with taps set is never captured) record
+    // each model's last step of the frame
+    const bool tc = C->tap_hidden || C->tap_logits, tt = m->tap_hidden || m->tap_logits;
     CU(launch_frame_cp_prefill(fr->args, s));
-    qd_status st = enqueue_step(C, s, false, false);   // position 0: the Talker's hidden state
-    if (!st) st = enqueue_step(C, s, true, false);     // position 1: E_0[primary], head 0
+    qd_status st = enqueue_step(C, s, false, tc);      // position 0: the Talker's hidden state
+    if (!st) st = enqueue_step(C, s, true, tc);        // position 1: E_0[primary], head 0
     for (int j = 1; j < kCodePredictorHeads && !st; ++j) {
         CU(launch_frame_cp_input(fr->args, j, s));
-        st = enqueue_step(C, s, true, false);
+        st = enqueue_step(C, s, true, tc);
     }
     if (st) return fail(m, st, "code predictor step: %s", C->err.c_str());
     CU(launch_frame_sum(fr->args, s));
-    if (talker_step) return enqueue_step(m, s, true, false);
+    if (talker_step) return enqueue_step(m, s, true, tt);
     return QD_OK;
 }
 
