@@ -365,16 +365,17 @@ __device__ __forceinline__ bool kc_consume(const Ring &R, uint32_t &sidx, int nr
 }
 
 // Consumer warp: the CTA's `nrows` rows of W, arriving in ring stages of `rps` rows,
-// against this warp's K-chunk held as NC column chunks of 32 x EL: lane l holds
-// columns colw + c * 32 EL + l EL .. + EL of chunk c in x[c].  Rows go in groups of 8
-// (all loads of a group in flight at once), each group through one transposing
-// butterfly; part[r] (this warp's row of the partial-sum table) gets the chunk's sum
-// of row r.  The loops stay rolled: this code runs for every phase of every layer,
-// and what the instruction cache holds, not trip counts, sets its speed.  False if a
-// stage never arrived.
-template <typename WT, int EL, int NC, int NCMAX>
+// against this warp's K-chunk: nc column chunks of 32 x EL, whose values (already
+// scaled by the RMSNorm gamma) the warp keeps in shared memory at xw, chunk c at
+// xw[c * 32 EL ..], lane l's columns at l EL.  Rows go in groups of 8 (all loads of a
+// group in flight at once), the chunks of a group in a rolled loop, then one
+// transposing butterfly; part[r] (this warp's row of the partial-sum table) gets the
+// chunk's sum of row r.  One body serves every phase: it runs for every phase of
+// every layer, and what the instruction cache holds, not trip counts, sets its speed.
+// False if a stage never arrived.
+template <typename WT, int EL>
 __device__ __forceinline__ bool kc_gemv(const Ring &R, uint32_t &sidx, int nrows, int rps, uint32_t row_bytes,
-                                        int colw, const float (*x)[EL], float *part) {
+                                        int colw, int nc, const float *xw, float *part) {
     const int lane = threadIdx.x & 31;
     const int nst = (nrows + rps - 1) / rps;
 #pragma unroll 1
@@ -384,22 +385,27 @@ __device__ __forceinline__ bool kc_gemv(const Ring &R, uint32_t &sidx, int nrows
         const int n = min_c(rps, nrows - st * rps);
 #pragma unroll 1
         for (int g0 = 0; g0 < n; g0 += 8) {
-            // every load unconditional (rows past n re-read row n - 1 and count zero)
             float acc[8];
 #pragma unroll
-            for (int r = 0; r < 8; ++r) {
-                const int row = g0 + r < n ? g0 + r : n - 1;
-                const WT *wr = reinterpret_cast<const WT *>(sb + (size_t)row * row_bytes) + colw + lane * EL;
-                float d = 0.f;
+            for (int r = 0; r < 8; ++r) acc[r] = 0.f;
+#pragma unroll 1
+            for (int c = 0; c < nc; ++c) {
+                float xv[EL];
+                load_elems<float, EL>(xw + c * 32 * EL + lane * EL, xv);
+                // every load unconditional (rows past n re-read row n - 1, counted zero below)
 #pragma unroll
-                for (int c = 0; c < NC; ++c) {
+                for (int r = 0; r < 8; ++r) {
+                    const int row = g0 + r < n ? g0 + r : n - 1;
                     float f[EL];
-                    load_elems<WT, EL>(wr + c * 32 * EL, f);
+                    load_elems<WT, EL>(reinterpret_cast<const WT *>(sb + (size_t)row * row_bytes) + colw + c * 32 * EL +
+                                           lane * EL,
+                                       f);
 #pragma unroll
-                    for (int e = 0; e < EL; ++e) d = fmaf(f[e], x[c][e], d);
+                    for (int e = 0; e < EL; ++e) acc[r] = fmaf(f[e], xv[e], acc[r]);
                 }
-                acc[r] = g0 + r < n ? d : 0.f;
             }
+#pragma unroll
+            for (int r = 0; r < 8; ++r) acc[r] = g0 + r < n ? acc[r] : 0.f;
             const float v = treduce<8>(acc, lane);
             const int row = g0 + lane / 4;
             if ((lane & 3) == 0 && row < n) part[st * rps + row] = v;
@@ -422,7 +428,7 @@ __device__ __forceinline__ float rms_scale(const float *ss, int K, float eps) {
     float t = 0.f;
 #pragma unroll
     for (int w = 0; w < kNW; ++w) t += ss[w];
-    return 1.0f / sqrtf(t / (float)K + eps);
+    return rsqrtf(t / (float)K + eps);
 }
 
 // This lane's E columns of the step's input vector (token row of the embedding
@@ -463,7 +469,7 @@ __device__ __forceinline__ void head_norm(float *v, const float *gam, int hd, fl
 #pragma unroll
     for (int e = 0; e < E; ++e) ss = fmaf(v[e], v[e], ss);
     ss = warp_sum(ss);
-    const float inv = 1.0f / sqrtf(ss / (float)hd + eps);
+    const float inv = rsqrtf(ss / (float)hd + eps);
 #pragma unroll
     for (int e = 0; e < E; ++e) v[e] = v[e] * inv * gam[e];
 }
@@ -523,8 +529,8 @@ __device__ __forceinline__ void warp_attention(const KT *Ks, const KT *Vs, const
             const bool live = lane / LPV < nb;
             sc = live ? sc * scale : -INFINITY;
             const float mn = fmaxf(mh[h], warp_max(sc));
-            const float corr = expf(mh[h] - mn);   // 0 for the first block
-            const float ex = live ? expf(sc - mn) : 0.f;
+            const float corr = __expf(mh[h] - mn);   // 0 for the first block
+            const float ex = live ? __expf(sc - mn) : 0.f;
             lh[h] = lh[h] * corr + warp_sum(lane % LPV == 0 ? ex : 0.f);
 #pragma unroll
             for (int e = 0; e < E; ++e) o[h][e] *= corr;
@@ -571,7 +577,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
     // hidden size); the phases need NC0 <= NC1 <= NC2 chunks (one GEMV body each)
     constexpr int EL = KH / kNC;
     constexpr int NCA = KH / (256 * EL), NCQ = KQ / (256 * EL), NCF = KF / (256 * EL);
-    constexpr int NC0 = NCA, NC1 = NCQ, NC2 = NCF, NCMAX = NCF;
+    constexpr int NCMAX = NCF;
+    constexpr int XSW = NCMAX * 32 * EL;                         // floats of a warp's input slice
     static_assert(NCA == 1 && NCQ >= 1 && NCF >= NCQ && KQ == NCQ * 256 * EL && KF == NCF * 256 * EL, "chunks");
     // row groups of the GEMV phases: 8, or fewer when a CTA holds fewer rows
     constexpr int A_RG = min_c(8, phase_rps(KQ + 2 * KV, 1, KH, ES));
@@ -597,6 +604,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
     float *kc_part = reinterpret_cast<float *>(smem + a.off_kc);  // [2][kNW][PS] row partials
     float *kc_ss = kc_part + 2 * kNW * PS;                          // [2][kNW] sums of squares
     float *xres = reinterpret_cast<float *>(smem + a.off_xres);    // residual rows of this CTA
+    float *xs = reinterpret_cast<float *>(smem + a.off_xs);        // [kNW][ffn / kNW] input slices
     const Ring R{smem, full, empty, a.nst};
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -821,13 +829,13 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
                     for (int w = h * WPH; w < (h + 1) * WPH; ++w) {
                         const float mw = wml[w * 2];
                         if (mw != -INFINITY) {
-                            const float f = expf(mw - M);
+                            const float f = __expf(mw - M);
                             den = fmaf(f, wml[w * 2 + 1], den);
                             num = fmaf(f, wo[(size_t)w * HD + d], num);
                         }
                     }
-                    st_tag(Tpo + t, num / den, seq);
-                    if (d == 0) st_tag(Tml + 2 * h, M + logf(den), seq);
+                    st_tag(Tpo + t, __fdividef(num, den), seq);
+                    if (d == 0) st_tag(Tml + 2 * h, M + __logf(den), seq);
                 }
                 // this CTA's slice [d0, d1) of the group's merged output: every split's output
                 // weighted by exp(lse_s - max) over their sum.  A group of LP lanes (LP >=
@@ -861,13 +869,13 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
                         const float ov = lv ? wv[2 * k + 1] : 0.f;
                         float M = lse;
                         for (int o = 1; o < LP; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-                        float f = lv ? expf(lse - M) : 0.f;
+                        float f = lv ? __expf(lse - M) : 0.f;
                         float num = f * ov;
                         for (int o = 1; o < LP; o <<= 1) {
                             f += __shfl_xor_sync(0xffffffffu, f, o);
                             num += __shfl_xor_sync(0xffffffffu, num, o);
                         }
-                        if (lv && sp == 0) st_tag(T + a.tg_att + (size_t)ig * GD + (k == 0 ? cola : colb), num / f, seq);
+                        if (lv && sp == 0) st_tag(T + a.tg_att + (size_t)ig * GD + (k == 0 ? cola : colb), __fdividef(num, f), seq);
                     }
                 }
                 if (!okm) ok = false;
@@ -970,19 +978,19 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
             }
             okw = __all_sync(0xffffffffu, okw);
             float ss = 0.f;
+            float *xw = xs + (size_t)warp * XSW;      // this warp's slice of the input, times gamma
 #pragma unroll
             for (int cc = 0; cc < NCMAX; ++cc)
+                if (cc < nc) {
 #pragma unroll
-                for (int e = 0; e < EL; ++e) {
-                    ss = fmaf(x[cc][e], x[cc][e], ss);
-                    x[cc][e] *= gv[cc][e];
+                    for (int e = 0; e < EL; ++e) {
+                        ss = fmaf(x[cc][e], x[cc][e], ss);
+                        xw[cc * 32 * EL + lane * EL + e] = x[cc][e] * gv[cc][e];
+                    }
                 }
+            __syncwarp();
             float *part = kc_part + buf * kNW * PS;
-            if (okw) {
-                if (nc == NC0) okw = kc_gemv<WT, EL, NC0, NCMAX>(R, sidx, nrows, rps, rbytes, colw, x, part + warp * PS);
-                else if (nc == NC1) okw = kc_gemv<WT, EL, NC1, NCMAX>(R, sidx, nrows, rps, rbytes, colw, x, part + warp * PS);
-                else okw = kc_gemv<WT, EL, NC2, NCMAX>(R, sidx, nrows, rps, rbytes, colw, x, part + warp * PS);
-            }
+            if (okw) okw = kc_gemv<WT, EL>(R, sidx, nrows, rps, rbytes, colw, nc, xw, part + warp * PS);
             if (gam) {
                 ss = warp_sum(ss);
                 if (lane == 0) kc_ss[buf * kNW + warp] = ss;
@@ -999,7 +1007,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
                     const float r = rms_scale(kc_ss + buf * kNW, hidden, a.eps);
                     const float gt = r * warp_parts(part, PS, 2 * tid);
                     const float up = r * warp_parts(part, PS, 2 * tid + 1);
-                    st_tag(T + a.tg_act + r0_gu / 2 + tid, gt / (1.0f + expf(-gt)) * up, seq);
+                    st_tag(T + a.tg_act + r0_gu / 2 + tid, __fdividef(gt, 1.0f + __expf(-gt)) * up, seq);
                 }
             } else if (tid < n_x) {
                 const float xn = xres[tid] + warp_parts(part, PS, tid);

@@ -355,6 +355,7 @@ static StepArgs step_args(qd_model *m, bool with_head, bool taps) {
     a.off_kc = m->off_kc;
     a.off_xres = m->off_xres;
     a.off_ldev = m->off_ldev;
+    a.off_xs = m->off_xs;
     return a;
 }
 
@@ -665,6 +666,7 @@ static qd_status setup_persistent(qd_model *m) {
         tail += ((size_t)2 * kConsumerWarps * kStepRowsMax + 2 * kConsumerWarps) * 4 + 16;   // row partials
         tail += (size_t)kStepRowsMax * 4 + 16;                         // residual rows
         tail += sizeof(LayerDev) * (size_t)c.n_layers + 16;            // layer table
+        tail += (size_t)c.ffn * 4 + 16;                                // the warps' input slices
     }
     const size_t max_smem = kStepMaxSmem;
     const int nst = kStepRingStages;
@@ -681,6 +683,7 @@ static qd_status setup_persistent(qd_model *m) {
     m->off_kc = take(((size_t)2 * kConsumerWarps * kStepRowsMax + 2 * kConsumerWarps) * 4, 16);
     m->off_xres = take((size_t)kStepRowsMax * 4, 16);
     m->off_ldev = take(sizeof(LayerDev) * (size_t)c.n_layers, 16);
+    m->off_xs = take((size_t)c.ffn * 4, 16);
     m->smem_step = align_up(off, 16);
     m->nst_step = nst;
     if (m->smem_step > max_smem) return QD_OK;

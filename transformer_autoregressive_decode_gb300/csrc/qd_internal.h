@@ -149,7 +149,8 @@ struct StepArgs {
     unsigned *seq;                 // launch sequence number (starts at 1, never 0)
     unsigned *emit_flag;           // CTA 0 stores the launch's seq (release) once the step's
                                    // token is in the emitted set
-    int off_kc, off_xres, off_ldev;// shared memory: row-partial tables, residual rows, layer table
+    int off_kc, off_xres, off_ldev, off_xs;   // shared memory: row-partial tables, residual rows,
+                                              // layer table, the warps' input slices
     DevState *st;
 };
 

@@ -86,7 +86,7 @@ struct qd_model {
     unsigned *barrier = nullptr;
     size_t smem_step = 0;
     int nst_step = 0, off_full = 0, off_gsm = 0, off_misc = 0, off_res = 0, off_att = 0, off_emw = 0, off_xin = 0;
-    int off_kc = 0, off_xres = 0, off_ldev = 0;
+    int off_kc = 0, off_xres = 0, off_ldev = 0, off_xs = 0;
 
     std::vector<qd_frame *> frames;          // frame generators bound to this handle
     bool use_graphs = true;
