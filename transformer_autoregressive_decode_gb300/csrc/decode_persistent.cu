@@ -310,59 +310,7 @@ __device__ __forceinline__ void stage_put(const Ring &R, uint32_t sidx, int lane
     if (lane == 0) mbar_arrive(&R.empty[sidx % kStepStages]);
 }
 
-// Compile-time shape of a GEMV phase: the most rows a CTA holds (the step runs on at
-// least kMinSms SMs), and the rows of a ring stage (padded to a power of two) that can
-// be the CTA's.
-constexpr int kMinSms = kStepMinSms;
-__host__ __device__ constexpr int phase_rows_max(int rows, int unit) {
-    return ((rows / unit) + kMinSms - 1) / kMinSms * unit;
-}
 __host__ __device__ constexpr int min_c(int a, int b) { return a < b ? a : b; }
-__host__ __device__ constexpr int phase_rps(int rows, int unit, int K, int es) {
-    return min_c(pow2_ceil(kSlotBytes / (K * es)), pow2_ceil(phase_rows_max(rows, unit)));
-}
-
-// Consumer warp: the CTA's `nrows` rows of W, arriving in ring stages of `rps` rows,
-// against this warp's K-chunk (lane: E values xv of columns col0 ..).  Rows go in
-// groups of RG (a power of two <= 8): all loads of a group in flight at once, then one
-// transposing butterfly; part[r] (this warp's row of the partial-sum table) gets the
-// chunk's sum of row r.  The loops stay rolled: this code runs once per layer and
-// phase, and its size, not its trip count, is what the instruction cache sees.
-// False if a stage never arrived.
-template <typename WT, int E, int RG>
-__device__ __forceinline__ bool kc_consume(const Ring &R, uint32_t &sidx, int nrows, int rps, uint32_t row_bytes,
-                                           int col0, const float *xv, float *part) {
-    static_assert(RG >= 1 && RG <= 8, "row group");
-    const int lane = threadIdx.x & 31;
-    const int nst = (nrows + rps - 1) / rps;
-#pragma unroll 1
-    for (int st = 0; st < nst; ++st) {
-        const uint8_t *sb = stage_get(R, sidx + st);
-        if (!sb) return false;
-        const int n = min_c(rps, nrows - st * rps);
-#pragma unroll 1
-        for (int g0 = 0; g0 < n; g0 += RG) {
-            // every load unconditional (rows past n re-read row n - 1 and count zero)
-            float acc[RG];
-#pragma unroll
-            for (int r = 0; r < RG; ++r) {
-                const int row = g0 + r < n ? g0 + r : n - 1;
-                float f[E];
-                load_elems<WT, E>(reinterpret_cast<const WT *>(sb + (size_t)row * row_bytes) + col0, f);
-                float d = 0.f;
-#pragma unroll
-                for (int e = 0; e < E; ++e) d = fmaf(f[e], xv[e], d);
-                acc[r] = g0 + r < n ? d : 0.f;
-            }
-            const float v = treduce<RG>(acc, lane);
-            const int row = g0 + lane / (32 / RG);
-            if (lane % (32 / RG) == 0 && row < n) part[st * rps + row] = v;
-        }
-        stage_put(R, sidx + st, lane);
-    }
-    sidx += nst;
-    return true;
-}
 
 // Consumer warp: the CTA's `nrows` rows of W, arriving in ring stages of `rps` rows,
 // against this warp's K-chunk: nc column chunks of 32 x EL, whose values (already
@@ -569,7 +517,6 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
     constexpr int SEGW = 32 * EPL;
     constexpr int NS_H = KH / SEGW;                       // the head's segments per warp
     constexpr int ES = (int)sizeof(WT);
-    constexpr int EA = KH / kNC, EQ = KQ / kNC, EF = KF / kNC;   // columns per lane of each K-chunk
     constexpr int KV = KVH * HD;                                  // k (and v) rows
     constexpr int GQ = KQ / KV;                                   // q heads per kv head
     // stage shapes of the GEMV phases (rows per stage padded, stages per butterfly)
@@ -580,11 +527,6 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
     constexpr int NCMAX = NCF;
     constexpr int XSW = NCMAX * 32 * EL;                         // floats of a warp's input slice
     static_assert(NCA == 1 && NCQ >= 1 && NCF >= NCQ && KQ == NCQ * 256 * EL && KF == NCF * 256 * EL, "chunks");
-    // row groups of the GEMV phases: 8, or fewer when a CTA holds fewer rows
-    constexpr int A_RG = min_c(8, phase_rps(KQ + 2 * KV, 1, KH, ES));
-    constexpr int C_RG = min_c(8, phase_rps(KH, 1, KQ, ES));
-    constexpr int D_RG = min_c(8, phase_rps(2 * KF, 2, KH, ES));
-    constexpr int E_RG = min_c(8, phase_rps(KH, 1, KF, ES));
     constexpr int EH = HD / 32;
     constexpr int HALF = HD / 2;
     constexpr int PS = kStepRowsMax;
