@@ -426,8 +426,18 @@ qd_status qd_batch_destroy(qd_batch_handle b);
  * emitted set is cleared.  Synchronises. */
 qd_status qd_batch_set_stream(qd_batch_handle b, int stream, const void *kv_dev, int length, int32_t token);
 
-/* qd_batch_decode -- n_steps greedy steps of every stream.  ids_dev: DEVICE int32
- * [n_steps][B] receives each stream's argmax per step.  force_dev: DEVICE int32
+/* qd_batch_set_sampling -- draw every stream's ids instead of taking the greedy argmax,
+ * after the repetition penalty and the EOS mask, with the settings of qd_set_sampling
+ * (top_k <= 64 candidates, temperature, top_p; "qwen3-tts-hip OPTIMIZATION_LOG",
+ * sampling entries): stream b draws u from SplitMix64 of seed + b at its own counter
+ * (ids it has drawn since its last qd_batch_set_stream).  top_k 0 restores the argmax.
+ * The settings live in device memory, so captured step graphs keep serving.
+ * Synchronises.  Errors: QD_EINVAL, QD_EUNSUPPORTED (vocabulary above 32768). */
+qd_status qd_batch_set_sampling(qd_batch_handle b, int top_k, float temperature, float top_p, uint64_t seed);
+
+/* qd_batch_decode -- n_steps steps of every stream (greedy unless qd_batch_set_sampling
+ * turned sampling on).  ids_dev: DEVICE int32 [n_steps][B] receives each stream's id
+ * per step.  force_dev: DEVICE int32
  * [n_steps][B] or NULL: when given, these ids are fed back as the next input tokens
  * instead of the argmaxes (teacher forcing).  Asynchronous; device-side errors are
  * reported by qd_batch_sync.  Errors: QD_EINVAL, QD_ESTATE (a stream never set),

@@ -153,6 +153,67 @@ def test_batch_multi_step_call_equals_single_steps_and_graphs_equal_eager():
             assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("k,t", [(50, 0.9), (8, 0.7)])
+def test_batch_sampled_streams_match_oracle(k, t):
+    """Sampling in the batched decode (the pages' generation defaults top-k 50,
+    temperature 0.9, top-p 1.0; and 8 candidates at 0.7, where more draws are decidable
+    on this 2-layer shape): stream b draws from seed + b at its own counter, as the
+    oracle stream does with set_sampling(seed + b), teacher-forced with the oracle's
+    draws.  The sampler exactly: every GPU id equals the oracle's sampler applied to the
+    GPU's own final logits (the oracle's penalty and EOS mask over the same emitted set,
+    the same u).  Against the oracle's whole step: the logits within 2e-3, and every id
+    whose draw the oracle's margin decides (beyond ten times a 2e-3 logit error over the
+    temperature) equal."""
+    import torch
+    import oracle as O
+    B, smax, n = 6, 512, 10
+    p, seed = 1.0, 77
+    lens = W.batch_initial_lengths(n=B, lo=100, hi=400)
+    bp = BatchPair(TALKER2, B, smax, lens)
+    bp.qd.qd_batch_set_sampling(bp.bh, k, t, p, seed)
+    for b, o in bp.ref.items():
+        o.set_sampling(k, t, p, seed + b)
+    s = bp.shape
+    decided = 0
+    for i in range(n):
+        out = bp.step()
+        g_log = bp.logits.cpu().numpy()
+        for b, (gid, rid, margin, lrel) in out.items():
+            assert lrel <= REL_TOL
+            em = bp.ref[b].emitted()
+            ids_em = [v for v in range(s.vocab) if (em[v >> 5] >> (v & 31)) & 1]
+            _, final, _ = O.penalty_argmax(g_log[b], ids_em, s.rep_penalty, s.eos_mask_id)
+            want, m_own = O.sample(final, k, t, p, O.uniform(seed + b, i))
+            assert gid == want or m_own < 1e-6, (i, b, gid, want, m_own)
+            if margin > 10 * 2e-3 / t:
+                decided += 1
+                assert gid == rid, (i, b, gid, rid, margin)
+    if k == 8:
+        assert decided >= B * n // 10, decided
+    bp.close()
+    # the draws are not the argmaxes, and top_k 0 is greedy again
+    ids_g = torch.empty((n, B), dtype=torch.int32, device="cuda")
+    g = BatchPair(TALKER2, B, smax, lens, oracle_streams=[])
+    g.qd.qd_batch_decode(g.bh, n, ids_g)
+    g.close()
+    ids_s = torch.empty((n, B), dtype=torch.int32, device="cuda")
+    sp = BatchPair(TALKER2, B, smax, lens, oracle_streams=[])
+    sp.qd.qd_batch_set_sampling(sp.bh, k, t, p, seed)
+    sp.qd.qd_batch_decode(sp.bh, n, ids_s)
+    assert (ids_s.cpu().numpy() != ids_g.cpu().numpy()).any()
+    sp.qd.qd_batch_set_sampling(sp.bh, 0, 1.0, 1.0, 0)
+    for b in range(B):
+        sp.qd.qd_batch_set_stream(sp.bh, b, torch.from_numpy(W.batch_stream_kv(TALKER2, b, sp.lens[b])).cuda(),
+                                  sp.lens[b], int(sp.tokens[b]))
+    ids_g2 = torch.empty((n, B), dtype=torch.int32, device="cuda")
+    sp.qd.qd_batch_decode(sp.bh, n, ids_g2)
+    assert np.array_equal(ids_g2.cpu().numpy(), ids_g.cpu().numpy())
+    with pytest.raises(sp.qd.QDError) as ei:
+        sp.qd.qd_batch_set_sampling(sp.bh, 65, t, p, seed)
+    assert ei.value.status == sp.qd.QD_EINVAL
+    sp.close()
+
+
 def test_batch_greedy_feeds_back_its_own_ids():
     import torch
     B, smax, n = 4, 256, 5

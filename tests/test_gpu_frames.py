@@ -239,6 +239,40 @@ def test_destroying_a_model_first_detaches_the_frame_handle():
     fp.oc.close()
 
 
+def test_frames_sampled_match_oracle():
+    """Sampling in the frame loop on the Talker and the Code Predictor: each model draws
+    u from its seed at its own counter (ids produced since its last reset; the predictor
+    restarts every frame, as its id history does), on both sides.  Teacher-forced with
+    the oracle's draws, every code whose draw the oracle's margin decides (beyond ten
+    times a 2e-3 logit error over the temperature) equals the oracle's.  8 candidates at
+    temperature 0.7: on these 2-layer shapes the 50 best logits of the pages' default
+    lie too close together for most draws to be decidable (the batched test checks the
+    sampler itself at the default settings)."""
+    n, k, t, p = 6, 8, 0.7, 1.0
+    fp = FramePair(TALKER2, CP2)
+    for h, o, seed in ((fp.T, fp.ot, 11), (fp.C, fp.oc, 22)):
+        fp.qd.qd_set_sampling(h, k, t, p, seed)
+        o.set_sampling(k, t, p, seed)
+    text = W.frame_text_embeds(n, hidden=TALKER2.hidden)
+    g0, r0, m0 = fp.prefill()
+    codes_r, margins_r, next_r, _ = fp.oracle_frames(n, text, r0, m0)
+    force = codes_r.copy()
+    force[0, 0] = r0
+    codes_g, next_g = fp.gpu_frames(n, text, force)
+    decided = margins_r > 10 * 2e-3 / t
+    bad = np.argwhere(decided & (codes_g != codes_r))
+    assert len(bad) == 0, f"sampled codes differ at (frame, code) {bad[:10].tolist()}"
+    assert decided.mean() >= 0.1, decided.mean()           # the comparison is not vacuous
+    assert rel_l2(next_g, next_r[-1]) <= REL_TOL
+    # and the draws are not the argmax throughout: sampling took effect
+    fg = FramePair(TALKER2, CP2)
+    fg.prefill()
+    greedy, _ = fg.gpu_frames(n, text, force)
+    assert (greedy[:, 1:] != codes_g[:, 1:]).any()
+    fg.close()
+    fp.close()
+
+
 @pytest.mark.slow
 def test_frames_full_size():
     """The frame workload at full size: 28-layer Talker, 5-layer Code Predictor,

@@ -37,7 +37,8 @@ EXPORTS = ("qd_create", "qd_destroy", "qd_reset", "qd_prefill", "qd_prefill_mrop
            "qd_frame_generate", "qd_frame_set_graphs", "qd_gemm_bf16", "qd_quantize_q8", "qd_gemv_q8",
            "qd_conv1d_causal", "qd_conv_transpose1d_causal", "qd_batch_create", "qd_batch_destroy",
            "qd_batch_set_stream", "qd_batch_decode", "qd_batch_sync", "qd_batch_get_logits", "qd_batch_copy_kv",
-           "qd_batch_get_pos", "qd_batch_get_launch_count", "qd_batch_set_graphs", "qd_batch_time_kernel", "qd_batch_prefill")
+           "qd_batch_get_pos", "qd_batch_get_launch_count", "qd_batch_set_graphs", "qd_batch_time_kernel", "qd_batch_prefill",
+           "qd_batch_set_sampling")
 
 
 class qd_config(ctypes.Structure):
@@ -96,6 +97,7 @@ _SIGS = {
     "qd_batch_destroy": ([_vp], _i32),
     "qd_batch_set_stream": ([_vp, _i32, _vp, _i32, ctypes.c_int32], _i32),
     "qd_batch_decode": ([_vp, _i32, _vp, _vp], _i32),
+    "qd_batch_set_sampling": ([_vp, _i32, ctypes.c_float, ctypes.c_float, ctypes.c_uint64], _i32),
     "qd_batch_sync": ([_vp], _i32),
     "qd_batch_get_logits": ([_vp, _vp], _i32),
     "qd_batch_copy_kv": ([_vp, _i32, _vp, _P(_sz)], _i32),
@@ -408,6 +410,10 @@ def qd_batch_destroy(b: BatchHandle):
 def qd_batch_set_stream(b: BatchHandle, stream: int, kv_dev, length: int, token: int):
     """kv_dev: device bf16 tensor [n_layers, 2, n_kv_heads, length, head_dim] (or None when length is 0)."""
     _check(b.model, _lib.qd_batch_set_stream(b.b, int(stream), _ptr(kv_dev), int(length), int(token)))
+
+
+def qd_batch_set_sampling(b: BatchHandle, top_k: int, temperature: float, top_p: float, seed: int):
+    _check(b.model, _lib.qd_batch_set_sampling(b.b, int(top_k), float(temperature), float(top_p), int(seed)))
 
 
 def qd_batch_decode(b: BatchHandle, n_steps: int, ids_dev, force_dev=None):

@@ -115,6 +115,8 @@ struct qd_batch {
     uint32_t *emitted = nullptr;
     int words = 0;
     BatchCtl *ctl = nullptr;
+    BatchSampling *samp = nullptr;   // device; top_k 0 = greedy
+    int *drawn = nullptr;            // [B] draws of each stream since it was set
     TcGemmPlan p_qkv{}, p_o{}, p_gu{}, p_d{}, p_head{};
     std::vector<int> h_pos;     // host view of each stream's position
     std::vector<char> h_ready;  // stream has a cache and an input token
@@ -249,6 +251,8 @@ qd_status enqueue_batch_step(qd_batch *b, cudaStream_t s) {
     am.tokens = b->tokens;
     am.pos = b->pos;
     am.status = b->status;
+    am.samp = b->samp;
+    am.drawn = b->drawn;
     ++n;
     if (launch_batch_argmax(am, B, s, true)) return batch_fail(b, QD_ECUDA, "argmax launch failed");
     b->kernels_per_step = n;
@@ -623,7 +627,8 @@ qd_status qd_batch_create(qd_handle model, int n_streams, int smax, qd_batch_han
                  o_cos = take((size_t)smax * (c.head_dim / 2) * 4), o_sin = take((size_t)smax * (c.head_dim / 2) * 4),
                  o_ap = take((size_t)B * c.n_kv_heads * batch_attn_max_chunks(smax) *
                              (c.n_q_heads / c.n_kv_heads) * (c.head_dim + 2) * 4),
-                 o_ac = take((size_t)B * c.n_kv_heads * 4);
+                 o_ac = take((size_t)B * c.n_kv_heads * 4), o_smp = take(sizeof(BatchSampling)),
+                 o_drn = take((size_t)B * 4);
     b->stream_elems = (size_t)c.n_layers * 2 * c.n_kv_heads * smax * c.head_dim;
     qd_status st = QD_OK;
     auto check = [&](cudaError_t e, const char *what) {
@@ -653,6 +658,8 @@ qd_status qd_batch_create(qd_handle model, int n_streams, int smax, qd_batch_han
         b->rope_sin = reinterpret_cast<float *>(A + o_sin);
         b->att_part = reinterpret_cast<float *>(A + o_ap);
         b->att_count = reinterpret_cast<int *>(A + o_ac);
+        b->samp = reinterpret_cast<BatchSampling *>(A + o_smp);
+        b->drawn = reinterpret_cast<int *>(A + o_drn);
         check(cudaMemsetAsync(b->arena, 0, off, b->ls), "cudaMemsetAsync");
         // positions past a stream's length hold zeros or values this library wrote
         check(cudaMemsetAsync(b->kv, 0, b->stream_elems * 2 * B, b->ls), "cudaMemsetAsync(batch KV caches)");
@@ -698,10 +705,32 @@ qd_status qd_batch_set_stream(qd_batch_handle b, int stream, const void *kv_dev,
     CU(cudaMemcpyAsync(b->pos + stream, &length, 4, cudaMemcpyHostToDevice, b->ls));
     CU(cudaMemcpyAsync(b->tokens + stream, &token, 4, cudaMemcpyHostToDevice, b->ls));
     CU(cudaMemsetAsync(b->emitted + (size_t)stream * b->words, 0, (size_t)b->words * 4, b->ls));
+    CU(cudaMemsetAsync(b->drawn + stream, 0, 4, b->ls));
     CU(cudaStreamSynchronize(b->ls));
     batch_leave(b);
     b->h_pos[stream] = length;
     b->h_ready[stream] = 1;
+    return QD_OK;
+}
+
+qd_status qd_batch_set_sampling(qd_batch_handle b, int top_k, float temperature, float top_p, uint64_t seed) {
+    if (!b) return QD_EINVAL;
+    qd_model *m = b->m;
+    if (top_k < 0 || top_k > kMaxTopK) return fail(m, QD_EINVAL, "top_k %d outside [0, %d]", top_k, kMaxTopK);
+    if (!(temperature > 0.f) || !(top_p > 0.f) || top_p > 1.f)
+        return fail(m, QD_EINVAL, "temperature must be > 0 and top_p in (0, 1]");
+    if (top_k > 0 && m->cfg.vocab > kBatchSampleVocabMax)
+        return fail(m, QD_EUNSUPPORTED, "batched sampling keeps at most %d logits per stream", kBatchSampleVocabMax);
+    BatchSampling h = {};
+    h.top_k = top_k;
+    h.temperature = temperature;
+    h.top_p = top_p;
+    h.seed_lo = (uint32_t)seed;
+    h.seed_hi = (uint32_t)(seed >> 32);
+    batch_enter(b);
+    CU(cudaMemcpyAsync(b->samp, &h, sizeof(h), cudaMemcpyHostToDevice, b->ls));
+    CU(cudaStreamSynchronize(b->ls));
+    batch_leave(b);
     return QD_OK;
 }
 

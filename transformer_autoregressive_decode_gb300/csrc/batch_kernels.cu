@@ -438,6 +438,8 @@ __global__ void __launch_bounds__(kRowThreads) norm_split_kernel(const NormSplit
 
 // ---- per-stream penalty + EOS mask + argmax; the last CTA of the step advances the
 // control block's step index
+static_assert(kRowThreads == kConsumerWarps * 32, "the block top-k selection runs on every thread of the CTA");
+
 __global__ void __launch_bounds__(kRowThreads) batch_argmax_kernel(const BatchArgmaxArgs a) {
     __shared__ float bv_s[kRowThreads / 32];
     __shared__ int bi_s[kRowThreads / 32];
@@ -446,9 +448,36 @@ __global__ void __launch_bounds__(kRowThreads) batch_argmax_kernel(const BatchAr
     const int b = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const float *lg = a.logits + (size_t)b * a.V;
     const uint32_t *em = a.emitted + (size_t)b * a.words;
+    const int sk = a.samp->top_k;
+    if (sk > 0) {
+        // sampling: the stream's final logits in shared memory, its top-k candidates, one
+        // draw (the same selection and draw as the single-stream head)
+        extern __shared__ __align__(16) float sm_v[];
+        float *cv = sm_v + a.V;
+        int *ci = reinterpret_cast<int *>(cv + kMaxTopK);
+        int *scr = ci + kMaxTopK;                 // 8-byte aligned: V + 2 kMaxTopK words before it
+        for (int i = tid; i < a.V; i += kRowThreads) {
+            float v = lg[i];
+            if (a.penalty != 1.0f && ((em[i >> 5] >> (i & 31)) & 1u)) v = v > 0.f ? v / a.penalty : v * a.penalty;
+            if (i == a.eos) v = -INFINITY;
+            sm_v[i] = v;
+        }
+        named_sync(1, kRowThreads);
+        block_topk(sm_v, 1, nullptr, 0, a.V, sk, cv, ci, scr);
+        if (warp == 0) {
+            const BatchSampling sp = *a.samp;
+            const uint64_t seed = (((uint64_t)sp.seed_hi << 32) | sp.seed_lo) + (uint64_t)b;
+            const int id = warp_sample(cv, ci, sk, sp.temperature, sp.top_p, uniform53(seed, (uint64_t)a.drawn[b]));
+            if (lane == 0) {
+                bi_s[0] = id;
+                a.drawn[b] = a.drawn[b] + 1;
+            }
+        }
+        __syncthreads();
+    }
     float best_v = -INFINITY;
     int best_i = 0x7fffffff;
-    for (int i = tid; i < a.V; i += kRowThreads) {
+    for (int i = tid; i < a.V && sk == 0; i += kRowThreads) {
         float v = lg[i];
         if (a.penalty != 1.0f && ((em[i >> 5] >> (i & 31)) & 1u)) v = v > 0.f ? v / a.penalty : v * a.penalty;
         if (i == a.eos) v = -INFINITY;
@@ -466,7 +495,7 @@ __global__ void __launch_bounds__(kRowThreads) batch_argmax_kernel(const BatchAr
             best_i = oi;
         }
     }
-    if (lane == 0) {
+    if (lane == 0 && sk == 0) {
         bv_s[warp] = best_v;
         bi_s[warp] = best_i;
     }
@@ -474,7 +503,7 @@ __global__ void __launch_bounds__(kRowThreads) batch_argmax_kernel(const BatchAr
     if (tid == 0) {
         float bv = bv_s[0];
         int bi = bi_s[0];
-        for (int w = 1; w < kRowThreads / 32; ++w)
+        for (int w = 1; w < kRowThreads / 32 && sk == 0; ++w)
             if (arg_better(bv_s[w], bi_s[w], bv, bi)) {
                 bv = bv_s[w];
                 bi = bi_s[w];
@@ -521,6 +550,10 @@ size_t batch_attention_smem_bytes(int hd, int group) {
 bool batch_attention_supported(int hd, int group) { return batt_fn(hd, group) != nullptr; }
 
 cudaError_t batch_kernels_init() {
+    cudaError_t ea = cudaFuncSetAttribute(reinterpret_cast<const void *>(batch_argmax_kernel),
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)((size_t)kBatchSampleVocabMax * 4 + (2 * kMaxTopK + kTopkScratchWords) * 4));
+    if (ea != cudaSuccess) return ea;
     for (int hd : {64, 128})
         for (int g : {1, 2, 4, 8}) {
             cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void *>(batt_fn(hd, g)),
@@ -564,7 +597,10 @@ cudaError_t launch_norm_split(const NormSplitArgs &a, int rows, cudaStream_t s, 
 
 cudaError_t launch_batch_argmax(const BatchArgmaxArgs &a, int B, cudaStream_t s, bool pdl) {
     void *args[1] = {const_cast<BatchArgmaxArgs *>(&a)};
-    return launch_ex(reinterpret_cast<const void *>(batch_argmax_kernel), dim3(B), dim3(kRowThreads), 0, s, pdl,
+    // shared memory for the sampling branch (the greedy branch uses none of it)
+    const size_t smem =
+        a.V <= kBatchSampleVocabMax ? (size_t)a.V * 4 + (size_t)(2 * kMaxTopK + kTopkScratchWords) * 4 : 0;
+    return launch_ex(reinterpret_cast<const void *>(batch_argmax_kernel), dim3(B), dim3(kRowThreads), smem, s, pdl,
                      args);
 }
 

@@ -326,9 +326,20 @@ struct NormSplitArgs {
 };
 cudaError_t launch_norm_split(const NormSplitArgs &a, int rows, cudaStream_t s, bool pdl = false);
 
-// Per stream b: penalty over its emitted set, EOS mask, argmax (lowest index on ties)
-// of logits[b]; ids and the next input token go through the control block; the
-// stream's position advances.
+// Sampling settings of a batch, in device memory (read by the step at run time, so a
+// captured step graph serves every setting): top_k 0 = greedy argmax.
+struct BatchSampling {
+    int top_k;
+    float temperature, top_p;
+    uint32_t seed_lo, seed_hi;
+    int pad[3];
+};
+constexpr int kBatchSampleVocabMax = 32768;   // logits a stream's selection keeps in shared memory
+
+// Per stream b: penalty over its emitted set, EOS mask, then the argmax (lowest index on
+// ties) of logits[b], or (sampling on) a draw among its top-k (stream b draws u at its
+// own counter from seed + b); ids and the next input token go through the control
+// block; the stream's position advances.
 struct BatchArgmaxArgs {
     const float *logits;           // [B][V]
     int V;
@@ -340,6 +351,8 @@ struct BatchArgmaxArgs {
     int32_t *tokens;               // [B] next input tokens
     int *pos;                      // [B]
     int *status;
+    const BatchSampling *samp;
+    int *drawn;                    // [B] ids each stream has drawn since it was set
 };
 cudaError_t launch_batch_argmax(const BatchArgmaxArgs &a, int B, cudaStream_t s, bool pdl = false);
 
