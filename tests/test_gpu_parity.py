@@ -316,10 +316,13 @@ def test_time_kernel_leaves_state_unchanged():
 @pytest.mark.parametrize("shape_name", ["tiny", "asr2", "talker2"])
 def test_persistent_step_equals_per_phase_kernels(shape_name, monkeypatch):
     """The persistent decode step and the per-phase kernels compute the same step with
-    fp32 sums in different orders (the persistent step splits each GEMV's K over its
-    warps and applies the RMSNorm scale after the dot products): equal ids, hidden
-    states within fp32 summation noise, caches equal up to the odd last-bit bf16
-    rounding of those sums."""
+    sums in different orders: the persistent step splits each GEMV's K over its warps,
+    applies the RMSNorm scale after the dot products and, on bf16 weights, takes the
+    dot products on the tensor cores with the fp32 input as two bf16 parts (16
+    significant bits, fp32 accumulation in the tensor cores' order).  Equal ids, hidden
+    states within 5e-4 relative L2 (a few ulp of bf16 input splitting and summation
+    order, compounded over the layers and steps), caches equal up to the bf16 rounding
+    flips those differences cause."""
     s = {"tiny": W.TINY, "asr2": W.scaled(W.ASR, n_layers=2, name="asr2"),
          "talker2": W.scaled(W.TALKER, n_layers=2, name="talker2")}[shape_name]
     w = W.model_weights(s)
@@ -329,15 +332,18 @@ def test_persistent_step_equals_per_phase_kernels(shape_name, monkeypatch):
     monkeypatch.setenv("QD_PER_PHASE", "1")
     b = _ids_logits(s, w, e, n)
     assert a[0] == b[0]
-    for ya, yb in zip(a[1], b[1]):
-        assert rel_l2(ya, yb) <= 1e-4
+    worst = max(rel_l2(ya, yb) for ya, yb in zip(a[1], b[1]))
+    print(f"{shape_name}: hidden rel_l2 max {worst:.3g}")
+    assert worst <= 5e-4, worst
     ka = _valid_kv(a[2], s, a[4], a[3])
     kb = _valid_kv(b[2], s, b[4], b[3])
     if s.bf16:
         ka, kb = _bf16_to_f32(ka), _bf16_to_f32(kb)
     else:
         ka, kb = ka.view(np.float32), kb.view(np.float32)
-    assert rel_l2(ka, kb) <= 1e-3
+    kv = rel_l2(ka, kb)
+    print(f"{shape_name}: kv rel_l2 {kv:.3g}")
+    assert kv <= 1e-3, kv
 
 
 @pytest.mark.parametrize("shape_name,prompt", [("asr2", "embeds"), ("talker2", "embeds"), ("asr2", "tokens")])

@@ -364,6 +364,92 @@ __device__ __forceinline__ bool kc_gemv(const Ring &R, uint32_t &sidx, int nrows
     return true;
 }
 
+// Row pitch in the ring of the bf16 layer phases: each row 16 bytes past a multiple of
+// 128, so the 8 rows a tensor-core fragment reads at one column fall in 8 different
+// 16-byte bank groups (conflict-free), and the rows of a stage that fit in a slot.
+__host__ __device__ constexpr uint32_t mma_pitch(int K) { return (uint32_t)(K * 2 + 16); }
+__host__ __device__ constexpr int mma_rps(int K) { return kSlotBytes / (int)mma_pitch(K); }
+
+// Producer: rows [0, nrows) of a row-major matrix into ring stages of `rps` rows, row
+// i of a stage at i * pitch (one bulk copy per row).
+__device__ __forceinline__ bool produce_rows_pitched(const Ring &R, uint32_t &sidx, const uint8_t *src, int nrows,
+                                                     uint32_t row_bytes, uint32_t pitch, int rps, uint64_t pol) {
+    for (int r = 0; r < nrows; r += rps) {
+        const int slot = (int)(sidx % (uint32_t)kStepStages);
+        const uint32_t use = sidx / (uint32_t)kStepStages;
+        if (use > 0 && !mbar_wait_bounded(&R.empty[slot], (use - 1) & 1)) return false;
+        const int n = nrows - r < rps ? nrows - r : rps;
+        mbar_arrive_expect_tx(&R.full[slot], n * row_bytes);
+        uint8_t *dst = R.base + (size_t)slot * kSlotBytes;
+        for (int i = 0; i < n; ++i)
+            bulk_copy_g2s(dst + (size_t)i * pitch, src + (size_t)(r + i) * row_bytes, row_bytes, &R.full[slot], pol);
+        ++sidx;
+    }
+    return true;
+}
+
+// d += a b for one m16n8k16 tile (bf16 operands, fp32 accumulation)
+__device__ __forceinline__ void mma_bf16(float &d0, float &d1, float &d2, float &d3, uint32_t a0, uint32_t a1,
+                                         uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The bf16 form of kc_gemv: the same partial sums (rows of the CTA's stages against
+// this warp's K-chunk [colw, colw + 16 nks)) from one m16n8k16 tensor-core product per
+// 16 rows x 16 columns.  The rows are the tile's M; its N holds the fp32 input as two
+// bf16 columns, x0 = bf16(x) and x1 = bf16(x - x0) (16 significant bits: |x - x0 - x1|
+// <= 2^-17 |x|), the other six columns zero, so row r's sum is D[r][0] + D[r][1]
+// (fp32 accumulation of exact bf16 x bf16 products).  xp: the warp's chunk as the two
+// bf16 parts in shared memory, part j at xp + j K / 16 words.  At batch 1 this is not
+// about tensor throughput: one instruction replaces the conversions, FMAs and shuffle
+// reduction of 16 rows x 16 columns, whose issue and latency bound this phase on the
+// CUDA cores.  (A third part, x - x0 - x1, makes the split exact; it measured 3 %
+// slower per step and left the difference to the CUDA-core step at the same ~1e-4,
+// which the tensor cores' accumulation sets.)
+__device__ __forceinline__ bool kc_gemv_mma(const Ring &R, uint32_t &sidx, int nrows, int rps, uint32_t pitch,
+                                            int colw, int nks, const uint32_t *xp, float *part) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int nst = (nrows + rps - 1) / rps;
+    const uint32_t *xb = xp + (g < 2 ? g : 0) * nks * 8;   // N column g < 2: part g
+    const bool live = g < 2;
+#pragma unroll 1
+    for (int st = 0; st < nst; ++st) {
+        const uint8_t *sb = stage_get(R, sidx + st);
+        if (!sb) return false;
+        const int n = min_c(rps, nrows - st * rps);
+#pragma unroll 1
+        for (int r0 = 0; r0 < n; r0 += 16) {
+            // rows past n re-read row n - 1 (results dropped below)
+            const int ra = min_c(r0 + g, n - 1), rb = min_c(r0 + g + 8, n - 1);
+            const uint8_t *pa = sb + (size_t)ra * pitch + (size_t)colw * 2 + t * 4;
+            const uint8_t *pb = sb + (size_t)rb * pitch + (size_t)colw * 2 + t * 4;
+            float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f, e0 = 0.f, e1 = 0.f, e2 = 0.f, e3 = 0.f;
+#pragma unroll 2
+            for (int ks = 0; ks < nks; ks += 2) {
+                // two independent accumulators: k-steps ks (c) and ks + 1 (e)
+                const uint32_t b0 = live ? xb[ks * 8 + t] : 0u, b1 = live ? xb[ks * 8 + t + 4] : 0u;
+                const uint32_t b2 = live ? xb[ks * 8 + 8 + t] : 0u, b3 = live ? xb[ks * 8 + 12 + t] : 0u;
+                const uint32_t *qa = reinterpret_cast<const uint32_t *>(pa + ks * 32);
+                const uint32_t *qb = reinterpret_cast<const uint32_t *>(pb + ks * 32);
+                mma_bf16(c0, c1, c2, c3, qa[0], qb[0], qa[4], qb[4], b0, b1);
+                mma_bf16(e0, e1, e2, e3, qa[8], qb[8], qa[12], qb[12], b2, b3);
+            }
+            // columns 0 and 1 sit in lane t = 0
+            if (t == 0) {
+                if (r0 + g < n) part[st * rps + r0 + g] = (c0 + c1) + (e0 + e1);
+                if (r0 + g + 8 < n) part[st * rps + r0 + g + 8] = (c2 + c3) + (e2 + e3);
+            }
+        }
+        stage_put(R, sidx + st, lane);
+    }
+    sidx += nst;
+    return true;
+}
+
 // Sum over the consumer warps, in warp order, of entry i of a [kNW][ps] table.
 __device__ __forceinline__ float warp_parts(const float *tab, int ps, int i) {
     float v = 0.f;
@@ -602,8 +688,15 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
             bool ok = true;
             for (int l = 0; l < a.n_layers && ok && !ctl[0]; ++l) {
                 const LayerDev &Ld = a.layers[l];
-                ok = ok && produce_rows(R, sidx, reinterpret_cast<const uint8_t *>(Ld.w_qkv) + (size_t)r0_qkv * rb_h,
-                                        n_qkv, rb_h, a.rps_h, pw);
+                // bf16 layer rows at the tensor-core pitch; fp32 rows packed
+                auto rows = [&](const void *w, int r0, int n, uint32_t rb, int K, int rps) {
+                    const uint8_t *src = reinterpret_cast<const uint8_t *>(w) + (size_t)r0 * rb;
+                    if constexpr (sizeof(WT) == 2)
+                        return produce_rows_pitched(R, sidx, src, n, rb, mma_pitch(K), mma_rps(K), pw);
+                    else
+                        return produce_rows(R, sidx, src, n, rb, rps, pw);
+                };
+                ok = ok && rows(Ld.w_qkv, r0_qkv, n_qkv, rb_h, KH, a.rps_h);
                 if (has_item) {
                     // K and V rows [j0, j0 + n_old) of this CTA's group: written by earlier steps
                     const uint8_t *kb = reinterpret_cast<const uint8_t *>(a.kv) + (size_t)l * layer_kv +
@@ -612,12 +705,9 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
                     ok = ok && produce_block(R, sidx, kb, bytes, pf);
                     ok = ok && produce_block(R, sidx, kb + layer_kv / 2, bytes, pf);
                 }
-                ok = ok && produce_rows(R, sidx, reinterpret_cast<const uint8_t *>(Ld.w_o) + (size_t)r0_x * rb_q, n_x,
-                                        rb_q, a.rps_q, pw);
-                ok = ok && produce_rows(R, sidx, reinterpret_cast<const uint8_t *>(Ld.w_gu) + (size_t)r0_gu * rb_h,
-                                        n_gu, rb_h, a.rps_h, pw);
-                ok = ok && produce_rows(R, sidx, reinterpret_cast<const uint8_t *>(Ld.w_d) + (size_t)r0_x * rb_f, n_x,
-                                        rb_f, a.rps_f, pw);
+                ok = ok && rows(Ld.w_o, r0_x, n_x, rb_q, KQ, a.rps_q);
+                ok = ok && rows(Ld.w_gu, r0_gu, n_gu, rb_h, KH, a.rps_h);
+                ok = ok && rows(Ld.w_d, r0_x, n_x, rb_f, KF, a.rps_f);
             }
             if (ok && a.with_head && !ctl[0]) {
                 const uint8_t *Wh = reinterpret_cast<const uint8_t *>(a.heads[a.st->head_idx]);
@@ -831,15 +921,16 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
             const float *gam;
             int K, nrows, rps;
             uint32_t rbytes;
+            constexpr bool kMma = sizeof(WT) == 2;
             if (ph == 0) {
                 src = l ? a.tg + (size_t)(l - 1) * a.tg_stride + a.tg_xe : nullptr;
-                gam = Ld.attn_norm; K = KH; nrows = n_qkv; rps = a.rps_h; rbytes = rb_h;
+                gam = Ld.attn_norm; K = KH; nrows = n_qkv; rps = kMma ? mma_rps(KH) : a.rps_h; rbytes = rb_h;
             } else if (ph == 1) {
-                src = T + a.tg_att; gam = nullptr; K = KQ; nrows = n_x; rps = a.rps_q; rbytes = rb_q;
+                src = T + a.tg_att; gam = nullptr; K = KQ; nrows = n_x; rps = kMma ? mma_rps(KQ) : a.rps_q; rbytes = rb_q;
             } else if (ph == 2) {
-                src = T + a.tg_xc; gam = Ld.mlp_norm; K = KH; nrows = n_gu; rps = a.rps_h; rbytes = rb_h;
+                src = T + a.tg_xc; gam = Ld.mlp_norm; K = KH; nrows = n_gu; rps = kMma ? mma_rps(KH) : a.rps_h; rbytes = rb_h;
             } else {
-                src = T + a.tg_act; gam = nullptr; K = KF; nrows = n_x; rps = a.rps_f; rbytes = rb_f;
+                src = T + a.tg_act; gam = nullptr; K = KF; nrows = n_x; rps = kMma ? mma_rps(KF) : a.rps_f; rbytes = rb_f;
             }
             const int nc = K / (256 * EL);          // column chunks of 32 x EL per warp
             const int colw = warp * (K / kNW);       // this warp's first column
@@ -851,16 +942,21 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
                     x[cc][e] = 0.f;
                     gv[cc][e] = 1.f;
                 }
+            // lane-contiguous order: element (cc, e) of this lane is column
+            // colw + cc * 32 EL + e * 32 + lane, so each load instruction of the warp
+            // reads 32 consecutive words (every L2 sector once per poll)
             if (gam)
 #pragma unroll
                 for (int cc = 0; cc < NCMAX; ++cc)
-                    if (cc < nc) load_elems<float, EL>(gam + colw + cc * 32 * EL + lane * EL, gv[cc]);
+#pragma unroll
+                    for (int e = 0; e < EL; ++e)
+                        if (cc < nc) gv[cc][e] = gam[colw + cc * 32 * EL + e * 32 + lane];
             bool okw = true;
             if (src) {
                 // this lane's words of every chunk, in one batch of polls
                 float wv[NCMAX * EL];
                 okw = poll_batch<NCMAX * EL>(nc * EL, seq,
-                                             [&](int i) { return src + colw + (i / EL) * 32 * EL + lane * EL + i % EL; },
+                                             [&](int i) { return src + colw + i * 32 + lane; },
                                              wv);
 #pragma unroll
                 for (int cc = 0; cc < NCMAX; ++cc)
@@ -871,7 +967,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
                     for (int cc = 0; cc < NCMAX; ++cc)
 #pragma unroll
                         for (int e = 0; e < EL; ++e)
-                            if (cc < nc) a.tap_hidden[(size_t)l * hidden + colw + cc * 32 * EL + lane * EL + e] = x[cc][e];
+                            if (cc < nc) a.tap_hidden[(size_t)l * hidden + colw + cc * 32 * EL + e * 32 + lane] = x[cc][e];
             } else {
                 // the step input: thread 0 resolves the step description; CTA 0 records
                 // the token in the emitted set and publishes that with a release flag
@@ -902,16 +998,16 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
                 const bool bad = misc_i[2] != 0;
 #pragma unroll
                 for (int cc = 0; cc < NCMAX; ++cc)
-                    if (cc < nc) {
-                        const int col = colw + cc * 32 * EL + lane * EL;
-                        input_cols<WT, EL>(a.in, hidden, mode, tok, p, bad, col, x[cc]);
-                        if (blockIdx.x == 0)
+                    if (cc < nc)
 #pragma unroll
-                            for (int e = 0; e < EL; ++e) {
-                                a.x[col + e] = x[cc][e];
-                                if (a.tap_hidden) a.tap_hidden[col + e] = x[cc][e];
+                        for (int e = 0; e < EL; ++e) {
+                            const int col = colw + cc * 32 * EL + e * 32 + lane;
+                            input_cols<WT, 1>(a.in, hidden, mode, tok, p, bad, col, &x[cc][e]);
+                            if (blockIdx.x == 0) {
+                                a.x[col] = x[cc][e];
+                                if (a.tap_hidden) a.tap_hidden[col] = x[cc][e];
                             }
-                    }
+                        }
                 if (tid < n_x) {
                     float xo;
                     input_cols<WT, 1>(a.in, hidden, mode, tok, p, bad, r0_x + tid, &xo);
@@ -921,18 +1017,40 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
             okw = __all_sync(0xffffffffu, okw);
             float ss = 0.f;
             float *xw = xs + (size_t)warp * XSW;      // this warp's slice of the input, times gamma
-#pragma unroll
-            for (int cc = 0; cc < NCMAX; ++cc)
-                if (cc < nc) {
-#pragma unroll
-                    for (int e = 0; e < EL; ++e) {
-                        ss = fmaf(x[cc][e], x[cc][e], ss);
-                        xw[cc * 32 * EL + lane * EL + e] = x[cc][e] * gv[cc][e];
-                    }
-                }
-            __syncwarp();
             float *part = kc_part + buf * kNW * PS;
-            if (okw) okw = kc_gemv<WT, EL>(R, sidx, nrows, rps, rbytes, colw, nc, xw, part + warp * PS);
+            if constexpr (kMma) {
+                // as two bf16 parts (the slice's K / 8 values twice: the same bytes as fp32)
+                __nv_bfloat16 *x0 = reinterpret_cast<__nv_bfloat16 *>(xw), *x1 = x0 + K / kNW;
+#pragma unroll
+                for (int cc = 0; cc < NCMAX; ++cc)
+                    if (cc < nc) {
+#pragma unroll
+                        for (int e = 0; e < EL; ++e) {
+                            ss = fmaf(x[cc][e], x[cc][e], ss);
+                            const float v = x[cc][e] * gv[cc][e];
+                            const __nv_bfloat16 h = __float2bfloat16_rn(v);
+                            const int i = cc * 32 * EL + e * 32 + lane;
+                            x0[i] = h;
+                            x1[i] = __float2bfloat16_rn(v - __bfloat162float(h));
+                        }
+                    }
+                __syncwarp();
+                if (okw)
+                    okw = kc_gemv_mma(R, sidx, nrows, rps, rbytes + 16, colw, K / (kNW * 16),
+                                      reinterpret_cast<const uint32_t *>(x0), part + warp * PS);
+            } else {
+#pragma unroll
+                for (int cc = 0; cc < NCMAX; ++cc)
+                    if (cc < nc) {
+#pragma unroll
+                        for (int e = 0; e < EL; ++e) {
+                            ss = fmaf(x[cc][e], x[cc][e], ss);
+                            xw[cc * 32 * EL + e * 32 + lane] = x[cc][e] * gv[cc][e];
+                        }
+                    }
+                __syncwarp();
+                if (okw) okw = kc_gemv<WT, EL>(R, sidx, nrows, rps, rbytes, colw, nc, xw, part + warp * PS);
+            }
             if (gam) {
                 ss = warp_sum(ss);
                 if (lane == 0) kc_ss[buf * kNW + warp] = ss;
