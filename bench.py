@@ -39,8 +39,8 @@ METRIC = "decode tokens/s at 1 GB300; per-step HBM GB/s as fraction of peak"
 # (profiles/decode_step_kernel_asr.md, profiles/decode_step_kernel_talker.md), at
 # attended length L, for the kernel sources
 # with this digest; null in the JSON line once the sources differ.
-_STEP_TRAFFIC = {"asr": {"digest": "6c77cc52b34c0155", "bytes": 224761856 + 3463168, "L": 116},
-                 "talker": {"digest": "186e08de67105744", "bytes": 897147904 + 4611840, "L": 70}}
+_STEP_TRAFFIC = {"asr": {"digest": "f161bc38e9db3cac", "bytes": 224888320 + 3283200, "L": 116},
+                 "talker": {"digest": "f161bc38e9db3cac", "bytes": 896986880 + 4575488, "L": 70}}
 _STEP_SOURCES = ("decode_persistent.cu", "decode_common.cuh", "qd_device.cuh")
 # DRAM bytes of one batch_attn_kernel launch (profiles/batch_attn_kernel_batch64.md) at
 # the initial lengths + 3, for the kernel sources with this digest.

@@ -15,7 +15,9 @@ from typing import Dict, Optional, Sequence
 import numpy as np
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libqd.so")
+# QD_LIBRARY names another build of the same library (the phase-timeline build of
+# step_timeline.py); by default the in-tree libqd.so.
+LIB_PATH = os.environ.get("QD_LIBRARY") or os.path.join(_PKG, "libqd.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build the CUDA library first "

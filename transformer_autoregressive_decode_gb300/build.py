@@ -37,18 +37,22 @@ def _deps():
         glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    """Compile every CUDA source for sm_103a and link ``libqd.so``; returns its path."""
+def build(force: bool = False, verbose: bool = False, extra_flags=None, lib=None, objdir=None) -> str:
+    """Compile every CUDA source for sm_103a and link ``libqd.so`` (or ``lib``, with its
+    objects under ``objdir``: a variant build such as the phase-timeline one); returns
+    the library's path."""
+    LIB_ = lib or LIB
+    OBJDIR_ = objdir or OBJDIR
     newest = max(os.path.getmtime(p) for p in _deps())
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= newest and not extra_flags:
-        return LIB
-    os.makedirs(OBJDIR, exist_ok=True)
+    if not force and os.path.exists(LIB_) and os.path.getmtime(LIB_) >= newest and not extra_flags:
+        return LIB_
+    os.makedirs(OBJDIR_, exist_ok=True)
     nvcc = _nvcc()
     flags = NVCC_FLAGS + list(extra_flags or [])
     procs = []
     objs = []
     for src in sources():
-        obj = os.path.join(OBJDIR, os.path.basename(src) + ".o")
+        obj = os.path.join(OBJDIR_, os.path.basename(src) + ".o")
         objs.append(obj)
         cmd = [nvcc] + ARCH + flags + ["-c", src, "-o", obj]
         if verbose:
@@ -64,10 +68,10 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     if failed:
         msg = "\n".join(" ".join(c) + "\n" + o for c, o in failed)
         raise RuntimeError("nvcc failed:\n" + msg)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = LIB_ + f".tmp{os.getpid()}"
     subprocess.check_call([nvcc] + ARCH + ["-shared", "-o", tmp] + objs)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, LIB_)
+    return LIB_
 
 
 if __name__ == "__main__":

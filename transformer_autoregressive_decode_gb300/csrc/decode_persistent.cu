@@ -44,6 +44,27 @@
 
 namespace qd {
 
+// Phase timeline (built only with -DQD_STEP_TRACE, by step_timeline.py): thread 0 of
+// every CTA records %globaltimer at the phase boundaries of one layer.  Slots: 4 ph + 0
+// phase start, + 1 input gathered, + 2 GEMV done, + 3 rows published (ph 0 = QKV,
+// 1 = O-projection, 2 = gate/up, 3 = down); 16 q/k/v polled, 17 attention done,
+// 18 split partial published, 19 merged output published; 22 next layer's input
+// gathered.  The product build compiles none of it.
+#ifdef QD_STEP_TRACE
+__device__ unsigned long long g_step_trace[kStepTraceCtas][kStepTraceSlots];
+__device__ int g_step_trace_layer = 3;
+#define QD_TS(l, k)                                                                                     \
+    do {                                                                                                \
+        if ((l) == g_step_trace_layer && threadIdx.x == 0 && blockIdx.x < kStepTraceCtas) {             \
+            unsigned long long t_;                                                                      \
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                                      \
+            g_step_trace[blockIdx.x][(k)] = t_;                                                         \
+        }                                                                                               \
+    } while (0)
+#else
+#define QD_TS(l, k) do { } while (0)
+#endif
+
 constexpr int kNW = kConsumerWarps;          // consumer warps
 constexpr int kNC = kNW * 32;                // consumer threads
 constexpr int kGMax = kStepGroupMax;         // q heads per kv head handled by the step kernel
@@ -766,6 +787,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
         // D act = silu(Wg x^) * (Wu x^), x^ = RMSNorm(x); E x += Wd act.
 #pragma unroll 1
         for (int ph = 0; ph < 4 && ok; ++ph) {
+            QD_TS(l, ph * 4);
             if (ph == 1) {
                 // ---- B: attention of this CTA's (group, split), then its share of the merge
                 bool okb = true;
@@ -791,6 +813,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
                                               },
                                               wv);
                 okw = __all_sync(0xffffffffu, okw);
+                QD_TS(l, 16);
                 float q[1][EH], kr[EH], vr[EH];
 #pragma unroll
                 for (int e = 0; e < EH; ++e) {
@@ -846,6 +869,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
                 sidx += 2;
                 ok = !named_sync_or(1, kNC, !okw);
                 if (!ok) { okb = false; break; }
+                QD_TS(l, 17);
                 // the split's partial, the warps of each head merged in order: its
                 // normalised output o / l and, per head, its log-sum-exp m + log(l)
                 const int GD = G * HD;
@@ -874,6 +898,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
                 // splits, a power of two) takes one column, lane s its split s; each thread
                 // takes two (column, split) pairs, polled in one batch, and the group reduces
                 // them with shuffles.
+                QD_TS(l, 18);
                 const int d0 = is * GD / nsplit, d1 = (is + 1) * GD / nsplit;
                 const int LP = nsplit <= 1 ? 1 : (nsplit <= 2 ? 2 : (nsplit <= 4 ? 4 : 8));
                 const uint64_t *Gpo = T + a.tg_po + (size_t)ig * kAttnMaxSplits * GD;
@@ -911,6 +936,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
                     }
                 }
                 if (!okm) ok = false;
+                QD_TS(l, 19);
             }
 
                 } while (false);
@@ -1015,6 +1041,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
                 }
             }
             okw = __all_sync(0xffffffffu, okw);
+            QD_TS(l, ph * 4 + 1);
+            if (ph == 0) QD_TS(l - 1, 22);
             float ss = 0.f;
             float *xw = xs + (size_t)warp * XSW;      // this warp's slice of the input, times gamma
             float *part = kc_part + buf * kNW * PS;
@@ -1056,6 +1084,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
                 if (lane == 0) kc_ss[buf * kNW + warp] = ss;
             }
             ok = !named_sync_or(1, kNC, !okw);
+            QD_TS(l, ph * 4 + 2);
             if (!ok) break;
             // the phase's rows: thread i sums row i over the warps, in warp order
             if (ph == 0) {
@@ -1075,6 +1104,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
                 a.x[r0_x + tid] = xn;
                 st_tag(T + (ph == 1 ? a.tg_xc : a.tg_xe) + r0_x + tid, xn, seq);
             }
+            QD_TS(l, ph * 4 + 3);
             buf ^= 1;
         }
     }
@@ -1318,3 +1348,18 @@ cudaError_t launch_persistent(bool bf16, int hd, int hidden, int q_dim, int ffn,
 }
 
 }  // namespace qd
+
+#ifdef QD_STEP_TRACE
+// Timeline readers of the traced build (not declared in include/qd.h: the product
+// library has no such symbols).
+extern "C" int qd_step_trace_read(unsigned long long *host, int slots) {
+    if (slots != qd::kStepTraceCtas * qd::kStepTraceSlots) return -1;
+    return (int)cudaMemcpyFromSymbol(host, qd::g_step_trace, sizeof(unsigned long long) * slots);
+}
+extern "C" int qd_step_trace_reset(int layer) {
+    static unsigned long long zero[qd::kStepTraceCtas * qd::kStepTraceSlots];
+    cudaError_t e = cudaMemcpyToSymbol(qd::g_step_trace, zero, sizeof(zero));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(qd::g_step_trace_layer, &layer, sizeof(int));
+    return (int)e;
+}
+#endif

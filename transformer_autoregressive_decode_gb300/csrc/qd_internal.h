@@ -162,6 +162,9 @@ constexpr int kStepRowsMax = 64;
 constexpr int kStepRingStages = 6;
 constexpr int kStepMinSms = 148;
 constexpr int kStepGroupMax = 2;
+// Phase timeline of the traced build: CTAs and stamp slots recorded.
+constexpr int kStepTraceCtas = 160;
+constexpr int kStepTraceSlots = 24;
 
 // Dynamic shared memory ceiling of the persistent step kernel.  The kernel's
 // max-dynamic-smem attribute is set to this once for every instantiation, so
