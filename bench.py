@@ -421,15 +421,39 @@ def gpu_line(args, workload, ctx):
         tconv_ms = timed(lambda: qd.qd_conv_transpose1d_causal(tx, tw, None, stride=4))
         sm_mhz = (clk or {}).get("sm_mhz") or 2070.0
         alu_peak = 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
-        conv_tf = 2 * 512 * 512 * 7 * 4096 / (conv_ms / 1e3) / 1e12
-        tconv_tf = 2 * 512 * 256 * 2 * 1024 * 4 / (tconv_ms / 1e3) / 1e12
+        conv_flop = 2 * 512 * 512 * 7 * 4096
+        tconv_flop = 2 * 512 * 256 * 2 * 1024 * 4
+        conv_tf = conv_flop / (conv_ms / 1e3) / 1e12
+        tconv_tf = tconv_flop / (tconv_ms / 1e3) / 1e12
+        # the tensor-core forms (bf16 weights, x as bf16 hi + lo: two products per
+        # k-step, counted once): weight packing, signal transpose and the GEMMs, 20 runs
+        # back to back between CUDA events (the inputs, 15 MB, stay in L2)
+        torch.cuda.nvtx.range_push("codec_conv_tc")
+        _, conv_tc_ms = qd.qd_conv1d_causal_tc(cx, cw, None, dilation=1, time_reps=20)
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.nvtx.range_push("codec_tconv_tc")
+        _, tconv_tc_ms = qd.qd_conv_transpose1d_causal_tc(tx, tw, None, stride=4, time_reps=20)
+        torch.cuda.nvtx.range_pop()
+        _, bf16_peak, peak_src = _peaks()
+        conv_tc_tf = conv_flop / (conv_tc_ms / 1e3) / 1e12
+        tconv_tc_tf = tconv_flop / (tconv_tc_ms / 1e3) / 1e12
         codec = {"conv1d_causal": {"shape": "512 -> 512 channels, K 7, 4096 frames", "ms": conv_ms,
                                    "tflops": conv_tf, "frac": conv_tf / alu_peak},
                  "conv_transpose1d_causal": {"shape": "512 -> 256 channels, stride 4, 1024 -> 4096 frames",
                                              "ms": tconv_ms, "tflops": tconv_tf, "frac": tconv_tf / alu_peak},
                  "bound": "alu", "peak_tflops": alu_peak,
                  "note": "fp32 CUDA-core kernels (parity first); peak = 152 SMs x 128 fp32 lanes x 2 flops x SM "
-                         "clock; median of 5 after a warm launch, L2 flushed before each"}
+                         "clock; median of 5 after a warm launch, L2 flushed before each",
+                 "tensor_cores": {
+                     "conv1d_causal_tc": {"ms": conv_tc_ms, "tflops": conv_tc_tf, "frac": conv_tc_tf / bf16_peak,
+                                          "speedup": conv_ms / conv_tc_ms},
+                     "conv_transpose1d_causal_tc": {"ms": tconv_tc_ms, "tflops": tconv_tc_tf,
+                                                    "frac": tconv_tc_tf / bf16_peak,
+                                                    "speedup": tconv_ms / tconv_tc_ms},
+                     "bound": "tensor", "peak_tflops": bf16_peak, "peak_source": peak_src,
+                     "note": "qd_*_tc: shifted-tap tcgen05 GEMMs (one per transposed-convolution phase) with the "
+                             "bias in the epilogue; the time includes packing the weights to bf16 and the signal "
+                             "to time-major hi/lo parts; mean of 20 back-to-back runs (inputs L2-resident)"}}
         del flush, cx, cw, tw, tx
 
     # end to end through the public API with host buffers: the prompt embeddings

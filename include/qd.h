@@ -253,6 +253,33 @@ qd_status qd_conv1d_causal(const float *x_dev, int Cin, int T, const float *w_de
 qd_status qd_conv_transpose1d_causal(const float *x_dev, int Cin, int T, const float *w_dev, const float *bias_dev,
                                      int Cout, int stride, float *y_dev, void *cuda_stream);
 
+/* qd_conv1d_causal_tc -- qd_conv1d_causal's convolution on the tensor cores: the GEMM
+ * of qd_gemm_bf16 over the time-major signal with one weight slab per tap, tap k
+ * reading the frames shifted by (K-1-k) * dilation ("qwen3-tts-hip OPTIMIZATION_LOG",
+ * codec entries).  Same arguments and layouts as qd_conv1d_causal (x DEVICE fp32
+ * [Cin][T], W DEVICE fp32 [Cout][Cin][K], bias DEVICE fp32 [Cout] or NULL, y DEVICE
+ * fp32 [Cout][T]); the weights are rounded to bf16 (round to nearest even) and x is
+ * carried as bf16 hi + lo parts (16 significant bits), fp32 accumulation.  Any Cin,
+ * Cout (padded internally to 64 / 128), K <= 64.  Allocates its scratch (about
+ * 2 K Cout Cin + 4 T Cin bytes), runs on cuda_stream and synchronises it.  When avg_ms
+ * (HOST) is non-NULL the whole convolution (weight packing, signal transpose, GEMM) is
+ * then run `reps` more times between CUDA events and its mean duration written there.
+ * Errors: QD_EINVAL, QD_EUNSUPPORTED, QD_ENOMEM, QD_ECUDA, QD_EDEVICE (a bounded wait
+ * expired). */
+qd_status qd_conv1d_causal_tc(const float *x_dev, int Cin, int T, const float *w_dev, const float *bias_dev, int Cout,
+                              int K, int dilation, float *y_dev, void *cuda_stream, int reps, float *avg_ms);
+
+/* qd_conv_transpose1d_causal_tc -- qd_conv_transpose1d_causal's convolution on the
+ * tensor cores in the page's per-phase form ("qwen3-tts-hip OPTIMIZATION_LOG",
+ * transposed-convolution entry): for each phase p < stride one GEMM with two taps,
+ * slab p of the weights on frame t and slab p + stride on frame t - 1, written to
+ * samples t * stride + p.  Same arguments and layouts as qd_conv_transpose1d_causal
+ * (W DEVICE fp32 [Cin][Cout][2 * stride]); precision, scratch, synchronisation, timing
+ * and errors as qd_conv1d_causal_tc.  stride <= 64. */
+qd_status qd_conv_transpose1d_causal_tc(const float *x_dev, int Cin, int T, const float *w_dev,
+                                        const float *bias_dev, int Cout, int stride, float *y_dev, void *cuda_stream,
+                                        int reps, float *avg_ms);
+
 /* qd_gemm_bf16 -- the batched paths' tensor-core contraction on its own (a check
  * and measurement tap): out[t][r] = sum_k W[r][k] * x[t][k] for W (DEVICE bf16
  * [R, K] row-major, 16-byte aligned) and x (DEVICE fp32 [T, K] row-major), with x

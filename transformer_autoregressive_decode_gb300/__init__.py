@@ -37,7 +37,8 @@ EXPORTS = ("qd_create", "qd_destroy", "qd_reset", "qd_prefill", "qd_prefill_mrop
            "qd_get_emitted", "qd_get_pos", "qd_get_launch_count", "qd_time_kernel", "qd_last_error",
            "qd_status_string", "qd_head_argmax_noalloc", "qd_frame_create", "qd_frame_destroy",
            "qd_frame_generate", "qd_frame_set_graphs", "qd_gemm_bf16", "qd_quantize_q8", "qd_gemv_q8",
-           "qd_conv1d_causal", "qd_conv_transpose1d_causal", "qd_batch_create", "qd_batch_destroy",
+           "qd_conv1d_causal", "qd_conv_transpose1d_causal", "qd_conv1d_causal_tc",
+           "qd_conv_transpose1d_causal_tc", "qd_batch_create", "qd_batch_destroy",
            "qd_batch_set_stream", "qd_batch_decode", "qd_batch_sync", "qd_batch_get_logits", "qd_batch_copy_kv",
            "qd_batch_get_pos", "qd_batch_get_launch_count", "qd_batch_set_graphs", "qd_batch_time_kernel", "qd_batch_prefill",
            "qd_batch_set_sampling")
@@ -94,6 +95,8 @@ _SIGS = {
     "qd_quantize_q8": ([_vp, _i32, _i32, _i32, _vp, _vp, _vp], _i32),
     "qd_conv1d_causal": ([_vp, _i32, _i32, _vp, _vp, _i32, _i32, _i32, _vp, _vp], _i32),
     "qd_conv_transpose1d_causal": ([_vp, _i32, _i32, _vp, _vp, _i32, _i32, _vp, _vp], _i32),
+    "qd_conv1d_causal_tc": ([_vp, _i32, _i32, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _i32, _vp], _i32),
+    "qd_conv_transpose1d_causal_tc": ([_vp, _i32, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _i32, _vp], _i32),
     "qd_gemv_q8": ([_vp, _vp, _vp, _vp, _i32, _i32, _vp, _i32, _P(ctypes.c_float)], _i32),
     "qd_batch_create": ([_vp, _i32, _i32, _P(_vp)], _i32),
     "qd_batch_destroy": ([_vp], _i32),
@@ -526,3 +529,38 @@ def qd_conv_transpose1d_causal(x_dev, w_dev, bias_dev=None, stride: int = 2, str
     if st != QD_OK:
         raise QDError(st, "qd_conv_transpose1d_causal failed")
     return y
+
+
+def qd_conv1d_causal_tc(x_dev, w_dev, bias_dev=None, dilation: int = 1, stream=None, time_reps: int = 0):
+    """qd_conv1d_causal on the tensor cores (weights rounded to bf16, x as bf16 hi + lo);
+    returns y [Cout, T], and with time_reps > 0 also the mean ms of that many runs."""
+    import torch
+    Cin, T = x_dev.shape
+    Cout, _, K = w_dev.shape
+    y = torch.empty((Cout, T), dtype=torch.float32, device=x_dev.device)
+    s = (stream or torch.cuda.current_stream()).cuda_stream
+    ms = ctypes.c_float(0.0)
+    st = _lib.qd_conv1d_causal_tc(_ptr(x_dev), Cin, T, _ptr(w_dev), _ptr(bias_dev), Cout, K, int(dilation), _ptr(y),
+                                  s, int(time_reps), ctypes.byref(ms) if time_reps > 0 else None)
+    if st != QD_OK:
+        raise QDError(st, "qd_conv1d_causal_tc failed")
+    return (y, ms.value) if time_reps > 0 else y
+
+
+def qd_conv_transpose1d_causal_tc(x_dev, w_dev, bias_dev=None, stride: int = 2, stream=None, time_reps: int = 0):
+    """qd_conv_transpose1d_causal on the tensor cores, per output phase (weights rounded to
+    bf16, x as bf16 hi + lo); returns y [Cout, T * stride], and with time_reps > 0 also
+    the mean ms of that many runs."""
+    import torch
+    Cin, T = x_dev.shape
+    _, Cout, K = w_dev.shape
+    if K != 2 * stride:
+        raise ValueError("kernel must be 2 * stride")
+    y = torch.empty((Cout, T * stride), dtype=torch.float32, device=x_dev.device)
+    s = (stream or torch.cuda.current_stream()).cuda_stream
+    ms = ctypes.c_float(0.0)
+    st = _lib.qd_conv_transpose1d_causal_tc(_ptr(x_dev), Cin, T, _ptr(w_dev), _ptr(bias_dev), Cout, int(stride),
+                                            _ptr(y), s, int(time_reps), ctypes.byref(ms) if time_reps > 0 else None)
+    if st != QD_OK:
+        raise QDError(st, "qd_conv_transpose1d_causal_tc failed")
+    return (y, ms.value) if time_reps > 0 else y

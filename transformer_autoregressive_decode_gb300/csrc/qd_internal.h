@@ -239,6 +239,8 @@ enum TcEpilogue : int {
     TC_RESIDUAL = 1,   // out[t][r] += acc
     TC_SWIGLU = 2,     // rows (2i, 2i+1) = (gate_i, up_i): act[t][i] = silu(gate) * up,
                        // written as bf16 hi/lo parts (and fp32 when out != null)
+    TC_STORE_RT = 3,   // out[r * ldo + t * ldt] = acc + bias[r] for rows r < r_valid
+                       // (channel-major outputs of the codec convolutions)
 };
 
 struct TcGemmArgs {
@@ -250,6 +252,14 @@ struct TcGemmArgs {
     float *partial;                // split-K partial sums [units][BN][128], or null when splits == 1
     int *tile_counter;             // [row tiles x token tiles][2] (arrive, depart), zero at rest
     int *status;                   // DEV_ERR_* bits
+    // Shifted taps (the codec convolutions; taps <= 1 is the plain product):
+    // out[t][r] = sum_j sum_k W[slab(j)][r][k] * x[t - shift(j)][k], j < taps, with
+    // slab(j) = w_slab0 + j w_slab_step, shift(j) = x_shift0 + j x_shift_step, rows of x
+    // outside [0, T) read as zero; W then has w_rows = slabs x R rows.
+    int taps, w_slab0, w_slab_step, x_shift0, x_shift_step, w_rows;
+    int ldt;                       // TC_STORE_RT: token stride of out
+    int r_valid;                   // TC_STORE_RT: rows written
+    const float *bias;             // TC_STORE_RT: [r_valid] or null
 };
 
 struct TcGemmPlan {

@@ -165,6 +165,8 @@ __device__ __forceinline__ Unit unit_of(int u, int splits, int tok_tiles, int KC
 __device__ __forceinline__ void epi_apply(const TcGemmArgs &a, int t, int r, float v, int lane) {
     if (a.mode == TC_STORE) {
         a.out[(size_t)t * a.ldo + r] = v;
+    } else if (a.mode == TC_STORE_RT) {
+        if (r < a.r_valid) a.out[(size_t)r * a.ldo + (size_t)t * a.ldt] = v + (a.bias ? a.bias[r] : 0.f);
     } else if (a.mode == TC_RESIDUAL) {
         float *p = a.out + (size_t)t * a.ldo + r;
         *p = *p + v;
@@ -201,6 +203,17 @@ __device__ __forceinline__ void epi_apply_n(const TcGemmArgs &a, int t0, int r, 
     }
 }
 
+// TMA coordinates of reduction chunk kc (tap kc / KCt, columns of chunk kc % KCt) for
+// the unit's row tile rt and token tile nt: the weight tile (wx, wy) and the token
+// tile (xx, xy); xy may be negative or past T (those rows load as zero).
+__device__ __forceinline__ void chunk_xy(const TcGemmArgs &a, int KCt, int kc, int rt, int nt, int bn, int &wx,
+                                         int &wy, int &xy) {
+    const int tap = kc / KCt, kk = kc - tap * KCt;
+    wx = kk * kBK;
+    wy = (a.w_slab0 + tap * a.w_slab_step) * a.R + rt * kBM;
+    xy = nt * bn - (a.x_shift0 + tap * a.x_shift_step);
+}
+
 template <int BN>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_xh,
@@ -219,7 +232,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int *is_last = reinterpret_cast<int *>(tmem_slot + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int KC = a.K / kBK;
+    const int KCt = a.K / kBK;          // chunks of one tap
+    const int KC = KCt * a.taps;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -256,15 +270,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const Unit x0 = unit_of(blockIdx.x, splits, tok_tiles, KC);
                 pre = x0.k1 - x0.k0 < C::kStages ? x0.k1 - x0.k0 : C::kStages;
                 for (int i = 0; i < pre; ++i) {
+                    int wx, wy, xy;
+                    chunk_xy(a, KCt, x0.k0 + i, x0.rt, x0.nt, BN, wx, wy, xy);
                     mbar_arrive_expect_tx(&full[i], C::kStage);
-                    tma_load_2d(sm + (size_t)i * C::kStage, &tm_w, (x0.k0 + i) * kBK, x0.rt * kBM, &full[i]);
+                    tma_load_2d(sm + (size_t)i * C::kStage, &tm_w, wx, wy, &full[i]);
                 }
                 pdl_wait();
                 pdl_launch_dependents();
                 for (int i = 0; i < pre; ++i) {
+                    int wx, wy, xy;
+                    chunk_xy(a, KCt, x0.k0 + i, x0.rt, x0.nt, BN, wx, wy, xy);
                     uint8_t *st = sm + (size_t)i * C::kStage;
-                    tma_load_2d(st + kTileA, &tm_xh, (x0.k0 + i) * kBK, x0.nt * BN, &full[i]);
-                    tma_load_2d(st + kTileA + C::kTileB, &tm_xl, (x0.k0 + i) * kBK, x0.nt * BN, &full[i]);
+                    tma_load_2d(st + kTileA, &tm_xh, wx, xy, &full[i]);
+                    tma_load_2d(st + kTileA + C::kTileB, &tm_xl, wx, xy, &full[i]);
                 }
                 armed = (1u << pre) - 1u;
                 stage = pre % C::kStages;
@@ -281,11 +299,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         ok = false;
                         break;
                     }
+                    int wx, wy, xy;
+                    chunk_xy(a, KCt, kc, x.rt, x.nt, BN, wx, wy, xy);
                     mbar_arrive_expect_tx(&full[stage], C::kStage);
                     uint8_t *st = sm + (size_t)stage * C::kStage;
-                    tma_load_2d(st, &tm_w, kc * kBK, x.rt * kBM, &full[stage]);
-                    tma_load_2d(st + kTileA, &tm_xh, kc * kBK, x.nt * BN, &full[stage]);
-                    tma_load_2d(st + kTileA + C::kTileB, &tm_xl, kc * kBK, x.nt * BN, &full[stage]);
+                    tma_load_2d(st, &tm_w, wx, wy, &full[stage]);
+                    tma_load_2d(st + kTileA, &tm_xh, wx, xy, &full[stage]);
+                    tma_load_2d(st + kTileA + C::kTileB, &tm_xl, wx, xy, &full[stage]);
                     armed |= 1u << stage;
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::kStages) {
@@ -504,7 +524,8 @@ template <int BN> cudaError_t launch_bn(const TcGemmPlan &p, const void *w, cons
     cudaError_t attr = set_attr<BN>();
     if (attr != cudaSuccess) return attr;
     CUtensorMap mw, mh, ml;
-    if (!make_map(&mw, w, a.R, a.K, kBM) || !make_map(&mh, xh, a.T, a.K, BN) || !make_map(&ml, xl, a.T, a.K, BN))
+    if (!make_map(&mw, w, a.w_rows, a.K, kBM) || !make_map(&mh, xh, a.T, a.K, BN) ||
+        !make_map(&ml, xl, a.T, a.K, BN))
         return cudaErrorInvalidValue;
     if (p.splits == 1 && !pdl) {
         tc_gemm_kernel<BN><<<p.grid, kTcThreads, TcCfg<BN>::kSmem, s>>>(mw, mh, ml, a, p.tok_tiles, p.splits,
@@ -563,9 +584,22 @@ bool tc_gemm_plan(int R, int K, int T, int num_sms, TcGemmPlan *p) {
 }
 
 cudaError_t launch_tc_gemm(const TcGemmPlan &p, const void *w, const void *x_hi, const void *x_lo,
-                           const TcGemmArgs &a, cudaStream_t s, bool pdl) {
+                           const TcGemmArgs &a_in, cudaStream_t s, bool pdl) {
+    TcGemmArgs a = a_in;
+    if (a.taps < 1) {
+        // the plain product: one tap, the first slab, no shift
+        a.taps = 1;
+        a.w_slab0 = a.w_slab_step = a.x_shift0 = a.x_shift_step = 0;
+    }
+    if (a.w_rows <= 0) a.w_rows = a.R;
     if (p.splits > 1 && (!a.partial || !a.tile_counter || p.units > p.grid)) return cudaErrorInvalidValue;
     if (a.mode == TC_SWIGLU && (!a.act_hi || !a.act_lo)) return cudaErrorInvalidValue;
+    if (a.mode == TC_STORE_RT && a.ldt <= 0) return cudaErrorInvalidValue;
+    // every tap's weight slab inside W
+    for (int j = 0; j < a.taps; j += a.taps - 1 > 0 ? a.taps - 1 : 1) {
+        const int slab = a.w_slab0 + j * a.w_slab_step;
+        if (slab < 0 || (long long)(slab + 1) * a.R > a.w_rows) return cudaErrorInvalidValue;
+    }
     return p.bn == 64 ? launch_bn<64>(p, w, x_hi, x_lo, a, s, pdl) : launch_bn<128>(p, w, x_hi, x_lo, a, s, pdl);
 }
 
