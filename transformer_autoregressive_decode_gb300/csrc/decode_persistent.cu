@@ -425,7 +425,8 @@ __device__ __forceinline__ void mma_bf16(float &d0, float &d1, float &d2, float 
 // bf16 columns, x0 = bf16(x) and x1 = bf16(x - x0) (16 significant bits: |x - x0 - x1|
 // <= 2^-17 |x|), the other six columns zero, so row r's sum is D[r][0] + D[r][1]
 // (fp32 accumulation of exact bf16 x bf16 products).  xp: the warp's chunk as the two
-// bf16 parts in shared memory, part j at xp + j K / 16 words.  At batch 1 this is not
+// bf16 parts in shared memory, k-step by k-step: 8 words of x0's 16 columns, then 8 of
+// x1's (the two parts' loads fall in different banks).  At batch 1 this is not
 // about tensor throughput: one instruction replaces the conversions, FMAs and shuffle
 // reduction of 16 rows x 16 columns, whose issue and latency bound this phase on the
 // CUDA cores.  (A third part, x - x0 - x1, makes the split exact; it measured 3 %
@@ -435,7 +436,7 @@ __device__ __forceinline__ bool kc_gemv_mma(const Ring &R, uint32_t &sidx, int n
                                             int colw, int nks, const uint32_t *xp, float *part) {
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int nst = (nrows + rps - 1) / rps;
-    const uint32_t *xb = xp + (g < 2 ? g : 0) * nks * 8;   // N column g < 2: part g
+    const uint32_t *xb = xp + (g < 2 ? g : 0) * 8;   // N column g < 2: part g of each k-step
     const bool live = g < 2;
 #pragma unroll 1
     for (int st = 0; st < nst; ++st) {
@@ -449,11 +450,11 @@ __device__ __forceinline__ bool kc_gemv_mma(const Ring &R, uint32_t &sidx, int n
             const uint8_t *pa = sb + (size_t)ra * pitch + (size_t)colw * 2 + t * 4;
             const uint8_t *pb = sb + (size_t)rb * pitch + (size_t)colw * 2 + t * 4;
             float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f, e0 = 0.f, e1 = 0.f, e2 = 0.f, e3 = 0.f;
-#pragma unroll 2
+#pragma unroll 4
             for (int ks = 0; ks < nks; ks += 2) {
                 // two independent accumulators: k-steps ks (c) and ks + 1 (e)
-                const uint32_t b0 = live ? xb[ks * 8 + t] : 0u, b1 = live ? xb[ks * 8 + t + 4] : 0u;
-                const uint32_t b2 = live ? xb[ks * 8 + 8 + t] : 0u, b3 = live ? xb[ks * 8 + 12 + t] : 0u;
+                const uint32_t b0 = live ? xb[ks * 16 + t] : 0u, b1 = live ? xb[ks * 16 + t + 4] : 0u;
+                const uint32_t b2 = live ? xb[ks * 16 + 16 + t] : 0u, b3 = live ? xb[ks * 16 + 20 + t] : 0u;
                 const uint32_t *qa = reinterpret_cast<const uint32_t *>(pa + ks * 32);
                 const uint32_t *qb = reinterpret_cast<const uint32_t *>(pb + ks * 32);
                 mma_bf16(c0, c1, c2, c3, qa[0], qb[0], qa[4], qb[4], b0, b1);
@@ -1048,7 +1049,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
             float *part = kc_part + buf * kNW * PS;
             if constexpr (kMma) {
                 // as two bf16 parts (the slice's K / 8 values twice: the same bytes as fp32)
-                __nv_bfloat16 *x0 = reinterpret_cast<__nv_bfloat16 *>(xw), *x1 = x0 + K / kNW;
+                __nv_bfloat16 *x0 = reinterpret_cast<__nv_bfloat16 *>(xw), *x1 = x0 + 16;
 #pragma unroll
                 for (int cc = 0; cc < NCMAX; ++cc)
                     if (cc < nc) {
@@ -1058,8 +1059,9 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
                             const float v = x[cc][e] * gv[cc][e];
                             const __nv_bfloat16 h = __float2bfloat16_rn(v);
                             const int i = cc * 32 * EL + e * 32 + lane;
-                            x0[i] = h;
-                            x1[i] = __float2bfloat16_rn(v - __bfloat162float(h));
+                            const int j = (i >> 4) * 32 + (i & 15);   // k-step i / 16: x0's 16, then x1's
+                            x0[j] = h;
+                            x1[j] = __float2bfloat16_rn(v - __bfloat162float(h));
                         }
                     }
                 __syncwarp();
