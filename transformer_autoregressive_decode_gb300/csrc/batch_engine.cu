@@ -105,6 +105,7 @@ struct qd_batch {
     void *arena = nullptr;
     void *kv = nullptr;
     size_t stream_elems = 0;
+    CUtensorMap kv_map;           // the caches as [S][hd] planes, for the attention's TMA loads
     float *x = nullptr, *qkv = nullptr, *logits = nullptr, *rope_cos = nullptr, *rope_sin = nullptr;
     __nv_bfloat16 *xh = nullptr, *xl = nullptr, *ah = nullptr, *al = nullptr;
     float *partial = nullptr;
@@ -226,7 +227,7 @@ qd_status enqueue_batch_step(qd_batch *b, cudaStream_t s) {
         if (gemm(b->p_qkv, L.w_qkv, b->xh, b->xl, rows_qkv, h, TC_STORE, b->qkv, rows_qkv))
             return batch_fail(b, QD_ECUDA, "QKV GEMM launch failed");
         ++n;
-        if (launch_batch_attention(c.head_dim, B, batch_attn_args(b, l), s, true))
+        if (launch_batch_attention(c.head_dim, B, batch_attn_args(b, l), b->kv_map, s, true))
             return batch_fail(b, QD_ECUDA, "attention launch failed");
         if (gemm(b->p_o, L.w_o, b->xh, b->xl, h, qd_, TC_RESIDUAL, b->x, h))
             return batch_fail(b, QD_ECUDA, "O GEMM launch failed");
@@ -270,7 +271,7 @@ qd_status enqueue_batch_kernel(qd_batch *b, int which, cudaStream_t s) {
     const Layer &L0 = m->layers[0];
     cudaError_t e = cudaSuccess;
     switch (which) {
-        case 1: e = launch_batch_attention(c.head_dim, b->B, batch_attn_args(b, c.n_layers - 1), s); break;
+        case 1: e = launch_batch_attention(c.head_dim, b->B, batch_attn_args(b, c.n_layers - 1), b->kv_map, s); break;
         case 2: e = batch_gemm(b, b->p_qkv, L0.w_qkv, b->xh, b->xl, rows_qkv, h, TC_STORE, b->qkv, rows_qkv, s); break;
         case 3: e = batch_gemm(b, b->p_o, L0.w_o, b->xh, b->xl, h, qd_, TC_RESIDUAL, b->x, h, s); break;
         case 4: e = batch_gemm(b, b->p_gu, L0.w_gu, b->xh, b->xl, 2 * c.ffn, h, TC_SWIGLU, nullptr, c.ffn, s); break;
@@ -661,8 +662,13 @@ qd_status qd_batch_create(qd_handle model, int n_streams, int smax, qd_batch_han
         b->samp = reinterpret_cast<BatchSampling *>(A + o_smp);
         b->drawn = reinterpret_cast<int *>(A + o_drn);
         check(cudaMemsetAsync(b->arena, 0, off, b->ls), "cudaMemsetAsync");
-        // positions past a stream's length hold zeros or values this library wrote
+        // positions past a stream's length hold zeros or values this library wrote (the
+        // attention loads whole 32-position tiles and gives the rows past a chunk
+        // probability 0, which needs them finite)
         check(cudaMemsetAsync(b->kv, 0, b->stream_elems * 2 * B, b->ls), "cudaMemsetAsync(batch KV caches)");
+        if (!st && !make_kv_tile_map(&b->kv_map, b->kv, c.head_dim, smax,
+                                     (long long)B * c.n_layers * 2 * c.n_kv_heads))
+            st = fail(m, QD_EUNSUPPORTED, "TMA map of the batch KV caches refused");
         check(launch_rope_table(b->rope_cos, b->rope_sin, smax, c.head_dim, c.rope_theta, b->ls), "RoPE table");
         check(cudaStreamSynchronize(b->ls), "cudaStreamSynchronize");
     }

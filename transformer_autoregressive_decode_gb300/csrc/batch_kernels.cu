@@ -9,109 +9,106 @@
 //    argmax, per stream.
 //  - "qwen3-tts-hip OPTIMIZATION_LOG", decode-step profile: the stages of one step,
 //    here run for every stream at once.
+#include <cuda.h>
+
 #include "decode_common.cuh"
+#include "mma_sync.cuh"
 
 namespace qd {
 
 namespace {
 
-// ---- attention: one CTA per (stream, kv group, chunk of 256 cached positions), 8
-// consumer warps and a producer warp.  The producer streams the chunk's K rows, then
-// its V rows, in 32-position tiles through a 6-slot shared-memory ring (1-D bulk
-// copies; full/empty mbarriers per slot).  Consumer warp w owns rows 4w..4w+3 of every
-// tile, so 32 rows of the chunk, one per lane: pass 1 computes their scores (4 rows x
-// G heads reduced with one butterfly, then each score moved to its row's lane), a
-// softmax over the warp's rows runs lane-parallel, pass 2 accumulates P.V.  The
-// warps' partials (and, in the chunk that holds it, the new position, whose k and v
-// are QK-normed, rotated, rounded to the cache type and appended) are combined into
+// ---- attention: one CTA per (stream, kv group, chunk of 256 cached positions), 4
+// consumer warps and a producer warp.  The producer streams the chunk's tiles of 32
+// positions, each tile's K rows then its V rows, into 4 shared-memory slots (3-D tiled
+// TMA loads of the cache's [S][head_dim] planes with the 128-byte swizzle; full/empty
+// mbarriers per slot).  The consumer warps go in pairs: pair i takes tiles i, i + 2,
+// i + 4, i + 6 through its own two slots (K and V; so every waiter sees every phase of the
+// barriers it waits on), warp 2i + j the tile's positions 16 j .. 16 j + 15.  They
+// compute on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate) with the
+// positions as the fragments' M: the scores (A = the 16 K rows, B = the G q heads of
+// the group as bf16 hi and lo columns, so a score is column 2h + column 2h + 1), an
+// online-softmax update per head (running max and sum; the output rescaled when the
+// max grows), then P.V (A = the V rows transposed, 16 head dimensions at a time;
+// B = the probabilities as bf16 hi and lo columns, moved from the score fragments'
+// layout through a small per-warp buffer).  The tensor cores serve here to cut the
+// instruction count per cached row (one product per 16 positions x 16 dimensions),
+// not for their FLOP rate: the kernel is bound by the bytes of the cache.
+// The warps' partials (and, in the chunk that holds it, the new position, whose k and
+// v are QK-normed, rotated, rounded to the cache type and appended) are combined into
 // the chunk's (max, sum, output); the last chunk CTA of a (stream, group) to finish
 // merges the chunks in order (flash-decoding merge) and writes the output.  Equal
 // chunks keep the work balanced whatever the lengths; no CTA waits for another.  As a
 // programmatic dependent of the QKV GEMM, the producer starts on the cached rows
 // (written by earlier steps) before the consumers wait for the GEMM's q, k and v.
-constexpr int kBattConsumers = 8;
+constexpr int kBattConsumers = 4;
 constexpr int kBattThreads = (kBattConsumers + 1) * 32;
 constexpr int kBattTile = 32;        // positions per ring slot
-constexpr int kBattSlots = 6;
+constexpr int kBattSlots = 4;        // two per warp pair
 constexpr int kBattMaxGroup = 8;     // q heads per kv head
-constexpr int kBattRowsPerWarp = kBattTile / kBattConsumers;   // 4
-static_assert(kBattChunk / kBattTile * kBattRowsPerWarp == 32, "one chunk row per lane of each warp");
+constexpr int kBattPairs = kBattConsumers / 2;
+constexpr int kBattTiles = kBattChunk / kBattTile;
+constexpr int kBattUnits = kBattTiles / kBattPairs;   // tiles per pair
+static_assert(kBattTiles % kBattPairs == 0 && kBattSlots == 2 * kBattPairs, "whole tiles per warp pair");
 
-// Sums N per-lane values over the lanes of a warp with one butterfly: each halving
-// step trades half of the values with the partner lane, so N values cost about N
-// shuffles instead of 5 N.  Afterwards v[0] of lane l holds the total of value idx,
-// where idx collects the halves lane l kept; lanes with (l & (32 / N - 1)) == 0 own
-// the N distinct indices.
-template <int N, int MASK> struct ReduceScatter {
-    __device__ __forceinline__ static void run(float *v, int lane, int &idx) {
-        if constexpr (N > 1 && MASK > 0) {
-            const bool up = (lane & MASK) != 0;
-#pragma unroll
-            for (int i = 0; i < N / 2; ++i) {
-                const float send = up ? v[i] : v[i + N / 2];
-                const float keep = up ? v[i + N / 2] : v[i];
-                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, MASK);
-            }
-            if (up) idx += N / 2;
-            ReduceScatter<N / 2, MASK / 2>::run(v, lane, idx);
-        } else if constexpr (MASK > 0) {
-            v[0] += __shfl_xor_sync(0xffffffffu, v[0], MASK);
-            ReduceScatter<1, MASK / 2>::run(v, lane, idx);
-        }
-    }
+// Slots of tile i: pair (i mod pairs)'s two slots, K in the first and V in the second;
+// the pair's u-th tile (i / pairs) is the slots' use u (barrier phase parity u & 1).
+__host__ __device__ constexpr int batt_kslot(int i) { return 2 * (i % kBattPairs); }
+
+// Byte offset of 16-byte chunk `ch` of row r in a tile written by TMA with the 128-byte
+// swizzle: head_dim / 64 boxes of kBattTile rows x 128 bytes, the chunk index XOR
+// (r mod 8) inside each (1024-byte aligned) box.
+__device__ __forceinline__ uint32_t kv_swz(int r, int ch) {
+    return (uint32_t)((ch >> 3) * (kBattTile * 128) + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int c0, int c1, int c2, uint64_t *bar,
+                                            uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar)), "l"(pol)
+        : "memory");
+}
+
+template <int HD, int G> struct BattShape {
+    static constexpr int NT = (2 * G + 7) / 8;   // 8-column n-tiles holding the heads' hi/lo columns
+    static constexpr uint32_t kTileBytes = kBattTile * HD * 2;
+    static constexpr int RS = HD + 2;            // partial record: output, max, sum
+    // after the 1024-byte alignment: ring (the warps' records once it is idle), q heads,
+    // k, v, cos/sin, the warps' P^T buffers, barriers, flags
+    static constexpr size_t kRing = (size_t)kBattSlots * kTileBytes;
+    static constexpr size_t kRed = (size_t)(kBattConsumers + 2) * G * RS * 4;
+    static constexpr size_t kPt = (size_t)kBattConsumers * NT * 8 * 16 * 2;
+    static constexpr size_t kSmem = 1024 + (kRing > kRed ? kRing : kRed) + (size_t)G * HD * 4 + 3 * (size_t)HD * 4 +
+                                    kPt + 2 * kBattSlots * 8 + 16;
 };
 
-// Row jj of a tile of bf16 rows of HD elements: this lane's DPL consecutive elements
-// (zeros when the row is past the tile's end).
-template <int DPL, int HD>
-__device__ __forceinline__ void tile_row(const __nv_bfloat16 *tile, int jj, int lane, bool in, float *f) {
-    if (!in) {
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) f[e] = 0.f;
-        return;
-    }
-    if constexpr (DPL == 4) {
-        const uint2 u = *reinterpret_cast<const uint2 *>(tile + (size_t)jj * HD + lane * 4);
-        f[0] = bf16lo(u.x);
-        f[1] = bf16hi(u.x);
-        f[2] = bf16lo(u.y);
-        f[3] = bf16hi(u.y);
-    } else {
-        const uint32_t u = *reinterpret_cast<const uint32_t *>(tile + (size_t)jj * HD + lane * 2);
-        f[0] = bf16lo(u);
-        f[1] = bf16hi(u);
-    }
-}
-
-// Owner lane of value i after ReduceScatter<N, 16>: the lane bits set by the halving
-// steps that kept the upper half.
-template <int N> __device__ __forceinline__ int scatter_owner(int i) {
-    int lane = 0, mask = 16;
-#pragma unroll
-    for (int half = N / 2; half >= 1; half >>= 1, mask >>= 1)
-        if (i & half) lane |= mask;
-    return lane;
-}
-
 template <int HD, int G>
-__global__ void __launch_bounds__(kBattThreads, G <= 2 ? 4 : 2) batch_attn_kernel(const BatchAttnArgs a) {
+__global__ void __launch_bounds__(kBattThreads, 4)
+    batch_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const BatchAttnArgs a) {
     using KT = __nv_bfloat16;
+    using S_ = BattShape<HD, G>;
     constexpr int HALF = HD / 2;
-    constexpr int DPL = HD / 32;                       // dimensions per lane
-    constexpr uint32_t kTileBytes = kBattTile * HD * 2;
-    constexpr int NV = kBattRowsPerWarp * G;           // scores of one warp per tile
-    constexpr int RS = HD + 2;                         // partial record: output, max, sum
-    static_assert(G >= 1 && G <= kBattMaxGroup && NV <= 32, "group size");
-    extern __shared__ __align__(1024) uint8_t smem[];
-    uint8_t *ring = smem;                                                    // [slots][tile]
-    float *red = reinterpret_cast<float *>(ring);                            // [warps + 1][G][RS], after the ring
-    float *qs = reinterpret_cast<float *>(ring + kBattSlots * kTileBytes);  // [G][HD]
-    float *kn = qs + G * HD;                                                 // [HD]
-    float *vn = kn + HD;                                                     // [HD]
-    float *rc = vn + HD;                                                     // [HALF] cos, [HALF] sin
-    uint64_t *full = reinterpret_cast<uint64_t *>(rc + HD);                  // [slots]
-    uint64_t *empty = full + kBattSlots;                                     // [slots]
-    int *flag = reinterpret_cast<int *>(empty + kBattSlots);                 // [0] abort, [1] last chunk
+    constexpr int NT = S_::NT;
+    constexpr uint32_t kTileBytes = S_::kTileBytes;
+    constexpr int RS = S_::RS;
+    constexpr int KS = HD / 16;                        // k-steps of a score
+    constexpr int MT = HD / 16;                        // 16-dimension m-tiles of the output
+    static_assert(G >= 1 && G <= kBattMaxGroup && HD % 64 == 0, "group size / head_dim");
+    extern __shared__ uint8_t smem_raw[];
+    // the swizzle pattern is anchored at 1024-byte boundaries of the shared window
+    uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    uint8_t *ring = smem;                                                           // [slots][tile]
+    float *red = reinterpret_cast<float *>(ring);                                   // [warps + 2][G][RS]
+    float *qs = reinterpret_cast<float *>(ring + (S_::kRing > S_::kRed ? S_::kRing : S_::kRed));  // [G][HD]
+    float *kn = qs + G * HD;                                                        // [HD]
+    float *vn = kn + HD;                                                            // [HD]
+    float *rc = vn + HD;                                                            // [HALF] cos, [HALF] sin
+    KT *pt = reinterpret_cast<KT *>(rc + HD);                                       // [warps][NT * 8][16]
+    uint64_t *full = reinterpret_cast<uint64_t *>(pt + (size_t)kBattConsumers * NT * 8 * 16);   // [slots]
+    uint64_t *empty = full + kBattSlots;                                            // [slots]
+    int *flag = reinterpret_cast<int *>(empty + kBattSlots);                        // [0] abort, [1] last chunk
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int pairs = gridDim.x / batch_attn_max_chunks(a.S);
@@ -130,15 +127,17 @@ __global__ void __launch_bounds__(kBattThreads, G <= 2 ? 4 : 2) batch_attn_kerne
     const int j0 = c * kBattChunk;
     const int rows_c = (holds_new ? p : j0 + kBattChunk) - j0;   // cached rows of the chunk
     const int nT = (rows_c + kBattTile - 1) / kBattTile;
-    const int total = 2 * nT;                          // K tiles, then V tiles
+    const int total = 2 * nT;                          // each tile K, then its V
     const size_t grp_off = (size_t)g * a.S * HD;
     KT *kbase = reinterpret_cast<KT *>(a.kv) + (size_t)b * a.stream_elems + a.layer_elems + grp_off;
     KT *vbase = kbase + (size_t)a.kvh * a.S * HD;
+    // [S][HD] planes of the caches: this pair's K plane; its V plane kvh further
+    const int plane_k = (int)(((size_t)b * a.stream_elems + a.layer_elems) / ((size_t)a.S * HD)) + g;
 
     if (tid == 0) {
         for (int i = 0; i < kBattSlots; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kBattConsumers);
+            mbar_init(&empty[i], 2);                   // the two warps of the pair that reads it
         }
         flag[0] = 0;
         fence_barrier_init();
@@ -151,26 +150,29 @@ __global__ void __launch_bounds__(kBattThreads, G <= 2 ? 4 : 2) batch_attn_kerne
             const uint64_t pol = policy_evict_first();
             int issued = 0;
             for (; issued < total; ++issued) {
-                const int slot = issued % kBattSlots;
-                if (issued >= kBattSlots &&
-                    !mbar_wait_bounded(&empty[slot], (uint32_t)(issued / kBattSlots - 1) & 1u)) {
+                // tile i's K then its V; the pair's second tile reuses its slots once both
+                // of its warps have read the first
+                const int i = issued >> 1, kv = issued & 1;
+                const int slot = batt_kslot(i) + kv;
+                if (i >= kBattPairs && !mbar_wait_bounded(&empty[slot], (uint32_t)(i / kBattPairs - 1) & 1u)) {
                     atomicOr(a.status, DEV_ERR_WAIT_TIMEOUT);
                     *reinterpret_cast<volatile int *>(flag) = 1;
                     break;
                 }
-                const int i = issued < nT ? issued : issued - nT;
-                const int rows = rows_c - i * kBattTile < kBattTile ? rows_c - i * kBattTile : kBattTile;
-                const uint32_t bytes = (uint32_t)rows * HD * 2;
-                mbar_arrive_expect_tx(&full[slot], bytes);
-                bulk_copy_g2s(ring + (size_t)slot * kTileBytes,
-                              (issued < nT ? kbase : vbase) + (size_t)(j0 + i * kBattTile) * HD, bytes, &full[slot],
-                              pol);
+                const int z = plane_k + kv * a.kvh;
+                // whole tiles: positions past the plane's S load as zeros; those past
+                // the chunk's rows get probability 0
+                mbar_arrive_expect_tx(&full[slot], kTileBytes);
+#pragma unroll
+                for (int h = 0; h < HD / 64; ++h)
+                    tma_load_3d(ring + (size_t)slot * kTileBytes + h * (kBattTile * 128), &kv_map, h * 64,
+                                j0 + i * kBattTile, z, &full[slot], pol);
             }
-            // copies in flight land before the CTA can leave
-            for (int k = 0; k < kBattSlots; ++k) {
-                int last = -1;
-                for (int t = k; t < issued; t += kBattSlots) last = t;
-                if (last >= 0) (void)mbar_wait_bounded(&full[k], (uint32_t)(last / kBattSlots) & 1u, 10000000ull);
+            // copies in flight land before the CTA can leave: each slot's last use
+            for (int k = 0; k < issued; ++k) {
+                const int i = k >> 1;
+                if (k + 2 * kBattPairs >= issued)   // no later use of this slot was issued
+                    (void)mbar_wait_bounded(&full[batt_kslot(i) + (k & 1)], (uint32_t)(i / kBattPairs) & 1u, 10000000ull);
             }
         }
         return;
@@ -190,6 +192,8 @@ __global__ void __launch_bounds__(kBattThreads, G <= 2 ? 4 : 2) batch_attn_kerne
         kn[i] = __ldcg(row + (size_t)a.qh * HD + (size_t)g * HD + i);
         vn[i] = __ldcg(row + (size_t)(a.qh + a.kvh) * HD + (size_t)g * HD + i);
     }
+    // the P^T columns past the heads' stay zero
+    for (int i = tid; i < kBattConsumers * NT * 8 * 16; i += NC) pt[i] = __float2bfloat16_rn(0.f);
     named_sync(1, NC);
     qk_norm_rope<HD, kBattConsumers>(qs, kn, G, a.q_gamma, a.k_gamma, a.eps, rc, 1);
     if (holds_new) {
@@ -202,117 +206,169 @@ __global__ void __launch_bounds__(kBattThreads, G <= 2 ? 4 : 2) batch_attn_kerne
         }
         named_sync(1, NC);
     }
-    float qr[G][DPL];
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) qr[hh][e] = qs[hh * HD + lane * DPL + e];
 
-    // pass 1: scores; lane l ends with the score of this warp's row l (tile l / 4,
-    // row 4 * warp + l % 4 of that tile), -inf past the chunk's rows
-    bool ok = true;
-    float smine[G];
+    // B fragments of the scores: column n of n-tile nt is q head (8 nt + n) / 2, its hi
+    // part for even n, lo for odd (zero past the G heads); lane (gl, tl) holds rows
+    // (k) 2 tl, 2 tl + 1 and 2 tl + 8, 2 tl + 9 of column gl
+    const int gl = lane >> 2, tl = lane & 3;
+    uint32_t qb[NT][KS][2];
 #pragma unroll
-    for (int hh = 0; hh < G; ++hh) smine[hh] = -INFINITY;
-    for (int t = 0; t < nT; ++t) {
-        const int slot = t % kBattSlots;
-        if (!mbar_wait_bounded(&full[slot], (uint32_t)(t / kBattSlots) & 1u)) {
-            ok = false;
-            break;
+    for (int nt = 0; nt < NT; ++nt) {
+        const int n = nt * 8 + gl, hq = n >> 1;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const float *qr = qs + (size_t)(hq < G ? hq : 0) * HD + ks * 16 + 2 * tl;
+            const float x0 = hq < G ? qr[0] : 0.f, x1 = hq < G ? qr[1] : 0.f;
+            const float x2 = hq < G ? qr[8] : 0.f, x3 = hq < G ? qr[9] : 0.f;
+            uint32_t h01, l01, h89, l89;
+            split_pack(x0, x1, h01, l01);
+            split_pack(x2, x3, h89, l89);
+            qb[nt][ks][0] = (n & 1) ? l01 : h01;
+            qb[nt][ks][1] = (n & 1) ? l89 : h89;
         }
-        const KT *tile = reinterpret_cast<const KT *>(ring + (size_t)slot * kTileBytes);
-        const int rows = rows_c - t * kBattTile < kBattTile ? rows_c - t * kBattTile : kBattTile;
-        float v[NV];
+    }
+
+    const int pr = warp >> 1, mb = warp & 1;           // warp pair, 16-position half of its tiles
+    const int mi = lane >> 3, rr = lane & 7;           // ldmatrix: matrix and row this lane addresses
+    bool ok = true;
+    // One pass over the warp's units (tiles pr, pr + pairs, ...; its 16 positions of each): the
+    // scores of the unit's K tile, an online-softmax update (running max and sum per
+    // head, the output rescaled when the max grows), then P.V over the unit's V tile.
+    // Lane (gl, tl) keeps head 4 nt + tl's running max / sum, and its output dimensions
+    // 16 mt + gl (+ 8) as the hi + lo columns of the accumulators.
+    float pm_[NT], pl_[NT];
+    float o[NT][MT][4];
 #pragma unroll
-        for (int r = 0; r < kBattRowsPerWarp; ++r) {
-            const int jj = warp * kBattRowsPerWarp + r;
-            float kf[DPL];
-            tile_row<DPL, HD>(tile, jj, lane, jj < rows, kf);
+    for (int nt = 0; nt < NT; ++nt) {
+        pm_[nt] = -INFINITY;
+        pl_[nt] = 0.f;
 #pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-                float d = 0.f;
+        for (int mt = 0; mt < MT; ++mt) o[nt][mt][0] = o[nt][mt][1] = o[nt][mt][2] = o[nt][mt][3] = 0.f;
+    }
+    KT *ptw = pt + (size_t)warp * NT * 8 * 16;         // [NT * 8 columns][16 positions]
+#pragma unroll 1
+    for (int u = 0; u < kBattUnits; ++u) {
+        const int t = pr + u * kBattPairs;
+        if (t >= nT || !ok) continue;
+        const int ks_slot = batt_kslot(t), vs_slot = ks_slot + 1;
+        if (!mbar_wait_bounded(&full[ks_slot], (uint32_t)u & 1u)) {
+            ok = false;
+            continue;
+        }
+        uint32_t tile = smem_addr(ring + (size_t)ks_slot * kTileBytes);
+        float d[NT][4];
 #pragma unroll
-                for (int e = 0; e < DPL; ++e) d = fmaf(qr[hh][e], kf[e], d);
-                v[r * G + hh] = d;
-            }
+        for (int nt = 0; nt < NT; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            uint32_t af[4];
+            ldsm_x4(tile + kv_swz(16 * mb + rr + 8 * (mi & 1), 2 * ks + (mi >> 1)), af[0], af[1], af[2], af[3]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma16816(d[nt], af, qb[nt][ks][0], qb[nt][ks][1]);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
-        int idx = 0;
-        ReduceScatter<NV, 16>::run(v, lane, idx);
+        if (lane == 0) mbar_arrive(&empty[ks_slot]);
+        const int pos = t * kBattTile + 16 * mb + gl;
+        float pv[NT][2];
 #pragma unroll
-        for (int r = 0; r < kBattRowsPerWarp; ++r)
+        for (int nt = 0; nt < NT; ++nt) {
+            const float s0 = pos < rows_c ? (d[nt][0] + d[nt][1]) * a.scale : -INFINITY;
+            const float s1 = pos + 8 < rows_c ? (d[nt][2] + d[nt][3]) * a.scale : -INFINITY;
+            float mx = fmaxf(s0, s1);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float mn = fmaxf(pm_[nt], mx);
+            // rescale what came before (nothing to rescale while the max is -inf)
+            const float f = pm_[nt] == -INFINITY ? 0.f : expf(pm_[nt] - mn);
+            pv[nt][0] = mn == -INFINITY || s0 == -INFINITY ? 0.f : expf(s0 - mn);
+            pv[nt][1] = mn == -INFINITY || s1 == -INFINITY ? 0.f : expf(s1 - mn);
+            float sum = pv[nt][0] + pv[nt][1];
+            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 8);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+            pl_[nt] = pl_[nt] * f + sum;
+            pm_[nt] = mn;
+            // lane (gl, tl)'s accumulators hold head 4 nt + tl: the same head as its
+            // scores, so the factor needs no exchange
 #pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-                const float x = __shfl_sync(0xffffffffu, v[0], scatter_owner<NV>(r * G + hh));
-                if (lane == t * kBattRowsPerWarp + r && warp * kBattRowsPerWarp + r < rows) smine[hh] = x * a.scale;
+            for (int mt = 0; mt < MT; ++mt) {
+                o[nt][mt][0] *= f;
+                o[nt][mt][1] *= f;
+                o[nt][mt][2] *= f;
+                o[nt][mt][3] *= f;
             }
-    }
-    // softmax over this warp's rows, one per lane
-    float pm_[G], pl_[G], pr[G];
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-        const float mx = warp_max(smine[hh]);
-        pr[hh] = mx == -INFINITY ? 0.f : expf(smine[hh] - mx);
-        pm_[hh] = mx;
-        pl_[hh] = warp_sum(pr[hh]);
-    }
-    // pass 2: P.V
-    float acc[G][DPL];
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh)
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) acc[hh][e] = 0.f;
-    for (int t = nT; t < total && ok; ++t) {
-        const int slot = t % kBattSlots;
-        if (!mbar_wait_bounded(&full[slot], (uint32_t)(t / kBattSlots) & 1u)) {
-            ok = false;
-            break;
         }
-        const KT *tile = reinterpret_cast<const KT *>(ring + (size_t)slot * kTileBytes);
-        const int i = t - nT;
-        const int rows = rows_c - i * kBattTile < kBattTile ? rows_c - i * kBattTile : kBattTile;
+        // this unit's probabilities, hi/lo columns 2h, 2h + 1 of head h = 4 nt + tl
 #pragma unroll
-        for (int r = 0; r < kBattRowsPerWarp; ++r) {
-            const int jj = warp * kBattRowsPerWarp + r;
-            if (jj < rows) {
-                float vf[DPL];
-                tile_row<DPL, HD>(tile, jj, lane, true, vf);
+        for (int nt = 0; nt < NT; ++nt) {
+            const int hq = nt * 4 + tl;
+            if (hq < G) {
 #pragma unroll
-                for (int hh = 0; hh < G; ++hh) {
-                    const float pj = __shfl_sync(0xffffffffu, pr[hh], i * kBattRowsPerWarp + r);
-#pragma unroll
-                    for (int e = 0; e < DPL; ++e) acc[hh][e] = fmaf(pj, vf[e], acc[hh][e]);
+                for (int e = 0; e < 2; ++e) {
+                    const KT hi = __float2bfloat16_rn(pv[nt][e]);
+                    ptw[(2 * hq) * 16 + gl + 8 * e] = hi;
+                    ptw[(2 * hq + 1) * 16 + gl + 8 * e] = __float2bfloat16_rn(pv[nt][e] - __bfloat162float(hi));
                 }
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
+        uint32_t pb[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const KT *col = ptw + (size_t)(nt * 8 + gl) * 16;
+            pb[nt][0] = *reinterpret_cast<const uint32_t *>(col + 2 * tl);
+            pb[nt][1] = *reinterpret_cast<const uint32_t *>(col + 2 * tl + 8);
+        }
+        __syncwarp();
+        if (!mbar_wait_bounded(&full[vs_slot], (uint32_t)u & 1u)) {
+            ok = false;
+            continue;
+        }
+        tile = smem_addr(ring + (size_t)vs_slot * kTileBytes);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            // A = V^T: head dimensions 16 mt .. + 15 x the unit's 16 positions
+            uint32_t af[4];
+            ldsm_x4_t(tile + kv_swz(16 * mb + rr + 8 * (mi >> 1), 2 * mt + (mi & 1)), af[0], af[1], af[2], af[3]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma16816(o[nt][mt], af, pb[nt][0], pb[nt][1]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[vs_slot]);
     }
     if (!ok) {
         if (lane == 0) atomicOr(a.status, DEV_ERR_WAIT_TIMEOUT);
         *reinterpret_cast<volatile int *>(flag) = 1;
     }
     // combine the warps and the new position into the chunk's record (the ring is
-    // idle once every tile was consumed)
+    // idle once every tile was consumed): lane (gl, tl) holds head 4 nt + tl's output
+    // dimensions 16 mt + gl and 16 mt + gl + 8 as its hi + lo columns
     named_sync(1, NC);
 #pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-        float *rw = red + ((size_t)warp * G + hh) * RS;
+    for (int nt = 0; nt < NT; ++nt) {
+        const int hq = nt * 4 + tl;
+        if (hq < G) {
+            float *rw = red + ((size_t)warp * G + hq) * RS;
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) rw[lane * DPL + e] = acc[hh][e];
-        if (lane == 0) {
-            rw[HD] = pm_[hh];
-            rw[HD + 1] = pl_[hh];
+            for (int mt = 0; mt < MT; ++mt) {
+                rw[16 * mt + gl] = o[nt][mt][0] + o[nt][mt][1];
+                rw[16 * mt + gl + 8] = o[nt][mt][2] + o[nt][mt][3];
+            }
+            if (gl == 0) {
+                rw[HD] = pm_[nt];
+                rw[HD + 1] = pl_[nt];
+            }
         }
     }
     const int nrec = holds_new ? kBattConsumers + 1 : kBattConsumers;
     if (holds_new && warp == 0) {
+        constexpr int DPL = HD / 32;
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
             float d = 0.f;
 #pragma unroll
-            for (int e = 0; e < DPL; ++e) d = fmaf(qr[hh][e], kn[lane * DPL + e], d);
+            for (int e = 0; e < DPL; ++e) d = fmaf(qs[hh * HD + lane * DPL + e], kn[lane * DPL + e], d);
             d = warp_sum(d) * a.scale;
             float *rw = red + ((size_t)kBattConsumers * G + hh) * RS;
             for (int i = lane; i < HD; i += 32) rw[i] = vn[i];
@@ -526,7 +582,7 @@ __global__ void __launch_bounds__(kRowThreads) batch_argmax_kernel(const BatchAr
     }
 }
 
-typedef void (*BattFn)(const BatchAttnArgs);
+typedef void (*BattFn)(const CUtensorMap, const BatchAttnArgs);
 
 BattFn batt_fn(int hd, int group) {
 #define QD_BATT(HDV, GV) \
@@ -540,11 +596,12 @@ BattFn batt_fn(int hd, int group) {
 }  // namespace
 
 size_t batch_attention_smem_bytes(int hd, int group) {
-    // ring (holds the records of the warps, the new position and the chunk at the
-    // end), q heads, k, v, cos/sin, barriers, flags
-    const size_t ring = (size_t)kBattSlots * kBattTile * hd * 2;
-    const size_t red = (size_t)(kBattConsumers + 2) * group * (hd + 2) * 4;
-    return (ring > red ? ring : red) + (size_t)group * hd * 4 + 3 * (size_t)hd * 4 + 2 * kBattSlots * 8 + 16;
+#define QD_BATT(HDV, GV) \
+    if (hd == HDV && group == GV) return BattShape<HDV, GV>::kSmem;
+    QD_BATT(128, 1) QD_BATT(128, 2) QD_BATT(128, 4) QD_BATT(128, 8)
+    QD_BATT(64, 1) QD_BATT(64, 2) QD_BATT(64, 4) QD_BATT(64, 8)
+#undef QD_BATT
+    return 0;
 }
 
 bool batch_attention_supported(int hd, int group) { return batt_fn(hd, group) != nullptr; }
@@ -579,12 +636,13 @@ cudaError_t launch_ex(const void *fn, dim3 grid, dim3 block, size_t smem, cudaSt
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
-cudaError_t launch_batch_attention(int hd, int B, const BatchAttnArgs &a, cudaStream_t s, bool pdl) {
-    const size_t smem = batch_attention_smem_bytes(hd, a.qh / a.kvh);
+cudaError_t launch_batch_attention(int hd, int B, const BatchAttnArgs &a, const CUtensorMap &kv_map, cudaStream_t s,
+                                   bool pdl) {
     const BattFn fn = a.qh % a.kvh ? nullptr : batt_fn(hd, a.qh / a.kvh);
+    const size_t smem = fn ? batch_attention_smem_bytes(hd, a.qh / a.kvh) : 0;
     if (!fn || smem > 160 * 1024 || !a.partial || !a.counter) return cudaErrorInvalidValue;
     // chunk-major order: every pair's first chunk, then every pair's second, ...
-    void *args[1] = {const_cast<BatchAttnArgs *>(&a)};
+    void *args[2] = {const_cast<CUtensorMap *>(&kv_map), const_cast<BatchAttnArgs *>(&a)};
     return launch_ex(reinterpret_cast<const void *>(fn), dim3(batch_attn_max_chunks(a.S) * B * a.kvh),
                      dim3(kBattThreads), smem, s, pdl, args);
 }

@@ -1,6 +1,7 @@
 // Internal interface between the decode-step kernels and the engine (host C++).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -319,7 +320,13 @@ __host__ __device__ inline int batch_attn_max_chunks(int S) { return (S + kBattC
 size_t batch_attention_smem_bytes(int hd, int group);
 bool batch_attention_supported(int hd, int group);   // head_dim 64/128, 1, 2, 4 or 8 q heads per kv head
 cudaError_t batch_kernels_init();   // call before any capture
-cudaError_t launch_batch_attention(int hd, int B, const BatchAttnArgs &a, cudaStream_t s, bool pdl = false);
+// kv_map: make_kv_tile_map over the caches the arguments point into.
+cudaError_t launch_batch_attention(int hd, int B, const BatchAttnArgs &a, const CUtensorMap &kv_map, cudaStream_t s,
+                                   bool pdl = false);
+// TMA map of bf16 caches seen as `planes` planes of [S][hd] (rows of hd elements), box
+// of 64 elements x 32 rows with the 128-byte swizzle (the batched attention's tiles);
+// false if the driver refuses it.
+bool make_kv_tile_map(CUtensorMap *m, const void *kv, int hd, int S, long long planes);
 
 // Per row b < rows: optionally x[b] = E[tokens[b]] (the token joins stream b's emitted
 // set), then hi/lo bf16 parts of gamma * x[b] / sqrt(mean(x[b]^2) + eps).

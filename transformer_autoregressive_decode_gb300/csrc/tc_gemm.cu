@@ -565,6 +565,19 @@ cudaError_t tc_gemm_init() {
     return e != cudaSuccess ? e : set_attr<128>();
 }
 
+bool make_kv_tile_map(CUtensorMap *m, const void *kv, int hd, int S, long long planes) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || (reinterpret_cast<uintptr_t>(kv) & 15) || hd % 64 || S % 32 || planes < 1 || planes > INT32_MAX)
+        return false;
+    cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)S, (cuuint64_t)planes};
+    cuuint64_t strides[2] = {(cuuint64_t)hd * 2, (cuuint64_t)hd * 2 * S};
+    cuuint32_t box[3] = {64, 32, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(kv), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool tc_gemm_plan(int R, int K, int T, int num_sms, TcGemmPlan *p) {
     if (R <= 0 || K <= 0 || T <= 0 || R % kBM || K % kBK || num_sms <= 0) return false;
     TcGemmPlan q = {};
