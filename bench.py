@@ -44,8 +44,8 @@ _STEP_TRAFFIC = {"asr": {"digest": "f161bc38e9db3cac", "bytes": 224888320 + 3283
 _STEP_SOURCES = ("decode_persistent.cu", "decode_common.cuh", "qd_device.cuh")
 # DRAM bytes of one batch_attn_kernel launch (profiles/batch_attn_kernel_batch64.md) at
 # the initial lengths + 3, for the kernel sources with this digest.
-_BATT_TRAFFIC = {"digest": "4d797d556b20c614", "bytes": 256654336 + 3633920, "rows": 62239 + 3 * 64}
-_BATT_SOURCES = ("batch_kernels.cu", "decode_common.cuh", "qd_device.cuh")
+_BATT_TRAFFIC = {"digest": "ff6e64d610d9f6d3", "bytes": 260624384 + 3836416, "rows": 62239 + 3 * 64}
+_BATT_SOURCES = ("batch_kernels.cu", "decode_common.cuh", "qd_device.cuh", "mma_sync.cuh")
 
 
 def _step_digest(sources=_STEP_SOURCES) -> str:
