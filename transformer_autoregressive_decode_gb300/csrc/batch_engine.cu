@@ -108,6 +108,11 @@ struct qd_batch {
     CUtensorMap kv_map;           // the caches as [S][hd] planes, for the attention's TMA loads
     float *x = nullptr, *qkv = nullptr, *logits = nullptr, *rope_cos = nullptr, *rope_sin = nullptr;
     __nv_bfloat16 *xh = nullptr, *xl = nullptr, *ah = nullptr, *al = nullptr;
+    // the next RMSNorm's input: bf16 hi/lo parts of gamma * x [B][hidden] and the sums of
+    // squares of x per 32 rows [hidden / 32][B] (written by the residual GEMMs'
+    // epilogue; the GEMM that consumes them applies the norm's scale)
+    __nv_bfloat16 *nh = nullptr, *nl = nullptr;
+    float *ssp = nullptr;
     float *partial = nullptr;
     float *att_part = nullptr;   // attention chunk records [B * kvh][chunks][G][hd + 2]
     int *att_count = nullptr;    // [B * kvh]
@@ -142,11 +147,33 @@ constexpr size_t kAlign = 256;
 
 qd_status batch_fail(qd_batch *b, qd_status st, const char *what) { return fail(b->m, st, "%s", what); }
 
+// The RMSNorms between the step's GEMMs: `next_gamma` makes a residual GEMM also write
+// the next norm's input parts and sums of squares (TC_RESIDUAL_NORM); `scaled` makes a
+// GEMM apply the norm's scale from those sums to its products.
+struct NormFold {
+    const float *next_gamma = nullptr;
+    bool scaled = false;
+};
+
 // One tensor-core GEMM of the step over the B streams.
 cudaError_t batch_gemm(qd_batch *b, const TcGemmPlan &p, const void *w, const __nv_bfloat16 *xh,
                        const __nv_bfloat16 *xl, int R, int K, int mode, float *out, int ldo, cudaStream_t s,
-                       bool pdl = false) {
+                       bool pdl = false, NormFold nf = NormFold()) {
     TcGemmArgs a = {};
+    const qd_config &c = b->m->cfg;
+    if (nf.next_gamma) {
+        mode = TC_RESIDUAL_NORM;
+        a.norm_gamma = nf.next_gamma;
+        a.nh = b->nh;
+        a.nl = b->nl;
+        a.ss_out = b->ssp;
+    }
+    if (nf.scaled) {
+        a.rs_part = b->ssp;
+        a.rs_tiles = c.hidden / 32;
+        a.rs_K = c.hidden;
+        a.rs_eps = (float)c.rms_eps;
+    }
     a.R = R;
     a.K = K;
     a.T = b->B;
@@ -202,8 +229,8 @@ qd_status enqueue_batch_step(qd_batch *b, cudaStream_t s) {
         a.K = h;
         a.gamma = gamma;
         a.eps = (float)c.rms_eps;
-        a.hi = b->xh;
-        a.lo = b->xl;
+        a.hi = b->nh;
+        a.lo = b->nl;
         if (gather) {
             a.table = m->embed;
             a.table_rows = c.embed_rows;
@@ -217,29 +244,40 @@ qd_status enqueue_batch_step(qd_batch *b, cudaStream_t s) {
         return launch_norm_split(a, B, s, true);
     };
     auto gemm = [&](const TcGemmPlan &p, const void *w, const __nv_bfloat16 *xh, const __nv_bfloat16 *xl, int R,
-                    int K, int mode, float *out, int ldo) -> cudaError_t {
+                    int K, int mode, float *out, int ldo, NormFold nf = NormFold()) -> cudaError_t {
         ++n;
-        return batch_gemm(b, p, w, xh, xl, R, K, mode, out, ldo, s, true);
+        return batch_gemm(b, p, w, xh, xl, R, K, mode, out, ldo, s, true, nf);
     };
+    // Only the step's first RMSNorm (with the embedding gather) is a kernel of its own;
+    // each later one is folded into the GEMMs around it: the residual GEMM before it
+    // writes gamma * x as bf16 parts and the per-tile sums of squares, the GEMM after it
+    // scales its products by 1 / sqrt(mean(x^2) + eps).
     if (norm(m->layers[0].attn_norm, true)) return batch_fail(b, QD_ECUDA, "norm/embedding launch failed");
     for (int l = 0; l < c.n_layers; ++l) {
         const Layer &L = m->layers[l];
-        if (gemm(b->p_qkv, L.w_qkv, b->xh, b->xl, rows_qkv, h, TC_STORE, b->qkv, rows_qkv))
+        NormFold in_qkv;
+        in_qkv.scaled = l > 0;
+        if (gemm(b->p_qkv, L.w_qkv, b->nh, b->nl, rows_qkv, h, TC_STORE, b->qkv, rows_qkv, in_qkv))
             return batch_fail(b, QD_ECUDA, "QKV GEMM launch failed");
         ++n;
         if (launch_batch_attention(c.head_dim, B, batch_attn_args(b, l), b->kv_map, s, true))
             return batch_fail(b, QD_ECUDA, "attention launch failed");
-        if (gemm(b->p_o, L.w_o, b->xh, b->xl, h, qd_, TC_RESIDUAL, b->x, h))
+        NormFold o_out;
+        o_out.next_gamma = L.mlp_norm;
+        if (gemm(b->p_o, L.w_o, b->xh, b->xl, h, qd_, TC_RESIDUAL, b->x, h, o_out))
             return batch_fail(b, QD_ECUDA, "O GEMM launch failed");
-        if (norm(L.mlp_norm, false)) return batch_fail(b, QD_ECUDA, "norm launch failed");
-        if (gemm(b->p_gu, L.w_gu, b->xh, b->xl, 2 * c.ffn, h, TC_SWIGLU, nullptr, c.ffn))
+        NormFold gu_in;
+        gu_in.scaled = true;
+        if (gemm(b->p_gu, L.w_gu, b->nh, b->nl, 2 * c.ffn, h, TC_SWIGLU, nullptr, c.ffn, gu_in))
             return batch_fail(b, QD_ECUDA, "gate/up GEMM launch failed");
-        if (gemm(b->p_d, L.w_d, b->ah, b->al, h, c.ffn, TC_RESIDUAL, b->x, h))
+        NormFold d_out;
+        d_out.next_gamma = l + 1 < c.n_layers ? m->layers[l + 1].attn_norm : m->final_norm;
+        if (gemm(b->p_d, L.w_d, b->ah, b->al, h, c.ffn, TC_RESIDUAL, b->x, h, d_out))
             return batch_fail(b, QD_ECUDA, "down GEMM launch failed");
-        const float *next = l + 1 < c.n_layers ? m->layers[l + 1].attn_norm : m->final_norm;
-        if (norm(next, false)) return batch_fail(b, QD_ECUDA, "norm launch failed");
     }
-    if (gemm(b->p_head, m->heads[0], b->xh, b->xl, c.vocab, h, TC_STORE, b->logits, c.vocab))
+    NormFold head_in;
+    head_in.scaled = true;
+    if (gemm(b->p_head, m->heads[0], b->nh, b->nl, c.vocab, h, TC_STORE, b->logits, c.vocab, head_in))
         return batch_fail(b, QD_ECUDA, "head GEMM launch failed");
     BatchArgmaxArgs am = {};
     am.logits = b->logits;
@@ -272,11 +310,31 @@ qd_status enqueue_batch_kernel(qd_batch *b, int which, cudaStream_t s) {
     cudaError_t e = cudaSuccess;
     switch (which) {
         case 1: e = launch_batch_attention(c.head_dim, b->B, batch_attn_args(b, c.n_layers - 1), b->kv_map, s); break;
-        case 2: e = batch_gemm(b, b->p_qkv, L0.w_qkv, b->xh, b->xl, rows_qkv, h, TC_STORE, b->qkv, rows_qkv, s); break;
-        case 3: e = batch_gemm(b, b->p_o, L0.w_o, b->xh, b->xl, h, qd_, TC_RESIDUAL, b->x, h, s); break;
-        case 4: e = batch_gemm(b, b->p_gu, L0.w_gu, b->xh, b->xl, 2 * c.ffn, h, TC_SWIGLU, nullptr, c.ffn, s); break;
-        case 5: e = batch_gemm(b, b->p_d, L0.w_d, b->ah, b->al, h, c.ffn, TC_RESIDUAL, b->x, h, s); break;
-        case 6: e = batch_gemm(b, b->p_head, m->heads[0], b->xh, b->xl, c.vocab, h, TC_STORE, b->logits, c.vocab, s); break;
+        case 2: e = batch_gemm(b, b->p_qkv, L0.w_qkv, b->nh, b->nl, rows_qkv, h, TC_STORE, b->qkv, rows_qkv, s); break;
+        case 3: {
+            NormFold nf;
+            nf.next_gamma = L0.mlp_norm;
+            e = batch_gemm(b, b->p_o, L0.w_o, b->xh, b->xl, h, qd_, TC_RESIDUAL, b->x, h, s, false, nf);
+            break;
+        }
+        case 4: {
+            NormFold nf;
+            nf.scaled = true;
+            e = batch_gemm(b, b->p_gu, L0.w_gu, b->nh, b->nl, 2 * c.ffn, h, TC_SWIGLU, nullptr, c.ffn, s, false, nf);
+            break;
+        }
+        case 5: {
+            NormFold nf;
+            nf.next_gamma = c.n_layers > 1 ? m->layers[1].attn_norm : m->final_norm;
+            e = batch_gemm(b, b->p_d, L0.w_d, b->ah, b->al, h, c.ffn, TC_RESIDUAL, b->x, h, s, false, nf);
+            break;
+        }
+        case 6: {
+            NormFold nf;
+            nf.scaled = true;
+            e = batch_gemm(b, b->p_head, m->heads[0], b->nh, b->nl, c.vocab, h, TC_STORE, b->logits, c.vocab, s, false, nf);
+            break;
+        }
         default: return fail(m, QD_EINVAL, "kernel %d: use 1..6", which);
     }
     CU(e);
@@ -629,7 +687,8 @@ qd_status qd_batch_create(qd_handle model, int n_streams, int smax, qd_batch_han
                  o_ap = take((size_t)B * c.n_kv_heads * batch_attn_max_chunks(smax) *
                              (c.n_q_heads / c.n_kv_heads) * (c.head_dim + 2) * 4),
                  o_ac = take((size_t)B * c.n_kv_heads * 4), o_smp = take(sizeof(BatchSampling)),
-                 o_drn = take((size_t)B * 4);
+                 o_drn = take((size_t)B * 4), o_nh = take((size_t)B * h * 2), o_nl = take((size_t)B * h * 2),
+                 o_ssp = take((size_t)(h / 32) * B * 4);
     b->stream_elems = (size_t)c.n_layers * 2 * c.n_kv_heads * smax * c.head_dim;
     qd_status st = QD_OK;
     auto check = [&](cudaError_t e, const char *what) {
@@ -661,6 +720,9 @@ qd_status qd_batch_create(qd_handle model, int n_streams, int smax, qd_batch_han
         b->att_count = reinterpret_cast<int *>(A + o_ac);
         b->samp = reinterpret_cast<BatchSampling *>(A + o_smp);
         b->drawn = reinterpret_cast<int *>(A + o_drn);
+        b->nh = reinterpret_cast<__nv_bfloat16 *>(A + o_nh);
+        b->nl = reinterpret_cast<__nv_bfloat16 *>(A + o_nl);
+        b->ssp = reinterpret_cast<float *>(A + o_ssp);
         check(cudaMemsetAsync(b->arena, 0, off, b->ls), "cudaMemsetAsync");
         // positions past a stream's length hold zeros or values this library wrote (the
         // attention loads whole 32-position tiles and gives the rows past a chunk

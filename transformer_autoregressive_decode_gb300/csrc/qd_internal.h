@@ -242,6 +242,9 @@ enum TcEpilogue : int {
                        // written as bf16 hi/lo parts (and fp32 when out != null)
     TC_STORE_RT = 3,   // out[r * ldo + t * ldt] = acc + bias[r] for rows r < r_valid
                        // (channel-major outputs of the codec convolutions)
+    TC_RESIDUAL_NORM = 4,  // out[t][r] += acc, then the next RMSNorm's input parts:
+                           // nh/nl[t][r] = bf16 hi/lo of norm_gamma[r] * out[t][r], and
+                           // ss_out[r / 32][t] = sum over those 32 rows of out^2
 };
 
 struct TcGemmArgs {
@@ -261,6 +264,15 @@ struct TcGemmArgs {
     int ldt;                       // TC_STORE_RT: token stride of out
     int r_valid;                   // TC_STORE_RT: rows written
     const float *bias;             // TC_STORE_RT: [r_valid] or null
+    // TC_RESIDUAL_NORM outputs
+    const float *norm_gamma;       // [R]
+    __nv_bfloat16 *nh, *nl;        // [T][R]
+    float *ss_out;                 // [R / 32][T]: one partial per 32-row quarter of a row tile
+    // RMSNorm folded into this GEMM (its input parts were gamma * x, not yet scaled):
+    // acc *= 1 / sqrt(sum_i rs_part[i][t] / rs_K + rs_eps) before the epilogue, i < rs_tiles
+    const float *rs_part;
+    int rs_tiles, rs_K;
+    float rs_eps;
 };
 
 struct TcGemmPlan {

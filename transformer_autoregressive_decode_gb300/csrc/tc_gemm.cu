@@ -56,7 +56,8 @@ template <int BN> struct TcCfg {
     static constexpr uint32_t kStage = kTileA + 2 * kTileB;
     static constexpr int kStages = BN == 64 ? 6 : 4;
     static constexpr uint32_t kTmemCols = 2 * BN;   // two accumulators of BN fp32 columns
-    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + 256;
+    // stages, barriers (256 bytes), the folded RMSNorm's scales of a token tile (<= 1 KB)
+    static constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + 256 + 1024;
 };
 
 // ---- PTX wrappers (tensor memory, MMA, TMA)
@@ -184,18 +185,52 @@ __device__ __forceinline__ void epi_apply(const TcGemmArgs &a, int t, int r, flo
     }
 }
 
-// Epilogue of tokens t0..t0+n-1 (n <= N) of weight row r.  The residual reads are all
-// issued before any write: a read after a write to the same array cannot be moved
-// ahead of it, so element-by-element read-add-write would queue N round trips.
+// The folded RMSNorm's scale of token t: the producing GEMM's partial sums of squares
+// (one per 32-row quarter of each row tile), summed in order.
+__device__ __forceinline__ float rms_scale_of(const TcGemmArgs &a, int t) {
+    float s = 0.f;
+    for (int i = 0; i < a.rs_tiles; ++i) s += __ldcg(a.rs_part + (size_t)i * a.T + t);
+    return 1.0f / sqrtf(s / (float)a.rs_K + a.rs_eps);
+}
+
+// Epilogue of tokens t0..t0+n-1 (n <= N) of weight row r (row q * 32 + lane of row tile
+// rt).  The residual reads are all issued before any write: a read after a write to the
+// same array cannot be moved ahead of it, so element-by-element read-add-write would
+// queue N round trips.  rsc: the folded norm's scales of tokens t0.. (null: none).
 template <int N>
-__device__ __forceinline__ void epi_apply_n(const TcGemmArgs &a, int t0, int r, const float *v, int n, int lane) {
-    if (a.mode == TC_RESIDUAL) {
+__device__ __forceinline__ void epi_apply_n(const TcGemmArgs &a, int t0, int r, float *v, int n, int lane, int q,
+                                            int rt, const float *rsc) {
+    if (rsc) {
+#pragma unroll
+        for (int j = 0; j < N; ++j) v[j] *= rsc[j];
+    }
+    if (a.mode == TC_RESIDUAL || a.mode == TC_RESIDUAL_NORM) {
         float old[N];
 #pragma unroll
         for (int j = 0; j < N; ++j) old[j] = j < n ? a.out[(size_t)(t0 + j) * a.ldo + r] : 0.f;
 #pragma unroll
-        for (int j = 0; j < N; ++j)
-            if (j < n) a.out[(size_t)(t0 + j) * a.ldo + r] = old[j] + v[j];
+        for (int j = 0; j < N; ++j) {
+            old[j] += v[j];
+            if (j < n) a.out[(size_t)(t0 + j) * a.ldo + r] = old[j];
+        }
+        if (a.mode == TC_RESIDUAL_NORM) {
+            // the next norm's input parts, and this warp's 32 rows' sum of squares per
+            // token (a shuffle tree; one partial per row-tile quarter)
+            const float g = a.norm_gamma[r];
+#pragma unroll
+            for (int j = 0; j < N; ++j) {
+                if (j < n) {
+                    const float y = g * old[j];
+                    const __nv_bfloat16 h = __float2bfloat16_rn(y);
+                    a.nh[(size_t)(t0 + j) * a.R + r] = h;
+                    a.nl[(size_t)(t0 + j) * a.R + r] = __float2bfloat16_rn(y - __bfloat162float(h));
+                }
+                float sq = j < n ? old[j] * old[j] : 0.f;
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                if (lane == 0 && j < n) a.ss_out[(size_t)(rt * 4 + q) * a.T + t0 + j] = sq;
+            }
+        }
     } else {
 #pragma unroll
         for (int j = 0; j < N; ++j)
@@ -230,6 +265,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *is_last = reinterpret_cast<int *>(tmem_slot + 2);
+    float *rsm = reinterpret_cast<float *>(sm + (size_t)C::kStages * C::kStage + 256);   // [BN] folded-norm scales
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KCt = a.K / kBK;          // chunks of one tap
@@ -370,11 +406,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int row_in_tile = q * 32 + lane;
         constexpr int kEpiT = kEpiWarps * 32;
         pdl_wait();   // outputs, residuals, scratch and counters may belong to the previous kernel
-        int local = 0;
+        int local = 0, rs_tile = -1;
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++local) {
             const Unit x = unit_of(u, splits, tok_tiles, KC);
             const int acc = local & 1;
             const uint32_t use = (uint32_t)(local >> 1);
+            if (a.rs_part && x.nt != rs_tile) {
+                // the folded norm's scales of this token tile, while the products run
+                named_sync(1, kEpiT);   // the previous tile's scales are no longer read
+                const int et = (warp - 2) * 32 + lane;
+                for (int t = et; t < BN; t += kEpiT) {
+                    const int tt = x.nt * BN + t;
+                    rsm[t] = tt < a.T ? rms_scale_of(a, tt) : 0.f;
+                }
+                named_sync(1, kEpiT);
+                rs_tile = x.nt;
+            }
             bool ok = true;
             if (lane == 0) ok = role_wait(&acc_full[acc], use & 1, abort_flag, a.status);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -389,7 +436,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     float v[16];
                     tc_ld16(tbase + (uint32_t)c0, v);
                     const int t0 = x.nt * BN + c0;
-                    epi_apply_n<16>(a, t0, r, v, a.T - t0 < 16 ? a.T - t0 : 16, lane);
+                    epi_apply_n<16>(a, t0, r, v, a.T - t0 < 16 ? a.T - t0 : 16, lane, q, x.rt,
+                                    a.rs_part ? rsm + (t0 - x.nt * BN) : nullptr);
                 }
             } else {
                 float *part = a.partial + (size_t)u * BN * kBM;
@@ -446,7 +494,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         const int t0 = x.nt * BN + c;
                         int n = c_hi - c < 4 ? c_hi - c : 4;
                         if (a.T - t0 < n) n = a.T - t0;
-                        epi_apply_n<4>(a, t0, r, v, n, lane);
+                        epi_apply_n<4>(a, t0, r, v, n, lane, q, x.rt, a.rs_part ? rsm + (t0 - x.nt * BN) : nullptr);
                     }
                 }
                 named_sync(1, kEpiT);
@@ -608,6 +656,8 @@ cudaError_t launch_tc_gemm(const TcGemmPlan &p, const void *w, const void *x_hi,
     if (p.splits > 1 && (!a.partial || !a.tile_counter || p.units > p.grid)) return cudaErrorInvalidValue;
     if (a.mode == TC_SWIGLU && (!a.act_hi || !a.act_lo)) return cudaErrorInvalidValue;
     if (a.mode == TC_STORE_RT && a.ldt <= 0) return cudaErrorInvalidValue;
+    if (a.mode == TC_RESIDUAL_NORM && (!a.norm_gamma || !a.nh || !a.nl || !a.ss_out)) return cudaErrorInvalidValue;
+    if (a.rs_part && (a.rs_tiles < 1 || a.rs_K < 1)) return cudaErrorInvalidValue;
     // every tap's weight slab inside W
     for (int j = 0; j < a.taps; j += a.taps - 1 > 0 ? a.taps - 1 : 1) {
         const int slab = a.w_slab0 + j * a.w_slab_step;
