@@ -93,6 +93,16 @@ typedef struct {
      * All 0: plain RoPE.  Otherwise t >= h == w > 0 and t + h + w == head_dim/2.
      * The streams differ only for prompt positions given to qd_prefill_mrope. */
     int mrope_section[3];
+    /* Weight-only 8-bit matrices ("audio.cpp Rockchip NPU build notes": the talker's
+     * Q8_0 weights): 1 quantises every layer matrix and output head at qd_create into
+     * rows of K int8 codes and K/32 IEEE-half block scales (d = max|w| / 127 per 32
+     * weights along K, code = round(w / d) half away from zero, d rounded to a half;
+     * qd_quantize_q8's arithmetic); the step multiplies each code by its block's
+     * stored scale.  The embedding table, norms and KV cache keep dtype.  Only the
+     * persistent decode step runs such a model (bf16 ASR and Talker shapes):
+     * QD_EUNSUPPORTED otherwise, for the batched API, and for qd_time_kernel's GEMV
+     * kernels (which 0-3, 5).  Prompts run one step per position.  0: off. */
+    int weight_q8;
 } qd_config;
 
 /* Per-layer weights: device pointers, row-major [out, in], in the config's

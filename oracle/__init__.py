@@ -156,13 +156,17 @@ def sample(logits: np.ndarray, top_k: int, temperature: float, top_p: float, u: 
     return int(i), mg.value
 
 
-def make_config(shape, acc64: bool = False, buckets: Optional[Sequence[int]] = None) -> Config:
-    """Oracle config from a ``workloads.Shape``."""
+def make_config(shape, acc64: bool = False, buckets: Optional[Sequence[int]] = None,
+                weights_f32: bool = False) -> Config:
+    """Oracle config from a ``workloads.Shape``; ``weights_f32`` takes every weight as
+    float32 while the cache keeps the shape's type (a bf16 model whose matrices were
+    replaced by their dequantised 8-bit rows, ``dequantize_q8``)."""
     c = Config()
     c.hidden, c.n_layers = shape.hidden, shape.n_layers
     c.n_q_heads, c.n_kv_heads, c.head_dim = shape.n_q_heads, shape.n_kv_heads, shape.head_dim
     c.ffn, c.vocab, c.embed_rows = shape.ffn, shape.vocab, shape.embed_rows
-    c.w_bf16 = c.kv_bf16 = int(shape.bf16)
+    c.w_bf16 = 0 if weights_f32 else int(shape.bf16)
+    c.kv_bf16 = int(shape.bf16)
     c.qk_norm, c.n_heads_out, c.eos_mask_id = int(shape.qk_norm), shape.n_heads_out, shape.eos_mask_id
     b = list(shape.buckets if buckets is None else buckets)
     c.n_buckets = len(b)
@@ -198,10 +202,10 @@ class Oracle:
     """One decode stream on the CPU oracle."""
 
     def __init__(self, shape, weights: Dict[str, np.ndarray], acc64: bool = False,
-                 buckets: Optional[Sequence[int]] = None):
+                 buckets: Optional[Sequence[int]] = None, weights_f32: bool = False):
         self.L = _lib_handle()
         self.shape = shape
-        self.cfg = make_config(shape, acc64, buckets)
+        self.cfg = make_config(shape, acc64, buckets, weights_f32)
         self._table, self._keep = weight_table(shape, weights)
         st = ctypes.c_int(0)
         self.h = self.L.orc_create(ctypes.byref(self.cfg), ctypes.cast(self._table, ctypes.c_void_p), ctypes.byref(st))
@@ -496,6 +500,33 @@ def quantize_q8(w: np.ndarray):
     if st != OK:
         raise OracleError(st, "quantize_q8")
     return codes, scales
+
+
+def dequantize_q8(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """The matrix the 8-bit rows stand for: each code times its 32-weight block's half
+    scale, float32 [rows, K] (exact: an 8-bit integer times an 11-bit significand)."""
+    codes = np.asarray(codes, np.int8)
+    d = np.asarray(scales, np.uint16).view(np.float16).astype(np.float32)
+    return codes.astype(np.float32) * np.repeat(d, 32, axis=1)
+
+
+def q8_model_weights(shape, weights: Dict[str, np.ndarray]) -> Dict[str, np.ndarray]:
+    """Weights of a model whose layer matrices and output heads are held as 8-bit rows
+    (the weight-only Q8_0 scheme of "audio.cpp Rockchip NPU build notes"): those are
+    quantised from their float32 values and replaced by the dequantised matrices; the
+    embedding table and the norm gammas are the same values as float32.  For an Oracle
+    with ``weights_f32``."""
+    mats = ("wq", "wk", "wv", "wo", "wg", "wu", "wd")
+    out = {}
+    for k, v in weights.items():
+        if v.dtype == np.uint16:                       # bfloat16 bits: the upper half of a float32
+            f = (np.asarray(v).astype(np.uint32) << 16).view(np.float32)
+        else:
+            f = np.asarray(v, np.float32)
+        if k.startswith("lm_head.") or k.rsplit(".", 1)[-1] in mats:
+            f = dequantize_q8(*quantize_q8(f))
+        out[k] = np.ascontiguousarray(f, np.float32)
+    return out
 
 
 def gemv_q8(codes: np.ndarray, scales: np.ndarray, x: np.ndarray) -> np.ndarray:

@@ -40,7 +40,9 @@ class Trace:
 
 
 class Pair:
-    def __init__(self, shape, weights, buckets=None, taps: bool = True, graphs: bool = True):
+    def __init__(self, shape, weights, buckets=None, taps: bool = True, graphs: bool = True, q8: bool = False):
+        """``q8``: the GPU model holds its matrices as 8-bit rows (qd_config.weight_q8) and
+        the oracle runs on the dequantised matrices (float32 weights, the shape's cache)."""
         import torch
         import oracle as O
         import transformer_autoregressive_decode_gb300 as qd
@@ -48,9 +50,12 @@ class Pair:
 
         self.qd, self.torch, self.shape = qd, torch, shape
         self.dev_w = upload(weights)
-        self.h = qd.qd_create(self.dev_w, config_from_shape(shape, buckets))
+        self.h = qd.qd_create(self.dev_w, config_from_shape(shape, buckets, weight_q8=q8))
         qd.qd_set_graphs(self.h, graphs)
-        self.ref = O.Oracle(shape, weights, buckets=buckets)
+        if q8:
+            self.ref = O.Oracle(shape, O.q8_model_weights(shape, weights), buckets=buckets, weights_f32=True)
+        else:
+            self.ref = O.Oracle(shape, weights, buckets=buckets)
         self.taps = taps
         if taps:
             self.t_hidden = torch.empty((shape.n_layers + 1, shape.hidden), dtype=torch.float32, device="cuda")

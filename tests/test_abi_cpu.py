@@ -63,9 +63,14 @@ def _cfg(qd, **kw):
     (dict(eos_mask_id=1024), "QD_EINVAL"),
     (dict(rep_penalty=0.0), "QD_EINVAL"),
     (dict(n_layers=0), "QD_EINVAL"),
+    (dict(weight_q8=True), "QD_EUNSUPPORTED"),               # 8-bit rows need bf16
+    (dict(bf16=True, weight_q8=2), "QD_EINVAL"),
 ])
 def test_create_validates_config_before_device_work(qd, bad, expect):
+    q8 = bad.pop("weight_q8", None) if bad.get("weight_q8") == 2 else None
     cfg = _cfg(qd, **bad)
+    if q8 is not None:
+        cfg.weight_q8 = q8                                     # past make_config's bool
     out = ctypes.c_void_p(123)
     st = qd._lib.qd_create(None, ctypes.byref(cfg), None, ctypes.byref(out))
     assert qd.qd_status_string(st).startswith(expect)

@@ -89,3 +89,34 @@ def test_gemv_is_the_dequantised_matvec():
 def test_bad_shapes():
     with pytest.raises(O.OracleError):
         O.quantize_q8(np.zeros((2, 48), np.float32))
+
+
+def test_dequantized_rows_reproduce_the_gemv():
+    """dequantize_q8 (numpy) against the oracle's own 8-bit GEMV (C): the product of the
+    dequantised matrix in float64 is within the GEMV's fp32 accumulation bound."""
+    rng = np.random.default_rng(5)
+    w = rng.normal(0.0, 0.02, size=(37, 256)).astype(np.float32)
+    w[3, 32:64] = 0.0
+    codes, scales = O.quantize_q8(w)
+    deq = O.dequantize_q8(codes, scales)
+    assert deq.dtype == np.float32 and deq.shape == w.shape
+    assert np.all(deq[3, 32:64] == 0.0)
+    assert np.max(np.abs(deq - w)) <= np.max(np.abs(w)) / 127 * 0.5 * (1 + 2.0 ** -10) + 1e-12
+    x = rng.normal(size=256).astype(np.float32)
+    ref = deq.astype(np.float64) @ x.astype(np.float64)
+    mag = np.abs(deq.astype(np.float64)) @ np.abs(x.astype(np.float64))
+    assert np.all(np.abs(O.gemv_q8(codes, scales, x) - ref) <= 2 * 256 * 2.0 ** -24 * mag + 1e-30)
+
+
+def test_q8_model_weights_replace_only_the_matrices():
+    import workloads as W
+    s = W.scaled(W.ASR, n_layers=1, name="asr1q")
+    w = W.model_weights(s)
+    q = O.q8_model_weights(s, w)
+    assert set(q) == set(w)
+    as_f32 = lambda v: (v.astype(np.uint32) << 16).view(np.float32)
+    for k in ("embed", "final_norm", "layers.0.attn_norm", "layers.0.mlp_norm"):
+        assert np.array_equal(q[k], as_f32(w[k]))
+    for k in ("layers.0.wq", "layers.0.wd", "lm_head.0"):
+        assert not np.array_equal(q[k], as_f32(w[k]))
+        assert np.array_equal(q[k], O.dequantize_q8(*O.quantize_q8(as_f32(w[k]))))

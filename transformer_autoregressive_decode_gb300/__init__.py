@@ -50,7 +50,7 @@ class qd_config(ctypes.Structure):
         "qk_norm", "n_heads_out", "eos_mask_id", "n_buckets")] + [
         ("buckets", ctypes.c_int * QD_MAX_BUCKETS),
         ("rms_eps", ctypes.c_double), ("rope_theta", ctypes.c_double), ("rep_penalty", ctypes.c_double),
-        ("mrope_section", ctypes.c_int * 3)]
+        ("mrope_section", ctypes.c_int * 3), ("weight_q8", ctypes.c_int)]
 
 
 class qd_layer_weights(ctypes.Structure):
@@ -153,7 +153,7 @@ def _check(h: Optional[Handle], st: int):
 
 def make_config(hidden, n_layers, n_q_heads, n_kv_heads, head_dim, ffn, vocab, embed_rows, bf16, qk_norm,
                 n_heads_out=1, eos_mask_id=-1, buckets: Sequence[int] = (128,), rms_eps=1e-6, rope_theta=1e6,
-                rep_penalty=1.0, mrope_section: Sequence[int] = (0, 0, 0)) -> qd_config:
+                rep_penalty=1.0, mrope_section: Sequence[int] = (0, 0, 0), weight_q8: bool = False) -> qd_config:
     c = qd_config()
     c.hidden, c.n_layers, c.n_q_heads, c.n_kv_heads = hidden, n_layers, n_q_heads, n_kv_heads
     c.head_dim, c.ffn, c.vocab, c.embed_rows = head_dim, ffn, vocab, embed_rows
@@ -165,6 +165,7 @@ def make_config(hidden, n_layers, n_q_heads, n_kv_heads, head_dim, ffn, vocab, e
     c.rms_eps, c.rope_theta, c.rep_penalty = rms_eps, rope_theta, rep_penalty
     for i, v in enumerate(mrope_section):
         c.mrope_section[i] = int(v)
+    c.weight_q8 = int(bool(weight_q8))
     return c
 
 

@@ -584,7 +584,7 @@ qd_status model_prefill_batched(qd_model *m, const float *embeds_dev, const int3
                                 const int *rope_pos, int rope_stride) {
     const qd_config &c = m->cfg;
     TcGemmPlan plans[5];
-    if (!m->bf16 || c.n_heads_out != 1 || !m->embed || !prefill_plans(m, 1, n, plans)) return QD_EUNSUPPORTED;
+    if (!m->bf16 || m->q8 || c.n_heads_out != 1 || !m->embed || !prefill_plans(m, 1, n, plans)) return QD_EUNSUPPORTED;
     if (!m->pf_batch) {
         qd_batch_handle nb = nullptr;
         const std::string err = m->err;
@@ -634,7 +634,7 @@ qd_status qd_batch_create(qd_handle model, int n_streams, int smax, qd_batch_han
     const qd_config &c = m->cfg;
     if (n_streams < 1 || n_streams > 1024) return fail(m, QD_EINVAL, "n_streams %d out of range", n_streams);
     if (smax < 32 || smax % 32) return fail(m, QD_EINVAL, "smax must be a positive multiple of 32");
-    if (!m->bf16) return fail(m, QD_EUNSUPPORTED, "the batched path needs bf16 weights");
+    if (!m->bf16 || m->q8) return fail(m, QD_EUNSUPPORTED, "the batched path needs bf16 weights");
     if (c.n_heads_out != 1 || !m->embed) return fail(m, QD_EUNSUPPORTED, "the batched path needs one head and an embedding table");
     const int rows_qkv = m->q_dim() + 2 * m->kv_dim();
     int sms = m->num_sms;

@@ -40,6 +40,10 @@
 // chunk sums in warp order.  RMSNorm is a scalar per vector, so W (g * x * r) is
 // computed as r * W (g * x): the chunk sums of squares travel beside the row partials
 // and r is applied by the row's thread.
+#include <cuda_fp16.h>
+
+#include <type_traits>
+
 #include "decode_common.cuh"
 
 namespace qd {
@@ -472,6 +476,139 @@ __device__ __forceinline__ bool kc_gemv_mma(const Ring &R, uint32_t &sidx, int n
     return true;
 }
 
+// ---- weight-only 8-bit rows (q8_row_bytes: K int8 codes, then K / 32 half scales)
+
+// Marker of the 8-bit head's register slices: a lane holds 16 consecutive columns of
+// each 512-column segment (the 16 codes of one 16-byte load).
+struct Q8Code {};
+template <> struct Elem<Q8Code> {
+    static constexpr int kPer16B = 16;
+};
+
+// The four int8 codes of a 32-bit word as floats, lowest byte first.
+__device__ __forceinline__ void q8_word(int u, float *f) {
+    f[0] = (float)((u << 24) >> 24);
+    f[1] = (float)((u << 16) >> 24);
+    f[2] = (float)((u << 8) >> 24);
+    f[3] = (float)(u >> 24);
+}
+// E consecutive int8 codes at p as floats (p aligned to E bytes).
+template <int E>
+__device__ __forceinline__ void q8_codes(const uint8_t *p, float *f) {
+    if constexpr (E == 4) {
+        q8_word(*reinterpret_cast<const int *>(p), f);
+    } else if constexpr (E == 2) {
+        const int u = *reinterpret_cast<const short *>(p);
+        f[0] = (float)((u << 24) >> 24);
+        f[1] = (float)(u >> 8);
+    } else {
+        static_assert(E == 1, "codes per lane");
+        f[0] = (float)*reinterpret_cast<const int8_t *>(p);
+    }
+}
+__device__ __forceinline__ float q8_scale(const uint8_t *row, int K, int col) {
+    return __half2float(*reinterpret_cast<const __half *>(row + K + (col >> 5) * 2));
+}
+
+// kc_gemv on 8-bit rows: the same partial sums, each lane's E codes of a row times its
+// E input values, scaled by their 32-weight block's half scale (the codes of a lane
+// never straddle a block), accumulated over the chunks.
+template <int EL>
+__device__ __forceinline__ bool kc_gemv_q8(const Ring &R, uint32_t &sidx, int nrows, int rps, int K, int colw, int nc,
+                                           const float *xw, float *part) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t rb = q8_row_bytes(K);
+    const int nst = (nrows + rps - 1) / rps;
+#pragma unroll 1
+    for (int st = 0; st < nst; ++st) {
+        const uint8_t *sb = stage_get(R, sidx + st);
+        if (!sb) return false;
+        const int n = min_c(rps, nrows - st * rps);
+#pragma unroll 1
+        for (int g0 = 0; g0 < n; g0 += 8) {
+            float acc[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) acc[r] = 0.f;
+#pragma unroll 1
+            for (int c = 0; c < nc; ++c) {
+                float xv[EL];
+                load_elems<float, EL>(xw + c * 32 * EL + lane * EL, xv);
+                const int col = colw + c * 32 * EL + lane * EL;
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    // rows past n re-read row n - 1 (counted zero below)
+                    const uint8_t *rp = sb + (size_t)(g0 + r < n ? g0 + r : n - 1) * rb;
+                    float f[EL];
+                    q8_codes<EL>(rp + col, f);
+                    float d = 0.f;
+#pragma unroll
+                    for (int e = 0; e < EL; ++e) d = fmaf(f[e], xv[e], d);
+                    acc[r] = fmaf(q8_scale(rp, K, col), d, acc[r]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 8; ++r) acc[r] = g0 + r < n ? acc[r] : 0.f;
+            const float v = treduce<8>(acc, lane);
+            const int row = g0 + lane / 4;
+            if ((lane & 3) == 0 && row < n) part[st * rps + row] = v;
+        }
+        stage_put(R, sidx + st, lane);
+    }
+    sidx += nst;
+    return true;
+}
+
+// The head on 8-bit rows: each consumer warp takes whole rows (two at a time), a lane
+// 16 codes of each 512-column segment against xr (Elem<Q8Code> slices), scaled per
+// half block; one butterfly leaves row q's sum in lane 16 q; res[row] gets it.
+template <int NSEG>
+__device__ __forceinline__ bool gemv_consume_q8(const Ring &R, uint32_t &sidx, int nrows, int rps, int K,
+                                                const float *xr, float *res) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rb = q8_row_bytes(K);
+    for (int rbase = 0; rbase < nrows; rbase += rps) {
+        const uint8_t *sbase = stage_get(R, sidx);
+        if (!sbase) return false;
+        const int n = nrows - rbase < rps ? nrows - rbase : rps;
+        for (int r = warp; r < n; r += 2 * kNW) {
+            float acc[2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int rq = r + q * kNW;
+                const uint8_t *rp = sbase + (size_t)(rq < n ? rq : r) * rb;
+                float a2 = 0.f;
+#pragma unroll
+                for (int sg = 0; sg < NSEG; ++sg) {
+                    const uint4 w = *reinterpret_cast<const uint4 *>(rp + sg * 512 + lane * 16);
+                    float f[16];
+                    q8_word((int)w.x, f);
+                    q8_word((int)w.y, f + 4);
+                    q8_word((int)w.z, f + 8);
+                    q8_word((int)w.w, f + 12);
+                    float d = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) d = fmaf(f[e], xr[sg * 16 + e], d);
+                    a2 = fmaf(q8_scale(rp, K, sg * 512 + lane * 16), d, a2);
+                }
+                acc[q] = rq < n ? a2 : 0.f;
+            }
+            const bool b4 = (lane & 16) != 0;
+            float v = b4 ? acc[1] : acc[0];
+            const float sx = b4 ? acc[0] : acc[1];
+            v += __shfl_xor_sync(0xffffffffu, sx, 16);
+            v += __shfl_xor_sync(0xffffffffu, v, 8);
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            const int rq = r + (b4 ? kNW : 0);
+            if ((lane & 15) == 0 && rq < n) res[rbase + rq] = v;
+        }
+        stage_put(R, sidx, lane);
+        ++sidx;
+    }
+    return true;
+}
+
 // Sum over the consumer warps, in warp order, of entry i of a [kNW][ps] table.
 __device__ __forceinline__ float warp_parts(const float *tab, int ps, int i) {
     float v = 0.f;
@@ -617,11 +754,14 @@ constexpr int kStepThreads = (kNW + 4) * 32;
 constexpr int kProducerRegs = 40, kConsumerRegs = 232;
 static_assert(4 * 32 * kProducerRegs + kNW * 32 * kConsumerRegs == kStepThreads * 168, "register split");
 
-template <typename WT, int HD, int KH, int KQ, int KF, int KVH>
+template <typename WT, int HD, int KH, int KQ, int KF, int KVH, bool Q8 = false>
 __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const StepArgs a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     typedef WT KT;
-    constexpr int EPL = Elem<WT>::kPer16B;
+    // Q8: the layer matrices and heads as 8-bit rows (q8_row_bytes); the embedding table
+    // and the cache stay WT
+    using HT = typename std::conditional<Q8, Q8Code, WT>::type;   // the head's slices
+    constexpr int EPL = Elem<HT>::kPer16B;
     constexpr int SEGW = 32 * EPL;
     constexpr int NS_H = KH / SEGW;                       // the head's segments per warp
     constexpr int ES = (int)sizeof(WT);
@@ -710,13 +850,19 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
             bool ok = true;
             for (int l = 0; l < a.n_layers && ok && !ctl[0]; ++l) {
                 const LayerDev &Ld = a.layers[l];
-                // bf16 layer rows at the tensor-core pitch; fp32 rows packed
+                // bf16 layer rows at the tensor-core pitch; 8-bit and fp32 rows packed
                 auto rows = [&](const void *w, int r0, int n, uint32_t rb, int K, int rps) {
-                    const uint8_t *src = reinterpret_cast<const uint8_t *>(w) + (size_t)r0 * rb;
-                    if constexpr (sizeof(WT) == 2)
-                        return produce_rows_pitched(R, sidx, src, n, rb, mma_pitch(K), mma_rps(K), pw);
-                    else
-                        return produce_rows(R, sidx, src, n, rb, rps, pw);
+                    if constexpr (Q8) {
+                        const uint32_t qb = q8_row_bytes(K);
+                        return produce_rows(R, sidx, reinterpret_cast<const uint8_t *>(w) + (size_t)r0 * qb, n, qb,
+                                            q8_rps(K), pw);
+                    } else if constexpr (sizeof(WT) == 2) {
+                        return produce_rows_pitched(R, sidx, reinterpret_cast<const uint8_t *>(w) + (size_t)r0 * rb,
+                                                    n, rb, mma_pitch(K), mma_rps(K), pw);
+                    } else {
+                        return produce_rows(R, sidx, reinterpret_cast<const uint8_t *>(w) + (size_t)r0 * rb, n, rb,
+                                            rps, pw);
+                    }
                 };
                 ok = ok && rows(Ld.w_qkv, r0_qkv, n_qkv, rb_h, KH, a.rps_h);
                 if (has_item) {
@@ -733,7 +879,11 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
             }
             if (ok && a.with_head && !ctl[0]) {
                 const uint8_t *Wh = reinterpret_cast<const uint8_t *>(a.heads[a.st->head_idx]);
-                ok = produce_rows(R, sidx, Wh + (size_t)r0_hd * rb_h, n_hd, rb_h, a.rps_h, pf);
+                if constexpr (Q8)
+                    ok = produce_rows(R, sidx, Wh + (size_t)r0_hd * q8_row_bytes(KH), n_hd, q8_row_bytes(KH),
+                                      q8_rps(KH), pf);
+                else
+                    ok = produce_rows(R, sidx, Wh + (size_t)r0_hd * rb_h, n_hd, rb_h, a.rps_h, pf);
             }
             if (!ok) atomicOr(&a.st->status, DEV_ERR_WAIT_TIMEOUT);
             ctl[1] = (int)sidx;
@@ -948,16 +1098,20 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
             const float *gam;
             int K, nrows, rps;
             uint32_t rbytes;
-            constexpr bool kMma = sizeof(WT) == 2;
+            constexpr bool kMma = sizeof(WT) == 2 && !Q8;
+            // rows of a ring stage of each phase's K
+            constexpr int rpsH = Q8 ? q8_rps(KH) : mma_rps(KH), rpsQ = Q8 ? q8_rps(KQ) : mma_rps(KQ),
+                          rpsF = Q8 ? q8_rps(KF) : mma_rps(KF);
+            constexpr bool kPacked = Q8 || kMma;   // rows per stage from the layout, not the host
             if (ph == 0) {
                 src = l ? a.tg + (size_t)(l - 1) * a.tg_stride + a.tg_xe : nullptr;
-                gam = Ld.attn_norm; K = KH; nrows = n_qkv; rps = kMma ? mma_rps(KH) : a.rps_h; rbytes = rb_h;
+                gam = Ld.attn_norm; K = KH; nrows = n_qkv; rps = kPacked ? rpsH : a.rps_h; rbytes = rb_h;
             } else if (ph == 1) {
-                src = T + a.tg_att; gam = nullptr; K = KQ; nrows = n_x; rps = kMma ? mma_rps(KQ) : a.rps_q; rbytes = rb_q;
+                src = T + a.tg_att; gam = nullptr; K = KQ; nrows = n_x; rps = kPacked ? rpsQ : a.rps_q; rbytes = rb_q;
             } else if (ph == 2) {
-                src = T + a.tg_xc; gam = Ld.mlp_norm; K = KH; nrows = n_gu; rps = kMma ? mma_rps(KH) : a.rps_h; rbytes = rb_h;
+                src = T + a.tg_xc; gam = Ld.mlp_norm; K = KH; nrows = n_gu; rps = kPacked ? rpsH : a.rps_h; rbytes = rb_h;
             } else {
-                src = T + a.tg_act; gam = nullptr; K = KF; nrows = n_x; rps = kMma ? mma_rps(KF) : a.rps_f; rbytes = rb_f;
+                src = T + a.tg_act; gam = nullptr; K = KF; nrows = n_x; rps = kPacked ? rpsF : a.rps_f; rbytes = rb_f;
             }
             const int nc = K / (256 * EL);          // column chunks of 32 x EL per warp
             const int colw = warp * (K / kNW);       // this warp's first column
@@ -1047,7 +1201,19 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
             float ss = 0.f;
             float *xw = xs + (size_t)warp * XSW;      // this warp's slice of the input, times gamma
             float *part = kc_part + buf * kNW * PS;
-            if constexpr (kMma) {
+            if constexpr (Q8) {
+#pragma unroll
+                for (int cc = 0; cc < NCMAX; ++cc)
+                    if (cc < nc) {
+#pragma unroll
+                        for (int e = 0; e < EL; ++e) {
+                            ss = fmaf(x[cc][e], x[cc][e], ss);
+                            xw[cc * 32 * EL + e * 32 + lane] = x[cc][e] * gv[cc][e];
+                        }
+                    }
+                __syncwarp();
+                if (okw) okw = kc_gemv_q8<EL>(R, sidx, nrows, rps, K, colw, nc, xw, part + warp * PS);
+            } else if constexpr (kMma) {
                 // as two bf16 parts (the slice's K / 8 values twice: the same bytes as fp32)
                 __nv_bfloat16 *x0 = reinterpret_cast<__nv_bfloat16 *>(xw), *x1 = x0 + 16;
 #pragma unroll
@@ -1134,7 +1300,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
             for (int i = tid; i < nw; i += kNC) emw[i] = __ldcg(a.in.emitted + w0 + i);
         if (ok) {
             float xr[NS_H * EPL];
-            smem_slice<WT, NS_H>(xin, colb_h, xr);
+            smem_slice<HT, NS_H>(xin, colb_h, xr);
             if (a.tap_hidden && blockIdx.x == 0 && rr_h == 0) {
 #pragma unroll
                 for (int sg = 0; sg < NS_H; ++sg)
@@ -1143,9 +1309,13 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
                         a.tap_hidden[(size_t)a.n_layers * hidden + colb_h + sg * SEGW + lane * EPL + e] =
                             xr[sg * EPL + e];
             }
-            rmsnorm_slice<WT, NS_H>(xr, gsm, hidden, a.rs_h, colb_h, a.eps, misc,
+            rmsnorm_slice<HT, NS_H>(xr, gsm, hidden, a.rs_h, colb_h, a.eps, misc,
                                     blockIdx.x == 0 ? a.y_out : nullptr);
-            const bool got = gemv_consume<WT, NS_H>(R, sidx, n_hd, a.rps_h, rb_h, a.rs_h, colb_h, xr, res);
+            bool got;
+            if constexpr (Q8)
+                got = gemv_consume_q8<NS_H>(R, sidx, n_hd, q8_rps(KH), KH, xr, res);
+            else
+                got = gemv_consume<WT, NS_H>(R, sidx, n_hd, a.rps_h, rb_h, a.rs_h, colb_h, xr, res);
             ok = !named_sync_or(1, kNC, !got || (tid == 0 && misc_i[6] != 0));
         }
         if (ok) {
@@ -1301,18 +1471,20 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
 typedef void (*StepFn)(const StepArgs);
 
 // Shapes with an instantiation: (dtype, head_dim, hidden, q_dim, ffn)
-static StepFn step_fn(bool bf16, int hd, int hidden, int q_dim, int ffn, int kvh) {
-    if (!bf16 && hd == 64 && hidden == 256 && q_dim == 256 && ffn == 768 && kvh == 2)
+static StepFn step_fn(bool bf16, int hd, int hidden, int q_dim, int ffn, int kvh, bool q8) {
+    if (!q8 && !bf16 && hd == 64 && hidden == 256 && q_dim == 256 && ffn == 768 && kvh == 2)
         return decode_step_kernel<float, 64, 256, 256, 768, 2>;             // one-layer fp32 decoder
-    if (bf16 && hd == 64 && hidden == 512 && q_dim == 512 && ffn == 2048 && kvh == 8)
-        return decode_step_kernel<__nv_bfloat16, 64, 512, 512, 2048, 8>;    // ASR decoder
-    if (bf16 && hd == 128 && hidden == 1024 && q_dim == 2048 && ffn == 3072 && kvh == 8)
-        return decode_step_kernel<__nv_bfloat16, 128, 1024, 2048, 3072, 8>; // talker / code predictor
+    if (bf16 && hd == 64 && hidden == 512 && q_dim == 512 && ffn == 2048 && kvh == 8)   // ASR decoder
+        return q8 ? decode_step_kernel<__nv_bfloat16, 64, 512, 512, 2048, 8, true>
+                  : decode_step_kernel<__nv_bfloat16, 64, 512, 512, 2048, 8>;
+    if (bf16 && hd == 128 && hidden == 1024 && q_dim == 2048 && ffn == 3072 && kvh == 8)   // talker / code predictor
+        return q8 ? decode_step_kernel<__nv_bfloat16, 128, 1024, 2048, 3072, 8, true>
+                  : decode_step_kernel<__nv_bfloat16, 128, 1024, 2048, 3072, 8>;
     return nullptr;
 }
 
-bool persistent_supported(bool bf16, int hd, int hidden, int q_dim, int ffn, int kvh) {
-    return step_fn(bf16, hd, hidden, q_dim, ffn, kvh) != nullptr;
+bool persistent_supported(bool bf16, int hd, int hidden, int q_dim, int ffn, int kvh, bool q8) {
+    return step_fn(bf16, hd, hidden, q_dim, ffn, kvh, q8) != nullptr;
 }
 
 size_t persistent_att_bytes(int group, int hd, int chunk_max) {
@@ -1322,16 +1494,16 @@ size_t persistent_att_bytes(int group, int hd, int chunk_max) {
     return ((size_t)kNW * hd + (size_t)kNW * 2 + (size_t)hd) * 4;
 }
 
-cudaError_t persistent_init(bool bf16, int hd, int hidden, int q_dim, int ffn, int kvh) {
-    StepFn f = step_fn(bf16, hd, hidden, q_dim, ffn, kvh);
+cudaError_t persistent_init(bool bf16, int hd, int hidden, int q_dim, int ffn, int kvh, bool q8) {
+    StepFn f = step_fn(bf16, hd, hidden, q_dim, ffn, kvh, q8);
     if (!f) return cudaErrorInvalidValue;
     return cudaFuncSetAttribute(reinterpret_cast<const void *>(f), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kStepMaxSmem);
 }
 
 cudaError_t launch_persistent(bool bf16, int hd, int hidden, int q_dim, int ffn, int kvh, const StepArgs &a, int grid,
-                              size_t smem, cudaStream_t s) {
-    StepFn f = step_fn(bf16, hd, hidden, q_dim, ffn, kvh);
+                              size_t smem, cudaStream_t s, bool q8) {
+    StepFn f = step_fn(bf16, hd, hidden, q_dim, ffn, kvh, q8);
     if (!f) return cudaErrorInvalidValue;
     cudaError_t e = cudaMemsetAsync(a.barrier, 0, sizeof(unsigned), s);
     if (e != cudaSuccess) return e;

@@ -86,6 +86,8 @@ static qd_status validate_config(qd_model *m, const qd_config *c) {
                         sec[0], sec[1], sec[2]);
     }
     const bool bf = c->dtype == QD_BF16;
+    if (c->weight_q8 != 0 && c->weight_q8 != 1) return fail(m, QD_EINVAL, "weight_q8 must be 0 or 1");
+    if (c->weight_q8 && !bf) return fail(m, QD_EUNSUPPORTED, "8-bit weights need dtype QD_BF16");
     const int max_pos = c->buckets[c->n_buckets - 1];
     if (c->hidden > 16 * 1024)
         return fail(m, QD_EUNSUPPORTED, "hidden %d too large", c->hidden);
@@ -366,7 +368,7 @@ qd_status enqueue_step(qd_model *m, cudaStream_t s, bool with_head, bool taps) {
     const int h = c.hidden;
     if (m->persistent) {
         CU(launch_persistent(bf, c.head_dim, h, m->q_dim(), c.ffn, c.n_kv_heads, step_args(m, with_head, taps), m->num_sms,
-                             m->smem_step, s));
+                             m->smem_step, s, m->q8));
         return QD_OK;
     }
     for (int l = 0; l < c.n_layers; ++l) {
@@ -461,14 +463,16 @@ static qd_status load_weights(qd_model *m, const qd_weights *w) {
     };
     std::vector<size_t> o_qkv(c.n_layers), o_o(c.n_layers), o_gu(c.n_layers), o_d(c.n_layers), o_an(c.n_layers),
         o_mn(c.n_layers), o_qn(c.n_layers), o_kn(c.n_layers);
+    // bytes of a row of K weights: es per weight, or an 8-bit row (codes + half scales)
+    auto rowb = [&](int K) { return m->q8 ? (size_t)q8_row_bytes(K) : (size_t)K * es; };
     for (int l = 0; l < c.n_layers; ++l) {
-        o_qkv[l] = take((size_t)(qd_ + 2 * kd) * h * es);
-        o_o[l] = take((size_t)h * qd_ * es);
-        o_gu[l] = take((size_t)2 * F * h * es);
-        o_d[l] = take((size_t)h * F * es);
+        o_qkv[l] = take((size_t)(qd_ + 2 * kd) * rowb(h));
+        o_o[l] = take((size_t)h * rowb(qd_));
+        o_gu[l] = take((size_t)2 * F * rowb(h));
+        o_d[l] = take((size_t)h * rowb(F));
     }
     size_t o_heads[QD_MAX_HEADS];
-    for (int j = 0; j < c.n_heads_out; ++j) o_heads[j] = take((size_t)c.vocab * h * es);
+    for (int j = 0; j < c.n_heads_out; ++j) o_heads[j] = take((size_t)c.vocab * rowb(h));
     const size_t o_embed = c.embed_rows ? take((size_t)c.embed_rows * h * es) : 0;
     for (int l = 0; l < c.n_layers; ++l) {
         o_an[l] = take((size_t)h * 4);
@@ -495,16 +499,28 @@ static qd_status load_weights(qd_model *m, const qd_weights *w) {
         L.q_norm = reinterpret_cast<float *>(A + o_qn[l]);
         L.k_norm = reinterpret_cast<float *>(A + o_kn[l]);
         uint8_t *q = reinterpret_cast<uint8_t *>(L.w_qkv);
-        CU(cudaMemcpyAsync(q, W.wq, (size_t)qd_ * h * es, cudaMemcpyDeviceToDevice, s));
-        CU(cudaMemcpyAsync(q + (size_t)qd_ * h * es, W.wk, (size_t)kd * h * es, cudaMemcpyDeviceToDevice, s));
-        CU(cudaMemcpyAsync(q + (size_t)(qd_ + kd) * h * es, W.wv, (size_t)kd * h * es, cudaMemcpyDeviceToDevice, s));
-        CU(cudaMemcpyAsync(L.w_o, W.wo, (size_t)h * qd_ * es, cudaMemcpyDeviceToDevice, s));
-        // gate/up rows interleaved: row 2i = wg[i], row 2i+1 = wu[i]
-        const size_t rb = (size_t)h * es;
-        CU(cudaMemcpy2DAsync(L.w_gu, 2 * rb, W.wg, rb, rb, F, cudaMemcpyDeviceToDevice, s));
-        CU(cudaMemcpy2DAsync(reinterpret_cast<uint8_t *>(L.w_gu) + rb, 2 * rb, W.wu, rb, rb, F,
-                             cudaMemcpyDeviceToDevice, s));
-        CU(cudaMemcpyAsync(L.w_d, W.wd, (size_t)h * F * es, cudaMemcpyDeviceToDevice, s));
+        if (m->q8) {
+            // the same fused layouts, quantised row by row: [wq; wk; wv], gate/up interleaved
+            CU(launch_quantize_rows_q8(W.wq, m->bf16, qd_, h, q, 0, 1, s));
+            CU(launch_quantize_rows_q8(W.wk, m->bf16, kd, h, q, qd_, 1, s));
+            CU(launch_quantize_rows_q8(W.wv, m->bf16, kd, h, q, qd_ + kd, 1, s));
+            CU(launch_quantize_rows_q8(W.wo, m->bf16, h, qd_, L.w_o, 0, 1, s));
+            CU(launch_quantize_rows_q8(W.wg, m->bf16, F, h, L.w_gu, 0, 2, s));
+            CU(launch_quantize_rows_q8(W.wu, m->bf16, F, h, L.w_gu, 1, 2, s));
+            CU(launch_quantize_rows_q8(W.wd, m->bf16, h, F, L.w_d, 0, 1, s));
+        } else {
+            CU(cudaMemcpyAsync(q, W.wq, (size_t)qd_ * h * es, cudaMemcpyDeviceToDevice, s));
+            CU(cudaMemcpyAsync(q + (size_t)qd_ * h * es, W.wk, (size_t)kd * h * es, cudaMemcpyDeviceToDevice, s));
+            CU(cudaMemcpyAsync(q + (size_t)(qd_ + kd) * h * es, W.wv, (size_t)kd * h * es, cudaMemcpyDeviceToDevice,
+                               s));
+            CU(cudaMemcpyAsync(L.w_o, W.wo, (size_t)h * qd_ * es, cudaMemcpyDeviceToDevice, s));
+            // gate/up rows interleaved: row 2i = wg[i], row 2i+1 = wu[i]
+            const size_t rb = (size_t)h * es;
+            CU(cudaMemcpy2DAsync(L.w_gu, 2 * rb, W.wg, rb, rb, F, cudaMemcpyDeviceToDevice, s));
+            CU(cudaMemcpy2DAsync(reinterpret_cast<uint8_t *>(L.w_gu) + rb, 2 * rb, W.wu, rb, rb, F,
+                                 cudaMemcpyDeviceToDevice, s));
+            CU(cudaMemcpyAsync(L.w_d, W.wd, (size_t)h * F * es, cudaMemcpyDeviceToDevice, s));
+        }
         CU(launch_to_f32(W.attn_norm, m->bf16, L.attn_norm, h, s));
         CU(launch_to_f32(W.mlp_norm, m->bf16, L.mlp_norm, h, s));
         if (c.qk_norm) {
@@ -514,7 +530,10 @@ static qd_status load_weights(qd_model *m, const qd_weights *w) {
     }
     for (int j = 0; j < c.n_heads_out; ++j) {
         m->heads[j] = A + o_heads[j];
-        CU(cudaMemcpyAsync(m->heads[j], w->lm_head[j], (size_t)c.vocab * h * es, cudaMemcpyDeviceToDevice, s));
+        if (m->q8)
+            CU(launch_quantize_rows_q8(w->lm_head[j], m->bf16, c.vocab, h, m->heads[j], 0, 1, s));
+        else
+            CU(cudaMemcpyAsync(m->heads[j], w->lm_head[j], (size_t)c.vocab * h * es, cudaMemcpyDeviceToDevice, s));
     }
     if (c.embed_rows) {
         m->embed = A + o_embed;
@@ -610,9 +629,10 @@ static bool plan_launches(qd_model *m) {
     // Layer weights that fit in 60% of L2 stay resident across steps (evict_last);
     // the output head always streams (evict_first).
     size_t layer_bytes = 0;
+    auto mat = [&](int rows, int K) { return (size_t)rows * (m->q8 ? q8_row_bytes(K) : (size_t)K * m->esize); };
     for (int l = 0; l < c.n_layers; ++l)
-        layer_bytes += (size_t)(m->q_dim() + 2 * m->kv_dim() + 3 * c.ffn) * c.hidden * m->esize +
-                       (size_t)c.hidden * m->q_dim() * m->esize;
+        layer_bytes += mat(m->q_dim() + 2 * m->kv_dim() + 2 * c.ffn, c.hidden) + mat(c.hidden, m->q_dim()) +
+                       mat(c.hidden, c.ffn);
     int l2 = 0;
     cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, m->device);
     m->evict_last_layers = layer_bytes * 10 <= (size_t)l2 * 6 ? 1 : 0;
@@ -626,8 +646,11 @@ static bool plan_launches(qd_model *m) {
 static qd_status setup_persistent(qd_model *m) {
     const qd_config &c = m->cfg;
     m->persistent = false;
-    if (std::getenv("QD_PER_PHASE")) return QD_OK;   // debug and profiling only
-    if (!persistent_supported(m->bf16, c.head_dim, c.hidden, m->q_dim(), c.ffn, c.n_kv_heads)) return QD_OK;
+    // 8-bit rows exist only in the persistent step: no per-phase fallback
+    if (std::getenv("QD_PER_PHASE")) return m->q8 ? QD_EUNSUPPORTED : QD_OK;   // debug and profiling only
+    // the 8-bit head takes whole rows per warp
+    if (m->q8) m->rs_h = 1;
+    if (!persistent_supported(m->bf16, c.head_dim, c.hidden, m->q_dim(), c.ffn, c.n_kv_heads, m->q8)) return QD_OK;
     if (m->num_sms < kStepMinSms) return QD_OK;
     const int G = c.n_q_heads / c.n_kv_heads;
     if (c.n_kv_heads * kAttnMaxSplits > m->num_sms) return QD_OK;
@@ -687,7 +710,7 @@ static qd_status setup_persistent(qd_model *m) {
     m->smem_step = align_up(off, 16);
     m->nst_step = nst;
     if (m->smem_step > max_smem) return QD_OK;
-    CU(persistent_init(m->bf16, c.head_dim, c.hidden, m->q_dim(), c.ffn, c.n_kv_heads));
+    CU(persistent_init(m->bf16, c.head_dim, c.hidden, m->q_dim(), c.ffn, c.n_kv_heads, m->q8));
     // layer table
     std::vector<LayerDev> host(c.n_layers);
     for (int l = 0; l < c.n_layers; ++l) {
@@ -773,6 +796,7 @@ qd_status qd_create(const qd_weights *weights, const qd_config *cfg, void *cuda_
     qd_model *m = new qd_model();
     m->cfg = *cfg;
     m->bf16 = cfg->dtype == QD_BF16;
+    m->q8 = cfg->weight_q8 != 0;
     m->esize = m->bf16 ? 2 : 4;
     m->user = reinterpret_cast<cudaStream_t>(cuda_stream);
     // debug and profiling only: launch every kernel without programmatic dependent
@@ -805,6 +829,7 @@ qd_status qd_create(const qd_weights *weights, const qd_config *cfg, void *cuda_
     }
     st = setup_persistent(m);
     if (st) return bail(st);
+    if (m->q8 && !m->persistent) return bail(QD_EUNSUPPORTED);
     m->kv.assign(cfg->n_buckets, nullptr);
     m->graphs[0].assign(cfg->n_buckets, nullptr);
     m->graphs[1].assign(cfg->n_buckets, nullptr);
@@ -1202,6 +1227,8 @@ qd_status qd_time_kernel(qd_handle h, int which, int reps, float *avg_ms) {
     if (reps < 1 || which < 0 || which > 6) return fail(m, QD_EINVAL, "bad which/reps");
     if (m->h_pos == 0) return fail(m, QD_ESTATE, "time_kernel needs a prefilled handle");
     if (which == 6) return time_step(m, reps, avg_ms);
+    if (m->q8 && which != 4)
+        return fail(m, QD_EUNSUPPORTED, "8-bit weights: only the whole step and the attention kernel are timed");
     enter(m);
     CU(cudaStreamSynchronize(m->ls));
     // Save what the timed kernel overwrites (x, the device state and, for attention,

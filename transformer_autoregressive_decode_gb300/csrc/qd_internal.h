@@ -163,6 +163,16 @@ constexpr int kStepRowsMax = 64;
 constexpr int kStepRingStages = 6;
 constexpr int kStepMinSms = 148;
 constexpr int kStepGroupMax = 2;
+
+// Weight-only 8-bit rows of the persistent step ("audio.cpp Rockchip NPU build notes",
+// the talker's Q8_0 weights): a row of K weights is its K int8 codes, then its K / 32
+// block scales as IEEE halves (d = max |w| / 127 per 32 weights, w ~ code * d); rows
+// contiguous.  Bytes of a row, and the rows of a ring slot.
+__host__ __device__ constexpr uint32_t q8_row_bytes(int K) { return (uint32_t)(K + K / 16); }
+__host__ __device__ constexpr int q8_rps(int K) { return kSlotBytes / (int)q8_row_bytes(K); }
+// W [rows, K] (bf16 or fp32) as 8-bit rows at dst: row r to row row0 + r * rstep.
+cudaError_t launch_quantize_rows_q8(const void *w, bool bf16, int rows, int K, void *dst, int row0, int rstep,
+                                    cudaStream_t s);
 // Phase timeline of the traced build: CTAs and stamp slots recorded.
 constexpr int kStepTraceCtas = 160;
 constexpr int kStepTraceSlots = 24;
@@ -174,10 +184,10 @@ constexpr int kStepMaxSmem = 227 * 1024;
 
 // Persistent kernel for (dtype, head_dim, hidden, q_dim, ffn): false if there is no
 // instantiation for the shape (the per-phase kernels are used then).
-bool persistent_supported(bool bf16, int hd, int hidden, int q_dim, int ffn, int kvh);
-cudaError_t persistent_init(bool bf16, int hd, int hidden, int q_dim, int ffn, int kvh);
+bool persistent_supported(bool bf16, int hd, int hidden, int q_dim, int ffn, int kvh, bool q8 = false);
+cudaError_t persistent_init(bool bf16, int hd, int hidden, int q_dim, int ffn, int kvh, bool q8 = false);
 cudaError_t launch_persistent(bool bf16, int hd, int hidden, int q_dim, int ffn, int kvh, const StepArgs &a, int grid,
-                              size_t smem, cudaStream_t s);
+                              size_t smem, cudaStream_t s, bool q8 = false);
 size_t persistent_att_bytes(int group, int hd, int chunk_max);
 
 // Picks (nseg, rs) for K; false if K is not supported.

@@ -27,6 +27,7 @@ struct qd_frame;
 struct qd_model {
     qd_config cfg{};
     bool bf16 = false;
+    bool q8 = false;    // layer matrices and heads as 8-bit rows (qd_config.weight_q8)
     size_t esize = 4;
     int device = 0, num_sms = 0;
     cudaStream_t user = nullptr, ls = nullptr;

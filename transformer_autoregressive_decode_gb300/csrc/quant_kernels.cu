@@ -42,20 +42,48 @@ __device__ __forceinline__ float to_f32<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 
+// One 32-weight block, a warp (lane = weight): the block's code of this lane and the
+// half bits of its scale.
+__device__ __forceinline__ void q8_block(float v, int8_t &code, uint16_t &scale) {
+    float amax = fabsf(v);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float q = d > 0.0f ? roundf(__fdiv_rn(v, d)) : 0.0f;
+    code = (int8_t)q;
+    scale = __half_as_ushort(__float2half_rn(d));
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) quantize_q8_kernel(const T *w, long long n_blocks, int8_t *codes,
                                                           uint16_t *scales) {
     const int lane = threadIdx.x & 31;
     const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
     for (long long b = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < n_blocks; b += warps) {
-        const float v = to_f32(w[b * kQBlock + lane]);
-        float amax = fabsf(v);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float d = __fdiv_rn(amax, 127.0f);
-        const float q = d > 0.0f ? roundf(__fdiv_rn(v, d)) : 0.0f;
-        codes[b * kQBlock + lane] = (int8_t)q;
-        if (lane == 0) scales[b] = __half_as_ushort(__float2half_rn(d));
+        int8_t c;
+        uint16_t d;
+        q8_block(to_f32(w[b * kQBlock + lane]), c, d);
+        codes[b * kQBlock + lane] = c;
+        if (lane == 0) scales[b] = d;
+    }
+}
+
+// Rows of W [rows, K] as 8-bit rows (q8_row_bytes: codes, then half scales): row r goes
+// to row row0 + r * rstep of dst.
+template <typename T>
+__global__ void __launch_bounds__(256) quantize_rows_q8_kernel(const T *w, int rows, int K, uint8_t *dst, int row0,
+                                                               int rstep) {
+    const int lane = threadIdx.x & 31, nb = K / kQBlock;
+    const long long n_blocks = (long long)rows * nb, warps = (long long)gridDim.x * (blockDim.x >> 5);
+    const size_t rb = q8_row_bytes(K);
+    for (long long b = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < n_blocks; b += warps) {
+        const int r = (int)(b / nb), j = (int)(b - (long long)r * nb);
+        int8_t c;
+        uint16_t d;
+        q8_block(to_f32(w[(size_t)r * K + (size_t)j * kQBlock + lane]), c, d);
+        uint8_t *row = dst + (size_t)(row0 + (size_t)r * rstep) * rb;
+        row[(size_t)j * kQBlock + lane] = (uint8_t)c;
+        if (lane == 0) *reinterpret_cast<uint16_t *>(row + K + (size_t)j * 2) = d;
     }
 }
 
@@ -154,6 +182,21 @@ int sm_count() {
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 }  // namespace
+
+cudaError_t launch_quantize_rows_q8(const void *w, bool bf16, int rows, int K, void *dst, int row0, int rstep,
+                                    cudaStream_t s) {
+    if (rows <= 0 || K <= 0 || K % kQBlock) return cudaErrorInvalidValue;
+    const long long n_blocks = (long long)rows * (K / kQBlock);
+    const int grid = (int)std::min<long long>((n_blocks + 7) / 8, (long long)sm_count() * 16);
+    uint8_t *d = static_cast<uint8_t *>(dst);
+    if (bf16)
+        quantize_rows_q8_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(w), rows, K, d,
+                                                                    row0, rstep);
+    else
+        quantize_rows_q8_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float *>(w), rows, K, d, row0, rstep);
+    return cudaGetLastError();
+}
+
 }  // namespace qd
 
 using namespace qd;
