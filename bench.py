@@ -393,6 +393,37 @@ def gpu_line(args, workload, ctx):
               "note": "the LM head quantised to 32-weight blocks with half scales; median of 10 launches "
                       "(after 2), each between CUDA events after a 256 MB write that flushes L2"}
         del codes, scales
+        # the whole decode step with every layer matrix and the head as 8-bit rows
+        # (qd_config.weight_q8): the same trajectory's decode steps, and the step kernel
+        # against the quantised bytes
+        hq = qd.qd_create(upload(w_np), config_from_shape(shape, weight_q8=True))
+        qd.qd_reset(hq)
+        first = qd.qd_prefill(hq, embeds=e_dev)
+        qd.qd_decode_greedy(hq, 4, first, ids)
+        nq = traj - 4
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        qd.qd_decode_greedy(hq, nq, -1, ids)
+        b.record(stream)
+        torch.cuda.synchronize()
+        q8_step_us = 1e3 * a.elapsed_time(b) / nq
+        qd.qd_reset(hq)
+        first = qd.qd_prefill(hq, embeds=e_dev)
+        qd.qd_decode_greedy(hq, traj // 2, first, ids)
+        pq, sq = qd.qd_get_pos(hq)
+        rq = max(1, min(64, sq - pq - 4))
+        q8_kms = qd.qd_time_kernel(hq, qd.KERNEL_STEP, rq)
+        Lq = pq + (rq + 1) // 2 + 3
+        mp = shape.matrix_params()
+        q8_wb = mp * (1 + 2 / 32) + (shape.weight_bytes_per_step() - 2 * mp)
+        q8_kb = q8_wb + Lq * shape.kv_bytes_per_position()
+        qd.qd_destroy(hq)
+        q8["step"] = {"config": "weight_q8: every layer matrix and the head as 8-bit rows; embedding, norms, "
+                                "KV cache bf16",
+                      "decode_step_us": q8_step_us, "bf16_decode_step_us": dec_step_us,
+                      "kernel_ms": q8_kms, "kernel_bytes": q8_kb, "L": Lq,
+                      "achieved_gbs": q8_kb / (q8_kms / 1e3) / 1e9,
+                      "frac": q8_kb / (q8_kms / 1e3) / 1e9 / hbm_peak, "peak_source": peak_src}
 
     # the codec decoder's convolution stages (fp32, CUDA cores: "alu" bound against the
     # fp32 FMA rate of 152 SMs x 128 lanes x 2 flops at the sampled SM clock), each launch

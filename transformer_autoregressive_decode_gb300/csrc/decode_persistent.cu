@@ -336,6 +336,7 @@ __device__ __forceinline__ void stage_put(const Ring &R, uint32_t sidx, int lane
 }
 
 __host__ __device__ constexpr int min_c(int a, int b) { return a < b ? a : b; }
+__host__ __device__ constexpr int max_c(int a, int b) { return a > b ? a : b; }
 
 // Consumer warp: the CTA's `nrows` rows of W, arriving in ring stages of `rps` rows,
 // against this warp's K-chunk: nc column chunks of 32 x EL, whose values (already
@@ -492,65 +493,112 @@ __device__ __forceinline__ void q8_word(int u, float *f) {
     f[2] = (float)((u << 8) >> 24);
     f[3] = (float)(u >> 24);
 }
-// E consecutive int8 codes at p as floats (p aligned to E bytes).
-template <int E>
-__device__ __forceinline__ void q8_codes(const uint8_t *p, float *f) {
-    if constexpr (E == 4) {
-        q8_word(*reinterpret_cast<const int *>(p), f);
-    } else if constexpr (E == 2) {
-        const int u = *reinterpret_cast<const short *>(p);
-        f[0] = (float)((u << 24) >> 24);
-        f[1] = (float)(u >> 8);
-    } else {
-        static_assert(E == 1, "codes per lane");
-        f[0] = (float)*reinterpret_cast<const int8_t *>(p);
-    }
-}
 __device__ __forceinline__ float q8_scale(const uint8_t *row, int K, int col) {
     return __half2float(*reinterpret_cast<const __half *>(row + K + (col >> 5) * 2));
 }
 
-// kc_gemv on 8-bit rows: the same partial sums, each lane's E codes of a row times its
-// E input values, scaled by their 32-weight block's half scale (the codes of a lane
-// never straddle a block), accumulated over the chunks.
-template <int EL>
-__device__ __forceinline__ bool kc_gemv_q8(const Ring &R, uint32_t &sidx, int nrows, int rps, int K, int colw, int nc,
-                                           const float *xw, float *part) {
-    const int lane = threadIdx.x & 31;
-    const uint32_t rb = q8_row_bytes(K);
+// Row pitch in the ring of 8-bit layer rows (codes then scales), 16 bytes past a
+// multiple of 32 words for every supported K (as mma_pitch: the 8 rows a fragment
+// reads at one column fall in different bank groups), and the rows of a stage.
+__host__ __device__ constexpr uint32_t q8_pitch(int K) { return q8_row_bytes(K) + 16; }
+__host__ __device__ constexpr int q8_prs(int K) { return kSlotBytes / (int)q8_pitch(K); }
+
+// d += a b for one m16n8k16 tile (f16 operands, fp32 accumulation)
+__device__ __forceinline__ void mma_f16(float &d0, float &d1, float &d2, float &d3, uint32_t a0, uint32_t a1,
+                                        uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d0), "+f"(d1), "+f"(d2), "+f"(d3)
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The four int8 codes of a word (lowest byte first) as two f16x2 registers, (c0, c1)
+// and (c2, c3), exactly: the code's sign bit flipped gives c + 128 in [0, 255]; placed
+// under the exponent byte 0x64 it is the half 1024 + c + 128, and subtracting 1152
+// leaves c.
+__device__ __forceinline__ void q8_f16x4(uint32_t w, uint32_t &c01, uint32_t &c23) {
+    const uint32_t u = w ^ 0x80808080u;
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(u), "r"(0x64646464u));
+    asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(0x64646464u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(c01) : "r"(a), "r"(0x64806480u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(c23) : "r"(b), "r"(0x64806480u));
+}
+
+// kc_gemv on 8-bit rows on the tensor cores: the same partial sums, per 16 rows and
+// per group of KG k-steps (KG / 2 blocks of 32 columns) one m16n8k16 f16 product per
+// k-step.  The codes are the tile's M x K, exact in f16; within a k-step lane t takes
+// columns 4t .. 4t + 3 of its rows (one word) as the k slots 2t, 2t + 1, 2t + 8, 2t + 9,
+// and the input goes through the same permutation.  N column 2j + p carries part p
+// (x = x0 + x1, two f16 parts of the input times 2^e, e from the warp's largest
+// magnitude so that neither part overflows nor loses its low bits) on block j of the
+// group and zero elsewhere, so D[r][2j + p] is block j's sum of part p for row r and
+// lane t holds block t's two sums: it scales them by row r's half scale of that block
+// and accumulates; a 4-lane butterfly adds the blocks, and `post` = 2^-e undoes the
+// input scaling.  xh, xl: the warp's K / 8 columns of x0 and x1 as f16, column order.
+template <int KG>
+__device__ __forceinline__ bool kc_gemv_q8_mma(const Ring &R, uint32_t &sidx, int nrows, int rps, int K, int colw,
+                                               const __half *xh, const __half *xl, float post, float *part) {
+    static_assert(KG == 4 || KG == 8, "k-steps per group");
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
     const int nst = (nrows + rps - 1) / rps;
+    const uint32_t pitch = q8_pitch(K);
+    const int ngroups = K / (kNW * 16 * KG);
+    const int jb = g >> 1;                                   // the block this lane's N column carries
+    const bool live = jb < KG / 2;
+    const __half *xs = ((g & 1) ? xl : xh) + jb * 32 + 4 * t;
 #pragma unroll 1
     for (int st = 0; st < nst; ++st) {
         const uint8_t *sb = stage_get(R, sidx + st);
         if (!sb) return false;
         const int n = min_c(rps, nrows - st * rps);
 #pragma unroll 1
-        for (int g0 = 0; g0 < n; g0 += 8) {
-            float acc[8];
-#pragma unroll
-            for (int r = 0; r < 8; ++r) acc[r] = 0.f;
+        for (int r0 = 0; r0 < n; r0 += 16) {
+            // rows past n re-read row n - 1 (results dropped below)
+            const int ra = min_c(r0 + g, n - 1), rb = min_c(r0 + g + 8, n - 1);
+            const uint8_t *pa = sb + (size_t)ra * pitch + colw + t * 4;
+            const uint8_t *pb = sb + (size_t)rb * pitch + colw + t * 4;
+            const __half *sca = reinterpret_cast<const __half *>(sb + (size_t)ra * pitch + K) + (colw >> 5) + t;
+            const __half *scb = reinterpret_cast<const __half *>(sb + (size_t)rb * pitch + K) + (colw >> 5) + t;
+            float acc_a = 0.f, acc_b = 0.f;
 #pragma unroll 1
-            for (int c = 0; c < nc; ++c) {
-                float xv[EL];
-                load_elems<float, EL>(xw + c * 32 * EL + lane * EL, xv);
-                const int col = colw + c * 32 * EL + lane * EL;
+            for (int gq = 0; gq < ngroups; ++gq) {
+                uint2 u0 = make_uint2(0u, 0u), u1 = make_uint2(0u, 0u);
+                if (live) {
+                    u0 = *reinterpret_cast<const uint2 *>(xs + gq * KG * 16);
+                    u1 = *reinterpret_cast<const uint2 *>(xs + gq * KG * 16 + 16);
+                }
+                // two independent accumulators: even (c) and odd (e) k-steps
+                float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f, e0 = 0.f, e1 = 0.f, e2 = 0.f, e3 = 0.f;
 #pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    // rows past n re-read row n - 1 (counted zero below)
-                    const uint8_t *rp = sb + (size_t)(g0 + r < n ? g0 + r : n - 1) * rb;
-                    float f[EL];
-                    q8_codes<EL>(rp + col, f);
-                    float d = 0.f;
-#pragma unroll
-                    for (int e = 0; e < EL; ++e) d = fmaf(f[e], xv[e], d);
-                    acc[r] = fmaf(q8_scale(rp, K, col), d, acc[r]);
+                for (int ks = 0; ks < KG; ++ks) {
+                    const int kb = (gq * KG + ks) * 16;
+                    uint32_t a0, a1, a2, a3;
+                    q8_f16x4(*reinterpret_cast<const uint32_t *>(pa + kb), a0, a2);
+                    q8_f16x4(*reinterpret_cast<const uint32_t *>(pb + kb), a1, a3);
+                    const bool mine = (ks >> 1) == jb;
+                    const uint32_t b0 = mine ? ((ks & 1) ? u1.x : u0.x) : 0u;
+                    const uint32_t b1 = mine ? ((ks & 1) ? u1.y : u0.y) : 0u;
+                    if (ks & 1)
+                        mma_f16(e0, e1, e2, e3, a0, a1, a2, a3, b0, b1);
+                    else
+                        mma_f16(c0, c1, c2, c3, a0, a1, a2, a3, b0, b1);
+                }
+                if (t < KG / 2) {
+                    const int blk = gq * (KG / 2);
+                    acc_a = fmaf(__half2float(sca[blk]), (c0 + c1) + (e0 + e1), acc_a);
+                    acc_b = fmaf(__half2float(scb[blk]), (c2 + c3) + (e2 + e3), acc_b);
                 }
             }
-#pragma unroll
-            for (int r = 0; r < 8; ++r) acc[r] = g0 + r < n ? acc[r] : 0.f;
-            const float v = treduce<8>(acc, lane);
-            const int row = g0 + lane / 4;
-            if ((lane & 3) == 0 && row < n) part[st * rps + row] = v;
+            acc_a += __shfl_xor_sync(0xffffffffu, acc_a, 1);
+            acc_b += __shfl_xor_sync(0xffffffffu, acc_b, 1);
+            acc_a += __shfl_xor_sync(0xffffffffu, acc_a, 2);
+            acc_b += __shfl_xor_sync(0xffffffffu, acc_b, 2);
+            if (t == 0) {
+                if (r0 + g < n) part[st * rps + r0 + g] = acc_a * post;
+                if (r0 + g + 8 < n) part[st * rps + r0 + g + 8] = acc_b * post;
+            }
         }
         stage_put(R, sidx + st, lane);
     }
@@ -775,6 +823,7 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
     constexpr int NCMAX = NCF;
     constexpr int XSW = NCMAX * 32 * EL;                         // floats of a warp's input slice
     static_assert(NCA == 1 && NCQ >= 1 && NCF >= NCQ && KQ == NCQ * 256 * EL && KF == NCF * 256 * EL, "chunks");
+    static_assert(!Q8 || (KH % 512 == 0 && KQ % 512 == 0 && KF % 512 == 0), "8-bit rows: groups of 4 or 8 k-steps");
     constexpr int EH = HD / 32;
     constexpr int HALF = HD / 2;
     constexpr int PS = kStepRowsMax;
@@ -854,8 +903,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
                 auto rows = [&](const void *w, int r0, int n, uint32_t rb, int K, int rps) {
                     if constexpr (Q8) {
                         const uint32_t qb = q8_row_bytes(K);
-                        return produce_rows(R, sidx, reinterpret_cast<const uint8_t *>(w) + (size_t)r0 * qb, n, qb,
-                                            q8_rps(K), pw);
+                        return produce_rows_pitched(R, sidx, reinterpret_cast<const uint8_t *>(w) + (size_t)r0 * qb,
+                                                    n, qb, q8_pitch(K), q8_prs(K), pw);
                     } else if constexpr (sizeof(WT) == 2) {
                         return produce_rows_pitched(R, sidx, reinterpret_cast<const uint8_t *>(w) + (size_t)r0 * rb,
                                                     n, rb, mma_pitch(K), mma_rps(K), pw);
@@ -1100,8 +1149,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
             uint32_t rbytes;
             constexpr bool kMma = sizeof(WT) == 2 && !Q8;
             // rows of a ring stage of each phase's K
-            constexpr int rpsH = Q8 ? q8_rps(KH) : mma_rps(KH), rpsQ = Q8 ? q8_rps(KQ) : mma_rps(KQ),
-                          rpsF = Q8 ? q8_rps(KF) : mma_rps(KF);
+            constexpr int rpsH = Q8 ? q8_prs(KH) : mma_rps(KH), rpsQ = Q8 ? q8_prs(KQ) : mma_rps(KQ),
+                          rpsF = Q8 ? q8_prs(KF) : mma_rps(KF);
             constexpr bool kPacked = Q8 || kMma;   // rows per stage from the layout, not the host
             if (ph == 0) {
                 src = l ? a.tg + (size_t)(l - 1) * a.tg_stride + a.tg_xe : nullptr;
@@ -1202,17 +1251,42 @@ __global__ void __launch_bounds__(kStepThreads, 1) decode_step_kernel(const Step
             float *xw = xs + (size_t)warp * XSW;      // this warp's slice of the input, times gamma
             float *part = kc_part + buf * kNW * PS;
             if constexpr (Q8) {
+                // the slice as two f16 parts of x * 2^e (e: the largest magnitude lands
+                // in [2^13, 2^14)); x0 at xw, x1 XSW halves further
+                float vmax = 0.f;
 #pragma unroll
                 for (int cc = 0; cc < NCMAX; ++cc)
-                    if (cc < nc) {
+                    if (cc < nc)
 #pragma unroll
                         for (int e = 0; e < EL; ++e) {
                             ss = fmaf(x[cc][e], x[cc][e], ss);
-                            xw[cc * 32 * EL + e * 32 + lane] = x[cc][e] * gv[cc][e];
+                            vmax = fmaxf(vmax, fabsf(x[cc][e] * gv[cc][e]));
                         }
-                    }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+                const int ex = min_c(120, max_c(-120, 140 - ((__float_as_int(vmax) >> 23) & 0xff)));
+                const float up = __int_as_float((127 + ex) << 23), down = __int_as_float((127 - ex) << 23);
+                __half *xh = reinterpret_cast<__half *>(xw), *xl = xh + XSW;
+#pragma unroll
+                for (int cc = 0; cc < NCMAX; ++cc)
+                    if (cc < nc)
+#pragma unroll
+                        for (int e = 0; e < EL; ++e) {
+                            const float v = x[cc][e] * gv[cc][e] * up;
+                            const __half h = __float2half_rn(v);
+                            const int i = cc * 32 * EL + e * 32 + lane;
+                            xh[i] = h;
+                            xl[i] = __float2half_rn(v - __half2float(h));
+                        }
                 __syncwarp();
-                if (okw) okw = kc_gemv_q8<EL>(R, sidx, nrows, rps, K, colw, nc, xw, part + warp * PS);
+                if (okw) {
+                    if constexpr (KH % 1024 == 0 && KQ % 1024 == 0 && KF % 1024 == 0)
+                        okw = kc_gemv_q8_mma<8>(R, sidx, nrows, rps, K, colw, xh, xl, down, part + warp * PS);
+                    else if (K % 1024 == 0)
+                        okw = kc_gemv_q8_mma<8>(R, sidx, nrows, rps, K, colw, xh, xl, down, part + warp * PS);
+                    else
+                        okw = kc_gemv_q8_mma<4>(R, sidx, nrows, rps, K, colw, xh, xl, down, part + warp * PS);
+                }
             } else if constexpr (kMma) {
                 // as two bf16 parts (the slice's K / 8 values twice: the same bytes as fp32)
                 __nv_bfloat16 *x0 = reinterpret_cast<__nv_bfloat16 *>(xw), *x1 = x0 + 16;
