@@ -388,6 +388,39 @@ def test_batch_prefill_full_size_two_streams():
         o.close()
 
 
+@pytest.mark.parametrize("hd,qh,kvh,n,smax", [
+    (128, 16, 8, 300, 320),   # three query blocks, the last ragged; the cache ends inside the last key chunk
+    (128, 8, 1, 129, 256),    # a one-query last block; 8 q heads per kv head
+    (64, 8, 8, 257, 512),     # head_dim 64, one query past two whole chunks
+    (64, 8, 2, 384, 416),     # whole chunks only: no tail to zero
+])
+def test_batch_prefill_attention_variants(hd, qh, kvh, n, smax):
+    """The tensor-core prefill attention's shapes on one-layer models: several 128-query
+    blocks and 128-key chunks, ragged ends, GQA groups of 1, 2 and 8, both head sizes;
+    the logits and the written cache against the oracle's prefill."""
+    import torch
+    hidden = qh * hd
+    s = W.scaled(W.TALKER, name=f"pfa_{hd}_{qh}_{kvh}", n_layers=1, hidden=hidden, n_q_heads=qh,
+                 n_kv_heads=kvh, head_dim=hd, ffn=2 * hidden, vocab=1024, embed_rows=1024)
+    B, streams = 3, [2, 0]
+    qd, h, bh, first, logits, refs = _prefill_pair(s, B, smax, streams, n)
+    for k, st in enumerate(streams):
+        o, rid, rlog, margin = refs[k]
+        assert rel_l2(logits[st], rlog) <= REL_TOL, (st, rel_l2(logits[st], rlog))
+        if margin > MARGIN:
+            assert first[k] == rid
+        nb = qd.qd_batch_copy_kv(bh, st)
+        buf = torch.empty(nb, dtype=torch.uint8, device="cuda")
+        qd.qd_batch_copy_kv(bh, st, buf)
+        g = buf.view(torch.int16).cpu().numpy().view(np.uint16).reshape(1, 2, kvh, smax, hd)
+        for w_ in range(2):
+            assert rel_l2(_bf16_to_f32(g[0, w_, :, :n]), o.kv(0, w_)) <= REL_TOL, (st, w_)
+    qd.qd_batch_destroy(bh)
+    qd.qd_destroy(h)
+    for o, *_ in refs:
+        o.close()
+
+
 @pytest.mark.parametrize("hd,qh,kvh", [(64, 8, 8), (64, 8, 2), (64, 8, 1), (128, 8, 1)])
 def test_batch_attention_variants_match_oracle(hd, qh, kvh):
     """The attention's other instantiations (head_dim 64 or 128; 1, 4 or 8 q heads per

@@ -51,7 +51,8 @@ def _close(got, ref):
 @pytest.mark.parametrize("R,K,T", [
     (256, 128, 64),      # 2 tiles x 2 splits
     (4096, 1024, 64),    # fused QKV of the Talker at 64 streams: 32 tiles x 4 splits
-    (1024, 3072, 64),    # down projection: 8 tiles x 19 uneven splits
+    (1024, 3072, 64),    # down projection: 8 tiles x 8 splits of 6 chunks
+    (1024, 832, 64),     # 8 tiles x 8 uneven splits (13 chunks of 64)
     (1024, 2048, 5),     # 5 tokens: a partial token tile (zero-filled rows)
     (512, 1024, 300),    # 128-token tiles, ragged last tile
     (3072, 1024, 1024),  # prefill-like: 192 tiles, several per CTA, no split

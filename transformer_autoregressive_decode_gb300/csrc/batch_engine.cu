@@ -450,6 +450,7 @@ qd_status enqueue_prefill(qd_batch *b, int ns, int n, int32_t *first_ids, bool w
         b->launches++;
         return launch_norm_split(a, rows, s);
     };
+    PrefillAttnMaps fmaps;
     for (int l = 0; l < c.n_layers; ++l) {
         const Layer &L = m->layers[l];
         if (norm(b->pf_x, T, L.attn_norm)) return batch_fail(b, QD_ECUDA, "prefill norm launch failed");
@@ -494,8 +495,11 @@ qd_status enqueue_prefill(qd_batch *b, int ns, int n, int32_t *first_ids, bool w
         fa.out_hi = b->pf_xh;
         fa.out_lo = b->pf_xl;
         fa.status = b->status;
+        fa.cache_streams = b->B;
+        if (l == 0 && !make_prefill_attn_maps(c.head_dim, ns, fa, &fmaps))
+            return batch_fail(b, QD_ECUDA, "prefill attention tensor maps refused");
         b->launches++;
-        if (launch_prefill_attention(c.head_dim, ns, fa, s))
+        if (launch_prefill_attention_tc(c.head_dim, ns, fa, fmaps, s))
             return batch_fail(b, QD_ECUDA, "prefill attention launch failed");
         if (gemm(p_o, L.w_o, b->pf_xh, b->pf_xl, h, qd_, T, TC_RESIDUAL, b->pf_x, h))
             return batch_fail(b, QD_ECUDA, "prefill O GEMM launch failed");

@@ -29,6 +29,21 @@ template <int HD>
 __global__ void __launch_bounds__(kPqThreads) prefill_qk_kernel(const PrefillQkArgs a) {
     constexpr int DPL = HD / 32;
     constexpr int HALF = HD / 2;
+    if ((int)blockIdx.x >= gridDim.x - a.ns_tail) {
+        // one CTA per (prompt stream, K or V plane of a kv head): rows [n, next multiple
+        // of 128) of the layer are zeroed (below the cache's end), so the attention's last
+        // 128-key chunk reads finite values past the prompt; 16-byte stores (a row is
+        // HD * 2 bytes, a multiple of 16)
+        const int t = (int)blockIdx.x - (gridDim.x - a.ns_tail);
+        const int i = t / (2 * a.kvh), plane = t - i * 2 * a.kvh;
+        const int end = min((a.n + 127) / 128 * 128, a.S);
+        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(a.kv) +
+                                               (size_t)a.streams[i] * a.stream_elems + a.layer_elems +
+                                               ((size_t)plane * a.S + a.n) * HD);
+        const int n16 = (end - a.n) * HD / 8;
+        for (int k = threadIdx.x; k < n16; k += kPqThreads) dst[k] = make_uint4(0u, 0u, 0u, 0u);
+        return;
+    }
     const int tok = blockIdx.x;
     const int i = tok / a.n, j = tok - i * a.n;        // prompt stream, position
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -137,9 +152,12 @@ __global__ void __launch_bounds__(256) prefill_finish_kernel(const PrefillFinish
 
 }  // namespace
 
-cudaError_t launch_prefill_qk(int hd, int ns, const PrefillQkArgs &a, cudaStream_t s) {
-    if (hd == 128) prefill_qk_kernel<128><<<ns * a.n, kPqThreads, 0, s>>>(a);
-    else if (hd == 64) prefill_qk_kernel<64><<<ns * a.n, kPqThreads, 0, s>>>(a);
+cudaError_t launch_prefill_qk(int hd, int ns, const PrefillQkArgs &a_in, cudaStream_t s) {
+    PrefillQkArgs a = a_in;
+    a.ns_tail = a.n % 128 && a.n < a.S ? ns * 2 * a.kvh : 0;   // the streams' tail-zeroing CTAs
+    const int grid = ns * a.n + a.ns_tail;
+    if (hd == 128) prefill_qk_kernel<128><<<grid, kPqThreads, 0, s>>>(a);
+    else if (hd == 64) prefill_qk_kernel<64><<<grid, kPqThreads, 0, s>>>(a);
     else return cudaErrorInvalidValue;
     return cudaGetLastError();
 }

@@ -346,9 +346,13 @@ cudaError_t batch_kernels_init();   // call before any capture
 cudaError_t launch_batch_attention(int hd, int B, const BatchAttnArgs &a, const CUtensorMap &kv_map, cudaStream_t s,
                                    bool pdl = false);
 // TMA map of bf16 caches seen as `planes` planes of [S][hd] (rows of hd elements), box
-// of 64 elements x 32 rows with the 128-byte swizzle (the batched attention's tiles);
-// false if the driver refuses it.
-bool make_kv_tile_map(CUtensorMap *m, const void *kv, int hd, int S, long long planes);
+// of 64 elements x box_rows rows with the 128-byte swizzle (the batched attention's
+// 32-position tiles, the prefill attention's 128-key chunks); false if the driver
+// refuses it.
+bool make_kv_tile_map(CUtensorMap *m, const void *kv, int hd, int S, long long planes, int box_rows = 32);
+// TMA map of a row-major bf16 matrix [rows, K], box of 64 elements x box_rows rows with
+// the 128-byte swizzle; false if the driver refuses it.
+bool make_bf16_rows_map(CUtensorMap *m, const void *ptr, int rows, int K, int box_rows);
 
 // Per row b < rows: optionally x[b] = E[tokens[b]] (the token joins stream b's emitted
 // set), then hi/lo bf16 parts of gamma * x[b] / sqrt(mean(x[b]^2) + eps).
@@ -416,6 +420,7 @@ struct PrefillQkArgs {
     int S;
     const int *streams;            // [ns] cache index of each prompt stream
     __nv_bfloat16 *q_hi, *q_lo;    // [ns][qh][n][hd]: normalised, rotated q as bf16 parts
+    int ns_tail;                   // set by launch_prefill_qk: CTAs that zero the prompt's K/V tail
 };
 cudaError_t launch_prefill_qk(int hd, int ns, const PrefillQkArgs &a, cudaStream_t s);
 
@@ -428,10 +433,20 @@ struct PrefillAttnArgs {
     const int *streams;
     __nv_bfloat16 *out_hi, *out_lo;    // [ns * n][qh * hd]
     int *status;
+    int cache_streams;                 // streams of the cache buffer kv (its planes: cache_streams x stream_elems)
 };
 bool prefill_attention_supported(int hd, int group);
 cudaError_t prefill_kernels_init();
 cudaError_t launch_prefill_attention(int hd, int ns, const PrefillAttnArgs &a, cudaStream_t s);
+// The same attention on the tcgen05 tensor cores (head_dim 64 or 128, any group size),
+// with the TMA maps of one prefill call (q parts and the caches: the same for every
+// layer) made once by make_prefill_attn_maps.
+struct PrefillAttnMaps {
+    CUtensorMap qh, ql, kv;
+};
+bool make_prefill_attn_maps(int hd, int ns, const PrefillAttnArgs &a, PrefillAttnMaps *m);
+cudaError_t launch_prefill_attention_tc(int hd, int ns, const PrefillAttnArgs &a, const PrefillAttnMaps &m,
+                                        cudaStream_t s);
 
 // ns rows of x [T][K] at rows (i * n + n - 1): the last position of each prompt stream.
 cudaError_t launch_gather_last(const float *x, int n, int K, int ns, float *out, cudaStream_t s);

@@ -38,6 +38,7 @@
 
 #include "qd_device.cuh"
 #include "qd_internal.h"
+#include "tc_common.cuh"
 
 namespace qd {
 
@@ -60,85 +61,8 @@ template <int BN> struct TcCfg {
     static constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + 256 + 1024;
 };
 
-// ---- PTX wrappers (tensor memory, MMA, TMA)
-__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(slot)),
-                 "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// D (tensor memory) (+)= A * B^T, A/B described by shared-memory descriptors.
-__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
-        : "memory");
-}
-// Arrive on `bar` once every MMA issued so far by this thread has completed.
-__device__ __forceinline__ void tc_commit(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
-                 : "memory");
-}
-// 16 consecutive fp32 columns of this thread's tensor-memory lane.
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, float *v) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-// 2-D tiled TMA load of box (c0 = k element offset, c1 = row) into shared memory.
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-        "[%4];" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
-        : "memory");
-}
-
-// Shared-memory matrix descriptor of a K-major tile written by TMA with the 128-byte
-// swizzle: rows of 128 bytes, 8-row swizzle atoms of 1024 bytes (stride byte offset),
-// leading byte offset unused for this layout, descriptor version 1, layout 2 = 128B.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major,
-// N >> 3 at bit 17, M >> 4 at bit 24.
-template <int BN> __device__ __forceinline__ constexpr uint32_t tc_idesc() {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
-}
-
-// Bounded wait that also gives up when another role has aborted.
-__device__ __forceinline__ bool role_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, int *status) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_timer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (*abort_flag) return false;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
-            *abort_flag = 1;
-            atomicOr(status, DEV_ERR_WAIT_TIMEOUT);
-            return false;
-        }
-    }
-    return true;
-}
+// Instruction descriptor of this GEMM: M = kBM weight rows, N = BN tokens, both K-major.
+template <int BN> __device__ __forceinline__ constexpr uint32_t tc_idesc() { return tc_idesc_mn<kBM, BN>(); }
 
 __device__ __forceinline__ int ld_acquire_s32(const int *p) {
     int v;
@@ -613,18 +537,26 @@ cudaError_t tc_gemm_init() {
     return e != cudaSuccess ? e : set_attr<128>();
 }
 
-bool make_kv_tile_map(CUtensorMap *m, const void *kv, int hd, int S, long long planes) {
+bool make_bf16_rows_map(CUtensorMap *m, const void *ptr, int rows, int K, int box_rows) {
+    if (rows < 1 || K % 64 || box_rows < 1 || box_rows > 256) return false;
+    return make_map(m, ptr, rows, K, box_rows);
+}
+
+bool make_kv_tile_map(CUtensorMap *m, const void *kv, int hd, int S, long long planes, int box_rows) {
     EncodeTiledFn fn = encode_fn();
-    if (!fn || (reinterpret_cast<uintptr_t>(kv) & 15) || hd % 64 || S % 32 || planes < 1 || planes > INT32_MAX)
+    if (!fn || (reinterpret_cast<uintptr_t>(kv) & 15) || hd % 64 || S % 32 || planes < 1 || planes > INT32_MAX ||
+        box_rows < 1 || box_rows > 256)
         return false;
     cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)S, (cuuint64_t)planes};
     cuuint64_t strides[2] = {(cuuint64_t)hd * 2, (cuuint64_t)hd * 2 * S};
-    cuuint32_t box[3] = {64, 32, 1};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
     cuuint32_t es[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(kv), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+constexpr int kMaxSplits = 8;
 
 bool tc_gemm_plan(int R, int K, int T, int num_sms, TcGemmPlan *p) {
     if (R <= 0 || K <= 0 || T <= 0 || R % kBM || K % kBK || num_sms <= 0) return false;
@@ -635,7 +567,11 @@ bool tc_gemm_plan(int R, int K, int T, int num_sms, TcGemmPlan *p) {
     const int tiles = q.row_tiles * q.tok_tiles;
     const int KC = K / kBK;
     q.splits = 1;
-    if (tiles < num_sms) q.splits = std::max(1, std::min(KC, num_sms / tiles));
+    // split K to fill the SMs, at most kMaxSplits ways: the split CTAs of a tile meet
+    // and each reads every split's partial of its columns, which at 19 splits (a
+    // 1024-row product over K = 2048 or 3072 at 64 tokens) cost more than the
+    // streaming the extra splits spread out
+    if (tiles < num_sms) q.splits = std::max(1, std::min(std::min(KC, num_sms / tiles), kMaxSplits));
     q.units = tiles * q.splits;
     q.grid = std::min(q.units, num_sms);
     q.smem = q.bn == 64 ? TcCfg<64>::kSmem : TcCfg<128>::kSmem;
