@@ -662,7 +662,7 @@ qd_status qd_batch_create(qd_handle model, int n_streams, int smax, qd_batch_han
         delete b;
         return fail(m, QD_EUNSUPPORTED, "smax %d too long for the attention tile", smax);
     }
-    if (tc_gemm_init() != cudaSuccess || batch_kernels_init() != cudaSuccess || prefill_kernels_init() != cudaSuccess) {
+    if (tc_gemm_init() != cudaSuccess || batch_kernels_init() != cudaSuccess) {
         delete b;
         return fail(m, QD_ECUDA, "tensor-core GEMM or attention kernel setup failed");
     }

@@ -435,9 +435,6 @@ struct PrefillAttnArgs {
     int *status;
     int cache_streams;                 // streams of the cache buffer kv (its planes: cache_streams x stream_elems)
 };
-bool prefill_attention_supported(int hd, int group);
-cudaError_t prefill_kernels_init();
-cudaError_t launch_prefill_attention(int hd, int ns, const PrefillAttnArgs &a, cudaStream_t s);
 // The same attention on the tcgen05 tensor cores (head_dim 64 or 128, any group size),
 // with the TMA maps of one prefill call (q parts and the caches: the same for every
 // layer) made once by make_prefill_attn_maps.
