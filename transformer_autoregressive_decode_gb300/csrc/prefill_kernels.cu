@@ -19,6 +19,31 @@ namespace {
 // ---- QK-norm + RoPE + append, one CTA (8 warps) per prompt token
 constexpr int kPqThreads = 256;
 
+// N consecutive floats (16- or 8-byte aligned for N = 4 or 2) in one load, through L2.
+template <int N> __device__ __forceinline__ void load_f32(const float *p, float *v) {
+    if constexpr (N == 4) {
+        const float4 t = __ldcg(reinterpret_cast<const float4 *>(p));
+        v[0] = t.x, v[1] = t.y, v[2] = t.z, v[3] = t.w;
+    } else {
+        static_assert(N == 2, "elements per lane");
+        const float2 t = __ldcg(reinterpret_cast<const float2 *>(p));
+        v[0] = t.x, v[1] = t.y;
+    }
+}
+// N consecutive bf16 (8- or 4-byte aligned for N = 4 or 2) in one store.
+template <int N> __device__ __forceinline__ void store_bf16(__nv_bfloat16 *p, const __nv_bfloat16 *h) {
+    if constexpr (N == 4) {
+        __nv_bfloat162 a2 = __halves2bfloat162(h[0], h[1]), b2 = __halves2bfloat162(h[2], h[3]);
+        uint2 u;
+        u.x = *reinterpret_cast<uint32_t *>(&a2);
+        u.y = *reinterpret_cast<uint32_t *>(&b2);
+        *reinterpret_cast<uint2 *>(p) = u;
+    } else {
+        static_assert(N == 2, "elements per lane");
+        *reinterpret_cast<__nv_bfloat162 *>(p) = __halves2bfloat162(h[0], h[1]);
+    }
+}
+
 template <int HD>
 __global__ void __launch_bounds__(kPqThreads) prefill_qk_kernel(const PrefillQkArgs a) {
     constexpr int DPL = HD / 32;
@@ -45,50 +70,59 @@ __global__ void __launch_bounds__(kPqThreads) prefill_qk_kernel(const PrefillQkA
     const int stream = a.streams[i];
     __nv_bfloat16 *kc = reinterpret_cast<__nv_bfloat16 *>(a.kv) + (size_t)stream * a.stream_elems + a.layer_elems;
     __nv_bfloat16 *vc = kc + (size_t)a.kvh * a.S * HD;
+    // the lane's rotary cos / sin (dims lane * DPL .. of the rotate-half pairs, at position
+    // j or the prompt's rotary positions) and gammas: the same for every head of the token
+    float rcos[DPL], rsin[DPL], gq[DPL], gk[DPL];
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) {
+        const int m = (lane & 15) * DPL + e;
+        const size_t r = (size_t)rope_row(m, a.mrope_h, a.rope_pos, a.rope_stride, j, j, a.rope_rows);
+        rcos[e] = a.rope_cos[r * HALF + m];
+        rsin[e] = a.rope_sin[r * HALF + m];
+        gq[e] = a.q_gamma ? a.q_gamma[lane * DPL + e] : 1.f;
+        gk[e] = a.k_gamma ? a.k_gamma[lane * DPL + e] : 1.f;
+    }
     // vectors: q heads 0..qh-1, k heads qh..qh+kvh-1 (normed, rotated), v heads (copied)
     for (int vec = warp; vec < a.qh + 2 * a.kvh; vec += kPqThreads / 32) {
         float v[DPL];
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) v[e] = __ldcg(row + (size_t)vec * HD + lane * DPL + e);
+        load_f32<DPL>(row + (size_t)vec * HD + lane * DPL, v);
         if (vec < a.qh + a.kvh) {
-            const float *gam = vec < a.qh ? a.q_gamma : a.k_gamma;
-            if (gam) {
+            const bool isq = vec < a.qh;
+            if (isq ? a.q_gamma != nullptr : a.k_gamma != nullptr) {
                 float ss = 0.f;
 #pragma unroll
                 for (int e = 0; e < DPL; ++e) ss = fmaf(v[e], v[e], ss);
                 ss = warp_sum(ss);
                 const float inv = 1.0f / sqrtf(ss / (float)HD + a.eps);
 #pragma unroll
-                for (int e = 0; e < DPL; ++e) v[e] = v[e] * inv * gam[lane * DPL + e];
+                for (int e = 0; e < DPL; ++e) v[e] = v[e] * inv * (isq ? gq[e] : gk[e]);
             }
-            // rotate-half RoPE at position j (or the prompt's rotary positions): dims d
-            // and d + HD/2 sit 16 lanes apart
+            // rotate-half RoPE: dims d and d + HD/2 sit 16 lanes apart
             float w[DPL];
 #pragma unroll
             for (int e = 0; e < DPL; ++e) w[e] = __shfl_xor_sync(0xffffffffu, v[e], 16);
             const bool low = lane < 16;
 #pragma unroll
-            for (int e = 0; e < DPL; ++e) {
-                const int m = (lane & 15) * DPL + e;
-                const size_t r = (size_t)rope_row(m, a.mrope_h, a.rope_pos, a.rope_stride, j, j, a.rope_rows);
-                const float c = a.rope_cos[r * HALF + m], sn = a.rope_sin[r * HALF + m];
-                v[e] = low ? v[e] * c - w[e] * sn : v[e] * c + w[e] * sn;
-            }
+            for (int e = 0; e < DPL; ++e) v[e] = low ? v[e] * rcos[e] - w[e] * rsin[e] : v[e] * rcos[e] + w[e] * rsin[e];
         }
         if (vec < a.qh) {
             const size_t o = (((size_t)i * a.qh + vec) * a.n + j) * HD + lane * DPL;
+            __nv_bfloat16 h[DPL], l[DPL];
 #pragma unroll
             for (int e = 0; e < DPL; ++e) {
-                const __nv_bfloat16 h = __float2bfloat16_rn(v[e]);
-                a.q_hi[o + e] = h;
-                a.q_lo[o + e] = __float2bfloat16_rn(v[e] - __bfloat162float(h));
+                h[e] = __float2bfloat16_rn(v[e]);
+                l[e] = __float2bfloat16_rn(v[e] - __bfloat162float(h[e]));
             }
+            store_bf16<DPL>(a.q_hi + o, h);
+            store_bf16<DPL>(a.q_lo + o, l);
         } else {
             const bool isk = vec < a.qh + a.kvh;
             const int g = isk ? vec - a.qh : vec - a.qh - a.kvh;
             __nv_bfloat16 *dst = (isk ? kc : vc) + ((size_t)g * a.S + j) * HD + lane * DPL;
+            __nv_bfloat16 h[DPL];
 #pragma unroll
-            for (int e = 0; e < DPL; ++e) dst[e] = __float2bfloat16_rn(v[e]);
+            for (int e = 0; e < DPL; ++e) h[e] = __float2bfloat16_rn(v[e]);
+            store_bf16<DPL>(dst, h);
         }
     }
 }
