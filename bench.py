@@ -44,8 +44,8 @@ _STEP_TRAFFIC = {"asr": {"digest": "2d9d7695997abbd2", "bytes": 224889088 + 3907
 _STEP_SOURCES = ("decode_persistent.cu", "decode_common.cuh", "qd_device.cuh")
 # DRAM bytes of one batch_attn_kernel launch (profiles/batch_attn_kernel_batch64.md) at
 # the initial lengths + 3, for the kernel sources with this digest.
-_BATT_TRAFFIC = {"digest": "ff6e64d610d9f6d3", "bytes": 260624384 + 3836416, "rows": 62239 + 3 * 64}
-_BATT_SOURCES = ("batch_kernels.cu", "decode_common.cuh", "qd_device.cuh", "mma_sync.cuh")
+_BATT_TRAFFIC = {"digest": "15451e5cfb3ef81d", "bytes": 260572160 + 3373568, "rows": 62239 + 3 * 64}
+_BATT_SOURCES = ("batch_kernels.cu", "decode_common.cuh", "qd_device.cuh", "mma_sync.cuh", "qd_internal.h")
 
 
 def _step_digest(sources=_STEP_SOURCES) -> str:
@@ -1085,7 +1085,7 @@ def all_arm(args):
     """The default line: the Talker decode step (the DRAM-bound batch-1 decoder the metric
     is about) as the headline, with the ASR decoder, the two-level frame loop and the
     batched multi-stream decode as keys of the same line, each with its own value,
-    roofline, CPU baseline and end-to-end number.  The driver's --steps / --warmup apply
+    roofline, CPU baseline and end-to-end number.  The --steps / --warmup arguments apply
     to the headline and the ASR decoder (decode tokens); the frame loop runs one
     150-frame trajectory and the batched decode 64 steps of its 256."""
     import copy

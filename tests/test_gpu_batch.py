@@ -424,12 +424,13 @@ def test_batch_prefill_attention_variants(hd, qh, kvh, n, smax):
 @pytest.mark.parametrize("hd,qh,kvh", [(64, 8, 8), (64, 8, 2), (64, 8, 1), (128, 8, 1)])
 def test_batch_attention_variants_match_oracle(hd, qh, kvh):
     """The attention's other instantiations (head_dim 64 or 128; 1, 4 or 8 q heads per
-    kv head) on one-layer models, cached lengths across several 256-position attention chunks."""
+    kv head) on one-layer models, cached lengths from one to three 512-position attention
+    chunks (the merge of several, and the single-chunk path)."""
     hidden = qh * hd
     s = W.scaled(W.TALKER, name=f"batt_{hd}_{qh}_{kvh}", n_layers=1, hidden=hidden, n_q_heads=qh,
                  n_kv_heads=kvh, head_dim=hd, ffn=2 * hidden, vocab=1024, embed_rows=1024)
-    B, smax, n = 4, 768, 3
-    lens = W.batch_initial_lengths(n=B, lo=200, hi=700)
+    B, smax, n = 4, 1600, 3
+    lens = W.batch_initial_lengths(n=B, lo=100, hi=1500)   # 1001, 445, 1412, 590: 1 to 3 chunks
     bp = BatchPair(s, B, smax, lens)
     _check_steps(bp, n)
     bp.close()

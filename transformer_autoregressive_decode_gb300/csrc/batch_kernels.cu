@@ -18,12 +18,12 @@ namespace qd {
 
 namespace {
 
-// ---- attention: one CTA per (stream, kv group, chunk of 256 cached positions), 4
-// consumer warps and a producer warp.  The producer streams the chunk's tiles of 32
+// ---- attention: one CTA per (stream, kv group, chunk of kBattChunk = 512 cached
+// positions), 4 consumer warps and a producer warp.  The producer streams the chunk's tiles of 32
 // positions, each tile's K rows then its V rows, into 4 shared-memory slots (3-D tiled
 // TMA loads of the cache's [S][head_dim] planes with the 128-byte swizzle; full/empty
 // mbarriers per slot).  The consumer warps go in pairs: pair i takes tiles i, i + 2,
-// i + 4, i + 6 through its own two slots (K and V; so every waiter sees every phase of the
+// i + 4, ... through its own two slots (K and V; so every waiter sees every phase of the
 // barriers it waits on), warp 2i + j the tile's positions 16 j .. 16 j + 15.  They
 // compute on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate) with the
 // positions as the fragments' M: the scores (A = the 16 K rows, B = the G q heads of

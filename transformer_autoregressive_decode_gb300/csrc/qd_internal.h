@@ -336,7 +336,7 @@ struct BatchAttnArgs {
 
 // The batched attention works in chunks of kBattChunk cached positions: one CTA per
 // (stream, kv group, chunk); the chunks of a pair are merged by the last of them.
-constexpr int kBattChunk = 256;
+constexpr int kBattChunk = 512;
 __host__ __device__ inline int batch_attn_max_chunks(int S) { return (S + kBattChunk - 1) / kBattChunk; }
 
 size_t batch_attention_smem_bytes(int hd, int group);
