@@ -39,8 +39,8 @@ METRIC = "decode tokens/s at 1 GB300; per-step HBM GB/s as fraction of peak"
 # (profiles/decode_step_kernel_asr.md, profiles/decode_step_kernel_talker.md), at
 # attended length L, for the kernel sources
 # with this digest; null in the JSON line once the sources differ.
-_STEP_TRAFFIC = {"asr": {"digest": "2d9d7695997abbd2", "bytes": 224889088 + 3907840, "L": 116},
-                 "talker": {"digest": "2d9d7695997abbd2", "bytes": 896905472 + 4811520, "L": 70}}
+_STEP_TRAFFIC = {"asr": {"digest": "51c8f2ba2df52b4f", "bytes": 224889088 + 3907840, "L": 116},
+                 "talker": {"digest": "51c8f2ba2df52b4f", "bytes": 896905472 + 4811520, "L": 70}}
 _STEP_SOURCES = ("decode_persistent.cu", "decode_common.cuh", "qd_device.cuh")
 # DRAM bytes of one batch_attn_kernel launch (profiles/batch_attn_kernel_batch64.md) at
 # the initial lengths + 3, for the kernel sources with this digest.

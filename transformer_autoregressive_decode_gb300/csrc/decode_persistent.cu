@@ -33,13 +33,15 @@
 //
 // The GEMV phases split K over the consumer warps: warp w owns a contiguous chunk of
 // the input vector's columns and polls exactly those words, straight into registers,
-// so it can start on its rows as soon as its own chunk has arrived.  Each lane
-// multiplies its columns of every row of a ring stage; one transposing butterfly per
-// stage reduces the stage's rows across the lanes (lane i ends with row i's chunk
-// sum), and after the last stage one CTA barrier lets a thread per row add the warps'
-// chunk sums in warp order.  RMSNorm is a scalar per vector, so W (g * x * r) is
-// computed as r * W (g * x): the chunk sums of squares travel beside the row partials
-// and r is applied by the row's thread.
+// so it can start on its rows as soon as its own chunk has arrived.  The chunk's dot
+// products with the rows of each ring stage run on the tensor cores (mma.sync
+// m16n8k16: 16 rows x 16 columns per instruction, the input as two bf16 parts, or, for
+// 8-bit rows, as two f16 parts against the exactly converted codes, one block scale
+// per lane and 32 columns) on bf16 and 8-bit weights, and as per-lane FMAs with one
+// transposing butterfly per stage on fp32 weights; after the last stage one CTA
+// barrier lets a thread per row add the warps' chunk sums in warp order.  RMSNorm is a
+// scalar per vector, so W (g * x * r) is computed as r * W (g * x): the chunk sums of
+// squares travel beside the row partials and r is applied by the row's thread.
 #include <cuda_fp16.h>
 
 #include <type_traits>
