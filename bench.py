@@ -393,6 +393,30 @@ def gpu_line(args, workload, ctx):
               "note": "the LM head quantised to 32-weight blocks with half scales; median of 10 launches "
                       "(after 2), each between CUDA events after a 256 MB write that flushes L2"}
         del codes, scales
+        # the same head as Q4_K super-blocks (qd_quantize_q4k / qd_gemv_q4k): 144 bytes
+        # per 256 weights, timed the same way
+        w_head = to_device(w_np["lm_head.0"])
+        q4b = torch.empty((shape.vocab, shape.hidden // 256, 144), dtype=torch.uint8, device="cuda")
+        qd.qd_quantize_q4k(w_head, q4b)
+        del w_head
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        ts = []
+        for _ in range(12):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            qd.qd_gemv_q4k(q4b, xq, yq)
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        del flush, q4b
+        q4_ms = float(np.median(ts[2:]))
+        q4_bytes = shape.vocab * shape.hidden * 144 / 256
+        q8["q4k"] = {"kernel": "gemv_q4k_kernel (qd_gemv_q4k)", "bytes": q4_bytes, "avg_launch_ms": q4_ms,
+                     "achieved_gbs": q4_bytes / (q4_ms / 1e3) / 1e9,
+                     "frac": q4_bytes / (q4_ms / 1e3) / 1e9 / hbm_peak, "peak_source": peak_src,
+                     "note": "Q4_K super-blocks (256 weights: half d and dm, 6-bit sub-block scales and mins, "
+                             "4-bit codes); median of 10 launches (after 2), L2 flushed before each"}
         # the whole decode step with every layer matrix and the head as 8-bit rows
         # (qd_config.weight_q8): the same trajectory's decode steps, and the step kernel
         # against the quantised bytes

@@ -243,6 +243,33 @@ qd_status qd_quantize_q8(const void *w_dev, int dtype, int rows, int K, int8_t *
 qd_status qd_gemv_q8(const int8_t *codes_dev, const uint16_t *scales_dev, const float *x_dev, float *y_dev, int rows,
                      int K, void *cuda_stream, int reps, float *avg_ms);
 
+/* qd_quantize_q4k -- Q4_K super-block quantisation of W (DEVICE [rows, K], row-major,
+ * fp32 or bf16 per dtype; K a multiple of 256), the talker's 4.5-bit format of "audio.cpp
+ * Rockchip NPU build notes" ("The talker is the only DRAM-bound candidate, and it is not
+ * at the ceiling": 251 MB per token against 471 MB as Q8_0).  Per row, super-blocks of
+ * 256 weights along K, 144 bytes each in blocks_dev (DEVICE uint8 [rows][K/256][144],
+ * 16-byte aligned): bytes 0-1 the half scale d, 2-3 the half min dm, 4-9 the 8
+ * sub-blocks' 6-bit scales sc_j and 10-15 their 6-bit mins m_j (each a 48-bit
+ * little-endian word, field j at bit 6 j), 16-143 the 4-bit codes q (byte i: weight 2i in
+ * the low nibble, 2i + 1 in the high one); weight = d sc_j q - dm m_j.  Quantiser, in fp32
+ * with IEEE division and half-away rounding: per 32-weight sub-block mn_j = -min(0, min
+ * w), s_j = (max w + mn_j) / 15; d = half(max s_j / 63), dm = half(max mn_j / 63); sc_j =
+ * clamp(round(s_j / d), 0, 63), m_j = clamp(round(mn_j / dm), 0, 63), q = clamp(round((w +
+ * dm m_j) / (d sc_j)), 0, 15) (0 where a divisor is 0).  Runs on cuda_stream and
+ * synchronises it.  Errors: QD_EINVAL (shape, dtype, alignment, a non-device pointer),
+ * QD_ECUDA. */
+qd_status qd_quantize_q4k(const void *w_dev, int dtype, int rows, int K, uint8_t *blocks_dev, void *cuda_stream);
+
+/* qd_gemv_q4k -- y[r] = sum_k (d sc_j q - dm m_j)[r][k] * x[k] for the layout of
+ * qd_quantize_q4k (blocks DEVICE, 16-byte aligned; x DEVICE fp32 [K], 16-byte aligned;
+ * y DEVICE fp32 [rows]): 0.5625 bytes per weight streamed once.  K is 512, 1024 or
+ * 2048.  Asynchronous on cuda_stream; with avg_ms (HOST) non-NULL the kernel is then
+ * launched `reps` more times between CUDA events, synchronised, and their mean
+ * duration written there.  Errors: QD_EINVAL (arguments, alignment), QD_EUNSUPPORTED
+ * (K), QD_ECUDA. */
+qd_status qd_gemv_q4k(const uint8_t *blocks_dev, const float *x_dev, float *y_dev, int rows, int K, void *cuda_stream,
+                      int reps, float *avg_ms);
+
 /* qd_conv1d_causal -- the codec decoder's causal dilated convolution ("qwen3-tts-hip
  * OPTIMIZATION_LOG", codec entries): y[o][t] = bias[o] + sum_i sum_k W[o][i][k] *
  * x[i][t - (K-1-k) * dilation], zero history.  x DEVICE fp32 [Cin][T], W DEVICE fp32

@@ -101,6 +101,10 @@ def _lib_handle():
             L.orc_quantize_q8.restype = i32
             L.orc_gemv_q8.argtypes = [vp, vp, i32, i32, vp, vp]
             L.orc_gemv_q8.restype = i32
+            L.orc_quantize_q4k.argtypes = [vp, i32, i32, vp]
+            L.orc_quantize_q4k.restype = i32
+            L.orc_gemv_q4k.argtypes = [vp, i32, i32, vp, vp]
+            L.orc_gemv_q4k.restype = i32
             L.orc_rope_mrope.argtypes = [vp, i32, P(i32), P(i32), dp]
             L.orc_rope_mrope.restype = None
             L.orc_mrope_stream.argtypes = [i32, P(i32)]
@@ -538,6 +542,31 @@ def gemv_q8(codes: np.ndarray, scales: np.ndarray, x: np.ndarray) -> np.ndarray:
     st = _lib_handle().orc_gemv_q8(codes.ctypes.data, scales.ctypes.data, rows, K, x.ctypes.data, y.ctypes.data)
     if st != OK:
         raise OracleError(st, "gemv_q8")
+    return y
+
+
+Q4K_BLOCK_BYTES = 144   # 256 weights: half d, half dm, 8 + 8 six-bit fields, 128 code bytes
+
+
+def quantize_q4k(w: np.ndarray) -> np.ndarray:
+    """Q4_K super-blocks of W [rows, K] (fp32, K a multiple of 256): uint8 [rows, K/256, 144]."""
+    w = np.ascontiguousarray(w, np.float32)
+    rows, K = w.shape
+    out = np.zeros((rows, K // 256, Q4K_BLOCK_BYTES), np.uint8)
+    st = _lib_handle().orc_quantize_q4k(w.ctypes.data, rows, K, out.ctypes.data)
+    if st != OK:
+        raise OracleError(st, "quantize_q4k")
+    return out
+
+
+def gemv_q4k(blocks: np.ndarray, x: np.ndarray) -> np.ndarray:
+    blocks = np.ascontiguousarray(blocks, np.uint8)
+    x = np.ascontiguousarray(x, np.float32)
+    rows, nsb = blocks.shape[:2]
+    y = np.empty(rows, np.float32)
+    st = _lib_handle().orc_gemv_q4k(blocks.ctypes.data, rows, nsb * 256, x.ctypes.data, y.ctypes.data)
+    if st != OK:
+        raise OracleError(st, "gemv_q4k")
     return y
 
 

@@ -146,6 +146,107 @@ int orc_gemv_q8(const int8_t *codes, const uint16_t *scales, int rows, int K, co
     return ORC_OK;
 }
 
+/* Q4_K super-blocks ("audio.cpp Rockchip NPU build notes", "The talker is the only
+ * DRAM-bound candidate, and it is not at the ceiling": the talker's matrices as Q4_K,
+ * 251 MB per token against 471 MB as Q8_0).  The format, read as the k-quant layout:
+ * 256 weights along K in 8 sub-blocks of 32; the super-block holds a half scale d and a
+ * half min dm, each sub-block j a 6-bit scale sc_j and a 6-bit min m_j, each weight a
+ * 4-bit code q; the weight it stands for is d sc_j q - dm m_j.  144 bytes per
+ * super-block (4.5 bits per weight): d, dm (half bits, little-endian), the 8 scales then
+ * the 8 mins as 6-bit fields of two 48-bit little-endian words, then 128 bytes of codes
+ * (byte i: code 2i in the low nibble, code 2i + 1 in the high one).
+ * The pages do not print the quantiser; the plain reading taken here, in fp32 with
+ * IEEE division and half-away rounding: per sub-block mn_j = -min(0, min w) and
+ * s_j = (max w + mn_j) / 15; d = half(max_j s_j / 63), dm = half(max_j mn_j / 63);
+ * sc_j = clamp(round(s_j / d), 0, 63) (0 when d is 0), m_j = clamp(round(mn_j / dm),
+ * 0, 63) (0 when dm is 0); q = clamp(round((w + dm m_j) / (d sc_j)), 0, 15) (0 when
+ * d sc_j is 0).  d sc_j and dm m_j are exact in fp32 (11-bit by 6-bit significands). */
+static void q4k_put6(uint8_t *p, const int *v) {
+    uint64_t w = 0;
+    for (int j = 0; j < 8; ++j) w |= (uint64_t)(v[j] & 63) << (6 * j);
+    for (int b = 0; b < 6; ++b) p[b] = (uint8_t)(w >> (8 * b));
+}
+static void q4k_get6(const uint8_t *p, int *v) {
+    uint64_t w = 0;
+    for (int b = 0; b < 6; ++b) w |= (uint64_t)p[b] << (8 * b);
+    for (int j = 0; j < 8; ++j) v[j] = (int)((w >> (6 * j)) & 63);
+}
+static float q4k_round_clamp(float v, float hi) {
+    const float r = roundf(v);
+    return r < 0.0f ? 0.0f : (r > hi ? hi : r);
+}
+
+int orc_quantize_q4k(const float *w, int rows, int K, uint8_t *blocks) {
+    if (rows < 0 || K <= 0 || K % 256) return ORC_EINVAL;
+    const int nsb = K / 256;
+    for (int r = 0; r < rows; ++r)
+        for (int b = 0; b < nsb; ++b) {
+            const float *x = w + (size_t)r * K + (size_t)b * 256;
+            uint8_t *o = blocks + ((size_t)r * nsb + b) * 144;
+            float s[8], mn[8], smax = 0.0f, mnmax = 0.0f;
+            for (int j = 0; j < 8; ++j) {
+                float lo = x[32 * j], hi = x[32 * j];
+                for (int i = 1; i < 32; ++i) {
+                    if (x[32 * j + i] < lo) lo = x[32 * j + i];
+                    if (x[32 * j + i] > hi) hi = x[32 * j + i];
+                }
+                mn[j] = lo < 0.0f ? -lo : 0.0f;
+                s[j] = (hi + mn[j]) / 15.0f;
+                if (s[j] > smax) smax = s[j];
+                if (mn[j] > mnmax) mnmax = mn[j];
+            }
+            const uint16_t dh = orc_f32_to_f16(smax / 63.0f), dmh = orc_f32_to_f16(mnmax / 63.0f);
+            const float d = orc_f16_to_f32(dh), dm = orc_f16_to_f32(dmh);
+            int sc[8], m[8];
+            for (int j = 0; j < 8; ++j) {
+                sc[j] = d > 0.0f ? (int)q4k_round_clamp(s[j] / d, 63.0f) : 0;
+                m[j] = dm > 0.0f ? (int)q4k_round_clamp(mn[j] / dm, 63.0f) : 0;
+            }
+            o[0] = (uint8_t)(dh & 0xff);
+            o[1] = (uint8_t)(dh >> 8);
+            o[2] = (uint8_t)(dmh & 0xff);
+            o[3] = (uint8_t)(dmh >> 8);
+            q4k_put6(o + 4, sc);
+            q4k_put6(o + 10, m);
+            for (int j = 0; j < 8; ++j) {
+                const float step = d * (float)sc[j], off = dm * (float)m[j];
+                for (int i = 0; i < 32; ++i) {
+                    const int k = 32 * j + i;
+                    const float t = x[k] + off;
+                    const int q = step > 0.0f ? (int)q4k_round_clamp(t / step, 15.0f) : 0;
+                    if (k & 1) o[16 + k / 2] |= (uint8_t)(q << 4);
+                    else o[16 + k / 2] = (uint8_t)q;
+                }
+            }
+        }
+    return ORC_OK;
+}
+
+/* y[r] = sum_k w'[r][k] x[k] with w' = d sc_j q - dm m_j of the super-block layout
+ * above: each weight formed in fp32, each product in fp32, summed in fp64. */
+int orc_gemv_q4k(const uint8_t *blocks, int rows, int K, const float *x, float *y) {
+    if (rows < 0 || K <= 0 || K % 256) return ORC_EINVAL;
+    const int nsb = K / 256;
+    for (int r = 0; r < rows; ++r) {
+        double acc = 0.0;
+        for (int b = 0; b < nsb; ++b) {
+            const uint8_t *o = blocks + ((size_t)r * nsb + b) * 144;
+            const float d = orc_f16_to_f32((uint16_t)(o[0] | (o[1] << 8)));
+            const float dm = orc_f16_to_f32((uint16_t)(o[2] | (o[3] << 8)));
+            int sc[8], m[8];
+            q4k_get6(o + 4, sc);
+            q4k_get6(o + 10, m);
+            for (int k = 0; k < 256; ++k) {
+                const int q = (k & 1) ? (o[16 + k / 2] >> 4) : (o[16 + k / 2] & 15);
+                const float wq = d * (float)sc[k / 32] * (float)q - dm * (float)m[k / 32];
+                acc += (double)(wq * x[(size_t)b * 256 + k]);
+            }
+        }
+        y[r] = (float)acc;
+    }
+    return ORC_OK;
+}
+
 /* Causal dilated 1-D convolution, written out from its definition: each output is the
  * bias plus the K taps of every input channel at t, t - d, ..., t - (K-1) d. */
 int orc_conv1d_causal(const float *x, int Cin, int T, const float *W, const float *bias, int Cout, int K, int dil,

@@ -141,6 +141,9 @@ int orc_quantize_q8(const float *w, int rows, int K, int8_t *codes, uint16_t *sc
 /* y[r] = sum_k (codes[r][k] * half(scales[r][k / 32])) * x[k], fp32 products summed in
  * fp64 in index order, rounded to fp32. */
 int orc_gemv_q8(const int8_t *codes, const uint16_t *scales, int rows, int K, const float *x, float *y);
+/* Q4_K super-blocks of 256 weights (144 bytes each, [rows][K/256]): see oracle.c. */
+int orc_quantize_q4k(const float *w, int rows, int K, uint8_t *blocks);
+int orc_gemv_q4k(const uint8_t *blocks, int rows, int K, const float *x, float *y);
 
 /* Codec decoder convolution stages ("qwen3-tts-hip OPTIMIZATION_LOG", codec-profile and
  * transposed-convolution entries; the codec's SEANet upsampler in "Qwen3-TTS ncnn

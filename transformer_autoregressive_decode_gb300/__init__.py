@@ -37,6 +37,7 @@ EXPORTS = ("qd_create", "qd_destroy", "qd_reset", "qd_prefill", "qd_prefill_mrop
            "qd_get_emitted", "qd_get_pos", "qd_get_launch_count", "qd_time_kernel", "qd_last_error",
            "qd_status_string", "qd_head_argmax_noalloc", "qd_frame_create", "qd_frame_destroy",
            "qd_frame_generate", "qd_frame_set_graphs", "qd_gemm_bf16", "qd_quantize_q8", "qd_gemv_q8",
+           "qd_quantize_q4k", "qd_gemv_q4k",
            "qd_conv1d_causal", "qd_conv_transpose1d_causal", "qd_conv1d_causal_tc",
            "qd_conv_transpose1d_causal_tc", "qd_batch_create", "qd_batch_destroy",
            "qd_batch_set_stream", "qd_batch_decode", "qd_batch_sync", "qd_batch_get_logits", "qd_batch_copy_kv",
@@ -98,6 +99,8 @@ _SIGS = {
     "qd_conv1d_causal_tc": ([_vp, _i32, _i32, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _i32, _vp], _i32),
     "qd_conv_transpose1d_causal_tc": ([_vp, _i32, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _i32, _vp], _i32),
     "qd_gemv_q8": ([_vp, _vp, _vp, _vp, _i32, _i32, _vp, _i32, _P(ctypes.c_float)], _i32),
+    "qd_quantize_q4k": ([_vp, _i32, _i32, _i32, _vp, _vp], _i32),
+    "qd_gemv_q4k": ([_vp, _vp, _vp, _i32, _i32, _vp, _i32, _P(ctypes.c_float)], _i32),
     "qd_batch_create": ([_vp, _i32, _i32, _P(_vp)], _i32),
     "qd_batch_destroy": ([_vp], _i32),
     "qd_batch_set_stream": ([_vp, _i32, _vp, _i32, ctypes.c_int32], _i32),
@@ -498,6 +501,32 @@ def qd_gemv_q8(codes_dev, scales_dev, x_dev, y_dev, stream=None, time_reps: int 
                          ctypes.byref(ms) if time_reps else None)
     if st != QD_OK:
         raise QDError(st, "qd_gemv_q8 failed")
+    return ms.value if time_reps else None
+
+
+def qd_quantize_q4k(w_dev, blocks_dev, stream=None):
+    """Q4_K super-blocks of the device matrix w_dev [rows, K] (fp32 or bf16, K a multiple
+    of 256) into blocks_dev (uint8 [rows, K/256, 144])."""
+    import torch
+    rows, K = w_dev.shape
+    s = (stream or torch.cuda.current_stream()).cuda_stream
+    st = _lib.qd_quantize_q4k(_ptr(w_dev), QD_BF16 if w_dev.dtype == torch.bfloat16 else QD_F32, rows, K,
+                              _ptr(blocks_dev), s)
+    if st != QD_OK:
+        raise QDError(st, "qd_quantize_q4k failed")
+
+
+def qd_gemv_q4k(blocks_dev, x_dev, y_dev, stream=None, time_reps: int = 0):
+    """y = dequant(blocks) x on the device (blocks uint8 [rows, K/256, 144]); returns the
+    mean kernel time (ms) of ``time_reps`` extra launches, or None."""
+    import torch
+    rows, nsb = int(blocks_dev.shape[0]), int(blocks_dev.shape[1])
+    s = (stream or torch.cuda.current_stream()).cuda_stream
+    ms = ctypes.c_float(0.0)
+    st = _lib.qd_gemv_q4k(_ptr(blocks_dev), _ptr(x_dev), _ptr(y_dev), rows, nsb * 256, s, int(time_reps),
+                          ctypes.byref(ms) if time_reps else None)
+    if st != QD_OK:
+        raise QDError(st, "qd_gemv_q4k failed")
     return ms.value if time_reps else None
 
 

@@ -181,6 +181,163 @@ int sm_count() {
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// ---- Q4_K super-blocks: 256 weights along K in 8 sub-blocks of 32, 144 bytes each
+// (half d, half dm, the 8 six-bit scales and the 8 six-bit mins as two 48-bit
+// little-endian words, then 128 bytes of 4-bit codes, low nibble first); weight =
+// d sc_j q - dm m_j.  The quantiser takes the same fp32 steps as its definition
+// (IEEE division, half-away rounding, round-to-nearest-even halves), so the bytes are
+// exact.
+constexpr int kQ4Bytes = 144;
+constexpr int kGemvQ4Warps = 16;
+
+__device__ __forceinline__ float q4k_rc(float v, float hi) {
+    const float r = roundf(v);
+    return r < 0.f ? 0.f : (r > hi ? hi : r);
+}
+
+// One warp per super-block: lane l holds weights 8 l .. 8 l + 7 (sub-block l / 4).
+template <typename T>
+__global__ void __launch_bounds__(256) quantize_q4k_kernel(const T *w, long long n_sb, int nsb_row, int K,
+                                                           uint8_t *out) {
+    const int lane = threadIdx.x & 31;
+    const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+    for (long long b = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); b < n_sb; b += warps) {
+        const long long r = b / nsb_row;
+        const int sb = (int)(b - r * nsb_row);
+        const T *x = w + (size_t)r * K + (size_t)sb * 256 + lane * 8;
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = to_f32(x[e]);
+        float lo = v[0], hi = v[0];
+#pragma unroll
+        for (int e = 1; e < 8; ++e) {
+            lo = v[e] < lo ? v[e] : lo;
+            hi = v[e] > hi ? v[e] : hi;
+        }
+#pragma unroll
+        for (int o = 1; o < 4; o <<= 1) {   // the sub-block's four lanes
+            const float l2 = __shfl_xor_sync(0xffffffffu, lo, o), h2 = __shfl_xor_sync(0xffffffffu, hi, o);
+            lo = l2 < lo ? l2 : lo;
+            hi = h2 > hi ? h2 : hi;
+        }
+        const float mn = lo < 0.f ? -lo : 0.f;
+        const float sj = __fdiv_rn(__fadd_rn(hi, mn), 15.f);
+        float smax = sj, mnmax = mn;
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, o));
+            mnmax = fmaxf(mnmax, __shfl_xor_sync(0xffffffffu, mnmax, o));
+        }
+        const __half dh = __float2half_rn(__fdiv_rn(smax, 63.f)), dmh = __float2half_rn(__fdiv_rn(mnmax, 63.f));
+        const float d = __half2float(dh), dm = __half2float(dmh);
+        const int sc = d > 0.f ? (int)q4k_rc(__fdiv_rn(sj, d), 63.f) : 0;
+        const int m = dm > 0.f ? (int)q4k_rc(__fdiv_rn(mn, dm), 63.f) : 0;
+        const float step = __fmul_rn(d, (float)sc), off = __fmul_rn(dm, (float)m);
+        uint32_t packed = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int q = step > 0.f ? (int)q4k_rc(__fdiv_rn(__fadd_rn(v[e], off), step), 15.f) : 0;
+            packed |= (uint32_t)q << (4 * e);
+        }
+        uint8_t *o = out + (size_t)b * kQ4Bytes;
+        *reinterpret_cast<uint32_t *>(o + 16 + lane * 4) = packed;
+        // the header: sub-block j's scale and min from lane 4 j
+        unsigned long long ws = 0, wm = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            ws |= (unsigned long long)__shfl_sync(0xffffffffu, sc, 4 * j) << (6 * j);
+            wm |= (unsigned long long)__shfl_sync(0xffffffffu, m, 4 * j) << (6 * j);
+        }
+        if (lane == 0) {
+            uint4 h;
+            h.x = (uint32_t)__half_as_ushort(dh) | ((uint32_t)__half_as_ushort(dmh) << 16);
+            h.y = (uint32_t)ws;                                             // scale bytes 0-3
+            h.z = (uint32_t)(ws >> 32) | ((uint32_t)(wm & 0xffffu) << 16);  // scale bytes 4-5, min bytes 0-1
+            h.w = (uint32_t)(wm >> 16);                                     // min bytes 2-5
+            *reinterpret_cast<uint4 *>(o) = h;
+        }
+    }
+}
+
+__device__ __forceinline__ uint32_t ld_stream4(const void *p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+// y[r] = sum over super-blocks of d sc_j (sum_e q_e x_e) - dm m_j (sum_e x_e): lane l
+// owns columns 8 l .. 8 l + 7 of every super-block (one 4-byte code load each), its x
+// values and their sum in registers; RU rows per warp in flight.
+template <int NSB, int RU>
+__global__ void __launch_bounds__(kGemvQ4Warps * 32)
+    gemv_q4k_kernel(const uint8_t *blocks, const float *x, float *y, int rows) {
+    const int lane = threadIdx.x & 31, j = lane >> 2;
+    float xr[NSB][8], xsum[NSB];
+#pragma unroll
+    for (int sb = 0; sb < NSB; ++sb) {
+        const float4 a = *reinterpret_cast<const float4 *>(x + sb * 256 + lane * 8);
+        const float4 b = *reinterpret_cast<const float4 *>(x + sb * 256 + lane * 8 + 4);
+        xr[sb][0] = a.x, xr[sb][1] = a.y, xr[sb][2] = a.z, xr[sb][3] = a.w;
+        xr[sb][4] = b.x, xr[sb][5] = b.y, xr[sb][6] = b.z, xr[sb][7] = b.w;
+        float t = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) t += xr[sb][e];
+        xsum[sb] = t;
+    }
+    const int warps = gridDim.x * kGemvQ4Warps;
+    for (int r0 = (blockIdx.x * kGemvQ4Warps + (threadIdx.x >> 5)) * RU; r0 < rows; r0 += warps * RU) {
+        uint32_t cw[RU][NSB];
+        uint4 hd[RU][NSB];
+#pragma unroll
+        for (int q = 0; q < RU; ++q) {
+            const int r = r0 + q < rows ? r0 + q : rows - 1;
+#pragma unroll
+            for (int sb = 0; sb < NSB; ++sb) {
+                const uint8_t *o = blocks + ((size_t)r * NSB + sb) * kQ4Bytes;
+                cw[q][sb] = ld_stream4(o + 16 + lane * 4);
+                hd[q][sb] = __ldg(reinterpret_cast<const uint4 *>(o));
+            }
+        }
+        float acc[RU];
+#pragma unroll
+        for (int q = 0; q < RU; ++q) {
+            acc[q] = 0.f;
+#pragma unroll
+            for (int sb = 0; sb < NSB; ++sb) {
+                const uint4 h = hd[q][sb];
+                const float d = __half2float(__ushort_as_half((unsigned short)(h.x & 0xffffu)));
+                const float dm = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
+                const unsigned long long ws = (unsigned long long)h.y | ((unsigned long long)(h.z & 0xffffu) << 32);
+                const unsigned long long wm = (unsigned long long)(h.z >> 16) | ((unsigned long long)h.w << 16);
+                const int sc = (int)((ws >> (6 * j)) & 63), m = (int)((wm >> (6 * j)) & 63);
+                float sq = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) sq = fmaf((float)((cw[q][sb] >> (4 * e)) & 15u), xr[sb][e], sq);
+                acc[q] = fmaf(d * (float)sc, sq, acc[q]);
+                acc[q] = fmaf(-(dm * (float)m), xsum[sb], acc[q]);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < RU; ++q)
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
+        if (lane == 0)
+#pragma unroll
+            for (int q = 0; q < RU; ++q)
+                if (r0 + q < rows) y[r0 + q] = acc[q];
+    }
+}
+
+typedef void (*GemvQ4Fn)(const uint8_t *, const float *, float *, int);
+GemvQ4Fn gemv_q4k_fn(int nsb) {
+    switch (nsb) {
+        case 2: return gemv_q4k_kernel<2, 4>;
+        case 4: return gemv_q4k_kernel<4, 2>;
+        case 8: return gemv_q4k_kernel<8, 1>;
+        default: return nullptr;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_quantize_rows_q8(const void *w, bool bf16, int rows, int K, void *dst, int row0, int rstep,
@@ -242,6 +399,55 @@ qd_status qd_gemv_q8(const int8_t *codes_dev, const uint16_t *scales_dev, const 
         }
         cudaEventRecord(e0, s);
         for (int i = 0; i < reps; ++i) fn<<<grid, kGemvQWarps * 32, 0, s>>>(codes_dev, scales_dev, x_dev, y_dev, rows);
+        cudaEventRecord(e1, s);
+        const bool ok = cudaEventSynchronize(e1) == cudaSuccess && cudaGetLastError() == cudaSuccess;
+        float ms = 0.f;
+        cudaEventElapsedTime(&ms, e0, e1);
+        *avg_ms = ms / (float)reps;
+        cudaEventDestroy(e0);
+        cudaEventDestroy(e1);
+        if (!ok) return QD_ECUDA;
+    }
+    return QD_OK;
+}
+
+qd_status qd_quantize_q4k(const void *w_dev, int dtype, int rows, int K, uint8_t *blocks_dev, void *cuda_stream) {
+    if (rows <= 0 || K <= 0 || K % 256 || (dtype != QD_F32 && dtype != QD_BF16)) return QD_EINVAL;
+    if (!is_device_ptr(w_dev) || !is_device_ptr(blocks_dev) || !aligned(blocks_dev, 16)) return QD_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    const long long n_sb = (long long)rows * (K / 256);
+    const int grid = (int)std::min<long long>((n_sb + 7) / 8, (long long)sm_count() * 16);
+    if (dtype == QD_BF16)
+        quantize_q4k_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(w_dev), n_sb,
+                                                                K / 256, K, blocks_dev);
+    else
+        quantize_q4k_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float *>(w_dev), n_sb, K / 256, K,
+                                                        blocks_dev);
+    if (cudaGetLastError() != cudaSuccess) return QD_ECUDA;
+    return cudaStreamSynchronize(s) == cudaSuccess ? QD_OK : QD_ECUDA;
+}
+
+qd_status qd_gemv_q4k(const uint8_t *blocks_dev, const float *x_dev, float *y_dev, int rows, int K, void *cuda_stream,
+                      int reps, float *avg_ms) {
+    if (rows <= 0 || K <= 0 || reps < 0) return QD_EINVAL;
+    if (!is_device_ptr(blocks_dev) || !is_device_ptr(x_dev) || !is_device_ptr(y_dev)) return QD_EINVAL;
+    if (!aligned(blocks_dev, 16) || !aligned(x_dev, 16)) return QD_EINVAL;
+    const GemvQ4Fn fn = K % 256 == 0 ? gemv_q4k_fn(K / 256) : nullptr;
+    if (!fn) return QD_EUNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+    const int ru = 8 / (K / 256), per_cta = kGemvQ4Warps * ru;
+    const int grid = std::max(1, std::min((rows + per_cta - 1) / per_cta, 2 * sm_count()));
+    fn<<<grid, kGemvQ4Warps * 32, 0, s>>>(blocks_dev, x_dev, y_dev, rows);
+    if (cudaGetLastError() != cudaSuccess) return QD_ECUDA;
+    if (reps > 0 && avg_ms) {
+        cudaEvent_t e0, e1;
+        if (cudaEventCreate(&e0) != cudaSuccess) return QD_ECUDA;
+        if (cudaEventCreate(&e1) != cudaSuccess) {
+            cudaEventDestroy(e0);
+            return QD_ECUDA;
+        }
+        cudaEventRecord(e0, s);
+        for (int i = 0; i < reps; ++i) fn<<<grid, kGemvQ4Warps * 32, 0, s>>>(blocks_dev, x_dev, y_dev, rows);
         cudaEventRecord(e1, s);
         const bool ok = cudaEventSynchronize(e1) == cudaSuccess && cudaGetLastError() == cudaSuccess;
         float ms = 0.f;
