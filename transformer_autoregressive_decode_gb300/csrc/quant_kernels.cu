@@ -259,81 +259,82 @@ __global__ void __launch_bounds__(256) quantize_q4k_kernel(const T *w, long long
     }
 }
 
-__device__ __forceinline__ uint32_t ld_stream4(const void *p) {
-    uint32_t v;
-    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
-}
-
-// y[r] = sum over super-blocks of d sc_j (sum_e q_e x_e) - dm m_j (sum_e x_e): lane l
-// owns columns 8 l .. 8 l + 7 of every super-block (one 4-byte code load each), its x
-// values and their sum in registers; RU rows per warp in flight.
+// y[r] = sum over sub-blocks of d sc_j (sum_i q_i x_i) - dm m_j (sum_i x_i).  A lane owns
+// whole 32-weight sub-blocks of a row (one 16-byte code load each: LPR lanes per row,
+// SPL sub-blocks per lane), their 32 x values and their sum in registers; RU rows per
+// lane in flight; the row's lanes add their partials with a butterfly.
 template <int NSB, int RU>
 __global__ void __launch_bounds__(kGemvQ4Warps * 32)
     gemv_q4k_kernel(const uint8_t *blocks, const float *x, float *y, int rows) {
-    const int lane = threadIdx.x & 31, j = lane >> 2;
-    float xr[NSB][8], xsum[NSB];
+    constexpr int LPR = NSB * 8 < 32 ? NSB * 8 : 32;   // lanes per row
+    constexpr int SPL = NSB * 8 / LPR;                  // sub-blocks per lane
+    constexpr int RPW = 32 / LPR;                       // rows per warp
+    const int lane = threadIdx.x & 31, rl = lane / LPR, li = lane % LPR;
+    float xr[SPL][32], xsum[SPL];
 #pragma unroll
-    for (int sb = 0; sb < NSB; ++sb) {
-        const float4 a = *reinterpret_cast<const float4 *>(x + sb * 256 + lane * 8);
-        const float4 b = *reinterpret_cast<const float4 *>(x + sb * 256 + lane * 8 + 4);
-        xr[sb][0] = a.x, xr[sb][1] = a.y, xr[sb][2] = a.z, xr[sb][3] = a.w;
-        xr[sb][4] = b.x, xr[sb][5] = b.y, xr[sb][6] = b.z, xr[sb][7] = b.w;
+    for (int k = 0; k < SPL; ++k) {
+        const float *xp = x + (li + k * LPR) * 32;      // sub-block g covers columns 32 g ..
         float t = 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) t += xr[sb][e];
-        xsum[sb] = t;
+        for (int e = 0; e < 32; e += 4) {
+            const float4 f = *reinterpret_cast<const float4 *>(xp + e);
+            xr[k][e] = f.x, xr[k][e + 1] = f.y, xr[k][e + 2] = f.z, xr[k][e + 3] = f.w;
+            t += (f.x + f.y) + (f.z + f.w);
+        }
+        xsum[k] = t;
     }
     const int warps = gridDim.x * kGemvQ4Warps;
-    for (int r0 = (blockIdx.x * kGemvQ4Warps + (threadIdx.x >> 5)) * RU; r0 < rows; r0 += warps * RU) {
-        uint32_t cw[RU][NSB];
-        uint4 hd[RU][NSB];
+    const int w = blockIdx.x * kGemvQ4Warps + (threadIdx.x >> 5);
+    for (int r0 = w * RPW * RU; r0 < rows; r0 += warps * RPW * RU) {
+        uint4 cw[RU][SPL], hd[RU][SPL];
 #pragma unroll
-        for (int q = 0; q < RU; ++q) {
-            const int r = r0 + q < rows ? r0 + q : rows - 1;
+        for (int u = 0; u < RU; ++u) {
+            const int r = r0 + u * RPW + rl;
+            const int rc = r < rows ? r : rows - 1;
 #pragma unroll
-            for (int sb = 0; sb < NSB; ++sb) {
-                const uint8_t *o = blocks + ((size_t)r * NSB + sb) * kQ4Bytes;
-                cw[q][sb] = ld_stream4(o + 16 + lane * 4);
-                hd[q][sb] = __ldg(reinterpret_cast<const uint4 *>(o));
+            for (int k = 0; k < SPL; ++k) {
+                const int g = li + k * LPR;
+                const uint8_t *o = blocks + ((size_t)rc * NSB + (g >> 3)) * kQ4Bytes;
+                cw[u][k] = ld_stream16(o + 16 + 16 * (g & 7));
+                hd[u][k] = __ldg(reinterpret_cast<const uint4 *>(o));
             }
         }
-        float acc[RU];
 #pragma unroll
-        for (int q = 0; q < RU; ++q) {
-            acc[q] = 0.f;
+        for (int u = 0; u < RU; ++u) {
+            float acc = 0.f;
 #pragma unroll
-            for (int sb = 0; sb < NSB; ++sb) {
-                const uint4 h = hd[q][sb];
+            for (int k = 0; k < SPL; ++k) {
+                const int j = (li + k * LPR) & 7;
+                const uint4 h = hd[u][k];
                 const float d = __half2float(__ushort_as_half((unsigned short)(h.x & 0xffffu)));
                 const float dm = __half2float(__ushort_as_half((unsigned short)(h.x >> 16)));
                 const unsigned long long ws = (unsigned long long)h.y | ((unsigned long long)(h.z & 0xffffu) << 32);
                 const unsigned long long wm = (unsigned long long)(h.z >> 16) | ((unsigned long long)h.w << 16);
                 const int sc = (int)((ws >> (6 * j)) & 63), m = (int)((wm >> (6 * j)) & 63);
+                const uint32_t cws[4] = {cw[u][k].x, cw[u][k].y, cw[u][k].z, cw[u][k].w};
                 float sq = 0.f;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) sq = fmaf((float)((cw[q][sb] >> (4 * e)) & 15u), xr[sb][e], sq);
-                acc[q] = fmaf(d * (float)sc, sq, acc[q]);
-                acc[q] = fmaf(-(dm * (float)m), xsum[sb], acc[q]);
+                for (int wd = 0; wd < 4; ++wd)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) sq = fmaf((float)((cws[wd] >> (4 * e)) & 15u), xr[k][8 * wd + e], sq);
+                acc = fmaf(d * (float)sc, sq, acc);
+                acc = fmaf(-(dm * (float)m), xsum[k], acc);
             }
+#pragma unroll
+            for (int o = LPR / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            const int r = r0 + u * RPW + rl;
+            if (li == 0 && r < rows) y[r] = acc;
         }
-#pragma unroll
-        for (int q = 0; q < RU; ++q)
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], o);
-        if (lane == 0)
-#pragma unroll
-            for (int q = 0; q < RU; ++q)
-                if (r0 + q < rows) y[r0 + q] = acc[q];
     }
 }
 
 typedef void (*GemvQ4Fn)(const uint8_t *, const float *, float *, int);
+constexpr int kQ4Ru = 2;   // rows per lane in flight
 GemvQ4Fn gemv_q4k_fn(int nsb) {
     switch (nsb) {
-        case 2: return gemv_q4k_kernel<2, 4>;
-        case 4: return gemv_q4k_kernel<4, 2>;
-        case 8: return gemv_q4k_kernel<8, 1>;
+        case 2: return gemv_q4k_kernel<2, kQ4Ru>;
+        case 4: return gemv_q4k_kernel<4, kQ4Ru>;
+        case 8: return gemv_q4k_kernel<8, kQ4Ru>;
         default: return nullptr;
     }
 }
@@ -435,7 +436,8 @@ qd_status qd_gemv_q4k(const uint8_t *blocks_dev, const float *x_dev, float *y_de
     const GemvQ4Fn fn = K % 256 == 0 ? gemv_q4k_fn(K / 256) : nullptr;
     if (!fn) return QD_EUNSUPPORTED;
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
-    const int ru = 8 / (K / 256), per_cta = kGemvQ4Warps * ru;
+    const int nsb = K / 256, lpr = nsb * 8 < 32 ? nsb * 8 : 32;
+    const int per_cta = kGemvQ4Warps * (32 / lpr) * kQ4Ru;   // rows a CTA takes per pass
     const int grid = std::max(1, std::min((rows + per_cta - 1) / per_cta, 2 * sm_count()));
     fn<<<grid, kGemvQ4Warps * 32, 0, s>>>(blocks_dev, x_dev, y_dev, rows);
     if (cudaGetLastError() != cudaSuccess) return QD_ECUDA;
