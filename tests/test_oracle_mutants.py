@@ -36,6 +36,11 @@ MUTANTS = {
     "mrope_decode_restarts_at_cache_position": ("m->rope_delta = top + 1 - n;", "m->rope_delta = 0;"),
     "conv_taps_reversed": ("const int ts = t - (K - 1 - k) * dil;", "const int ts = t - k * dil;"),
     "transconv_one_frame_late": ("const int u = t * stride + k;", "const int u = (t + 1) * stride + k;"),
+    "q8_scale_over_128": ("const float d = amax / 127.0f;", "const float d = amax / 128.0f;"),
+    "q4k_nibbles_swapped": ("if (k & 1) o[16 + k / 2] |= (uint8_t)(q << 4);\n                    else o[16 + k / 2] = (uint8_t)q;",
+                            "if (k & 1) o[16 + k / 2] |= (uint8_t)q;\n                    else o[16 + k / 2] = (uint8_t)(q << 4);"),
+    "q4k_range_over_16": ("s[j] = (hi + mn[j]) / 15.0f;", "s[j] = (hi + mn[j]) / 16.0f;"),
+    "q4k_min_added_in_gemv": ("(float)q - dm * (float)m[k / 32];", "(float)q + dm * (float)m[k / 32];"),
     # the same swap of gate and up in the cached step and in the full recompute, so
     # the two still agree with each other
     "gate_up_swapped": [("matvec(c, W_(m, l, S_WG), F, h, xn, g);\n        matvec(c, W_(m, l, S_WU), F, h, xn, u);",
@@ -43,7 +48,8 @@ MUTANTS = {
                         ("matvec(c, lw[S_WG], F, h, xn, g);\n            matvec(c, lw[S_WU], F, h, xn, u);",
                          "matvec(c, lw[S_WG], F, h, xn, u);\n            matvec(c, lw[S_WU], F, h, xn, g);")],
 }
-PIN_FILES = ("test_oracle_pins.py", "test_oracle_mrope.py", "test_oracle_codec_conv.py")
+PIN_FILES = ("test_oracle_pins.py", "test_oracle_mrope.py", "test_oracle_codec_conv.py", "test_oracle_q8.py",
+             "test_oracle_q4k.py")
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
